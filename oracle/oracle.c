@@ -1,0 +1,600 @@
+/*
+ * oracle.c -- plain, slow fp64 CPU reference of one Mixture-of-Experts layer,
+ * forward and backward.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load this file's library. The product
+ * (the CUDA library and its Python binding) never calls it and shares no
+ * code, header, table or helper with it.
+ *
+ * Source of the method: "Scalable Training of Mixture-of-Experts Models with
+ * Megatron Core", §2 (Megatron-Core MoE Architecture): an MoE layer runs
+ * Route (token hidden states -> expert logits -> probabilities -> top-k
+ * experts; the router outputs routing weights and a token-expert
+ * assignment), Dispatch (permute tokens by destination expert), Expert
+ * Computation (each expert's FFN over its tokens; "SequentialMLP" runs one
+ * expert at a time, which is how this file is organised) and Combine
+ * (restore token order, add the shared expert's output). §5 (Selective
+ * precision) keeps the router in FP32; here everything is fp64.
+ *
+ * Readings where the pages are silent (the layer's formulas are not printed):
+ *   - score: softmax over all E logits, or the logistic sigmoid of each logit;
+ *     the per-expert bias b is added to the logits before scoring and is used
+ *     for both selection and gate values;
+ *   - top-k: the k largest scores; slots ordered by score, descending; equal
+ *     scores resolved towards the lower expert index;
+ *   - gates: the selected scores divided by their sum (for softmax this equals
+ *     the softmax over the selected logits);
+ *   - expert FFN (SwiGLU): a = x Wg_e, u = x Wu_e, h = silu(a) * u,
+ *     y_e = h Wd_e with silu(a) = a / (1 + exp(-a));
+ *   - output: y_t = sum_j g_tj y_{e_tj}(x_t) + shared(x_t), the shared expert
+ *     unweighted;
+ *   - backward: the exact gradient of L = sum(dY * y) with the routing held
+ *     fixed (top-k selection is piecewise constant); no gradient reaches b.
+ *
+ * Layouts (row-major): x T*H, Wr H*E, b E, Wg/Wu E*H*F, Wd E*F*H,
+ * Wsg/Wsu H*Fs, Wsd Fs*H, topk and gates T*k, Yp and dXp R*H with R = T*k.
+ *
+ * Every function returns 0 on success and -1 on a bad argument.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define SCORE_SOFTMAX 0
+#define SCORE_SIGMOID 1
+
+static double silu(double a) { return a / (1.0 + exp(-a)); }
+static double sigm(double a) { return 1.0 / (1.0 + exp(-a)); }
+/* d silu / da = s(a) (1 + a (1 - s(a))) */
+static double dsilu(double a) {
+    double s = sigm(a);
+    return s * (1.0 + a * (1.0 - s));
+}
+
+/* ------------------------------------------------------------------ Route */
+/*
+ * Route (§2, "Route"): logits z = x Wr + b, scores, top-k, gates.
+ *
+ * replay (optional, with replay_topk): for tokens with replay[t] != 0 the
+ * selection and its slot order are taken from replay_topk instead of being
+ * recomputed ("Router replay" in §10 records an assignment and enforces it).
+ * Gates are still the oracle's own, from its own scores.
+ *
+ * gap_set[t]  = relative gap between the k-th and (k+1)-th largest score
+ *               (+HUGE_VAL when k == E);
+ * gap_order[t] = smallest relative gap between consecutive scores among the
+ *               top k (+HUGE_VAL when k == 1).
+ */
+int oracle_route(int T, int H, int E, int k, int score_fn,
+                 const double* x, const double* Wr, const double* b,
+                 const int* replay_topk, const unsigned char* replay,
+                 double* logits, double* scores, int* topk, double* gates,
+                 double* gap_set, double* gap_order)
+{
+    if (T < 0 || H <= 0 || E <= 0 || E > 1024 || k <= 0 || k > E) return -1;
+    if (score_fn != SCORE_SOFTMAX && score_fn != SCORE_SIGMOID) return -1;
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        double* z = logits + (size_t)t * E;
+        double* s = scores + (size_t)t * E;
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h) acc += x[(size_t)t * H + h] * Wr[(size_t)h * E + e];
+            z[e] = acc + (b ? b[e] : 0.0);
+        }
+        if (score_fn == SCORE_SOFTMAX) {
+            double zmax = z[0];
+            for (int e = 1; e < E; ++e) if (z[e] > zmax) zmax = z[e];
+            double den = 0.0;
+            for (int e = 0; e < E; ++e) den += exp(z[e] - zmax);
+            for (int e = 0; e < E; ++e) s[e] = exp(z[e] - zmax) / den;
+        } else {
+            for (int e = 0; e < E; ++e) s[e] = sigm(z[e]);
+        }
+        /* k+1 rounds of "largest remaining score, lower index on equality" */
+        int order[1024];
+        int nsel = (k < E) ? k + 1 : k;
+        unsigned char taken[1024];
+        memset(taken, 0, (size_t)E);
+        for (int r = 0; r < nsel; ++r) {
+            int best = -1;
+            for (int e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || s[e] > s[best])) best = e;
+            taken[best] = 1;
+            order[r] = best;
+        }
+        double gs = HUGE_VAL, go = HUGE_VAL;
+        if (k < E) gs = (s[order[k - 1]] - s[order[k]]) / fabs(s[order[k - 1]]);
+        for (int r = 0; r + 1 < k; ++r) {
+            double g = (s[order[r]] - s[order[r + 1]]) / fabs(s[order[r]]);
+            if (g < go) go = g;
+        }
+        gap_set[t] = gs;
+        gap_order[t] = go;
+        int* sel = topk + (size_t)t * k;
+        if (replay && replay[t]) {
+            for (int j = 0; j < k; ++j) sel[j] = replay_topk[(size_t)t * k + j];
+        } else {
+            for (int j = 0; j < k; ++j) sel[j] = order[j];
+        }
+        double den = 0.0;
+        for (int j = 0; j < k; ++j) den += s[sel[j]];
+        for (int j = 0; j < k; ++j) gates[(size_t)t * k + j] = s[sel[j]] / den;
+    }
+    return 0;
+}
+
+/* --------------------------------------------------------------- Dispatch */
+/*
+ * Dispatch (§2, "Dispatch"): group the T*k (token, slot) pairs by expert.
+ * counts[e] = number of tokens that chose e; offsets = exclusive prefix sum
+ * (E+1 entries). Rows are ordered by expert, then by token. row_of[t*k+j] is
+ * the row of pair (t, j); slot_of[row] = t*k + j is its inverse.
+ */
+int oracle_dispatch(int T, int E, int k, const int* topk,
+                    int* counts, int* offsets, int* row_of, int* slot_of)
+{
+    if (T < 0 || E <= 0 || k <= 0) return -1;
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (int i = 0; i < T * k; ++i) {
+        if (topk[i] < 0 || topk[i] >= E) return -1;
+        counts[topk[i]] += 1;
+    }
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    int row = 0;
+    for (int e = 0; e < E; ++e)
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < k; ++j)
+                if (topk[(size_t)t * k + j] == e) {
+                    row_of[(size_t)t * k + j] = row;
+                    slot_of[row] = t * k + j;
+                    ++row;
+                }
+    return 0;
+}
+
+/* ------------------------------------------------------- one expert (SwiGLU) */
+/* For M rows X (M*H): A = X Wg, U = X Wu (M*F), Hh = silu(A) * U, Y = Hh Wd. */
+static void swiglu_forward(int M, int H, int F, const double* X,
+                           const double* Wg, const double* Wu, const double* Wd,
+                           double* A, double* U, double* Hh, double* Y)
+{
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m) {
+        for (int f = 0; f < F; ++f) {
+            double a = 0.0, u = 0.0;
+            for (int h = 0; h < H; ++h) {
+                a += X[(size_t)m * H + h] * Wg[(size_t)h * F + f];
+                u += X[(size_t)m * H + h] * Wu[(size_t)h * F + f];
+            }
+            A[(size_t)m * F + f] = a;
+            U[(size_t)m * F + f] = u;
+            Hh[(size_t)m * F + f] = silu(a) * u;
+        }
+        for (int h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int f = 0; f < F; ++f) acc += Hh[(size_t)m * F + f] * Wd[(size_t)f * H + h];
+            Y[(size_t)m * H + h] = acc;
+        }
+    }
+}
+
+/*
+ * Backward of one expert over M rows, given dY (M*H) for its output and the
+ * forward intermediates: dH = dY Wd^T, dA = dH * U * silu'(A),
+ * dU = dH * silu(A); dWd = Hh^T dY, dWg = X^T dA, dWu = X^T dU,
+ * dX = dA Wg^T + dU Wu^T. Weight gradients are overwritten.
+ */
+static void swiglu_backward(int M, int H, int F, const double* X,
+                            const double* Wg, const double* Wu, const double* Wd,
+                            const double* A, const double* U, const double* Hh,
+                            const double* dY, double* dX,
+                            double* dWg, double* dWu, double* dWd)
+{
+    double* dA = (double*)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1) * F);
+    double* dU = (double*)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1) * F);
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m) {
+        for (int f = 0; f < F; ++f) {
+            double dh = 0.0;
+            for (int h = 0; h < H; ++h) dh += dY[(size_t)m * H + h] * Wd[(size_t)f * H + h];
+            double a = A[(size_t)m * F + f];
+            dA[(size_t)m * F + f] = dh * U[(size_t)m * F + f] * dsilu(a);
+            dU[(size_t)m * F + f] = dh * silu(a);
+        }
+        for (int h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int f = 0; f < F; ++f)
+                acc += dA[(size_t)m * F + f] * Wg[(size_t)h * F + f]
+                     + dU[(size_t)m * F + f] * Wu[(size_t)h * F + f];
+            dX[(size_t)m * H + h] = acc;
+        }
+    }
+#pragma omp parallel for schedule(static)
+    for (int f = 0; f < F; ++f)
+        for (int h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int m = 0; m < M; ++m) acc += Hh[(size_t)m * F + f] * dY[(size_t)m * H + h];
+            dWd[(size_t)f * H + h] = acc;
+        }
+#pragma omp parallel for schedule(static)
+    for (int h = 0; h < H; ++h)
+        for (int f = 0; f < F; ++f) {
+            double ag = 0.0, au = 0.0;
+            for (int m = 0; m < M; ++m) {
+                ag += X[(size_t)m * H + h] * dA[(size_t)m * F + f];
+                au += X[(size_t)m * H + h] * dU[(size_t)m * F + f];
+            }
+            dWg[(size_t)h * F + f] = ag;
+            dWu[(size_t)h * F + f] = au;
+        }
+    free(dA);
+    free(dU);
+}
+
+/* ---------------------------------------------------------------- Forward */
+/*
+ * Forward of the layer with a given routing (topk, gates): Dispatch, then
+ * Expert Computation one expert at a time, then Combine (§2).
+ * Yp (optional, R*H) receives the unweighted expert outputs in dispatch
+ * order; y (T*H) the layer output.
+ */
+int oracle_forward(int T, int H, int E, int k, int F, int Fs,
+                   const double* x, const double* Wg, const double* Wu, const double* Wd,
+                   const double* Wsg, const double* Wsu, const double* Wsd,
+                   const int* topk, const double* gates, double* y, double* Yp_out)
+{
+    if (T <= 0 || H <= 0 || E <= 0 || k <= 0 || k > E || F <= 0 || Fs < 0) return -1;
+    const int R = T * k;
+    int* counts = (int*)malloc(sizeof(int) * E);
+    int* offsets = (int*)malloc(sizeof(int) * (E + 1));
+    int* row_of = (int*)malloc(sizeof(int) * R);
+    int* slot_of = (int*)malloc(sizeof(int) * R);
+    if (oracle_dispatch(T, E, k, topk, counts, offsets, row_of, slot_of)) return -1;
+    double* Xp = (double*)malloc(sizeof(double) * (size_t)R * H);
+    double* Yp = (double*)malloc(sizeof(double) * (size_t)R * H);
+    /* permute */
+    for (int r = 0; r < R; ++r)
+        memcpy(Xp + (size_t)r * H, x + (size_t)(slot_of[r] / k) * H, sizeof(double) * H);
+    /* experts, one at a time */
+    for (int e = 0; e < E; ++e) {
+        int M = counts[e];
+        if (M == 0) continue;
+        double* A = (double*)malloc(sizeof(double) * (size_t)M * F);
+        double* U = (double*)malloc(sizeof(double) * (size_t)M * F);
+        double* Hh = (double*)malloc(sizeof(double) * (size_t)M * F);
+        swiglu_forward(M, H, F, Xp + (size_t)offsets[e] * H,
+                       Wg + (size_t)e * H * F, Wu + (size_t)e * H * F, Wd + (size_t)e * F * H,
+                       A, U, Hh, Yp + (size_t)offsets[e] * H);
+        free(A); free(U); free(Hh);
+    }
+    /* combine: restore token order, weight by gates, add the shared expert */
+    for (int t = 0; t < T; ++t)
+        for (int h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j)
+                acc += gates[(size_t)t * k + j] * Yp[(size_t)row_of[(size_t)t * k + j] * H + h];
+            y[(size_t)t * H + h] = acc;
+        }
+    if (Fs > 0) {
+        double* A = (double*)malloc(sizeof(double) * (size_t)T * Fs);
+        double* U = (double*)malloc(sizeof(double) * (size_t)T * Fs);
+        double* Hh = (double*)malloc(sizeof(double) * (size_t)T * Fs);
+        double* Ys = (double*)malloc(sizeof(double) * (size_t)T * H);
+        swiglu_forward(T, H, Fs, x, Wsg, Wsu, Wsd, A, U, Hh, Ys);
+        for (size_t i = 0; i < (size_t)T * H; ++i) y[i] += Ys[i];
+        free(A); free(U); free(Hh); free(Ys);
+    }
+    if (Yp_out) memcpy(Yp_out, Yp, sizeof(double) * (size_t)R * H);
+    free(Xp); free(Yp); free(counts); free(offsets); free(row_of); free(slot_of);
+    return 0;
+}
+
+/* ------------------------------------------------------- router backward */
+/*
+ * dz for one token from the gate gradients dg (k values): gates
+ * g_j = s_j / sum_i s_i over the selected set S.
+ *   softmax: g is the softmax over the selected logits, so
+ *            dz_j = g_j (dg_j - sum_i g_i dg_i);
+ *   sigmoid: dL/ds_j = (dg_j - sum_i g_i dg_i) / sum_i s_i and
+ *            ds_j/dz_j = s_j (1 - s_j).
+ * Experts outside S get dz = 0 (the gates do not depend on their logits).
+ */
+static void router_dz(int k, int score_fn, const int* sel, const double* g, const double* s_all,
+                      const double* dg, double* dz)
+{
+    double gd = 0.0;
+    for (int j = 0; j < k; ++j) gd += g[j] * dg[j];
+    if (score_fn == SCORE_SOFTMAX) {
+        for (int j = 0; j < k; ++j) dz[j] = g[j] * (dg[j] - gd);
+    } else {
+        double ssum = 0.0;
+        for (int j = 0; j < k; ++j) ssum += s_all[sel[j]];
+        for (int j = 0; j < k; ++j) {
+            double s = s_all[sel[j]];
+            dz[j] = s * (1.0 - s) * (dg[j] - gd) / ssum;
+        }
+    }
+}
+
+/* --------------------------------------------------------------- Backward */
+/*
+ * Backward of the layer for L = sum(dY * y), routing fixed. scores is the
+ * T*E output of oracle_route (softmax probabilities or sigmoids).
+ * Outputs (overwritten): dX T*H, dWr H*E, dWg/dWu E*H*F, dWd E*F*H,
+ * dWsg/dWsu H*Fs, dWsd Fs*H (when Fs > 0), dg T*k (optional).
+ * Experts that received no token get zero weight gradients.
+ */
+int oracle_backward(int T, int H, int E, int k, int F, int Fs, int score_fn,
+                    const double* x, const double* Wr,
+                    const double* Wg, const double* Wu, const double* Wd,
+                    const double* Wsg, const double* Wsu, const double* Wsd,
+                    const int* topk, const double* gates, const double* scores,
+                    const double* dY,
+                    double* dX, double* dWr, double* dWg, double* dWu, double* dWd,
+                    double* dWsg, double* dWsu, double* dWsd, double* dg_out)
+{
+    if (T <= 0 || H <= 0 || E <= 0 || k <= 0 || k > E || k > 1024 || F <= 0 || Fs < 0) return -1;
+    const int R = T * k;
+    int* counts = (int*)malloc(sizeof(int) * E);
+    int* offsets = (int*)malloc(sizeof(int) * (E + 1));
+    int* row_of = (int*)malloc(sizeof(int) * R);
+    int* slot_of = (int*)malloc(sizeof(int) * R);
+    if (oracle_dispatch(T, E, k, topk, counts, offsets, row_of, slot_of)) return -1;
+    double* Xp = (double*)malloc(sizeof(double) * (size_t)R * H);
+    double* Yp = (double*)malloc(sizeof(double) * (size_t)R * H);
+    double* dYp = (double*)malloc(sizeof(double) * (size_t)R * H);
+    double* dXp = (double*)malloc(sizeof(double) * (size_t)R * H);
+    double* dg = (double*)malloc(sizeof(double) * (size_t)R);
+    for (int r = 0; r < R; ++r)
+        memcpy(Xp + (size_t)r * H, x + (size_t)(slot_of[r] / k) * H, sizeof(double) * H);
+
+    /* recompute the forward per expert, then its backward */
+    for (int e = 0; e < E; ++e) {
+        int M = counts[e];
+        double* dWg_e = dWg + (size_t)e * H * F;
+        double* dWu_e = dWu + (size_t)e * H * F;
+        double* dWd_e = dWd + (size_t)e * F * H;
+        if (M == 0) {
+            memset(dWg_e, 0, sizeof(double) * (size_t)H * F);
+            memset(dWu_e, 0, sizeof(double) * (size_t)H * F);
+            memset(dWd_e, 0, sizeof(double) * (size_t)F * H);
+            continue;
+        }
+        const double* Xe = Xp + (size_t)offsets[e] * H;
+        double* A = (double*)malloc(sizeof(double) * (size_t)M * F);
+        double* U = (double*)malloc(sizeof(double) * (size_t)M * F);
+        double* Hh = (double*)malloc(sizeof(double) * (size_t)M * F);
+        swiglu_forward(M, H, F, Xe, Wg + (size_t)e * H * F, Wu + (size_t)e * H * F,
+                       Wd + (size_t)e * F * H, A, U, Hh, Yp + (size_t)offsets[e] * H);
+        /* gate gradient and the gate-scaled output gradient of each row */
+        for (int m = 0; m < M; ++m) {
+            int r = offsets[e] + m;
+            int t = slot_of[r] / k;
+            double g = gates[slot_of[r]];
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h) {
+                acc += dY[(size_t)t * H + h] * Yp[(size_t)r * H + h];
+                dYp[(size_t)r * H + h] = g * dY[(size_t)t * H + h];
+            }
+            dg[slot_of[r]] = acc;
+        }
+        swiglu_backward(M, H, F, Xe, Wg + (size_t)e * H * F, Wu + (size_t)e * H * F,
+                        Wd + (size_t)e * F * H, A, U, Hh, dYp + (size_t)offsets[e] * H,
+                        dXp + (size_t)offsets[e] * H, dWg_e, dWu_e, dWd_e);
+        free(A); free(U); free(Hh);
+    }
+
+    /* router: dz (dense T*E), dWr = x^T dz, dX_router = dz Wr^T */
+    double* dz = (double*)calloc((size_t)T * E, sizeof(double));
+    for (int t = 0; t < T; ++t) {
+        double dzs[1024];
+        router_dz(k, score_fn, topk + (size_t)t * k, gates + (size_t)t * k,
+                  scores + (size_t)t * E, dg + (size_t)t * k, dzs);
+        for (int j = 0; j < k; ++j) dz[(size_t)t * E + topk[(size_t)t * k + j]] = dzs[j];
+    }
+#pragma omp parallel for schedule(static)
+    for (int h = 0; h < H; ++h)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int t = 0; t < T; ++t) acc += x[(size_t)t * H + h] * dz[(size_t)t * E + e];
+            dWr[(size_t)h * E + e] = acc;
+        }
+    /* dX = sum over the token's rows of dXp + router term */
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t)
+        for (int h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j) acc += dXp[(size_t)row_of[(size_t)t * k + j] * H + h];
+            for (int e = 0; e < E; ++e) acc += dz[(size_t)t * E + e] * Wr[(size_t)h * E + e];
+            dX[(size_t)t * H + h] = acc;
+        }
+    /* shared expert: every token, unweighted, so its output gradient is dY */
+    if (Fs > 0) {
+        double* A = (double*)malloc(sizeof(double) * (size_t)T * Fs);
+        double* U = (double*)malloc(sizeof(double) * (size_t)T * Fs);
+        double* Hh = (double*)malloc(sizeof(double) * (size_t)T * Fs);
+        double* Ys = (double*)malloc(sizeof(double) * (size_t)T * H);
+        double* dXs = (double*)malloc(sizeof(double) * (size_t)T * H);
+        swiglu_forward(T, H, Fs, x, Wsg, Wsu, Wsd, A, U, Hh, Ys);
+        swiglu_backward(T, H, Fs, x, Wsg, Wsu, Wsd, A, U, Hh, dY, dXs, dWsg, dWsu, dWsd);
+        for (size_t i = 0; i < (size_t)T * H; ++i) dX[i] += dXs[i];
+        free(A); free(U); free(Hh); free(Ys); free(dXs);
+    }
+    if (dg_out) memcpy(dg_out, dg, sizeof(double) * (size_t)R);
+    free(dz); free(Xp); free(Yp); free(dYp); free(dXp); free(dg);
+    free(counts); free(offsets); free(row_of); free(slot_of);
+    return 0;
+}
+
+/* ------------------------------------------------- sampled, large layers */
+/*
+ * The two functions below compute single outputs of the same definitions
+ * without materialising the whole layer, for layers too large for the
+ * functions above. Weights are read in their storage format and widened
+ * exactly: wtype 0 = float32, 1 = bfloat16 bits (uint16). Per-expert weight
+ * blocks are passed as pointer arrays (entries may be NULL for experts that
+ * are not touched).
+ */
+static double ld(const void* p, int wtype, size_t i)
+{
+    if (wtype == 0) return (double)((const float*)p)[i];
+    uint32_t bits = (uint32_t)((const uint16_t*)p)[i] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* Forward of one expert for one token: a, u, hh (F each) and y (H). */
+static void token_expert_fwd(int H, int F, const double* xt, const void* Wg, const void* Wu,
+                             const void* Wd, int wtype, double* a, double* u, double* hh,
+                             double* y)
+{
+    for (int f = 0; f < F; ++f) {
+        double sa = 0.0, su = 0.0;
+        for (int h = 0; h < H; ++h) {
+            sa += xt[h] * ld(Wg, wtype, (size_t)h * F + f);
+            su += xt[h] * ld(Wu, wtype, (size_t)h * F + f);
+        }
+        a[f] = sa; u[f] = su; hh[f] = silu(sa) * su;
+    }
+    for (int h = 0; h < H; ++h) y[h] = 0.0;
+    for (int f = 0; f < F; ++f)
+        for (int h = 0; h < H; ++h) y[h] += hh[f] * ld(Wd, wtype, (size_t)f * H + h);
+}
+
+/* dX contribution of one expert for one token, given that row's output
+ * gradient dyr (H): dh = Wd dyr, dA, dU, then dA Wg^T + dU Wu^T into dxt. */
+static void token_expert_dx(int H, int F, const void* Wg, const void* Wu, const void* Wd, int wtype,
+                            const double* a, const double* u, const double* dyr, double* dxt)
+{
+    for (int f = 0; f < F; ++f) {
+        double dh = 0.0;
+        for (int h = 0; h < H; ++h) dh += dyr[h] * ld(Wd, wtype, (size_t)f * H + h);
+        double dA = dh * u[f] * dsilu(a[f]);
+        double dU = dh * silu(a[f]);
+        for (int h = 0; h < H; ++h)
+            dxt[h] += dA * ld(Wg, wtype, (size_t)h * F + f) + dU * ld(Wu, wtype, (size_t)h * F + f);
+    }
+}
+
+/*
+ * Output rows y[t] and dX[t] (and dg[t, :]) for n listed tokens.
+ * xs, dYs: n*H fp64 rows of those tokens; topk, gates: n*k; scores: n*E
+ * (from oracle_route on the same rows). Wg_e/Wu_e/Wd_e: E pointers to the
+ * H*F, H*F, F*H blocks; Ws*: the shared expert (Fs may be 0).
+ * Outputs: y n*H, dX n*H, dg n*k.
+ */
+int oracle_token_rows(int n, int H, int E, int k, int F, int Fs, int score_fn, int wtype,
+                      const double* xs, const double* dYs, const double* Wr,
+                      const void* const* Wg_e, const void* const* Wu_e, const void* const* Wd_e,
+                      const void* Wsg, const void* Wsu, const void* Wsd,
+                      const int* topk, const double* gates, const double* scores,
+                      double* y, double* dX, double* dg)
+{
+    if (n < 0 || H <= 0 || E <= 0 || k <= 0 || k > E || k > 1024 || F <= 0 || Fs < 0) return -1;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int i = 0; i < n; ++i) {
+        const double* xt = xs + (size_t)i * H;
+        const double* dyt = dYs + (size_t)i * H;
+        int Fm = F > Fs ? F : Fs;
+        double* a = (double*)malloc(sizeof(double) * Fm);
+        double* u = (double*)malloc(sizeof(double) * Fm);
+        double* hh = (double*)malloc(sizeof(double) * Fm);
+        double* ye = (double*)malloc(sizeof(double) * H);
+        double* dyr = (double*)malloc(sizeof(double) * H);
+        double* yt = y + (size_t)i * H;
+        double* dxt = dX + (size_t)i * H;
+        const int* sel = topk + (size_t)i * k;
+        const double* g = gates + (size_t)i * k;
+        double dgt[1024], dz[1024];
+        for (int h = 0; h < H; ++h) { yt[h] = 0.0; dxt[h] = 0.0; }
+        for (int j = 0; j < k; ++j) {
+            int e = sel[j];
+            if (e < 0 || e >= E || !Wg_e[e] || !Wu_e[e] || !Wd_e[e]) { bad = 1; continue; }
+            token_expert_fwd(H, F, xt, Wg_e[e], Wu_e[e], Wd_e[e], wtype, a, u, hh, ye);
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h) {
+                yt[h] += g[j] * ye[h];
+                acc += dyt[h] * ye[h];
+                dyr[h] = g[j] * dyt[h];
+            }
+            dgt[j] = acc;
+            token_expert_dx(H, F, Wg_e[e], Wu_e[e], Wd_e[e], wtype, a, u, dyr, dxt);
+        }
+        router_dz(k, score_fn, sel, g, scores + (size_t)i * E, dgt, dz);
+        for (int j = 0; j < k; ++j) {
+            dg[(size_t)i * k + j] = dgt[j];
+            for (int h = 0; h < H; ++h) dxt[h] += dz[j] * Wr[(size_t)h * E + sel[j]];
+        }
+        if (Fs > 0) {
+            token_expert_fwd(H, Fs, xt, Wsg, Wsu, Wsd, wtype, a, u, hh, ye);
+            for (int h = 0; h < H; ++h) yt[h] += ye[h];
+            token_expert_dx(H, Fs, Wsg, Wsu, Wsd, wtype, a, u, dyt, dxt);
+        }
+        free(a); free(u); free(hh); free(ye); free(dyr);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Single weight-gradient entries. which: 0 dWg[e][i][j] (i = h, j = f),
+ * 1 dWu[e][i][j], 2 dWd[e][i][j] (i = f, j = h), 3 dWsg[i][j], 4 dWsu[i][j],
+ * 5 dWsd[i][j]. Each is a sum over the tokens that chose expert e (all
+ * tokens for the shared expert) of that token's contribution.
+ * x, dY: T*H fp64; topk, gates: T*k of the whole layer.
+ */
+int oracle_dw_entries(int T, int H, int E, int k, int F, int Fs, int wtype,
+                      const double* x, const double* dY,
+                      const void* const* Wg_e, const void* const* Wu_e, const void* const* Wd_e,
+                      const void* Wsg, const void* Wsu, const void* Wsd,
+                      const int* topk, const double* gates,
+                      int n, const int* which, const int* ee, const int* ii, const int* jj,
+                      double* out)
+{
+    if (T <= 0 || H <= 0 || E <= 0 || k <= 0 || F <= 0 || Fs < 0) return -1;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int q = 0; q < n; ++q) {
+        int w = which[q], e = ee[q], i = ii[q], j = jj[q];
+        int shared = w >= 3;
+        int Fw = shared ? Fs : F;
+        const void *Wg = shared ? Wsg : (e >= 0 && e < E ? Wg_e[e] : NULL);
+        const void *Wu = shared ? Wsu : (e >= 0 && e < E ? Wu_e[e] : NULL);
+        const void *Wd = shared ? Wsd : (e >= 0 && e < E ? Wd_e[e] : NULL);
+        if (!Wg || !Wu || !Wd || Fw <= 0) { bad = 1; out[q] = NAN; continue; }
+        int kind = w % 3;
+        double acc = 0.0;
+        for (int t = 0; t < T; ++t) {
+            double g = 1.0;
+            if (!shared) {
+                int hit = -1;
+                for (int s = 0; s < k; ++s) if (topk[(size_t)t * k + s] == e) hit = s;
+                if (hit < 0) continue;
+                g = gates[(size_t)t * k + hit];
+            }
+            const double* xt = x + (size_t)t * H;
+            const double* dyt = dY + (size_t)t * H;
+            int f = (kind == 2) ? i : j;
+            double a = 0.0, u = 0.0;
+            for (int h = 0; h < H; ++h) {
+                a += xt[h] * ld(Wg, wtype, (size_t)h * Fw + f);
+                u += xt[h] * ld(Wu, wtype, (size_t)h * Fw + f);
+            }
+            if (kind == 2) {
+                acc += silu(a) * u * g * dyt[j];
+            } else {
+                double dh = 0.0;
+                for (int h = 0; h < H; ++h) dh += g * dyt[h] * ld(Wd, wtype, (size_t)f * H + h);
+                double d = (kind == 0) ? dh * u * dsilu(a) : dh * silu(a);
+                acc += xt[i] * d;
+            }
+        }
+        out[q] = acc;
+    }
+    return bad ? -1 : 0;
+}
