@@ -1,0 +1,172 @@
+/*
+ * moe.h -- C ABI of a single-GPU Mixture-of-Experts layer for GB300 (sm_103a),
+ * forward and backward.
+ *
+ * The layer is the one described in "Scalable Training of Mixture-of-Experts
+ * Models with Megatron Core", §2 (Megatron-Core MoE Architecture): Route
+ * (router logits -> probabilities -> top-k experts, routing weights and a
+ * token-expert assignment), Dispatch (permute tokens by destination expert),
+ * Expert Computation (all experts' FFNs as grouped GEMMs) and Combine
+ * (restore token order, weight by the gates, add a shared expert's output).
+ * §5 (Selective precision) keeps the router in FP32; §5 (Kernel and shape
+ * optimization) pads expert segments with zero rows to aligned sizes; §7
+ * (Load Balancing) lists dropless dispatch, which is the only mode here.
+ *
+ * Formulas (the pages print none; these are the plain readings):
+ *   z = x Wr + b                     (fp32; b optional, per expert)
+ *   softmax: p = softmax(z);  sigmoid: s = 1 / (1 + exp(-z))
+ *   S_t = the k experts with the largest score, slots in descending score
+ *   g_tj = score_{e_tj} / sum_{i in S_t} score_i
+ *   expert e (SwiGLU): a = x Wg_e, u = x Wu_e, h = silu(a) u, y_e = h Wd_e
+ *   y_t = sum_j g_tj y_{e_tj}(x_t) + shared(x_t)
+ * The backward returns the gradient of sum(dY * y) with the routing held
+ * fixed; no gradient flows to b.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers on the plan's device, row-major,
+ *     16-byte aligned, owned by the caller. The library never allocates,
+ *     frees or keeps device memory; the plan holds host state only.
+ *   - Work is enqueued on `stream` (a cudaStream_t) and returns without
+ *     synchronising. No call copies device data to the host, so forward and
+ *     backward can be captured in a CUDA graph.
+ *   - Arguments are validated before anything is enqueued; on any error
+ *     nothing is launched and the status says why.
+ *   - Errors detected on the device (a pipeline wait that timed out) are
+ *     written to a status word at the start of the workspace; read them
+ *     with moe_read_status.
+ *   - Calls on different streams must use different workspaces.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,          /* null pointer, bad size or enum     */
+    MOE_ERR_UNSUPPORTED = 2,          /* valid request this build cannot run */
+    MOE_ERR_MISALIGNED = 3,           /* a pointer is not 16-byte aligned    */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 4,  /* saved or workspace buffer too small */
+    MOE_ERR_CUDA = 5,                 /* a CUDA runtime call failed          */
+    MOE_ERR_DEVICE_TIMEOUT = 6        /* a device-side wait ran out          */
+} moe_status_t;
+
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
+
+/* Storage and arithmetic type of activations and expert weights.
+ *   MOE_FP32: fp32 storage, fp32 FMA arithmetic throughout.
+ *   MOE_BF16: bf16 storage, tensor-core GEMMs with fp32 accumulation.
+ *   MOE_FP8_BLOCK: blockwise-scaled E4M3 (not available in this build). */
+typedef enum { MOE_FP32 = 0, MOE_BF16 = 1, MOE_FP8_BLOCK = 2 } moe_dtype_t;
+
+typedef struct {
+    int H;       /* hidden size; multiple of 128                          */
+    int E;       /* routed experts, 1..256                                  */
+    int F;       /* routed expert FFN width; multiple of 128                */
+    int Fs;      /* shared expert FFN width; 0 = no shared expert, else a
+                    multiple of 128                                         */
+    int top_k;   /* experts per token, 1..min(E, 8)                         */
+    int T_max;   /* largest token count a call may pass, >= 1               */
+    int score;   /* moe_score_t                                             */
+    int dtype;   /* moe_dtype_t                                             */
+    unsigned flags; /* reserved, must be 0                                  */
+} moe_config_t;
+
+typedef struct moe_plan_s* moe_plan_t;
+
+/* Opaque CUDA stream handle; pass a cudaStream_t (0 = legacy default). */
+typedef struct CUstream_st* moe_stream_t;
+
+/* Forward arguments. Element type "act" = fp32 for MOE_FP32, bf16 for
+ * MOE_BF16. Optional outputs may be NULL. */
+typedef struct {
+    const void*  x;        /* T×H act: token hidden states                */
+    const float* Wr;       /* H×E fp32: router weight                      */
+    const float* b;        /* E fp32 router logit bias, or NULL            */
+    const void*  W_gate;   /* E×H×F act                                    */
+    const void*  W_up;     /* E×H×F act                                    */
+    const void*  W_down;   /* E×F×H act                                    */
+    const void*  Ws_gate;  /* H×Fs act (NULL iff Fs == 0)                   */
+    const void*  Ws_up;    /* H×Fs act                                      */
+    const void*  Ws_down;  /* Fs×H act                                      */
+    void*        y;        /* out, T×H act                                  */
+    int32_t*     topk_idx; /* optional out, T×k: chosen experts, slot order */
+    float*       gates;    /* optional out, T×k: renormalised gates         */
+    int32_t*     counts;   /* optional out, E: tokens per expert            */
+    int32_t*     offsets;  /* optional out, E+1: first padded row of each
+                              expert's segment (segments padded to 128 rows) */
+    int32_t*     row_of;   /* optional out, T×k: padded row of (t, j)        */
+} moe_fwd_args_t;
+
+/* Backward arguments. Gradients are overwritten (not accumulated); experts
+ * that received no token get zero weight gradients. */
+typedef struct {
+    const void*  dY;       /* T×H act: gradient of the layer output         */
+    const void*  x;        /* the forward's x                                */
+    const float* Wr;       /* the forward's router weight                     */
+    const void*  W_gate;   /* the forward's expert weights                    */
+    const void*  W_up;
+    const void*  W_down;
+    const void*  Ws_gate;  /* the forward's shared-expert weights (or NULL)   */
+    const void*  Ws_up;
+    const void*  Ws_down;
+    void*        dX;       /* out, T×H act                                   */
+    float*       dWr;      /* out, H×E fp32                                  */
+    void*        dW_gate;  /* out, E×H×F act                                 */
+    void*        dW_up;    /* out, E×H×F act                                 */
+    void*        dW_down;  /* out, E×F×H act                                 */
+    void*        dWs_gate; /* out, H×Fs act (NULL iff Fs == 0)                */
+    void*        dWs_up;
+    void*        dWs_down;
+} moe_bwd_args_t;
+
+/* Validate `cfg` for `device` and build a plan (host memory only).
+ * Errors: INVALID_ARG (null, sizes out of range, flags != 0),
+ *         UNSUPPORTED (dtype not built, device not sm_103), CUDA. */
+moe_status_t moe_plan_create(const moe_config_t* cfg, int device, moe_plan_t* out);
+
+/* Free a plan. NULL is accepted. */
+moe_status_t moe_plan_destroy(moe_plan_t plan);
+
+/* Bytes of the two caller-owned buffers for a call with T tokens:
+ *   saved: written by moe_forward, read by moe_backward (routing, permuted
+ *          activations and FFN intermediates of that forward);
+ *   ws:    scratch for either call; its first 256 bytes hold the status word.
+ * Errors: INVALID_ARG (null, T < 1 or T > T_max). */
+moe_status_t moe_workspace_size(moe_plan_t plan, int T, size_t* saved_bytes, size_t* ws_bytes);
+
+/* Enqueue the forward pass for T tokens: Route, Dispatch, Expert
+ * Computation, Combine. Writes args->y, the optional outputs and `saved`.
+ * Errors: INVALID_ARG, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA. */
+moe_status_t moe_forward(moe_plan_t plan, int T, const moe_fwd_args_t* args,
+                         void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                         moe_stream_t stream);
+
+/* Enqueue the backward pass for T tokens, using the `saved` buffer of the
+ * forward with the same T, inputs and weights (it is only read).
+ * Errors: INVALID_ARG, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA. */
+moe_status_t moe_backward(moe_plan_t plan, int T, const moe_bwd_args_t* args,
+                          const void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                          moe_stream_t stream);
+
+/* Synchronise `stream`, then return the device status word kept in `ws`
+ * (MOE_OK or MOE_ERR_DEVICE_TIMEOUT); CUDA errors give MOE_ERR_CUDA. */
+moe_status_t moe_read_status(moe_plan_t plan, const void* ws, moe_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* moe_status_string(moe_status_t status);
+
+/* MOE_ABI_VERSION of the loaded library. */
+int moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,466 @@
+// api.cu -- the C ABI of include/moe.h: argument validation, the layout of
+// the caller-owned `saved` and workspace buffers, and the launch sequence of
+// the forward and backward passes.
+//
+// Stage order follows "Scalable Training of Mixture-of-Experts Models with
+// Megatron Core", §2: Route -> Dispatch (permute) -> Expert Computation
+// (grouped GEMMs) -> Combine; the backward runs the same stages in reverse.
+// Nothing here reads device data on the host, so a call is a pure sequence of
+// kernel launches (and one status-word memset) on the caller's stream.
+#include "internal.h"
+
+#include <new>
+#include <string.h>
+
+namespace moe {
+namespace {
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Layout {
+    int T, R, Rp_max, MT_max, NB;
+    // saved
+    size_t topk, gates, selsc, counts, poff, meta, tiletab, rowof, slotof;
+    size_t Xp, A, U, Hh, Yp, As, Us, Hs, saved_bytes;
+    // workspace
+    size_t status, hist, blkbase, Ys, dYp, dA, dU, dXp, dz, WrT, dAs, dUs, dXs, ws_bytes;
+};
+
+Layout make_layout(const moe_config_t& c, int T)
+{
+    Layout L;
+    const size_t es = (c.dtype == MOE_FP32) ? 4 : 2;
+    L.T = T;
+    L.R = T * c.top_k;
+    const int nonempty = L.R < c.E ? L.R : c.E;
+    L.Rp_max = (int)align_up((size_t)L.R + (size_t)nonempty * (kTileM - 1), kTileM);
+    L.MT_max = L.Rp_max / kTileM;
+    L.NB = (T + kRouterTokens - 1) / kRouterTokens;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
+    L.topk = take(sizeof(int) * L.R);
+    L.gates = take(sizeof(float) * L.R);
+    L.selsc = take(sizeof(float) * L.R);
+    L.counts = take(sizeof(int) * c.E);
+    L.poff = take(sizeof(int) * (c.E + 1));
+    L.meta = take(sizeof(int) * 4);
+    L.tiletab = take(sizeof(int) * L.MT_max);
+    L.rowof = take(sizeof(int) * L.R);
+    L.slotof = take(sizeof(int) * L.Rp_max);
+    L.Xp = take(es * L.Rp_max * c.H);
+    L.A = take(es * L.Rp_max * c.F);
+    L.U = take(es * L.Rp_max * c.F);
+    L.Hh = take(es * L.Rp_max * c.F);
+    L.Yp = take(es * L.Rp_max * c.H);
+    L.As = take(es * (size_t)T * c.Fs);
+    L.Us = take(es * (size_t)T * c.Fs);
+    L.Hs = take(es * (size_t)T * c.Fs);
+    L.saved_bytes = o;
+    o = 0;
+    L.status = take(256);
+    L.hist = take(sizeof(int) * (size_t)L.NB * c.E);
+    L.blkbase = take(sizeof(int) * (size_t)L.NB * c.E);
+    L.Ys = take(c.Fs ? es * (size_t)T * c.H : 0);
+    L.dYp = take(es * L.Rp_max * c.H);
+    L.dA = take(es * L.Rp_max * c.F);
+    L.dU = take(es * L.Rp_max * c.F);
+    L.dXp = take(es * L.Rp_max * c.H);
+    L.dz = take(sizeof(float) * L.R);
+    L.WrT = take(sizeof(float) * (size_t)c.E * c.H);
+    L.dAs = take(es * (size_t)T * c.Fs);
+    L.dUs = take(es * (size_t)T * c.Fs);
+    L.dXs = take(c.Fs ? es * (size_t)T * c.H : 0);
+    L.ws_bytes = o;
+    return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t check_config(const moe_config_t* c)
+{
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->H <= 0 || c->H % 128 || c->E < 1 || c->E > kMaxE || c->F <= 0 || c->F % 128 ||
+        c->Fs < 0 || c->Fs % 128 || c->top_k < 1 || c->top_k > kMaxK || c->top_k > c->E ||
+        c->T_max < 1 || c->flags != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+    if (c->dtype != MOE_FP32 && c->dtype != MOE_BF16 && c->dtype != MOE_FP8_BLOCK)
+        return MOE_ERR_INVALID_ARG;
+    if (c->dtype == MOE_FP8_BLOCK) return MOE_ERR_UNSUPPORTED;
+    // int32 row indices: R_pad * max(H, F) elements must stay addressable per
+    // buffer with 32-bit row numbers
+    const long long R = (long long)c->T_max * c->top_k + (long long)c->E * kTileM;
+    if (R > (1ll << 30)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+// Keeps the caller's current device and switches to the plan's for a call.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) return;
+        ok = (prev == dev) || cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard() {
+        int cur;
+        if (ok && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+}  // namespace moe
+
+struct moe_plan_s {
+    moe_config_t cfg;
+    int device;
+    int num_sms;
+};
+
+using namespace moe;
+
+// The functions below are declared extern "C" in moe.h, which gives them C linkage.
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_status_string(moe_status_t s)
+{
+    switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "saved or workspace buffer too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side pipeline wait timed out";
+    }
+    return "unknown status";
+}
+
+moe_status_t moe_plan_create(const moe_config_t* cfg, int device, moe_plan_t* out)
+{
+    if (!out) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    moe_status_t st = check_config(cfg);
+    if (st != MOE_OK) return st;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (device < 0 || device >= ndev) return MOE_ERR_INVALID_ARG;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MOE_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return MOE_ERR_UNSUPPORTED;   // built for sm_103a only
+    {
+        DeviceGuard g(device);
+        if (!g.ok) return MOE_ERR_CUDA;
+        if (cfg->dtype == MOE_BF16 && gemm_tc_prepare(device) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    moe_plan_s* p = new (std::nothrow) moe_plan_s;
+    if (!p) return MOE_ERR_CUDA;
+    p->cfg = *cfg;
+    p->device = device;
+    p->num_sms = prop.multiProcessorCount;
+    *out = p;
+    return MOE_OK;
+}
+
+moe_status_t moe_plan_destroy(moe_plan_t plan)
+{
+    delete plan;
+    return MOE_OK;
+}
+
+moe_status_t moe_workspace_size(moe_plan_t plan, int T, size_t* saved_bytes, size_t* ws_bytes)
+{
+    if (!plan || !saved_bytes || !ws_bytes || T < 1 || T > plan->cfg.T_max) return MOE_ERR_INVALID_ARG;
+    Layout L = make_layout(plan->cfg, T);
+    *saved_bytes = L.saved_bytes;
+    *ws_bytes = L.ws_bytes;
+    return MOE_OK;
+}
+
+#define MOE_CUDA(call)                                   \
+    do {                                                 \
+        if ((call) != cudaSuccess) return MOE_ERR_CUDA;  \
+    } while (0)
+
+template <typename T>
+static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, uint8_t* sv,
+                                 uint8_t* ws, cudaStream_t s)
+{
+    const moe_config_t& c = p->cfg;
+    const Layout L = make_layout(c, T_);
+    const int H = c.H, E = c.E, k = c.top_k, F = c.F, Fs = c.Fs;
+    DeviceStatus* status = reinterpret_cast<DeviceStatus*>(ws + L.status);
+    int* topk = reinterpret_cast<int*>(sv + L.topk);
+    float* gates = reinterpret_cast<float*>(sv + L.gates);
+    float* selsc = reinterpret_cast<float*>(sv + L.selsc);
+    int* counts = reinterpret_cast<int*>(sv + L.counts);
+    int* poff = reinterpret_cast<int*>(sv + L.poff);
+    int* meta = reinterpret_cast<int*>(sv + L.meta);
+    int* tiletab = reinterpret_cast<int*>(sv + L.tiletab);
+    int* rowof = reinterpret_cast<int*>(sv + L.rowof);
+    int* slotof = reinterpret_cast<int*>(sv + L.slotof);
+    T* Xp = reinterpret_cast<T*>(sv + L.Xp);
+    T* A = reinterpret_cast<T*>(sv + L.A);
+    T* U = reinterpret_cast<T*>(sv + L.U);
+    T* Hh = reinterpret_cast<T*>(sv + L.Hh);
+    T* Yp = reinterpret_cast<T*>(sv + L.Yp);
+    T* Ys = Fs ? reinterpret_cast<T*>(ws + L.Ys) : nullptr;
+    const T* x = static_cast<const T*>(a->x);
+
+    MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
+    MOE_CUDA(launch_router<T>(x, a->Wr, a->b, T_, H, E, k, c.score, topk, gates, selsc,
+                              reinterpret_cast<int*>(ws + L.hist), s));
+    MOE_CUDA(launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
+                         reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s));
+    MOE_CUDA(launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
+    MOE_CUDA(launch_permute<T>(x, rowof, poff, counts, T_, H, E, k, Xp, s));
+
+    auto gemm = [&](const GemmDesc& d) -> cudaError_t {
+        if (c.dtype == MOE_FP32) return launch_gemm_simt_f32(d, L.MT_max, s);
+        return launch_gemm_tc_bf16(d, L.MT_max, p->num_sms, s);
+    };
+    GemmDesc d;
+    // fc1 + SwiGLU over the routed rows: [A | U] = Xp [Wg | Wu], Hh = silu(A) U
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
+    d.N = F; d.K = H; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.A0 = Xp; d.lda = H; d.a_rows = L.Rp_max;
+    d.B0 = a->W_gate; d.B1 = a->W_up; d.ldb = F; d.b_kmajor = 0; d.b_estride = (long long)H * F;
+    d.b_rows = E * H;
+    d.O0 = A; d.O1 = U; d.O2 = Hh; d.ldo = F; d.status = status;
+    MOE_CUDA(gemm(d));
+    // fc2: Yp = Hh Wd
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
+    d.N = H; d.K = F; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.A0 = Hh; d.lda = F; d.a_rows = L.Rp_max;
+    d.B0 = a->W_down; d.ldb = H; d.b_kmajor = 0; d.b_estride = (long long)F * H; d.b_rows = E * F;
+    d.O0 = Yp; d.ldo = H; d.status = status;
+    MOE_CUDA(gemm(d));
+    if (Fs) {
+        T* As = reinterpret_cast<T*>(sv + L.As);
+        T* Us = reinterpret_cast<T*>(sv + L.Us);
+        T* Hs = reinterpret_cast<T*>(sv + L.Hs);
+        memset(&d, 0, sizeof d);
+        d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
+        d.N = Fs; d.K = H; d.E = 1; d.dense_rows = T_;
+        d.A0 = x; d.lda = H; d.a_rows = T_;
+        d.B0 = a->Ws_gate; d.B1 = a->Ws_up; d.ldb = Fs; d.b_kmajor = 0; d.b_rows = H;
+        d.O0 = As; d.O1 = Us; d.O2 = Hs; d.ldo = Fs; d.status = status;
+        MOE_CUDA(gemm(d));
+        memset(&d, 0, sizeof d);
+        d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
+        d.N = H; d.K = Fs; d.E = 1; d.dense_rows = T_;
+        d.A0 = Hs; d.lda = Fs; d.a_rows = T_;
+        d.B0 = a->Ws_down; d.ldb = H; d.b_kmajor = 0; d.b_rows = Fs;
+        d.O0 = Ys; d.ldo = H; d.status = status;
+        MOE_CUDA(gemm(d));
+    }
+    MOE_CUDA(launch_combine<T>(Yp, Ys, rowof, gates, T_, H, k, static_cast<T*>(a->y), s));
+
+    if (a->topk_idx) MOE_CUDA(cudaMemcpyAsync(a->topk_idx, topk, sizeof(int) * L.R, cudaMemcpyDeviceToDevice, s));
+    if (a->gates) MOE_CUDA(cudaMemcpyAsync(a->gates, gates, sizeof(float) * L.R, cudaMemcpyDeviceToDevice, s));
+    if (a->counts) MOE_CUDA(cudaMemcpyAsync(a->counts, counts, sizeof(int) * E, cudaMemcpyDeviceToDevice, s));
+    if (a->offsets) MOE_CUDA(cudaMemcpyAsync(a->offsets, poff, sizeof(int) * (E + 1), cudaMemcpyDeviceToDevice, s));
+    if (a->row_of) MOE_CUDA(cudaMemcpyAsync(a->row_of, rowof, sizeof(int) * L.R, cudaMemcpyDeviceToDevice, s));
+    return MOE_OK;
+}
+
+template <typename T>
+static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a, const uint8_t* svc,
+                                  uint8_t* ws, cudaStream_t s)
+{
+    const moe_config_t& c = p->cfg;
+    const Layout L = make_layout(c, T_);
+    const int H = c.H, E = c.E, k = c.top_k, F = c.F, Fs = c.Fs;
+    uint8_t* sv = const_cast<uint8_t*>(svc);   // only read below
+    DeviceStatus* status = reinterpret_cast<DeviceStatus*>(ws + L.status);
+    const int* topk = reinterpret_cast<const int*>(sv + L.topk);
+    const float* gates = reinterpret_cast<const float*>(sv + L.gates);
+    const float* selsc = reinterpret_cast<const float*>(sv + L.selsc);
+    const int* counts = reinterpret_cast<const int*>(sv + L.counts);
+    const int* poff = reinterpret_cast<const int*>(sv + L.poff);
+    const int* meta = reinterpret_cast<const int*>(sv + L.meta);
+    const int* tiletab = reinterpret_cast<const int*>(sv + L.tiletab);
+    const int* rowof = reinterpret_cast<const int*>(sv + L.rowof);
+    const int* slotof = reinterpret_cast<const int*>(sv + L.slotof);
+    const T* Xp = reinterpret_cast<const T*>(sv + L.Xp);
+    const T* A = reinterpret_cast<const T*>(sv + L.A);
+    const T* U = reinterpret_cast<const T*>(sv + L.U);
+    const T* Hh = reinterpret_cast<const T*>(sv + L.Hh);
+    const T* Yp = reinterpret_cast<const T*>(sv + L.Yp);
+    T* dYp = reinterpret_cast<T*>(ws + L.dYp);
+    T* dA = reinterpret_cast<T*>(ws + L.dA);
+    T* dU = reinterpret_cast<T*>(ws + L.dU);
+    T* dXp = reinterpret_cast<T*>(ws + L.dXp);
+    float* dz = reinterpret_cast<float*>(ws + L.dz);
+    float* WrT = reinterpret_cast<float*>(ws + L.WrT);
+    const T* dY = static_cast<const T*>(a->dY);
+
+    auto gemm = [&](const GemmDesc& d) -> cudaError_t {
+        if (c.dtype == MOE_FP32) return launch_gemm_simt_f32(d, L.MT_max, s);
+        return launch_gemm_tc_bf16(d, L.MT_max, p->num_sms, s);
+    };
+
+    MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
+    // Combine backward: gate gradients, gate-scaled output gradients, router dz
+    MOE_CUDA(launch_gate_grad<T>(dY, Yp, rowof, topk, gates, selsc, poff, counts, T_, H, E, k,
+                                 c.score, dYp, dz, s));
+    GemmDesc d;
+    // fc2 dgrad + SwiGLU backward: dh = dYp Wd^T -> dA, dU
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_BWD; d.dual = DUAL_NONE;
+    d.N = F; d.K = H; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.A0 = dYp; d.lda = H; d.a_rows = L.Rp_max;
+    d.B0 = a->W_down; d.ldb = H; d.b_kmajor = 1; d.b_estride = (long long)F * H; d.b_rows = E * F;
+    d.X0 = A; d.X1 = U; d.O0 = dA; d.O1 = dU; d.ldo = F; d.status = status;
+    MOE_CUDA(gemm(d));
+    // fc2 wgrad: dWd[e] = Hh_e^T dYp_e
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
+    d.N = H; d.M_out = F; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.A0 = Hh; d.lda = F; d.a_rows = L.Rp_max;
+    d.B0 = dYp; d.ldb = H; d.b_rows = L.Rp_max;
+    d.O0 = a->dW_down; d.ldo = H; d.o_estride = (long long)F * H; d.status = status;
+    MOE_CUDA(gemm(d));
+    // fc1 dgrad: dXp = dA Wg^T + dU Wu^T
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
+    d.N = H; d.K = F; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.A0 = dA; d.A1 = dU; d.lda = F; d.a_rows = L.Rp_max;
+    d.B0 = a->W_gate; d.B1 = a->W_up; d.ldb = F; d.b_kmajor = 1; d.b_estride = (long long)H * F;
+    d.b_rows = E * H;
+    d.O0 = dXp; d.ldo = H; d.status = status;
+    MOE_CUDA(gemm(d));
+    // fc1 wgrad: dWg[e] = Xp_e^T dA_e, dWu[e] = Xp_e^T dU_e
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
+    d.N = F; d.M_out = H; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.A0 = Xp; d.lda = H; d.a_rows = L.Rp_max;
+    d.B0 = dA; d.B1 = dU; d.ldb = F; d.b_rows = L.Rp_max;
+    d.O0 = a->dW_gate; d.O1 = a->dW_up; d.ldo = F; d.o_estride = (long long)H * F; d.status = status;
+    MOE_CUDA(gemm(d));
+
+    T* dXs = nullptr;
+    if (Fs) {
+        const T* As = reinterpret_cast<const T*>(sv + L.As);
+        const T* Us = reinterpret_cast<const T*>(sv + L.Us);
+        const T* Hs = reinterpret_cast<const T*>(sv + L.Hs);
+        T* dAs = reinterpret_cast<T*>(ws + L.dAs);
+        T* dUs = reinterpret_cast<T*>(ws + L.dUs);
+        dXs = reinterpret_cast<T*>(ws + L.dXs);
+        // shared expert: its output gradient is dY itself (unweighted add)
+        memset(&d, 0, sizeof d);
+        d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_BWD; d.dual = DUAL_NONE;
+        d.N = Fs; d.K = H; d.E = 1; d.dense_rows = T_;
+        d.A0 = dY; d.lda = H; d.a_rows = T_;
+        d.B0 = a->Ws_down; d.ldb = H; d.b_kmajor = 1; d.b_rows = Fs;
+        d.X0 = As; d.X1 = Us; d.O0 = dAs; d.O1 = dUs; d.ldo = Fs; d.status = status;
+        MOE_CUDA(gemm(d));
+        memset(&d, 0, sizeof d);
+        d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
+        d.N = H; d.M_out = Fs; d.E = 1; d.dense_rows = T_;
+        d.A0 = Hs; d.lda = Fs; d.a_rows = T_;
+        d.B0 = dY; d.ldb = H; d.b_rows = T_;
+        d.O0 = a->dWs_down; d.ldo = H; d.status = status;
+        MOE_CUDA(gemm(d));
+        memset(&d, 0, sizeof d);
+        d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
+        d.N = H; d.K = Fs; d.E = 1; d.dense_rows = T_;
+        d.A0 = dAs; d.A1 = dUs; d.lda = Fs; d.a_rows = T_;
+        d.B0 = a->Ws_gate; d.B1 = a->Ws_up; d.ldb = Fs; d.b_kmajor = 1; d.b_rows = H;
+        d.O0 = dXs; d.ldo = H; d.status = status;
+        MOE_CUDA(gemm(d));
+        memset(&d, 0, sizeof d);
+        d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
+        d.N = Fs; d.M_out = H; d.E = 1; d.dense_rows = T_;
+        d.A0 = a->x; d.lda = H; d.a_rows = T_;
+        d.B0 = dAs; d.B1 = dUs; d.ldb = Fs; d.b_rows = T_;
+        d.O0 = a->dWs_gate; d.O1 = a->dWs_up; d.ldo = Fs; d.status = status;
+        MOE_CUDA(gemm(d));
+    }
+    // router backward and the unpermute-reduce of dX
+    MOE_CUDA(launch_router_wgrad<T>(Xp, slotof, poff, counts, dz, H, E, k, a->dWr, s));
+    MOE_CUDA(launch_transpose_f32(a->Wr, H, E, WrT, s));
+    MOE_CUDA(launch_unpermute_reduce<T>(dXp, dXs, rowof, topk, dz, WrT, T_, H, k,
+                                        static_cast<T*>(a->dX), s));
+    return MOE_OK;
+}
+
+static moe_status_t check_call(moe_plan_t plan, int T, const void* saved, size_t saved_bytes,
+                               const void* ws, size_t ws_bytes)
+{
+    if (!plan || T < 1 || T > plan->cfg.T_max || !saved || !ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(saved) || !aligned16(ws)) return MOE_ERR_MISALIGNED;
+    Layout L = make_layout(plan->cfg, T);
+    if (saved_bytes < L.saved_bytes || ws_bytes < L.ws_bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return MOE_OK;
+}
+
+moe_status_t moe_forward(moe_plan_t plan, int T, const moe_fwd_args_t* a, void* saved,
+                         size_t saved_bytes, void* ws, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!a) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_call(plan, T, saved, saved_bytes, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    const bool shared = plan->cfg.Fs > 0;
+    if (!a->x || !a->Wr || !a->W_gate || !a->W_up || !a->W_down || !a->y) return MOE_ERR_INVALID_ARG;
+    if (shared != (a->Ws_gate != nullptr) || shared != (a->Ws_up != nullptr) ||
+        shared != (a->Ws_down != nullptr))
+        return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {a->x, a->Wr, a->b, a->W_gate, a->W_up, a->W_down, a->Ws_gate, a->Ws_up,
+                          a->Ws_down, a->y, a->topk_idx, a->gates, a->counts, a->offsets, a->row_of};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return MOE_ERR_MISALIGNED;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return MOE_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (plan->cfg.dtype == MOE_FP32)
+        return forward_impl<float>(plan, T, a, static_cast<uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
+    return forward_impl<__nv_bfloat16>(plan, T, a, static_cast<uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
+}
+
+moe_status_t moe_backward(moe_plan_t plan, int T, const moe_bwd_args_t* a, const void* saved,
+                          size_t saved_bytes, void* ws, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!a) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_call(plan, T, saved, saved_bytes, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    const bool shared = plan->cfg.Fs > 0;
+    if (!a->dY || !a->x || !a->Wr || !a->W_gate || !a->W_up || !a->W_down || !a->dX || !a->dWr ||
+        !a->dW_gate || !a->dW_up || !a->dW_down)
+        return MOE_ERR_INVALID_ARG;
+    const void* sh[] = {a->Ws_gate, a->Ws_up, a->Ws_down, a->dWs_gate, a->dWs_up, a->dWs_down};
+    for (const void* q : sh)
+        if (shared != (q != nullptr)) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {a->dY, a->x, a->Wr, a->W_gate, a->W_up, a->W_down, a->Ws_gate,
+                          a->Ws_up, a->Ws_down, a->dX, a->dWr, a->dW_gate, a->dW_up, a->dW_down,
+                          a->dWs_gate, a->dWs_up, a->dWs_down};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return MOE_ERR_MISALIGNED;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return MOE_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (plan->cfg.dtype == MOE_FP32)
+        return backward_impl<float>(plan, T, a, static_cast<const uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
+    return backward_impl<__nv_bfloat16>(plan, T, a, static_cast<const uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
+}
+
+moe_status_t moe_read_status(moe_plan_t plan, const void* ws, moe_stream_t stream)
+{
+    if (!plan || !ws) return MOE_ERR_INVALID_ARG;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return MOE_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    DeviceStatus h;
+    if (cudaMemcpy(&h, ws, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    return h.code == 0 ? MOE_OK : static_cast<moe_status_t>(h.code);
+}

@@ -1,0 +1,337 @@
+// dispatch.cu -- memory-bound stages of the MoE layer: Dispatch (permute),
+// Combine, and their backward counterparts.
+//
+// "Scalable Training of Mixture-of-Experts Models with Megatron Core", §2:
+// Dispatch "permutes tokens by destination expert"; Combine "restores
+// sequence order" and "can add a shared expert's output". §5 ("Kernel and
+// shape optimization"): expert activations are emitted zero-padded to aligned
+// sizes, here 128-row segments. Every kernel moves whole rows with 16-byte
+// vector loads and stores and sums in fp32 in a fixed slot order, so results
+// are deterministic (no floating-point atomics).
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+// 16-byte vectors of 4 fp32 or 8 bf16 values.
+template <typename T> struct Vec;
+template <> struct Vec<float> {
+    static constexpr int N = 4;
+    __device__ static void load(const float* p, float (&v)[4]) {
+        float4 q = *reinterpret_cast<const float4*>(p);
+        v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    }
+    __device__ static void store(float* p, const float (&v)[4]) {
+        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+};
+template <> struct Vec<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
+        uint4 q = *reinterpret_cast<const uint4*>(p);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(h[i]);
+            v[2 * i] = f.x; v[2 * i + 1] = f.y;
+        }
+    }
+    __device__ static void store(__nv_bfloat16* p, const float (&v)[8]) {
+        uint4 q;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        *reinterpret_cast<uint4*>(p) = q;
+    }
+};
+
+constexpr int kRowThreads = 128;
+
+// Zero the pad rows [poff[e] + counts[e], poff[e+1]) of expert e.
+template <typename T>
+__device__ void zero_pad_rows(T* buf, int H, int e, const int* poff, const int* counts)
+{
+    const int r0 = poff[e] + counts[e], r1 = poff[e + 1];
+    const size_t nvec = (size_t)(r1 - r0) * H * sizeof(T) / 16;
+    uint4* p = reinterpret_cast<uint4*>(buf + (size_t)r0 * H);
+    for (size_t i = threadIdx.x; i < nvec; i += blockDim.x) p[i] = make_uint4(0, 0, 0, 0);
+}
+
+// Blocks [0, T): copy x[t] to its k rows. Blocks [T, T+E): zero pad rows.
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads)
+permute_kernel(const T* __restrict__ x, const int* __restrict__ row_of, const int* __restrict__ poff,
+               const int* __restrict__ counts, int T_, int H, int k, T* __restrict__ Xp)
+{
+    const int b = blockIdx.x;
+    if (b >= T_) { zero_pad_rows(Xp, H, b - T_, poff, counts); return; }
+    constexpr int V = 16 / sizeof(T);
+    int rows[kMaxK];
+    for (int j = 0; j < k; ++j) rows[j] = row_of[(size_t)b * k + j];
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)b * H);
+    for (int v = threadIdx.x; v < H / V; v += kRowThreads) {
+        uint4 q = src[v];
+        for (int j = 0; j < k; ++j) reinterpret_cast<uint4*>(Xp + (size_t)rows[j] * H)[v] = q;
+    }
+}
+
+// y[t] = sum_j gates[t, j] Yp[row_of(t, j)] (+ Ys[t]), fp32, slot order.
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads)
+combine_kernel(const T* __restrict__ Yp, const T* __restrict__ Ys, const int* __restrict__ row_of,
+               const float* __restrict__ gates, int H, int k, T* __restrict__ y)
+{
+    constexpr int V = Vec<T>::N;
+    const int t = blockIdx.x;
+    int rows[kMaxK];
+    float g[kMaxK];
+    for (int j = 0; j < k; ++j) { rows[j] = row_of[(size_t)t * k + j]; g[j] = gates[(size_t)t * k + j]; }
+    for (int v = threadIdx.x; v < H / V; v += kRowThreads) {
+        float acc[V], in[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = 0.f;
+        for (int j = 0; j < k; ++j) {
+            Vec<T>::load(Yp + (size_t)rows[j] * H + v * V, in);
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] = fmaf(g[j], in[i], acc[i]);
+        }
+        if (Ys) {
+            Vec<T>::load(Ys + (size_t)t * H + v * V, in);
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] += in[i];
+        }
+        Vec<T>::store(y + (size_t)t * H + v * V, acc);
+    }
+}
+
+// Backward of Combine for token t (blocks [0, T)):
+//   dg_j = <dY_t, Yp[row_j]>,  dYp[row_j] = g_j dY_t,
+// then the router logit gradient of the k selected experts:
+//   softmax: dz_j = g_j (dg_j - sum_i g_i dg_i)
+//   sigmoid: dz_j = s_j (1 - s_j) (dg_j - sum_i g_i dg_i) / sum_i s_i
+// Blocks [T, T+E) zero the pad rows of dYp.
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads)
+gate_grad_kernel(const T* __restrict__ dY, const T* __restrict__ Yp, const int* __restrict__ row_of,
+                 const float* __restrict__ gates, const float* __restrict__ selsc,
+                 const int* __restrict__ poff, const int* __restrict__ counts, int T_, int H, int k,
+                 int score, T* __restrict__ dYp, float* __restrict__ dz)
+{
+    const int b = blockIdx.x;
+    if (b >= T_) { zero_pad_rows(dYp, H, b - T_, poff, counts); return; }
+    constexpr int V = Vec<T>::N;
+    __shared__ float red[kRowThreads / 32][kMaxK];
+    const int t = b;
+    int rows[kMaxK];
+    float g[kMaxK], dot[kMaxK];
+    for (int j = 0; j < kMaxK; ++j) {
+        dot[j] = 0.f;
+        if (j < k) { rows[j] = row_of[(size_t)t * k + j]; g[j] = gates[(size_t)t * k + j]; }
+    }
+    for (int v = threadIdx.x; v < H / V; v += kRowThreads) {
+        float dy[V], yp[V], o[V];
+        Vec<T>::load(dY + (size_t)t * H + v * V, dy);
+        for (int j = 0; j < k; ++j) {
+            Vec<T>::load(Yp + (size_t)rows[j] * H + v * V, yp);
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < V; ++i) { s = fmaf(dy[i], yp[i], s); o[i] = g[j] * dy[i]; }
+            dot[j] += s;
+            Vec<T>::store(dYp + (size_t)rows[j] * H + v * V, o);
+        }
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int j = 0; j < k; ++j) {
+        float s = dot[j];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) red[warp][j] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float dg[kMaxK], gd = 0.f, ssum = 0.f;
+        for (int j = 0; j < k; ++j) {
+            float s = 0.f;
+            for (int w = 0; w < kRowThreads / 32; ++w) s += red[w][j];
+            dg[j] = s;
+            gd += g[j] * s;
+            ssum += selsc[(size_t)t * k + j];
+        }
+        for (int j = 0; j < k; ++j) {
+            float d;
+            if (score == MOE_SCORE_SOFTMAX) {
+                d = g[j] * (dg[j] - gd);
+            } else {
+                float s = selsc[(size_t)t * k + j];
+                d = s * (1.f - s) * (dg[j] - gd) / ssum;
+            }
+            dz[(size_t)t * k + j] = d;
+        }
+    }
+}
+
+// dWr[h][e] = sum over expert e's rows r (token order) of Xp[r][h] dz[slot(r)].
+template <typename T>
+__global__ void __launch_bounds__(256)
+router_wgrad_kernel(const T* __restrict__ Xp, const int* __restrict__ slot_of,
+                    const int* __restrict__ poff, const int* __restrict__ counts,
+                    const float* __restrict__ dz, int H, int E, float* __restrict__ dWr)
+{
+    const int e = blockIdx.y;
+    const int h = blockIdx.x * 256 + threadIdx.x;
+    __shared__ float dzs[256];
+    const int r0 = poff[e], n = counts[e];
+    float acc = 0.f;
+    for (int c0 = 0; c0 < n; c0 += 256) {
+        __syncthreads();
+        if (c0 + threadIdx.x < n) dzs[threadIdx.x] = dz[slot_of[r0 + c0 + threadIdx.x]];
+        __syncthreads();
+        const int m = min(256, n - c0);
+        if (h < H)
+            for (int i = 0; i < m; ++i) {
+                float xv;
+                if constexpr (sizeof(T) == 4) xv = Xp[(size_t)(r0 + c0 + i) * H + h];
+                else xv = __bfloat162float(Xp[(size_t)(r0 + c0 + i) * H + h]);
+                acc = fmaf(xv, dzs[i], acc);
+            }
+    }
+    if (h < H) dWr[(size_t)h * E + e] = acc;
+}
+
+__global__ void transpose_kernel(const float* __restrict__ in, int rows, int cols, float* __restrict__ out)
+{
+    __shared__ float tile[32][33];
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        int r = r0 + i, c = c0 + threadIdx.x;
+        tile[i][threadIdx.x] = (r < rows && c < cols) ? in[(size_t)r * cols + c] : 0.f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        int c = c0 + i, r = r0 + threadIdx.x;
+        if (c < cols && r < rows) out[(size_t)c * rows + r] = tile[threadIdx.x][i];
+    }
+}
+
+// dX[t] = sum_j dXp[row_j] + sum_j dz_j WrT[e_j] (+ dXs[t]), fp32, slot order.
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads)
+unpermute_reduce_kernel(const T* __restrict__ dXp, const T* __restrict__ dXs,
+                        const int* __restrict__ row_of, const int* __restrict__ topk,
+                        const float* __restrict__ dz, const float* __restrict__ WrT, int H, int k,
+                        T* __restrict__ dX)
+{
+    constexpr int V = Vec<T>::N;
+    const int t = blockIdx.x;
+    int rows[kMaxK], ex[kMaxK];
+    float d[kMaxK];
+    for (int j = 0; j < k; ++j) {
+        rows[j] = row_of[(size_t)t * k + j];
+        ex[j] = topk[(size_t)t * k + j];
+        d[j] = dz[(size_t)t * k + j];
+    }
+    for (int v = threadIdx.x; v < H / V; v += kRowThreads) {
+        float acc[V], in[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = 0.f;
+        for (int j = 0; j < k; ++j) {
+            Vec<T>::load(dXp + (size_t)rows[j] * H + v * V, in);
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] += in[i];
+        }
+        for (int j = 0; j < k; ++j) {
+            const float4* w = reinterpret_cast<const float4*>(WrT + (size_t)ex[j] * H + v * V);
+#pragma unroll
+            for (int i = 0; i < V / 4; ++i) {
+                float4 q = w[i];
+                acc[4 * i + 0] = fmaf(d[j], q.x, acc[4 * i + 0]);
+                acc[4 * i + 1] = fmaf(d[j], q.y, acc[4 * i + 1]);
+                acc[4 * i + 2] = fmaf(d[j], q.z, acc[4 * i + 2]);
+                acc[4 * i + 3] = fmaf(d[j], q.w, acc[4 * i + 3]);
+            }
+        }
+        if (dXs) {
+            Vec<T>::load(dXs + (size_t)t * H + v * V, in);
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] += in[i];
+        }
+        Vec<T>::store(dX + (size_t)t * H + v * V, acc);
+    }
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t launch_permute(const T* x, const int* row_of, const int* poff, const int* counts,
+                           int T_, int H, int E, int k, T* Xp, cudaStream_t s)
+{
+    permute_kernel<T><<<T_ + E, kRowThreads, 0, s>>>(x, row_of, poff, counts, T_, H, k, Xp);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_combine(const T* Yp, const T* Ys, const int* row_of, const float* gates,
+                           int T_, int H, int k, T* y, cudaStream_t s)
+{
+    combine_kernel<T><<<T_, kRowThreads, 0, s>>>(Yp, Ys, row_of, gates, H, k, y);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_gate_grad(const T* dY, const T* Yp, const int* row_of, const int* topk,
+                             const float* gates, const float* selsc, const int* poff,
+                             const int* counts, int T_, int H, int E, int k, int score, T* dYp,
+                             float* dz, cudaStream_t s)
+{
+    (void)topk;
+    gate_grad_kernel<T><<<T_ + E, kRowThreads, 0, s>>>(dY, Yp, row_of, gates, selsc, poff, counts,
+                                                       T_, H, k, score, dYp, dz);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_router_wgrad(const T* Xp, const int* slot_of, const int* poff,
+                                const int* counts, const float* dz, int H, int E, int k,
+                                float* dWr, cudaStream_t s)
+{
+    (void)k;
+    dim3 grid((H + 255) / 256, E);
+    router_wgrad_kernel<T><<<grid, 256, 0, s>>>(Xp, slot_of, poff, counts, dz, H, E, dWr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_f32(const float* in, int rows, int cols, float* out, cudaStream_t s)
+{
+    dim3 grid((cols + 31) / 32, (rows + 31) / 32);
+    transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(in, rows, cols, out);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_unpermute_reduce(const T* dXp, const T* dXs, const int* row_of,
+                                    const int* topk, const float* dz, const float* WrT, int T_,
+                                    int H, int k, T* dX, cudaStream_t s)
+{
+    unpermute_reduce_kernel<T><<<T_, kRowThreads, 0, s>>>(dXp, dXs, row_of, topk, dz, WrT, H, k, dX);
+    return cudaGetLastError();
+}
+
+#define MOE_INST(T)                                                                              \
+    template cudaError_t launch_permute<T>(const T*, const int*, const int*, const int*, int, int, \
+                                           int, int, T*, cudaStream_t);                          \
+    template cudaError_t launch_combine<T>(const T*, const T*, const int*, const float*, int, int, \
+                                           int, T*, cudaStream_t);                               \
+    template cudaError_t launch_gate_grad<T>(const T*, const T*, const int*, const int*,         \
+                                             const float*, const float*, const int*, const int*, \
+                                             int, int, int, int, int, T*, float*, cudaStream_t); \
+    template cudaError_t launch_router_wgrad<T>(const T*, const int*, const int*, const int*,    \
+                                                const float*, int, int, int, float*,             \
+                                                cudaStream_t);                                   \
+    template cudaError_t launch_unpermute_reduce<T>(const T*, const T*, const int*, const int*,  \
+                                                    const float*, const float*, int, int, int,   \
+                                                    T*, cudaStream_t);
+MOE_INST(float)
+MOE_INST(__nv_bfloat16)
+#undef MOE_INST
+
+}  // namespace moe

@@ -1,0 +1,112 @@
+// internal.h -- declarations shared by the CUDA translation units of the
+// MoE layer library (not part of the public ABI; see include/moe.h).
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Rows of one grouped-GEMM M tile; every expert segment of the permuted
+// buffers is padded with zero rows to a multiple of this.
+constexpr int kTileM = 128;
+// Tokens per router block (one per-block expert histogram each).
+constexpr int kRouterTokens = 32;
+// Largest number of routed experts / top-k the kernels accept.
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 8;
+// Device-side wait limit of the pipelined kernels, in nanoseconds.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// Status word at the start of the workspace.
+struct DeviceStatus {
+    int code;   // moe_status_t
+    int where;  // kernel-specific location of the first error
+};
+
+// ----------------------------------------------------------- grouped GEMM
+// Scheduling of output tiles.
+enum Sched : int {
+    SCHED_ROWS = 0,   // M = permuted rows (one expert per 128-row tile), fixed K
+    SCHED_WGRAD = 1,  // per expert: M_out x N output, K = the expert's rows
+};
+// What the epilogue does with the fp32 accumulator(s).
+enum Epi : int {
+    EPI_SWIGLU_FWD = 0,  // acc0 = a, acc1 = u -> O0 = a, O1 = u, O2 = silu(a) u
+    EPI_STORE = 1,       // acc0 -> O0
+    EPI_SWIGLU_BWD = 2,  // acc0 = dh; X0 = a, X1 = u -> O0 = dA, O1 = dU
+    EPI_WGRAD = 3,       // acc0 -> O0[e], acc1 -> O1[e] (dual)
+};
+// Two operand sources.
+enum Dual : int {
+    DUAL_NONE = 0,
+    DUAL_N = 1,  // two B operands, two accumulators over the same A
+    DUAL_K = 2,  // A0 B0 + A1 B1 into one accumulator (K = 2 x K0)
+};
+
+struct GemmDesc {
+    int sched, epi, dual;
+    int N;          // columns of each accumulator (whole output width)
+    int K;          // SCHED_ROWS: contraction length of each source
+    int M_out;      // SCHED_WGRAD: output rows per expert
+    int E;          // expert groups (SCHED_WGRAD) -- 1 for a dense group
+    int dense_rows; // > 0: a single dense group of rows [0, dense_rows)
+    // row tables (routed groups)
+    const int* tile_tab;  // expert of each 128-row tile
+    const int* meta;      // meta[0] = number of 128-row tiles, meta[1] = padded rows
+    const int* poff;      // E+1 padded segment offsets
+    const int* counts;    // E token counts
+    // operands (element pointers; the tensor-core path builds TMA maps from them)
+    const void* A0; const void* A1; int lda;      // ROWS: A[row][k]; WGRAD: A[row][m]
+    const void* B0; const void* B1; int ldb;
+    int b_kmajor;              // ROWS: 1 -> B(k,n) = B[e*bstride + n*ldb + k]
+                               //       0 -> B(k,n) = B[e*bstride + k*ldb + n]
+    long long b_estride;       // elements between experts' B blocks
+    int a_rows, b_rows;        // rows of the A / B tensors (TMA bounds)
+    // epilogue
+    void* O0; void* O1; void* O2; int ldo;
+    long long o_estride;       // WGRAD: elements between experts' outputs
+    const void* X0; const void* X1;  // SWIGLU_BWD: saved a, u (ld = ldo)
+    DeviceStatus* status;
+};
+
+// Launchers (return cudaGetLastError()).
+cudaError_t launch_gemm_simt_f32(const GemmDesc& d, int max_m_tiles, cudaStream_t s);
+cudaError_t launch_gemm_tc_bf16(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s);
+cudaError_t gemm_tc_prepare(int device);
+
+// ------------------------------------------------------------- routing etc.
+template <typename T>
+cudaError_t launch_router(const T* x, const float* Wr, const float* b, int T_, int H, int E, int k,
+                          int score, int* topk, float* gates, float* selsc, int* hist,
+                          cudaStream_t s);
+cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff, int* blkbase,
+                        int* tile_tab, int* meta, int* slot_of, cudaStream_t s);
+cudaError_t launch_index(const int* topk, const int* blkbase, int T_, int E, int k, int* row_of,
+                         int* slot_of, cudaStream_t s);
+template <typename T>
+cudaError_t launch_permute(const T* x, const int* row_of, const int* poff, const int* counts,
+                           int T_, int H, int E, int k, T* Xp, cudaStream_t s);
+template <typename T>
+cudaError_t launch_combine(const T* Yp, const T* Ys, const int* row_of, const float* gates,
+                           int T_, int H, int k, T* y, cudaStream_t s);
+template <typename T>
+cudaError_t launch_gate_grad(const T* dY, const T* Yp, const int* row_of, const int* topk,
+                             const float* gates, const float* selsc, const int* poff,
+                             const int* counts, int T_, int H, int E, int k, int score, T* dYp,
+                             float* dz, cudaStream_t s);
+template <typename T>
+cudaError_t launch_router_wgrad(const T* Xp, const int* slot_of, const int* poff,
+                                const int* counts, const float* dz, int H, int E, int k,
+                                float* dWr, cudaStream_t s);
+cudaError_t launch_transpose_f32(const float* in, int rows, int cols, float* out, cudaStream_t s);
+template <typename T>
+cudaError_t launch_unpermute_reduce(const T* dXp, const T* dXs, const int* row_of,
+                                    const int* topk, const float* dz, const float* WrT, int T_,
+                                    int H, int k, T* dX, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,239 @@
+// router.cu -- Route stage and the dispatch tables of the MoE layer.
+//
+// "Scalable Training of Mixture-of-Experts Models with Megatron Core", §2
+// ("Route"): token hidden states -> expert logits -> probabilities -> the
+// top-k experts, producing routing weights and a token-expert assignment.
+// §5 ("Selective precision"): the router runs in FP32.
+//
+// Kernels:
+//   router_kernel  logits z = x Wr + b (fp32 FMA, fixed summation order),
+//                  warp-shuffle top-k on z (score order equals logit order for
+//                  both softmax and sigmoid; equal values go to the lower
+//                  expert index), renormalised gates, and a per-block expert
+//                  histogram counted without atomics.
+//   scan_kernel    per-expert counts, segment sizes padded to 128 rows, their
+//                  exclusive scan, per-block bases, the 128-row tile -> expert
+//                  table and the pad-row markers.
+//   index_kernel   row_of(t, j) = block base + rank of t among the block's
+//                  tokens that chose the same expert (stable, token order),
+//                  and its inverse slot_of.
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// (value, index) ordering: larger value first, then lower index.
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+    return v > bv || (v == bv && i < bi);
+}
+
+template <typename T, int EPL>
+__global__ void __launch_bounds__(256)
+router_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float* __restrict__ b,
+              int T_, int H, int E, int k, int score, int* __restrict__ topk,
+              float* __restrict__ gates, float* __restrict__ selsc, int* __restrict__ hist)
+{
+    constexpr int HC = 32;                 // h chunk
+    constexpr int EW = EPL * 32;           // padded expert width
+    __shared__ float xs[kRouterTokens][HC + 1];
+    __shared__ float ws[HC][EW];
+    __shared__ int sel_s[kRouterTokens][kMaxK];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = blockIdx.x * kRouterTokens;
+    float acc[4][EPL];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) acc[q][i] = 0.f;
+
+    for (int h0 = 0; h0 < H; h0 += HC) {
+        for (int idx = tid; idx < HC * EW; idx += 256) {
+            int hh = idx / EW, e = idx % EW;
+            ws[hh][e] = (e < E) ? Wr[(size_t)(h0 + hh) * E + e] : 0.f;
+        }
+        for (int idx = tid; idx < kRouterTokens * HC; idx += 256) {
+            int tt = idx / HC, hh = idx % HC;
+            int t = t0 + tt;
+            xs[tt][hh] = (t < T_) ? to_f32(x[(size_t)t * H + h0 + hh]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int hh = 0; hh < HC; ++hh) {
+            float wv[EPL];
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) wv[i] = ws[hh][lane + 32 * i];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float xv = xs[warp * 4 + q][hh];
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) acc[q][i] = fmaf(xv, wv[i], acc[q][i]);
+            }
+        }
+        __syncthreads();
+    }
+
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int tt = warp * 4 + q;
+        const int t = t0 + tt;
+        if (t >= T_) continue;                       // warp-uniform
+        float z[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            int e = lane + 32 * i;
+            z[i] = (e < E) ? acc[q][i] + (b ? b[e] : 0.f) : -INFINITY;
+        }
+        unsigned taken = 0;
+        int sel_e[kMaxK];
+        float sel_z[kMaxK];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            if (j >= k) break;
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                int e = lane + 32 * i;
+                if (e < E && !((taken >> i) & 1u) && better(z[i], e, bv, bi)) { bv = z[i]; bi = e; }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+            }
+            sel_e[j] = bi;
+            sel_z[j] = bv;
+            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        }
+        if (lane == 0) {
+            float sc[kMaxK], den = 0.f;
+            for (int j = 0; j < k; ++j) {
+                sc[j] = (score == MOE_SCORE_SOFTMAX) ? expf(sel_z[j] - sel_z[0])
+                                                     : 1.f / (1.f + expf(-sel_z[j]));
+                den += sc[j];
+            }
+            for (int j = 0; j < k; ++j) {
+                topk[(size_t)t * k + j] = sel_e[j];
+                gates[(size_t)t * k + j] = sc[j] / den;
+                selsc[(size_t)t * k + j] = sc[j];
+                sel_s[tt][j] = sel_e[j];
+            }
+        }
+    }
+    __syncthreads();
+    const int ntok = min(kRouterTokens, T_ - t0);
+    for (int e = tid; e < E; e += 256) {
+        int c = 0;
+        for (int tt = 0; tt < ntok; ++tt)
+            for (int j = 0; j < k; ++j) c += (sel_s[tt][j] == e);
+        hist[(size_t)blockIdx.x * E + e] = c;
+    }
+}
+
+__global__ void __launch_bounds__(kMaxE)
+scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ counts,
+            int* __restrict__ poff, int* __restrict__ blkbase, int* __restrict__ tile_tab,
+            int* __restrict__ meta, int* __restrict__ slot_of)
+{
+    __shared__ int sc[kMaxE];
+    const int e = threadIdx.x;
+    int c = 0;
+    if (e < E)
+        for (int blk = 0; blk < nblk; ++blk) c += hist[(size_t)blk * E + e];
+    const int pc = (c + kTileM - 1) / kTileM * kTileM;
+    sc[e] = (e < E) ? pc : 0;
+    __syncthreads();
+    // inclusive Hillis-Steele scan over kMaxE entries
+    for (int off = 1; off < kMaxE; off <<= 1) {
+        int v = (e >= off) ? sc[e - off] : 0;
+        __syncthreads();
+        sc[e] += v;
+        __syncthreads();
+    }
+    const int start = sc[e] - ((e < E) ? pc : 0);
+    if (e < E) {
+        counts[e] = c;
+        poff[e] = start;
+        int run = start;
+        for (int blk = 0; blk < nblk; ++blk) {
+            blkbase[(size_t)blk * E + e] = run;
+            run += hist[(size_t)blk * E + e];
+        }
+        for (int i = 0; i < pc / kTileM; ++i) tile_tab[start / kTileM + i] = e;
+        for (int r = start + c; r < start + pc; ++r) slot_of[r] = -1;
+    }
+    if (e == 0) {
+        const int total = sc[kMaxE - 1];
+        poff[E] = total;
+        meta[0] = total / kTileM;
+        meta[1] = total;
+    }
+}
+
+__global__ void __launch_bounds__(256)
+index_kernel(const int* __restrict__ topk, const int* __restrict__ blkbase, int T_, int E, int k,
+             int* __restrict__ row_of, int* __restrict__ slot_of)
+{
+    __shared__ int sel[kRouterTokens * kMaxK];
+    const int t0 = blockIdx.x * kRouterTokens;
+    const int ntok = min(kRouterTokens, T_ - t0);
+    for (int i = threadIdx.x; i < ntok * k; i += blockDim.x) sel[i] = topk[(size_t)t0 * k + i];
+    __syncthreads();
+    for (int p = threadIdx.x; p < ntok * k; p += blockDim.x) {
+        const int tt = p / k;
+        const int e = sel[p];
+        int rank = 0;
+        for (int u = 0; u < tt; ++u)
+            for (int j = 0; j < k; ++j) rank += (sel[u * k + j] == e);
+        const int row = blkbase[(size_t)blockIdx.x * E + e] + rank;
+        const int slot = (t0 + tt) * k + (p % k);
+        row_of[slot] = row;
+        slot_of[row] = slot;
+    }
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t launch_router(const T* x, const float* Wr, const float* b, int T_, int H, int E, int k,
+                          int score, int* topk, float* gates, float* selsc, int* hist,
+                          cudaStream_t s)
+{
+    const int nblk = (T_ + kRouterTokens - 1) / kRouterTokens;
+    if (E <= 32)
+        router_kernel<T, 1><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+    else if (E <= 64)
+        router_kernel<T, 2><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+    else if (E <= 128)
+        router_kernel<T, 4><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+    else
+        router_kernel<T, 8><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+    return cudaGetLastError();
+}
+template cudaError_t launch_router<float>(const float*, const float*, const float*, int, int, int,
+                                          int, int, int*, float*, float*, int*, cudaStream_t);
+template cudaError_t launch_router<__nv_bfloat16>(const __nv_bfloat16*, const float*, const float*,
+                                                  int, int, int, int, int, int*, float*, float*,
+                                                  int*, cudaStream_t);
+
+cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff, int* blkbase,
+                        int* tile_tab, int* meta, int* slot_of, cudaStream_t s)
+{
+    scan_kernel<<<1, kMaxE, 0, s>>>(hist, nblk, E, counts, poff, blkbase, tile_tab, meta, slot_of);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_index(const int* topk, const int* blkbase, int T_, int E, int k, int* row_of,
+                         int* slot_of, cudaStream_t s)
+{
+    const int nblk = (T_ + kRouterTokens - 1) / kRouterTokens;
+    index_kernel<<<nblk, 256, 0, s>>>(topk, blkbase, T_, E, k, row_of, slot_of);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

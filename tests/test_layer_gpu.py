@@ -1,0 +1,87 @@
+"""Parity of the CUDA layer (through its C ABI) with the fp64 oracle, on
+seeded inputs small enough for the oracle to finish in seconds but spanning
+several 128-row tiles, ragged expert segments, both score functions, the
+shared expert, skewed routing, empty experts and the degenerate cases
+(one expert; k = E)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from harness import full_parity, run_gpu, check_routing, oracle_layer, assert_close, to_np, GRAD_NAMES
+
+pytestmark = pytest.mark.gpu
+
+W = mi.WORKLOADS
+CASES = {
+    "tiny_fp32": W["tiny_fp32"],
+    "mixtral_small": mi.scaled(W["mixtral_8x7b"], T=333, H=256, F=512),
+    "deepseek_small": mi.scaled(W["deepseek_v3"], T=260, H=256, E=16, F=256, Fs=256),
+    "qwen_small_ragged_n": mi.scaled(W["qwen3_235b"], T=520, H=384, E=32, F=384),
+    "fp32_sigmoid_shared": mi.scaled(W["deepseek_v3"], T=100, H=128, E=4, k=2, F=128, Fs=128,
+                                     dtype=mi.FP32),
+    "single_expert_top1": mi.scaled(W["mixtral_8x7b"], T=150, H=128, E=1, k=1, F=256),
+    "k_equals_E": mi.scaled(W["mixtral_8x7b"], T=100, H=128, E=4, k=4, F=128),
+    "softmax_bias_k3": mi.scaled(W["qwen3_235b"], T=400, H=256, E=12, k=3, F=256),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_layer_matches_oracle(name):
+    rep, _ = full_parity(CASES[name])
+    print(name, rep)
+
+
+def test_empty_experts_get_zero_gradients():
+    w = mi.scaled(W["mixtral_8x7b"], T=200, H=256, E=8, k=2, F=256)
+    inp = mi.make_inputs(w)
+    b = torch.zeros(8)
+    b[[1, 4]] = -30.0                       # experts 1 and 4 receive no token
+    inp["b"] = b
+    gpu, _ = run_gpu(w, inp)
+    assert gpu["counts"][1] == 0 and gpu["counts"][4] == 0
+    r, _ = check_routing(w, inp, gpu)
+    ref = oracle_layer(w, inp, r)
+    for e in (1, 4):
+        for n in ("dW_gate", "dW_up", "dW_down"):
+            assert torch.count_nonzero(gpu[n][e]) == 0
+    assert_close("y", to_np(gpu["y"]), ref["y"], w.dtype)
+    for gname, oname in GRAD_NAMES:
+        if oname in ref:
+            assert_close(gname, to_np(gpu[gname]), ref[oname], w.dtype)
+
+
+def test_deterministic_bitwise():
+    w = CASES["deepseek_small"]
+    inp = mi.make_inputs(w)
+    a, layer = run_gpu(w, inp)
+    b, _ = run_gpu(w, inp, layer=layer)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_bad_call_arguments_are_rejected_before_launch():
+    import ctypes
+    import mixture_experts_layer_sigmoid_gb300 as moe
+    w = CASES["mixtral_small"]
+    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T)
+    lib = moe.load_library()
+    saved, ws = layer.buffers(w.T)
+    x = torch.zeros(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+    args = moe.moe_fwd_args_t(x=x.data_ptr(), Wr=x.data_ptr(), W_gate=x.data_ptr(), W_up=x.data_ptr(),
+                              W_down=x.data_ptr(), y=x.data_ptr())
+    st = lib.moe_forward(layer.plan, w.T, ctypes.byref(args), saved.data_ptr(), 16, ws.data_ptr(),
+                         ws.numel(), None)
+    assert st == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    st = lib.moe_forward(layer.plan, w.T + 1, ctypes.byref(args), saved.data_ptr(), saved.numel(),
+                         ws.data_ptr(), ws.numel(), None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    args.x = x.data_ptr() + 2
+    st = lib.moe_forward(layer.plan, w.T, ctypes.byref(args), saved.data_ptr(), saved.numel(),
+                         ws.data_ptr(), ws.numel(), None)
+    assert st == moe.MOE_ERR_MISALIGNED
+    args.x = x.data_ptr()
+    args.Ws_gate = x.data_ptr()            # shared weights on a layer without a shared expert
+    st = lib.moe_forward(layer.plan, w.T, ctypes.byref(args), saved.data_ptr(), saved.numel(),
+                         ws.data_ptr(), ws.numel(), None)
+    assert st == moe.MOE_ERR_INVALID_ARG
