@@ -1,0 +1,353 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE layer forward + backward on GB300.
+
+One step = one forward and one backward pass of the whole layer (router,
+top-k, dispatch tables, permute, fc1 + SwiGLU, fc2, combine; gate gradient,
+fc2 dgrad + SwiGLU backward, fc2 wgrad, fc1 dgrad, fc1 wgrad, router
+backward, unpermute-reduce) through the C ABI, on seeded synthetic inputs of
+the Mixtral-8x7B-shaped expert layer (T=4096, H=4096, E=8, top-2 softmax,
+SwiGLU F=14336, bf16). Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+token sample of the same workload (the layer has no runnable reference
+implementation). Multi-GPU runs are independent replicas (weak scaling):
+every rank runs its own layer and the time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "MoE layer fwd+bwd TFLOPS and % of GB300 tensor peak; tokens/s per layer"
+GEMM_STAGES = ("fc1_swiglu", "fc2", "fc2_dgrad_swiglu", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad",
+               "shared_fc1_swiglu", "shared_fc2", "shared_fc2_dgrad", "shared_fc2_wgrad",
+               "shared_fc1_dgrad", "shared_fc1_wgrad")
+
+
+def stage_flops(name: str, w: mi.Workload) -> float:
+    """Algorithmic FLOPs of one launch of a grouped-GEMM stage (2 per MAC,
+    routed rows R = T k; zero padding rows not counted)."""
+    rows, F = (w.T, w.Fs) if name.startswith("shared_") else (w.R, w.F)
+    base = name[len("shared_"):] if name.startswith("shared_") else name
+    per = 2.0 * rows * w.H * F
+    return {"fc1_swiglu": 2 * per, "fc2": per, "fc2_dgrad_swiglu": per, "fc2_wgrad": per,
+            "fc1_dgrad": 2 * per, "fc1_wgrad": 2 * per}[base]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    for line in open(p):
+        if line.startswith("traffic_bytes_per_launch:"):
+            v = line.split(":", 1)[1].strip()
+            return None if v in ("", "null") else float(v)
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons every 200 ms."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows = []
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                       "-lms", "200", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                                      stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.p = None
+
+    def _read(self):
+        for line in self.p.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self, t0, t1):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        rows = [r for t, r in self.rows if t0 <= t <= t1 and len(r) >= 10]
+        window = "timed region"
+        if len(rows) < 3:
+            rows = [r for _, r in self.rows if len(r) >= 10]
+            window = "warm-up and timed region (timed region shorter than 3 samples)"
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "window": window}
+
+
+# ---------------------------------------------------------------- oracle leg
+def oracle_inputs(inp_host):
+    """fp64 host arrays of the inputs (exact widening of the stored values)."""
+    return {k: (None if v is None else v.double().numpy()) for k, v in inp_host.items()}
+
+
+def oracle_sample(w: mi.Workload, d, n_tok: int):
+    """Time the fp64 oracle (route + forward + backward) on the first n_tok
+    tokens of the workload with all of its expert weights. Returns
+    (seconds, flops of that sample, threads)."""
+    import oracle
+    oracle.build()
+    x, dY = d["x"][:n_tok], d["dY"][:n_tok]
+    t0 = time.perf_counter()
+    r = oracle.route(x, d["Wr"], d["b"], w.k, w.score)
+    oracle.forward(x, d["Wg"], d["Wu"], d["Wd"], r["topk"], r["gates"], d["Wsg"], d["Wsu"], d["Wsd"])
+    oracle.backward(x, d["Wr"], d["Wg"], d["Wu"], d["Wd"], r["topk"], r["gates"], r["scores"], dY,
+                    w.score, d["Wsg"], d["Wsu"], d["Wsd"])
+    dt = time.perf_counter() - t0
+    ws = mi.scaled(w, T=n_tok)
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return dt, ws.flops_fwd_bwd(), threads
+
+
+def host_inputs(w: mi.Workload, device):
+    """Seeded inputs generated on `device`, returned on the host."""
+    g = mi.make_inputs(w, device)
+    return {k: (None if v is None else v.cpu()) for k, v in g.items()}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = oracle_inputs(host_inputs(w, dev))
+    n_tok = args.ref_tokens
+    for _ in range(args.warmup):
+        oracle_sample(w, inp, n_tok)
+    total_s, total_f, threads = 0.0, 0.0, 1
+    for _ in range(args.steps):
+        dt, fl, threads = oracle_sample(w, inp, n_tok)
+        total_s += dt
+        total_f += fl
+    value = total_f / total_s / 1e12
+    sample = f"first {n_tok} tokens of {w.name} with all expert weights; fp64 oracle route+forward+backward per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "tokens_per_s": n_tok * args.steps / total_s,
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "top_k": w.k, "F": w.F,
+                       "Fs": w.Fs, "score": "sigmoid" if w.score else "softmax", "sample_tokens": n_tok},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU leg
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+    from mixture_experts_layer_sigmoid_gb300 import MoELayer, MOE_BF16, MOE_FP32
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    inp = mi.make_inputs(w, dev)
+    layer = MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score,
+                     dtype=MOE_FP32 if w.dtype == mi.FP32 else MOE_BF16, Fs=w.Fs, device=local,
+                     stage_timing=True)
+    x, dY = inp["x"], inp["dY"]
+    W = (inp["Wr"], inp["Wg"], inp["Wu"], inp["Wd"], inp["Wsg"], inp["Wsu"], inp["Wsd"])
+    y = torch.empty_like(x)
+    grads = dict(dX=torch.empty_like(x), dWr=torch.empty_like(inp["Wr"]), dW_gate=torch.empty_like(inp["Wg"]),
+                 dW_up=torch.empty_like(inp["Wu"]), dW_down=torch.empty_like(inp["Wd"]))
+    if w.Fs:
+        grads.update(dWs_gate=torch.empty_like(inp["Wsg"]), dWs_up=torch.empty_like(inp["Wsu"]),
+                     dWs_down=torch.empty_like(inp["Wsd"]))
+
+    def step(xx, dd):
+        layer.forward(xx, W[0], inp["b"], W[1], W[2], W[3], W[4], W[5], W[6], y=y)
+        layer.backward(dd, xx, W[0], W[1], W[2], W[3], W[4], W[5], W[6], grads=grads)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return t.item()
+
+    # ---- device-timed region (inputs resident in HBM)
+    sampler = ClockSampler(local)
+    for _ in range(args.warmup):
+        step(x, dY)
+    torch.cuda.synchronize()
+    if layer.status(w.T) != 0:
+        raise RuntimeError("device status word reports an error after warm-up")
+    layer.stage_times()                      # clear the warm-up record
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(x, dY)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    clocks = sampler.stop(t0, t1)
+    ms = max_over_ranks(e0.elapsed_time(e1)) / args.steps
+    stages = layer.stage_times()
+    if layer.status(w.T) != 0:
+        raise RuntimeError("device status word reports an error in the timed region")
+
+    # ---- end to end through the C ABI with host buffers
+    x_h = x.cpu().pin_memory()
+    dY_h = dY.cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    dX_h = torch.empty_like(x_h).pin_memory()
+    x_d, dY_d = torch.empty_like(x), torch.empty_like(dY)
+    e2e_steps = max(1, args.steps)
+    for _ in range(2):
+        x_d.copy_(x_h, non_blocking=True)
+        dY_d.copy_(dY_h, non_blocking=True)
+        step(x_d, dY_d)
+        y_h.copy_(y, non_blocking=True)
+        dX_h.copy_(grads["dX"], non_blocking=True)
+    torch.cuda.synchronize()
+    layer.stage_times()
+    barrier()
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        x_d.copy_(x_h, non_blocking=True)
+        dY_d.copy_(dY_h, non_blocking=True)
+        step(x_d, dY_d)
+        y_h.copy_(y, non_blocking=True)
+        dX_h.copy_(grads["dX"], non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = max_over_ranks(f0.elapsed_time(f1)) / e2e_steps
+    layer.stage_times()
+
+    flops = w.flops_fwd_bwd()
+    value = world * flops / (ms * 1e-3) / 1e12
+    peaks, peaks_kind = load_peaks()
+    peak_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+
+    # ---- roofline of the dominant kernel (largest device time in the timed region)
+    gemms = {n: v for n, v in stages.items() if n in GEMM_STAGES}
+    dom = max(gemms, key=lambda n: gemms[n][1])
+    launches, tot_ms = gemms[dom]
+    achieved = stage_flops(dom, w) / (tot_ms / launches * 1e-3) / 1e12
+    gemm_ms = sum(v[1] for v in gemms.values()) / args.steps
+    gemm_flops = sum(stage_flops(n, w) * v[0] for n, v in gemms.items()) / args.steps
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_sust,
+                "unit": "TFLOP/s", "frac": achieved / peak_sust,
+                "peak_source": f"bf16_tflops_sustained of {peaks_kind} peaks",
+                "traffic": profiled_traffic(dom, w.name),
+                "all_grouped_gemms": {"achieved": gemm_flops / (gemm_ms * 1e-3) / 1e12,
+                                      "frac": gemm_flops / (gemm_ms * 1e-3) / 1e12 / peak_sust,
+                                      "share_of_step": gemm_ms / ms}}
+    per_stage = {n: {"launches_per_step": v[0] / args.steps, "ms_per_step": v[1] / args.steps}
+                 for n, v in stages.items()}
+    launches_total = sum(v[0] for v in stages.values())
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        inp_h = oracle_inputs({k: (None if v is None else v.cpu()) for k, v in inp.items()})
+        del layer
+        dt, fl, threads = oracle_sample(w, inp_h, args.cpu_tokens)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"first {args.cpu_tokens} tokens of {w.name} with all expert weights; "
+                         f"fp64 oracle route+forward+backward took {dt:.1f} s",
+               "tokens_per_s": args.cpu_tokens / dt}
+
+    if rank == 0:
+        es = 4 if w.dtype == mi.FP32 else 2
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if w.dtype == mi.BF16 else "f32", "data": "synthetic",
+                "tokens_per_s": world * w.T / (ms * 1e-3),
+                "pct_of_bf16_peak": 100.0 * value / world / peak_sust,
+                "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "top_k": w.k, "F": w.F,
+                           "Fs": w.Fs, "score": "sigmoid" if w.score else "softmax",
+                           "routing_bias": w.bias, "seed": w.seed,
+                           "l2": "inputs larger than L2 (expert weights %.2f GB), no flush" %
+                                 ((3 * w.E * w.H * w.F + 3 * w.H * w.Fs) * es / 1e9),
+                           "parallelism": f"replicas x{world}"},
+                "roofline": roofline,
+                "cpu_baseline": cpu,
+                "e2e": {"value": world * flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                        "h2d_bytes_per_step": 2 * x.numel() * x.element_size(),
+                        "d2h_bytes_per_step": 2 * x.numel() * x.element_size()},
+                "gpu_launches": launches_total,
+                "clocks": clocks,
+                "stages": per_stage}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="mixtral_8x7b", choices=sorted(mi.WORKLOADS))
+    ap.add_argument("--cpu-tokens", type=int, default=8, help="oracle sample for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=2, help="oracle sample per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = mi.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -76,8 +76,20 @@ typedef struct {
     int T_max;   /* largest token count a call may pass, >= 1               */
     int score;   /* moe_score_t                                             */
     int dtype;   /* moe_dtype_t                                             */
-    unsigned flags; /* reserved, must be 0                                  */
+    unsigned flags; /* 0 or MOE_FLAG_STAGE_TIMING                          */
 } moe_config_t;
+
+/* Plan flag: bracket every kernel launch of moe_forward / moe_backward with
+ * CUDA events on the call's stream, for moe_stage_times. A plan with this
+ * flag must not be used by two host threads at once. */
+#define MOE_FLAG_STAGE_TIMING 1u
+
+/* Per-stage device time accumulated since the previous moe_stage_times. */
+typedef struct {
+    char  name[24];   /* stage, e.g. "fc1_swiglu", "fc1_wgrad", "combine"  */
+    int   launches;   /* kernel launches of this stage                      */
+    float total_ms;   /* summed event-timed duration of those launches      */
+} moe_stage_time_t;
 
 typedef struct moe_plan_s* moe_plan_t;
 
@@ -162,6 +174,14 @@ moe_status_t moe_read_status(moe_plan_t plan, const void* ws, moe_stream_t strea
 
 /* Static, NUL-terminated description of a status code. */
 const char* moe_status_string(moe_status_t status);
+
+/* Device time per stage of every moe_forward / moe_backward enqueued since
+ * the previous call (plans created with MOE_FLAG_STAGE_TIMING only; the
+ * measurement covers eagerly launched calls, not graph replays). Waits for
+ * the recorded events, writes up to `capacity` entries in first-launch
+ * order, sets *count to the number of stages and clears the record.
+ * Errors: INVALID_ARG (null, or a plan without the flag), CUDA. */
+moe_status_t moe_stage_times(moe_plan_t plan, moe_stage_time_t* out, int capacity, int* count);
 
 /* MOE_ABI_VERSION of the loaded library. */
 int moe_abi_version(void);

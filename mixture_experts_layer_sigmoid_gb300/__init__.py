@@ -28,10 +28,12 @@ MOE_ERR_CUDA = 5
 MOE_ERR_DEVICE_TIMEOUT = 6
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_FP32, MOE_BF16, MOE_FP8_BLOCK = 0, 1, 2
+MOE_FLAG_STAGE_TIMING = 1
 
 # Names the library exports (include/moe.h).
 EXPORTS = ("moe_plan_create", "moe_plan_destroy", "moe_workspace_size", "moe_forward",
-           "moe_backward", "moe_read_status", "moe_status_string", "moe_abi_version")
+           "moe_backward", "moe_read_status", "moe_status_string", "moe_stage_times",
+           "moe_abi_version")
 
 
 class moe_config_t(ctypes.Structure):
@@ -53,6 +55,10 @@ class moe_bwd_args_t(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("dY", "x", "Wr", "W_gate", "W_up", "W_down", "Ws_gate", "Ws_up",
                                    "Ws_down", "dX", "dWr", "dW_gate", "dW_up", "dW_down", "dWs_gate",
                                    "dWs_up", "dWs_down")]
+
+
+class moe_stage_time_t(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 24), ("launches", ctypes.c_int), ("total_ms", ctypes.c_float)]
 
 
 class MoEError(RuntimeError):
@@ -83,6 +89,7 @@ def load_library() -> ctypes.CDLL:
         lib.moe_read_status.argtypes = [_vp, _vp, _vp]
         lib.moe_status_string.argtypes = [ctypes.c_int]
         lib.moe_status_string.restype = ctypes.c_char_p
+        lib.moe_stage_times.argtypes = [_vp, P(moe_stage_time_t), ctypes.c_int, P(ctypes.c_int)]
         lib.moe_abi_version.argtypes = []
         for n in EXPORTS:
             if n not in ("moe_status_string", "moe_abi_version"):
@@ -140,6 +147,17 @@ def moe_read_status(plan: int, ws: int, stream: int) -> int:
     return load_library().moe_read_status(plan, ws, stream)
 
 
+def moe_stage_times(plan: int):
+    """{stage: (launches, total_ms)} since the previous call (timing plans)."""
+    cap = 64
+    buf = (moe_stage_time_t * cap)()
+    n = ctypes.c_int()
+    st = load_library().moe_stage_times(plan, buf, cap, ctypes.byref(n))
+    if st != MOE_OK:
+        raise MoEError(st, "moe_stage_times")
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(min(n.value, cap))}
+
+
 # ------------------------------------------------- torch-allocated wrapper
 def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
@@ -153,11 +171,11 @@ class MoELayer:
     W_down E×F×H, shared expert H×Fs, H×Fs, Fs×H."""
 
     def __init__(self, H, E, F, top_k, T_max, score=MOE_SCORE_SOFTMAX, dtype=MOE_BF16, Fs=0,
-                 device=0):
+                 device=0, stage_timing=False):
         import torch
         self.torch = torch
         self.cfg = moe_config_t(H=H, E=E, F=F, Fs=Fs, top_k=top_k, T_max=T_max, score=score,
-                                dtype=dtype, flags=0)
+                                dtype=dtype, flags=MOE_FLAG_STAGE_TIMING if stage_timing else 0)
         self.device = torch.device("cuda", device)
         self.plan = moe_plan_create(self.cfg, device)
         self._bufs: Dict[int, tuple] = {}
@@ -224,6 +242,9 @@ class MoELayer:
         moe_backward(self.plan, T, a, saved.data_ptr(), saved.numel(), ws.data_ptr(), ws.numel(),
                      self.stream())
         return grads
+
+    def stage_times(self):
+        return moe_stage_times(self.plan)
 
     def status(self, T) -> int:
         _, ws = self.buffers(T)

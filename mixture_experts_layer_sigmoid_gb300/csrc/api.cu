@@ -10,6 +10,7 @@
 #include "internal.h"
 
 #include <new>
+#include <vector>
 #include <string.h>
 
 namespace moe {
@@ -81,7 +82,7 @@ moe_status_t check_config(const moe_config_t* c)
     if (!c) return MOE_ERR_INVALID_ARG;
     if (c->H <= 0 || c->H % 128 || c->E < 1 || c->E > kMaxE || c->F <= 0 || c->F % 128 ||
         c->Fs < 0 || c->Fs % 128 || c->top_k < 1 || c->top_k > kMaxK || c->top_k > c->E ||
-        c->T_max < 1 || c->flags != 0)
+        c->T_max < 1 || (c->flags & ~MOE_FLAG_STAGE_TIMING) != 0)
         return MOE_ERR_INVALID_ARG;
     if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
     if (c->dtype != MOE_FP32 && c->dtype != MOE_BF16 && c->dtype != MOE_FP8_BLOCK)
@@ -111,10 +112,33 @@ struct DeviceGuard {
 }  // namespace
 }  // namespace moe
 
+namespace moe {
+namespace {
+enum Stage : int {
+    ST_ROUTER, ST_SCAN, ST_INDEX, ST_PERMUTE, ST_FC1, ST_FC2, ST_FC1S, ST_FC2S, ST_COMBINE,
+    ST_GATEGRAD, ST_FC2_DGRAD, ST_FC2_WGRAD, ST_FC1_DGRAD, ST_FC1_WGRAD, ST_FC2S_DGRAD,
+    ST_FC2S_WGRAD, ST_FC1S_DGRAD, ST_FC1S_WGRAD, ST_ROUTER_WGRAD, ST_TRANSPOSE, ST_UNPERMUTE,
+    ST_COUNT
+};
+const char* const kStageNames[ST_COUNT] = {
+    "router", "scan", "index", "permute", "fc1_swiglu", "fc2", "shared_fc1_swiglu", "shared_fc2",
+    "combine", "gate_grad", "fc2_dgrad_swiglu", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad",
+    "shared_fc2_dgrad", "shared_fc2_wgrad", "shared_fc1_dgrad", "shared_fc1_wgrad",
+    "router_wgrad", "wr_transpose", "unpermute_reduce"};
+struct StageRec {
+    int stage;
+    cudaEvent_t start, stop;
+};
+}  // namespace
+}  // namespace moe
+
 struct moe_plan_s {
     moe_config_t cfg;
     int device;
     int num_sms;
+    bool timing;
+    std::vector<moe::StageRec> recs;    // recorded since the last moe_stage_times
+    std::vector<cudaEvent_t> spare;     // events free for reuse
 };
 
 using namespace moe;
@@ -159,14 +183,55 @@ moe_status_t moe_plan_create(const moe_config_t* cfg, int device, moe_plan_t* ou
     p->cfg = *cfg;
     p->device = device;
     p->num_sms = prop.multiProcessorCount;
+    p->timing = (cfg->flags & MOE_FLAG_STAGE_TIMING) != 0;
     *out = p;
     return MOE_OK;
 }
 
 moe_status_t moe_plan_destroy(moe_plan_t plan)
 {
+    if (!plan) return MOE_OK;
+    {
+        DeviceGuard g(plan->device);
+        for (auto& r : plan->recs) {
+            cudaEventDestroy(r.start);
+            cudaEventDestroy(r.stop);
+        }
+        for (auto e : plan->spare) cudaEventDestroy(e);
+    }
     delete plan;
     return MOE_OK;
+}
+
+moe_status_t moe_stage_times(moe_plan_t plan, moe_stage_time_t* out, int capacity, int* count)
+{
+    if (!plan || !count || capacity < 0 || (capacity > 0 && !out) || !plan->timing)
+        return MOE_ERR_INVALID_ARG;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return MOE_ERR_CUDA;
+    int order[ST_COUNT], n = 0;
+    int launches[ST_COUNT] = {0};
+    double ms[ST_COUNT] = {0.0};
+    moe_status_t st = MOE_OK;
+    for (auto& r : plan->recs) {
+        float t = 0.f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess ||
+            cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+            st = MOE_ERR_CUDA;
+        if (launches[r.stage]++ == 0) order[n++] = r.stage;
+        ms[r.stage] += t;
+        plan->spare.push_back(r.start);
+        plan->spare.push_back(r.stop);
+    }
+    plan->recs.clear();
+    *count = n;
+    for (int i = 0; i < n && i < capacity; ++i) {
+        memset(out[i].name, 0, sizeof out[i].name);
+        strncpy(out[i].name, kStageNames[order[i]], sizeof out[i].name - 1);
+        out[i].launches = launches[order[i]];
+        out[i].total_ms = (float)ms[order[i]];
+    }
+    return st;
 }
 
 moe_status_t moe_workspace_size(moe_plan_t plan, int T, size_t* saved_bytes, size_t* ws_bytes)
@@ -182,6 +247,29 @@ moe_status_t moe_workspace_size(moe_plan_t plan, int T, size_t* saved_bytes, siz
     do {                                                 \
         if ((call) != cudaSuccess) return MOE_ERR_CUDA;  \
     } while (0)
+
+// Runs one kernel launch; with stage timing on, brackets it with events.
+template <typename Fn>
+static cudaError_t run_stage(moe_plan_t p, int stage, cudaStream_t s, Fn&& launch)
+{
+    if (!p->timing) return launch();
+    cudaEvent_t ev[2];
+    for (int i = 0; i < 2; ++i) {
+        if (!p->spare.empty()) {
+            ev[i] = p->spare.back();
+            p->spare.pop_back();
+        } else if (cudaEventCreate(&ev[i]) != cudaSuccess) {
+            return cudaErrorMemoryAllocation;
+        }
+    }
+    cudaError_t e = cudaEventRecord(ev[0], s);
+    if (e == cudaSuccess) e = launch();
+    if (e == cudaSuccess) e = cudaEventRecord(ev[1], s);
+    p->recs.push_back({stage, ev[0], ev[1]});
+    return e;
+}
+#define MOE_STAGE(stage, call) \
+    MOE_CUDA(run_stage(p, stage, s, [&]() -> cudaError_t { return (call); }))
 
 template <typename T>
 static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, uint8_t* sv,
@@ -209,12 +297,12 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     const T* x = static_cast<const T*>(a->x);
 
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
-    MOE_CUDA(launch_router<T>(x, a->Wr, a->b, T_, H, E, k, c.score, topk, gates, selsc,
+    MOE_STAGE(ST_ROUTER, launch_router<T>(x, a->Wr, a->b, T_, H, E, k, c.score, topk, gates, selsc,
                               reinterpret_cast<int*>(ws + L.hist), s));
-    MOE_CUDA(launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
+    MOE_STAGE(ST_SCAN, launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
                          reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s));
-    MOE_CUDA(launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
-    MOE_CUDA(launch_permute<T>(x, rowof, poff, counts, T_, H, E, k, Xp, s));
+    MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
+    MOE_STAGE(ST_PERMUTE, launch_permute<T>(x, rowof, poff, counts, T_, H, E, k, Xp, s));
 
     auto gemm = [&](const GemmDesc& d) -> cudaError_t {
         if (c.dtype == MOE_FP32) return launch_gemm_simt_f32(d, L.MT_max, s);
@@ -230,7 +318,7 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     d.B0 = a->W_gate; d.B1 = a->W_up; d.ldb = F; d.b_kmajor = 0; d.b_estride = (long long)H * F;
     d.b_rows = E * H;
     d.O0 = A; d.O1 = U; d.O2 = Hh; d.ldo = F; d.status = status;
-    MOE_CUDA(gemm(d));
+    MOE_STAGE(ST_FC1, gemm(d));
     // fc2: Yp = Hh Wd
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
@@ -239,7 +327,7 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     d.A0 = Hh; d.lda = F; d.a_rows = L.Rp_max;
     d.B0 = a->W_down; d.ldb = H; d.b_kmajor = 0; d.b_estride = (long long)F * H; d.b_rows = E * F;
     d.O0 = Yp; d.ldo = H; d.status = status;
-    MOE_CUDA(gemm(d));
+    MOE_STAGE(ST_FC2, gemm(d));
     if (Fs) {
         T* As = reinterpret_cast<T*>(sv + L.As);
         T* Us = reinterpret_cast<T*>(sv + L.Us);
@@ -250,16 +338,16 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
         d.A0 = x; d.lda = H; d.a_rows = T_;
         d.B0 = a->Ws_gate; d.B1 = a->Ws_up; d.ldb = Fs; d.b_kmajor = 0; d.b_rows = H;
         d.O0 = As; d.O1 = Us; d.O2 = Hs; d.ldo = Fs; d.status = status;
-        MOE_CUDA(gemm(d));
+        MOE_STAGE(ST_FC1S, gemm(d));
         memset(&d, 0, sizeof d);
         d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
         d.N = H; d.K = Fs; d.E = 1; d.dense_rows = T_;
         d.A0 = Hs; d.lda = Fs; d.a_rows = T_;
         d.B0 = a->Ws_down; d.ldb = H; d.b_kmajor = 0; d.b_rows = Fs;
         d.O0 = Ys; d.ldo = H; d.status = status;
-        MOE_CUDA(gemm(d));
+        MOE_STAGE(ST_FC2S, gemm(d));
     }
-    MOE_CUDA(launch_combine<T>(Yp, Ys, rowof, gates, T_, H, k, static_cast<T*>(a->y), s));
+    MOE_STAGE(ST_COMBINE, launch_combine<T>(Yp, Ys, rowof, gates, T_, H, k, static_cast<T*>(a->y), s));
 
     if (a->topk_idx) MOE_CUDA(cudaMemcpyAsync(a->topk_idx, topk, sizeof(int) * L.R, cudaMemcpyDeviceToDevice, s));
     if (a->gates) MOE_CUDA(cudaMemcpyAsync(a->gates, gates, sizeof(float) * L.R, cudaMemcpyDeviceToDevice, s));
@@ -307,7 +395,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
 
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
     // Combine backward: gate gradients, gate-scaled output gradients, router dz
-    MOE_CUDA(launch_gate_grad<T>(dY, Yp, rowof, topk, gates, selsc, poff, counts, T_, H, E, k,
+    MOE_STAGE(ST_GATEGRAD, launch_gate_grad<T>(dY, Yp, rowof, topk, gates, selsc, poff, counts, T_, H, E, k,
                                  c.score, dYp, dz, s));
     GemmDesc d;
     // fc2 dgrad + SwiGLU backward: dh = dYp Wd^T -> dA, dU
@@ -318,7 +406,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     d.A0 = dYp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = a->W_down; d.ldb = H; d.b_kmajor = 1; d.b_estride = (long long)F * H; d.b_rows = E * F;
     d.X0 = A; d.X1 = U; d.O0 = dA; d.O1 = dU; d.ldo = F; d.status = status;
-    MOE_CUDA(gemm(d));
+    MOE_STAGE(ST_FC2_DGRAD, gemm(d));
     // fc2 wgrad: dWd[e] = Hh_e^T dYp_e
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
@@ -327,7 +415,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     d.A0 = Hh; d.lda = F; d.a_rows = L.Rp_max;
     d.B0 = dYp; d.ldb = H; d.b_rows = L.Rp_max;
     d.O0 = a->dW_down; d.ldo = H; d.o_estride = (long long)F * H; d.status = status;
-    MOE_CUDA(gemm(d));
+    MOE_STAGE(ST_FC2_WGRAD, gemm(d));
     // fc1 dgrad: dXp = dA Wg^T + dU Wu^T
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
@@ -337,7 +425,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     d.B0 = a->W_gate; d.B1 = a->W_up; d.ldb = F; d.b_kmajor = 1; d.b_estride = (long long)H * F;
     d.b_rows = E * H;
     d.O0 = dXp; d.ldo = H; d.status = status;
-    MOE_CUDA(gemm(d));
+    MOE_STAGE(ST_FC1_DGRAD, gemm(d));
     // fc1 wgrad: dWg[e] = Xp_e^T dA_e, dWu[e] = Xp_e^T dU_e
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
@@ -346,7 +434,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     d.A0 = Xp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = dA; d.B1 = dU; d.ldb = F; d.b_rows = L.Rp_max;
     d.O0 = a->dW_gate; d.O1 = a->dW_up; d.ldo = F; d.o_estride = (long long)H * F; d.status = status;
-    MOE_CUDA(gemm(d));
+    MOE_STAGE(ST_FC1_WGRAD, gemm(d));
 
     T* dXs = nullptr;
     if (Fs) {
@@ -363,33 +451,33 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
         d.A0 = dY; d.lda = H; d.a_rows = T_;
         d.B0 = a->Ws_down; d.ldb = H; d.b_kmajor = 1; d.b_rows = Fs;
         d.X0 = As; d.X1 = Us; d.O0 = dAs; d.O1 = dUs; d.ldo = Fs; d.status = status;
-        MOE_CUDA(gemm(d));
+        MOE_STAGE(ST_FC2S_DGRAD, gemm(d));
         memset(&d, 0, sizeof d);
         d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
         d.N = H; d.M_out = Fs; d.E = 1; d.dense_rows = T_;
         d.A0 = Hs; d.lda = Fs; d.a_rows = T_;
         d.B0 = dY; d.ldb = H; d.b_rows = T_;
         d.O0 = a->dWs_down; d.ldo = H; d.status = status;
-        MOE_CUDA(gemm(d));
+        MOE_STAGE(ST_FC2S_WGRAD, gemm(d));
         memset(&d, 0, sizeof d);
         d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
         d.N = H; d.K = Fs; d.E = 1; d.dense_rows = T_;
         d.A0 = dAs; d.A1 = dUs; d.lda = Fs; d.a_rows = T_;
         d.B0 = a->Ws_gate; d.B1 = a->Ws_up; d.ldb = Fs; d.b_kmajor = 1; d.b_rows = H;
         d.O0 = dXs; d.ldo = H; d.status = status;
-        MOE_CUDA(gemm(d));
+        MOE_STAGE(ST_FC1S_DGRAD, gemm(d));
         memset(&d, 0, sizeof d);
         d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
         d.N = Fs; d.M_out = H; d.E = 1; d.dense_rows = T_;
         d.A0 = a->x; d.lda = H; d.a_rows = T_;
         d.B0 = dAs; d.B1 = dUs; d.ldb = Fs; d.b_rows = T_;
         d.O0 = a->dWs_gate; d.O1 = a->dWs_up; d.ldo = Fs; d.status = status;
-        MOE_CUDA(gemm(d));
+        MOE_STAGE(ST_FC1S_WGRAD, gemm(d));
     }
     // router backward and the unpermute-reduce of dX
-    MOE_CUDA(launch_router_wgrad<T>(Xp, slotof, poff, counts, dz, H, E, k, a->dWr, s));
-    MOE_CUDA(launch_transpose_f32(a->Wr, H, E, WrT, s));
-    MOE_CUDA(launch_unpermute_reduce<T>(dXp, dXs, rowof, topk, dz, WrT, T_, H, k,
+    MOE_STAGE(ST_ROUTER_WGRAD, launch_router_wgrad<T>(Xp, slotof, poff, counts, dz, H, E, k, a->dWr, s));
+    MOE_STAGE(ST_TRANSPOSE, launch_transpose_f32(a->Wr, H, E, WrT, s));
+    MOE_STAGE(ST_UNPERMUTE, launch_unpermute_reduce<T>(dXp, dXs, rowof, topk, dz, WrT, T_, H, k,
                                         static_cast<T*>(a->dX), s));
     return MOE_OK;
 }

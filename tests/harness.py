@@ -10,7 +10,16 @@ Training of Mixture-of-Experts Models with Megatron Core", §2):
     the GPU's choice is checked to be one of them and the oracle then uses
     that choice (router replay) so downstream tensors compare like with like;
   - floating-point tensors: relative L2 error and max |error| / rms(reference)
-    within the bounds of the dtype (bf16: 1e-2 and 4e-2; fp32: 1e-4 and 1e-3).
+    within the bounds of the dtype (bf16: 1e-2 and 4e-2; fp32: 1e-4 and 1e-3);
+  - bf16 expert weight gradients (dW_gate, dW_up, dW_down and the shared
+    expert's): relative L2 <= 1e-2 over the whole tensor AND over each
+    expert's block, and every element within the first-order forward-error
+    bound of the bf16/fp32 arithmetic that produces it (wgrad_bounds). The
+    max |error| / rms criterion is not used for them: each entry is a sum over
+    the expert's rows of products of bf16-rounded MMA operands, the entries
+    are heavy-tailed (max/rms up to ~15 with skewed routing), and rounding
+    alone then exceeds 4e-2 * rms at the largest entries for any bf16-operand
+    implementation.
 """
 from __future__ import annotations
 
@@ -22,6 +31,9 @@ import oracle
 
 TIE_REL = 1e-5
 BOUNDS = {mi.BF16: (1e-2, 4e-2), mi.FP32: (1e-4, 1e-3)}
+WGRAD_BOUND_SLACK = 1.5      # headroom over the first-order bound (second-order terms)
+BF16_U = 2.0 ** -8           # bf16 unit roundoff
+FP32_U = 2.0 ** -24          # fp32 unit roundoff, per accumulated term (worst case)
 
 
 def to_np(t):
@@ -45,6 +57,85 @@ def assert_close(name, got, ref, dtype):
     rl2, mr = rel_errors(got, ref)
     assert rl2 <= l2b and mr <= mab, f"{name}: rel L2 {rl2:.3e} (<= {l2b}), max/rms {mr:.3e} (<= {mab})"
     return rl2, mr
+
+
+def _sig(a):
+    return 1.0 / (1.0 + np.exp(-a))
+
+
+def _expert_wgrad_bounds(X, Wg, Wu, Wd, g, dY, dYp_rounded=True):
+    """First-order worst-case |error| bounds of the bf16 path's weight
+    gradients of one expert (rows X with gates g and output gradients dY).
+
+    Each stage's error bound is carried forward: a, u (fp32 sums over H,
+    rounded to bf16), h = silu(a) u (bf16), dYp = g dY (bf16), dh = dYp Wd^T
+    (fp32 sum over H), dA = dh u silu'(a) and dU = dh silu(a) (bf16); then
+    the wgrad sums over the M rows (fp32) and the bf16 output rounding."""
+    U, V = BF16_U, FP32_U
+    M, H = X.shape
+    a = X @ Wg
+    uu = X @ Wu
+    s = _sig(a)
+    silu = a * s
+    d1 = s * (1 + a * (1 - s))
+    d2 = s * (1 - s) * (2 + a * (1 - 2 * s))
+    aX = np.abs(X)
+    a_err = U * np.abs(a) + H * V * (aX @ np.abs(Wg))
+    u_err = U * np.abs(uu) + H * V * (aX @ np.abs(Wu))
+    h = silu * uu
+    h_err = U * np.abs(h) + np.abs(d1 * uu) * a_err + np.abs(silu) * u_err
+    dYp = g * dY
+    dYp_err = U * np.abs(dYp) if dYp_rounded else np.zeros_like(dYp)
+    dh = dYp @ Wd.T
+    dh_err = (U + H * V) * (np.abs(dYp) @ np.abs(Wd).T)
+    dU = dh * silu
+    dU_err = U * np.abs(dU) + np.abs(silu) * dh_err + np.abs(dh * d1) * a_err
+    dA = dh * uu * d1
+    dA_err = (U * np.abs(dA) + np.abs(uu * d1) * dh_err + np.abs(dh * d1) * u_err
+              + np.abs(dh * uu * d2) * a_err)
+    mv = M * V
+    bd = (h_err.T @ np.abs(dYp) + np.abs(h).T @ dYp_err + mv * (np.abs(h).T @ np.abs(dYp))
+          + U * np.abs(h.T @ dYp))
+    bg = aX.T @ dA_err + mv * (aX.T @ np.abs(dA)) + U * np.abs(X.T @ dA)
+    bu = aX.T @ dU_err + mv * (aX.T @ np.abs(dU)) + U * np.abs(X.T @ dU)
+    return bg, bu, bd
+
+
+def wgrad_bounds(w, inp, r):
+    """Elementwise error bounds for every expert weight gradient (bf16)."""
+    x, dY = to_np(inp["x"]), to_np(inp["dY"])
+    Wg, Wu, Wd = to_np(inp["Wg"]), to_np(inp["Wu"]), to_np(inp["Wd"])
+    out = {n: np.zeros_like(v) for n, v in (("dWg", Wg), ("dWu", Wu), ("dWd", Wd))}
+    for e in range(w.E):
+        toks, slots = np.nonzero(r["topk"] == e)
+        if len(toks) == 0:
+            continue
+        out["dWg"][e], out["dWu"][e], out["dWd"][e] = _expert_wgrad_bounds(
+            x[toks], Wg[e], Wu[e], Wd[e], r["gates"][toks, slots][:, None], dY[toks])
+    if w.Fs:
+        out["dWsg"], out["dWsu"], out["dWsd"] = _expert_wgrad_bounds(
+            x, to_np(inp["Wsg"]), to_np(inp["Wsu"]), to_np(inp["Wsd"]), np.ones((w.T, 1)), dY,
+            dYp_rounded=False)
+    return out
+
+
+def assert_wgrad(name, got, ref, bound):
+    """bf16 weight gradient: rel L2 (whole and per expert block) + elementwise bound."""
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    rl2, mr = rel_errors(got, ref)
+    assert rl2 <= 1e-2, f"{name}: rel L2 {rl2:.3e} > 1e-2"
+    blocks = [(got, ref)] if ref.ndim == 2 else list(zip(got, ref))
+    for e, (g_, r_) in enumerate(blocks):
+        nr = np.linalg.norm(r_)
+        if nr == 0:
+            assert np.all(g_ == 0), f"{name}[{e}]: expert without tokens has a nonzero gradient"
+            continue
+        assert np.linalg.norm(g_ - r_) / nr <= 1e-2, f"{name}[{e}]: block rel L2 > 1e-2"
+    ratio = np.abs(got - ref) / (WGRAD_BOUND_SLACK * bound + 1e-30)
+    worst = float(ratio.max())
+    assert worst <= 1.0, (f"{name}: |error| above the bf16 forward-error bound "
+                          f"(worst ratio {worst:.3f} at {np.unravel_index(ratio.argmax(), ratio.shape)})")
+    return rl2, mr, worst
 
 
 def upload(inp, device="cuda"):
@@ -118,6 +209,24 @@ def oracle_layer(w, inp, r, backward=True):
 
 GRAD_NAMES = [("dX", "dX"), ("dWr", "dWr"), ("dW_gate", "dWg"), ("dW_up", "dWu"),
               ("dW_down", "dWd"), ("dWs_gate", "dWsg"), ("dWs_up", "dWsu"), ("dWs_down", "dWsd")]
+EXPERT_WGRADS = {"dWg", "dWu", "dWd", "dWsg", "dWsu", "dWsd"}
+
+
+def compare_all(w, inp, r, gpu, ref, backward=True):
+    """Compare every output and gradient with the rules of this module."""
+    report = {"y": assert_close("y", to_np(gpu["y"]), ref["y"], w.dtype)}
+    if not backward:
+        return report
+    bounds = wgrad_bounds(w, inp, r) if w.dtype == mi.BF16 else None
+    for gname, oname in GRAD_NAMES:
+        if oname not in ref:
+            continue
+        got = to_np(gpu[gname])
+        if bounds is not None and oname in EXPERT_WGRADS:
+            report[gname] = assert_wgrad(gname, got, ref[oname], bounds[oname])
+        else:
+            report[gname] = assert_close(gname, got, ref[oname], w.dtype)
+    return report
 
 
 def full_parity(w: mi.Workload, backward=True):
@@ -126,10 +235,6 @@ def full_parity(w: mi.Workload, backward=True):
     r, nties = check_routing(w, inp, gpu)
     np.testing.assert_allclose(gpu["gates"].numpy(), r["gates"], rtol=1e-4, atol=1e-6)
     ref = oracle_layer(w, inp, r, backward)
-    report = {"near_ties": nties}
-    report["y"] = assert_close("y", to_np(gpu["y"]), ref["y"], w.dtype)
-    if backward:
-        for gname, oname in GRAD_NAMES:
-            if oname in ref:
-                report[gname] = assert_close(gname, to_np(gpu[gname]), ref[oname], w.dtype)
+    report = compare_all(w, inp, r, gpu, ref, backward)
+    report["near_ties"] = nties
     return report, gpu

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import moe_inputs as mi
-from harness import full_parity, run_gpu, check_routing, oracle_layer, assert_close, to_np, GRAD_NAMES
+from harness import full_parity, run_gpu, check_routing, oracle_layer, compare_all
 
 pytestmark = pytest.mark.gpu
 
@@ -45,10 +45,7 @@ def test_empty_experts_get_zero_gradients():
     for e in (1, 4):
         for n in ("dW_gate", "dW_up", "dW_down"):
             assert torch.count_nonzero(gpu[n][e]) == 0
-    assert_close("y", to_np(gpu["y"]), ref["y"], w.dtype)
-    for gname, oname in GRAD_NAMES:
-        if oname in ref:
-            assert_close(gname, to_np(gpu[gname]), ref[oname], w.dtype)
+    compare_all(w, inp, r, gpu, ref)
 
 
 def test_deterministic_bitwise():
