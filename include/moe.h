@@ -183,6 +183,32 @@ const char* moe_status_string(moe_status_t status);
  * Errors: INVALID_ARG (null, or a plan without the flag), CUDA. */
 moe_status_t moe_stage_times(moe_plan_t plan, moe_stage_time_t* out, int capacity, int* count);
 
+/* Routing without a caller-provided workspace. The paper has no
+ * counterpart: this entry exists for callers that cannot allocate device
+ * memory -- their memory is owned by a framework pool or a budget fixed at
+ * start-up, or they run in loops that must not call cudaMalloc (it can
+ * synchronise the device) -- and so cannot pass the `ws` buffer that
+ * moe_forward needs.
+ * Computes, for T tokens, the same routing outputs as moe_forward's optional
+ * outputs: topk_idx (T×k), gates (T×k), counts (E), offsets (E+1, padded
+ * segment starts) and row_of (T×k), from x (T×H act), Wr (H×E fp32) and the
+ * optional bias b (E fp32). All pointers are caller-owned device pointers,
+ * 16-byte aligned; nothing is allocated or freed.
+ * Scratch: a 4 MiB array inside the library's device image, held on every GPU
+ * that loads the library until the process exits. A call needs about
+ * 8·T·k + 8·ceil(T/32)·E + 508·min(E, T·k) bytes of it; larger T returns
+ * MOE_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any
+ * stream capture. All calls share the array and it keeps the last call's
+ * contents (every entry a call reads is written earlier in the same call);
+ * calls whose work overlaps on the GPU -- from different streams or host
+ * threads -- race on it and must be serialised by the caller.
+ * Errors: INVALID_ARG, MISALIGNED, WORKSPACE_TOO_SMALL, CUDA. */
+moe_status_t moe_route_static(moe_plan_t plan, int T, const void* x, const float* Wr,
+                              const float* b, int32_t* topk_idx, float* gates, int32_t* counts,
+                              int32_t* offsets, int32_t* row_of, moe_stream_t stream);
+
 /* MOE_ABI_VERSION of the loaded library. */
 int moe_abi_version(void);
 

@@ -33,7 +33,7 @@ MOE_FLAG_STAGE_TIMING = 1
 # Names the library exports (include/moe.h).
 EXPORTS = ("moe_plan_create", "moe_plan_destroy", "moe_workspace_size", "moe_forward",
            "moe_backward", "moe_read_status", "moe_status_string", "moe_stage_times",
-           "moe_abi_version")
+           "moe_route_static", "moe_abi_version")
 
 
 class moe_config_t(ctypes.Structure):
@@ -90,6 +90,7 @@ def load_library() -> ctypes.CDLL:
         lib.moe_status_string.argtypes = [ctypes.c_int]
         lib.moe_status_string.restype = ctypes.c_char_p
         lib.moe_stage_times.argtypes = [_vp, P(moe_stage_time_t), ctypes.c_int, P(ctypes.c_int)]
+        lib.moe_route_static.argtypes = [_vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
         lib.moe_abi_version.argtypes = []
         for n in EXPORTS:
             if n not in ("moe_status_string", "moe_abi_version"):

@@ -552,3 +552,11 @@ moe_status_t moe_read_status(moe_plan_t plan, const void* ws, moe_stream_t strea
     if (cudaMemcpy(&h, ws, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
     return h.code == 0 ? MOE_OK : static_cast<moe_status_t>(h.code);
 }
+
+bool moe::plan_info(const moe_plan_s* plan, moe_config_t* cfg, int* device)
+{
+    if (!plan) return false;
+    *cfg = plan->cfg;
+    *device = plan->device;
+    return true;
+}

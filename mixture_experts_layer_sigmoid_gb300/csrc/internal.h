@@ -9,6 +9,8 @@
 
 #include "moe.h"
 
+struct moe_plan_s;
+
 namespace moe {
 
 // Rows of one grouped-GEMM M tile; every expert segment of the permuted
@@ -108,5 +110,8 @@ template <typename T>
 cudaError_t launch_unpermute_reduce(const T* dXp, const T* dXs, const int* row_of,
                                     const int* topk, const float* dz, const float* WrT, int T_,
                                     int H, int k, T* dX, cudaStream_t s);
+
+// Configuration and device of a plan; false for a null plan.
+bool plan_info(const moe_plan_s* plan, moe_config_t* cfg, int* device);
 
 }  // namespace moe
