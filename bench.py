@@ -341,8 +341,14 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=8, help="oracle sample for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=2, help="oracle sample per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--override", default="",
+                    help="comma-separated shape overrides, e.g. F=4096,T=2048 (profiling runs)")
     args = ap.parse_args()
     w = mi.WORKLOADS[args.workload]
+    if args.override:
+        kv = dict(item.split("=") for item in args.override.split(","))
+        w = mi.scaled(w, **{k: int(v) for k, v in kv.items()},
+                      name=w.name + "[" + args.override + "]")
     if args.impl == "reference":
         run_reference(args, w)
     else:

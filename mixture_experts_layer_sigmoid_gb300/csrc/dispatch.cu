@@ -170,32 +170,35 @@ gate_grad_kernel(const T* __restrict__ dY, const T* __restrict__ Yp, const int* 
     }
 }
 
-// dWr[h][e] = sum over expert e's rows r (token order) of Xp[r][h] dz[slot(r)].
+// dWr[h][e] = sum over expert e's rows r of Xp[r][h] dz[slot(r)]. Block
+// (64 columns h, expert e): 4 row phases of 64 threads each sum every 4th row
+// of the segment, then the phases are added in fixed order.
 template <typename T>
 __global__ void __launch_bounds__(256)
 router_wgrad_kernel(const T* __restrict__ Xp, const int* __restrict__ slot_of,
                     const int* __restrict__ poff, const int* __restrict__ counts,
                     const float* __restrict__ dz, int H, int E, float* __restrict__ dWr)
 {
+    __shared__ float part[4][64];
     const int e = blockIdx.y;
-    const int h = blockIdx.x * 256 + threadIdx.x;
-    __shared__ float dzs[256];
+    const int hh = threadIdx.x & 63, ph = threadIdx.x >> 6;
+    const int h = blockIdx.x * 64 + hh;
     const int r0 = poff[e], n = counts[e];
     float acc = 0.f;
-    for (int c0 = 0; c0 < n; c0 += 256) {
-        __syncthreads();
-        if (c0 + threadIdx.x < n) dzs[threadIdx.x] = dz[slot_of[r0 + c0 + threadIdx.x]];
-        __syncthreads();
-        const int m = min(256, n - c0);
-        if (h < H)
-            for (int i = 0; i < m; ++i) {
-                float xv;
-                if constexpr (sizeof(T) == 4) xv = Xp[(size_t)(r0 + c0 + i) * H + h];
-                else xv = __bfloat162float(Xp[(size_t)(r0 + c0 + i) * H + h]);
-                acc = fmaf(xv, dzs[i], acc);
-            }
+    if (h < H) {
+#pragma unroll 4
+        for (int i = ph; i < n; i += 4) {
+            const int r = r0 + i;
+            float xv;
+            if constexpr (sizeof(T) == 4) xv = Xp[(size_t)r * H + h];
+            else xv = __bfloat162float(Xp[(size_t)r * H + h]);
+            acc = fmaf(xv, __ldg(dz + slot_of[r]), acc);
+        }
     }
-    if (h < H) dWr[(size_t)h * E + e] = acc;
+    part[ph][hh] = acc;
+    __syncthreads();
+    if (ph == 0 && h < H)
+        dWr[(size_t)h * E + e] = ((part[0][hh] + part[1][hh]) + part[2][hh]) + part[3][hh];
 }
 
 __global__ void transpose_kernel(const float* __restrict__ in, int rows, int cols, float* __restrict__ out)
@@ -295,7 +298,7 @@ cudaError_t launch_router_wgrad(const T* Xp, const int* slot_of, const int* poff
                                 float* dWr, cudaStream_t s)
 {
     (void)k;
-    dim3 grid((H + 255) / 256, E);
+    dim3 grid((H + 63) / 64, E);
     router_wgrad_kernel<T><<<grid, 256, 0, s>>>(Xp, slot_of, poff, counts, dz, H, E, dWr);
     return cudaGetLastError();
 }

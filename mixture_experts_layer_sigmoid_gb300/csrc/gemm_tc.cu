@@ -39,6 +39,7 @@ constexpr int TBK = 64;        // K block (128 bytes of bf16)
 constexpr int STRIPE = 64 * 128;  // bytes of one 64-wide MN stripe of a 64-deep k block
 constexpr int kThreads = 192;
 constexpr int kSmemBudget = 200 * 1024;
+constexpr int kGroupN = 16;    // n tiles per raster group (row-scheduled GEMMs)
 
 template <int BN>
 struct TcCfg {
@@ -74,8 +75,14 @@ __device__ __forceinline__ Tile decode_tile(const GemmDesc& d, int w, int num_m,
 {
     Tile t;
     if (SCHED == SCHED_ROWS) {
-        t.m = w % num_m;
-        t.n = w / num_m;
+        // Groups of kGroupN n-tiles: consecutive tiles share the A rows (one
+        // 128-row tile against kGroupN weight column tiles), and consecutive
+        // groups of them walk the m tiles, which share the expert's weights.
+        const int group = w / (num_m * kGroupN);
+        const int r = w - group * num_m * kGroupN;
+        const int gsz = min(kGroupN, num_n - group * kGroupN);
+        t.m = r / gsz;
+        t.n = group * kGroupN + r % gsz;
         t.row0 = t.m * TBM;
         if (d.dense_rows > 0) {
             t.e = 0;

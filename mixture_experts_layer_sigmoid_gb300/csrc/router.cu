@@ -6,7 +6,7 @@
 // §5 ("Selective precision"): the router runs in FP32.
 //
 // Kernels:
-//   router_kernel  logits z = x Wr + b (fp32 FMA, fixed summation order),
+//   router_warp_kernel (E <= 32) and router_kernel (tiled, larger E): logits z = x Wr + b (fp32 FMA, fixed summation order),
 //                  warp-shuffle top-k on z (score order equals logit order for
 //                  both softmax and sigmoid; equal values go to the lower
 //                  expert index), renormalised gates, and a per-block expert
@@ -135,6 +135,113 @@ router_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float
     }
 }
 
+// Router for E <= 32: one warp per TPW tokens. Each lane sums the logits of
+// all experts over its share of H (16-byte x vectors, Wr rows from L1/L2),
+// the partial sums are combined by a fixed butterfly, and lane e then holds
+// logit e for the warp top-k. Blocks cover kRouterTokens tokens, so the
+// per-block histogram layout is the same as router_kernel's.
+template <typename T, int EMAX, int TPW>
+__global__ void __launch_bounds__(32 * (kRouterTokens / TPW))
+router_warp_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float* __restrict__ b,
+                   int T_, int H, int E, int k, int score, int* __restrict__ topk,
+                   float* __restrict__ gates, float* __restrict__ selsc, int* __restrict__ hist)
+{
+    constexpr int V = 16 / sizeof(T);          // x elements per 16-byte vector
+    __shared__ int sel_s[kRouterTokens][kMaxK];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * kRouterTokens + warp * TPW;
+    float acc[TPW][EMAX];
+#pragma unroll
+    for (int q = 0; q < TPW; ++q)
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) acc[q][e] = 0.f;
+
+    for (int h0 = lane * V; h0 < H; h0 += 32 * V) {
+        float xv[TPW][V];
+#pragma unroll
+        for (int q = 0; q < TPW; ++q) {
+            const int t = t0 + q;
+            if (t < T_) {
+                const uint4 u = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h0);
+                const T* p = reinterpret_cast<const T*>(&u);
+#pragma unroll
+                for (int i = 0; i < V; ++i) xv[q][i] = to_f32(p[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < V; ++i) xv[q][i] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const float* wrow = Wr + (size_t)(h0 + i) * E;
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e) {
+                const float wv = (e < E) ? __ldg(wrow + e) : 0.f;
+#pragma unroll
+                for (int q = 0; q < TPW; ++q) acc[q][e] = fmaf(xv[q][i], wv, acc[q][e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < TPW; ++q)
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                acc[q][e] += __shfl_xor_sync(0xffffffffu, acc[q][e], off);
+
+#pragma unroll
+    for (int q = 0; q < TPW; ++q) {
+        const int t = t0 + q;
+        if (t >= T_) continue;                       // warp-uniform
+        float z = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e)
+            if (e == lane && e < E) z = acc[q][e] + (b ? b[e] : 0.f);
+        bool taken = false;
+        int sel_e[kMaxK];
+        float sel_z[kMaxK];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            if (j >= k) break;
+            float bv = (lane < E && !taken) ? z : -INFINITY;
+            int bi = (lane < E && !taken) ? lane : 0x7fffffff;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+            }
+            sel_e[j] = bi;
+            sel_z[j] = bv;
+            if (bi == lane) taken = true;
+        }
+        if (lane == 0) {
+            float sc[kMaxK], den = 0.f;
+            for (int j = 0; j < k; ++j) {
+                sc[j] = (score == MOE_SCORE_SOFTMAX) ? expf(sel_z[j] - sel_z[0])
+                                                     : 1.f / (1.f + expf(-sel_z[j]));
+                den += sc[j];
+            }
+            for (int j = 0; j < k; ++j) {
+                topk[(size_t)t * k + j] = sel_e[j];
+                gates[(size_t)t * k + j] = sc[j] / den;
+                selsc[(size_t)t * k + j] = sc[j];
+                sel_s[warp * TPW + q][j] = sel_e[j];
+            }
+        }
+    }
+    __syncthreads();
+    const int tb = blockIdx.x * kRouterTokens;
+    const int ntok = min(kRouterTokens, T_ - tb);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int c = 0;
+        for (int tt = 0; tt < ntok; ++tt)
+            for (int j = 0; j < k; ++j) c += (sel_s[tt][j] == e);
+        hist[(size_t)blockIdx.x * E + e] = c;
+    }
+}
+
 __global__ void __launch_bounds__(kMaxE)
 scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ counts,
             int* __restrict__ poff, int* __restrict__ blkbase, int* __restrict__ tile_tab,
@@ -205,8 +312,15 @@ cudaError_t launch_router(const T* x, const float* Wr, const float* b, int T_, i
                           cudaStream_t s)
 {
     const int nblk = (T_ + kRouterTokens - 1) / kRouterTokens;
-    if (E <= 32)
-        router_kernel<T, 1><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+    if (E <= 8)
+        router_warp_kernel<T, 8, 4><<<nblk, 32 * (kRouterTokens / 4), 0, s>>>(
+            x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+    else if (E <= 16)
+        router_warp_kernel<T, 16, 4><<<nblk, 32 * (kRouterTokens / 4), 0, s>>>(
+            x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+    else if (E <= 32)
+        router_warp_kernel<T, 32, 2><<<nblk, 32 * (kRouterTokens / 2), 0, s>>>(
+            x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
     else if (E <= 64)
         router_kernel<T, 2><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
     else if (E <= 128)

@@ -11,8 +11,9 @@ Training of Mixture-of-Experts Models with Megatron Core", §2):
     that choice (router replay) so downstream tensors compare like with like;
   - floating-point tensors: relative L2 error and max |error| / rms(reference)
     within the bounds of the dtype (bf16: 1e-2 and 4e-2; fp32: 1e-4 and 1e-3);
-  - bf16 expert weight gradients (dW_gate, dW_up, dW_down and the shared
-    expert's): relative L2 <= 1e-2 over the whole tensor AND over each
+  - bf16 weight gradients (dW_gate, dW_up, dW_down, the shared expert's, and
+    the router's dWr, whose expert columns are sums over each expert's
+    tokens): relative L2 <= 1e-2 over the whole tensor AND over each
     expert's block, and every element within the first-order forward-error
     bound of the bf16/fp32 arithmetic that produces it (wgrad_bounds). The
     max |error| / rms criterion is not used for them: each entry is a sum over
@@ -98,24 +99,57 @@ def _expert_wgrad_bounds(X, Wg, Wu, Wd, g, dY, dYp_rounded=True):
           + U * np.abs(h.T @ dYp))
     bg = aX.T @ dA_err + mv * (aX.T @ np.abs(dA)) + U * np.abs(X.T @ dA)
     bu = aX.T @ dU_err + mv * (aX.T @ np.abs(dU)) + U * np.abs(X.T @ dU)
-    return bg, bu, bd
+    # gate gradient dg = <dY, Yp> with Yp = h Wd (fp32 sum over F, bf16 output)
+    F = Wd.shape[0]
+    yp = h @ Wd
+    yp_err = h_err @ np.abs(Wd) + F * V * (np.abs(h) @ np.abs(Wd)) + U * np.abs(yp)
+    dg_err = (np.abs(dY) * yp_err).sum(1) + H * V * (np.abs(dY) * np.abs(yp)).sum(1)
+    return bg, bu, bd, dg_err
 
 
 def wgrad_bounds(w, inp, r):
-    """Elementwise error bounds for every expert weight gradient (bf16)."""
+    """Elementwise error bounds for every weight gradient of the bf16 path:
+    the experts' (stacked E×…), the shared expert's and the router's dWr.
+
+    dWr[h][e] = sum over e's tokens of x[t][h] dz[t][e]; dz is linear in the
+    gate gradients dg = <dY, Yp>, whose error comes from the bf16 expert
+    output Yp (h rounding, fp32 sum over F, bf16 output) and the fp32 sum
+    over H; the dz formula's coefficients carry it to dz."""
+    U, V = BF16_U, FP32_U
     x, dY = to_np(inp["x"]), to_np(inp["dY"])
     Wg, Wu, Wd = to_np(inp["Wg"]), to_np(inp["Wu"]), to_np(inp["Wd"])
     out = {n: np.zeros_like(v) for n, v in (("dWg", Wg), ("dWu", Wu), ("dWd", Wd))}
+    dg_err = np.zeros_like(r["gates"])
     for e in range(w.E):
         toks, slots = np.nonzero(r["topk"] == e)
         if len(toks) == 0:
             continue
-        out["dWg"][e], out["dWu"][e], out["dWd"][e] = _expert_wgrad_bounds(
+        out["dWg"][e], out["dWu"][e], out["dWd"][e], dg_err[toks, slots] = _expert_wgrad_bounds(
             x[toks], Wg[e], Wu[e], Wd[e], r["gates"][toks, slots][:, None], dY[toks])
     if w.Fs:
-        out["dWsg"], out["dWsu"], out["dWsd"] = _expert_wgrad_bounds(
+        out["dWsg"], out["dWsu"], out["dWsd"], _ = _expert_wgrad_bounds(
             x, to_np(inp["Wsg"]), to_np(inp["Wsu"]), to_np(inp["Wsd"]), np.ones((w.T, 1)), dY,
             dYp_rounded=False)
+    g = r["gates"]
+    spread = dg_err + (g * dg_err).sum(1, keepdims=True)
+    if w.score == mi.SOFTMAX:
+        dz_err = g * spread
+    else:
+        s = np.take_along_axis(r["scores"], r["topk"].astype(np.int64), 1)
+        dz_err = s * (1 - s) / s.sum(1, keepdims=True) * spread
+    # magnitude of dz itself, for the fp32 accumulation term of the router wgrad
+    dz_mag = np.zeros_like(g)
+    ref_dg = r.get("dg")
+    if ref_dg is not None:
+        spread_m = np.abs(ref_dg) + (g * np.abs(ref_dg)).sum(1, keepdims=True)
+        dz_mag = g * spread_m if w.score == mi.SOFTMAX else s * (1 - s) / s.sum(1, keepdims=True) * spread_m
+    dz_err_dense = np.zeros((w.T, w.E))
+    dz_mag_dense = np.zeros((w.T, w.E))
+    np.put_along_axis(dz_err_dense, r["topk"].astype(np.int64), dz_err, 1)
+    np.put_along_axis(dz_mag_dense, r["topk"].astype(np.int64), dz_mag, 1)
+    counts = np.bincount(r["topk"].ravel(), minlength=w.E)
+    ax = np.abs(x)
+    out["dWr"] = ax.T @ dz_err_dense + counts[None, :] * V * (ax.T @ dz_mag_dense)
     return out
 
 
@@ -210,6 +244,7 @@ def oracle_layer(w, inp, r, backward=True):
 GRAD_NAMES = [("dX", "dX"), ("dWr", "dWr"), ("dW_gate", "dWg"), ("dW_up", "dWu"),
               ("dW_down", "dWd"), ("dWs_gate", "dWsg"), ("dWs_up", "dWsu"), ("dWs_down", "dWsd")]
 EXPERT_WGRADS = {"dWg", "dWu", "dWd", "dWsg", "dWsu", "dWsd"}
+COLUMN_BLOCKS = {"dWr"}      # one block per expert column
 
 
 def compare_all(w, inp, r, gpu, ref, backward=True):
@@ -217,13 +252,15 @@ def compare_all(w, inp, r, gpu, ref, backward=True):
     report = {"y": assert_close("y", to_np(gpu["y"]), ref["y"], w.dtype)}
     if not backward:
         return report
-    bounds = wgrad_bounds(w, inp, r) if w.dtype == mi.BF16 else None
+    bounds = wgrad_bounds(w, inp, dict(r, dg=ref.get("dg"))) if w.dtype == mi.BF16 else None
     for gname, oname in GRAD_NAMES:
         if oname not in ref:
             continue
         got = to_np(gpu[gname])
         if bounds is not None and oname in EXPERT_WGRADS:
             report[gname] = assert_wgrad(gname, got, ref[oname], bounds[oname])
+        elif bounds is not None and oname in COLUMN_BLOCKS:
+            report[gname] = assert_wgrad(gname, got.T, ref[oname].T, bounds[oname].T)
         else:
             report[gname] = assert_close(gname, got, ref[oname], w.dtype)
     return report
