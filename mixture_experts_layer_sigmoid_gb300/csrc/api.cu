@@ -21,7 +21,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct Layout {
     int T, R, Rp_max, MT_max, NB;
     // saved
-    size_t topk, gates, selsc, counts, poff, meta, tiletab, rowof, slotof;
+    size_t topk, gates, selsc, counts, poff, meta, tiletab, pairtab, rowof, slotof;
     size_t Xp, A, U, Hh, Yp, As, Us, Hs, saved_bytes;
     // workspace
     size_t status, hist, blkbase, Ys, dYp, dA, dU, dXp, dz, WrT, dAs, dUs, dXs, ws_bytes;
@@ -46,6 +46,7 @@ Layout make_layout(const moe_config_t& c, int T)
     L.poff = take(sizeof(int) * (c.E + 1));
     L.meta = take(sizeof(int) * 4);
     L.tiletab = take(sizeof(int) * L.MT_max);
+    L.pairtab = take(sizeof(int) * L.MT_max);
     L.rowof = take(sizeof(int) * L.R);
     L.slotof = take(sizeof(int) * L.Rp_max);
     L.Xp = take(es * L.Rp_max * c.H);
@@ -286,6 +287,7 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     int* poff = reinterpret_cast<int*>(sv + L.poff);
     int* meta = reinterpret_cast<int*>(sv + L.meta);
     int* tiletab = reinterpret_cast<int*>(sv + L.tiletab);
+    int* pairtab = reinterpret_cast<int*>(sv + L.pairtab);
     int* rowof = reinterpret_cast<int*>(sv + L.rowof);
     int* slotof = reinterpret_cast<int*>(sv + L.slotof);
     T* Xp = reinterpret_cast<T*>(sv + L.Xp);
@@ -300,7 +302,7 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     MOE_STAGE(ST_ROUTER, launch_router<T>(x, a->Wr, a->b, T_, H, E, k, c.score, topk, gates, selsc,
                               reinterpret_cast<int*>(ws + L.hist), s));
     MOE_STAGE(ST_SCAN, launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
-                         reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s));
+                         reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab));
     MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
     MOE_STAGE(ST_PERMUTE, launch_permute<T>(x, rowof, poff, counts, T_, H, E, k, Xp, s));
 
@@ -313,7 +315,8 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
     d.N = F; d.K = H; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab;
+    d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = Xp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = a->W_gate; d.B1 = a->W_up; d.ldb = F; d.b_kmajor = 0; d.b_estride = (long long)H * F;
     d.b_rows = E * H;
@@ -323,7 +326,8 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
     d.N = H; d.K = F; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab;
+    d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = Hh; d.lda = F; d.a_rows = L.Rp_max;
     d.B0 = a->W_down; d.ldb = H; d.b_kmajor = 0; d.b_estride = (long long)F * H; d.b_rows = E * F;
     d.O0 = Yp; d.ldo = H; d.status = status;
@@ -373,6 +377,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     const int* poff = reinterpret_cast<const int*>(sv + L.poff);
     const int* meta = reinterpret_cast<const int*>(sv + L.meta);
     const int* tiletab = reinterpret_cast<const int*>(sv + L.tiletab);
+    const int* pairtab = reinterpret_cast<const int*>(sv + L.pairtab);
     const int* rowof = reinterpret_cast<const int*>(sv + L.rowof);
     const int* slotof = reinterpret_cast<const int*>(sv + L.slotof);
     const T* Xp = reinterpret_cast<const T*>(sv + L.Xp);
@@ -402,7 +407,8 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_BWD; d.dual = DUAL_NONE;
     d.N = F; d.K = H; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab;
+    d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = dYp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = a->W_down; d.ldb = H; d.b_kmajor = 1; d.b_estride = (long long)F * H; d.b_rows = E * F;
     d.X0 = A; d.X1 = U; d.O0 = dA; d.O1 = dU; d.ldo = F; d.status = status;
@@ -411,7 +417,8 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
     d.N = H; d.M_out = F; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab;
+    d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = Hh; d.lda = F; d.a_rows = L.Rp_max;
     d.B0 = dYp; d.ldb = H; d.b_rows = L.Rp_max;
     d.O0 = a->dW_down; d.ldo = H; d.o_estride = (long long)F * H; d.status = status;
@@ -420,7 +427,8 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
     d.N = H; d.K = F; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab;
+    d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = dA; d.A1 = dU; d.lda = F; d.a_rows = L.Rp_max;
     d.B0 = a->W_gate; d.B1 = a->W_up; d.ldb = F; d.b_kmajor = 1; d.b_estride = (long long)H * F;
     d.b_rows = E * H;
@@ -430,7 +438,8 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
     d.N = F; d.M_out = H; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab;
+    d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = Xp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = dA; d.B1 = dU; d.ldb = F; d.b_rows = L.Rp_max;
     d.O0 = a->dW_gate; d.O1 = a->dW_up; d.ldo = F; d.o_estride = (long long)H * F; d.status = status;

@@ -41,63 +41,76 @@ constexpr int kThreads = 192;
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kGroupN = 16;    // n tiles per raster group (row-scheduled GEMMs)
 
-template <int BN>
+template <int BN, bool PAIR>
 struct TcCfg {
-    static constexpr int A_BYTES = TBM * TBK * 2;
-    static constexpr int B_BYTES = BN * TBK * 2;
+    static constexpr int A_BYTES = TBM * TBK * 2;            // this CTA's 128 rows of A
+    static constexpr int B_COLS = PAIR ? BN / 2 : BN;        // this CTA's share of B
+    static constexpr int B_BYTES = B_COLS * TBK * 2;
     static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int STAGES = kSmemBudget / STAGE;
+    // Pair mode leaves one spare B-sized block after the ring.
+    static constexpr int GUARD = PAIR ? B_BYTES : 0;
+    static constexpr int BUDGET = PAIR ? 216 * 1024 : kSmemBudget;
+    static constexpr int STAGES = (BUDGET - GUARD) / STAGE;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM = 1024 + STAGES * STAGE + 256;
+    static constexpr int SMEM = 1024 + STAGES * STAGE + GUARD + 256;
 };
 
 struct Tile {
     int e, m, n, row0, kblocks, valid_end, alloc_end;
 };
 
-template <int BN, int DUAL, int SCHED>
+// Scheduling units: single CTAs work on 128-row tiles; CTA pairs on 256-row
+// units (two 128-row tiles, one per CTA).
+template <int BN, int DUAL, int SCHED, bool PAIR>
 __device__ __forceinline__ void tile_counts(const GemmDesc& d, int& num_m, int& num_n, int& total)
 {
     constexpr int NW = (DUAL == DUAL_N) ? BN / 2 : BN;   // output columns per tile
     if (SCHED == SCHED_ROWS) {
-        num_m = d.dense_rows > 0 ? (d.dense_rows + TBM - 1) / TBM : d.meta[0];
+        const int tiles = d.dense_rows > 0 ? (d.dense_rows + TBM - 1) / TBM : d.meta[0];
+        num_m = PAIR ? (d.dense_rows > 0 ? (tiles + 1) / 2 : d.meta[2]) : tiles;
         num_n = d.N / NW;
         total = num_m * num_n;
     } else {
-        num_m = d.M_out / TBM;
+        num_m = d.M_out / (PAIR ? 2 * TBM : TBM);
         num_n = d.N / NW;
         total = d.E * num_m * num_n;
     }
 }
 
-template <int BN, int DUAL, int SCHED>
-__device__ __forceinline__ Tile decode_tile(const GemmDesc& d, int w, int num_m, int num_n)
+template <int BN, int DUAL, int SCHED, bool PAIR>
+__device__ __forceinline__ Tile decode_tile(const GemmDesc& d, int w, int num_m, int num_n, int rank)
 {
     Tile t;
     if (SCHED == SCHED_ROWS) {
-        // Groups of kGroupN n-tiles: consecutive tiles share the A rows (one
-        // 128-row tile against kGroupN weight column tiles), and consecutive
-        // groups of them walk the m tiles, which share the expert's weights.
+        // Groups of kGroupN n-tiles: consecutive units share the A rows (one
+        // row unit against kGroupN weight column tiles), and consecutive
+        // groups of them walk the row units, which share the expert's weights.
         const int group = w / (num_m * kGroupN);
         const int r = w - group * num_m * kGroupN;
         const int gsz = min(kGroupN, num_n - group * kGroupN);
-        t.m = r / gsz;
+        const int mu = r / gsz;
         t.n = group * kGroupN + r % gsz;
-        t.row0 = t.m * TBM;
         if (d.dense_rows > 0) {
+            t.m = PAIR ? 2 * mu + rank : mu;
             t.e = 0;
             t.valid_end = t.alloc_end = d.dense_rows;
         } else {
-            t.e = d.tile_tab[t.m];
+            // a pair's second tile may lie past its expert's segment ("ghost"):
+            // its rows are beyond alloc_end, so nothing of it is stored
+            const int first = PAIR ? d.pair_tab[mu] : mu;
+            t.m = first + rank;
+            t.e = d.tile_tab[first];
             t.valid_end = d.poff[t.e] + d.counts[t.e];
             t.alloc_end = d.poff[t.e + 1];
         }
+        t.row0 = t.m * TBM;
         t.kblocks = ((DUAL == DUAL_K) ? 2 * d.K : d.K) / TBK;
     } else {
         const int per = num_m * num_n;
         t.e = w / per;
         const int r = w % per;
-        t.m = r % num_m;
+        const int mu = r % num_m;
+        t.m = PAIR ? 2 * mu + rank : mu;
         t.n = r / num_m;
         if (d.dense_rows > 0) {
             t.row0 = 0;
@@ -152,25 +165,31 @@ __device__ __forceinline__ void tmem_load32f(uint32_t taddr, float (&v)[32])
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int BN, bool B_MN, int DUAL, int EPI, int SCHED>
+// PAIR: launched as clusters of 2; the even CTA issues M=256 MMAs whose A
+// rows 0-127 / 128-255 and B columns are split between the two CTAs'
+// shared memory, and each CTA reads its own 128 rows of the accumulator.
+template <int BN, bool B_MN, int DUAL, int EPI, int SCHED, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
                const GemmDesc d)
 {
-    using C = TcCfg<BN>;
+    using C = TcCfg<BN, PAIR>;
     constexpr bool A_MN = (SCHED == SCHED_WGRAD);
-    constexpr uint32_t IDESC = ptx::idesc_bf16<BN, A_MN, B_MN>();
+    constexpr uint32_t IDESC = ptx::idesc_bf16<BN, A_MN, B_MN, PAIR ? 2 * TBM : TBM>();
     constexpr int NW = (DUAL == DUAL_N) ? BN / 2 : BN;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE + C::GUARD);
     // bars: full[STAGES], empty[STAGES], accf[2], acce[2], final
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = PAIR ? (int)ptx::cluster_ctarank() : 0;
+    const int unit0 = PAIR ? (int)ptx::cluster_id_x() : (int)blockIdx.x;
+    const int nunits = PAIR ? (int)ptx::nclusters_x() : (int)gridDim.x;
     const uint32_t bar0 = ptx::smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
@@ -185,7 +204,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(accf_bar(a), 1);
-            ptx::mbar_init(acce_bar(a), 4);
+            ptx::mbar_init(acce_bar(a), PAIR ? 8 : 4);
         }
         ptx::mbar_init(final_bar, 1);
         *abort_flag = 0;
@@ -200,16 +219,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
         }
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
-        ptx::tmem_relinquish();
+        if (PAIR) {
+            ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    if (PAIR) ptx::cluster_sync();   // peer barriers initialised before any remote signal
+    else __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     int num_m, num_n, total;
-    tile_counts<BN, DUAL, SCHED>(d, num_m, num_n, total);
+    tile_counts<BN, DUAL, SCHED, PAIR>(d, num_m, num_n, total);
 
     // Each role runs its loop with the whole warp; lane 0 waits and issues, and
     // the wait's outcome is broadcast so the warp stays converged.
@@ -218,50 +243,62 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
         if (lane == 0) ok = ptx::wait_bounded(bar, parity, abort_flag, d.status, where) ? 1 : 0;
         return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
+    auto load = [&](uint32_t dst, const CUtensorMap* m, int s, int x, int y) {
+        if (PAIR) ptx::tma_load_2d_pair(dst, m, ptx::mapa_shared(full_bar(s), 0), x, y);
+        else ptx::tma_load_2d(dst, m, full_bar(s), x, y);
+    };
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
         uint32_t it = 0;
         const int kb_half = d.K / TBK;
         bool ok = true;
-        for (int w = blockIdx.x; ok && w < total; w += gridDim.x) {
-            const Tile t = decode_tile<BN, DUAL, SCHED>(d, w, num_m, num_n);
+        for (int w = unit0; ok && w < total; w += nunits) {
+            const Tile t = decode_tile<BN, DUAL, SCHED, PAIR>(d, w, num_m, num_n, rank);
             for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
                 const int s = it % C::STAGES;
                 const uint32_t ph = (it / C::STAGES) & 1u;
                 if (!wait_uniform(empty_bar(s), ph ^ 1u, 1)) { ok = false; break; }
                 if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(full_bar(s), C::STAGE);
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(s), (PAIR ? 2 : 1) * C::STAGE);
                     const uint32_t a_dst = ptx::smem_u32(smem + s * C::STAGE);
                     const uint32_t b_dst = a_dst + C::A_BYTES;
+                    // this CTA's B columns: a DUAL_N pair splits [B0 | B1] between
+                    // the CTAs; otherwise the CTA takes its half of the BN columns
+                    const CUtensorMap* bmap = (DUAL == DUAL_N && (PAIR ? rank == 1 : false)) ? &mB1 : &mB0;
+                    const int bcol0 = t.n * NW + ((PAIR && DUAL != DUAL_N) ? rank * C::B_COLS : 0);
                     if (SCHED == SCHED_ROWS) {
                         const bool second = (DUAL == DUAL_K) && kb >= kb_half;
                         const int kx = (second ? kb - kb_half : kb) * TBK;
-                        ptx::tma_load_2d(a_dst, second ? &mA1 : &mA0, full_bar(s), kx, t.row0);
+                        load(a_dst, second ? &mA1 : &mA0, s, kx, t.row0);
                         if (B_MN) {
 #pragma unroll
-                            for (int s2 = 0; s2 < BN / 64; ++s2) {
-                                const bool hi = (DUAL == DUAL_N) && s2 >= BN / 128;
-                                const int x = (DUAL == DUAL_N) ? t.n * NW + 64 * (s2 % (BN / 128))
-                                                               : t.n * NW + 64 * s2;
-                                ptx::tma_load_2d(b_dst + s2 * STRIPE, hi ? &mB1 : &mB0, full_bar(s), x,
-                                                 t.e * d.K + kb * TBK);
+                            for (int s2 = 0; s2 < C::B_COLS / 64; ++s2) {
+                                const CUtensorMap* m = bmap;
+                                int x = bcol0 + 64 * s2;
+                                if (!PAIR && DUAL == DUAL_N) {
+                                    m = s2 >= BN / 128 ? &mB1 : &mB0;
+                                    x = t.n * NW + 64 * (s2 % (BN / 128));
+                                }
+                                load(b_dst + s2 * STRIPE, m, s, x, t.e * d.K + kb * TBK);
                             }
                         } else {
-                            ptx::tma_load_2d(b_dst, second ? &mB1 : &mB0, full_bar(s), kx,
-                                             t.e * d.N + t.n * NW);
+                            load(b_dst, second ? &mB1 : &mB0, s, kx, t.e * d.N + bcol0);
                         }
                     } else {
                         const int krow = t.row0 + kb * TBK;
 #pragma unroll
                         for (int s2 = 0; s2 < TBM / 64; ++s2)
-                            ptx::tma_load_2d(a_dst + s2 * STRIPE, &mA0, full_bar(s), t.m * TBM + 64 * s2, krow);
+                            load(a_dst + s2 * STRIPE, &mA0, s, t.m * TBM + 64 * s2, krow);
 #pragma unroll
-                        for (int s2 = 0; s2 < BN / 64; ++s2) {
-                            const bool hi = (DUAL == DUAL_N) && s2 >= BN / 128;
-                            const int x = (DUAL == DUAL_N) ? t.n * NW + 64 * (s2 % (BN / 128))
-                                                           : t.n * NW + 64 * s2;
-                            ptx::tma_load_2d(b_dst + s2 * STRIPE, hi ? &mB1 : &mB0, full_bar(s), x, krow);
+                        for (int s2 = 0; s2 < C::B_COLS / 64; ++s2) {
+                            const CUtensorMap* m = bmap;
+                            int x = bcol0 + 64 * s2;
+                            if (!PAIR && DUAL == DUAL_N) {
+                                m = s2 >= BN / 128 ? &mB1 : &mB0;
+                                x = t.n * NW + 64 * (s2 % (BN / 128));
+                            }
+                            load(b_dst + s2 * STRIPE, m, s, x, krow);
                         }
                     }
                 }
@@ -269,42 +306,54 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
-        uint32_t it = 0, tc = 0;
-        bool ok = true;
-        for (int w = blockIdx.x; ok && w < total; w += gridDim.x, ++tc) {
-            const Tile t = decode_tile<BN, DUAL, SCHED>(d, w, num_m, num_n);
-            const int a = tc & 1;
-            const uint32_t aph = (tc >> 1) & 1u;
-            if (!wait_uniform(acce_bar(a), aph ^ 1u, 2)) { ok = false; break; }
-            ptx::tc_fence_after();
-            const uint32_t d_tmem = tmem_base + (uint32_t)(a * BN);
-            for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
-                const int s = it % C::STAGES;
-                const uint32_t ph = (it / C::STAGES) & 1u;
-                if (!wait_uniform(full_bar(s), ph, 3)) { ok = false; break; }
+        if (rank == 0) {
+            // --------------------------------------------------- MMA issuer
+            uint32_t it = 0, tc = 0;
+            bool ok = true;
+            for (int w = unit0; ok && w < total; w += nunits, ++tc) {
+                const Tile t = decode_tile<BN, DUAL, SCHED, PAIR>(d, w, num_m, num_n, rank);
+                const int a = tc & 1;
+                const uint32_t aph = (tc >> 1) & 1u;
+                if (!wait_uniform(acce_bar(a), aph ^ 1u, 2)) { ok = false; break; }
                 ptx::tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t a_addr = ptx::smem_u32(smem + s * C::STAGE);
-                    const uint32_t b_addr = a_addr + C::A_BYTES;
+                const uint32_t d_tmem = tmem_base + (uint32_t)(a * BN);
+                for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
+                    const int s = it % C::STAGES;
+                    const uint32_t ph = (it / C::STAGES) & 1u;
+                    if (!wait_uniform(full_bar(s), ph, 3)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t a_addr = ptx::smem_u32(smem + s * C::STAGE);
+                        const uint32_t b_addr = a_addr + C::A_BYTES;
 #pragma unroll
-                    for (int k = 0; k < TBK / 16; ++k) {
-                        const uint64_t ad = A_MN ? ptx::smem_desc_sw128(a_addr + k * 2048, STRIPE, 1024)
-                                                 : ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
-                        const uint64_t bd = B_MN ? ptx::smem_desc_sw128(b_addr + k * 2048, STRIPE, 1024)
-                                                 : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
-                        ptx::tc_mma_f16(d_tmem, ad, bd, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < TBK / 16; ++k) {
+                            const uint64_t ad = A_MN ? ptx::smem_desc_sw128(a_addr + k * 2048, STRIPE, 1024)
+                                                     : ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
+                            const uint64_t bd = B_MN ? ptx::smem_desc_sw128(b_addr + k * 2048, STRIPE, 1024)
+                                                     : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
+                            const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+                            if (PAIR) ptx::tc_mma_f16_pair(d_tmem, ad, bd, IDESC, acc);
+                            else ptx::tc_mma_f16(d_tmem, ad, bd, IDESC, acc);
+                        }
+                        if (PAIR) ptx::tc_commit_pair(empty_bar(s), 3);
+                        else ptx::tc_commit(empty_bar(s));
                     }
-                    ptx::tc_commit(empty_bar(s));
+                    __syncwarp();
+                }
+                if (ok && lane == 0) {
+                    if (PAIR) ptx::tc_commit_pair(accf_bar(a), 3);
+                    else ptx::tc_commit(accf_bar(a));
                 }
                 __syncwarp();
             }
-            if (ok && lane == 0) ptx::tc_commit(accf_bar(a));
-            __syncwarp();
+            // every MMA issued by this warp has completed before TMEM is freed
+            if (lane == 0) {
+                if (PAIR) ptx::tc_commit_pair(final_bar, 3);
+                else ptx::tc_commit(final_bar);
+            }
         }
-        // every MMA issued by this warp has completed before TMEM is freed
+        // (in a pair, the odd CTA's TMEM is written by its peer's MMAs)
         if (lane == 0) {
-            ptx::tc_commit(final_bar);
             volatile int never = 0;
             ptx::wait_bounded(final_bar, 0, &never, d.status, 4);
         }
@@ -314,8 +363,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
         const int r_in = q * 32 + lane;         // row of the tile owned by this thread
         uint32_t tc = 0;
-        for (int w = blockIdx.x; w < total; w += gridDim.x, ++tc) {
-            const Tile t = decode_tile<BN, DUAL, SCHED>(d, w, num_m, num_n);
+        for (int w = unit0; w < total; w += nunits, ++tc) {
+            const Tile t = decode_tile<BN, DUAL, SCHED, PAIR>(d, w, num_m, num_n, rank);
             const int a = tc & 1;
             const uint32_t aph = (tc >> 1) & 1u;
             if (!wait_uniform(accf_bar(a), aph, 5)) break;
@@ -397,15 +446,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(acce_bar(a));
+            if (lane == 0) {
+                if (PAIR) ptx::mbar_arrive_cluster(ptx::mapa_shared(acce_bar(a), 0));
+                else ptx::mbar_arrive(acce_bar(a));
+            }
         }
     }
 
-    __syncthreads();
+    ptx::tc_fence_before();
+    if (PAIR) ptx::cluster_sync();   // both CTAs done with TMEM and with remote signals
+    else __syncthreads();
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+        if (PAIR) ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
 }
 
@@ -442,20 +497,48 @@ bool make_map(CUtensorMap* m, const void* ptr, long long rows, long long cols, l
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool B_MN, int DUAL, int EPI, int SCHED>
+template <int BN, bool B_MN, int DUAL, int EPI, int SCHED, bool PAIR>
 cudaError_t set_attr()
 {
-    return cudaFuncSetAttribute(gemm_tc_kernel<BN, B_MN, DUAL, EPI, SCHED>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BN>::SMEM);
+    return cudaFuncSetAttribute(gemm_tc_kernel<BN, B_MN, DUAL, EPI, SCHED, PAIR>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BN, PAIR>::SMEM);
 }
 
+// Co-resident clusters of two for a pair kernel (0 if it cannot launch).
 template <int BN, bool B_MN, int DUAL, int EPI, int SCHED>
+int pair_slots()
+{
+    static int slots = -1;
+    if (slots < 0) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = TcCfg<BN, true>::SMEM;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, B_MN, DUAL, EPI, SCHED, true>, &cfg) !=
+            cudaSuccess)
+            n = 0;
+        cudaGetLastError();
+        slots = n;
+    }
+    return slots;
+}
+
+template <int BN, bool B_MN, int DUAL, int EPI, int SCHED, bool PAIR>
 cudaError_t run(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
 {
     constexpr int NW = (DUAL == DUAL_N) ? BN / 2 : BN;
+    constexpr int BROWS = TcCfg<BN, PAIR>::B_COLS;   // K-major B box rows
     CUtensorMap mA0, mA1, mB0, mB1;
     bool ok = true;
-    long long total;
+    long long units;
     if (SCHED == SCHED_ROWS) {
         // A: [a_rows][K] read as 128-row boxes. B: per-expert blocks stacked.
         ok &= make_map(&mA0, d.A0, d.a_rows, d.K, d.lda, TBM);
@@ -464,24 +547,58 @@ cudaError_t run(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
             ok &= make_map(&mB0, d.B0, d.b_rows, d.N, d.ldb, 64);
             ok &= make_map(&mB1, d.B1 ? d.B1 : d.B0, d.b_rows, d.N, d.ldb, 64);
         } else {      // B[e*N + n][k]
-            ok &= make_map(&mB0, d.B0, d.b_rows, d.K, d.ldb, BN);
-            ok &= make_map(&mB1, d.B1 ? d.B1 : d.B0, d.b_rows, d.K, d.ldb, BN);
+            ok &= make_map(&mB0, d.B0, d.b_rows, d.K, d.ldb, BROWS);
+            ok &= make_map(&mB1, d.B1 ? d.B1 : d.B0, d.b_rows, d.K, d.ldb, BROWS);
         }
-        const long long m_tiles = d.dense_rows > 0 ? (d.dense_rows + TBM - 1) / TBM : max_m_tiles;
-        total = m_tiles * (d.N / NW);
+        long long m_tiles = d.dense_rows > 0 ? (d.dense_rows + TBM - 1) / TBM : max_m_tiles;
+        if (PAIR) m_tiles = (m_tiles + 1) / 2;
+        units = m_tiles * (d.N / NW);
     } else {
         // A: [rows][M_out], B: [rows][N], read as 64-row boxes of 64 columns.
         ok &= make_map(&mA0, d.A0, d.a_rows, d.M_out, d.lda, 64);
         mA1 = mA0;
-        ok &= make_map(&mB0, d.B0, d.b_rows, DUAL == DUAL_N ? d.N : d.N, d.ldb, 64);
+        ok &= make_map(&mB0, d.B0, d.b_rows, d.N, d.ldb, 64);
         ok &= make_map(&mB1, d.B1 ? d.B1 : d.B0, d.b_rows, d.N, d.ldb, 64);
-        total = (long long)d.E * (d.M_out / TBM) * (d.N / NW);
+        units = (long long)d.E * (d.M_out / (PAIR ? 2 * TBM : TBM)) * (d.N / NW);
     }
     if (!ok) return cudaErrorInvalidValue;
-    if (total <= 0) return cudaSuccess;
-    const int grid = (int)(total < num_sms ? total : num_sms);
-    gemm_tc_kernel<BN, B_MN, DUAL, EPI, SCHED><<<grid, kThreads, TcCfg<BN>::SMEM, s>>>(mA0, mA1, mB0, mB1, d);
-    return cudaGetLastError();
+    if (units <= 0) return cudaSuccess;
+    if (!PAIR) {
+        const int grid = (int)(units < num_sms ? units : num_sms);
+        gemm_tc_kernel<BN, B_MN, DUAL, EPI, SCHED, false>
+            <<<grid, kThreads, TcCfg<BN, false>::SMEM, s>>>(mA0, mA1, mB0, mB1, d);
+        return cudaGetLastError();
+    }
+    const int slots = pair_slots<BN, B_MN, DUAL, EPI, SCHED>();
+    if (slots <= 0) return cudaErrorLaunchOutOfResources;
+    const long long clusters = units < slots ? units : slots;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = TcCfg<BN, true>::SMEM;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, B_MN, DUAL, EPI, SCHED, true>, mA0, mA1, mB0,
+                              mB1, d);
+}
+
+// Single-CTA or CTA-pair instance: pairs when the row units come in
+// (mostly) complete pairs.
+template <int BN, bool B_MN, int DUAL, int EPI, int SCHED>
+cudaError_t run_any(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
+{
+    bool pair;
+    if (SCHED == SCHED_WGRAD) pair = d.M_out % (2 * TBM) == 0;
+    else if (d.dense_rows > 0) pair = d.dense_rows > TBM;
+    else pair = d.pair_tab != nullptr && d.prefer_pair;
+    if (pair) return run<BN, B_MN, DUAL, EPI, SCHED, true>(d, max_m_tiles, num_sms, s);
+    return run<BN, B_MN, DUAL, EPI, SCHED, false>(d, max_m_tiles, num_sms, s);
 }
 
 }  // namespace
@@ -492,16 +609,20 @@ cudaError_t gemm_tc_prepare(int device)
     if (!get_encode()) return cudaErrorNotSupported;
     cudaError_t e = cudaSuccess;
     auto acc = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
-    acc(set_attr<256, true, DUAL_N, EPI_SWIGLU_FWD, SCHED_ROWS>());
-    acc(set_attr<256, true, DUAL_NONE, EPI_STORE, SCHED_ROWS>());
-    acc(set_attr<128, true, DUAL_NONE, EPI_STORE, SCHED_ROWS>());
-    acc(set_attr<256, false, DUAL_NONE, EPI_SWIGLU_BWD, SCHED_ROWS>());
-    acc(set_attr<128, false, DUAL_NONE, EPI_SWIGLU_BWD, SCHED_ROWS>());
-    acc(set_attr<256, false, DUAL_K, EPI_STORE, SCHED_ROWS>());
-    acc(set_attr<128, false, DUAL_K, EPI_STORE, SCHED_ROWS>());
-    acc(set_attr<256, true, DUAL_NONE, EPI_WGRAD, SCHED_WGRAD>());
-    acc(set_attr<128, true, DUAL_NONE, EPI_WGRAD, SCHED_WGRAD>());
-    acc(set_attr<256, true, DUAL_N, EPI_WGRAD, SCHED_WGRAD>());
+#define MOE_ATTR(BN, BMN, DUAL, EPI, SCHED)                       \
+    acc(set_attr<BN, BMN, DUAL, EPI, SCHED, false>());             \
+    acc(set_attr<BN, BMN, DUAL, EPI, SCHED, true>());
+    MOE_ATTR(256, true, DUAL_N, EPI_SWIGLU_FWD, SCHED_ROWS)
+    MOE_ATTR(256, true, DUAL_NONE, EPI_STORE, SCHED_ROWS)
+    MOE_ATTR(128, true, DUAL_NONE, EPI_STORE, SCHED_ROWS)
+    MOE_ATTR(256, false, DUAL_NONE, EPI_SWIGLU_BWD, SCHED_ROWS)
+    MOE_ATTR(128, false, DUAL_NONE, EPI_SWIGLU_BWD, SCHED_ROWS)
+    MOE_ATTR(256, false, DUAL_K, EPI_STORE, SCHED_ROWS)
+    MOE_ATTR(128, false, DUAL_K, EPI_STORE, SCHED_ROWS)
+    MOE_ATTR(256, true, DUAL_NONE, EPI_WGRAD, SCHED_WGRAD)
+    MOE_ATTR(128, true, DUAL_NONE, EPI_WGRAD, SCHED_WGRAD)
+    MOE_ATTR(256, true, DUAL_N, EPI_WGRAD, SCHED_WGRAD)
+#undef MOE_ATTR
     return e;
 }
 
@@ -512,23 +633,23 @@ cudaError_t launch_gemm_tc_bf16(const GemmDesc& d, int max_m_tiles, int num_sms,
     if (d.sched == SCHED_ROWS) {
         switch (d.epi) {
         case EPI_SWIGLU_FWD:
-            return run<256, true, DUAL_N, EPI_SWIGLU_FWD, SCHED_ROWS>(d, max_m_tiles, num_sms, s);
+            return run_any<256, true, DUAL_N, EPI_SWIGLU_FWD, SCHED_ROWS>(d, max_m_tiles, num_sms, s);
         case EPI_STORE:
             if (d.dual == DUAL_K)
-                return n256 ? run<256, false, DUAL_K, EPI_STORE, SCHED_ROWS>(d, max_m_tiles, num_sms, s)
-                            : run<128, false, DUAL_K, EPI_STORE, SCHED_ROWS>(d, max_m_tiles, num_sms, s);
-            return n256 ? run<256, true, DUAL_NONE, EPI_STORE, SCHED_ROWS>(d, max_m_tiles, num_sms, s)
-                        : run<128, true, DUAL_NONE, EPI_STORE, SCHED_ROWS>(d, max_m_tiles, num_sms, s);
+                return n256 ? run_any<256, false, DUAL_K, EPI_STORE, SCHED_ROWS>(d, max_m_tiles, num_sms, s)
+                            : run_any<128, false, DUAL_K, EPI_STORE, SCHED_ROWS>(d, max_m_tiles, num_sms, s);
+            return n256 ? run_any<256, true, DUAL_NONE, EPI_STORE, SCHED_ROWS>(d, max_m_tiles, num_sms, s)
+                        : run_any<128, true, DUAL_NONE, EPI_STORE, SCHED_ROWS>(d, max_m_tiles, num_sms, s);
         case EPI_SWIGLU_BWD:
-            return n256 ? run<256, false, DUAL_NONE, EPI_SWIGLU_BWD, SCHED_ROWS>(d, max_m_tiles, num_sms, s)
-                        : run<128, false, DUAL_NONE, EPI_SWIGLU_BWD, SCHED_ROWS>(d, max_m_tiles, num_sms, s);
+            return n256 ? run_any<256, false, DUAL_NONE, EPI_SWIGLU_BWD, SCHED_ROWS>(d, max_m_tiles, num_sms, s)
+                        : run_any<128, false, DUAL_NONE, EPI_SWIGLU_BWD, SCHED_ROWS>(d, max_m_tiles, num_sms, s);
         default:
             return cudaErrorInvalidValue;
         }
     }
-    if (d.dual == DUAL_N) return run<256, true, DUAL_N, EPI_WGRAD, SCHED_WGRAD>(d, max_m_tiles, num_sms, s);
-    return n256 ? run<256, true, DUAL_NONE, EPI_WGRAD, SCHED_WGRAD>(d, max_m_tiles, num_sms, s)
-                : run<128, true, DUAL_NONE, EPI_WGRAD, SCHED_WGRAD>(d, max_m_tiles, num_sms, s);
+    if (d.dual == DUAL_N) return run_any<256, true, DUAL_N, EPI_WGRAD, SCHED_WGRAD>(d, max_m_tiles, num_sms, s);
+    return n256 ? run_any<256, true, DUAL_NONE, EPI_WGRAD, SCHED_WGRAD>(d, max_m_tiles, num_sms, s)
+                : run_any<128, true, DUAL_NONE, EPI_WGRAD, SCHED_WGRAD>(d, max_m_tiles, num_sms, s);
 }
 
 }  // namespace moe

@@ -59,7 +59,10 @@ struct GemmDesc {
     int dense_rows; // > 0: a single dense group of rows [0, dense_rows)
     // row tables (routed groups)
     const int* tile_tab;  // expert of each 128-row tile
-    const int* meta;      // meta[0] = number of 128-row tiles, meta[1] = padded rows
+    const int* meta;      // meta[0] = number of 128-row tiles, meta[1] = padded rows,
+                          // meta[2] = number of tile pairs
+    const int* pair_tab;  // first tile of each pair of one expert's tiles (or null)
+    int prefer_pair;      // routed rows per expert are large enough for CTA pairs
     const int* poff;      // E+1 padded segment offsets
     const int* counts;    // E token counts
     // operands (element pointers; the tensor-core path builds TMA maps from them)
@@ -87,7 +90,8 @@ cudaError_t launch_router(const T* x, const float* Wr, const float* b, int T_, i
                           int score, int* topk, float* gates, float* selsc, int* hist,
                           cudaStream_t s);
 cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff, int* blkbase,
-                        int* tile_tab, int* meta, int* slot_of, cudaStream_t s);
+                        int* tile_tab, int* meta, int* slot_of, cudaStream_t s,
+                        int* pair_tab = nullptr);
 cudaError_t launch_index(const int* topk, const int* blkbase, int T_, int E, int k, int* row_of,
                          int* slot_of, cudaStream_t s);
 template <typename T>

@@ -245,7 +245,7 @@ router_warp_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const 
 __global__ void __launch_bounds__(kMaxE)
 scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ counts,
             int* __restrict__ poff, int* __restrict__ blkbase, int* __restrict__ tile_tab,
-            int* __restrict__ meta, int* __restrict__ slot_of)
+            int* __restrict__ meta, int* __restrict__ slot_of, int* __restrict__ pair_tab)
 {
     __shared__ int sc[kMaxE];
     const int e = threadIdx.x;
@@ -274,11 +274,27 @@ scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ cou
         for (int i = 0; i < pc / kTileM; ++i) tile_tab[start / kTileM + i] = e;
         for (int r = start + c; r < start + pc; ++r) slot_of[r] = -1;
     }
+    const int total = sc[kMaxE - 1];
     if (e == 0) {
-        const int total = sc[kMaxE - 1];
         poff[E] = total;
         meta[0] = total / kTileM;
         meta[1] = total;
+    }
+    if (pair_tab) {
+        // pairs of consecutive tiles of one expert (the last one may be alone)
+        const int np = (e < E) ? (pc / kTileM + 1) / 2 : 0;
+        __syncthreads();
+        sc[e] = np;
+        __syncthreads();
+        for (int off = 1; off < kMaxE; off <<= 1) {
+            int v = (e >= off) ? sc[e - off] : 0;
+            __syncthreads();
+            sc[e] += v;
+            __syncthreads();
+        }
+        const int pstart = sc[e] - np;
+        for (int i = 0; i < np; ++i) pair_tab[pstart + i] = start / kTileM + 2 * i;
+        if (e == 0) meta[2] = sc[kMaxE - 1];
     }
 }
 
@@ -336,9 +352,10 @@ template cudaError_t launch_router<__nv_bfloat16>(const __nv_bfloat16*, const fl
                                                   int*, cudaStream_t);
 
 cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff, int* blkbase,
-                        int* tile_tab, int* meta, int* slot_of, cudaStream_t s)
+                        int* tile_tab, int* meta, int* slot_of, cudaStream_t s, int* pair_tab)
 {
-    scan_kernel<<<1, kMaxE, 0, s>>>(hist, nblk, E, counts, poff, blkbase, tile_tab, meta, slot_of);
+    scan_kernel<<<1, kMaxE, 0, s>>>(hist, nblk, E, counts, poff, blkbase, tile_tab, meta, slot_of,
+                                    pair_tab);
     return cudaGetLastError();
 }
 

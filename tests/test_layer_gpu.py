@@ -23,6 +23,7 @@ CASES = {
     "single_expert_top1": mi.scaled(W["mixtral_8x7b"], T=150, H=128, E=1, k=1, F=256),
     "k_equals_E": mi.scaled(W["mixtral_8x7b"], T=100, H=128, E=4, k=4, F=128),
     "softmax_bias_k3": mi.scaled(W["qwen3_235b"], T=400, H=256, E=12, k=3, F=256),
+    "rows_in_cta_pairs": mi.scaled(W["mixtral_8x7b"], T=1100, H=256, E=4, k=2, F=256),
     "qwen_e128_tiled_router": mi.scaled(W["qwen3_235b"], T=700, H=256, E=128, F=128),
     "deepseek_e256_sigmoid_shared": mi.scaled(W["deepseek_v3"], T=512, H=256, E=256, F=128, Fs=128),
 }
