@@ -171,34 +171,53 @@ gate_grad_kernel(const T* __restrict__ dY, const T* __restrict__ Yp, const int* 
 }
 
 // dWr[h][e] = sum over expert e's rows r of Xp[r][h] dz[slot(r)]. Block
-// (64 columns h, expert e): 4 row phases of 64 threads each sum every 4th row
-// of the segment, then the phases are added in fixed order.
+// (64 columns h, expert e), 256 threads = 32 row phases x 8 column groups of
+// 8 columns (one 16-byte vector each). The segment is walked in chunks of 256
+// rows whose dz values are first gathered into shared memory; each phase sums
+// every 32nd row of a chunk, and the 32 phases are added in fixed order.
 template <typename T>
 __global__ void __launch_bounds__(256)
 router_wgrad_kernel(const T* __restrict__ Xp, const int* __restrict__ slot_of,
                     const int* __restrict__ poff, const int* __restrict__ counts,
                     const float* __restrict__ dz, int H, int E, float* __restrict__ dWr)
 {
-    __shared__ float part[4][64];
+    constexpr int V = 16 / sizeof(T);            // columns per vector
+    constexpr int CG = 64 / V;                   // column groups per block
+    constexpr int PH = 256 / CG;                 // row phases
+    __shared__ float part[PH][64 + 1];
+    __shared__ float dzs[256];
     const int e = blockIdx.y;
-    const int hh = threadIdx.x & 63, ph = threadIdx.x >> 6;
-    const int h = blockIdx.x * 64 + hh;
+    const int cg = threadIdx.x % CG, ph = threadIdx.x / CG;
+    const int h0 = blockIdx.x * 64 + cg * V;
     const int r0 = poff[e], n = counts[e];
-    float acc = 0.f;
-    if (h < H) {
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    for (int c0 = 0; c0 < n; c0 += 256) {
+        __syncthreads();
+        if (c0 + (int)threadIdx.x < n) dzs[threadIdx.x] = dz[slot_of[r0 + c0 + threadIdx.x]];
+        __syncthreads();
+        const int m = min(256, n - c0);
+        if (h0 < H) {
 #pragma unroll 4
-        for (int i = ph; i < n; i += 4) {
-            const int r = r0 + i;
-            float xv;
-            if constexpr (sizeof(T) == 4) xv = Xp[(size_t)r * H + h];
-            else xv = __bfloat162float(Xp[(size_t)r * H + h]);
-            acc = fmaf(xv, __ldg(dz + slot_of[r]), acc);
+            for (int i = ph; i < m; i += PH) {
+                const float d = dzs[i];
+                float xv[V];
+                Vec<T>::load(Xp + (size_t)(r0 + c0 + i) * H + h0, xv);
+#pragma unroll
+                for (int j = 0; j < V; ++j) acc[j] = fmaf(xv[j], d, acc[j]);
+            }
         }
     }
-    part[ph][hh] = acc;
+#pragma unroll
+    for (int j = 0; j < V; ++j) part[ph][cg * V + j] = acc[j];
     __syncthreads();
-    if (ph == 0 && h < H)
-        dWr[(size_t)h * E + e] = ((part[0][hh] + part[1][hh]) + part[2][hh]) + part[3][hh];
+    if (threadIdx.x < 64) {
+        const int h = blockIdx.x * 64 + threadIdx.x;
+        float v = 0.f;
+        for (int p2 = 0; p2 < PH; ++p2) v += part[p2][threadIdx.x];
+        if (h < H) dWr[(size_t)h * E + e] = v;
+    }
 }
 
 __global__ void transpose_kernel(const float* __restrict__ in, int rows, int cols, float* __restrict__ out)

@@ -6,7 +6,7 @@
 // §5 ("Selective precision"): the router runs in FP32.
 //
 // Kernels:
-//   router_warp_kernel (E <= 32) and router_kernel (tiled, larger E): logits z = x Wr + b (fp32 FMA, fixed summation order),
+//   router_small_kernel (E <= 32) and router_kernel (tiled, larger E): logits z = x Wr + b (fp32 FMA, fixed summation order),
 //                  warp-shuffle top-k on z (score order equals logit order for
 //                  both softmax and sigmoid; equal values go to the lower
 //                  expert index), renormalised gates, and a per-block expert
@@ -135,88 +135,71 @@ router_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float
     }
 }
 
-// Router for E <= 32: one warp per TPW tokens. Each lane sums the logits of
-// all experts over its share of H (16-byte x vectors, Wr rows from L1/L2),
-// the partial sums are combined by a fixed butterfly, and lane e then holds
-// logit e for the warp top-k. Blocks cover kRouterTokens tokens, so the
-// per-block histogram layout is the same as router_kernel's.
-template <typename T, int EMAX, int TPW>
-__global__ void __launch_bounds__(32 * (kRouterTokens / TPW))
-router_warp_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float* __restrict__ b,
-                   int T_, int H, int E, int k, int score, int* __restrict__ topk,
-                   float* __restrict__ gates, float* __restrict__ selsc, int* __restrict__ hist)
+// Router for E <= 32. A block routes kRouterTokens tokens: lane l of every
+// warp owns token l, warp w sums the logits of all experts over the w-th
+// eighth of H (16-byte x loads; each Wr row is read once per warp as a
+// broadcast), then one thread per token adds the eight partial sums in warp
+// order, selects the top k (largest logit, lower expert index on equality)
+// and writes the gates.
+template <typename T, int EMAX>
+__global__ void __launch_bounds__(256)
+router_small_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float* __restrict__ b,
+                    int T_, int H, int E, int k, int score, int* __restrict__ topk,
+                    float* __restrict__ gates, float* __restrict__ selsc, int* __restrict__ hist)
 {
-    constexpr int V = 16 / sizeof(T);          // x elements per 16-byte vector
+    constexpr int V = 16 / sizeof(T);
+    constexpr int NW = 8;
+    __shared__ float part[NW][kRouterTokens][EMAX + 1];
     __shared__ int sel_s[kRouterTokens][kMaxK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t0 = blockIdx.x * kRouterTokens + warp * TPW;
-    float acc[TPW][EMAX];
+    const int t = blockIdx.x * kRouterTokens + lane;
+    float acc[EMAX];
 #pragma unroll
-    for (int q = 0; q < TPW; ++q)
+    for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
+    const int hs = H / NW;                       // H is a multiple of 128
+    const int h_lo = warp * hs, h_hi = h_lo + hs;
+    if (t < T_) {
+        for (int h0 = h_lo; h0 < h_hi; h0 += V) {
+            const uint4 u = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h0);
+            const T* p = reinterpret_cast<const T*>(&u);
 #pragma unroll
-        for (int e = 0; e < EMAX; ++e) acc[q][e] = 0.f;
-
-    for (int h0 = lane * V; h0 < H; h0 += 32 * V) {
-        float xv[TPW][V];
+            for (int i = 0; i < V; ++i) {
+                const float xv = to_f32(p[i]);
+                const float* wrow = Wr + (size_t)(h0 + i) * E;
 #pragma unroll
-        for (int q = 0; q < TPW; ++q) {
-            const int t = t0 + q;
-            if (t < T_) {
-                const uint4 u = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h0);
-                const T* p = reinterpret_cast<const T*>(&u);
-#pragma unroll
-                for (int i = 0; i < V; ++i) xv[q][i] = to_f32(p[i]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < V; ++i) xv[q][i] = 0.f;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < V; ++i) {
-            const float* wrow = Wr + (size_t)(h0 + i) * E;
-#pragma unroll
-            for (int e = 0; e < EMAX; ++e) {
-                const float wv = (e < E) ? __ldg(wrow + e) : 0.f;
-#pragma unroll
-                for (int q = 0; q < TPW; ++q) acc[q][e] = fmaf(xv[q][i], wv, acc[q][e]);
+                for (int e = 0; e < EMAX; ++e)
+                    if (e < E) acc[e] = fmaf(xv, __ldg(wrow + e), acc[e]);
             }
         }
     }
 #pragma unroll
-    for (int q = 0; q < TPW; ++q)
+    for (int e = 0; e < EMAX; ++e) part[warp][lane][e] = acc[e];
+    __syncthreads();
+    if (threadIdx.x < kRouterTokens) {
+        const int tt = threadIdx.x;
+        const int tok = blockIdx.x * kRouterTokens + tt;
+        if (tok < T_) {
+            float z[EMAX];
 #pragma unroll
-        for (int e = 0; e < EMAX; ++e)
+            for (int e = 0; e < EMAX; ++e) {
+                float v = 0.f;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                acc[q][e] += __shfl_xor_sync(0xffffffffu, acc[q][e], off);
-
-#pragma unroll
-    for (int q = 0; q < TPW; ++q) {
-        const int t = t0 + q;
-        if (t >= T_) continue;                       // warp-uniform
-        float z = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < EMAX; ++e)
-            if (e == lane && e < E) z = acc[q][e] + (b ? b[e] : 0.f);
-        bool taken = false;
-        int sel_e[kMaxK];
-        float sel_z[kMaxK];
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
-            if (j >= k) break;
-            float bv = (lane < E && !taken) ? z : -INFINITY;
-            int bi = (lane < E && !taken) ? lane : 0x7fffffff;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+                for (int w = 0; w < NW; ++w) v += part[w][tt][e];
+                z[e] = (e < E) ? v + (b ? b[e] : 0.f) : -INFINITY;
             }
-            sel_e[j] = bi;
-            sel_z[j] = bv;
-            if (bi == lane) taken = true;
-        }
-        if (lane == 0) {
+            unsigned taken = 0;
+            int sel_e[kMaxK];
+            float sel_z[kMaxK];
+            for (int j = 0; j < k; ++j) {
+                float bv = -INFINITY;
+                int bi = 0x7fffffff;
+#pragma unroll
+                for (int e = 0; e < EMAX; ++e)
+                    if (e < E && !((taken >> e) & 1u) && better(z[e], e, bv, bi)) { bv = z[e]; bi = e; }
+                taken |= 1u << bi;
+                sel_e[j] = bi;
+                sel_z[j] = bv;
+            }
             float sc[kMaxK], den = 0.f;
             for (int j = 0; j < k; ++j) {
                 sc[j] = (score == MOE_SCORE_SOFTMAX) ? expf(sel_z[j] - sel_z[0])
@@ -224,10 +207,10 @@ router_warp_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const 
                 den += sc[j];
             }
             for (int j = 0; j < k; ++j) {
-                topk[(size_t)t * k + j] = sel_e[j];
-                gates[(size_t)t * k + j] = sc[j] / den;
-                selsc[(size_t)t * k + j] = sc[j];
-                sel_s[warp * TPW + q][j] = sel_e[j];
+                topk[(size_t)tok * k + j] = sel_e[j];
+                gates[(size_t)tok * k + j] = sc[j] / den;
+                selsc[(size_t)tok * k + j] = sc[j];
+                sel_s[tt][j] = sel_e[j];
             }
         }
     }
@@ -329,14 +312,11 @@ cudaError_t launch_router(const T* x, const float* Wr, const float* b, int T_, i
 {
     const int nblk = (T_ + kRouterTokens - 1) / kRouterTokens;
     if (E <= 8)
-        router_warp_kernel<T, 8, 4><<<nblk, 32 * (kRouterTokens / 4), 0, s>>>(
-            x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+        router_small_kernel<T, 8><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
     else if (E <= 16)
-        router_warp_kernel<T, 16, 4><<<nblk, 32 * (kRouterTokens / 4), 0, s>>>(
-            x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+        router_small_kernel<T, 16><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
     else if (E <= 32)
-        router_warp_kernel<T, 32, 2><<<nblk, 32 * (kRouterTokens / 2), 0, s>>>(
-            x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+        router_small_kernel<T, 32><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
     else if (E <= 64)
         router_kernel<T, 2><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
     else if (E <= 128)
