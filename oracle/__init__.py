@@ -237,3 +237,73 @@ def dw_entries(x, dY, W: ExpertWeights, topk, gates, entries):
     if rc:
         raise ValueError("oracle_dw_entries: bad arguments or missing expert weights")
     return out
+
+
+# ------------------------------------------------------------ blockwise FP8
+def e4m3_decode(codes):
+    """fp64 values of E4M3 codes (OCP format definition)."""
+    lib = _load()
+    lib.oracle_e4m3_decode.restype = ctypes.c_double
+    lib.oracle_e4m3_decode.argtypes = [ctypes.c_ubyte]
+    return np.array([lib.oracle_e4m3_decode(int(c)) for c in np.asarray(codes).ravel()]).reshape(np.shape(codes))
+
+
+def e4m3_encode(values):
+    """E4M3 codes of fp32 values (round to nearest even, saturating)."""
+    lib = _load()
+    lib.oracle_e4m3_encode.restype = ctypes.c_ubyte
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    v = np.asarray(values, np.float32)
+    return np.array([lib.oracle_e4m3_encode(float(f)) for f in v.ravel()], np.uint8).reshape(v.shape)
+
+
+FP8_ROWS, FP8_TILES, FP8_COLS = 0, 1, 2
+
+
+def fp8_quantize(X, mode):
+    """(codes, scales) of an fp32 matrix: mode FP8_ROWS (1x128 along rows),
+    FP8_TILES (128x128), FP8_COLS (per column over 128-row blocks)."""
+    lib = _load()
+    X = np.ascontiguousarray(X, np.float32)
+    M, K = X.shape
+    codes = np.empty((M, K), np.uint8)
+    if mode == FP8_ROWS:
+        scales = np.empty((M, K // 128), np.float32)
+    elif mode == FP8_TILES:
+        scales = np.empty(((M + 127) // 128, (K + 127) // 128), np.float32)
+    else:
+        scales = np.empty(((M + 127) // 128, K), np.float32)
+    rc = lib.oracle_fp8_quantize(M, K, mode, X.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                 codes.ctypes.data_as(ctypes.c_void_p),
+                                 scales.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    if rc:
+        raise ValueError("oracle_fp8_quantize: bad arguments")
+    return codes, scales
+
+
+def layer_fp8(x, Wr, Wg, Wu, Wd, topk, gates, scores, score, dY=None, Wsg=None, Wsu=None,
+              Wsd=None):
+    """Blockwise-FP8 layer: y, and when dY is given every gradient."""
+    lib = _load()
+    x, Wr, Wg, Wu, Wd = _f64(x), _f64(Wr), _f64(Wg), _f64(Wu), _f64(Wd)
+    Wsg, Wsu, Wsd = _f64(Wsg), _f64(Wsu), _f64(Wsd)
+    topk, gates, scores, dY = _i32(topk), _f64(gates), _f64(scores), _f64(dY)
+    T, H = x.shape
+    E, _, F = Wg.shape
+    k = topk.shape[1]
+    Fs = 0 if Wsg is None else Wsg.shape[1]
+    out = dict(y=np.empty((T, H)))
+    if dY is not None:
+        out.update(dX=np.empty((T, H)), dWr=np.empty((H, E)), dWg=np.empty((E, H, F)),
+                   dWu=np.empty((E, H, F)), dWd=np.empty((E, F, H)), dg=np.empty((T, k)))
+        if Fs:
+            out.update(dWsg=np.empty((H, Fs)), dWsu=np.empty((H, Fs)), dWsd=np.empty((Fs, H)))
+    rc = lib.oracle_layer_fp8(T, H, E, k, F, Fs, score, _d(x), _d(Wr), _d(Wg), _d(Wu), _d(Wd),
+                              _d(Wsg), _d(Wsu), _d(Wsd), _i(topk), _d(gates), _d(scores), _d(dY),
+                              _d(out["y"]), _d(out.get("dX")), _d(out.get("dWr")),
+                              _d(out.get("dWg")), _d(out.get("dWu")), _d(out.get("dWd")),
+                              _d(out.get("dWsg")), _d(out.get("dWsu")), _d(out.get("dWsd")),
+                              _d(out.get("dg")))
+    if rc:
+        raise ValueError("oracle_layer_fp8: bad arguments")
+    return out

@@ -598,3 +598,394 @@ int oracle_dw_entries(int T, int H, int E, int k, int F, int Fs, int wtype,
     }
     return bad ? -1 : 0;
 }
+
+/* ====================================================================== */
+/* Blockwise FP8 (E4M3) variant.                                           */
+/*                                                                         */
+/* "Scalable Training of Mixture-of-Experts Models with Megatron Core", §5 */
+/* (Platform-specific recipes): blockwise FP8 scales 1x128 activation and  */
+/* gradient tiles and 128x128 weight blocks; §5 (Selective precision)      */
+/* keeps the router in higher precision.                                   */
+/*                                                                         */
+/* Readings (the pages give no formula):                                   */
+/*   - E4M3 is the OCP FP8 format: 1 sign, 4 exponent (bias 7), 3 mantissa */
+/*     bits, subnormals, no infinities, S.1111.111 = NaN, largest finite   */
+/*     magnitude 448. Encoding rounds to nearest, ties to even, and        */
+/*     saturates to +-448.                                                 */
+/*   - block scale s = amax / 448 computed in fp32 (s = 1 when amax = 0);  */
+/*     a value v is stored as q = E4M3(fp32(v / s)) and read as q * s.     */
+/*   - in every GEMM C = A B (contraction over K), A -- whose rows are the */
+/*     output rows -- is quantised in 1x128 blocks along K, and B in       */
+/*     128x128 blocks. So activations and gradients feeding fprop/dgrad    */
+/*     are 1x128 along their feature dimension, weights 128x128, and the   */
+/*     weight-gradient GEMMs (K = the expert's tokens) quantise the left   */
+/*     operand (Xp^T, h^T) per feature column over 128-token blocks and    */
+/*     the right one (dA, dU, dYp) in 128x128 (tokens x features) blocks,  */
+/*     token blocks counted from the start of each expert's segment.       */
+/*   - the router, gates and gate gradients stay in full precision; the    */
+/*     expert outputs (a, u, h, y) are not rounded.                        */
+/* ====================================================================== */
+
+double oracle_e4m3_decode(unsigned char c)
+{
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = (e == 0) ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* Nearest E4M3 code to f (ties to the even code), saturating to +-448. */
+unsigned char oracle_e4m3_encode(float f)
+{
+    if (f != f) return 0x7F;
+    unsigned char sign = (f < 0.0f || (f == 0.0f && signbit(f))) ? 0x80 : 0x00;
+    double a = fabs((double)f);
+    if (a >= 448.0) return sign | 0x7E;
+    /* codes 0..126 are the finite non-negative values in increasing order */
+    int lo = 0, hi = 126;
+    while (lo < hi) {                      /* largest code with value <= a */
+        int mid = (lo + hi + 1) / 2;
+        if (oracle_e4m3_decode((unsigned char)mid) <= a) lo = mid; else hi = mid - 1;
+    }
+    int c = lo;
+    if (c < 126) {
+        double d0 = a - oracle_e4m3_decode((unsigned char)c);
+        double d1 = oracle_e4m3_decode((unsigned char)(c + 1)) - a;
+        if (d1 < d0 || (d1 == d0 && (c & 1))) c = c + 1;
+    }
+    return sign | (unsigned char)c;
+}
+
+/* fp32 scale of a block with largest magnitude amax */
+static float block_scale(float amax) { return amax == 0.0f ? 1.0f : amax / 448.0f; }
+
+/*
+ * Quantise-dequantise the n values v[i*stride] (one block): returns the
+ * values q*s in place (fp64) and optionally the codes and the scale.
+ */
+static void qdq_block(double* v, int n, long stride, unsigned char* codes, float* scale)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float f = fabsf((float)v[(long)i * stride]);
+        if (f > amax) amax = f;
+    }
+    float s = block_scale(amax);
+    for (int i = 0; i < n; ++i) {
+        float f = (float)v[(long)i * stride];
+        unsigned char q = oracle_e4m3_encode(f / s);
+        if (codes) codes[(long)i * stride] = q;
+        v[(long)i * stride] = oracle_e4m3_decode(q) * (double)s;
+    }
+    if (scale) *scale = s;
+}
+
+/* 1x128 blocks along the rows of an M x K matrix (K a multiple of 128). */
+static void qdq_rows(int M, int K, double* X)
+{
+    for (int m = 0; m < M; ++m)
+        for (int k0 = 0; k0 < K; k0 += 128) qdq_block(X + (long)m * K + k0, 128, 1, NULL, NULL);
+}
+
+/* Per column, blocks of 128 consecutive rows (the last block may be short). */
+static void qdq_cols(int M, int N, double* X)
+{
+    for (int n = 0; n < N; ++n)
+        for (int m0 = 0; m0 < M; m0 += 128) {
+            int len = M - m0 < 128 ? M - m0 : 128;
+            qdq_block(X + (long)m0 * N + n, len, N, NULL, NULL);
+        }
+}
+
+/* 128x128 blocks of an R x C matrix (edge blocks may be smaller). */
+static void qdq_tiles(int R, int C, double* X)
+{
+    for (int r0 = 0; r0 < R; r0 += 128)
+        for (int c0 = 0; c0 < C; c0 += 128) {
+            int rl = R - r0 < 128 ? R - r0 : 128, cl = C - c0 < 128 ? C - c0 : 128;
+            float amax = 0.0f;
+            for (int r = 0; r < rl; ++r)
+                for (int c = 0; c < cl; ++c) {
+                    float f = fabsf((float)X[(long)(r0 + r) * C + c0 + c]);
+                    if (f > amax) amax = f;
+                }
+            float s = block_scale(amax);
+            for (int r = 0; r < rl; ++r)
+                for (int c = 0; c < cl; ++c) {
+                    double* p = &X[(long)(r0 + r) * C + c0 + c];
+                    *p = oracle_e4m3_decode(oracle_e4m3_encode((float)*p / s)) * (double)s;
+                }
+        }
+}
+
+/* Quantised bytes and scales of one matrix, for comparison with a GPU quantiser.
+ * mode 0: 1x128 along rows (scales M x K/128); 1: 128x128 tiles (scales
+ * ceil(M/128) x ceil(K/128)); 2: per column over 128-row blocks (scales
+ * ceil(M/128) x K). Input in fp32. */
+int oracle_fp8_quantize(int M, int K, int mode, const float* X, unsigned char* codes, float* scales)
+{
+    if (M <= 0 || K <= 0 || mode < 0 || mode > 2) return -1;
+    double* v = (double*)malloc(sizeof(double) * (size_t)M * K);
+    for (size_t i = 0; i < (size_t)M * K; ++i) v[i] = X[i];
+    if (mode == 0) {
+        if (K % 128) { free(v); return -1; }
+        for (int m = 0; m < M; ++m)
+            for (int k0 = 0; k0 < K; k0 += 128)
+                qdq_block(v + (long)m * K + k0, 128, 1, codes + (long)m * K + k0, scales + (long)m * (K / 128) + k0 / 128);
+    } else if (mode == 1) {
+        int nc = (K + 127) / 128;
+        for (int r0 = 0; r0 < M; r0 += 128)
+            for (int c0 = 0; c0 < K; c0 += 128) {
+                int rl = M - r0 < 128 ? M - r0 : 128, cl = K - c0 < 128 ? K - c0 : 128;
+                float amax = 0.0f;
+                for (int r = 0; r < rl; ++r)
+                    for (int c = 0; c < cl; ++c) {
+                        float f = fabsf(X[(long)(r0 + r) * K + c0 + c]);
+                        if (f > amax) amax = f;
+                    }
+                float s = block_scale(amax);
+                scales[(r0 / 128) * nc + c0 / 128] = s;
+                for (int r = 0; r < rl; ++r)
+                    for (int c = 0; c < cl; ++c)
+                        codes[(long)(r0 + r) * K + c0 + c] = oracle_e4m3_encode(X[(long)(r0 + r) * K + c0 + c] / s);
+            }
+    } else {
+        for (int n = 0; n < K; ++n)
+            for (int m0 = 0; m0 < M; m0 += 128) {
+                int len = M - m0 < 128 ? M - m0 : 128;
+                qdq_block(v + (long)m0 * K + n, len, K, codes + (long)m0 * K + n, scales + (long)(m0 / 128) * K + n);
+            }
+    }
+    free(v);
+    return 0;
+}
+
+static double* dup(const double* p, size_t n)
+{
+    double* q = (double*)malloc(sizeof(double) * (n ? n : 1));
+    memcpy(q, p, sizeof(double) * n);
+    return q;
+}
+
+/* C (M x N) = A (M x K) B (K x N), plain fp64. */
+static void gemm(int M, int N, int K, const double* A, const double* B, double* C)
+{
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k) acc += A[(long)m * K + k] * B[(long)k * N + n];
+            C[(long)m * N + n] = acc;
+        }
+}
+
+/* C (M x N) = A^T B with A (K x M), B (K x N). */
+static void gemm_tn(int M, int N, int K, const double* A, const double* B, double* C)
+{
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k) acc += A[(long)k * M + m] * B[(long)k * N + n];
+            C[(long)m * N + n] = acc;
+        }
+}
+
+/* C (M x N) = A B^T with A (M x K), B (N x K). */
+static void gemm_nt(int M, int N, int K, const double* A, const double* B, double* C)
+{
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k) acc += A[(long)m * K + k] * B[(long)n * K + k];
+            C[(long)m * N + n] = acc;
+        }
+}
+
+/*
+ * One expert (or the shared expert) in FP8, forward and -- when dYr is not
+ * NULL -- backward, for its M rows X (M x H) in dispatch order. Wg, Wu: H x F;
+ * Wd: F x H (unquantised). Y receives the output rows; the gradients are
+ * written when dYr != NULL (dYr are the rows' output gradients, already
+ * gate-scaled).
+ */
+static void swiglu_fp8(int M, int H, int F, const double* X, const double* Wg, const double* Wu,
+                       const double* Wd, double* Y, const double* dYr, double* dX, double* dWg,
+                       double* dWu, double* dWd)
+{
+    size_t mf = (size_t)(M > 0 ? M : 1) * F, mh = (size_t)(M > 0 ? M : 1) * H;
+    double* Xq = dup(X, (size_t)M * H);
+    qdq_rows(M, H, Xq);
+    double* Wgq = dup(Wg, (size_t)H * F);
+    double* Wuq = dup(Wu, (size_t)H * F);
+    double* Wdq = dup(Wd, (size_t)F * H);
+    qdq_tiles(H, F, Wgq);
+    qdq_tiles(H, F, Wuq);
+    qdq_tiles(F, H, Wdq);
+    double* A = (double*)malloc(sizeof(double) * mf);
+    double* U = (double*)malloc(sizeof(double) * mf);
+    double* Hh = (double*)malloc(sizeof(double) * mf);
+    gemm(M, F, H, Xq, Wgq, A);
+    gemm(M, F, H, Xq, Wuq, U);
+    for (size_t i = 0; i < (size_t)M * F; ++i) Hh[i] = silu(A[i]) * U[i];
+    double* Hq = dup(Hh, (size_t)M * F);
+    qdq_rows(M, F, Hq);
+    gemm(M, H, F, Hq, Wdq, Y);
+    free(Hq);
+    if (dYr) {
+        /* fc2 dgrad: dh = q(dYr) Wd_q^T (Wd's 128x128 blocks, used transposed) */
+        double* dYq = dup(dYr, (size_t)M * H);
+        qdq_rows(M, H, dYq);
+        double* dh = (double*)malloc(sizeof(double) * mf);
+        gemm_nt(M, F, H, dYq, Wdq, dh);
+        double* dA = (double*)malloc(sizeof(double) * mf);
+        double* dU = (double*)malloc(sizeof(double) * mf);
+        for (size_t i = 0; i < (size_t)M * F; ++i) {
+            dA[i] = dh[i] * U[i] * dsilu(A[i]);
+            dU[i] = dh[i] * silu(A[i]);
+        }
+        /* fc2 wgrad: dWd = q_col(h)^T q_tile(dYr) */
+        double* Hc = dup(Hh, (size_t)M * F);
+        qdq_cols(M, F, Hc);
+        double* dYt = dup(dYr, (size_t)M * H);
+        qdq_tiles(M, H, dYt);
+        gemm_tn(F, H, M, Hc, dYt, dWd);
+        /* fc1 dgrad: dX = q(dA) Wg_q^T + q(dU) Wu_q^T */
+        double* dAq = dup(dA, mf);
+        double* dUq = dup(dU, mf);
+        qdq_rows(M, F, dAq);
+        qdq_rows(M, F, dUq);
+        double* t1 = (double*)malloc(sizeof(double) * mh);
+        gemm_nt(M, H, F, dAq, Wgq, dX);
+        gemm_nt(M, H, F, dUq, Wuq, t1);
+        for (size_t i = 0; i < (size_t)M * H; ++i) dX[i] += t1[i];
+        /* fc1 wgrad: dWg = q_col(X)^T q_tile(dA), dWu = q_col(X)^T q_tile(dU) */
+        double* Xc = dup(X, (size_t)M * H);
+        qdq_cols(M, H, Xc);
+        double* dAt = dup(dA, mf);
+        double* dUt = dup(dU, mf);
+        qdq_tiles(M, F, dAt);
+        qdq_tiles(M, F, dUt);
+        gemm_tn(H, F, M, Xc, dAt, dWg);
+        gemm_tn(H, F, M, Xc, dUt, dWu);
+        free(dYq); free(dh); free(dA); free(dU); free(Hc); free(dYt); free(dAq); free(dUq);
+        free(t1); free(Xc); free(dAt); free(dUt);
+    }
+    free(Xq); free(Wgq); free(Wuq); free(Wdq); free(A); free(U); free(Hh);
+}
+
+/*
+ * FP8 layer: same stages and outputs as oracle_forward / oracle_backward,
+ * with every expert GEMM operand quantised as described above. dY may be
+ * NULL (forward only); then only y (and dg, Yp if requested) are written.
+ */
+int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
+                     const double* x, const double* Wr,
+                     const double* Wg, const double* Wu, const double* Wd,
+                     const double* Wsg, const double* Wsu, const double* Wsd,
+                     const int* topk, const double* gates, const double* scores,
+                     const double* dY, double* y,
+                     double* dX, double* dWr, double* dWg, double* dWu, double* dWd,
+                     double* dWsg, double* dWsu, double* dWsd, double* dg_out)
+{
+    if (T <= 0 || H <= 0 || H % 128 || E <= 0 || k <= 0 || k > E || k > 1024 || F <= 0 ||
+        F % 128 || Fs < 0 || Fs % 128)
+        return -1;
+    const int R = T * k;
+    int* counts = (int*)malloc(sizeof(int) * E);
+    int* offsets = (int*)malloc(sizeof(int) * (E + 1));
+    int* row_of = (int*)malloc(sizeof(int) * R);
+    int* slot_of = (int*)malloc(sizeof(int) * R);
+    if (oracle_dispatch(T, E, k, topk, counts, offsets, row_of, slot_of)) return -1;
+    double* Xp = (double*)malloc(sizeof(double) * (size_t)R * H);
+    double* Yp = (double*)malloc(sizeof(double) * (size_t)R * H);
+    double* dYp = (double*)malloc(sizeof(double) * (size_t)R * H);
+    double* dXp = (double*)malloc(sizeof(double) * (size_t)R * H);
+    double* dg = (double*)malloc(sizeof(double) * (size_t)R);
+    for (int r = 0; r < R; ++r)
+        memcpy(Xp + (size_t)r * H, x + (size_t)(slot_of[r] / k) * H, sizeof(double) * H);
+    /* forward of every expert (Yp), then the gate-scaled output gradients */
+    for (int e = 0; e < E; ++e) {
+        int M = counts[e];
+        if (M == 0) continue;
+        swiglu_fp8(M, H, F, Xp + (size_t)offsets[e] * H, Wg + (size_t)e * H * F,
+                   Wu + (size_t)e * H * F, Wd + (size_t)e * F * H, Yp + (size_t)offsets[e] * H,
+                   NULL, NULL, NULL, NULL, NULL);
+    }
+    for (int t = 0; t < T; ++t)
+        for (int h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j)
+                acc += gates[(size_t)t * k + j] * Yp[(size_t)row_of[(size_t)t * k + j] * H + h];
+            y[(size_t)t * H + h] = acc;
+        }
+    double* Ys = NULL;
+    if (Fs > 0) {
+        Ys = (double*)malloc(sizeof(double) * (size_t)T * H);
+        swiglu_fp8(T, H, Fs, x, Wsg, Wsu, Wsd, Ys, NULL, NULL, NULL, NULL, NULL);
+        for (size_t i = 0; i < (size_t)T * H; ++i) y[i] += Ys[i];
+    }
+    if (dY) {
+        for (int r = 0; r < R; ++r) {
+            int t = slot_of[r] / k;
+            double g = gates[slot_of[r]], acc = 0.0;
+            for (int h = 0; h < H; ++h) {
+                acc += dY[(size_t)t * H + h] * Yp[(size_t)r * H + h];
+                dYp[(size_t)r * H + h] = g * dY[(size_t)t * H + h];
+            }
+            dg[slot_of[r]] = acc;
+        }
+        double* Ytmp = (double*)malloc(sizeof(double) * (size_t)(R > T ? R : T) * H);
+        for (int e = 0; e < E; ++e) {
+            int M = counts[e];
+            double* dWg_e = dWg + (size_t)e * H * F;
+            double* dWu_e = dWu + (size_t)e * H * F;
+            double* dWd_e = dWd + (size_t)e * F * H;
+            if (M == 0) {
+                memset(dWg_e, 0, sizeof(double) * (size_t)H * F);
+                memset(dWu_e, 0, sizeof(double) * (size_t)H * F);
+                memset(dWd_e, 0, sizeof(double) * (size_t)F * H);
+                continue;
+            }
+            swiglu_fp8(M, H, F, Xp + (size_t)offsets[e] * H, Wg + (size_t)e * H * F,
+                       Wu + (size_t)e * H * F, Wd + (size_t)e * F * H, Ytmp,
+                       dYp + (size_t)offsets[e] * H, dXp + (size_t)offsets[e] * H, dWg_e, dWu_e,
+                       dWd_e);
+        }
+        double* dz = (double*)calloc((size_t)T * E, sizeof(double));
+        for (int t = 0; t < T; ++t) {
+            double dzs[1024];
+            router_dz(k, score_fn, topk + (size_t)t * k, gates + (size_t)t * k,
+                      scores + (size_t)t * E, dg + (size_t)t * k, dzs);
+            for (int j = 0; j < k; ++j) dz[(size_t)t * E + topk[(size_t)t * k + j]] = dzs[j];
+        }
+#pragma omp parallel for schedule(static)
+        for (int h = 0; h < H; ++h)
+            for (int e = 0; e < E; ++e) {
+                double acc = 0.0;
+                for (int t = 0; t < T; ++t) acc += x[(size_t)t * H + h] * dz[(size_t)t * E + e];
+                dWr[(size_t)h * E + e] = acc;
+            }
+#pragma omp parallel for schedule(static)
+        for (int t = 0; t < T; ++t)
+            for (int h = 0; h < H; ++h) {
+                double acc = 0.0;
+                for (int j = 0; j < k; ++j) acc += dXp[(size_t)row_of[(size_t)t * k + j] * H + h];
+                for (int e = 0; e < E; ++e) acc += dz[(size_t)t * E + e] * Wr[(size_t)h * E + e];
+                dX[(size_t)t * H + h] = acc;
+            }
+        if (Fs > 0) {
+            double* dXs = (double*)malloc(sizeof(double) * (size_t)T * H);
+            swiglu_fp8(T, H, Fs, x, Wsg, Wsu, Wsd, Ytmp, dY, dXs, dWsg, dWsu, dWsd);
+            for (size_t i = 0; i < (size_t)T * H; ++i) dX[i] += dXs[i];
+            free(dXs);
+        }
+        free(Ytmp);
+        free(dz);
+        if (dg_out) memcpy(dg_out, dg, sizeof(double) * (size_t)R);
+    }
+    free(Ys); free(Xp); free(Yp); free(dYp); free(dXp); free(dg);
+    free(counts); free(offsets); free(row_of); free(slot_of);
+    return 0;
+}

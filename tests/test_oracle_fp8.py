@@ -1,0 +1,166 @@
+"""Pins of the oracle's blockwise-FP8 (E4M3) pieces (CPU only).
+
+E4M3 is pinned to PyTorch's float8_e4m3fn conversion (an independent
+implementation of the same OCP format) on every code and on random, tie and
+out-of-range values; the block quantiser to its exactness and locality
+properties; the FP8 layer to the exact layer within the E4M3 error scale
+("Scalable Training of Mixture-of-Experts Models with Megatron Core", §5,
+blockwise FP8: 1x128 activation/gradient tiles, 128x128 weight blocks).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def test_e4m3_decode_all_codes_match_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan) and nan.sum() == 2        # 0x7F, 0xFF
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9 and ours[0x08] == 2.0 ** -6
+
+
+def test_e4m3_encode_matches_torch_and_saturates():
+    rng = np.random.default_rng(0)
+    vals = np.concatenate([rng.standard_normal(20000) * 10 ** rng.uniform(-4, 2.5, 20000),
+                           rng.uniform(-448, 448, 5000)]).astype(np.float32)
+    grid = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))           # 0 .. 448
+    mids = ((grid[:-1] + grid[1:]) / 2).astype(np.float32)               # exact ties
+    vals = np.concatenate([vals, mids, -mids, grid.astype(np.float32)])
+    vals = vals[np.abs(vals) <= 448.0]          # torch's cast gives NaN beyond the range
+    ours = oracle.e4m3_encode(vals)
+    ref = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+    big = np.array([448.0, 449.0, 480.0, 1e4, 1e30, -500.0], np.float32)
+    assert list(oracle.e4m3_encode(big)) == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE]
+
+
+@pytest.mark.parametrize("mode", [oracle.FP8_ROWS, oracle.FP8_TILES, oracle.FP8_COLS])
+def test_block_quantiser_exactness_and_locality(mode):
+    rng = np.random.default_rng(1)
+    X = (rng.standard_normal((300, 256)) * 3).astype(np.float32)
+    codes, scales = oracle.fp8_quantize(X, mode)
+    dq = oracle.e4m3_decode(codes)
+    if mode == oracle.FP8_ROWS:
+        s = np.repeat(scales, 128, axis=1)
+        amax = np.abs(X).reshape(300, 2, 128).max(2)
+    elif mode == oracle.FP8_TILES:
+        s = np.repeat(np.repeat(scales, 128, 0), 128, 1)[:300, :256]
+        amax = np.array([[np.abs(X[r:r + 128, c:c + 128]).max() for c in range(0, 256, 128)]
+                         for r in range(0, 300, 128)])
+    else:
+        s = np.repeat(scales, 128, 0)[:300]
+        amax = np.array([np.abs(X[r:r + 128]).max(0) for r in range(0, 300, 128)])
+    np.testing.assert_array_equal(scales, (amax / np.float32(448)).astype(np.float32))
+    deq = dq * s
+    # every value within half an E4M3 step of itself (relative 2^-4, or 2^-10 * s near 0)
+    err = np.abs(deq - X)
+    assert np.all(err <= np.maximum(np.abs(X) * 2.0 ** -4, s * 2.0 ** -10) * (1 + 1e-6))
+    assert np.sum(np.abs(dq) == 448.0) >= scales.size        # each block's amax maps to 448
+    # locality: changing one element moves only its own block
+    X2 = X.copy()
+    X2[5, 7] *= 50
+    c2, s2 = oracle.fp8_quantize(X2, mode)
+    changed = np.argwhere(c2 != codes)
+    if mode == oracle.FP8_ROWS:
+        assert np.all(changed[:, 0] == 5) and np.all(changed[:, 1] < 128)
+    elif mode == oracle.FP8_TILES:
+        assert np.all(changed[:, 0] < 128) and np.all(changed[:, 1] < 128)
+    else:
+        assert np.all(changed[:, 1] == 7) and np.all(changed[:, 0] < 128)
+    # exactness: representable values with a power-of-two block maximum round-trip
+    Y = (oracle.e4m3_decode(rng.integers(0, 0x7E, (128, 128)).astype(np.uint8)) * 2.0 ** -3)
+    Y[0, 0] = 448.0 * 2.0 ** -3
+    cy, sy = oracle.fp8_quantize(Y.astype(np.float32), oracle.FP8_TILES)
+    assert sy[0, 0] == 2.0 ** -3
+    assert np.array_equal(oracle.e4m3_decode(cy) * 2.0 ** -3, Y)
+
+
+def _layer(T, H, E, k, F, Fs, score, seed):
+    rng = np.random.default_rng(seed)
+    p = dict(x=rng.standard_normal((T, H)), Wr=rng.standard_normal((H, E)) * 0.1,
+             Wg=rng.standard_normal((E, H, F)) * H ** -0.5, Wu=rng.standard_normal((E, H, F)) * H ** -0.5,
+             Wd=rng.standard_normal((E, F, H)) * F ** -0.5, dY=rng.standard_normal((T, H)))
+    if Fs:
+        p.update(Wsg=rng.standard_normal((H, Fs)) * H ** -0.5, Wsu=rng.standard_normal((H, Fs)) * H ** -0.5,
+                 Wsd=rng.standard_normal((Fs, H)) * Fs ** -0.5)
+    else:
+        p.update(Wsg=None, Wsu=None, Wsd=None)
+    return p
+
+
+@pytest.mark.parametrize("score,Fs", [(oracle.SOFTMAX, 0), (oracle.SIGMOID, 128)])
+def test_fp8_layer_tracks_the_exact_layer(score, Fs):
+    p = _layer(T=150, H=256, E=4, k=2, F=256, Fs=Fs, score=score, seed=3)
+    r = oracle.route(p["x"], p["Wr"], None, 2, score)
+    q = oracle.layer_fp8(p["x"], p["Wr"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"],
+                         r["scores"], score, p["dY"], p["Wsg"], p["Wsu"], p["Wsd"])
+    y = oracle.forward(p["x"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"], p["Wsg"], p["Wsu"], p["Wsd"])
+    g = oracle.backward(p["x"], p["Wr"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"], r["scores"],
+                        p["dY"], score, p["Wsg"], p["Wsu"], p["Wsd"])
+    g["y"] = y
+    # each E4M3 rounding perturbs a value by at most 2^-4 relative (2^-4/sqrt(3)
+    # = 3.6% rms); an output depends on up to ~6 successive roundings, so its
+    # deviation from the exact layer is sqrt(6) x 3.6% = 9% rms at most
+    for n in q:
+        if n == "dg":
+            continue
+        rel = np.linalg.norm(q[n] - g[n]) / np.linalg.norm(g[n])
+        assert 0.005 < rel < 0.09, (n, rel)
+
+
+# ---- an independent FP8 SwiGLU for one expert, codec = torch's float8_e4m3fn
+def _cast(v, s):
+    f = np.clip((v.astype(np.float32) / np.float32(s)).astype(np.float32), -448, 448)
+    return torch.from_numpy(np.ascontiguousarray(f)).to(torch.float8_e4m3fn).double().numpy() * float(s)
+
+
+def _q_rows(X):
+    out = np.empty_like(X)
+    for r in range(X.shape[0]):
+        for c in range(0, X.shape[1], 128):
+            v = X[r, c:c + 128]
+            a = np.float32(np.abs(v.astype(np.float32)).max())
+            out[r, c:c + 128] = _cast(v, np.float32(a / np.float32(448)) if a else np.float32(1))
+    return out
+
+
+def _q_cols(X):
+    return _q_rows(X.T).T if X.shape[0] % 128 == 0 else None
+
+
+def _q_tiles(X):
+    out = np.empty_like(X)
+    for r in range(0, X.shape[0], 128):
+        for c in range(0, X.shape[1], 128):
+            v = X[r:r + 128, c:c + 128]
+            a = np.float32(np.abs(v.astype(np.float32)).max())
+            out[r:r + 128, c:c + 128] = _cast(v, np.float32(a / np.float32(448)) if a else np.float32(1))
+    return out
+
+
+def test_fp8_single_expert_matches_independent_fp8_swiglu():
+    T, H, F = 256, 256, 384
+    p = _layer(T=T, H=H, E=1, k=1, F=F, Fs=0, score=oracle.SOFTMAX, seed=7)
+    r = oracle.route(p["x"], p["Wr"], None, 1, oracle.SOFTMAX)
+    q = oracle.layer_fp8(p["x"], p["Wr"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"],
+                         r["scores"], oracle.SOFTMAX, p["dY"])
+    x, dY = p["x"], p["dY"]
+    Wg, Wu, Wd = _q_tiles(p["Wg"][0]), _q_tiles(p["Wu"][0]), _q_tiles(p["Wd"][0])
+    xq = _q_rows(x)
+    a, u = xq @ Wg, xq @ Wu
+    sg = 1 / (1 + np.exp(-a))
+    h = a * sg * u
+    y = _q_rows(h) @ Wd
+    dh = _q_rows(dY) @ Wd.T
+    dA = dh * u * sg * (1 + a * (1 - sg))
+    dU = dh * a * sg
+    ref = dict(y=y, dWd=(_q_cols(h).T @ _q_tiles(dY))[None],
+               dX=_q_rows(dA) @ Wg.T + _q_rows(dU) @ Wu.T,
+               dWg=(_q_cols(x).T @ _q_tiles(dA))[None], dWu=(_q_cols(x).T @ _q_tiles(dU))[None])
+    for n, v in ref.items():
+        np.testing.assert_allclose(q[n], v, rtol=1e-9, atol=1e-9 * np.abs(v).max(), err_msg=n)
