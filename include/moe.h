@@ -63,7 +63,12 @@ typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
 /* Storage and arithmetic type of activations and expert weights.
  *   MOE_FP32: fp32 storage, fp32 FMA arithmetic throughout.
  *   MOE_BF16: bf16 storage, tensor-core GEMMs with fp32 accumulation.
- *   MOE_FP8_BLOCK: blockwise-scaled E4M3 (not available in this build). */
+ *   MOE_FP8_BLOCK: bf16 activations, weights and gradients; every expert
+ *     GEMM runs on E4M3 operands with fp32 block scales (1x128 blocks along
+ *     K for the operand indexing output rows, 128x128 for the other), fp32
+ *     accumulation ("Scalable Training of Mixture-of-Experts Models with
+ *     Megatron Core", §5, blockwise FP8). The router stays fp32. Layers with
+ *     a shared expert are not supported in this mode (MOE_ERR_UNSUPPORTED). */
 typedef enum { MOE_FP32 = 0, MOE_BF16 = 1, MOE_FP8_BLOCK = 2 } moe_dtype_t;
 
 typedef struct {
@@ -208,6 +213,26 @@ moe_status_t moe_stage_times(moe_plan_t plan, moe_stage_time_t* out, int capacit
 moe_status_t moe_route_static(moe_plan_t plan, int T, const void* x, const float* Wr,
                               const float* b, int32_t* topk_idx, float* gates, int32_t* counts,
                               int32_t* offsets, int32_t* row_of, moe_stream_t stream);
+
+/* Blockwise E4M3 quantiser used by the MOE_FP8_BLOCK layer, on a row-major
+ * rows x cols bf16 device matrix (both multiples of 128). Scale of a block =
+ * amax / 448 in fp32 (1 for an all-zero block); codes are E4M3 of
+ * value / scale, rounded to nearest even and saturated ("Scalable Training of
+ * Mixture-of-Experts Models with Megatron Core", §5, blockwise FP8).
+ *   MOE_Q_ROWS:    1x128 blocks along rows: codes rows x cols,
+ *                  scales rows x cols/128.
+ *   MOE_Q_TILES:   128x128 blocks: codes rows x cols and the transposed
+ *                  codes_t cols x rows; scales (rows/128) x (cols/128) and
+ *                  scales_t (cols/128) x (rows/128).
+ *   MOE_Q_COLS_T:  per column over 128-row blocks, transposed output:
+ *                  codes_t cols x rows, scales_t cols x rows/128.
+ *   MOE_Q_TILES_T: 128x128 blocks, transposed output: codes_t cols x rows,
+ *                  scales_t (cols/128) x (rows/128).
+ * Unused outputs may be NULL. Enqueued on `stream`.
+ * Errors: INVALID_ARG, MISALIGNED, CUDA. */
+enum { MOE_Q_ROWS = 0, MOE_Q_TILES = 1, MOE_Q_COLS_T = 2, MOE_Q_TILES_T = 3 };
+moe_status_t moe_fp8_quantize(int rows, int cols, int mode, const void* in, uint8_t* codes,
+                              float* scales, uint8_t* codes_t, float* scales_t, moe_stream_t stream);
 
 /* MOE_ABI_VERSION of the loaded library. */
 int moe_abi_version(void);

@@ -33,7 +33,8 @@ MOE_FLAG_STAGE_TIMING = 1
 # Names the library exports (include/moe.h).
 EXPORTS = ("moe_plan_create", "moe_plan_destroy", "moe_workspace_size", "moe_forward",
            "moe_backward", "moe_read_status", "moe_status_string", "moe_stage_times",
-           "moe_route_static", "moe_abi_version")
+           "moe_route_static", "moe_fp8_quantize", "moe_abi_version")
+MOE_Q_ROWS, MOE_Q_TILES, MOE_Q_COLS_T, MOE_Q_TILES_T = 0, 1, 2, 3
 
 
 class moe_config_t(ctypes.Structure):
@@ -91,6 +92,8 @@ def load_library() -> ctypes.CDLL:
         lib.moe_status_string.restype = ctypes.c_char_p
         lib.moe_stage_times.argtypes = [_vp, P(moe_stage_time_t), ctypes.c_int, P(ctypes.c_int)]
         lib.moe_route_static.argtypes = [_vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        lib.moe_fp8_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                         _vp, _vp]
         lib.moe_abi_version.argtypes = []
         for n in EXPORTS:
             if n not in ("moe_status_string", "moe_abi_version"):
@@ -157,6 +160,13 @@ def moe_stage_times(plan: int):
     if st != MOE_OK:
         raise MoEError(st, "moe_stage_times")
     return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(min(n.value, cap))}
+
+
+def moe_fp8_quantize(rows: int, cols: int, mode: int, x: int, codes: int, scales: int, codes_t: int,
+                     scales_t: int, stream: int) -> None:
+    st = load_library().moe_fp8_quantize(rows, cols, mode, x, codes, scales, codes_t, scales_t, stream)
+    if st != MOE_OK:
+        raise MoEError(st, "moe_fp8_quantize")
 
 
 # ------------------------------------------------- torch-allocated wrapper

@@ -25,12 +25,16 @@ struct Layout {
     size_t Xp, A, U, Hh, Yp, As, Us, Hs, saved_bytes;
     // workspace
     size_t status, hist, blkbase, Ys, dYp, dA, dU, dXp, dz, WrT, dAs, dUs, dXs, ws_bytes;
+    // blockwise FP8 (saved: permuted activations and weights; ws: the rest)
+    size_t Xq, sX, WgQ, sWg, WuQ, sWu, WgQT, sWgT, WuQT, sWuT, WdQ, sWd, WdQT, sWdT;
+    size_t hq, sh, dYq, sdY, dAq, sdA, dUq, sdU, hTq, shT, dYpTq, sdYpT, XpTq, sXpT, dATq, sdAT,
+        dUTq, sdUT;
 };
 
 Layout make_layout(const moe_config_t& c, int T)
 {
     Layout L;
-    const size_t es = (c.dtype == MOE_FP32) ? 4 : 2;
+    const size_t es = (c.dtype == MOE_FP32) ? 4 : 2;   // activations (bf16 for FP8 too)
     L.T = T;
     L.R = T * c.top_k;
     const int nonempty = L.R < c.E ? L.R : c.E;
@@ -57,6 +61,17 @@ Layout make_layout(const moe_config_t& c, int T)
     L.As = take(es * (size_t)T * c.Fs);
     L.Us = take(es * (size_t)T * c.Fs);
     L.Hs = take(es * (size_t)T * c.Fs);
+    const bool q8 = c.dtype == MOE_FP8_BLOCK;
+    const size_t Rp = L.Rp_max, HF = (size_t)c.H * c.F, EHF = (size_t)c.E * HF;
+    const size_t sHF = (size_t)(c.H / 128) * (c.F / 128) * c.E;
+    L.Xq = take(q8 ? Rp * c.H : 0);
+    L.sX = take(q8 ? 4 * Rp * (c.H / 128) : 0);
+    L.WgQ = take(q8 ? EHF : 0);   L.sWg = take(q8 ? 4 * sHF : 0);
+    L.WuQ = take(q8 ? EHF : 0);   L.sWu = take(q8 ? 4 * sHF : 0);
+    L.WgQT = take(q8 ? EHF : 0);  L.sWgT = take(q8 ? 4 * sHF : 0);
+    L.WuQT = take(q8 ? EHF : 0);  L.sWuT = take(q8 ? 4 * sHF : 0);
+    L.WdQ = take(q8 ? EHF : 0);   L.sWd = take(q8 ? 4 * sHF : 0);
+    L.WdQT = take(q8 ? EHF : 0);  L.sWdT = take(q8 ? 4 * sHF : 0);
     L.saved_bytes = o;
     o = 0;
     L.status = take(256);
@@ -72,6 +87,15 @@ Layout make_layout(const moe_config_t& c, int T)
     L.dAs = take(es * (size_t)T * c.Fs);
     L.dUs = take(es * (size_t)T * c.Fs);
     L.dXs = take(c.Fs ? es * (size_t)T * c.H : 0);
+    L.hq = take(q8 ? Rp * c.F : 0);       L.sh = take(q8 ? 4 * Rp * (c.F / 128) : 0);
+    L.dYq = take(q8 ? Rp * c.H : 0);      L.sdY = take(q8 ? 4 * Rp * (c.H / 128) : 0);
+    L.dAq = take(q8 ? Rp * c.F : 0);      L.sdA = take(q8 ? 4 * Rp * (c.F / 128) : 0);
+    L.dUq = take(q8 ? Rp * c.F : 0);      L.sdU = take(q8 ? 4 * Rp * (c.F / 128) : 0);
+    L.hTq = take(q8 ? Rp * c.F : 0);      L.shT = take(q8 ? 4 * (Rp / 128) * c.F : 0);
+    L.dYpTq = take(q8 ? Rp * c.H : 0);    L.sdYpT = take(q8 ? 4 * (Rp / 128) * (c.H / 128) : 0);
+    L.XpTq = take(q8 ? Rp * c.H : 0);     L.sXpT = take(q8 ? 4 * (Rp / 128) * c.H : 0);
+    L.dATq = take(q8 ? Rp * c.F : 0);     L.sdAT = take(q8 ? 4 * (Rp / 128) * (c.F / 128) : 0);
+    L.dUTq = take(q8 ? Rp * c.F : 0);     L.sdUT = take(q8 ? 4 * (Rp / 128) * (c.F / 128) : 0);
     L.ws_bytes = o;
     return L;
 }
@@ -88,7 +112,7 @@ moe_status_t check_config(const moe_config_t* c)
     if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
     if (c->dtype != MOE_FP32 && c->dtype != MOE_BF16 && c->dtype != MOE_FP8_BLOCK)
         return MOE_ERR_INVALID_ARG;
-    if (c->dtype == MOE_FP8_BLOCK) return MOE_ERR_UNSUPPORTED;
+    if (c->dtype == MOE_FP8_BLOCK && c->Fs > 0) return MOE_ERR_UNSUPPORTED;
     // int32 row indices: R_pad * max(H, F) elements must stay addressable per
     // buffer with 32-bit row numbers
     const long long R = (long long)c->T_max * c->top_k + (long long)c->E * kTileM;
@@ -119,13 +143,14 @@ enum Stage : int {
     ST_ROUTER, ST_SCAN, ST_INDEX, ST_PERMUTE, ST_FC1, ST_FC2, ST_FC1S, ST_FC2S, ST_COMBINE,
     ST_GATEGRAD, ST_FC2_DGRAD, ST_FC2_WGRAD, ST_FC1_DGRAD, ST_FC1_WGRAD, ST_FC2S_DGRAD,
     ST_FC2S_WGRAD, ST_FC1S_DGRAD, ST_FC1S_WGRAD, ST_ROUTER_WGRAD, ST_TRANSPOSE, ST_UNPERMUTE,
-    ST_COUNT
+    ST_WQUANT, ST_QROWS, ST_QT, ST_COUNT
 };
 const char* const kStageNames[ST_COUNT] = {
     "router", "scan", "index", "permute", "fc1_swiglu", "fc2", "shared_fc1_swiglu", "shared_fc2",
     "combine", "gate_grad", "fc2_dgrad_swiglu", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad",
     "shared_fc2_dgrad", "shared_fc2_wgrad", "shared_fc1_dgrad", "shared_fc1_wgrad",
-    "router_wgrad", "wr_transpose", "unpermute_reduce"};
+    "router_wgrad", "wr_transpose", "unpermute_reduce", "fp8_weight_quant", "fp8_quant_rows",
+    "fp8_quant_t"};
 struct StageRec {
     int stage;
     cudaEvent_t start, stop;
@@ -178,6 +203,7 @@ moe_status_t moe_plan_create(const moe_config_t* cfg, int device, moe_plan_t* ou
         DeviceGuard g(device);
         if (!g.ok) return MOE_ERR_CUDA;
         if (cfg->dtype == MOE_BF16 && gemm_tc_prepare(device) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cfg->dtype == MOE_FP8_BLOCK && gemm_fp8_prepare(device) != cudaSuccess) return MOE_ERR_CUDA;
     }
     moe_plan_s* p = new (std::nothrow) moe_plan_s;
     if (!p) return MOE_ERR_CUDA;
@@ -308,6 +334,7 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
 
     auto gemm = [&](const GemmDesc& d) -> cudaError_t {
         if (c.dtype == MOE_FP32) return launch_gemm_simt_f32(d, L.MT_max, s);
+        if (c.dtype == MOE_FP8_BLOCK) return launch_gemm_fp8(d, L.MT_max, p->num_sms, s);
         return launch_gemm_tc_bf16(d, L.MT_max, p->num_sms, s);
     };
     GemmDesc d;
@@ -395,6 +422,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
 
     auto gemm = [&](const GemmDesc& d) -> cudaError_t {
         if (c.dtype == MOE_FP32) return launch_gemm_simt_f32(d, L.MT_max, s);
+        if (c.dtype == MOE_FP8_BLOCK) return launch_gemm_fp8(d, L.MT_max, p->num_sms, s);
         return launch_gemm_tc_bf16(d, L.MT_max, p->num_sms, s);
     };
 
@@ -491,6 +519,174 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     return MOE_OK;
 }
 
+// ---------------------------------------------------------- blockwise FP8
+// Same stages as the bf16 layer; the expert GEMMs take E4M3 operands with
+// fp32 block scales (A: 1x128 along K, B: 128x128), all K-major, produced by
+// the quantisers in quant.cu; intermediates and outputs stay bf16.
+static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, uint8_t* sv,
+                                     uint8_t* ws, cudaStream_t s)
+{
+    using T = __nv_bfloat16;
+    const moe_config_t& c = p->cfg;
+    const Layout L = make_layout(c, T_);
+    const int H = c.H, E = c.E, k = c.top_k, F = c.F, Rp = L.Rp_max;
+    DeviceStatus* status = reinterpret_cast<DeviceStatus*>(ws + L.status);
+    int* topk = reinterpret_cast<int*>(sv + L.topk);
+    float* gates = reinterpret_cast<float*>(sv + L.gates);
+    float* selsc = reinterpret_cast<float*>(sv + L.selsc);
+    int* counts = reinterpret_cast<int*>(sv + L.counts);
+    int* poff = reinterpret_cast<int*>(sv + L.poff);
+    int* meta = reinterpret_cast<int*>(sv + L.meta);
+    int* tiletab = reinterpret_cast<int*>(sv + L.tiletab);
+    int* pairtab = reinterpret_cast<int*>(sv + L.pairtab);
+    int* rowof = reinterpret_cast<int*>(sv + L.rowof);
+    int* slotof = reinterpret_cast<int*>(sv + L.slotof);
+    T* Xp = reinterpret_cast<T*>(sv + L.Xp);
+    T* A = reinterpret_cast<T*>(sv + L.A);
+    T* U = reinterpret_cast<T*>(sv + L.U);
+    T* Hh = reinterpret_cast<T*>(sv + L.Hh);
+    T* Yp = reinterpret_cast<T*>(sv + L.Yp);
+    auto u8 = [&](uint8_t* base, size_t off) { return base + off; };
+    auto f32 = [&](uint8_t* base, size_t off) { return reinterpret_cast<float*>(base + off); };
+    const T* x = static_cast<const T*>(a->x);
+
+    MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
+    MOE_STAGE(ST_ROUTER, launch_router<T>(x, a->Wr, a->b, T_, H, E, k, c.score, topk, gates, selsc,
+                                          reinterpret_cast<int*>(ws + L.hist), s));
+    MOE_STAGE(ST_SCAN, launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
+                                   reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab));
+    MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
+    MOE_STAGE(ST_PERMUTE, launch_permute_quant(x, rowof, poff, counts, T_, H, E, k, Xp, u8(sv, L.Xq),
+                                               f32(sv, L.sX), s));
+    MOE_STAGE(ST_WQUANT, launch_quant_w(static_cast<const T*>(a->W_gate), E, H, F, u8(sv, L.WgQ),
+                                        f32(sv, L.sWg), u8(sv, L.WgQT), f32(sv, L.sWgT), s));
+    MOE_STAGE(ST_WQUANT, launch_quant_w(static_cast<const T*>(a->W_up), E, H, F, u8(sv, L.WuQ),
+                                        f32(sv, L.sWu), u8(sv, L.WuQT), f32(sv, L.sWuT), s));
+    MOE_STAGE(ST_WQUANT, launch_quant_w(static_cast<const T*>(a->W_down), E, F, H, u8(sv, L.WdQ),
+                                        f32(sv, L.sWd), u8(sv, L.WdQT), f32(sv, L.sWdT), s));
+    GemmDesc d;
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
+    d.N = F; d.K = H; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.A0 = u8(sv, L.Xq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(sv, L.sX); d.lds_a = H / 128;
+    d.B0 = u8(sv, L.WgQT); d.B1 = u8(sv, L.WuQT); d.ldb = H; d.b_rows = E * F;
+    d.SB0 = f32(sv, L.sWgT); d.SB1 = f32(sv, L.sWuT);
+    d.O0 = A; d.O1 = U; d.O2 = Hh; d.ldo = F; d.status = status;
+    MOE_STAGE(ST_FC1, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
+    MOE_STAGE(ST_QROWS, launch_quant_rows(Hh, meta + 1, Rp, F, u8(ws, L.hq), f32(ws, L.sh), s));
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
+    d.N = H; d.K = F; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.A0 = u8(ws, L.hq); d.lda = F; d.a_rows = Rp; d.SA0 = f32(ws, L.sh); d.lds_a = F / 128;
+    d.B0 = u8(sv, L.WdQT); d.ldb = F; d.b_rows = E * H; d.SB0 = f32(sv, L.sWdT);
+    d.O0 = Yp; d.ldo = H; d.status = status;
+    MOE_STAGE(ST_FC2, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
+    MOE_STAGE(ST_COMBINE, launch_combine<T>(Yp, nullptr, rowof, gates, T_, H, k, static_cast<T*>(a->y), s));
+
+    if (a->topk_idx) MOE_CUDA(cudaMemcpyAsync(a->topk_idx, topk, sizeof(int) * L.R, cudaMemcpyDeviceToDevice, s));
+    if (a->gates) MOE_CUDA(cudaMemcpyAsync(a->gates, gates, sizeof(float) * L.R, cudaMemcpyDeviceToDevice, s));
+    if (a->counts) MOE_CUDA(cudaMemcpyAsync(a->counts, counts, sizeof(int) * E, cudaMemcpyDeviceToDevice, s));
+    if (a->offsets) MOE_CUDA(cudaMemcpyAsync(a->offsets, poff, sizeof(int) * (E + 1), cudaMemcpyDeviceToDevice, s));
+    if (a->row_of) MOE_CUDA(cudaMemcpyAsync(a->row_of, rowof, sizeof(int) * L.R, cudaMemcpyDeviceToDevice, s));
+    return MOE_OK;
+}
+
+static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
+                                      const uint8_t* svc, uint8_t* ws, cudaStream_t s)
+{
+    using T = __nv_bfloat16;
+    const moe_config_t& c = p->cfg;
+    const Layout L = make_layout(c, T_);
+    const int H = c.H, E = c.E, k = c.top_k, F = c.F, Rp = L.Rp_max;
+    uint8_t* sv = const_cast<uint8_t*>(svc);   // only read below
+    DeviceStatus* status = reinterpret_cast<DeviceStatus*>(ws + L.status);
+    const int* topk = reinterpret_cast<const int*>(sv + L.topk);
+    const float* gates = reinterpret_cast<const float*>(sv + L.gates);
+    const float* selsc = reinterpret_cast<const float*>(sv + L.selsc);
+    const int* counts = reinterpret_cast<const int*>(sv + L.counts);
+    const int* poff = reinterpret_cast<const int*>(sv + L.poff);
+    const int* meta = reinterpret_cast<const int*>(sv + L.meta);
+    const int* tiletab = reinterpret_cast<const int*>(sv + L.tiletab);
+    const int* rowof = reinterpret_cast<const int*>(sv + L.rowof);
+    const int* slotof = reinterpret_cast<const int*>(sv + L.slotof);
+    const T* Xp = reinterpret_cast<const T*>(sv + L.Xp);
+    const T* A = reinterpret_cast<const T*>(sv + L.A);
+    const T* U = reinterpret_cast<const T*>(sv + L.U);
+    const T* Hh = reinterpret_cast<const T*>(sv + L.Hh);
+    const T* Yp = reinterpret_cast<const T*>(sv + L.Yp);
+    T* dYp = reinterpret_cast<T*>(ws + L.dYp);
+    T* dA = reinterpret_cast<T*>(ws + L.dA);
+    T* dU = reinterpret_cast<T*>(ws + L.dU);
+    T* dXp = reinterpret_cast<T*>(ws + L.dXp);
+    float* dz = reinterpret_cast<float*>(ws + L.dz);
+    float* WrT = reinterpret_cast<float*>(ws + L.WrT);
+    auto u8 = [&](uint8_t* base, size_t off) { return base + off; };
+    auto f32 = [&](uint8_t* base, size_t off) { return reinterpret_cast<float*>(base + off); };
+    const T* dY = static_cast<const T*>(a->dY);
+
+    MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
+    MOE_STAGE(ST_GATEGRAD, launch_gate_grad<T>(dY, Yp, rowof, topk, gates, selsc, poff, counts, T_, H,
+                                               E, k, c.score, dYp, dz, s));
+    // fc2 dgrad + SwiGLU backward
+    MOE_STAGE(ST_QROWS, launch_quant_rows(dYp, meta + 1, Rp, H, u8(ws, L.dYq), f32(ws, L.sdY), s));
+    GemmDesc d;
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_BWD; d.dual = DUAL_NONE;
+    d.N = F; d.K = H; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.A0 = u8(ws, L.dYq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(ws, L.sdY); d.lds_a = H / 128;
+    d.B0 = u8(sv, L.WdQ); d.ldb = H; d.b_rows = E * F; d.SB0 = f32(sv, L.sWd);
+    d.X0 = A; d.X1 = U; d.O0 = dA; d.O1 = dU; d.ldo = F; d.status = status;
+    MOE_STAGE(ST_FC2_DGRAD, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
+    // fc2 wgrad: dWd[e] = h_e^T dYp_e
+    MOE_STAGE(ST_QT, launch_quant_t(Hh, meta + 1, Rp, F, 0, u8(ws, L.hTq), f32(ws, L.shT), s));
+    MOE_STAGE(ST_QT, launch_quant_t(dYp, meta + 1, Rp, H, 1, u8(ws, L.dYpTq), f32(ws, L.sdYpT), s));
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
+    d.N = H; d.M_out = F; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.A0 = u8(ws, L.hTq); d.lda = Rp; d.SA0 = f32(ws, L.shT); d.lds_a = Rp / 128;
+    d.B0 = u8(ws, L.dYpTq); d.ldb = Rp; d.SB0 = f32(ws, L.sdYpT); d.lds_b = Rp / 128;
+    d.rows_cap = Rp;
+    d.O0 = a->dW_down; d.ldo = H; d.o_estride = (long long)F * H; d.status = status;
+    MOE_STAGE(ST_FC2_WGRAD, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
+    // fc1 dgrad: dXp = dA Wg^T + dU Wu^T
+    MOE_STAGE(ST_QROWS, launch_quant_rows(dA, meta + 1, Rp, F, u8(ws, L.dAq), f32(ws, L.sdA), s));
+    MOE_STAGE(ST_QROWS, launch_quant_rows(dU, meta + 1, Rp, F, u8(ws, L.dUq), f32(ws, L.sdU), s));
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
+    d.N = H; d.K = F; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.A0 = u8(ws, L.dAq); d.A1 = u8(ws, L.dUq); d.lda = F; d.a_rows = Rp;
+    d.SA0 = f32(ws, L.sdA); d.SA1 = f32(ws, L.sdU); d.lds_a = F / 128;
+    d.B0 = u8(sv, L.WgQ); d.B1 = u8(sv, L.WuQ); d.ldb = F; d.b_rows = E * H;
+    d.SB0 = f32(sv, L.sWg); d.SB1 = f32(sv, L.sWu);
+    d.O0 = dXp; d.ldo = H; d.status = status;
+    MOE_STAGE(ST_FC1_DGRAD, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
+    // fc1 wgrad: dWg[e] = Xp_e^T dA_e, dWu[e] = Xp_e^T dU_e
+    MOE_STAGE(ST_QT, launch_quant_t(Xp, meta + 1, Rp, H, 0, u8(ws, L.XpTq), f32(ws, L.sXpT), s));
+    MOE_STAGE(ST_QT, launch_quant_t(dA, meta + 1, Rp, F, 1, u8(ws, L.dATq), f32(ws, L.sdAT), s));
+    MOE_STAGE(ST_QT, launch_quant_t(dU, meta + 1, Rp, F, 1, u8(ws, L.dUTq), f32(ws, L.sdUT), s));
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
+    d.N = F; d.M_out = H; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.A0 = u8(ws, L.XpTq); d.lda = Rp; d.SA0 = f32(ws, L.sXpT); d.lds_a = Rp / 128;
+    d.B0 = u8(ws, L.dATq); d.B1 = u8(ws, L.dUTq); d.ldb = Rp;
+    d.SB0 = f32(ws, L.sdAT); d.SB1 = f32(ws, L.sdUT); d.lds_b = Rp / 128;
+    d.rows_cap = Rp;
+    d.O0 = a->dW_gate; d.O1 = a->dW_up; d.ldo = F; d.o_estride = (long long)H * F; d.status = status;
+    MOE_STAGE(ST_FC1_WGRAD, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
+    // router backward and the unpermute-reduce of dX
+    MOE_STAGE(ST_ROUTER_WGRAD, launch_router_wgrad<T>(Xp, slotof, poff, counts, dz, H, E, k, a->dWr, s));
+    MOE_STAGE(ST_TRANSPOSE, launch_transpose_f32(a->Wr, H, E, WrT, s));
+    MOE_STAGE(ST_UNPERMUTE, launch_unpermute_reduce<T>(dXp, nullptr, rowof, topk, dz, WrT, T_, H, k,
+                                                       static_cast<T*>(a->dX), s));
+    return MOE_OK;
+}
+
 static moe_status_t check_call(moe_plan_t plan, int T, const void* saved, size_t saved_bytes,
                                const void* ws, size_t ws_bytes)
 {
@@ -521,6 +717,8 @@ moe_status_t moe_forward(moe_plan_t plan, int T, const moe_fwd_args_t* a, void* 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (plan->cfg.dtype == MOE_FP32)
         return forward_impl<float>(plan, T, a, static_cast<uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
+    if (plan->cfg.dtype == MOE_FP8_BLOCK)
+        return forward_fp8_impl(plan, T, a, static_cast<uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
     return forward_impl<__nv_bfloat16>(plan, T, a, static_cast<uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
 }
 
@@ -547,6 +745,8 @@ moe_status_t moe_backward(moe_plan_t plan, int T, const moe_bwd_args_t* a, const
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (plan->cfg.dtype == MOE_FP32)
         return backward_impl<float>(plan, T, a, static_cast<const uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
+    if (plan->cfg.dtype == MOE_FP8_BLOCK)
+        return backward_fp8_impl(plan, T, a, static_cast<const uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
     return backward_impl<__nv_bfloat16>(plan, T, a, static_cast<const uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
 }
 
@@ -568,4 +768,33 @@ bool moe::plan_info(const moe_plan_s* plan, moe_config_t* cfg, int* device)
     *cfg = plan->cfg;
     *device = plan->device;
     return true;
+}
+
+moe_status_t moe_fp8_quantize(int rows, int cols, int mode, const void* in, uint8_t* codes,
+                              float* scales, uint8_t* codes_t, float* scales_t, moe_stream_t stream)
+{
+    if (rows < 1 || cols < 1 || rows % 128 || cols % 128 || !in) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(in) || (codes && !aligned16(codes)) || (codes_t && !aligned16(codes_t)))
+        return MOE_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(in);
+    cudaError_t e;
+    switch (mode) {
+    case MOE_Q_ROWS:
+        if (!codes || !scales) return MOE_ERR_INVALID_ARG;
+        e = launch_quant_rows(x, nullptr, rows, cols, codes, scales, s);
+        break;
+    case MOE_Q_TILES:
+        if (!codes || !scales || !codes_t || !scales_t) return MOE_ERR_INVALID_ARG;
+        e = launch_quant_w(x, 1, rows, cols, codes, scales, codes_t, scales_t, s);
+        break;
+    case MOE_Q_COLS_T:
+    case MOE_Q_TILES_T:
+        if (!codes_t || !scales_t) return MOE_ERR_INVALID_ARG;
+        e = launch_quant_t(x, nullptr, rows, cols, mode == MOE_Q_TILES_T ? 1 : 0, codes_t, scales_t, s);
+        break;
+    default:
+        return MOE_ERR_INVALID_ARG;
+    }
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -77,12 +77,18 @@ struct GemmDesc {
     long long o_estride;       // WGRAD: elements between experts' outputs
     const void* X0; const void* X1;  // SWIGLU_BWD: saved a, u (ld = ldo)
     DeviceStatus* status;
+    // blockwise FP8 only: fp32 block scales of the E4M3 operands
+    const float* SA0; const float* SA1; int lds_a;   // A: 1x128 blocks along K
+    const float* SB0; const float* SB1; int lds_b;   // B: 128x128 blocks
+    int rows_cap;   // SCHED_WGRAD: row capacity of the transposed operands
 };
 
 // Launchers (return cudaGetLastError()).
 cudaError_t launch_gemm_simt_f32(const GemmDesc& d, int max_m_tiles, cudaStream_t s);
 cudaError_t launch_gemm_tc_bf16(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s);
 cudaError_t gemm_tc_prepare(int device);
+cudaError_t launch_gemm_fp8(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s);
+cudaError_t gemm_fp8_prepare(int device);
 
 // ------------------------------------------------------------- routing etc.
 template <typename T>
@@ -114,6 +120,17 @@ template <typename T>
 cudaError_t launch_unpermute_reduce(const T* dXp, const T* dXs, const int* row_of,
                                     const int* topk, const float* dz, const float* WrT, int T_,
                                     int H, int k, T* dX, cudaStream_t s);
+
+// blockwise FP8 quantisers (quant.cu)
+cudaError_t launch_permute_quant(const __nv_bfloat16* x, const int* row_of, const int* poff,
+                                 const int* counts, int T_, int H, int E, int k, __nv_bfloat16* Xp,
+                                 uint8_t* Xq, float* sX, cudaStream_t s);
+cudaError_t launch_quant_rows(const __nv_bfloat16* in, const int* rows_dev, int rows_max, int C,
+                              uint8_t* q, float* sc, cudaStream_t s);
+cudaError_t launch_quant_t(const __nv_bfloat16* in, const int* rows_dev, int rows_cap, int C,
+                           int tiles, uint8_t* qT, float* sT, cudaStream_t s);
+cudaError_t launch_quant_w(const __nv_bfloat16* W, int E, int R, int C, uint8_t* q, float* sc,
+                           uint8_t* qT, float* sT, cudaStream_t s);
 
 // Configuration and device of a plan; false for a null plan.
 bool plan_info(const moe_plan_s* plan, moe_config_t* cfg, int* device);

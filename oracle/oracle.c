@@ -622,8 +622,12 @@ int oracle_dw_entries(int T, int H, int E, int k, int F, int Fs, int wtype,
 /*     operand (Xp^T, h^T) per feature column over 128-token blocks and    */
 /*     the right one (dA, dU, dYp) in 128x128 (tokens x features) blocks,  */
 /*     token blocks counted from the start of each expert's segment.       */
-/*   - the router, gates and gate gradients stay in full precision; the    */
-/*     expert outputs (a, u, h, y) are not rounded.                        */
+/*   - the router, gates and gate gradients stay in full precision;        */
+/*   - the FP8 workload fixes bf16 outputs and gradients: every GEMM       */
+/*     output (a, u, y, dA, dU), h = silu(a) u (formed from the GEMM       */
+/*     outputs before they are stored) and the gate-scaled output gradient */
+/*     g dY are bf16 values (round to nearest even) when they are stored   */
+/*     and quantised for the next GEMM; dA, dU use the stored a, u.        */
 /* ====================================================================== */
 
 double oracle_e4m3_decode(unsigned char c)
@@ -654,6 +658,20 @@ unsigned char oracle_e4m3_encode(float f)
         if (d1 < d0 || (d1 == d0 && (c & 1))) c = c + 1;
     }
     return sign | (unsigned char)c;
+}
+
+/* v rounded to bfloat16 (via fp32, ties to even) */
+static double bf16r(double v)
+{
+    float f = (float)v;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) != 0x7f800000u) {
+        u += 0x7fffu + ((u >> 16) & 1u);
+        u &= 0xffff0000u;
+        memcpy(&f, &u, sizeof f);
+    }
+    return (double)f;
 }
 
 /* fp32 scale of a block with largest magnitude amax */
@@ -828,10 +846,15 @@ static void swiglu_fp8(int M, int H, int F, const double* X, const double* Wg, c
     double* Hh = (double*)malloc(sizeof(double) * mf);
     gemm(M, F, H, Xq, Wgq, A);
     gemm(M, F, H, Xq, Wuq, U);
-    for (size_t i = 0; i < (size_t)M * F; ++i) Hh[i] = silu(A[i]) * U[i];
+    for (size_t i = 0; i < (size_t)M * F; ++i) {
+        Hh[i] = bf16r(silu(A[i]) * U[i]);   /* from the GEMM outputs themselves */
+        A[i] = bf16r(A[i]);
+        U[i] = bf16r(U[i]);
+    }
     double* Hq = dup(Hh, (size_t)M * F);
     qdq_rows(M, F, Hq);
     gemm(M, H, F, Hq, Wdq, Y);
+    for (size_t i = 0; i < (size_t)M * H; ++i) Y[i] = bf16r(Y[i]);
     free(Hq);
     if (dYr) {
         /* fc2 dgrad: dh = q(dYr) Wd_q^T (Wd's 128x128 blocks, used transposed) */
@@ -842,8 +865,8 @@ static void swiglu_fp8(int M, int H, int F, const double* X, const double* Wg, c
         double* dA = (double*)malloc(sizeof(double) * mf);
         double* dU = (double*)malloc(sizeof(double) * mf);
         for (size_t i = 0; i < (size_t)M * F; ++i) {
-            dA[i] = dh[i] * U[i] * dsilu(A[i]);
-            dU[i] = dh[i] * silu(A[i]);
+            dA[i] = bf16r(dh[i] * U[i] * dsilu(A[i]));
+            dU[i] = bf16r(dh[i] * silu(A[i]));
         }
         /* fc2 wgrad: dWd = q_col(h)^T q_tile(dYr) */
         double* Hc = dup(Hh, (size_t)M * F);
@@ -932,7 +955,7 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
             double g = gates[slot_of[r]], acc = 0.0;
             for (int h = 0; h < H; ++h) {
                 acc += dY[(size_t)t * H + h] * Yp[(size_t)r * H + h];
-                dYp[(size_t)r * H + h] = g * dY[(size_t)t * H + h];
+                dYp[(size_t)r * H + h] = bf16r(g * dY[(size_t)t * H + h]);
             }
             dg[slot_of[r]] = acc;
         }

@@ -21,7 +21,7 @@ def lib():
 def declared_entry_points():
     src = open(os.path.join(ROOT, "include", "moe.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_the_bound_names():
@@ -57,9 +57,9 @@ def test_plan_create_rejects_bad_configs(lib, bad):
     assert plan.value is None
 
 
-def test_fp8_is_reported_unsupported(lib):
+def test_fp8_with_shared_expert_is_reported_unsupported(lib):
     plan = ctypes.c_void_p()
-    assert lib.moe_plan_create(ctypes.byref(_cfg(dtype=2)), 0, ctypes.byref(plan)) == moe.MOE_ERR_UNSUPPORTED
+    assert lib.moe_plan_create(ctypes.byref(_cfg(dtype=2, Fs=256)), 0, ctypes.byref(plan)) == moe.MOE_ERR_UNSUPPORTED
 
 
 def test_null_arguments(lib):

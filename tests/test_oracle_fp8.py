@@ -150,17 +150,25 @@ def test_fp8_single_expert_matches_independent_fp8_swiglu():
     q = oracle.layer_fp8(p["x"], p["Wr"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"],
                          r["scores"], oracle.SOFTMAX, p["dY"])
     x, dY = p["x"], p["dY"]
+    bf = lambda v: torch.from_numpy(np.ascontiguousarray(v)).to(torch.bfloat16).double().numpy()
     Wg, Wu, Wd = _q_tiles(p["Wg"][0]), _q_tiles(p["Wu"][0]), _q_tiles(p["Wd"][0])
     xq = _q_rows(x)
-    a, u = xq @ Wg, xq @ Wu
+    a32, u32 = xq @ Wg, xq @ Wu
+    h = bf(a32 / (1 + np.exp(-a32)) * u32)
+    a, u = bf(a32), bf(u32)
     sg = 1 / (1 + np.exp(-a))
-    h = a * sg * u
-    y = _q_rows(h) @ Wd
+    y = bf(_q_rows(h) @ Wd)
+    dY = bf(dY)                                 # gate 1: the stored output gradient is bf16
     dh = _q_rows(dY) @ Wd.T
-    dA = dh * u * sg * (1 + a * (1 - sg))
-    dU = dh * a * sg
+    dA = bf(dh * u * sg * (1 + a * (1 - sg)))
+    dU = bf(dh * a * sg)
     ref = dict(y=y, dWd=(_q_cols(h).T @ _q_tiles(dY))[None],
                dX=_q_rows(dA) @ Wg.T + _q_rows(dU) @ Wu.T,
                dWg=(_q_cols(x).T @ _q_tiles(dA))[None], dWu=(_q_cols(x).T @ _q_tiles(dU))[None])
     for n, v in ref.items():
-        np.testing.assert_allclose(q[n], v, rtol=1e-9, atol=1e-9 * np.abs(v).max(), err_msg=n)
+        # both sides round the same fp64 values to bf16; an fp64 summation-order
+        # difference can move a value across a bf16 (or E4M3) rounding boundary,
+        # so compare in aggregate and require exact agreement almost everywhere
+        close = np.isclose(q[n], v, rtol=1e-9, atol=1e-9 * np.abs(v).max())
+        assert close.mean() > 0.999, (n, close.mean())
+        assert np.linalg.norm(q[n] - v) / np.linalg.norm(v) < 1e-3, n
