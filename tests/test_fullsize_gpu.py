@@ -122,3 +122,56 @@ def test_full_size_layer(name):
         bound = {"dWg": bg, "dWu": bu, "dWd": bd, "dWsg": bg, "dWsu": bu, "dWsd": bd}[n]
         bnd = bound[0, j] if n in ("dWd", "dWsd") else bound[i, 0]
         assert abs(got - want) <= WGRAD_BOUND_SLACK * bnd, (n, e, i, j, got, want, bnd)
+
+
+def test_full_size_fp8_layer():
+    """Qwen3-shaped layer in blockwise FP8: routing bit-exact, the layer's
+    weight quantiser bit-exact against the oracle on sampled experts, and
+    sampled output rows within the E4M3 deviation scale of the exact layer
+    (an output passes through up to ~6 successive E4M3 roundings of 3.6% rms
+    each: at most 9% relative, as pinned on the oracle's FP8 layer)."""
+    import mixture_experts_layer_sigmoid_gb300 as moe
+    w = mi.WORKLOADS["qwen3_235b_fp8"]
+    g = mi.make_inputs(w, "cuda")
+    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=moe.MOE_FP8_BLOCK)
+    y, rt = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"], routing=True)
+    gr = layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
+    torch.cuda.synchronize()
+    assert layer.status(w.T) == 0
+    assert torch.isfinite(y).all() and torch.isfinite(gr["dX"]).all()
+    x, dY, Wr, b = to_np(g["x"]), to_np(g["dY"]), to_np(g["Wr"]), to_np(g["b"])
+    r = oracle.route(x, Wr, b, w.k, w.score)
+    gt = rt["topk_idx"].cpu().numpy()
+    tie = (r["gap_set"] < TIE_REL) | (r["gap_order"] < TIE_REL)
+    mism = np.any(gt != r["topk"], axis=1)
+    assert not np.any(mism & ~tie)
+    if mism.any():
+        r = oracle.route(x, Wr, b, w.k, w.score, replay_topk=gt, replay_mask=mism)
+    counts = np.bincount(r["topk"].ravel(), minlength=w.E)
+    assert np.array_equal(rt["counts"].cpu().numpy(), counts)
+    hot = int(np.argmax(counts))
+    # the weight quantiser on two experts' full-size blocks
+    for e in (0, hot):
+        W = g["Wg"][e].contiguous()
+        R, C = W.shape
+        codes = torch.empty((R, C), dtype=torch.uint8, device="cuda")
+        codes_t = torch.empty((C, R), dtype=torch.uint8, device="cuda")
+        sc = torch.empty((R // 128, C // 128), device="cuda")
+        sct = torch.empty((C // 128, R // 128), device="cuda")
+        moe.moe_fp8_quantize(R, C, moe.MOE_Q_TILES, W.data_ptr(), codes.data_ptr(), sc.data_ptr(),
+                             codes_t.data_ptr(), sct.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        oc, os_ = oracle.fp8_quantize(W.float().cpu().numpy(), oracle.FP8_TILES)
+        assert np.array_equal(codes.cpu().numpy(), oc) and np.array_equal(sc.cpu().numpy(), os_)
+        assert np.array_equal(codes_t.cpu().numpy(), oc.T)
+    # sampled rows against the exact layer
+    toks = np.array(sorted({0, w.T - 1, int(np.nonzero((r["topk"] == hot).any(1))[0][0]), 777}))
+    need = sorted(set(r["topk"][toks].ravel().tolist()))
+    Wx = oracle.ExpertWeights(w.E, {e: _bits(g["Wg"][e]) for e in need},
+                              {e: _bits(g["Wu"][e]) for e in need},
+                              {e: _bits(g["Wd"][e]) for e in need})
+    tr = oracle.token_rows(x[toks], dY[toks], Wr, Wx, r["topk"][toks], r["gates"][toks],
+                           r["scores"][toks], w.score)
+    for nm, got in (("y", to_np(y)[toks]), ("dX", to_np(gr["dX"])[toks])):
+        rl2, _ = rel_errors(got, tr[nm])
+        assert 0.0 < rl2 < 0.09, (nm, rl2)
