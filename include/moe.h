@@ -234,6 +234,16 @@ enum { MOE_Q_ROWS = 0, MOE_Q_TILES = 1, MOE_Q_COLS_T = 2, MOE_Q_TILES_T = 3 };
 moe_status_t moe_fp8_quantize(int rows, int cols, int mode, const void* in, uint8_t* codes,
                               float* scales, uint8_t* codes_t, float* scales_t, moe_stream_t stream);
 
+/* Failure-detection check. Every pipelined kernel of the library waits on
+ * its shared-memory mbarriers with a bounded wait (2 s); when a wait runs out
+ * the kernel records MOE_ERR_DEVICE_TIMEOUT in the status word and returns,
+ * so a stalled pipeline ends with an error instead of hanging the GPU. This
+ * entry point runs that wait on an mbarrier that is never signalled: after
+ * the call, moe_read_status(plan, ws, stream) returns MOE_ERR_DEVICE_TIMEOUT
+ * and the device stays usable. `ws` is any workspace (its status word is
+ * overwritten). Errors: INVALID_ARG, CUDA. */
+moe_status_t moe_diag_wait_timeout(void* ws, moe_stream_t stream);
+
 /* MOE_ABI_VERSION of the loaded library. */
 int moe_abi_version(void);
 

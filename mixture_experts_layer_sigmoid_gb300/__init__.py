@@ -33,7 +33,7 @@ MOE_FLAG_STAGE_TIMING = 1
 # Names the library exports (include/moe.h).
 EXPORTS = ("moe_plan_create", "moe_plan_destroy", "moe_workspace_size", "moe_forward",
            "moe_backward", "moe_read_status", "moe_status_string", "moe_stage_times",
-           "moe_route_static", "moe_fp8_quantize", "moe_abi_version")
+           "moe_route_static", "moe_fp8_quantize", "moe_diag_wait_timeout", "moe_abi_version")
 MOE_Q_ROWS, MOE_Q_TILES, MOE_Q_COLS_T, MOE_Q_TILES_T = 0, 1, 2, 3
 
 
@@ -94,6 +94,7 @@ def load_library() -> ctypes.CDLL:
         lib.moe_route_static.argtypes = [_vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
         lib.moe_fp8_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp,
                                          _vp, _vp]
+        lib.moe_diag_wait_timeout.argtypes = [_vp, _vp]
         lib.moe_abi_version.argtypes = []
         for n in EXPORTS:
             if n not in ("moe_status_string", "moe_abi_version"):

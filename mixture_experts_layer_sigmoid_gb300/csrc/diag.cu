@@ -1,0 +1,40 @@
+// diag.cu -- moe_diag_wait_timeout: exercises the device-side bounded wait
+// (ptx::wait_bounded) that every pipelined kernel of the library uses, on an
+// mbarrier that nothing ever signals. The wait gives up after its limit and
+// records MOE_ERR_DEVICE_TIMEOUT in the status word, so a test can check
+// that a stalled pipeline ends with an error instead of hanging the GPU.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+__global__ void wait_timeout_kernel(DeviceStatus* status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bar), 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        ptx::wait_bounded(ptx::smem_u32(&bar), 0, &abort_flag, status, 99);
+    __syncthreads();
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+moe_status_t moe_diag_wait_timeout(void* ws, moe_stream_t stream)
+{
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    DeviceStatus* st = static_cast<DeviceStatus*>(ws);
+    if (cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s) != cudaSuccess) return MOE_ERR_CUDA;
+    wait_timeout_kernel<<<1, 32, 0, s>>>(st);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

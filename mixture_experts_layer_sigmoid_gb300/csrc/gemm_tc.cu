@@ -41,18 +41,18 @@ constexpr int kThreads = 192;
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kGroupN = 16;    // n tiles per raster group (row-scheduled GEMMs)
 
+constexpr int kSmemMax = 232448;               // 227 KB per CTA
+constexpr int kStaging = 4 * 2 * 4096;          // per epilogue warp: 2 x (32 rows x 128 B)
+
 template <int BN, bool PAIR>
 struct TcCfg {
     static constexpr int A_BYTES = TBM * TBK * 2;            // this CTA's 128 rows of A
     static constexpr int B_COLS = PAIR ? BN / 2 : BN;        // this CTA's share of B
     static constexpr int B_BYTES = B_COLS * TBK * 2;
     static constexpr int STAGE = A_BYTES + B_BYTES;
-    // Pair mode leaves one spare B-sized block after the ring.
-    static constexpr int GUARD = PAIR ? B_BYTES : 0;
-    static constexpr int BUDGET = PAIR ? 216 * 1024 : kSmemBudget;
-    static constexpr int STAGES = (BUDGET - GUARD) / STAGE;
+    static constexpr int STAGES = (kSmemMax - 1024 - 256 - kStaging) / STAGE;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM = 1024 + STAGES * STAGE + GUARD + 256;
+    static constexpr int SMEM = 1024 + STAGES * STAGE + kStaging + 256;
 };
 
 struct Tile {
@@ -172,6 +172,7 @@ template <int BN, bool B_MN, int DUAL, int EPI, int SCHED, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
+               const __grid_constant__ CUtensorMap mO0, const __grid_constant__ CUtensorMap mO1,
                const GemmDesc d)
 {
     using C = TcCfg<BN, PAIR>;
@@ -181,7 +182,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE + C::GUARD);
+    const uint32_t staging = ptx::smem_u32(smem + C::STAGES * C::STAGE);   // 1024-aligned
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE + kStaging);
     // bars: full[STAGES], empty[STAGES], accf[2], acce[2], final
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -362,6 +364,35 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
         // ------------------------------------------------------- epilogue
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
         const int r_in = q * 32 + lane;         // row of the tile owned by this thread
+        // Two 32-row x 128-byte staging buffers per warp, laid out with the
+        // 128-byte swizzle of the output tensor maps (16-byte chunk j of row r
+        // at chunk j ^ (r % 8)); lane 0 stores them with TMA.
+        const uint32_t stg = staging + (uint32_t)q * 8192u;
+        uint32_t nstore = 0;
+        auto stage_store = [&](const CUtensorMap* m, const float (&a)[32], const float (&b)[32], int x, int y) {
+            const uint32_t buf = stg + (nstore & 1u) * 4096u;
+            if (nstore >= 2 && lane == 0) ptx::bulk_wait_read<1>();   // this buffer's previous store
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float* src = (j < 4) ? a + 8 * j : b + 8 * (j - 4);
+                uint4 u4;
+                __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&u4);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) h2[i] = __floats2bfloat162_rn(src[2 * i], src[2 * i + 1]);
+                const uint32_t addr = buf + (uint32_t)lane * 128u + (uint32_t)((j ^ (lane & 7)) * 16);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(u4.x), "r"(u4.y),
+                             "r"(u4.z), "r"(u4.w)
+                             : "memory");
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::tma_store_2d(m, buf, x, y);
+                ptx::bulk_commit();
+            }
+            ++nstore;
+        };
         uint32_t tc = 0;
         for (int w = unit0; w < total; w += nunits, ++tc) {
             const Tile t = decode_tile<BN, DUAL, SCHED, PAIR>(d, w, num_m, num_n, rank);
@@ -372,16 +403,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * BN);
             float v0[32], v1[32];
             if (SCHED == SCHED_WGRAD) {
-                const int m = t.m * TBM + r_in;
+                // 64-column units through shared memory and TMA stores
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    if (t.kblocks > 0) tmem_load32f(taddr + c * 32, v0);
-                    else zero32(v0);
-                    int col, which = 0;
-                    if (DUAL == DUAL_N) { which = c / (NW / 32); col = t.n * NW + (c % (NW / 32)) * 32; }
-                    else col = t.n * NW + c * 32;
-                    __nv_bfloat16* O = static_cast<__nv_bfloat16*>(which ? d.O1 : d.O0);
-                    store32_bf16(O + (size_t)t.e * d.o_estride + (size_t)m * d.ldo + col, v0);
+                for (int u = 0; u < BN / 64; ++u) {
+                    if (t.kblocks > 0) {
+                        tmem_load32f(taddr + u * 64, v0);
+                        tmem_load32f(taddr + u * 64 + 32, v1);
+                    } else {
+                        zero32(v0);
+                        zero32(v1);
+                    }
+                    const bool hi = (DUAL == DUAL_N) && u >= NW / 64;
+                    const int col = t.n * NW + (u % (NW / 64)) * 64;
+                    stage_store(hi ? &mO1 : &mO0, v0, v1, col, t.e * d.M_out + t.m * TBM + q * 32);
                 }
             } else {
                 const int row = t.row0 + r_in;
@@ -433,13 +467,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                         }
                     }
                 } else {
+                    // segments are 128-row aligned, so a warp's 32 rows are all
+                    // inside the tile's expert or (a pair's ghost half) all past it
+                    const bool warp_in = t.row0 + q * 32 < t.alloc_end;
 #pragma unroll 1
-                    for (int c = 0; c < NW / 32; ++c) {
-                        tmem_load32f(taddr + c * 32, v0);
-                        if (in_alloc) {
-                            if (!valid) zero32(v0);
-                            const size_t o = (size_t)row * d.ldo + t.n * NW + c * 32;
-                            store32_bf16(static_cast<__nv_bfloat16*>(d.O0) + o, v0);
+                    for (int u = 0; u < NW / 64; ++u) {
+                        tmem_load32f(taddr + u * 64, v0);
+                        tmem_load32f(taddr + u * 64 + 32, v1);
+                        if (warp_in) {
+                            if (!valid) {
+                                zero32(v0);
+                                zero32(v1);
+                            }
+                            stage_store(&mO0, v0, v1, t.n * NW + u * 64, t.row0 + q * 32);
                         }
                     }
                 }
@@ -451,6 +491,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                 else ptx::mbar_arrive(acce_bar(a));
             }
         }
+        if (lane == 0) ptx::bulk_wait_all();   // stores complete before the CTA exits
+        __syncwarp();
     }
 
     ptx::tc_fence_before();
@@ -486,6 +528,14 @@ bool get_encode()
 bool make_map(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld,
               int box_rows)
 {
+    if (!ptr) {   // unused output map: any valid map will do
+        static __nv_bfloat16 dummy[64] __attribute__((aligned(16)));
+        ptr = dummy;
+        rows = 1;
+        cols = 64;
+        ld = 64;
+        box_rows = 1;
+    }
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
     cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
@@ -536,9 +586,18 @@ cudaError_t run(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
 {
     constexpr int NW = (DUAL == DUAL_N) ? BN / 2 : BN;
     constexpr int BROWS = TcCfg<BN, PAIR>::B_COLS;   // K-major B box rows
-    CUtensorMap mA0, mA1, mB0, mB1;
+    CUtensorMap mA0, mA1, mB0, mB1, mO0, mO1;
     bool ok = true;
     long long units;
+    // outputs written by TMA stores (store and weight-gradient epilogues)
+    const bool tma_out = (EPI == EPI_STORE || EPI == EPI_WGRAD);
+    if (SCHED == SCHED_ROWS) {
+        ok &= make_map(&mO0, tma_out ? d.O0 : nullptr, d.a_rows, d.N, d.ldo, 32);
+        mO1 = mO0;
+    } else {
+        ok &= make_map(&mO0, d.O0, (long long)d.E * d.M_out, d.N, d.ldo, 32);
+        ok &= make_map(&mO1, (DUAL == DUAL_N) ? d.O1 : d.O0, (long long)d.E * d.M_out, d.N, d.ldo, 32);
+    }
     if (SCHED == SCHED_ROWS) {
         // A: [a_rows][K] read as 128-row boxes. B: per-expert blocks stacked.
         ok &= make_map(&mA0, d.A0, d.a_rows, d.K, d.lda, TBM);
@@ -566,7 +625,7 @@ cudaError_t run(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
     if (!PAIR) {
         const int grid = (int)(units < num_sms ? units : num_sms);
         gemm_tc_kernel<BN, B_MN, DUAL, EPI, SCHED, false>
-            <<<grid, kThreads, TcCfg<BN, false>::SMEM, s>>>(mA0, mA1, mB0, mB1, d);
+            <<<grid, kThreads, TcCfg<BN, false>::SMEM, s>>>(mA0, mA1, mB0, mB1, mO0, mO1, d);
         return cudaGetLastError();
     }
     const int slots = pair_slots<BN, B_MN, DUAL, EPI, SCHED>();
@@ -585,7 +644,7 @@ cudaError_t run(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, B_MN, DUAL, EPI, SCHED, true>, mA0, mA1, mB0,
-                              mB1, d);
+                              mB1, mO0, mO1, d);
 }
 
 // Single-CTA or CTA-pair instance: pairs when the row units come in

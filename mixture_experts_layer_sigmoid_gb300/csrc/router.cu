@@ -50,17 +50,38 @@ router_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float
 #pragma unroll
         for (int i = 0; i < EPL; ++i) acc[q][i] = 0.f;
 
-    for (int h0 = 0; h0 < H; h0 += HC) {
-        for (int idx = tid; idx < HC * EW; idx += 256) {
-            int hh = idx / EW, e = idx % EW;
-            ws[hh][e] = (e < E) ? Wr[(size_t)(h0 + hh) * E + e] : 0.f;
+    // register double buffering: chunk c+1 is fetched from global memory
+    // while chunk c is multiplied out of shared memory
+    constexpr int WPT = HC * EW / 256;            // Wr values per thread per chunk
+    constexpr int XPT = kRouterTokens * HC / 256; // x values per thread per chunk
+    float wreg[WPT], xreg[XPT];
+    auto fetch = [&](int h0) {
+#pragma unroll
+        for (int i = 0; i < WPT; ++i) {
+            const int idx = tid + 256 * i, hh = idx / EW, e = idx % EW;
+            wreg[i] = (e < E) ? __ldg(Wr + (size_t)(h0 + hh) * E + e) : 0.f;
         }
-        for (int idx = tid; idx < kRouterTokens * HC; idx += 256) {
-            int tt = idx / HC, hh = idx % HC;
-            int t = t0 + tt;
-            xs[tt][hh] = (t < T_) ? to_f32(x[(size_t)t * H + h0 + hh]) : 0.f;
+#pragma unroll
+        for (int i = 0; i < XPT; ++i) {
+            const int idx = tid + 256 * i, tt = idx / HC, hh = idx % HC;
+            const int t = t0 + tt;
+            xreg[i] = (t < T_) ? to_f32(x[(size_t)t * H + h0 + hh]) : 0.f;
+        }
+    };
+    fetch(0);
+    for (int h0 = 0; h0 < H; h0 += HC) {
+#pragma unroll
+        for (int i = 0; i < WPT; ++i) {
+            const int idx = tid + 256 * i;
+            ws[idx / EW][idx % EW] = wreg[i];
+        }
+#pragma unroll
+        for (int i = 0; i < XPT; ++i) {
+            const int idx = tid + 256 * i;
+            xs[idx / HC][idx % HC] = xreg[i];
         }
         __syncthreads();
+        if (h0 + HC < H) fetch(h0 + HC);
 #pragma unroll 4
         for (int hh = 0; hh < HC; ++hh) {
             float wv[EPL];
