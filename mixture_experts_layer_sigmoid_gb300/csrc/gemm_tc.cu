@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
                const __grid_constant__ CUtensorMap mO0, const __grid_constant__ CUtensorMap mO1,
-               const GemmDesc d)
+               const __grid_constant__ CUtensorMap mO2, const GemmDesc d)
 {
     using C = TcCfg<BN, PAIR>;
     constexpr bool A_MN = (SCHED == SCHED_WGRAD);
@@ -419,57 +419,70 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                 }
             } else {
                 const int row = t.row0 + r_in;
-                const bool in_alloc = row < t.alloc_end;
                 const bool valid = row < t.valid_end;
+                const bool warp_in = t.row0 + q * 32 < t.alloc_end;
                 if (EPI == EPI_SWIGLU_FWD) {
+                    // 64-column units of a (gate half), u (up half) and h = silu(a) u
 #pragma unroll 1
-                    for (int c = 0; c < NW / 32; ++c) {
-                        tmem_load32f(taddr + c * 32, v0);
-                        tmem_load32f(taddr + NW + c * 32, v1);
-                        if (in_alloc) {
-                            float hv[32];
+                    for (int u = 0; u < NW / 64; ++u) {
+                        float g0[32], g1[32], u0[32], u1[32], h0[32], h1[32];
+                        tmem_load32f(taddr + u * 64, g0);
+                        tmem_load32f(taddr + u * 64 + 32, g1);
+                        tmem_load32f(taddr + NW + u * 64, u0);
+                        tmem_load32f(taddr + NW + u * 64 + 32, u1);
+                        if (warp_in) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
                                 if (valid) {
-                                    SwigluFwd r(v0[i], v1[i]);
-                                    v0[i] = r.a; v1[i] = r.u; hv[i] = r.h;
+                                    SwigluFwd r0(g0[i], u0[i]);
+                                    SwigluFwd r1(g1[i], u1[i]);
+                                    h0[i] = r0.h;
+                                    h1[i] = r1.h;
                                 } else {
-                                    v0[i] = 0.f; v1[i] = 0.f; hv[i] = 0.f;
+                                    g0[i] = g1[i] = u0[i] = u1[i] = h0[i] = h1[i] = 0.f;
                                 }
                             }
-                            const size_t o = (size_t)row * d.ldo + t.n * NW + c * 32;
-                            store32_bf16(static_cast<__nv_bfloat16*>(d.O0) + o, v0);
-                            store32_bf16(static_cast<__nv_bfloat16*>(d.O1) + o, v1);
-                            store32_bf16(static_cast<__nv_bfloat16*>(d.O2) + o, hv);
+                            const int col = t.n * NW + u * 64, y = t.row0 + q * 32;
+                            stage_store(&mO0, g0, g1, col, y);
+                            stage_store(&mO1, u0, u1, col, y);
+                            stage_store(&mO2, h0, h1, col, y);
                         }
                     }
                 } else if (EPI == EPI_SWIGLU_BWD) {
 #pragma unroll 1
-                    for (int c = 0; c < NW / 32; ++c) {
-                        tmem_load32f(taddr + c * 32, v0);
-                        if (in_alloc) {
-                            const size_t o = (size_t)row * d.ldo + t.n * NW + c * 32;
+                    for (int u = 0; u < NW / 64; ++u) {
+                        float d0[32], d1[32], e0[32], e1[32];
+                        tmem_load32f(taddr + u * 64, d0);
+                        tmem_load32f(taddr + u * 64 + 32, d1);
+                        if (warp_in) {
+                            const size_t o = (size_t)row * d.ldo + t.n * NW + u * 64;
                             if (valid) {
                                 float av[32], uv[32];
                                 load32_bf16(static_cast<const __nv_bfloat16*>(d.X0) + o, av);
                                 load32_bf16(static_cast<const __nv_bfloat16*>(d.X1) + o, uv);
 #pragma unroll
                                 for (int i = 0; i < 32; ++i) {
-                                    SwigluBwd r(v0[i], av[i], uv[i]);
-                                    v0[i] = r.dA; v1[i] = r.dU;
+                                    SwigluBwd r(d0[i], av[i], uv[i]);
+                                    d0[i] = r.dA; e0[i] = r.dU;
+                                }
+                                load32_bf16(static_cast<const __nv_bfloat16*>(d.X0) + o + 32, av);
+                                load32_bf16(static_cast<const __nv_bfloat16*>(d.X1) + o + 32, uv);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    SwigluBwd r(d1[i], av[i], uv[i]);
+                                    d1[i] = r.dA; e1[i] = r.dU;
                                 }
                             } else {
-                                zero32(v0);
-                                zero32(v1);
+                                zero32(d0); zero32(d1); zero32(e0); zero32(e1);
                             }
-                            store32_bf16(static_cast<__nv_bfloat16*>(d.O0) + o, v0);
-                            store32_bf16(static_cast<__nv_bfloat16*>(d.O1) + o, v1);
+                            const int col = t.n * NW + u * 64, y = t.row0 + q * 32;
+                            stage_store(&mO0, d0, d1, col, y);
+                            stage_store(&mO1, e0, e1, col, y);
                         }
                     }
                 } else {
                     // segments are 128-row aligned, so a warp's 32 rows are all
                     // inside the tile's expert or (a pair's ghost half) all past it
-                    const bool warp_in = t.row0 + q * 32 < t.alloc_end;
 #pragma unroll 1
                     for (int u = 0; u < NW / 64; ++u) {
                         tmem_load32f(taddr + u * 64, v0);
@@ -586,17 +599,18 @@ cudaError_t run(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
 {
     constexpr int NW = (DUAL == DUAL_N) ? BN / 2 : BN;
     constexpr int BROWS = TcCfg<BN, PAIR>::B_COLS;   // K-major B box rows
-    CUtensorMap mA0, mA1, mB0, mB1, mO0, mO1;
+    CUtensorMap mA0, mA1, mB0, mB1, mO0, mO1, mO2;
     bool ok = true;
     long long units;
-    // outputs written by TMA stores (store and weight-gradient epilogues)
-    const bool tma_out = (EPI == EPI_STORE || EPI == EPI_WGRAD);
+    // every output is written by TMA stores of 32-row x 64-column boxes
     if (SCHED == SCHED_ROWS) {
-        ok &= make_map(&mO0, tma_out ? d.O0 : nullptr, d.a_rows, d.N, d.ldo, 32);
-        mO1 = mO0;
+        ok &= make_map(&mO0, d.O0, d.a_rows, d.N, d.ldo, 32);
+        ok &= make_map(&mO1, d.O1, d.a_rows, d.N, d.ldo, 32);
+        ok &= make_map(&mO2, d.O2, d.a_rows, d.N, d.ldo, 32);
     } else {
         ok &= make_map(&mO0, d.O0, (long long)d.E * d.M_out, d.N, d.ldo, 32);
         ok &= make_map(&mO1, (DUAL == DUAL_N) ? d.O1 : d.O0, (long long)d.E * d.M_out, d.N, d.ldo, 32);
+        mO2 = mO0;
     }
     if (SCHED == SCHED_ROWS) {
         // A: [a_rows][K] read as 128-row boxes. B: per-expert blocks stacked.
@@ -625,7 +639,7 @@ cudaError_t run(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
     if (!PAIR) {
         const int grid = (int)(units < num_sms ? units : num_sms);
         gemm_tc_kernel<BN, B_MN, DUAL, EPI, SCHED, false>
-            <<<grid, kThreads, TcCfg<BN, false>::SMEM, s>>>(mA0, mA1, mB0, mB1, mO0, mO1, d);
+            <<<grid, kThreads, TcCfg<BN, false>::SMEM, s>>>(mA0, mA1, mB0, mB1, mO0, mO1, mO2, d);
         return cudaGetLastError();
     }
     const int slots = pair_slots<BN, B_MN, DUAL, EPI, SCHED>();
@@ -644,7 +658,7 @@ cudaError_t run(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, B_MN, DUAL, EPI, SCHED, true>, mA0, mA1, mB0,
-                              mB1, mO0, mO1, d);
+                              mB1, mO0, mO1, mO2, d);
 }
 
 // Single-CTA or CTA-pair instance: pairs when the row units come in
