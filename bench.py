@@ -112,6 +112,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "window": window}
 
 
+# ------------------------------------------------------- multi-rank logic
+def reduce_max(v: float, device=None) -> float:
+    """Maximum of a per-rank value over all ranks (no-op without a process
+    group). Replicas share nothing else: every rank runs its own layer."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def job_metrics(world: int, ms_per_step_max: float, flops_per_step: float, tokens_per_step: int):
+    """Whole-job throughput of `world` replicas timed by the slowest rank."""
+    s = ms_per_step_max * 1e-3
+    return {"tflops": world * flops_per_step / s / 1e12, "tokens_per_s": world * tokens_per_step / s}
+
+
 # ---------------------------------------------------------------- oracle leg
 def oracle_inputs(inp_host):
     """fp64 host arrays of the inputs (exact widening of the stored values)."""
@@ -209,11 +228,7 @@ def run_ours(args, w):
             dist.barrier()
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return t.item()
+        return reduce_max(v, dev)
 
     # ---- device-timed region (inputs resident in HBM)
     sampler = ClockSampler(local)
@@ -272,7 +287,8 @@ def run_ours(args, w):
     layer.stage_times()
 
     flops = w.flops_fwd_bwd()
-    value = world * flops / (ms * 1e-3) / 1e12
+    jm = job_metrics(world, ms, flops, w.T)
+    value = jm["tflops"]
     peaks, peaks_kind = load_peaks()
     peak_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     peak_name = "bf16_tflops_sustained of %s peaks" % peaks_kind
@@ -316,7 +332,7 @@ def run_ours(args, w):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": {mi.BF16: "bf16", mi.FP32: "f32", mi.FP8_BLOCK: "e4m3"}[w.dtype],
                 "data": "synthetic",
-                "tokens_per_s": world * w.T / (ms * 1e-3),
+                "tokens_per_s": jm["tokens_per_s"],
                 "pct_of_tensor_peak": 100.0 * value / world / peak_sust,
                 "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "top_k": w.k, "F": w.F,
                            "Fs": w.Fs, "score": "sigmoid" if w.score else "softmax",
@@ -326,7 +342,7 @@ def run_ours(args, w):
                            "parallelism": f"replicas x{world}"},
                 "roofline": roofline,
                 "cpu_baseline": cpu,
-                "e2e": {"value": world * flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "e2e": {"value": job_metrics(world, ms_e2e, flops, w.T)["tflops"], "unit": "TFLOP/s",
                         "h2d_bytes_per_step": 2 * x.numel() * x.element_size(),
                         "d2h_bytes_per_step": 2 * x.numel() * x.element_size()},
                 "gpu_launches": launches_total,
