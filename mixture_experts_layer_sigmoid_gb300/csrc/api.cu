@@ -569,6 +569,7 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
     d.N = F; d.K = H; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.pair_tab = pairtab; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(sv, L.Xq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(sv, L.sX); d.lds_a = H / 128;
     d.B0 = u8(sv, L.WgQT); d.B1 = u8(sv, L.WuQT); d.ldb = H; d.b_rows = E * F;
     d.SB0 = f32(sv, L.sWgT); d.SB1 = f32(sv, L.sWuT);
@@ -579,6 +580,7 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
     d.N = H; d.K = F; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.pair_tab = pairtab; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.hq); d.lda = F; d.a_rows = Rp; d.SA0 = f32(ws, L.sh); d.lds_a = F / 128;
     d.B0 = u8(sv, L.WdQT); d.ldb = F; d.b_rows = E * H; d.SB0 = f32(sv, L.sWdT);
     d.O0 = Yp; d.ldo = H; d.status = status;
@@ -609,6 +611,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     const int* poff = reinterpret_cast<const int*>(sv + L.poff);
     const int* meta = reinterpret_cast<const int*>(sv + L.meta);
     const int* tiletab = reinterpret_cast<const int*>(sv + L.tiletab);
+    const int* pairtab = reinterpret_cast<const int*>(sv + L.pairtab);
     const int* rowof = reinterpret_cast<const int*>(sv + L.rowof);
     const int* slotof = reinterpret_cast<const int*>(sv + L.slotof);
     const T* Xp = reinterpret_cast<const T*>(sv + L.Xp);
@@ -636,6 +639,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_BWD; d.dual = DUAL_NONE;
     d.N = F; d.K = H; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.pair_tab = pairtab; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.dYq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(ws, L.sdY); d.lds_a = H / 128;
     d.B0 = u8(sv, L.WdQ); d.ldb = H; d.b_rows = E * F; d.SB0 = f32(sv, L.sWd);
     d.X0 = A; d.X1 = U; d.O0 = dA; d.O1 = dU; d.ldo = F; d.status = status;
@@ -647,6 +651,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
     d.N = H; d.M_out = F; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.pair_tab = pairtab; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.hTq); d.lda = Rp; d.SA0 = f32(ws, L.shT); d.lds_a = Rp / 128;
     d.B0 = u8(ws, L.dYpTq); d.ldb = Rp; d.SB0 = f32(ws, L.sdYpT); d.lds_b = Rp / 128;
     d.rows_cap = Rp;
@@ -659,6 +664,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
     d.N = H; d.K = F; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.pair_tab = pairtab; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.dAq); d.A1 = u8(ws, L.dUq); d.lda = F; d.a_rows = Rp;
     d.SA0 = f32(ws, L.sdA); d.SA1 = f32(ws, L.sdU); d.lds_a = F / 128;
     d.B0 = u8(sv, L.WgQ); d.B1 = u8(sv, L.WuQ); d.ldb = F; d.b_rows = E * H;
@@ -673,6 +679,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
     d.N = F; d.M_out = H; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.pair_tab = pairtab; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.XpTq); d.lda = Rp; d.SA0 = f32(ws, L.sXpT); d.lds_a = Rp / 128;
     d.B0 = u8(ws, L.dATq); d.B1 = u8(ws, L.dUTq); d.ldb = Rp;
     d.SB0 = f32(ws, L.sdAT); d.SB1 = f32(ws, L.sdUT); d.lds_b = Rp / 128;

@@ -9,12 +9,19 @@
 //   C[r][n] = sum_kb sA[r][kb] sB[kb][n/128] (sum_{k in kb} qA[r][k] qB[k][n]).
 // Both operands are stored K-major in E4M3.
 //
-// One CTA per SM, 6 warps: warp 0 TMA producer (stages of A 128x128 B and
-// B 128x128 B, 128-byte swizzle); warp 1 TMEM allocator and single-thread
-// issuer of tcgen05.mma.kind::f8f6f4 (4 x K=32 per k block) into one of two
-// TMEM partial buffers; warps 2-5 promote each finished k block into fp32
-// registers (one output row per thread, 128 columns) with its two scales and,
-// at the end of the tile, run the fused epilogue from the registers.
+// Ten warps per CTA: warp 0 TMA producer (stages of A 128x128 B and this
+// CTA's share of B, 128-byte swizzle); warp 1 TMEM allocator and, in the
+// even CTA, single-thread issuer of tcgen05.mma.kind::f8f6f4 (N = 256, 4 x
+// K=32 per k block) into one of two 256-column TMEM partial buffers; warps
+// 2-9 promote each finished k block into fp32 registers with its two scales
+// (two warps per TMEM lane quarter, 128 columns per thread, packed f32x2
+// FMAs) and, at the end of the tile, run the fused epilogue from registers.
+// They release a partial buffer with a relaxed mbarrier arrive: a release
+// arrive would first wait for their outstanding scale loads and stores, and
+// that wait, once per k block, cost more than the MMAs themselves.
+// PAIR: clusters of two CTAs issue M = 256 MMAs (A rows split between the
+// CTAs, B columns split between them), so each SM loads 32 KB per 128-deep
+// k block for 128 x 256 x 128 MACs.
 #include "internal.h"
 #include "epilogue.cuh"
 #include "ptx.cuh"
@@ -25,12 +32,26 @@
 namespace moe {
 namespace {
 
-constexpr int QBM = 128, QBK = 128, QBN = 128;   // tile M, K block, MMA N
-constexpr int kQThreads = 192;
-constexpr int kQStage = QBM * QBK + QBN * QBK;    // 32 KB
-constexpr int kQStages = 6;
-constexpr int kQSmem = 1024 + kQStages * kQStage + 256;
+constexpr int QBM = 128, QBK = 128, QBN = 256;   // rows per CTA, K block, MMA N
+constexpr int kQThreads = 320;
+constexpr int kQSmemMax = 232448;
 constexpr int kQGroupN = 16;
+// MMA unit per partial buffer: false -> one N = 256 MMA per k block into two
+// 256-column TMEM buffers; true -> two N = 128 halves into four 128-column
+// buffers (deeper, but each half re-reads the A tile from shared memory).
+constexpr bool kSplitN = false;
+constexpr int kPBuf = kSplitN ? 4 : 2;
+constexpr int kPCols = kSplitN ? 128 : 256;
+constexpr int kUnitsPerKb = kSplitN ? 2 : 1;
+
+template <bool PAIR>
+struct QCfg {
+    static constexpr int A_BYTES = QBM * QBK;
+    static constexpr int B_ROWS = PAIR ? QBN / 2 : QBN;   // B rows (n) staged by this CTA
+    static constexpr int STAGE = A_BYTES + B_ROWS * QBK;
+    static constexpr int STAGES = (kQSmemMax - 1024 - 256) / STAGE;
+    static constexpr int SMEM = 1024 + STAGES * STAGE + 256;
+};
 
 // f8f6f4 instruction descriptor: E4M3 A and B (format 0), fp32 D, K-major.
 __host__ __device__ constexpr uint32_t idesc_e4m3(int N, int M)
@@ -50,36 +71,103 @@ __device__ __forceinline__ void mma_e4m3(uint32_t tmem_d, uint64_t adesc, uint64
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+__device__ __forceinline__ void mma_e4m3_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// Packed pairs of fp32 accumulators: acc += v * s on both halves at once.
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ void fma2(uint64_t& acc, uint64_t v, uint64_t s)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(v), "l"(s));
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v)
+{
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+    return f;
+}
+// 8 fp32 -> 8 bf16 in one 16-byte store
+__device__ __forceinline__ void st8(__nv_bfloat16* dst, const float* v)
+{
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    *reinterpret_cast<uint4*>(dst) = u;
+}
+// eight consecutive accumulators (four packed pairs) starting at pair p
+__device__ __forceinline__ void get8(const uint64_t* acc, int p, float* v)
+{
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = unpack2(acc[p + i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
 
 struct QTile {
     int e, m, n, row0, kblocks, kb0, valid_end, alloc_end;
 };
 
-template <int DUAL, int SCHED>
+template <int DUAL, int SCHED, bool PAIR>
 __device__ __forceinline__ void qtile_counts(const GemmDesc& d, int& num_m, int& num_n, int& total)
 {
     constexpr int NW = (DUAL == DUAL_N) ? QBN / 2 : QBN;
-    num_n = d.N / NW;
+    num_n = (d.N + NW - 1) / NW;
     if (SCHED == SCHED_ROWS) {
-        num_m = d.meta[0];
+        num_m = PAIR ? d.meta[2] : d.meta[0];
         total = num_m * num_n;
     } else {
-        num_m = d.M_out / QBM;
+        num_m = d.M_out / (PAIR ? 2 * QBM : QBM);
         total = d.E * num_m * num_n;
     }
 }
 
-template <int DUAL, int SCHED>
-__device__ __forceinline__ QTile qdecode(const GemmDesc& d, int w, int num_m, int num_n)
+// Row-scheduled tiles walk groups of kQGroupN column tiles over the row
+// units (one unit = a 128-row tile, or a pair of one expert's consecutive
+// tiles, the second possibly a "ghost" past the segment that is never
+// stored); weight-gradient tiles walk each expert's (m, n) grid m-fastest.
+template <int DUAL, int SCHED, bool PAIR>
+__device__ __forceinline__ QTile qdecode(const GemmDesc& d, int w, int num_m, int num_n, int rank)
 {
     QTile t;
     if (SCHED == SCHED_ROWS) {
         const int group = w / (num_m * kQGroupN);
         const int r = w - group * num_m * kQGroupN;
         const int gsz = min(kQGroupN, num_n - group * kQGroupN);
-        t.m = r / gsz;
+        const int mu = r / gsz;
         t.n = group * kQGroupN + r % gsz;
-        t.e = d.tile_tab[t.m];
+        const int first = PAIR ? d.pair_tab[mu] : mu;
+        t.m = first + rank;
+        t.e = d.tile_tab[first];
         t.row0 = t.m * QBM;
         t.valid_end = d.poff[t.e] + d.counts[t.e];
         t.alloc_end = d.poff[t.e + 1];
@@ -88,8 +176,9 @@ __device__ __forceinline__ QTile qdecode(const GemmDesc& d, int w, int num_m, in
     } else {
         const int per = num_m * num_n;
         t.e = w / per;
-        const int r = w % per;
-        t.m = r % num_m;
+        const int r = w - t.e * per;
+        const int mu = r % num_m;
+        t.m = PAIR ? 2 * mu + rank : mu;
         t.n = r / num_m;
         t.row0 = d.poff[t.e];
         t.kb0 = t.row0 / QBK;
@@ -99,64 +188,41 @@ __device__ __forceinline__ QTile qdecode(const GemmDesc& d, int w, int num_m, in
     return t;
 }
 
-__device__ __forceinline__ void st32(__nv_bfloat16* dst, const float* v)
-{
-    uint4* p = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 u;
-        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
-        p[q] = u;
-    }
-}
-__device__ __forceinline__ void ld32(const __nv_bfloat16* src, float* v)
-{
-    const uint4* p = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 u = p[q];
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float2 f = __bfloat1622float2(h[i]);
-            v[8 * q + 2 * i] = f.x;
-            v[8 * q + 2 * i + 1] = f.y;
-        }
-    }
-}
-
-template <int EPI, int SCHED, int DUAL>
+template <int EPI, int SCHED, int DUAL, bool PAIR>
 __global__ void __launch_bounds__(kQThreads, 1)
 gemm_fp8_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                 const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
                 const GemmDesc d)
 {
-    constexpr int NW = (DUAL == DUAL_N) ? QBN / 2 : QBN;
-    constexpr uint32_t IDESC = idesc_e4m3(QBN, QBM);
+    using C = QCfg<PAIR>;
+    constexpr int NW = (DUAL == DUAL_N) ? QBN / 2 : QBN;   // output columns per tile
+    constexpr uint32_t IDESC = idesc_e4m3(kPCols, PAIR ? 2 * QBM : QBM);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQStages * kQStage);
-    // full[S], empty[S], pfull[2], pempty[2], final
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kQStages + 5);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+    // full[S], empty[S], pfull[4], pempty[4], final
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 9);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = PAIR ? (int)ptx::cluster_ctarank() : 0;
+    const int unit0 = PAIR ? (int)ptx::cluster_id_x() : (int)blockIdx.x;
+    const int nunits = PAIR ? (int)ptx::nclusters_x() : (int)gridDim.x;
     const uint32_t bar0 = ptx::smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kQStages + s); };
-    auto pfull_bar = [&](int b) { return bar0 + 8u * (2 * kQStages + b); };
-    auto pempty_bar = [&](int b) { return bar0 + 8u * (2 * kQStages + 2 + b); };
-    const uint32_t final_bar = bar0 + 8u * (2 * kQStages + 4);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    auto pfull_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + b); };
+    auto pempty_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 4 + b); };
+    const uint32_t final_bar = bar0 + 8u * (2 * C::STAGES + 8);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kQStages; ++s) {
+        for (int s = 0; s < C::STAGES; ++s) {
             ptx::mbar_init(full_bar(s), 1);
             ptx::mbar_init(empty_bar(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < 4; ++b) {
             ptx::mbar_init(pfull_bar(b), 1);
-            ptx::mbar_init(pempty_bar(b), 4);
+            // the warps promoting one buffer, in each CTA
+            ptx::mbar_init(pempty_bar(b), (kSplitN ? 4 : 8) * (PAIR ? 2 : 1));
         }
         ptx::mbar_init(final_bar, 1);
         *abort_flag = 0;
@@ -171,20 +237,30 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__
         }
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 2 * QBN);
-        ptx::tmem_relinquish();
+        if (PAIR) {
+            ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), 2 * QBN);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 2 * QBN);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    if (PAIR) ptx::cluster_sync();   // peer barriers initialised before any remote signal
+    else __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     int num_m, num_n, total;
-    qtile_counts<DUAL, SCHED>(d, num_m, num_n, total);
+    qtile_counts<DUAL, SCHED, PAIR>(d, num_m, num_n, total);
     auto wait_uniform = [&](uint32_t bar, uint32_t parity, int where) -> bool {
         int ok = 1;
         if (lane == 0) ok = ptx::wait_bounded(bar, parity, abort_flag, d.status, where) ? 1 : 0;
         return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
+    auto load = [&](uint32_t dst, const CUtensorMap* m, int s, int x, int y) {
+        if (PAIR) ptx::tma_load_2d_pair(dst, m, ptx::mapa_shared(full_bar(s), 0), x, y);
+        else ptx::tma_load_2d(dst, m, full_bar(s), x, y);
     };
 
     if (warp == 0) {
@@ -192,196 +268,315 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__
         uint32_t it = 0;
         const int kb_half = d.K / QBK;
         bool ok = true;
-        for (int w = blockIdx.x; ok && w < total; w += gridDim.x) {
-            const QTile t = qdecode<DUAL, SCHED>(d, w, num_m, num_n);
+        for (int w = unit0; ok && w < total; w += nunits) {
+            const QTile t = qdecode<DUAL, SCHED, PAIR>(d, w, num_m, num_n, rank);
             for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
-                const int s = it % kQStages;
-                const uint32_t ph = (it / kQStages) & 1u;
+                const int s = it % C::STAGES;
+                const uint32_t ph = (it / C::STAGES) & 1u;
                 if (!wait_uniform(empty_bar(s), ph ^ 1u, 11)) { ok = false; break; }
                 if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(full_bar(s), kQStage);
-                    const uint32_t a_dst = ptx::smem_u32(smem + s * kQStage);
-                    const uint32_t b_dst = a_dst + QBM * QBK;
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(s), (PAIR ? 2 : 1) * C::STAGE);
+                    const uint32_t a_dst = ptx::smem_u32(smem + s * C::STAGE);
+                    const uint32_t b_dst = a_dst + C::A_BYTES;
+                    int kx, arow, brow;
+                    const CUtensorMap* am = &mA0;
+                    const CUtensorMap* bm = &mB0;
                     if (SCHED == SCHED_ROWS) {
                         const bool second = (DUAL == DUAL_K) && kb >= kb_half;
-                        const int kx = (second ? kb - kb_half : kb) * QBK;
-                        ptx::tma_load_2d(a_dst, second ? &mA1 : &mA0, full_bar(s), kx, t.row0);
-                        if (DUAL == DUAL_N) {
-                            ptx::tma_load_2d(b_dst, &mB0, full_bar(s), kx, t.e * d.N + t.n * NW);
-                            ptx::tma_load_2d(b_dst + 64 * QBK, &mB1, full_bar(s), kx, t.e * d.N + t.n * NW);
-                        } else {
-                            ptx::tma_load_2d(b_dst, second ? &mB1 : &mB0, full_bar(s), kx,
-                                             t.e * d.N + t.n * NW);
-                        }
+                        kx = (second ? kb - kb_half : kb) * QBK;
+                        arow = t.row0;
+                        brow = t.e * d.N + t.n * NW;
+                        if (second) { am = &mA1; bm = &mB1; }
                     } else {
-                        const int kx = (t.kb0 + kb) * QBK;
-                        ptx::tma_load_2d(a_dst, &mA0, full_bar(s), kx, t.m * QBM);
-                        if (DUAL == DUAL_N) {
-                            ptx::tma_load_2d(b_dst, &mB0, full_bar(s), kx, t.n * NW);
-                            ptx::tma_load_2d(b_dst + 64 * QBK, &mB1, full_bar(s), kx, t.n * NW);
-                        } else {
-                            ptx::tma_load_2d(b_dst, &mB0, full_bar(s), kx, t.n * NW);
-                        }
+                        kx = (t.kb0 + kb) * QBK;
+                        arow = t.m * QBM;
+                        brow = t.n * NW;
+                    }
+                    load(a_dst, am, s, kx, arow);
+                    // B "part 0" = tile columns [0, 128) (DUAL_N: B0 columns),
+                    // "part 1" = [128, 256) (DUAL_N: the same columns of B1).
+                    // A pair's CTA r stages part r (128 rows). A single CTA stages
+                    // [part0 | part1] for N = 256 MMAs, or, with split halves,
+                    // [part0 rows 0-63 | part1 rows 0-63 | part0 rows 64-127 |
+                    // part1 rows 64-127] so that half h reads 128 contiguous rows
+                    // at offset h x 16 KB: the same columns as a pair's half h.
+                    const CUtensorMap* p0 = (DUAL == DUAL_N) ? &mB0 : bm;
+                    const CUtensorMap* p1 = (DUAL == DUAL_N) ? &mB1 : bm;
+                    const int r1 = (DUAL == DUAL_N) ? brow : brow + 128;
+                    if (PAIR) {
+                        load(b_dst, rank ? p1 : p0, s, kx, rank ? r1 : brow);
+                    } else {
+                        load(b_dst, p0, s, kx, brow);
+                        load(b_dst + (kSplitN ? 64 : 128) * QBK, p1, s, kx, r1);
+                        load(b_dst + (kSplitN ? 128 : 64) * QBK, p0, s, kx, brow + 64);
+                        load(b_dst + 192 * QBK, p1, s, kx, r1 + 64);
                     }
                 }
                 __syncwarp();
             }
         }
     } else if (warp == 1) {
-        // --------------------------------------------------- MMA issuer
-        uint32_t it = 0, pc = 0;
-        bool ok = true;
-        for (int w = blockIdx.x; ok && w < total; w += gridDim.x) {
-            const QTile t = qdecode<DUAL, SCHED>(d, w, num_m, num_n);
-            for (int kb = 0; kb < t.kblocks; ++kb, ++it, ++pc) {
-                const int s = it % kQStages;
-                const uint32_t ph = (it / kQStages) & 1u;
-                const int pb = pc & 1;
-                const uint32_t pph = (pc >> 1) & 1u;
-                if (!wait_uniform(pempty_bar(pb), pph ^ 1u, 12)) { ok = false; break; }
-                if (!wait_uniform(full_bar(s), ph, 13)) { ok = false; break; }
-                ptx::tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t a_addr = ptx::smem_u32(smem + s * kQStage);
-                    const uint32_t b_addr = a_addr + QBM * QBK;
-                    const uint32_t dt = tmem_base + (uint32_t)(pb * QBN);
+        if (rank == 0) {
+            // --------------------------------------------------- MMA issuer
+            uint32_t it = 0, pc = 0;
+            bool ok = true;
+            for (int w = unit0; ok && w < total; w += nunits) {
+                const QTile t = qdecode<DUAL, SCHED, PAIR>(d, w, num_m, num_n, rank);
+                for (int kb = 0; kb < t.kblocks; ++kb, ++it, ++pc) {
+                    const int s = it % C::STAGES;
+                    const uint32_t ph = (it / C::STAGES) & 1u;
+                    if (!wait_uniform(full_bar(s), ph, 13)) { ok = false; break; }
+                    const uint32_t a_addr = ptx::smem_u32(smem + s * C::STAGE);
+                    const uint32_t b_addr = a_addr + C::A_BYTES;
+                    // the k block's MMA unit(s), into partial buffers u % kPBuf
 #pragma unroll
-                    for (int k = 0; k < QBK / 32; ++k)
-                        mma_e4m3(dt, ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024),
-                                 ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024), IDESC, k > 0 ? 1u : 0u);
-                    ptx::tc_commit(empty_bar(s));
-                    ptx::tc_commit(pfull_bar(pb));
+                    for (int h = 0; h < kUnitsPerKb; ++h) {
+                        const uint32_t u = kUnitsPerKb * pc + (uint32_t)h;
+                        const int pb = (int)(u % kPBuf);
+                        if (!wait_uniform(pempty_bar(pb), ((u / kPBuf) & 1u) ^ 1u, 12)) { ok = false; break; }
+                        ptx::tc_fence_after();
+                        if (lane == 0) {
+                            const uint32_t dt = tmem_base + (uint32_t)(pb * kPCols);
+                            const uint32_t bh = b_addr + (uint32_t)h * (PAIR ? 64 * QBK : 128 * QBK);
+#pragma unroll
+                            for (int k = 0; k < QBK / 32; ++k) {
+                                const uint64_t ad = ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
+                                const uint64_t bd = ptx::smem_desc_sw128(bh + k * 32, 16, 1024);
+                                if (PAIR) mma_e4m3_pair(dt, ad, bd, IDESC, k > 0 ? 1u : 0u);
+                                else mma_e4m3(dt, ad, bd, IDESC, k > 0 ? 1u : 0u);
+                            }
+                            if (PAIR) ptx::tc_commit_pair(pfull_bar(pb), 3);
+                            else ptx::tc_commit(pfull_bar(pb));
+                        }
+                        __syncwarp();
+                    }
+                    if (!ok) break;
+                    if (lane == 0) {
+                        if (PAIR) ptx::tc_commit_pair(empty_bar(s), 3);
+                        else ptx::tc_commit(empty_bar(s));
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
+            }
+            // every MMA issued by this warp has completed before TMEM is freed
+            if (lane == 0) {
+                if (PAIR) ptx::tc_commit_pair(final_bar, 3);
+                else ptx::tc_commit(final_bar);
             }
         }
         if (lane == 0) {
-            ptx::tc_commit(final_bar);
             volatile int never = 0;
             ptx::wait_bounded(final_bar, 0, &never, d.status, 14);
         }
         __syncwarp();
     } else {
         // ----------------------------------------- promotion + epilogue
-        const int q = warp & 3;
-        const int r_in = q * 32 + lane;
-        uint32_t pc = 0;
+        const int q = warp & 3;                  // TMEM lane quarter
+        const int hh = (warp - 2) >> 2;          // MMA half owned by this warp
+        const int r_in = q * 32 + lane;          // row of the CTA's 128
+        // This thread accumulates MMA half hh of its row: part-0 columns
+        // [64hh, +64) in acc pairs 0-31 ("lo") and part-1 columns [64hh, +64)
+        // in pairs 32-63 ("hi"). Part 0 is tile columns [0, 128) (DUAL_N: B0),
+        // part 1 tile columns [128, 256) (DUAL_N: the same columns of B1).
         const int kb_half = d.K / QBK;
-        for (int w = blockIdx.x; w < total; w += gridDim.x) {
-            const QTile t = qdecode<DUAL, SCHED>(d, w, num_m, num_n);
-            float acc[QBN];
-#pragma unroll
-            for (int j = 0; j < QBN; ++j) acc[j] = 0.f;
+        uint32_t pc = 0;
+        for (int w = unit0; w < total; w += nunits) {
+            const QTile t = qdecode<DUAL, SCHED, PAIR>(d, w, num_m, num_n, rank);
             const int arow = (SCHED == SCHED_ROWS) ? t.row0 + r_in : t.m * QBM + r_in;
+            const bool arow_ok = (SCHED == SCHED_ROWS) ? arow < d.a_rows : true;
+            // 128-wide B column blocks of the two parts, and the output columns
+            const int nb_lo = (DUAL == DUAL_N) ? t.n : 2 * t.n;
+            const int nb_hi = (DUAL == DUAL_N) ? t.n : 2 * t.n + 1;
+            const bool hi_ok = (DUAL == DUAL_N) || nb_hi < d.N / 128;
+            const int col_lo = (DUAL == DUAL_N) ? t.n * NW + 64 * hh : nb_lo * 128 + 64 * hh;
+            const int col_hi = (DUAL == DUAL_N) ? col_lo : nb_hi * 128 + 64 * hh;
+            if (EPI == EPI_SWIGLU_BWD && arow_ok && arow < t.alloc_end) {
+                // the saved a, u of this thread's columns, into L2 ahead of the epilogue
+                const __nv_bfloat16* X0 = static_cast<const __nv_bfloat16*>(d.X0) + (size_t)arow * d.ldo;
+                const __nv_bfloat16* X1 = static_cast<const __nv_bfloat16*>(d.X1) + (size_t)arow * d.ldo;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(X0 + col_lo));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(X1 + col_lo));
+                if (hi_ok) {
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(X0 + col_hi));
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(X1 + col_hi));
+                }
+            }
+            uint64_t acc[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc[j] = 0ull;
             bool ok = true;
-            for (int kb = 0; kb < t.kblocks; ++kb, ++pc) {
-                // scales of this k block (A: per row; B: per 128-column block)
-                float sa, sb0, sb1;
+            // the scales of k block kb (A: this thread's row; B: the two parts' blocks)
+            auto scales = [&](int kb, float& sa, float& sb_lo, float& sb_hi) {
+                sa = sb_lo = sb_hi = 0.f;
                 if (SCHED == SCHED_ROWS) {
                     const bool second = (DUAL == DUAL_K) && kb >= kb_half;
                     const int kk = second ? kb - kb_half : kb;
-                    sa = (second ? d.SA1 : d.SA0)[(size_t)arow * d.lds_a + kk];
-                    const int nb = (t.n * NW) / 128;
-                    const size_t bi = ((size_t)t.e * (d.N / 128) + nb) * (d.K / 128) + kk;
-                    sb0 = (second ? d.SB1 : d.SB0)[bi];
-                    sb1 = (DUAL == DUAL_N) ? d.SB1[bi] : sb0;
+                    if (arow_ok) sa = (second ? d.SA1 : d.SA0)[(size_t)arow * d.lds_a + kk];
+                    const size_t kbs = d.K / 128;
+                    const size_t e0 = (size_t)t.e * (d.N / 128);
+                    if (DUAL == DUAL_N) {
+                        sb_lo = d.SB0[(e0 + nb_lo) * kbs + kk];
+                        sb_hi = d.SB1[(e0 + nb_hi) * kbs + kk];
+                    } else {
+                        const float* SB = second ? d.SB1 : d.SB0;
+                        sb_lo = SB[(e0 + nb_lo) * kbs + kk];
+                        if (hi_ok) sb_hi = SB[(e0 + nb_hi) * kbs + kk];
+                    }
                 } else {
                     const int kg = t.kb0 + kb;
                     sa = d.SA0[(size_t)arow * d.lds_a + kg];
-                    const int nb = (t.n * NW) / 128;
-                    sb0 = d.SB0[(size_t)nb * d.lds_b + kg];
-                    sb1 = (DUAL == DUAL_N) ? d.SB1[(size_t)nb * d.lds_b + kg] : sb0;
+                    if (DUAL == DUAL_N) {
+                        sb_lo = d.SB0[(size_t)nb_lo * d.lds_b + kg];
+                        sb_hi = d.SB1[(size_t)nb_hi * d.lds_b + kg];
+                    } else {
+                        sb_lo = d.SB0[(size_t)nb_lo * d.lds_b + kg];
+                        if (hi_ok) sb_hi = d.SB0[(size_t)nb_hi * d.lds_b + kg];
+                    }
                 }
-                const int pb = pc & 1;
-                const uint32_t pph = (pc >> 1) & 1u;
-                if (!wait_uniform(pfull_bar(pb), pph, 15)) { ok = false; break; }
+            };
+            float nsa = 0.f, nsb_lo = 0.f, nsb_hi = 0.f;   // one k block ahead
+            if (t.kblocks > 0) scales(0, nsa, nsb_lo, nsb_hi);
+            for (int kb = 0; kb < t.kblocks; ++kb, ++pc) {
+                const float sa = nsa, sb_lo = nsb_lo, sb_hi = nsb_hi;
+                if (kb + 1 < t.kblocks) scales(kb + 1, nsa, nsb_lo, nsb_hi);
+                const float s_lo = sa * sb_lo, s_hi = sa * sb_hi;
+                const uint64_t s2_lo = pack2(__float_as_uint(s_lo), __float_as_uint(s_lo));
+                const uint64_t s2_hi = pack2(__float_as_uint(s_hi), __float_as_uint(s_hi));
+                const uint32_t u = kUnitsPerKb * pc + (kSplitN ? (uint32_t)hh : 0u);
+                const int pb = (int)(u % kPBuf);
+                if (!wait_uniform(pfull_bar(pb), (u / kPBuf) & 1u, 15)) { ok = false; break; }
                 ptx::tc_fence_after();
-                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(pb * QBN);
+                // this thread's part-0 and part-1 columns within the buffer
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(pb * kPCols) +
+                                       (kSplitN ? 0u : 64u * hh);
+                constexpr int kHiOff = kSplitN ? 64 : 128;
 #pragma unroll
-                for (int c = 0; c < QBN / 32; ++c) {
-                    uint32_t r[32];
-                    ptx::tmem_ld32(taddr + c * 32, r);
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t r[16];
+                    tmem_ld16(taddr + (c < 4 ? 16 * c : kHiOff + 16 * (c - 4)), r);
                     ptx::tmem_ld_wait();
-                    const float sc = sa * ((c * 32 < NW) ? sb0 : sb1);
+                    const uint64_t s2 = c < 4 ? s2_lo : s2_hi;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(__uint_as_float(r[i]), sc, acc[c * 32 + i]);
+                    for (int i = 0; i < 8; ++i) fma2(acc[8 * c + i], pack2(r[2 * i], r[2 * i + 1]), s2);
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(pempty_bar(pb));
+                if (lane == 0) {
+                    if (PAIR) ptx::mbar_arrive_cluster_relaxed(ptx::mapa_shared(pempty_bar(pb), 0));
+                    else ptx::mbar_arrive_relaxed(pempty_bar(pb));
+                }
             }
             if (!ok) break;
-            // ---- epilogue from registers
+            // ---- epilogue from registers (pairs 0-31: part-0 columns, 32-63: part 1)
+            float v[8], x[8];
             if (SCHED == SCHED_WGRAD) {
-                const int m = t.m * QBM + r_in;
-                if (DUAL == DUAL_N) {
-                    __nv_bfloat16* O0 = static_cast<__nv_bfloat16*>(d.O0) + (size_t)t.e * d.o_estride + (size_t)m * d.ldo + t.n * NW;
-                    __nv_bfloat16* O1 = static_cast<__nv_bfloat16*>(d.O1) + (size_t)t.e * d.o_estride + (size_t)m * d.ldo + t.n * NW;
-                    st32(O0, acc); st32(O0 + 32, acc + 32);
-                    st32(O1, acc + 64); st32(O1 + 32, acc + 96);
-                } else {
-                    __nv_bfloat16* O0 = static_cast<__nv_bfloat16*>(d.O0) + (size_t)t.e * d.o_estride + (size_t)m * d.ldo + t.n * NW;
+                const size_t ob = (size_t)t.e * d.o_estride + (size_t)arow * d.ldo;
+                __nv_bfloat16* Olo = static_cast<__nv_bfloat16*>(d.O0) + ob + col_lo;
+                __nv_bfloat16* Ohi = static_cast<__nv_bfloat16*>(DUAL == DUAL_N ? d.O1 : d.O0) + ob + col_hi;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) st32(O0 + 32 * c, acc + 32 * c);
+                for (int j = 0; j < 8; ++j) {
+                    get8(acc, 4 * j, v);
+                    st8(Olo + 8 * j, v);
                 }
-            } else {
-                const int row = t.row0 + r_in;
-                if (row < t.alloc_end) {
-                    const bool valid = row < t.valid_end;
-                    const size_t o = (size_t)row * d.ldo + t.n * NW;
-                    if (EPI == EPI_SWIGLU_FWD) {
-                        float a[64], u[64], hv[64];
+                if (hi_ok) {
 #pragma unroll
-                        for (int i = 0; i < 64; ++i) {
+                    for (int j = 0; j < 8; ++j) {
+                        get8(acc, 32 + 4 * j, v);
+                        st8(Ohi + 8 * j, v);
+                    }
+                }
+            } else if (arow < t.alloc_end) {
+                const bool valid = arow < t.valid_end;
+                const size_t orow = (size_t)arow * d.ldo;
+                if (EPI == EPI_SWIGLU_FWD) {
+                    __nv_bfloat16* O0 = static_cast<__nv_bfloat16*>(d.O0) + orow + col_lo;
+                    __nv_bfloat16* O1 = static_cast<__nv_bfloat16*>(d.O1) + orow + col_lo;
+                    __nv_bfloat16* O2 = static_cast<__nv_bfloat16*>(d.O2) + orow + col_lo;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float hv[8];
+                        get8(acc, 4 * j, v);
+                        get8(acc, 32 + 4 * j, x);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
                             if (valid) {
-                                SwigluFwd r(acc[i], acc[64 + i]);
-                                a[i] = r.a; u[i] = r.u; hv[i] = r.h;
+                                const SwigluFwd r(v[i], x[i]);
+                                hv[i] = r.h;
                             } else {
-                                a[i] = u[i] = hv[i] = 0.f;
+                                v[i] = x[i] = hv[i] = 0.f;
                             }
                         }
+                        st8(O0 + 8 * j, v);
+                        st8(O1 + 8 * j, x);
+                        st8(O2 + 8 * j, hv);
+                    }
+                } else if (EPI == EPI_SWIGLU_BWD) {
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+                        if (part == 1 && !hi_ok) break;
+                        const size_t o = orow + (part ? col_hi : col_lo);
+                        const __nv_bfloat16* X0 = static_cast<const __nv_bfloat16*>(d.X0) + o;
+                        const __nv_bfloat16* X1 = static_cast<const __nv_bfloat16*>(d.X1) + o;
                         __nv_bfloat16* O0 = static_cast<__nv_bfloat16*>(d.O0) + o;
                         __nv_bfloat16* O1 = static_cast<__nv_bfloat16*>(d.O1) + o;
-                        __nv_bfloat16* O2 = static_cast<__nv_bfloat16*>(d.O2) + o;
-                        st32(O0, a); st32(O0 + 32, a + 32);
-                        st32(O1, u); st32(O1 + 32, u + 32);
-                        st32(O2, hv); st32(O2 + 32, hv + 32);
-                    } else if (EPI == EPI_SWIGLU_BWD) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            float av[32], uv[32], da[32], du[32];
-                            if (valid) {
-                                ld32(static_cast<const __nv_bfloat16*>(d.X0) + o + 32 * c, av);
-                                ld32(static_cast<const __nv_bfloat16*>(d.X1) + o + 32 * c, uv);
+                        for (int j0 = 0; j0 < 8; j0 += 2) {
+                            uint4 ua[2], uu[2];
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) {
-                                    SwigluBwd r(acc[32 * c + i], av[i], uv[i]);
-                                    da[i] = r.dA; du[i] = r.dU;
-                                }
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) da[i] = du[i] = 0.f;
+                            for (int j = 0; j < 2; ++j) {
+                                ua[j] = valid ? *reinterpret_cast<const uint4*>(X0 + 8 * (j0 + j)) : make_uint4(0, 0, 0, 0);
+                                uu[j] = valid ? *reinterpret_cast<const uint4*>(X1 + 8 * (j0 + j)) : make_uint4(0, 0, 0, 0);
                             }
-                            st32(static_cast<__nv_bfloat16*>(d.O0) + o + 32 * c, da);
-                            st32(static_cast<__nv_bfloat16*>(d.O1) + o + 32 * c, du);
-                        }
-                    } else {
-                        if (!valid) {
 #pragma unroll
-                            for (int j = 0; j < QBN; ++j) acc[j] = 0.f;
-                        }
+                            for (int j = 0; j < 2; ++j) {
+                                uint4 oa, ou;
+                                const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&ua[j]);
+                                const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&uu[j]);
+                                __nv_bfloat162* da2 = reinterpret_cast<__nv_bfloat162*>(&oa);
+                                __nv_bfloat162* du2 = reinterpret_cast<__nv_bfloat162*>(&ou);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) st32(static_cast<__nv_bfloat16*>(d.O0) + o + 32 * c, acc + 32 * c);
+                                for (int i = 0; i < 4; ++i) {
+                                    const float2 dh = unpack2(acc[32 * part + 4 * (j0 + j) + i]);
+                                    const float2 av = __bfloat1622float2(a2[i]);
+                                    const float2 uv = __bfloat1622float2(u2[i]);
+                                    const SwigluBwd r0(dh.x, av.x, uv.x);
+                                    const SwigluBwd r1(dh.y, av.y, uv.y);
+                                    // pad rows (a = u = 0) give dA = dU = 0
+                                    da2[i] = __floats2bfloat162_rn(r0.dA, r1.dA);
+                                    du2[i] = __floats2bfloat162_rn(r0.dU, r1.dU);
+                                }
+                                *reinterpret_cast<uint4*>(O0 + 8 * (j0 + j)) = oa;
+                                *reinterpret_cast<uint4*>(O1 + 8 * (j0 + j)) = ou;
+                            }
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+                        if (part == 1 && !hi_ok) break;
+                        __nv_bfloat16* O0 = static_cast<__nv_bfloat16*>(d.O0) + orow + (part ? col_hi : col_lo);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            get8(acc, 32 * part + 4 * j, v);
+                            if (!valid) {
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) v[i] = 0.f;
+                            }
+                            st8(O0 + 8 * j, v);
+                        }
                     }
                 }
             }
         }
     }
-    __syncthreads();
+    ptx::tc_fence_before();
+    if (PAIR) ptx::cluster_sync();   // both CTAs done with TMEM and with remote signals
+    else __syncthreads();
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, 2 * QBN);
+        if (PAIR) ptx::tmem_dealloc_pair(tmem_base, 2 * QBN);
+        else ptx::tmem_dealloc(tmem_base, 2 * QBN);
     }
 }
 
@@ -415,39 +610,101 @@ bool map8(CUtensorMap* m, const void* ptr, long long rows, long long cols, long 
 }
 
 template <int EPI, int SCHED, int DUAL>
+int qpair_slots()
+{
+    static int slots = -1;
+    if (slots < 0) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(kQThreads, 1, 1);
+        cfg.dynamicSmemBytes = QCfg<true>::SMEM;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_fp8_kernel<EPI, SCHED, DUAL, true>, &cfg) != cudaSuccess)
+            n = 0;
+        cudaGetLastError();
+        slots = n;
+    }
+    return slots;
+}
+
+template <int EPI, int SCHED, int DUAL, bool PAIR>
 cudaError_t qrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
 {
+    using C = QCfg<PAIR>;
     constexpr int NW = (DUAL == DUAL_N) ? QBN / 2 : QBN;
-    constexpr int BROWS = (DUAL == DUAL_N) ? 64 : QBN;
+    // B box rows: a pair's CTA stages its 128-row part in one box; a single
+    // CTA stages both parts as four 64-row boxes
+    constexpr int BROWS = PAIR ? 128 : 64;
     CUtensorMap mA0, mA1, mB0, mB1;
     bool ok = true;
     long long units;
+    const long long num_n = (d.N + NW - 1) / NW;
     if (SCHED == SCHED_ROWS) {
         ok &= map8(&mA0, d.A0, d.a_rows, d.K, d.lda, QBM);
         ok &= map8(&mA1, d.A1 ? d.A1 : d.A0, d.a_rows, d.K, d.lda, QBM);
         ok &= map8(&mB0, d.B0, d.b_rows, d.K, d.ldb, BROWS);
         ok &= map8(&mB1, d.B1 ? d.B1 : d.B0, d.b_rows, d.K, d.ldb, BROWS);
-        units = (long long)max_m_tiles * (d.N / NW);
+        const long long m_units = PAIR ? (max_m_tiles + 1) / 2 : max_m_tiles;
+        units = m_units * num_n;
     } else {
         // A: [M_out][rows_cap], B: [N][rows_cap] (transposed operands)
         ok &= map8(&mA0, d.A0, d.M_out, d.rows_cap, d.lda, QBM);
         mA1 = mA0;
         ok &= map8(&mB0, d.B0, d.N, d.rows_cap, d.ldb, BROWS);
         ok &= map8(&mB1, d.B1 ? d.B1 : d.B0, d.N, d.rows_cap, d.ldb, BROWS);
-        units = (long long)d.E * (d.M_out / QBM) * (d.N / NW);
+        units = (long long)d.E * (d.M_out / (PAIR ? 2 * QBM : QBM)) * num_n;
     }
     if (!ok) return cudaErrorInvalidValue;
     if (units <= 0) return cudaSuccess;
-    const int grid = (int)(units < num_sms ? units : num_sms);
-    gemm_fp8_kernel<EPI, SCHED, DUAL><<<grid, kQThreads, kQSmem, s>>>(mA0, mA1, mB0, mB1, d);
-    return cudaGetLastError();
+    if (!PAIR) {
+        const int grid = (int)(units < num_sms ? units : num_sms);
+        gemm_fp8_kernel<EPI, SCHED, DUAL, false><<<grid, kQThreads, C::SMEM, s>>>(mA0, mA1, mB0, mB1, d);
+        return cudaGetLastError();
+    }
+    const int slots = qpair_slots<EPI, SCHED, DUAL>();
+    if (slots <= 0) return cudaErrorLaunchOutOfResources;
+    const long long clusters = units < slots ? units : slots;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(kQThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI, SCHED, DUAL, true>, mA0, mA1, mB0, mB1, d);
+}
+
+// CTA pairs when the row units come in (mostly) complete pairs, or the
+// weight-gradient rows split into 256-row pair tiles.
+template <int EPI, int SCHED, int DUAL>
+cudaError_t qrun_any(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
+{
+    const bool pair = (SCHED == SCHED_WGRAD) ? d.M_out % (2 * QBM) == 0
+                                             : d.pair_tab != nullptr && d.prefer_pair;
+    if (pair) return qrun<EPI, SCHED, DUAL, true>(d, max_m_tiles, num_sms, s);
+    return qrun<EPI, SCHED, DUAL, false>(d, max_m_tiles, num_sms, s);
 }
 
 template <int EPI, int SCHED, int DUAL>
 cudaError_t qattr()
 {
-    return cudaFuncSetAttribute(gemm_fp8_kernel<EPI, SCHED, DUAL>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+    cudaError_t e = cudaFuncSetAttribute(gemm_fp8_kernel<EPI, SCHED, DUAL, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<false>::SMEM);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gemm_fp8_kernel<EPI, SCHED, DUAL, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<true>::SMEM);
 }
 
 }  // namespace
@@ -472,16 +729,16 @@ cudaError_t launch_gemm_fp8(const GemmDesc& d, int max_m_tiles, int num_sms, cud
     if (!enc8()) return cudaErrorNotSupported;
     if (d.sched == SCHED_ROWS) {
         switch (d.epi) {
-        case EPI_SWIGLU_FWD: return qrun<EPI_SWIGLU_FWD, SCHED_ROWS, DUAL_N>(d, max_m_tiles, num_sms, s);
-        case EPI_SWIGLU_BWD: return qrun<EPI_SWIGLU_BWD, SCHED_ROWS, DUAL_NONE>(d, max_m_tiles, num_sms, s);
+        case EPI_SWIGLU_FWD: return qrun_any<EPI_SWIGLU_FWD, SCHED_ROWS, DUAL_N>(d, max_m_tiles, num_sms, s);
+        case EPI_SWIGLU_BWD: return qrun_any<EPI_SWIGLU_BWD, SCHED_ROWS, DUAL_NONE>(d, max_m_tiles, num_sms, s);
         case EPI_STORE:
-            return d.dual == DUAL_K ? qrun<EPI_STORE, SCHED_ROWS, DUAL_K>(d, max_m_tiles, num_sms, s)
-                                    : qrun<EPI_STORE, SCHED_ROWS, DUAL_NONE>(d, max_m_tiles, num_sms, s);
+            return d.dual == DUAL_K ? qrun_any<EPI_STORE, SCHED_ROWS, DUAL_K>(d, max_m_tiles, num_sms, s)
+                                    : qrun_any<EPI_STORE, SCHED_ROWS, DUAL_NONE>(d, max_m_tiles, num_sms, s);
         default: return cudaErrorInvalidValue;
         }
     }
-    return d.dual == DUAL_N ? qrun<EPI_WGRAD, SCHED_WGRAD, DUAL_N>(d, max_m_tiles, num_sms, s)
-                            : qrun<EPI_WGRAD, SCHED_WGRAD, DUAL_NONE>(d, max_m_tiles, num_sms, s);
+    return d.dual == DUAL_N ? qrun_any<EPI_WGRAD, SCHED_WGRAD, DUAL_N>(d, max_m_tiles, num_sms, s)
+                            : qrun_any<EPI_WGRAD, SCHED_WGRAD, DUAL_NONE>(d, max_m_tiles, num_sms, s);
 }
 
 }  // namespace moe

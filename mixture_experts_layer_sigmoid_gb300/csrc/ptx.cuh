@@ -218,6 +218,19 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                  : "memory");
 }
+// Arrivals that publish no memory writes, only "this role is done with a
+// buffer" (e.g. after tcgen05.wait::ld + tcgen05.fence::before_thread_sync):
+// no release fence, so they do not wait for the thread's outstanding loads
+// and stores.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+                 : "memory");
+}
 // Tile load by either CTA of a pair whose completion is counted on an
 // mbarrier that may live in the peer CTA (shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m,
