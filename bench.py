@@ -209,7 +209,7 @@ def run_ours(args, w):
     inp = mi.make_inputs(w, dev)
     layer = MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score,
                      dtype={mi.FP32: MOE_FP32, mi.BF16: MOE_BF16, mi.FP8_BLOCK: MOE_FP8_BLOCK}[w.dtype],
-                     Fs=w.Fs, device=local, stage_timing=True)
+                     Fs=w.Fs, device=local, stage_timing=True, fold_gates=args.fold_gates)
     x, dY = inp["x"], inp["dY"]
     W = (inp["Wr"], inp["Wg"], inp["Wu"], inp["Wd"], inp["Wsg"], inp["Wsu"], inp["Wsd"])
     y = torch.empty_like(x)
@@ -339,7 +339,8 @@ def run_ours(args, w):
                            "routing_bias": w.bias, "seed": w.seed,
                            "l2": "inputs larger than L2 (expert weights %.2f GB), no flush" %
                                  ((3 * w.E * w.H * w.F + 3 * w.H * w.Fs) * es / 1e9),
-                           "parallelism": f"replicas x{world}"},
+                           "parallelism": f"replicas x{world}",
+                           "fold_gates": bool(args.fold_gates)},
                 "roofline": roofline,
                 "cpu_baseline": cpu,
                 "e2e": {"value": job_metrics(world, ms_e2e, flops, w.T)["tflops"], "unit": "TFLOP/s",
@@ -363,6 +364,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=8, help="oracle sample for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=2, help="oracle sample per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fold-gates", action="store_true",
+                    help="memory-efficient permutation: routing weights folded into h")
     ap.add_argument("--override", default="",
                     help="comma-separated shape overrides, e.g. F=4096,T=2048 (profiling runs)")
     args = ap.parse_args()

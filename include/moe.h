@@ -81,13 +81,26 @@ typedef struct {
     int T_max;   /* largest token count a call may pass, >= 1               */
     int score;   /* moe_score_t                                             */
     int dtype;   /* moe_dtype_t                                             */
-    unsigned flags; /* 0 or MOE_FLAG_STAGE_TIMING                          */
+    unsigned flags; /* 0, or MOE_FLAG_STAGE_TIMING | MOE_FLAG_FOLD_GATES    */
 } moe_config_t;
 
 /* Plan flag: bracket every kernel launch of moe_forward / moe_backward with
  * CUDA events on the call's stream, for moe_stage_times. A plan with this
  * flag must not be used by two host threads at once. */
 #define MOE_FLAG_STAGE_TIMING 1u
+
+/* Plan flag: memory-efficient permutation ("Scalable Training of
+ * Mixture-of-Experts Models with Megatron Core", §4, Memory-Efficient
+ * Permutation: an algebraic rearrangement that drops intermediate tensors).
+ * The routing weight g of each routed row is folded into its activation
+ * before fc2 (h' = g silu(a) u), so fc2 yields g y_e directly and Combine is
+ * a plain sum; the backward pass forms dg = <dh', h> in the fc2-dgrad
+ * epilogue and recomputes h' = g h from the saved a, u for the fc2 weight
+ * gradient. Results equal the unfolded layer up to rounding; the saved
+ * buffer no longer holds h or the permuted expert outputs (R_pad x (F + H)
+ * elements less, R_pad = routed rows padded to 128 per expert), which move
+ * to the workspace. */
+#define MOE_FLAG_FOLD_GATES 2u
 
 /* Per-stage device time accumulated since the previous moe_stage_times. */
 typedef struct {
@@ -145,7 +158,7 @@ typedef struct {
 } moe_bwd_args_t;
 
 /* Validate `cfg` for `device` and build a plan (host memory only).
- * Errors: INVALID_ARG (null, sizes out of range, flags != 0),
+ * Errors: INVALID_ARG (null, sizes out of range, unknown flags),
  *         UNSUPPORTED (dtype not built, device not sm_103), CUDA. */
 moe_status_t moe_plan_create(const moe_config_t* cfg, int device, moe_plan_t* out);
 

@@ -29,6 +29,7 @@ MOE_ERR_DEVICE_TIMEOUT = 6
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_FP32, MOE_BF16, MOE_FP8_BLOCK = 0, 1, 2
 MOE_FLAG_STAGE_TIMING = 1
+MOE_FLAG_FOLD_GATES = 2
 
 # Names the library exports (include/moe.h).
 EXPORTS = ("moe_plan_create", "moe_plan_destroy", "moe_workspace_size", "moe_forward",
@@ -180,14 +181,19 @@ class MoELayer:
 
     Weights are passed per call (they are inputs of the C ABI). Layouts are
     those of include/moe.h: x T×H, Wr H×E fp32, b E fp32, W_gate/W_up E×H×F,
-    W_down E×F×H, shared expert H×Fs, H×Fs, Fs×H."""
+    W_down E×F×H, shared expert H×Fs, H×Fs, Fs×H.
+
+    ``fold_gates`` selects the memory-efficient permutation (MOE_FLAG_FOLD_GATES):
+    the routing weights are folded into the expert activations, and the saved
+    buffer keeps neither h nor the permuted expert outputs."""
 
     def __init__(self, H, E, F, top_k, T_max, score=MOE_SCORE_SOFTMAX, dtype=MOE_BF16, Fs=0,
-                 device=0, stage_timing=False):
+                 device=0, stage_timing=False, fold_gates=False):
         import torch
         self.torch = torch
+        flags = (MOE_FLAG_STAGE_TIMING if stage_timing else 0) | (MOE_FLAG_FOLD_GATES if fold_gates else 0)
         self.cfg = moe_config_t(H=H, E=E, F=F, Fs=Fs, top_k=top_k, T_max=T_max, score=score,
-                                dtype=dtype, flags=MOE_FLAG_STAGE_TIMING if stage_timing else 0)
+                                dtype=dtype, flags=flags)
         self.device = torch.device("cuda", device)
         self.plan = moe_plan_create(self.cfg, device)
         self._bufs: Dict[int, tuple] = {}

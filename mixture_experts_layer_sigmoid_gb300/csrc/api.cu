@@ -24,7 +24,8 @@ struct Layout {
     size_t topk, gates, selsc, counts, poff, meta, tiletab, pairtab, rowof, slotof;
     size_t Xp, A, U, Hh, Yp, As, Us, Hs, saved_bytes;
     // workspace
-    size_t status, hist, blkbase, Ys, dYp, dA, dU, dXp, dz, WrT, dAs, dUs, dXs, ws_bytes;
+    size_t status, hist, blkbase, Ys, dYp, dA, dU, dXp, dz, WrT, dAs, dUs, dXs, dgpart, ws_bytes;
+    bool fold;   // Hh and Yp live in the workspace (MOE_FLAG_FOLD_GATES)
     // blockwise FP8 (saved: permuted activations and weights; ws: the rest)
     size_t Xq, sX, WgQ, sWg, WuQ, sWu, WgQT, sWgT, WuQT, sWuT, WdQ, sWd, WdQT, sWdT;
     size_t hq, sh, dYq, sdY, dAq, sdA, dUq, sdU, hTq, shT, dYpTq, sdYpT, XpTq, sXpT, dATq, sdAT,
@@ -56,8 +57,9 @@ Layout make_layout(const moe_config_t& c, int T)
     L.Xp = take(es * L.Rp_max * c.H);
     L.A = take(es * L.Rp_max * c.F);
     L.U = take(es * L.Rp_max * c.F);
-    L.Hh = take(es * L.Rp_max * c.F);
-    L.Yp = take(es * L.Rp_max * c.H);
+    L.fold = (c.flags & MOE_FLAG_FOLD_GATES) != 0;
+    L.Hh = take(L.fold ? 0 : es * L.Rp_max * c.F);
+    L.Yp = take(L.fold ? 0 : es * L.Rp_max * c.H);
     L.As = take(es * (size_t)T * c.Fs);
     L.Us = take(es * (size_t)T * c.Fs);
     L.Hs = take(es * (size_t)T * c.Fs);
@@ -95,6 +97,11 @@ Layout make_layout(const moe_config_t& c, int T)
     L.dYpTq = take(q8 ? Rp * c.H : 0);    L.sdYpT = take(q8 ? 4 * (Rp / 128) * (c.H / 128) : 0);
     L.XpTq = take(q8 ? Rp * c.H : 0);     L.sXpT = take(q8 ? 4 * (Rp / 128) * c.H : 0);
     L.dATq = take(q8 ? Rp * c.F : 0);     L.sdAT = take(q8 ? 4 * (Rp / 128) * (c.F / 128) : 0);
+    L.dgpart = take(L.fold ? sizeof(float) * L.Rp_max * (c.F / 64) : 0);
+    if (L.fold) {
+        L.Hh = take(es * L.Rp_max * c.F);
+        L.Yp = take(es * L.Rp_max * c.H);
+    }
     L.dUTq = take(q8 ? Rp * c.F : 0);     L.sdUT = take(q8 ? 4 * (Rp / 128) * (c.F / 128) : 0);
     L.ws_bytes = o;
     return L;
@@ -107,7 +114,7 @@ moe_status_t check_config(const moe_config_t* c)
     if (!c) return MOE_ERR_INVALID_ARG;
     if (c->H <= 0 || c->H % 128 || c->E < 1 || c->E > kMaxE || c->F <= 0 || c->F % 128 ||
         c->Fs < 0 || c->Fs % 128 || c->top_k < 1 || c->top_k > kMaxK || c->top_k > c->E ||
-        c->T_max < 1 || (c->flags & ~MOE_FLAG_STAGE_TIMING) != 0)
+        c->T_max < 1 || (c->flags & ~(MOE_FLAG_STAGE_TIMING | MOE_FLAG_FOLD_GATES)) != 0)
         return MOE_ERR_INVALID_ARG;
     if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
     if (c->dtype != MOE_FP32 && c->dtype != MOE_BF16 && c->dtype != MOE_FP8_BLOCK)
@@ -143,14 +150,15 @@ enum Stage : int {
     ST_ROUTER, ST_SCAN, ST_INDEX, ST_PERMUTE, ST_FC1, ST_FC2, ST_FC1S, ST_FC2S, ST_COMBINE,
     ST_GATEGRAD, ST_FC2_DGRAD, ST_FC2_WGRAD, ST_FC1_DGRAD, ST_FC1_WGRAD, ST_FC2S_DGRAD,
     ST_FC2S_WGRAD, ST_FC1S_DGRAD, ST_FC1S_WGRAD, ST_ROUTER_WGRAD, ST_TRANSPOSE, ST_UNPERMUTE,
-    ST_WQUANT, ST_QROWS, ST_QT, ST_COUNT
+    ST_WQUANT, ST_QROWS, ST_QT, ST_GATEDZ, ST_COUNT
 };
 const char* const kStageNames[ST_COUNT] = {
     "router", "scan", "index", "permute", "fc1_swiglu", "fc2", "shared_fc1_swiglu", "shared_fc2",
     "combine", "gate_grad", "fc2_dgrad_swiglu", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad",
     "shared_fc2_dgrad", "shared_fc2_wgrad", "shared_fc1_dgrad", "shared_fc1_wgrad",
     "router_wgrad", "wr_transpose", "unpermute_reduce", "fp8_weight_quant", "fp8_quant_rows",
-    "fp8_quant_t"};
+    "fp8_quant_t", "gate_dz"
+};
 struct StageRec {
     int stage;
     cudaEvent_t start, stop;
@@ -319,8 +327,8 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     T* Xp = reinterpret_cast<T*>(sv + L.Xp);
     T* A = reinterpret_cast<T*>(sv + L.A);
     T* U = reinterpret_cast<T*>(sv + L.U);
-    T* Hh = reinterpret_cast<T*>(sv + L.Hh);
-    T* Yp = reinterpret_cast<T*>(sv + L.Yp);
+    T* Hh = reinterpret_cast<T*>((L.fold ? ws : sv) + L.Hh);
+    T* Yp = reinterpret_cast<T*>((L.fold ? ws : sv) + L.Yp);
     T* Ys = Fs ? reinterpret_cast<T*>(ws + L.Ys) : nullptr;
     const T* x = static_cast<const T*>(a->x);
 
@@ -348,6 +356,7 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     d.B0 = a->W_gate; d.B1 = a->W_up; d.ldb = F; d.b_kmajor = 0; d.b_estride = (long long)H * F;
     d.b_rows = E * H;
     d.O0 = A; d.O1 = U; d.O2 = Hh; d.ldo = F; d.status = status;
+    if (L.fold) { d.gates = gates; d.slot_of = slotof; }   // Hh = g silu(A) U
     MOE_STAGE(ST_FC1, gemm(d));
     // fc2: Yp = Hh Wd
     memset(&d, 0, sizeof d);
@@ -378,7 +387,8 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
         d.O0 = Ys; d.ldo = H; d.status = status;
         MOE_STAGE(ST_FC2S, gemm(d));
     }
-    MOE_STAGE(ST_COMBINE, launch_combine<T>(Yp, Ys, rowof, gates, T_, H, k, static_cast<T*>(a->y), s));
+    MOE_STAGE(ST_COMBINE, launch_combine<T>(Yp, Ys, rowof, L.fold ? nullptr : gates, T_, H, k,
+                                            static_cast<T*>(a->y), s));
 
     if (a->topk_idx) MOE_CUDA(cudaMemcpyAsync(a->topk_idx, topk, sizeof(int) * L.R, cudaMemcpyDeviceToDevice, s));
     if (a->gates) MOE_CUDA(cudaMemcpyAsync(a->gates, gates, sizeof(float) * L.R, cudaMemcpyDeviceToDevice, s));
@@ -410,7 +420,8 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     const T* Xp = reinterpret_cast<const T*>(sv + L.Xp);
     const T* A = reinterpret_cast<const T*>(sv + L.A);
     const T* U = reinterpret_cast<const T*>(sv + L.U);
-    const T* Hh = reinterpret_cast<const T*>(sv + L.Hh);
+    // folded gates: Hh is recomputed into the workspace, Yp is not needed
+    T* Hh = reinterpret_cast<T*>((L.fold ? ws : sv) + L.Hh);
     const T* Yp = reinterpret_cast<const T*>(sv + L.Yp);
     T* dYp = reinterpret_cast<T*>(ws + L.dYp);
     T* dA = reinterpret_cast<T*>(ws + L.dA);
@@ -418,6 +429,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     T* dXp = reinterpret_cast<T*>(ws + L.dXp);
     float* dz = reinterpret_cast<float*>(ws + L.dz);
     float* WrT = reinterpret_cast<float*>(ws + L.WrT);
+    float* dgpart = reinterpret_cast<float*>(ws + L.dgpart);
     const T* dY = static_cast<const T*>(a->dY);
 
     auto gemm = [&](const GemmDesc& d) -> cudaError_t {
@@ -427,9 +439,14 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     };
 
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
-    // Combine backward: gate gradients, gate-scaled output gradients, router dz
-    MOE_STAGE(ST_GATEGRAD, launch_gate_grad<T>(dY, Yp, rowof, topk, gates, selsc, poff, counts, T_, H, E, k,
-                                 c.score, dYp, dz, s));
+    // Combine backward: gate gradients, gate-scaled output gradients, router
+    // dz; with folded gates only the permuted copy of dY (dg and dz follow
+    // from the fc2-dgrad epilogue)
+    if (L.fold)
+        MOE_STAGE(ST_GATEGRAD, launch_permute<T>(dY, rowof, poff, counts, T_, H, E, k, dYp, s));
+    else
+        MOE_STAGE(ST_GATEGRAD, launch_gate_grad<T>(dY, Yp, rowof, topk, gates, selsc, poff, counts, T_, H,
+                                                   E, k, c.score, dYp, dz, s));
     GemmDesc d;
     // fc2 dgrad + SwiGLU backward: dh = dYp Wd^T -> dA, dU
     memset(&d, 0, sizeof d);
@@ -440,7 +457,13 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     d.A0 = dYp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = a->W_down; d.ldb = H; d.b_kmajor = 1; d.b_estride = (long long)F * H; d.b_rows = E * F;
     d.X0 = A; d.X1 = U; d.O0 = dA; d.O1 = dU; d.ldo = F; d.status = status;
+    if (L.fold) {
+        d.gates = gates; d.slot_of = slotof; d.dg_part = dgpart; d.dg_ld = F / 64;
+        d.O2 = Hh;   // g h, recomputed for the fc2 weight gradient
+    }
     MOE_STAGE(ST_FC2_DGRAD, gemm(d));
+    if (L.fold)
+        MOE_STAGE(ST_GATEDZ, launch_gate_dz(dgpart, F / 64, rowof, gates, selsc, T_, k, c.score, dz, s));
     // fc2 wgrad: dWd[e] = Hh_e^T dYp_e
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
@@ -544,8 +567,8 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     T* Xp = reinterpret_cast<T*>(sv + L.Xp);
     T* A = reinterpret_cast<T*>(sv + L.A);
     T* U = reinterpret_cast<T*>(sv + L.U);
-    T* Hh = reinterpret_cast<T*>(sv + L.Hh);
-    T* Yp = reinterpret_cast<T*>(sv + L.Yp);
+    T* Hh = reinterpret_cast<T*>((L.fold ? ws : sv) + L.Hh);
+    T* Yp = reinterpret_cast<T*>((L.fold ? ws : sv) + L.Yp);
     auto u8 = [&](uint8_t* base, size_t off) { return base + off; };
     auto f32 = [&](uint8_t* base, size_t off) { return reinterpret_cast<float*>(base + off); };
     const T* x = static_cast<const T*>(a->x);
@@ -574,6 +597,7 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     d.B0 = u8(sv, L.WgQT); d.B1 = u8(sv, L.WuQT); d.ldb = H; d.b_rows = E * F;
     d.SB0 = f32(sv, L.sWgT); d.SB1 = f32(sv, L.sWuT);
     d.O0 = A; d.O1 = U; d.O2 = Hh; d.ldo = F; d.status = status;
+    if (L.fold) { d.gates = gates; d.slot_of = slotof; }   // Hh = g silu(A) U
     MOE_STAGE(ST_FC1, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
     MOE_STAGE(ST_QROWS, launch_quant_rows(Hh, meta + 1, Rp, F, u8(ws, L.hq), f32(ws, L.sh), s));
     memset(&d, 0, sizeof d);
@@ -585,7 +609,8 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     d.B0 = u8(sv, L.WdQT); d.ldb = F; d.b_rows = E * H; d.SB0 = f32(sv, L.sWdT);
     d.O0 = Yp; d.ldo = H; d.status = status;
     MOE_STAGE(ST_FC2, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
-    MOE_STAGE(ST_COMBINE, launch_combine<T>(Yp, nullptr, rowof, gates, T_, H, k, static_cast<T*>(a->y), s));
+    MOE_STAGE(ST_COMBINE, launch_combine<T>(Yp, nullptr, rowof, L.fold ? nullptr : gates, T_, H, k,
+                                            static_cast<T*>(a->y), s));
 
     if (a->topk_idx) MOE_CUDA(cudaMemcpyAsync(a->topk_idx, topk, sizeof(int) * L.R, cudaMemcpyDeviceToDevice, s));
     if (a->gates) MOE_CUDA(cudaMemcpyAsync(a->gates, gates, sizeof(float) * L.R, cudaMemcpyDeviceToDevice, s));
@@ -617,7 +642,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     const T* Xp = reinterpret_cast<const T*>(sv + L.Xp);
     const T* A = reinterpret_cast<const T*>(sv + L.A);
     const T* U = reinterpret_cast<const T*>(sv + L.U);
-    const T* Hh = reinterpret_cast<const T*>(sv + L.Hh);
+    T* Hh = reinterpret_cast<T*>((L.fold ? ws : sv) + L.Hh);   // folded: recomputed below
     const T* Yp = reinterpret_cast<const T*>(sv + L.Yp);
     T* dYp = reinterpret_cast<T*>(ws + L.dYp);
     T* dA = reinterpret_cast<T*>(ws + L.dA);
@@ -625,13 +650,17 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     T* dXp = reinterpret_cast<T*>(ws + L.dXp);
     float* dz = reinterpret_cast<float*>(ws + L.dz);
     float* WrT = reinterpret_cast<float*>(ws + L.WrT);
+    float* dgpart = reinterpret_cast<float*>(ws + L.dgpart);
     auto u8 = [&](uint8_t* base, size_t off) { return base + off; };
     auto f32 = [&](uint8_t* base, size_t off) { return reinterpret_cast<float*>(base + off); };
     const T* dY = static_cast<const T*>(a->dY);
 
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
-    MOE_STAGE(ST_GATEGRAD, launch_gate_grad<T>(dY, Yp, rowof, topk, gates, selsc, poff, counts, T_, H,
-                                               E, k, c.score, dYp, dz, s));
+    if (L.fold)
+        MOE_STAGE(ST_GATEGRAD, launch_permute<T>(dY, rowof, poff, counts, T_, H, E, k, dYp, s));
+    else
+        MOE_STAGE(ST_GATEGRAD, launch_gate_grad<T>(dY, Yp, rowof, topk, gates, selsc, poff, counts, T_, H,
+                                                   E, k, c.score, dYp, dz, s));
     // fc2 dgrad + SwiGLU backward
     MOE_STAGE(ST_QROWS, launch_quant_rows(dYp, meta + 1, Rp, H, u8(ws, L.dYq), f32(ws, L.sdY), s));
     GemmDesc d;
@@ -643,7 +672,13 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.A0 = u8(ws, L.dYq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(ws, L.sdY); d.lds_a = H / 128;
     d.B0 = u8(sv, L.WdQ); d.ldb = H; d.b_rows = E * F; d.SB0 = f32(sv, L.sWd);
     d.X0 = A; d.X1 = U; d.O0 = dA; d.O1 = dU; d.ldo = F; d.status = status;
+    if (L.fold) {
+        d.gates = gates; d.slot_of = slotof; d.dg_part = dgpart; d.dg_ld = F / 64;
+        d.O2 = Hh;   // g h, recomputed for the fc2 weight gradient
+    }
     MOE_STAGE(ST_FC2_DGRAD, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
+    if (L.fold)
+        MOE_STAGE(ST_GATEDZ, launch_gate_dz(dgpart, F / 64, rowof, gates, selsc, T_, k, c.score, dz, s));
     // fc2 wgrad: dWd[e] = h_e^T dYp_e
     MOE_STAGE(ST_QT, launch_quant_t(Hh, meta + 1, Rp, F, 0, u8(ws, L.hTq), f32(ws, L.shT), s));
     MOE_STAGE(ST_QT, launch_quant_t(dYp, meta + 1, Rp, H, 1, u8(ws, L.dYpTq), f32(ws, L.sdYpT), s));

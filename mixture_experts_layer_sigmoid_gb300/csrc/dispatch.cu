@@ -85,7 +85,12 @@ combine_kernel(const T* __restrict__ Yp, const T* __restrict__ Ys, const int* __
     const int t = blockIdx.x;
     int rows[kMaxK];
     float g[kMaxK];
-    for (int j = 0; j < k; ++j) { rows[j] = row_of[(size_t)t * k + j]; g[j] = gates[(size_t)t * k + j]; }
+    // gates == null: the routing weights were folded into the expert
+    // activations, so the expert outputs are already weighted
+    for (int j = 0; j < k; ++j) {
+        rows[j] = row_of[(size_t)t * k + j];
+        g[j] = gates ? gates[(size_t)t * k + j] : 1.f;
+    }
     for (int v = threadIdx.x; v < H / V; v += kRowThreads) {
         float acc[V], in[V];
 #pragma unroll
@@ -101,6 +106,27 @@ combine_kernel(const T* __restrict__ Yp, const T* __restrict__ Ys, const int* __
             for (int i = 0; i < V; ++i) acc[i] += in[i];
         }
         Vec<T>::store(y + (size_t)t * H + v * V, acc);
+    }
+}
+
+// Router logit gradient of one token's k selected experts from dg:
+//   softmax: dz_j = g_j (dg_j - sum_i g_i dg_i)
+//   sigmoid: dz_j = s_j (1 - s_j) (dg_j - sum_i g_i dg_i) / sum_i s_i
+__device__ __forceinline__ void router_dz(const float* dg, const float* g, const float* sel, int k,
+                                          int score, float* dz)
+{
+    float gd = 0.f, ssum = 0.f;
+    for (int j = 0; j < k; ++j) {
+        gd += g[j] * dg[j];
+        ssum += sel[j];
+    }
+    for (int j = 0; j < k; ++j) {
+        if (score == MOE_SCORE_SOFTMAX) {
+            dz[j] = g[j] * (dg[j] - gd);
+        } else {
+            const float s = sel[j];
+            dz[j] = s * (1.f - s) * (dg[j] - gd) / ssum;
+        }
     }
 }
 
@@ -149,25 +175,39 @@ gate_grad_kernel(const T* __restrict__ dY, const T* __restrict__ Yp, const int* 
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        float dg[kMaxK], gd = 0.f, ssum = 0.f;
+        float dg[kMaxK];
         for (int j = 0; j < k; ++j) {
             float s = 0.f;
             for (int w = 0; w < kRowThreads / 32; ++w) s += red[w][j];
             dg[j] = s;
-            gd += g[j] * s;
-            ssum += selsc[(size_t)t * k + j];
         }
-        for (int j = 0; j < k; ++j) {
-            float d;
-            if (score == MOE_SCORE_SOFTMAX) {
-                d = g[j] * (dg[j] - gd);
-            } else {
-                float s = selsc[(size_t)t * k + j];
-                d = s * (1.f - s) * (dg[j] - gd) / ssum;
-            }
-            dz[(size_t)t * k + j] = d;
-        }
+        router_dz(dg, g, selsc + (size_t)t * k, k, score, dz + (size_t)t * k);
     }
+}
+
+// Folded routing weights: dg of token t's slot j is the sum of the fc2-dgrad
+// epilogue's partial dot products <dh', h> over the 64-column units of its
+// row (fixed order: lane-strided sums, then a butterfly), then dz as above.
+// One warp per token.
+__global__ void __launch_bounds__(256)
+gate_dz_kernel(const float* __restrict__ dg_part, int nslots, const int* __restrict__ row_of,
+               const float* __restrict__ gates, const float* __restrict__ selsc, int T_, int k,
+               int score, float* __restrict__ dz)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T_) return;
+    float dg[kMaxK], g[kMaxK];
+    for (int j = 0; j < k; ++j) {
+        const float* pr = dg_part + (size_t)row_of[(size_t)t * k + j] * nslots;
+        float s = 0.f;
+        for (int q = lane; q < nslots; q += 32) s += pr[q];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        dg[j] = s;
+        g[j] = gates[(size_t)t * k + j];
+    }
+    if (lane == 0) router_dz(dg, g, selsc + (size_t)t * k, k, score, dz + (size_t)t * k);
 }
 
 // dWr[h][e] = sum over expert e's rows r of Xp[r][h] dz[slot(r)]. Block
@@ -308,6 +348,13 @@ cudaError_t launch_gate_grad(const T* dY, const T* Yp, const int* row_of, const 
     (void)topk;
     gate_grad_kernel<T><<<T_ + E, kRowThreads, 0, s>>>(dY, Yp, row_of, gates, selsc, poff, counts,
                                                        T_, H, k, score, dYp, dz);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gate_dz(const float* dg_part, int nslots, const int* row_of, const float* gates,
+                           const float* selsc, int T_, int k, int score, float* dz, cudaStream_t s)
+{
+    gate_dz_kernel<<<(T_ + 7) / 8, 256, 0, s>>>(dg_part, nslots, row_of, gates, selsc, T_, k, score, dz);
     return cudaGetLastError();
 }
 

@@ -30,6 +30,26 @@ struct SwigluBwd {
     }
 };
 
+// Memory-efficient permutation ("Scalable Training of Mixture-of-Experts
+// Models with Megatron Core", §4, Memory-Efficient Permutation): the routing
+// weight g of a permuted row is folded into its activation before fc2,
+// h' = g h, so fc2 directly yields g y_e and Combine is a plain sum. In the
+// backward pass fc2 dgrad yields dh' = dY Wd^T for the row, and
+//   dg = <dh', h>,  dh = g dh',  then dA, dU as above;
+// h is recomputed from the saved a, u (and h' = g h for the fc2 weight
+// gradient), so neither h nor the expert outputs are kept between passes.
+struct SwigluBwdFold {
+    float dA, dU, h;
+    __device__ __forceinline__ SwigluBwdFold(float dhp, float g, float a, float u) {
+        const float s = sigmoid_f(a);
+        const float as = a * s;
+        h = as * u;
+        const float dh = g * dhp;
+        dU = dh * as;
+        dA = dh * u * s * (1.f + a * (1.f - s));
+    }
+};
+
 template <typename T> __device__ __forceinline__ T from_f32(float v);
 template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {

@@ -488,6 +488,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__
             } else if (arow < t.alloc_end) {
                 const bool valid = arow < t.valid_end;
                 const size_t orow = (size_t)arow * d.ldo;
+                // routing weight of the row when it is folded into h
+                const float grow = (d.gates && valid) ? d.gates[d.slot_of[arow]] : 1.f;
                 if (EPI == EPI_SWIGLU_FWD) {
                     __nv_bfloat16* O0 = static_cast<__nv_bfloat16*>(d.O0) + orow + col_lo;
                     __nv_bfloat16* O1 = static_cast<__nv_bfloat16*>(d.O1) + orow + col_lo;
@@ -501,7 +503,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__
                         for (int i = 0; i < 8; ++i) {
                             if (valid) {
                                 const SwigluFwd r(v[i], x[i]);
-                                hv[i] = r.h;
+                                hv[i] = r.h * grow;
                             } else {
                                 v[i] = x[i] = hv[i] = 0.f;
                             }
@@ -519,6 +521,10 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__
                         const __nv_bfloat16* X1 = static_cast<const __nv_bfloat16*>(d.X1) + o;
                         __nv_bfloat16* O0 = static_cast<__nv_bfloat16*>(d.O0) + o;
                         __nv_bfloat16* O1 = static_cast<__nv_bfloat16*>(d.O1) + o;
+                        const bool fold = d.gates != nullptr;
+                        // folded gates: g h (the fc2 weight-gradient operand), from registers
+                        __nv_bfloat16* O2 = fold && d.O2 ? static_cast<__nv_bfloat16*>(d.O2) + o : nullptr;
+                        float dgp = 0.f;
 #pragma unroll
                         for (int j0 = 0; j0 < 8; j0 += 2) {
                             uint4 ua[2], uu[2];
@@ -529,25 +535,41 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__
                             }
 #pragma unroll
                             for (int j = 0; j < 2; ++j) {
-                                uint4 oa, ou;
+                                uint4 oa, ou, oh;
                                 const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&ua[j]);
                                 const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&uu[j]);
                                 __nv_bfloat162* da2 = reinterpret_cast<__nv_bfloat162*>(&oa);
                                 __nv_bfloat162* du2 = reinterpret_cast<__nv_bfloat162*>(&ou);
+                                __nv_bfloat162* dh2 = reinterpret_cast<__nv_bfloat162*>(&oh);
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) {
                                     const float2 dh = unpack2(acc[32 * part + 4 * (j0 + j) + i]);
                                     const float2 av = __bfloat1622float2(a2[i]);
                                     const float2 uv = __bfloat1622float2(u2[i]);
-                                    const SwigluBwd r0(dh.x, av.x, uv.x);
-                                    const SwigluBwd r1(dh.y, av.y, uv.y);
                                     // pad rows (a = u = 0) give dA = dU = 0
-                                    da2[i] = __floats2bfloat162_rn(r0.dA, r1.dA);
-                                    du2[i] = __floats2bfloat162_rn(r0.dU, r1.dU);
+                                    if (fold) {
+                                        const SwigluBwdFold r0(dh.x, grow, av.x, uv.x);
+                                        const SwigluBwdFold r1(dh.y, grow, av.y, uv.y);
+                                        dgp = fmaf(dh.x, r0.h, dgp);
+                                        dgp = fmaf(dh.y, r1.h, dgp);
+                                        da2[i] = __floats2bfloat162_rn(r0.dA, r1.dA);
+                                        du2[i] = __floats2bfloat162_rn(r0.dU, r1.dU);
+                                        dh2[i] = __floats2bfloat162_rn(r0.h * grow, r1.h * grow);
+                                    } else {
+                                        const SwigluBwd r0(dh.x, av.x, uv.x);
+                                        const SwigluBwd r1(dh.y, av.y, uv.y);
+                                        da2[i] = __floats2bfloat162_rn(r0.dA, r1.dA);
+                                        du2[i] = __floats2bfloat162_rn(r0.dU, r1.dU);
+                                    }
                                 }
                                 *reinterpret_cast<uint4*>(O0 + 8 * (j0 + j)) = oa;
                                 *reinterpret_cast<uint4*>(O1 + 8 * (j0 + j)) = ou;
+                                if (O2) *reinterpret_cast<uint4*>(O2 + 8 * (j0 + j)) = oh;
                             }
+                        }
+                        if (fold) {
+                            const int col = part ? col_hi : col_lo;
+                            if (valid) d.dg_part[(size_t)arow * d.dg_ld + col / 64] = dgp;
                         }
                     }
                 } else {

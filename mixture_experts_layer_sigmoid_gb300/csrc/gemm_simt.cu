@@ -132,8 +132,13 @@ gemm_simt_kernel(const GemmDesc d)
     float* O2 = static_cast<float*>(d.O2);
     const float* X0 = static_cast<const float*>(d.X0);
     const float* X1 = static_cast<const float*>(d.X1);
+    const bool fold = d.gates != nullptr && d.sched == SCHED_ROWS;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
+        // folded routing weight of this row; dg partial over this tile's 64 columns
+        const int row_i = row0 + ty * 4 + i;
+        const float grow = (fold && d.sched == SCHED_ROWS && row_i < valid_end) ? d.gates[d.slot_of[row_i]] : 1.f;
+        float dgp = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int col = n0 + tx * 4 + j;
@@ -154,19 +159,32 @@ gemm_simt_kernel(const GemmDesc d)
                 SwigluFwd r(acc[0][i][j], acc[NACC - 1][i][j]);
                 O0[o] = valid ? r.a : 0.f;
                 O1[o] = valid ? r.u : 0.f;
-                O2[o] = valid ? r.h : 0.f;
+                O2[o] = valid ? r.h * grow : 0.f;
             } else if (d.epi == EPI_SWIGLU_BWD) {
-                if (valid) {
+                if (valid && fold) {
+                    SwigluBwdFold r(acc[0][i][j], grow, X0[o], X1[o]);
+                    O0[o] = r.dA;
+                    O1[o] = r.dU;
+                    dgp = fmaf(acc[0][i][j], r.h, dgp);
+                    if (O2) O2[o] = r.h * grow;
+                } else if (valid) {
                     SwigluBwd r(acc[0][i][j], X0[o], X1[o]);
                     O0[o] = r.dA;
                     O1[o] = r.dU;
                 } else {
                     O0[o] = 0.f;
                     O1[o] = 0.f;
+                    if (fold && O2) O2[o] = 0.f;
                 }
             } else {
                 O0[o] = valid ? acc[0][i][j] : 0.f;
             }
+        }
+        if (fold && d.epi == EPI_SWIGLU_BWD) {
+            // the 16 threads of a half-warp (tx) share these rows
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) dgp += __shfl_xor_sync(0xffffffffu, dgp, off);
+            if (tx == 0 && row_i < valid_end) d.dg_part[(size_t)row_i * d.dg_ld + n0 / 64] = dgp;
         }
     }
 }

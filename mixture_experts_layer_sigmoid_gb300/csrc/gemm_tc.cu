@@ -423,6 +423,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                 const bool warp_in = t.row0 + q * 32 < t.alloc_end;
                 if (EPI == EPI_SWIGLU_FWD) {
                     // 64-column units of a (gate half), u (up half) and h = silu(a) u
+                    // (g h with the routing weight folded in)
+                    const float grow = (d.gates && valid) ? d.gates[d.slot_of[row]] : 1.f;
 #pragma unroll 1
                     for (int u = 0; u < NW / 64; ++u) {
                         float g0[32], g1[32], u0[32], u1[32], h0[32], h1[32];
@@ -436,8 +438,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                                 if (valid) {
                                     SwigluFwd r0(g0[i], u0[i]);
                                     SwigluFwd r1(g1[i], u1[i]);
-                                    h0[i] = r0.h;
-                                    h1[i] = r1.h;
+                                    h0[i] = r0.h * grow;
+                                    h1[i] = r1.h * grow;
                                 } else {
                                     g0[i] = g1[i] = u0[i] = u1[i] = h0[i] = h1[i] = 0.f;
                                 }
@@ -449,6 +451,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                         }
                     }
                 } else if (EPI == EPI_SWIGLU_BWD) {
+                    const bool fold = d.gates != nullptr;
+                    const float grow = (fold && valid) ? d.gates[d.slot_of[row]] : 1.f;
 #pragma unroll 1
                     for (int u = 0; u < NW / 64; ++u) {
                         float d0[32], d1[32], e0[32], e1[32];
@@ -456,28 +460,48 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                         tmem_load32f(taddr + u * 64 + 32, d1);
                         if (warp_in) {
                             const size_t o = (size_t)row * d.ldo + t.n * NW + u * 64;
+                            const __nv_bfloat16* X0 = static_cast<const __nv_bfloat16*>(d.X0) + o;
+                            const __nv_bfloat16* X1 = static_cast<const __nv_bfloat16*>(d.X1) + o;
+                            float dgp = 0.f;
+                            // folded gates: g h of these columns (the fc2 weight-gradient
+                            // operand) is written by this thread straight from registers
+                            __nv_bfloat16* Hp = fold && d.O2 ? static_cast<__nv_bfloat16*>(d.O2) + o : nullptr;
                             if (valid) {
                                 float av[32], uv[32];
-                                load32_bf16(static_cast<const __nv_bfloat16*>(d.X0) + o, av);
-                                load32_bf16(static_cast<const __nv_bfloat16*>(d.X1) + o, uv);
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) {
-                                    SwigluBwd r(d0[i], av[i], uv[i]);
-                                    d0[i] = r.dA; e0[i] = r.dU;
-                                }
-                                load32_bf16(static_cast<const __nv_bfloat16*>(d.X0) + o + 32, av);
-                                load32_bf16(static_cast<const __nv_bfloat16*>(d.X1) + o + 32, uv);
+                                for (int hf = 0; hf < 2; ++hf) {
+                                    float (&dd)[32] = hf ? d1 : d0;
+                                    float (&ee)[32] = hf ? e1 : e0;
+                                    load32_bf16(X0 + 32 * hf, av);
+                                    load32_bf16(X1 + 32 * hf, uv);
+                                    if (fold) {
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) {
-                                    SwigluBwd r(d1[i], av[i], uv[i]);
-                                    d1[i] = r.dA; e1[i] = r.dU;
+                                        for (int i = 0; i < 32; ++i) {
+                                            const SwigluBwdFold r(dd[i], grow, av[i], uv[i]);
+                                            dgp = fmaf(dd[i], r.h, dgp);
+                                            dd[i] = r.dA; ee[i] = r.dU;
+                                            av[i] = r.h * grow;
+                                        }
+                                        if (Hp) store32_bf16(Hp + 32 * hf, av);
+                                    } else {
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i) {
+                                            const SwigluBwd r(dd[i], av[i], uv[i]);
+                                            dd[i] = r.dA; ee[i] = r.dU;
+                                        }
+                                    }
                                 }
                             } else {
                                 zero32(d0); zero32(d1); zero32(e0); zero32(e1);
+                                if (Hp) {
+                                    store32_bf16(Hp, d0);
+                                    store32_bf16(Hp + 32, d0);
+                                }
                             }
                             const int col = t.n * NW + u * 64, y = t.row0 + q * 32;
                             stage_store(&mO0, d0, d1, col, y);
                             stage_store(&mO1, e0, e1, col, y);
+                            if (fold && valid) d.dg_part[(size_t)row * d.dg_ld + col / 64] = dgp;
                         }
                     }
                 } else {

@@ -81,6 +81,15 @@ struct GemmDesc {
     const float* SA0; const float* SA1; int lds_a;   // A: 1x128 blocks along K
     const float* SB0; const float* SB1; int lds_b;   // B: 128x128 blocks
     int rows_cap;   // SCHED_WGRAD: row capacity of the transposed operands
+    // memory-efficient permutation (gates != null): g of permuted row r is
+    // gates[slot_of[r]]. SWIGLU_FWD stores O2 = g h; SWIGLU_BWD treats the
+    // accumulator as dh', writes dA, dU of dh = g dh', O2 = g h (if O2 is
+    // set) and dg_part[r][c / 64] = sum over the 64 columns from c of dh' h
+    // (row stride dg_ld floats).
+    const int* slot_of;
+    const float* gates;
+    float* dg_part;
+    int dg_ld;
 };
 
 // Launchers (return cudaGetLastError()).
@@ -111,6 +120,9 @@ cudaError_t launch_gate_grad(const T* dY, const T* Yp, const int* row_of, const 
                              const float* gates, const float* selsc, const int* poff,
                              const int* counts, int T_, int H, int E, int k, int score, T* dYp,
                              float* dz, cudaStream_t s);
+// Folded routing weights: dz from the fc2-dgrad partial dot products.
+cudaError_t launch_gate_dz(const float* dg_part, int nslots, const int* row_of, const float* gates,
+                           const float* selsc, int T_, int k, int score, float* dz, cudaStream_t s);
 template <typename T>
 cudaError_t launch_router_wgrad(const T* Xp, const int* slot_of, const int* poff,
                                 const int* counts, const float* dz, int H, int E, int k,

@@ -26,9 +26,21 @@ __device__ __forceinline__ float block_scale(float amax)
     return amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f);
 }
 
-__device__ __forceinline__ uint8_t e4m3(float v, float s)
+// E4M3(v / s), rounded to nearest even and saturated, given r = 1/s rounded
+// to nearest. y = v r is within two units in the last place of the rounded
+// quotient, so both round to the same E4M3 value unless y lies within a few
+// units of a rounding midpoint (the 20 mantissa bits E4M3 drops are within 4
+// of half) or below the E4M3 normal range, where the rounding position moves;
+// those rare values take the IEEE division itself.
+__device__ __forceinline__ uint8_t e4m3(float v, float s, float r)
 {
-    return (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(v, s), __NV_SATFINITE, __NV_E4M3);
+    float y = v * r;
+    const uint32_t b = __float_as_uint(y) & 0x7fffffffu;
+    if (b != 0u) {
+        const int dist = (int)(b & 0xFFFFFu) - 0x80000;
+        if ((b >> 23) < 121u || (dist >= -4 && dist <= 4)) y = __fdiv_rn(v, s);
+    }
+    return (uint8_t)__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
 }
 
 // 8 bf16 -> 8 fp32
@@ -45,11 +57,12 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8])
 
 __device__ __forceinline__ uint2 codes8(const float (&v)[8], float s)
 {
+    const float r = __frcp_rn(s);
     uint32_t lo = 0, hi = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) lo |= (uint32_t)e4m3(v[i], s) << (8 * i);
+    for (int i = 0; i < 4; ++i) lo |= (uint32_t)e4m3(v[i], s, r) << (8 * i);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) hi |= (uint32_t)e4m3(v[4 + i], s) << (8 * i);
+    for (int i = 0; i < 4; ++i) hi |= (uint32_t)e4m3(v[4 + i], s, r) << (8 * i);
     return make_uint2(lo, hi);
 }
 
@@ -126,6 +139,113 @@ quant_rows_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__ 
     }
 }
 
+// ---- 128x128 tiles: bf16 tile and its codes staged in shared memory.
+// Codes are kept row-major with 144-byte rows; the 16-byte chunk k of row r
+// sits at chunk k ^ ((r / 16) % 8), which makes the transposed read-out
+// (4 columns x 16 rows per thread) free of bank conflicts.
+constexpr int kQS = 144;
+__device__ __forceinline__ int qs_off(int r, int byte)
+{
+    return r * kQS + ((((byte >> 4) ^ (r >> 4)) & 7) << 4) + (byte & 15);
+}
+
+// Load a 128x128 bf16 tile (row stride ld elements) into tile[][136]; returns
+// this thread's amax over the 64 values it loaded.
+__device__ __forceinline__ float load_tile(const __nv_bfloat16* __restrict__ src, size_t ld,
+                                           __nv_bfloat16 (*tile)[136])
+{
+    uint4 u[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int i = threadIdx.x + 256 * j, rr = i >> 4, vv = i & 15;
+        u[j] = reinterpret_cast<const uint4*>(src + (size_t)rr * ld)[vv];
+    }
+    float a = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int i = threadIdx.x + 256 * j, rr = i >> 4, vv = i & 15;
+        *reinterpret_cast<uint4*>(&tile[rr][vv * 8]) = u[j];
+        float f[8];
+        unpack8(u[j], f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) a = fmaxf(a, fabsf(f[q]));
+    }
+    return a;
+}
+
+// max over the 256 threads of the block (red: 8 floats of shared memory)
+__device__ __forceinline__ float block_max(float a, float* red)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+    __syncthreads();
+    a = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) a = fmaxf(a, red[w]);
+    return a;
+}
+
+// Row-wise encoding: thread -> row t/2, columns 64 (t%2) + [0, 64), each
+// divided by its column's scale (sc_col, reciprocals rc_col) or the tile's
+// (sc_col == null).
+// Codes go to qs and, when dst is given, to dst (row stride ld bytes).
+__device__ __forceinline__ void encode_rows(__nv_bfloat16 (*tile)[136], float sc, const float* sc_col,
+                                            const float* rc_col, uint8_t* qs, uint8_t* dst, size_t ld)
+{
+    const int rr = threadIdx.x >> 1, hf = threadIdx.x & 1;
+    const float rc = __frcp_rn(sc);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const int c0 = hf * 64 + g * 16;
+        float f[16];
+        unpack8(*reinterpret_cast<const uint4*>(&tile[rr][c0]), *reinterpret_cast<float(*)[8]>(f));
+        unpack8(*reinterpret_cast<const uint4*>(&tile[rr][c0 + 8]), *reinterpret_cast<float(*)[8]>(f + 8));
+        uint32_t w[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int c = 4 * q4 + b;
+                word |= (uint32_t)(sc_col ? e4m3(f[c], sc_col[c0 + c], rc_col[c0 + c]) : e4m3(f[c], sc, rc))
+                        << (8 * b);
+            }
+            w[q4] = word;
+        }
+        const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(qs + qs_off(rr, c0)) = v;
+        if (dst) *reinterpret_cast<uint4*>(dst + (size_t)rr * ld + c0) = v;
+    }
+}
+
+// Transposed write-out of the staged codes: thread -> columns 4 (t/8) + [0, 4),
+// rows 16 (t%8) + [0, 16); dst row c (= tile column c) has stride ldT bytes.
+// Eight consecutive threads complete one 128-byte line of an output row.
+__device__ __forceinline__ void write_transposed(const uint8_t* qs, uint8_t* dstT, size_t ldT)
+{
+    const int cg = threadIdx.x >> 3, ch = threadIdx.x & 7;
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = *reinterpret_cast<const uint32_t*>(qs + qs_off(16 * ch + i, 4 * cg));
+    uint32_t o[4][4];   // [column j][group of 4 rows]
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const uint32_t lo01 = __byte_perm(w[4 * g], w[4 * g + 1], 0x5140);
+        const uint32_t hi01 = __byte_perm(w[4 * g], w[4 * g + 1], 0x7362);
+        const uint32_t lo23 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x5140);
+        const uint32_t hi23 = __byte_perm(w[4 * g + 2], w[4 * g + 3], 0x7362);
+        o[0][g] = __byte_perm(lo01, lo23, 0x5410);
+        o[1][g] = __byte_perm(lo01, lo23, 0x7632);
+        o[2][g] = __byte_perm(hi01, hi23, 0x5410);
+        o[3][g] = __byte_perm(hi01, hi23, 0x7632);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(dstT + (size_t)(4 * cg + j) * ldT + 16 * ch) =
+            make_uint4(o[j][0], o[j][1], o[j][2], o[j][3]);
+}
+
 // Tile (128 rows x 128 columns) of in [rows][C] -> qT [C][rows_cap].
 // tiles == 0: one scale per column of the tile, sT[c][rb] (row stride
 // rows_cap/128); tiles == 1: one scale per tile, sT[cb][rb].
@@ -135,52 +255,36 @@ quant_t_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__ row
                float* __restrict__ sT)
 {
     __shared__ __align__(16) __nv_bfloat16 tile[128][136];
+    __shared__ __align__(16) uint8_t qs[128 * kQS];
     __shared__ float red[256];
+    __shared__ float scol[128], rcol[128];
     const int cb = blockIdx.x, rb = blockIdx.y;
     const int r0 = rb * 128, c0 = cb * 128;
     if (r0 >= (rows_dev ? *rows_dev : rows_fixed)) return;
-    // load 128 x 128 (16 vectors of 8 per row)
-    for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
-        const int rr = i / 16, vv = i % 16;
-        *reinterpret_cast<uint4*>(&tile[rr][vv * 8]) =
-            reinterpret_cast<const uint4*>(in + (size_t)(r0 + rr) * C + c0)[vv];
-    }
-    __syncthreads();
-    // column amax: threads (c = tid % 128, half = tid / 128) over 64 rows each
-    const int c = threadIdx.x & 127, half = threadIdx.x >> 7;
-    float a = 0.f;
-    for (int rr = half * 64; rr < half * 64 + 64; ++rr) a = fmaxf(a, fabsf(__bfloat162float(tile[rr][c])));
-    red[threadIdx.x] = a;
-    __syncthreads();
-    float sc;
+    const float at = load_tile(in + (size_t)r0 * C + c0, C, tile);
+    float sc = 0.f;
     if (tiles) {
-        if (threadIdx.x < 128) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + 128]);
-        __syncthreads();
-        for (int off = 64; off > 0; off >>= 1) {
-            if (threadIdx.x < off) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + off]);
-            __syncthreads();
-        }
-        sc = block_scale(red[0]);
+        sc = block_scale(block_max(at, red));
         if (threadIdx.x == 0) sT[(size_t)cb * (rows_cap / 128) + rb] = sc;
     } else {
-        sc = block_scale(fmaxf(red[c], red[c + 128]));
-        if (half == 0) sT[(size_t)(c0 + c) * (rows_cap / 128) + rb] = sc;
-    }
-    // column c -> output row c0 + c, bytes [r0 + 64 half, +64)
-    uint8_t* dst = qT + (size_t)(c0 + c) * rows_cap + r0 + half * 64;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        uint32_t w[4];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-                word |= (uint32_t)e4m3(__bfloat162float(tile[half * 64 + g * 16 + q4 * 4 + b][c]), sc) << (8 * b);
-            w[q4] = word;
+        __syncthreads();
+        // column amax: threads (c = tid % 128, half = tid / 128) over 64 rows each
+        const int c = threadIdx.x & 127, half = threadIdx.x >> 7;
+        float a = 0.f;
+        for (int rr = half * 64; rr < half * 64 + 64; ++rr) a = fmaxf(a, fabsf(__bfloat162float(tile[rr][c])));
+        red[threadIdx.x] = a;
+        __syncthreads();
+        if (half == 0) {
+            const float s1 = block_scale(fmaxf(red[c], red[c + 128]));
+            scol[c] = s1;
+            rcol[c] = __frcp_rn(s1);
+            sT[(size_t)(c0 + c) * (rows_cap / 128) + rb] = s1;
         }
-        reinterpret_cast<uint4*>(dst)[g] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+    __syncthreads();
+    encode_rows(tile, tiles ? sc : 1.f, tiles ? nullptr : scol, rcol, qs, nullptr, 0);
+    __syncthreads();
+    write_transposed(qs, qT + (size_t)c0 * rows_cap + r0, rows_cap);
 }
 
 // 128x128 block (rb, cb) of expert e of W [E][R][C] -> codes in both
@@ -190,65 +294,19 @@ quant_w_kernel(const __nv_bfloat16* __restrict__ W, int R, int C, uint8_t* __res
                float* __restrict__ s, uint8_t* __restrict__ qT, float* __restrict__ sT)
 {
     __shared__ __align__(16) __nv_bfloat16 tile[128][136];
-    __shared__ float red[256];
+    __shared__ __align__(16) uint8_t qs[128 * kQS];
+    __shared__ float red[8];
     const int cb = blockIdx.x, rb = blockIdx.y, e = blockIdx.z;
     const size_t base = (size_t)e * R * C;
     const int r0 = rb * 128, c0 = cb * 128;
-    float a = 0.f;
-    for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
-        const int rr = i / 16, vv = i % 16;
-        const uint4 u = reinterpret_cast<const uint4*>(W + base + (size_t)(r0 + rr) * C + c0)[vv];
-        *reinterpret_cast<uint4*>(&tile[rr][vv * 8]) = u;
-        float f[8];
-        unpack8(u, f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(f[j]));
-    }
-    red[threadIdx.x] = a;
-    __syncthreads();
-    for (int off = 128; off > 0; off >>= 1) {
-        if (threadIdx.x < off) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + off]);
-        __syncthreads();
-    }
-    const float sc = block_scale(red[0]);
+    const float sc = block_scale(block_max(load_tile(W + base + (size_t)r0 * C + c0, C, tile), red));
     if (threadIdx.x == 0) {
         s[((size_t)e * (R / 128) + rb) * (C / 128) + cb] = sc;
         sT[((size_t)e * (C / 128) + cb) * (R / 128) + rb] = sc;
     }
-    // original orientation: thread -> (row, 64 columns)
-    {
-        const int rr = threadIdx.x >> 1, hf = threadIdx.x & 1;
-        uint8_t* dst = q + base + (size_t)(r0 + rr) * C + c0 + hf * 64;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            uint32_t w[4];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t word = 0;
-#pragma unroll
-                for (int b = 0; b < 4; ++b) word |= (uint32_t)e4m3(__bfloat162float(tile[rr][hf * 64 + g * 16 + q4 * 4 + b]), sc) << (8 * b);
-                w[q4] = word;
-            }
-            reinterpret_cast<uint4*>(dst)[g] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    }
-    // transposed: thread -> (column, 64 rows)
-    {
-        const int cc = threadIdx.x >> 1, hf = threadIdx.x & 1;
-        uint8_t* dst = qT + base + (size_t)(c0 + cc) * R + r0 + hf * 64;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            uint32_t w[4];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t word = 0;
-#pragma unroll
-                for (int b = 0; b < 4; ++b) word |= (uint32_t)e4m3(__bfloat162float(tile[hf * 64 + g * 16 + q4 * 4 + b][cc]), sc) << (8 * b);
-                w[q4] = word;
-            }
-            reinterpret_cast<uint4*>(dst)[g] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    }
+    encode_rows(tile, sc, nullptr, nullptr, qs, q + base + (size_t)r0 * C + c0, C);
+    __syncthreads();
+    write_transposed(qs, qT + base + (size_t)c0 * R + r0, R);
 }
 
 }  // namespace
@@ -264,6 +322,7 @@ cudaError_t launch_permute_quant(const __nv_bfloat16* x, const int* row_of, cons
 cudaError_t launch_quant_rows(const __nv_bfloat16* in, const int* rows_dev, int rows_max, int C,
                               uint8_t* q, float* sc, cudaStream_t s)
 {
+    if (rows_max <= 0) return cudaSuccess;
     quant_rows_kernel<<<rows_max, 128, 0, s>>>(in, rows_dev, rows_max, C, q, sc);
     return cudaGetLastError();
 }

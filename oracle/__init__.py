@@ -282,8 +282,10 @@ def fp8_quantize(X, mode):
 
 
 def layer_fp8(x, Wr, Wg, Wu, Wd, topk, gates, scores, score, dY=None, Wsg=None, Wsu=None,
-              Wsd=None):
-    """Blockwise-FP8 layer: y, and when dY is given every gradient."""
+              Wsd=None, fold=False):
+    """Blockwise-FP8 layer: y, and when dY is given every gradient. fold: the
+    memory-efficient permutation's order (routing weight folded into h
+    before fc2), with its rounding points."""
     lib = _load()
     x, Wr, Wg, Wu, Wd = _f64(x), _f64(Wr), _f64(Wg), _f64(Wu), _f64(Wd)
     Wsg, Wsu, Wsd = _f64(Wsg), _f64(Wsu), _f64(Wsd)
@@ -303,7 +305,7 @@ def layer_fp8(x, Wr, Wg, Wu, Wd, topk, gates, scores, score, dY=None, Wsg=None, 
                               _d(out["y"]), _d(out.get("dX")), _d(out.get("dWr")),
                               _d(out.get("dWg")), _d(out.get("dWu")), _d(out.get("dWd")),
                               _d(out.get("dWsg")), _d(out.get("dWsu")), _d(out.get("dWsd")),
-                              _d(out.get("dg")))
+                              _d(out.get("dg")), 1 if fold else 0)
     if rc:
         raise ValueError("oracle_layer_fp8: bad arguments")
     return out

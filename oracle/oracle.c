@@ -828,9 +828,18 @@ static void gemm_nt(int M, int N, int K, const double* A, const double* B, doubl
  * written when dYr != NULL (dYr are the rows' output gradients, already
  * gate-scaled).
  */
+/*
+ * g != NULL: memory-efficient permutation ("Scalable Training of
+ * Mixture-of-Experts Models with Megatron Core", §4: the routing weight is
+ * folded into the activation by an algebraic rearrangement). Row r's fc2
+ * input is h'_r = g_r h_r (rounded to bf16), so Y holds g_r y_r; dYr is then
+ * the unweighted output gradient, dh' = dYr Wd^T, dg_r = <dh'_r, h_r> (h from
+ * the bf16-stored a, u, as the backward pass recomputes it), dh = g_r dh',
+ * and the fc2 weight gradient uses h' recomputed from the stored a, u.
+ */
 static void swiglu_fp8(int M, int H, int F, const double* X, const double* Wg, const double* Wu,
                        const double* Wd, double* Y, const double* dYr, double* dX, double* dWg,
-                       double* dWu, double* dWd)
+                       double* dWu, double* dWd, const double* g, double* dg)
 {
     size_t mf = (size_t)(M > 0 ? M : 1) * F, mh = (size_t)(M > 0 ? M : 1) * H;
     double* Xq = dup(X, (size_t)M * H);
@@ -847,7 +856,8 @@ static void swiglu_fp8(int M, int H, int F, const double* X, const double* Wg, c
     gemm(M, F, H, Xq, Wgq, A);
     gemm(M, F, H, Xq, Wuq, U);
     for (size_t i = 0; i < (size_t)M * F; ++i) {
-        Hh[i] = bf16r(silu(A[i]) * U[i]);   /* from the GEMM outputs themselves */
+        const double gr = g ? g[i / F] : 1.0;
+        Hh[i] = bf16r(gr * silu(A[i]) * U[i]);   /* from the GEMM outputs themselves */
         A[i] = bf16r(A[i]);
         U[i] = bf16r(U[i]);
     }
@@ -864,6 +874,19 @@ static void swiglu_fp8(int M, int H, int F, const double* X, const double* Wg, c
         gemm_nt(M, F, H, dYq, Wdq, dh);
         double* dA = (double*)malloc(sizeof(double) * mf);
         double* dU = (double*)malloc(sizeof(double) * mf);
+        if (g) {
+            for (int r = 0; r < M; ++r) {
+                double acc = 0.0;
+                for (int f = 0; f < F; ++f) {
+                    const size_t i = (size_t)r * F + f;
+                    const double hr = silu(A[i]) * U[i];
+                    acc += dh[i] * hr;
+                    dh[i] *= g[r];
+                    Hh[i] = bf16r(g[r] * hr);   /* h' recomputed for the weight gradient */
+                }
+                dg[r] = acc;
+            }
+        }
         for (size_t i = 0; i < (size_t)M * F; ++i) {
             dA[i] = bf16r(dh[i] * U[i] * dsilu(A[i]));
             dU[i] = bf16r(dh[i] * silu(A[i]));
@@ -910,7 +933,7 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
                      const int* topk, const double* gates, const double* scores,
                      const double* dY, double* y,
                      double* dX, double* dWr, double* dWg, double* dWu, double* dWd,
-                     double* dWsg, double* dWsu, double* dWsd, double* dg_out)
+                     double* dWsg, double* dWsu, double* dWsd, double* dg_out, int fold)
 {
     if (T <= 0 || H <= 0 || H % 128 || E <= 0 || k <= 0 || k > E || k > 1024 || F <= 0 ||
         F % 128 || Fs < 0 || Fs % 128)
@@ -921,6 +944,9 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
     int* row_of = (int*)malloc(sizeof(int) * R);
     int* slot_of = (int*)malloc(sizeof(int) * R);
     if (oracle_dispatch(T, E, k, topk, counts, offsets, row_of, slot_of)) return -1;
+    /* routing weight of each permuted row (folded variant) */
+    double* grow = (double*)malloc(sizeof(double) * (size_t)R);
+    for (int r = 0; r < R; ++r) grow[r] = gates[slot_of[r]];
     double* Xp = (double*)malloc(sizeof(double) * (size_t)R * H);
     double* Yp = (double*)malloc(sizeof(double) * (size_t)R * H);
     double* dYp = (double*)malloc(sizeof(double) * (size_t)R * H);
@@ -934,31 +960,33 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
         if (M == 0) continue;
         swiglu_fp8(M, H, F, Xp + (size_t)offsets[e] * H, Wg + (size_t)e * H * F,
                    Wu + (size_t)e * H * F, Wd + (size_t)e * F * H, Yp + (size_t)offsets[e] * H,
-                   NULL, NULL, NULL, NULL, NULL);
+                   NULL, NULL, NULL, NULL, NULL, fold ? grow + offsets[e] : NULL, NULL);
     }
     for (int t = 0; t < T; ++t)
         for (int h = 0; h < H; ++h) {
             double acc = 0.0;
             for (int j = 0; j < k; ++j)
-                acc += gates[(size_t)t * k + j] * Yp[(size_t)row_of[(size_t)t * k + j] * H + h];
+                acc += (fold ? 1.0 : gates[(size_t)t * k + j]) *
+                       Yp[(size_t)row_of[(size_t)t * k + j] * H + h];
             y[(size_t)t * H + h] = acc;
         }
     double* Ys = NULL;
     if (Fs > 0) {
         Ys = (double*)malloc(sizeof(double) * (size_t)T * H);
-        swiglu_fp8(T, H, Fs, x, Wsg, Wsu, Wsd, Ys, NULL, NULL, NULL, NULL, NULL);
+        swiglu_fp8(T, H, Fs, x, Wsg, Wsu, Wsd, Ys, NULL, NULL, NULL, NULL, NULL, NULL, NULL);
         for (size_t i = 0; i < (size_t)T * H; ++i) y[i] += Ys[i];
     }
     if (dY) {
         for (int r = 0; r < R; ++r) {
             int t = slot_of[r] / k;
-            double g = gates[slot_of[r]], acc = 0.0;
+            double g = fold ? 1.0 : gates[slot_of[r]], acc = 0.0;
             for (int h = 0; h < H; ++h) {
                 acc += dY[(size_t)t * H + h] * Yp[(size_t)r * H + h];
                 dYp[(size_t)r * H + h] = bf16r(g * dY[(size_t)t * H + h]);
             }
-            dg[slot_of[r]] = acc;
+            dg[slot_of[r]] = acc;   /* folded: replaced below by <dh', h> */
         }
+        double* dgr = fold ? (double*)malloc(sizeof(double) * (size_t)R) : NULL;
         double* Ytmp = (double*)malloc(sizeof(double) * (size_t)(R > T ? R : T) * H);
         for (int e = 0; e < E; ++e) {
             int M = counts[e];
@@ -974,7 +1002,11 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
             swiglu_fp8(M, H, F, Xp + (size_t)offsets[e] * H, Wg + (size_t)e * H * F,
                        Wu + (size_t)e * H * F, Wd + (size_t)e * F * H, Ytmp,
                        dYp + (size_t)offsets[e] * H, dXp + (size_t)offsets[e] * H, dWg_e, dWu_e,
-                       dWd_e);
+                       dWd_e, fold ? grow + offsets[e] : NULL, fold ? dgr + offsets[e] : NULL);
+        }
+        if (fold) {
+            for (int r = 0; r < R; ++r) dg[slot_of[r]] = dgr[r];
+            free(dgr);
         }
         double* dz = (double*)calloc((size_t)T * E, sizeof(double));
         for (int t = 0; t < T; ++t) {
@@ -1000,7 +1032,7 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
             }
         if (Fs > 0) {
             double* dXs = (double*)malloc(sizeof(double) * (size_t)T * H);
-            swiglu_fp8(T, H, Fs, x, Wsg, Wsu, Wsd, Ytmp, dY, dXs, dWsg, dWsu, dWsd);
+            swiglu_fp8(T, H, Fs, x, Wsg, Wsu, Wsd, Ytmp, dY, dXs, dWsg, dWsu, dWsd, NULL, NULL);
             for (size_t i = 0; i < (size_t)T * H; ++i) dX[i] += dXs[i];
             free(dXs);
         }
@@ -1008,7 +1040,7 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
         free(dz);
         if (dg_out) memcpy(dg_out, dg, sizeof(double) * (size_t)R);
     }
-    free(Ys); free(Xp); free(Yp); free(dYp); free(dXp); free(dg);
+    free(Ys); free(Xp); free(Yp); free(dYp); free(dXp); free(dg); free(grow);
     free(counts); free(offsets); free(row_of); free(slot_of);
     return 0;
 }

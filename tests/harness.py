@@ -176,12 +176,14 @@ def upload(inp, device="cuda"):
     return {k: (None if v is None else v.to(device)) for k, v in inp.items()}
 
 
-def run_gpu(w: mi.Workload, inp, layer=None, backward=True):
-    """Forward (+ backward) through the C ABI; returns host copies."""
+def run_gpu(w: mi.Workload, inp, layer=None, backward=True, fold=False):
+    """Forward (+ backward) through the C ABI; returns host copies. fold:
+    memory-efficient permutation (routing weights folded into h)."""
     from mixture_experts_layer_sigmoid_gb300 import MoELayer
     g = upload(inp)
     if layer is None:
-        layer = MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=w.dtype, Fs=w.Fs)
+        layer = MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=w.dtype, Fs=w.Fs,
+                         fold_gates=fold)
     y, r = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"], g["Wsg"], g["Wsu"],
                          g["Wsd"], routing=True)
     out = dict(y=y, **r)
@@ -266,9 +268,9 @@ def compare_all(w, inp, r, gpu, ref, backward=True):
     return report
 
 
-def full_parity(w: mi.Workload, backward=True):
+def full_parity(w: mi.Workload, backward=True, fold=False):
     inp = mi.make_inputs(w, "cpu", with_grad_out=backward)
-    gpu, layer = run_gpu(w, inp, backward=backward)
+    gpu, layer = run_gpu(w, inp, backward=backward, fold=fold)
     r, nties = check_routing(w, inp, gpu)
     np.testing.assert_allclose(gpu["gates"].numpy(), r["gates"], rtol=1e-4, atol=1e-6)
     ref = oracle_layer(w, inp, r, backward)

@@ -49,7 +49,7 @@ def _cfg(**kw):
 @pytest.mark.parametrize("bad", [dict(H=100), dict(H=0), dict(F=200), dict(Fs=64), dict(E=0),
                                  dict(E=257), dict(top_k=0), dict(top_k=9), dict(top_k=9, E=16),
                                  dict(E=2, top_k=3), dict(T_max=0), dict(score=2), dict(dtype=7),
-                                 dict(flags=2)])
+                                 dict(flags=4), dict(flags=8)])
 def test_plan_create_rejects_bad_configs(lib, bad):
     plan = ctypes.c_void_p()
     st = lib.moe_plan_create(ctypes.byref(_cfg(**bad)), 0, ctypes.byref(plan))

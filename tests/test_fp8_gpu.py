@@ -74,10 +74,22 @@ FP8_CASES = {
 
 @pytest.mark.parametrize("name", list(FP8_CASES))
 def test_fp8_layer_matches_oracle(name):
+    _fp8_parity(name, False)
+
+
+@pytest.mark.parametrize("name", ["qwen_fp8_small", "qwen_fp8_rows_in_cta_pairs"])
+def test_fp8_folded_gates_match_oracle(name):
+    """Memory-efficient permutation on the FP8 layer: g h is quantised for
+    fc2 instead of h; the same deviation bounds hold."""
+    _fp8_parity(name, True)
+
+
+def _fp8_parity(name, fold):
     w = FP8_CASES[name]
     inp = mi.make_inputs(w)
     g = upload(inp)
-    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=moe.MOE_FP8_BLOCK)
+    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=moe.MOE_FP8_BLOCK,
+                         fold_gates=fold)
     y, rt = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"], routing=True)
     gr = layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
     torch.cuda.synchronize()
@@ -91,7 +103,7 @@ def test_fp8_layer_matches_oracle(name):
     if mism.any():
         r = oracle.route(d["x"], d["Wr"], d["b"], w.k, w.score, replay_topk=gt, replay_mask=mism)
     ref = oracle.layer_fp8(d["x"], d["Wr"], d["Wg"], d["Wu"], d["Wd"], r["topk"], r["gates"],
-                           r["scores"], w.score, d["dY"])
+                           r["scores"], w.score, d["dY"], fold=fold)
     rep = {}
     for gname, oname in (("y", "y"), ("dX", "dX")):
         got = to_np(y if gname == "y" else gr[gname])

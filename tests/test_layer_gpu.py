@@ -35,6 +35,29 @@ def test_layer_matches_oracle(name):
     print(name, rep)
 
 
+# Memory-efficient permutation: the same layer with the routing weights
+# folded into the expert activations must meet the same bounds.
+FOLD_CASES = ["tiny_fp32", "mixtral_small", "deepseek_small", "qwen_small_ragged_n",
+              "fp32_sigmoid_shared", "rows_in_cta_pairs", "deepseek_e256_sigmoid_shared"]
+
+
+@pytest.mark.parametrize("name", FOLD_CASES)
+def test_folded_gates_match_oracle(name):
+    rep, _ = full_parity(CASES[name], fold=True)
+    print(name, "folded", rep)
+
+
+def test_folded_gates_shrink_saved_buffer():
+    import mixture_experts_layer_sigmoid_gb300 as moe
+    w = CASES["deepseek_small"]
+    a = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, Fs=w.Fs)
+    b = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, Fs=w.Fs, fold_gates=True)
+    sa, _ = moe.moe_workspace_size(a.plan, w.T)
+    sb, _ = moe.moe_workspace_size(b.plan, w.T)
+    rp = -(-(w.T * w.k + w.E * 127) // 128) * 128     # row capacity of the permuted buffers
+    assert sa - sb >= 2 * rp * (w.F + w.H) - 2 * 256, (sa, sb)
+
+
 def test_empty_experts_get_zero_gradients():
     w = mi.scaled(W["mixtral_8x7b"], T=200, H=256, E=8, k=2, F=256)
     inp = mi.make_inputs(w)

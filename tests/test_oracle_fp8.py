@@ -93,12 +93,15 @@ def _layer(T, H, E, k, F, Fs, score, seed):
     return p
 
 
-@pytest.mark.parametrize("score,Fs", [(oracle.SOFTMAX, 0), (oracle.SIGMOID, 128)])
-def test_fp8_layer_tracks_the_exact_layer(score, Fs):
+@pytest.mark.parametrize("score,Fs,fold", [(oracle.SOFTMAX, 0, False), (oracle.SIGMOID, 128, False),
+                                           (oracle.SOFTMAX, 0, True), (oracle.SIGMOID, 128, True)])
+def test_fp8_layer_tracks_the_exact_layer(score, Fs, fold):
+    """Both rounding orders (routing weight applied after fc2, or folded into
+    h before it) stay within the E4M3 deviation scale of the exact layer."""
     p = _layer(T=150, H=256, E=4, k=2, F=256, Fs=Fs, score=score, seed=3)
     r = oracle.route(p["x"], p["Wr"], None, 2, score)
     q = oracle.layer_fp8(p["x"], p["Wr"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"],
-                         r["scores"], score, p["dY"], p["Wsg"], p["Wsu"], p["Wsd"])
+                         r["scores"], score, p["dY"], p["Wsg"], p["Wsu"], p["Wsd"], fold=fold)
     y = oracle.forward(p["x"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"], p["Wsg"], p["Wsu"], p["Wsd"])
     g = oracle.backward(p["x"], p["Wr"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"], r["scores"],
                         p["dY"], score, p["Wsg"], p["Wsu"], p["Wsd"])
