@@ -51,7 +51,7 @@ Layout make_layout(const moe_config_t& c, int T)
     L.poff = take(sizeof(int) * (c.E + 1));
     L.meta = take(sizeof(int) * 4);
     L.tiletab = take(sizeof(int) * L.MT_max);
-    L.pairtab = take(sizeof(int) * L.MT_max);
+    L.pairtab = take(sizeof(int) * ((size_t)L.MT_max + c.E + 1));   // pairs, then E+1 pair offsets
     L.rowof = take(sizeof(int) * L.R);
     L.slotof = take(sizeof(int) * L.Rp_max);
     L.Xp = take(es * L.Rp_max * c.H);
@@ -336,7 +336,8 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     MOE_STAGE(ST_ROUTER, launch_router<T>(x, a->Wr, a->b, T_, H, E, k, c.score, topk, gates, selsc,
                               reinterpret_cast<int*>(ws + L.hist), s));
     MOE_STAGE(ST_SCAN, launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
-                         reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab));
+                         reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab,
+                                   pairtab + L.MT_max));
     MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
     MOE_STAGE(ST_PERMUTE, launch_permute<T>(x, rowof, poff, counts, T_, H, E, k, Xp, s));
 
@@ -350,7 +351,7 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
     d.N = F; d.K = H; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = Xp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = a->W_gate; d.B1 = a->W_up; d.ldb = F; d.b_kmajor = 0; d.b_estride = (long long)H * F;
@@ -362,7 +363,7 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
     d.N = H; d.K = F; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = Hh; d.lda = F; d.a_rows = L.Rp_max;
     d.B0 = a->W_down; d.ldb = H; d.b_kmajor = 0; d.b_estride = (long long)F * H; d.b_rows = E * F;
@@ -452,7 +453,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_BWD; d.dual = DUAL_NONE;
     d.N = F; d.K = H; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = dYp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = a->W_down; d.ldb = H; d.b_kmajor = 1; d.b_estride = (long long)F * H; d.b_rows = E * F;
@@ -468,7 +469,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
     d.N = H; d.M_out = F; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = Hh; d.lda = F; d.a_rows = L.Rp_max;
     d.B0 = dYp; d.ldb = H; d.b_rows = L.Rp_max;
@@ -478,7 +479,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
     d.N = H; d.K = F; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = dA; d.A1 = dU; d.lda = F; d.a_rows = L.Rp_max;
     d.B0 = a->W_gate; d.B1 = a->W_up; d.ldb = F; d.b_kmajor = 1; d.b_estride = (long long)H * F;
@@ -489,7 +490,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
     d.N = F; d.M_out = H; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = Xp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = dA; d.B1 = dU; d.ldb = F; d.b_rows = L.Rp_max;
@@ -577,7 +578,8 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     MOE_STAGE(ST_ROUTER, launch_router<T>(x, a->Wr, a->b, T_, H, E, k, c.score, topk, gates, selsc,
                                           reinterpret_cast<int*>(ws + L.hist), s));
     MOE_STAGE(ST_SCAN, launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
-                                   reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab));
+                                   reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab,
+                                   pairtab + L.MT_max));
     MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
     MOE_STAGE(ST_PERMUTE, launch_permute_quant(x, rowof, poff, counts, T_, H, E, k, Xp, u8(sv, L.Xq),
                                                f32(sv, L.sX), s));
@@ -592,7 +594,7 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
     d.N = F; d.K = H; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
-    d.pair_tab = pairtab; d.prefer_pair = (long long)T_ * k >= 512ll * E;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(sv, L.Xq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(sv, L.sX); d.lds_a = H / 128;
     d.B0 = u8(sv, L.WgQT); d.B1 = u8(sv, L.WuQT); d.ldb = H; d.b_rows = E * F;
     d.SB0 = f32(sv, L.sWgT); d.SB1 = f32(sv, L.sWuT);
@@ -604,7 +606,7 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
     d.N = H; d.K = F; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
-    d.pair_tab = pairtab; d.prefer_pair = (long long)T_ * k >= 512ll * E;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.hq); d.lda = F; d.a_rows = Rp; d.SA0 = f32(ws, L.sh); d.lds_a = F / 128;
     d.B0 = u8(sv, L.WdQT); d.ldb = F; d.b_rows = E * H; d.SB0 = f32(sv, L.sWdT);
     d.O0 = Yp; d.ldo = H; d.status = status;
@@ -668,7 +670,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_BWD; d.dual = DUAL_NONE;
     d.N = F; d.K = H; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
-    d.pair_tab = pairtab; d.prefer_pair = (long long)T_ * k >= 512ll * E;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.dYq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(ws, L.sdY); d.lds_a = H / 128;
     d.B0 = u8(sv, L.WdQ); d.ldb = H; d.b_rows = E * F; d.SB0 = f32(sv, L.sWd);
     d.X0 = A; d.X1 = U; d.O0 = dA; d.O1 = dU; d.ldo = F; d.status = status;
@@ -686,7 +688,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
     d.N = H; d.M_out = F; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
-    d.pair_tab = pairtab; d.prefer_pair = (long long)T_ * k >= 512ll * E;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.hTq); d.lda = Rp; d.SA0 = f32(ws, L.shT); d.lds_a = Rp / 128;
     d.B0 = u8(ws, L.dYpTq); d.ldb = Rp; d.SB0 = f32(ws, L.sdYpT); d.lds_b = Rp / 128;
     d.rows_cap = Rp;
@@ -699,7 +701,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
     d.N = H; d.K = F; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
-    d.pair_tab = pairtab; d.prefer_pair = (long long)T_ * k >= 512ll * E;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.dAq); d.A1 = u8(ws, L.dUq); d.lda = F; d.a_rows = Rp;
     d.SA0 = f32(ws, L.sdA); d.SA1 = f32(ws, L.sdU); d.lds_a = F / 128;
     d.B0 = u8(sv, L.WgQ); d.B1 = u8(sv, L.WuQ); d.ldb = F; d.b_rows = E * H;
@@ -714,7 +716,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
     d.N = F; d.M_out = H; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
-    d.pair_tab = pairtab; d.prefer_pair = (long long)T_ * k >= 512ll * E;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.XpTq); d.lda = Rp; d.SA0 = f32(ws, L.sXpT); d.lds_a = Rp / 128;
     d.B0 = u8(ws, L.dATq); d.B1 = u8(ws, L.dUTq); d.ldb = Rp;
     d.SB0 = f32(ws, L.sdAT); d.SB1 = f32(ws, L.sdUT); d.lds_b = Rp / 128;

@@ -151,19 +151,26 @@ __device__ __forceinline__ void qtile_counts(const GemmDesc& d, int& num_m, int&
     }
 }
 
-// Row-scheduled tiles walk groups of kQGroupN column tiles over the row
-// units (one unit = a 128-row tile, or a pair of one expert's consecutive
-// tiles, the second possibly a "ghost" past the segment that is never
-// stored); weight-gradient tiles walk each expert's (m, n) grid m-fastest.
+// Row-scheduled tiles go expert by expert; within an expert, groups of
+// kQGroupN column tiles walk its row units (one unit = a 128-row tile, or a
+// pair of one expert's consecutive tiles, the second possibly a "ghost" past
+// the segment that is never stored); weight-gradient tiles walk each
+// expert's (m, n) grid m-fastest.
 template <int DUAL, int SCHED, bool PAIR>
 __device__ __forceinline__ QTile qdecode(const GemmDesc& d, int w, int num_m, int num_n, int rank)
 {
     QTile t;
     if (SCHED == SCHED_ROWS) {
-        const int group = w / (num_m * kQGroupN);
-        const int r = w - group * num_m * kQGroupN;
+        // expert by expert (each expert's units x num_n tiles are contiguous in w)
+        const int q = w / num_n;
+        const int e = d.tile_tab[PAIR ? d.pair_tab[q] : q];
+        const int u0 = PAIR ? d.pair_off[e] : d.poff[e] / QBM;
+        const int nu = (PAIR ? d.pair_off[e + 1] : d.poff[e + 1] / QBM) - u0;
+        w -= u0 * num_n;
+        const int group = w / (nu * kQGroupN);
+        const int r = w - group * nu * kQGroupN;
         const int gsz = min(kQGroupN, num_n - group * kQGroupN);
-        const int mu = r / gsz;
+        const int mu = u0 + r / gsz;
         t.n = group * kQGroupN + r % gsz;
         const int first = PAIR ? d.pair_tab[mu] : mu;
         t.m = first + rank;

@@ -84,11 +84,22 @@ __device__ __forceinline__ Tile decode_tile(const GemmDesc& d, int w, int num_m,
     if (SCHED == SCHED_ROWS) {
         // Groups of kGroupN n-tiles: consecutive units share the A rows (one
         // row unit against kGroupN weight column tiles), and consecutive
-        // groups of them walk the row units, which share the expert's weights.
-        const int group = w / (num_m * kGroupN);
-        const int r = w - group * num_m * kGroupN;
+        // groups of them walk the row units, which share the weights. Routed
+        // rows go expert by expert (each expert's block of units x num_n tiles
+        // is contiguous in w), so an expert's weight column group and its rows
+        // stay in L2 while its units pass over them.
+        int group, r, u0 = 0, nu = num_m;
+        if (d.dense_rows == 0) {
+            const int q = w / num_n;                        // some unit of w's expert
+            const int e = d.tile_tab[PAIR ? d.pair_tab[q] : q];
+            u0 = PAIR ? d.pair_off[e] : d.poff[e] / TBM;
+            nu = (PAIR ? d.pair_off[e + 1] : d.poff[e + 1] / TBM) - u0;
+            w -= u0 * num_n;
+        }
+        group = w / (nu * kGroupN);
+        r = w - group * nu * kGroupN;
         const int gsz = min(kGroupN, num_n - group * kGroupN);
-        const int mu = r / gsz;
+        const int mu = u0 + r / gsz;
         t.n = group * kGroupN + r % gsz;
         if (d.dense_rows > 0) {
             t.m = PAIR ? 2 * mu + rank : mu;

@@ -62,6 +62,7 @@ struct GemmDesc {
     const int* meta;      // meta[0] = number of 128-row tiles, meta[1] = padded rows,
                           // meta[2] = number of tile pairs
     const int* pair_tab;  // first tile of each pair of one expert's tiles (or null)
+    const int* pair_off;  // E+1: first pair of each expert (with pair_tab)
     int prefer_pair;      // routed rows per expert are large enough for CTA pairs
     const int* poff;      // E+1 padded segment offsets
     const int* counts;    // E token counts
@@ -106,7 +107,7 @@ cudaError_t launch_router(const T* x, const float* Wr, const float* b, int T_, i
                           cudaStream_t s);
 cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff, int* blkbase,
                         int* tile_tab, int* meta, int* slot_of, cudaStream_t s,
-                        int* pair_tab = nullptr);
+                        int* pair_tab = nullptr, int* pair_off = nullptr);
 cudaError_t launch_index(const int* topk, const int* blkbase, int T_, int E, int k, int* row_of,
                          int* slot_of, cudaStream_t s);
 template <typename T>

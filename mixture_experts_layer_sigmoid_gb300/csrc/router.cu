@@ -249,7 +249,8 @@ router_small_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const
 __global__ void __launch_bounds__(kMaxE)
 scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ counts,
             int* __restrict__ poff, int* __restrict__ blkbase, int* __restrict__ tile_tab,
-            int* __restrict__ meta, int* __restrict__ slot_of, int* __restrict__ pair_tab)
+            int* __restrict__ meta, int* __restrict__ slot_of, int* __restrict__ pair_tab,
+            int* __restrict__ pair_off)
 {
     __shared__ int sc[kMaxE];
     const int e = threadIdx.x;
@@ -298,7 +299,11 @@ scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ cou
         }
         const int pstart = sc[e] - np;
         for (int i = 0; i < np; ++i) pair_tab[pstart + i] = start / kTileM + 2 * i;
-        if (e == 0) meta[2] = sc[kMaxE - 1];
+        if (e < E) pair_off[e] = pstart;   // first pair of expert e
+        if (e == 0) {
+            meta[2] = sc[kMaxE - 1];
+            pair_off[E] = sc[kMaxE - 1];
+        }
     }
 }
 
@@ -353,10 +358,12 @@ template cudaError_t launch_router<__nv_bfloat16>(const __nv_bfloat16*, const fl
                                                   int*, cudaStream_t);
 
 cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff, int* blkbase,
-                        int* tile_tab, int* meta, int* slot_of, cudaStream_t s, int* pair_tab)
+                        int* tile_tab, int* meta, int* slot_of, cudaStream_t s, int* pair_tab,
+                        int* pair_off)
 {
+    if (pair_tab && !pair_off) return cudaErrorInvalidValue;
     scan_kernel<<<1, kMaxE, 0, s>>>(hist, nblk, E, counts, poff, blkbase, tile_tab, meta, slot_of,
-                                    pair_tab);
+                                    pair_tab, pair_off);
     return cudaGetLastError();
 }
 
