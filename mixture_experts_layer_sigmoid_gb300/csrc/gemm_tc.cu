@@ -534,9 +534,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
             }
             ptx::tc_fence_before();
             __syncwarp();
+            // relaxed: the arrive publishes no memory writes (the TMEM reads are
+            // complete after tcgen05.wait::ld), and a release arrive would first
+            // wait for this thread's outstanding global loads
             if (lane == 0) {
-                if (PAIR) ptx::mbar_arrive_cluster(ptx::mapa_shared(acce_bar(a), 0));
-                else ptx::mbar_arrive(acce_bar(a));
+                if (PAIR) ptx::mbar_arrive_cluster_relaxed(ptx::mapa_shared(acce_bar(a), 0));
+                else ptx::mbar_arrive_relaxed(acce_bar(a));
             }
         }
         if (lane == 0) ptx::bulk_wait_all();   // stores complete before the CTA exits
