@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 typedef enum {
     MOE_OK = 0,
@@ -82,6 +82,14 @@ typedef struct {
     int score;   /* moe_score_t                                             */
     int dtype;   /* moe_dtype_t                                             */
     unsigned flags; /* 0, or MOE_FLAG_STAGE_TIMING | MOE_FLAG_FOLD_GATES    */
+    float capacity_factor; /* 0 = dropless. > 0: capacity-limited dropping
+                    ("Scalable Training of Mixture-of-Experts Models with
+                    Megatron Core", §7 Load Balancing): expert e computes at
+                    most C = ceil(capacity_factor * T * top_k / E) of the
+                    (token, slot) assignments it received, the earliest tokens
+                    first; a dropped assignment adds nothing to y, gets no
+                    expert gradient and has dg = 0 (its routing gradient still
+                    flows through the other slots' renormalised gates). */
 } moe_config_t;
 
 /* Plan flag: bracket every kernel launch of moe_forward / moe_backward with
@@ -133,6 +141,14 @@ typedef struct {
     int32_t*     offsets;  /* optional out, E+1: first padded row of each
                               expert's segment (segments padded to 128 rows) */
     int32_t*     row_of;   /* optional out, T×k: padded row of (t, j)        */
+    const int32_t* replay_topk; /* optional in, T×k: router replay (§10, RL
+                              post-training) — expert of each (t, j) taken
+                              from here instead of the top-k selection; the
+                              logits, scores and gates are computed as usual
+                              over the given experts (gates = their scores
+                              over the sum of their scores). Indices outside
+                              [0, E) are clamped and reported as
+                              MOE_ERR_INVALID_ARG in the status word. */
 } moe_fwd_args_t;
 
 /* Backward arguments. Gradients are overwritten (not accumulated); experts
@@ -158,7 +174,8 @@ typedef struct {
 } moe_bwd_args_t;
 
 /* Validate `cfg` for `device` and build a plan (host memory only).
- * Errors: INVALID_ARG (null, sizes out of range, unknown flags),
+ * Errors: INVALID_ARG (null, sizes out of range, unknown flags,
+ *         capacity_factor negative or not finite),
  *         UNSUPPORTED (dtype not built, device not sm_103), CUDA. */
 moe_status_t moe_plan_create(const moe_config_t* cfg, int device, moe_plan_t* out);
 

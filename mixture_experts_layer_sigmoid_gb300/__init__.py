@@ -41,7 +41,7 @@ MOE_Q_ROWS, MOE_Q_TILES, MOE_Q_COLS_T, MOE_Q_TILES_T = 0, 1, 2, 3
 class moe_config_t(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int), ("E", ctypes.c_int), ("F", ctypes.c_int), ("Fs", ctypes.c_int),
                 ("top_k", ctypes.c_int), ("T_max", ctypes.c_int), ("score", ctypes.c_int),
-                ("dtype", ctypes.c_int), ("flags", ctypes.c_uint)]
+                ("dtype", ctypes.c_int), ("flags", ctypes.c_uint), ("capacity_factor", ctypes.c_float)]
 
 
 _vp = ctypes.c_void_p
@@ -50,7 +50,7 @@ _vp = ctypes.c_void_p
 class moe_fwd_args_t(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("x", "Wr", "b", "W_gate", "W_up", "W_down", "Ws_gate", "Ws_up",
                                    "Ws_down", "y", "topk_idx", "gates", "counts", "offsets",
-                                   "row_of")]
+                                   "row_of", "replay_topk")]
 
 
 class moe_bwd_args_t(ctypes.Structure):
@@ -185,15 +185,16 @@ class MoELayer:
 
     ``fold_gates`` selects the memory-efficient permutation (MOE_FLAG_FOLD_GATES):
     the routing weights are folded into the expert activations, and the saved
-    buffer keeps neither h nor the permuted expert outputs."""
+    buffer keeps neither h nor the permuted expert outputs. ``capacity_factor``
+    > 0 enables capacity-limited dropping (earliest tokens kept per expert)."""
 
     def __init__(self, H, E, F, top_k, T_max, score=MOE_SCORE_SOFTMAX, dtype=MOE_BF16, Fs=0,
-                 device=0, stage_timing=False, fold_gates=False):
+                 device=0, stage_timing=False, fold_gates=False, capacity_factor=0.0):
         import torch
         self.torch = torch
         flags = (MOE_FLAG_STAGE_TIMING if stage_timing else 0) | (MOE_FLAG_FOLD_GATES if fold_gates else 0)
         self.cfg = moe_config_t(H=H, E=E, F=F, Fs=Fs, top_k=top_k, T_max=T_max, score=score,
-                                dtype=dtype, flags=flags)
+                                dtype=dtype, flags=flags, capacity_factor=capacity_factor)
         self.device = torch.device("cuda", device)
         self.plan = moe_plan_create(self.cfg, device)
         self._bufs: Dict[int, tuple] = {}
@@ -217,7 +218,9 @@ class MoELayer:
         return self.torch.cuda.current_stream(self.device).cuda_stream
 
     def forward(self, x, Wr, b, W_gate, W_up, W_down, Ws_gate=None, Ws_up=None, Ws_down=None,
-                routing: bool = False, y=None):
+                routing: bool = False, y=None, replay_topk=None):
+        """replay_topk: optional T×k int32 device tensor of experts to route to
+        (router replay) instead of the top-k selection."""
         t = self.torch
         T = x.shape[0]
         saved, ws = self.buffers(T)
@@ -234,7 +237,8 @@ class MoELayer:
                            W_down=_ptr(W_down), Ws_gate=_ptr(Ws_gate), Ws_up=_ptr(Ws_up),
                            Ws_down=_ptr(Ws_down), y=_ptr(y), topk_idx=_ptr(out.get("topk_idx")),
                            gates=_ptr(out.get("gates")), counts=_ptr(out.get("counts")),
-                           offsets=_ptr(out.get("offsets")), row_of=_ptr(out.get("row_of")))
+                           offsets=_ptr(out.get("offsets")), row_of=_ptr(out.get("row_of")),
+                           replay_topk=_ptr(replay_topk))
         moe_forward(self.plan, T, a, saved.data_ptr(), saved.numel(), ws.data_ptr(), ws.numel(),
                     self.stream())
         return (y, out) if routing else y

@@ -9,6 +9,8 @@
 // kernel launches (and one status-word memset) on the caller's stream.
 #include "internal.h"
 
+#include <cmath>
+
 #include <new>
 #include <vector>
 #include <string.h>
@@ -21,7 +23,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct Layout {
     int T, R, Rp_max, MT_max, NB;
     // saved
-    size_t topk, gates, selsc, counts, poff, meta, tiletab, pairtab, rowof, slotof;
+    size_t topk, gates, selsc, counts, kept, poff, meta, tiletab, pairtab, rowof, slotof;
     size_t Xp, A, U, Hh, Yp, As, Us, Hs, saved_bytes;
     // workspace
     size_t status, hist, blkbase, Ys, dYp, dA, dU, dXp, dz, WrT, dAs, dUs, dXs, dgpart, ws_bytes;
@@ -48,6 +50,7 @@ Layout make_layout(const moe_config_t& c, int T)
     L.gates = take(sizeof(float) * L.R);
     L.selsc = take(sizeof(float) * L.R);
     L.counts = take(sizeof(int) * c.E);
+    L.kept = take(sizeof(int) * c.E);
     L.poff = take(sizeof(int) * (c.E + 1));
     L.meta = take(sizeof(int) * 4);
     L.tiletab = take(sizeof(int) * L.MT_max);
@@ -109,12 +112,22 @@ Layout make_layout(const moe_config_t& c, int T)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Rows each expert computes under capacity-limited dropping:
+// ceil(capacity_factor * T * k / E), or -1 (dropless).
+int capacity(const moe_config_t& c, int T)
+{
+    if (!(c.capacity_factor > 0.f)) return -1;
+    const double cap = std::ceil((double)c.capacity_factor * T * c.top_k / c.E);
+    return cap > 2147483647.0 ? 2147483647 : (int)cap;
+}
+
 moe_status_t check_config(const moe_config_t* c)
 {
     if (!c) return MOE_ERR_INVALID_ARG;
     if (c->H <= 0 || c->H % 128 || c->E < 1 || c->E > kMaxE || c->F <= 0 || c->F % 128 ||
         c->Fs < 0 || c->Fs % 128 || c->top_k < 1 || c->top_k > kMaxK || c->top_k > c->E ||
-        c->T_max < 1 || (c->flags & ~(MOE_FLAG_STAGE_TIMING | MOE_FLAG_FOLD_GATES)) != 0)
+        c->T_max < 1 || (c->flags & ~(MOE_FLAG_STAGE_TIMING | MOE_FLAG_FOLD_GATES)) != 0 ||
+        !(c->capacity_factor >= 0.f) || !std::isfinite(c->capacity_factor))
         return MOE_ERR_INVALID_ARG;
     if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
     if (c->dtype != MOE_FP32 && c->dtype != MOE_BF16 && c->dtype != MOE_FP8_BLOCK)
@@ -318,6 +331,7 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     float* gates = reinterpret_cast<float*>(sv + L.gates);
     float* selsc = reinterpret_cast<float*>(sv + L.selsc);
     int* counts = reinterpret_cast<int*>(sv + L.counts);
+    int* kept = reinterpret_cast<int*>(sv + L.kept);
     int* poff = reinterpret_cast<int*>(sv + L.poff);
     int* meta = reinterpret_cast<int*>(sv + L.meta);
     int* tiletab = reinterpret_cast<int*>(sv + L.tiletab);
@@ -334,10 +348,10 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
 
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
     MOE_STAGE(ST_ROUTER, launch_router<T>(x, a->Wr, a->b, T_, H, E, k, c.score, topk, gates, selsc,
-                              reinterpret_cast<int*>(ws + L.hist), s));
+                              reinterpret_cast<int*>(ws + L.hist), s, a->replay_topk, status));
     MOE_STAGE(ST_SCAN, launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
                          reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab,
-                                   pairtab + L.MT_max));
+                                   pairtab + L.MT_max, capacity(c, T_), kept));
     MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
     MOE_STAGE(ST_PERMUTE, launch_permute<T>(x, rowof, poff, counts, T_, H, E, k, Xp, s));
 
@@ -351,7 +365,7 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
     d.N = F; d.K = H; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = Xp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = a->W_gate; d.B1 = a->W_up; d.ldb = F; d.b_kmajor = 0; d.b_estride = (long long)H * F;
@@ -363,7 +377,7 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
     d.N = H; d.K = F; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = Hh; d.lda = F; d.a_rows = L.Rp_max;
     d.B0 = a->W_down; d.ldb = H; d.b_kmajor = 0; d.b_estride = (long long)F * H; d.b_rows = E * F;
@@ -412,6 +426,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     const float* gates = reinterpret_cast<const float*>(sv + L.gates);
     const float* selsc = reinterpret_cast<const float*>(sv + L.selsc);
     const int* counts = reinterpret_cast<const int*>(sv + L.counts);
+    const int* kept = reinterpret_cast<const int*>(sv + L.kept);
     const int* poff = reinterpret_cast<const int*>(sv + L.poff);
     const int* meta = reinterpret_cast<const int*>(sv + L.meta);
     const int* tiletab = reinterpret_cast<const int*>(sv + L.tiletab);
@@ -453,7 +468,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_BWD; d.dual = DUAL_NONE;
     d.N = F; d.K = H; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = dYp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = a->W_down; d.ldb = H; d.b_kmajor = 1; d.b_estride = (long long)F * H; d.b_rows = E * F;
@@ -469,7 +484,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
     d.N = H; d.M_out = F; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = Hh; d.lda = F; d.a_rows = L.Rp_max;
     d.B0 = dYp; d.ldb = H; d.b_rows = L.Rp_max;
@@ -479,7 +494,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
     d.N = H; d.K = F; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = dA; d.A1 = dU; d.lda = F; d.a_rows = L.Rp_max;
     d.B0 = a->W_gate; d.B1 = a->W_up; d.ldb = F; d.b_kmajor = 1; d.b_estride = (long long)H * F;
@@ -490,7 +505,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
     d.N = F; d.M_out = H; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = Xp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = dA; d.B1 = dU; d.ldb = F; d.b_rows = L.Rp_max;
@@ -559,6 +574,7 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     float* gates = reinterpret_cast<float*>(sv + L.gates);
     float* selsc = reinterpret_cast<float*>(sv + L.selsc);
     int* counts = reinterpret_cast<int*>(sv + L.counts);
+    int* kept = reinterpret_cast<int*>(sv + L.kept);
     int* poff = reinterpret_cast<int*>(sv + L.poff);
     int* meta = reinterpret_cast<int*>(sv + L.meta);
     int* tiletab = reinterpret_cast<int*>(sv + L.tiletab);
@@ -576,10 +592,10 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
 
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
     MOE_STAGE(ST_ROUTER, launch_router<T>(x, a->Wr, a->b, T_, H, E, k, c.score, topk, gates, selsc,
-                                          reinterpret_cast<int*>(ws + L.hist), s));
+                                          reinterpret_cast<int*>(ws + L.hist), s, a->replay_topk, status));
     MOE_STAGE(ST_SCAN, launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
                                    reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab,
-                                   pairtab + L.MT_max));
+                                   pairtab + L.MT_max, capacity(c, T_), kept));
     MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
     MOE_STAGE(ST_PERMUTE, launch_permute_quant(x, rowof, poff, counts, T_, H, E, k, Xp, u8(sv, L.Xq),
                                                f32(sv, L.sX), s));
@@ -593,7 +609,7 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
     d.N = F; d.K = H; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(sv, L.Xq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(sv, L.sX); d.lds_a = H / 128;
     d.B0 = u8(sv, L.WgQT); d.B1 = u8(sv, L.WuQT); d.ldb = H; d.b_rows = E * F;
@@ -605,7 +621,7 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
     d.N = H; d.K = F; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.hq); d.lda = F; d.a_rows = Rp; d.SA0 = f32(ws, L.sh); d.lds_a = F / 128;
     d.B0 = u8(sv, L.WdQT); d.ldb = F; d.b_rows = E * H; d.SB0 = f32(sv, L.sWdT);
@@ -635,6 +651,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     const float* gates = reinterpret_cast<const float*>(sv + L.gates);
     const float* selsc = reinterpret_cast<const float*>(sv + L.selsc);
     const int* counts = reinterpret_cast<const int*>(sv + L.counts);
+    const int* kept = reinterpret_cast<const int*>(sv + L.kept);
     const int* poff = reinterpret_cast<const int*>(sv + L.poff);
     const int* meta = reinterpret_cast<const int*>(sv + L.meta);
     const int* tiletab = reinterpret_cast<const int*>(sv + L.tiletab);
@@ -669,7 +686,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_BWD; d.dual = DUAL_NONE;
     d.N = F; d.K = H; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.dYq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(ws, L.sdY); d.lds_a = H / 128;
     d.B0 = u8(sv, L.WdQ); d.ldb = H; d.b_rows = E * F; d.SB0 = f32(sv, L.sWd);
@@ -687,7 +704,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
     d.N = H; d.M_out = F; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.hTq); d.lda = Rp; d.SA0 = f32(ws, L.shT); d.lds_a = Rp / 128;
     d.B0 = u8(ws, L.dYpTq); d.ldb = Rp; d.SB0 = f32(ws, L.sdYpT); d.lds_b = Rp / 128;
@@ -700,7 +717,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
     d.N = H; d.K = F; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.dAq); d.A1 = u8(ws, L.dUq); d.lda = F; d.a_rows = Rp;
     d.SA0 = f32(ws, L.sdA); d.SA1 = f32(ws, L.sdU); d.lds_a = F / 128;
@@ -715,7 +732,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
     d.N = F; d.M_out = H; d.E = E;
-    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = counts;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.XpTq); d.lda = Rp; d.SA0 = f32(ws, L.sXpT); d.lds_a = Rp / 128;
     d.B0 = u8(ws, L.dATq); d.B1 = u8(ws, L.dUTq); d.ldb = Rp;

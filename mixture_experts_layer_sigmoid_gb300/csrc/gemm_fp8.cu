@@ -576,7 +576,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__
                         }
                         if (fold) {
                             const int col = part ? col_hi : col_lo;
-                            if (valid) d.dg_part[(size_t)arow * d.dg_ld + col / 64] = dgp;
+                            d.dg_part[(size_t)arow * d.dg_ld + col / 64] = dgp;   // 0 past the computed rows
                         }
                     }
                 } else {

@@ -184,7 +184,7 @@ gemm_simt_kernel(const GemmDesc d)
             // the 16 threads of a half-warp (tx) share these rows
 #pragma unroll
             for (int off = 8; off > 0; off >>= 1) dgp += __shfl_xor_sync(0xffffffffu, dgp, off);
-            if (tx == 0 && row_i < valid_end) d.dg_part[(size_t)row_i * d.dg_ld + n0 / 64] = dgp;
+            if (tx == 0 && row_i < alloc_end) d.dg_part[(size_t)row_i * d.dg_ld + n0 / 64] = dgp;
         }
     }
 }

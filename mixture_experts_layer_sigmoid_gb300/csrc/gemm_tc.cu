@@ -512,7 +512,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                             const int col = t.n * NW + u * 64, y = t.row0 + q * 32;
                             stage_store(&mO0, d0, d1, col, y);
                             stage_store(&mO1, e0, e1, col, y);
-                            if (fold && valid) d.dg_part[(size_t)row * d.dg_ld + col / 64] = dgp;
+                            // every row of the segment (0 past the computed rows), so
+                            // that dropped assignments read dg = 0
+                            if (fold) d.dg_part[(size_t)row * d.dg_ld + col / 64] = dgp;
                         }
                     }
                 } else {

@@ -65,7 +65,8 @@ struct GemmDesc {
     const int* pair_off;  // E+1: first pair of each expert (with pair_tab)
     int prefer_pair;      // routed rows per expert are large enough for CTA pairs
     const int* poff;      // E+1 padded segment offsets
-    const int* counts;    // E token counts
+    const int* counts;    // E rows computed per expert (token counts, or the
+                          // kept counts under capacity-limited dropping)
     // operands (element pointers; the tensor-core path builds TMA maps from them)
     const void* A0; const void* A1; int lda;      // ROWS: A[row][k]; WGRAD: A[row][m]
     const void* B0; const void* B1; int ldb;
@@ -104,10 +105,12 @@ cudaError_t gemm_fp8_prepare(int device);
 template <typename T>
 cudaError_t launch_router(const T* x, const float* Wr, const float* b, int T_, int H, int E, int k,
                           int score, int* topk, float* gates, float* selsc, int* hist,
-                          cudaStream_t s);
+                          cudaStream_t s,
+                          const int* replay = nullptr, DeviceStatus* status = nullptr);
 cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff, int* blkbase,
                         int* tile_tab, int* meta, int* slot_of, cudaStream_t s,
-                        int* pair_tab = nullptr, int* pair_off = nullptr);
+                        int* pair_tab = nullptr, int* pair_off = nullptr, int cap = -1,
+                        int* kept = nullptr);
 cudaError_t launch_index(const int* topk, const int* blkbase, int T_, int E, int k, int* row_of,
                          int* slot_of, cudaStream_t s);
 template <typename T>

@@ -30,11 +30,37 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
 }
 
+// Router replay: expert of slot j of token t from the caller, clamped into
+// [0, E); an index outside it is reported once in the status word.
+__device__ __forceinline__ int replay_expert(const int* replay, size_t i, int E, DeviceStatus* status)
+{
+    int e = replay[i];
+    if (e < 0 || e >= E) {
+        if (status && atomicCAS(&status->code, 0, (int)MOE_ERR_INVALID_ARG) == 0) status->where = 1;
+        e = e < 0 ? 0 : E - 1;
+    }
+    return e;
+}
+
+// Gates of the selected logits: softmax over them (max-shifted), or the
+// sigmoid scores over their sum.
+__device__ __forceinline__ void gates_of(const float* sel_z, int k, int score, float* sc, float& den)
+{
+    float m = sel_z[0];
+    for (int j = 1; j < k; ++j) m = fmaxf(m, sel_z[j]);
+    den = 0.f;
+    for (int j = 0; j < k; ++j) {
+        sc[j] = (score == MOE_SCORE_SOFTMAX) ? expf(sel_z[j] - m) : 1.f / (1.f + expf(-sel_z[j]));
+        den += sc[j];
+    }
+}
+
 template <typename T, int EPL>
 __global__ void __launch_bounds__(256)
 router_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float* __restrict__ b,
               int T_, int H, int E, int k, int score, int* __restrict__ topk,
-              float* __restrict__ gates, float* __restrict__ selsc, int* __restrict__ hist)
+              float* __restrict__ gates, float* __restrict__ selsc, int* __restrict__ hist,
+              const int* __restrict__ replay, DeviceStatus* __restrict__ status)
 {
     constexpr int HC = 32;                 // h chunk
     constexpr int EW = EPL * 32;           // padded expert width
@@ -114,6 +140,17 @@ router_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float
 #pragma unroll
         for (int j = 0; j < kMaxK; ++j) {
             if (j >= k) break;
+            if (replay) {
+                // the given expert's logit, from the lane that holds it
+                const int e = replay_expert(replay, (size_t)t * k + j, E, lane == 0 ? status : nullptr);
+                float zi = z[0];
+#pragma unroll
+                for (int i = 1; i < EPL; ++i)
+                    if ((e >> 5) == i) zi = z[i];
+                sel_e[j] = e;
+                sel_z[j] = __shfl_sync(0xffffffffu, zi, e & 31);
+                continue;
+            }
             float bv = -INFINITY;
             int bi = 0x7fffffff;
 #pragma unroll
@@ -132,12 +169,8 @@ router_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float
             if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
         }
         if (lane == 0) {
-            float sc[kMaxK], den = 0.f;
-            for (int j = 0; j < k; ++j) {
-                sc[j] = (score == MOE_SCORE_SOFTMAX) ? expf(sel_z[j] - sel_z[0])
-                                                     : 1.f / (1.f + expf(-sel_z[j]));
-                den += sc[j];
-            }
+            float sc[kMaxK], den;
+            gates_of(sel_z, k, score, sc, den);
             for (int j = 0; j < k; ++j) {
                 topk[(size_t)t * k + j] = sel_e[j];
                 gates[(size_t)t * k + j] = sc[j] / den;
@@ -166,7 +199,8 @@ template <typename T, int EMAX>
 __global__ void __launch_bounds__(256)
 router_small_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float* __restrict__ b,
                     int T_, int H, int E, int k, int score, int* __restrict__ topk,
-                    float* __restrict__ gates, float* __restrict__ selsc, int* __restrict__ hist)
+                    float* __restrict__ gates, float* __restrict__ selsc, int* __restrict__ hist,
+                    const int* __restrict__ replay, DeviceStatus* __restrict__ status)
 {
     constexpr int V = 16 / sizeof(T);
     constexpr int NW = 8;
@@ -212,6 +246,16 @@ router_small_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const
             int sel_e[kMaxK];
             float sel_z[kMaxK];
             for (int j = 0; j < k; ++j) {
+                if (replay) {
+                    const int e = replay_expert(replay, (size_t)tok * k + j, E, status);
+                    float ze = z[0];
+#pragma unroll
+                    for (int i = 1; i < EMAX; ++i)
+                        if (e == i) ze = z[i];
+                    sel_e[j] = e;
+                    sel_z[j] = ze;
+                    continue;
+                }
                 float bv = -INFINITY;
                 int bi = 0x7fffffff;
 #pragma unroll
@@ -221,12 +265,8 @@ router_small_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const
                 sel_e[j] = bi;
                 sel_z[j] = bv;
             }
-            float sc[kMaxK], den = 0.f;
-            for (int j = 0; j < k; ++j) {
-                sc[j] = (score == MOE_SCORE_SOFTMAX) ? expf(sel_z[j] - sel_z[0])
-                                                     : 1.f / (1.f + expf(-sel_z[j]));
-                den += sc[j];
-            }
+            float sc[kMaxK], den;
+            gates_of(sel_z, k, score, sc, den);
             for (int j = 0; j < k; ++j) {
                 topk[(size_t)tok * k + j] = sel_e[j];
                 gates[(size_t)tok * k + j] = sc[j] / den;
@@ -250,7 +290,7 @@ __global__ void __launch_bounds__(kMaxE)
 scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ counts,
             int* __restrict__ poff, int* __restrict__ blkbase, int* __restrict__ tile_tab,
             int* __restrict__ meta, int* __restrict__ slot_of, int* __restrict__ pair_tab,
-            int* __restrict__ pair_off)
+            int* __restrict__ pair_off, int cap, int* __restrict__ kept)
 {
     __shared__ int sc[kMaxE];
     const int e = threadIdx.x;
@@ -270,6 +310,9 @@ scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ cou
     const int start = sc[e] - ((e < E) ? pc : 0);
     if (e < E) {
         counts[e] = c;
+        // capacity-limited dropping: the segment keeps all c rows (the router
+        // gradient needs them) but only the first min(c, cap) are computed
+        if (kept) kept[e] = (cap >= 0 && c > cap) ? cap : c;
         poff[e] = start;
         int run = start;
         for (int blk = 0; blk < nblk; ++blk) {
@@ -334,36 +377,43 @@ index_kernel(const int* __restrict__ topk, const int* __restrict__ blkbase, int 
 template <typename T>
 cudaError_t launch_router(const T* x, const float* Wr, const float* b, int T_, int H, int E, int k,
                           int score, int* topk, float* gates, float* selsc, int* hist,
-                          cudaStream_t s)
+                          cudaStream_t s,
+                          const int* replay, DeviceStatus* status)
 {
     const int nblk = (T_ + kRouterTokens - 1) / kRouterTokens;
     if (E <= 8)
-        router_small_kernel<T, 8><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+        router_small_kernel<T, 8><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
+                                                               replay, status);
     else if (E <= 16)
-        router_small_kernel<T, 16><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+        router_small_kernel<T, 16><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
+                                                               replay, status);
     else if (E <= 32)
-        router_small_kernel<T, 32><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+        router_small_kernel<T, 32><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
+                                                               replay, status);
     else if (E <= 64)
-        router_kernel<T, 2><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+        router_kernel<T, 2><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
+                                                               replay, status);
     else if (E <= 128)
-        router_kernel<T, 4><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+        router_kernel<T, 4><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
+                                                               replay, status);
     else
-        router_kernel<T, 8><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist);
+        router_kernel<T, 8><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
+                                                               replay, status);
     return cudaGetLastError();
 }
 template cudaError_t launch_router<float>(const float*, const float*, const float*, int, int, int,
-                                          int, int, int*, float*, float*, int*, cudaStream_t);
+                                          int, int, int*, float*, float*, int*, cudaStream_t, const int*, DeviceStatus*);
 template cudaError_t launch_router<__nv_bfloat16>(const __nv_bfloat16*, const float*, const float*,
                                                   int, int, int, int, int, int*, float*, float*,
-                                                  int*, cudaStream_t);
+                                                  int*, cudaStream_t, const int*, DeviceStatus*);
 
 cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff, int* blkbase,
                         int* tile_tab, int* meta, int* slot_of, cudaStream_t s, int* pair_tab,
-                        int* pair_off)
+                        int* pair_off, int cap, int* kept)
 {
     if (pair_tab && !pair_off) return cudaErrorInvalidValue;
     scan_kernel<<<1, kMaxE, 0, s>>>(hist, nblk, E, counts, poff, blkbase, tile_tab, meta, slot_of,
-                                    pair_tab, pair_off);
+                                    pair_tab, pair_off, cap, kept);
     return cudaGetLastError();
 }
 

@@ -62,6 +62,10 @@ def _i(a):
     return None if a is None else a.ctypes.data_as(_ip)
 
 
+def _u8(a):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte))
+
+
 def _f64(a):
     return None if a is None else np.ascontiguousarray(a, dtype=np.float64)
 
@@ -93,6 +97,30 @@ def route(x, Wr, b, k, score, replay_topk=None, replay_mask=None):
     return out
 
 
+def capacity_keep(topk, E, C):
+    """Capacity-limited dropping ("Scalable Training of Mixture-of-Experts
+    Models with Megatron Core", §7 Load Balancing; the pages give no rule for
+    which assignments an expert drops): expert e keeps the first C of its
+    assignments in token order and drops the rest. Returns the T×k mask of
+    kept slots (uint8)."""
+    topk = np.asarray(topk)
+    T, k = topk.shape
+    keep = np.zeros((T, k), np.uint8)
+    seen = np.zeros(E, np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = int(topk[t, j])
+            if seen[e] < C:
+                keep[t, j] = 1
+            seen[e] += 1
+    return keep
+
+
+def capacity(T, k, E, factor):
+    """Rows an expert computes: ceil(factor * T * k / E)."""
+    return int(np.ceil(np.float64(np.float32(factor)) * T * k / E))
+
+
 def dispatch(topk, E):
     """Dispatch: counts E, offsets E+1, row_of T×k, slot_of R (int32)."""
     lib = _load()
@@ -107,12 +135,14 @@ def dispatch(topk, E):
     return dict(counts=counts, offsets=offsets, row_of=row_of, slot_of=slot_of)
 
 
-def forward(x, Wg, Wu, Wd, topk, gates, Wsg=None, Wsu=None, Wsd=None, want_Yp=False):
-    """Layer output y (T×H) for a given routing; optionally Yp (R×H)."""
+def forward(x, Wg, Wu, Wd, topk, gates, Wsg=None, Wsu=None, Wsd=None, want_Yp=False, keep=None):
+    """Layer output y (T×H) for a given routing; optionally Yp (R×H). keep:
+    optional T×k mask of the slots not dropped (capacity_keep)."""
     lib = _load()
     x, Wg, Wu, Wd = _f64(x), _f64(Wg), _f64(Wu), _f64(Wd)
     Wsg, Wsu, Wsd = _f64(Wsg), _f64(Wsu), _f64(Wsd)
     topk, gates = _i32(topk), _f64(gates)
+    keep = None if keep is None else np.ascontiguousarray(keep, np.uint8)
     T, H = x.shape
     E, _, F = Wg.shape
     k = topk.shape[1]
@@ -120,18 +150,21 @@ def forward(x, Wg, Wu, Wd, topk, gates, Wsg=None, Wsu=None, Wsd=None, want_Yp=Fa
     y = np.empty((T, H))
     Yp = np.empty((T * k, H)) if want_Yp else None
     if lib.oracle_forward(T, H, E, k, F, Fs, _d(x), _d(Wg), _d(Wu), _d(Wd),
-                          _d(Wsg), _d(Wsu), _d(Wsd), _i(topk), _d(gates), _d(y), _d(Yp)):
+                          _d(Wsg), _d(Wsu), _d(Wsd), _i(topk), _d(gates), _d(y), _d(Yp),
+                          _u8(keep)):
         raise ValueError("oracle_forward: bad arguments")
     return (y, Yp) if want_Yp else y
 
 
 def backward(x, Wr, Wg, Wu, Wd, topk, gates, scores, dY, score,
-             Wsg=None, Wsu=None, Wsd=None):
-    """All gradients of L = sum(dY * y) with the routing held fixed."""
+             Wsg=None, Wsu=None, Wsd=None, keep=None):
+    """All gradients of L = sum(dY * y) with the routing (and, with keep, the
+    dropped slots) held fixed."""
     lib = _load()
     x, Wr, Wg, Wu, Wd = _f64(x), _f64(Wr), _f64(Wg), _f64(Wu), _f64(Wd)
     Wsg, Wsu, Wsd = _f64(Wsg), _f64(Wsu), _f64(Wsd)
     topk, gates, scores, dY = _i32(topk), _f64(gates), _f64(scores), _f64(dY)
+    keep = None if keep is None else np.ascontiguousarray(keep, np.uint8)
     T, H = x.shape
     E, _, F = Wg.shape
     k = topk.shape[1]
@@ -143,7 +176,8 @@ def backward(x, Wr, Wg, Wu, Wd, topk, gates, scores, dY, score,
     rc = lib.oracle_backward(T, H, E, k, F, Fs, score, _d(x), _d(Wr), _d(Wg), _d(Wu), _d(Wd),
                              _d(Wsg), _d(Wsu), _d(Wsd), _i(topk), _d(gates), _d(scores), _d(dY),
                              _d(g["dX"]), _d(g["dWr"]), _d(g["dWg"]), _d(g["dWu"]), _d(g["dWd"]),
-                             _d(g.get("dWsg")), _d(g.get("dWsu")), _d(g.get("dWsd")), _d(g["dg"]))
+                             _d(g.get("dWsg")), _d(g.get("dWsu")), _d(g.get("dWsd")), _d(g["dg"]),
+                             _u8(keep))
     if rc:
         raise ValueError("oracle_backward: bad arguments")
     return g

@@ -242,10 +242,16 @@ static void swiglu_backward(int M, int H, int F, const double* X,
  * Yp (optional, R*H) receives the unweighted expert outputs in dispatch
  * order; y (T*H) the layer output.
  */
+/*
+ * keep (optional, T*k): capacity-limited dropping ("Scalable Training of
+ * Mixture-of-Experts Models with Megatron Core", §7 Load Balancing); a slot
+ * with keep = 0 is dropped: its expert output does not enter y.
+ */
 int oracle_forward(int T, int H, int E, int k, int F, int Fs,
                    const double* x, const double* Wg, const double* Wu, const double* Wd,
                    const double* Wsg, const double* Wsu, const double* Wsd,
-                   const int* topk, const double* gates, double* y, double* Yp_out)
+                   const int* topk, const double* gates, double* y, double* Yp_out,
+                   const unsigned char* keep)
 {
     if (T <= 0 || H <= 0 || E <= 0 || k <= 0 || k > E || F <= 0 || Fs < 0) return -1;
     const int R = T * k;
@@ -275,8 +281,10 @@ int oracle_forward(int T, int H, int E, int k, int F, int Fs,
     for (int t = 0; t < T; ++t)
         for (int h = 0; h < H; ++h) {
             double acc = 0.0;
-            for (int j = 0; j < k; ++j)
+            for (int j = 0; j < k; ++j) {
+                if (keep && !keep[(size_t)t * k + j]) continue;
                 acc += gates[(size_t)t * k + j] * Yp[(size_t)row_of[(size_t)t * k + j] * H + h];
+            }
             y[(size_t)t * H + h] = acc;
         }
     if (Fs > 0) {
@@ -335,7 +343,8 @@ int oracle_backward(int T, int H, int E, int k, int F, int Fs, int score_fn,
                     const int* topk, const double* gates, const double* scores,
                     const double* dY,
                     double* dX, double* dWr, double* dWg, double* dWu, double* dWd,
-                    double* dWsg, double* dWsu, double* dWsd, double* dg_out)
+                    double* dWsg, double* dWsu, double* dWsd, double* dg_out,
+                    const unsigned char* keep)
 {
     if (T <= 0 || H <= 0 || E <= 0 || k <= 0 || k > E || k > 1024 || F <= 0 || Fs < 0) return -1;
     const int R = T * k;
@@ -370,17 +379,19 @@ int oracle_backward(int T, int H, int E, int k, int F, int Fs, int score_fn,
         double* Hh = (double*)malloc(sizeof(double) * (size_t)M * F);
         swiglu_forward(M, H, F, Xe, Wg + (size_t)e * H * F, Wu + (size_t)e * H * F,
                        Wd + (size_t)e * F * H, A, U, Hh, Yp + (size_t)offsets[e] * H);
-        /* gate gradient and the gate-scaled output gradient of each row */
+        /* gate gradient and the gate-scaled output gradient of each row; a
+         * dropped slot is not part of y: no output gradient, dg = 0 */
         for (int m = 0; m < M; ++m) {
             int r = offsets[e] + m;
             int t = slot_of[r] / k;
-            double g = gates[slot_of[r]];
+            const int kept = !keep || keep[slot_of[r]];
+            double g = kept ? gates[slot_of[r]] : 0.0;
             double acc = 0.0;
             for (int h = 0; h < H; ++h) {
                 acc += dY[(size_t)t * H + h] * Yp[(size_t)r * H + h];
                 dYp[(size_t)r * H + h] = g * dY[(size_t)t * H + h];
             }
-            dg[slot_of[r]] = acc;
+            dg[slot_of[r]] = kept ? acc : 0.0;
         }
         swiglu_backward(M, H, F, Xe, Wg + (size_t)e * H * F, Wu + (size_t)e * H * F,
                         Wd + (size_t)e * F * H, A, U, Hh, dYp + (size_t)offsets[e] * H,

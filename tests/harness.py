@@ -176,16 +176,20 @@ def upload(inp, device="cuda"):
     return {k: (None if v is None else v.to(device)) for k, v in inp.items()}
 
 
-def run_gpu(w: mi.Workload, inp, layer=None, backward=True, fold=False):
+def run_gpu(w: mi.Workload, inp, layer=None, backward=True, fold=False, capacity_factor=0.0,
+            replay=None):
     """Forward (+ backward) through the C ABI; returns host copies. fold:
-    memory-efficient permutation (routing weights folded into h)."""
+    memory-efficient permutation (routing weights folded into h);
+    capacity_factor: capacity-limited dropping; replay: T×k experts to route
+    to (router replay)."""
     from mixture_experts_layer_sigmoid_gb300 import MoELayer
     g = upload(inp)
     if layer is None:
         layer = MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=w.dtype, Fs=w.Fs,
-                         fold_gates=fold)
+                         fold_gates=fold, capacity_factor=capacity_factor)
+    rep = None if replay is None else torch.as_tensor(replay, dtype=torch.int32).cuda()
     y, r = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"], g["Wsg"], g["Wsu"],
-                         g["Wsd"], routing=True)
+                         g["Wsd"], routing=True, replay_topk=rep)
     out = dict(y=y, **r)
     if backward:
         out.update(layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], g["Wsg"],
@@ -233,12 +237,12 @@ def check_routing(w, inp, gpu):
 def oracle_layer(w, inp, r, backward=True):
     args = {k: to_np(inp[k]) for k in ("x", "Wg", "Wu", "Wd", "Wsg", "Wsu", "Wsd")}
     y = oracle.forward(args["x"], args["Wg"], args["Wu"], args["Wd"], r["topk"], r["gates"],
-                       args["Wsg"], args["Wsu"], args["Wsd"])
+                       args["Wsg"], args["Wsu"], args["Wsd"], keep=r.get("keep"))
     out = dict(y=y)
     if backward:
         g = oracle.backward(args["x"], to_np(inp["Wr"]), args["Wg"], args["Wu"], args["Wd"],
                             r["topk"], r["gates"], r["scores"], to_np(inp["dY"]), w.score,
-                            args["Wsg"], args["Wsu"], args["Wsd"])
+                            args["Wsg"], args["Wsu"], args["Wsd"], keep=r.get("keep"))
         out.update(g)
     return out
 
@@ -268,10 +272,13 @@ def compare_all(w, inp, r, gpu, ref, backward=True):
     return report
 
 
-def full_parity(w: mi.Workload, backward=True, fold=False):
+def full_parity(w: mi.Workload, backward=True, fold=False, capacity_factor=0.0):
     inp = mi.make_inputs(w, "cpu", with_grad_out=backward)
-    gpu, layer = run_gpu(w, inp, backward=backward, fold=fold)
+    gpu, layer = run_gpu(w, inp, backward=backward, fold=fold, capacity_factor=capacity_factor)
     r, nties = check_routing(w, inp, gpu)
+    if capacity_factor > 0:
+        C = oracle.capacity(w.T, w.k, w.E, capacity_factor)
+        r["keep"] = oracle.capacity_keep(r["topk"], w.E, C)
     np.testing.assert_allclose(gpu["gates"].numpy(), r["gates"], rtol=1e-4, atol=1e-6)
     ref = oracle_layer(w, inp, r, backward)
     report = compare_all(w, inp, r, gpu, ref, backward)

@@ -31,7 +31,7 @@ def test_header_declares_the_bound_names():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_entry_points():
         assert hasattr(lib, name), name
-    assert moe.moe_abi_version() == 1
+    assert moe.moe_abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -49,7 +49,8 @@ def _cfg(**kw):
 @pytest.mark.parametrize("bad", [dict(H=100), dict(H=0), dict(F=200), dict(Fs=64), dict(E=0),
                                  dict(E=257), dict(top_k=0), dict(top_k=9), dict(top_k=9, E=16),
                                  dict(E=2, top_k=3), dict(T_max=0), dict(score=2), dict(dtype=7),
-                                 dict(flags=4), dict(flags=8)])
+                                 dict(flags=4), dict(flags=8), dict(capacity_factor=-1.0),
+                                 dict(capacity_factor=float("nan")), dict(capacity_factor=float("inf"))])
 def test_plan_create_rejects_bad_configs(lib, bad):
     plan = ctypes.c_void_p()
     st = lib.moe_plan_create(ctypes.byref(_cfg(**bad)), 0, ctypes.byref(plan))

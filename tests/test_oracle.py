@@ -304,3 +304,91 @@ def test_sampled_rows_and_entries_match_full_oracle(storage):
     for (n, e, i, j), v in zip(ents, out):
         ref = g[n][i, j] if n.startswith("dWs") else g[n][e, i, j]
         assert v == pytest.approx(ref, rel=1e-12, abs=1e-13)
+
+
+# ------------------------------------------------- capacity-limited dropping
+def test_capacity_keep_rule_brute_force():
+    """Kept assignments of each expert are exactly its C earliest tokens."""
+    p = _layer(T=60, E=5, k=2, bias=True, seed=31)
+    r = _route(p)
+    for C in (0, 3, 17, 60):
+        keep = oracle.capacity_keep(r["topk"], 5, C)
+        for e in range(5):
+            toks = sorted(int(t) for t, j in zip(*np.nonzero(r["topk"] == e)))
+            kept = sorted(int(t) for t, j in zip(*np.nonzero((r["topk"] == e) & (keep == 1))))
+            assert kept == toks[:C]
+    assert oracle.capacity(T=4096, k=2, E=8, factor=1.25) == 1280
+    assert oracle.capacity(T=10, k=3, E=4, factor=1.0) == 8      # ceil(7.5)
+
+
+def test_capacity_above_max_load_is_dropless():
+    p = _layer(T=30, E=4, k=2, Fs=5, bias=True, seed=32)
+    r = _route(p)
+    keep = oracle.capacity_keep(r["topk"], 4, 60)
+    assert keep.all()
+    y0 = _fwd(p, r)
+    y1 = oracle.forward(p["x"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"], p["Wsg"],
+                        p["Wsu"], p["Wsd"], keep=keep)
+    assert np.array_equal(y0, y1)
+    g0 = oracle.backward(p["x"], p["Wr"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"],
+                         r["scores"], p["dY"], p["score"], p["Wsg"], p["Wsu"], p["Wsd"])
+    g1 = oracle.backward(p["x"], p["Wr"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"],
+                         r["scores"], p["dY"], p["score"], p["Wsg"], p["Wsu"], p["Wsd"], keep=keep)
+    for n in g0:
+        assert np.array_equal(g0[n], g1[n]), n
+
+
+def test_capacity_dropped_top1_token_gets_only_the_shared_expert():
+    p = _layer(T=20, E=3, k=1, Fs=4, seed=33)
+    r = _route(p)
+    keep = oracle.capacity_keep(r["topk"], 3, 2)
+    assert (keep == 0).any()
+    y = oracle.forward(p["x"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"], p["Wsg"],
+                       p["Wsu"], p["Wsd"], keep=keep)
+    shared = _swiglu_dense(p["x"], p["Wsg"], p["Wsu"], p["Wsd"])
+    dropped = keep[:, 0] == 0
+    np.testing.assert_allclose(y[dropped], shared[dropped], rtol=1e-12, atol=1e-12)
+    e0 = r["topk"][~dropped, 0]
+    ref = np.stack([_swiglu_dense(p["x"][[t]], p["Wg"][e], p["Wu"][e], p["Wd"][e])[0]
+                    for t, e in zip(np.nonzero(~dropped)[0], e0)]) + shared[~dropped]
+    np.testing.assert_allclose(y[~dropped], ref, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("score", [oracle.SOFTMAX, oracle.SIGMOID])
+def test_capacity_backward_finite_differences(score):
+    """Gradients with dropped slots (routing and drops held fixed) against
+    central differences of the dropping forward."""
+    p = _layer(T=16, H=8, E=3, k=2, F=6, Fs=4, score=score, bias=True, seed=34)
+    r = _route(p)
+    C = 7
+    keep = oracle.capacity_keep(r["topk"], 3, C)
+    assert (keep == 0).sum() >= 3
+    g = oracle.backward(p["x"], p["Wr"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"],
+                        r["scores"], p["dY"], score, p["Wsg"], p["Wsu"], p["Wsd"], keep=keep)
+    assert np.all(g["dg"][keep == 0] == 0.0)
+
+    def loss():
+        rr = _route(p)
+        kk = oracle.capacity_keep(rr["topk"], 3, C)
+        y = oracle.forward(p["x"], p["Wg"], p["Wu"], p["Wd"], rr["topk"], rr["gates"], p["Wsg"],
+                           p["Wsu"], p["Wsd"], keep=kk)
+        return float((p["dY"] * y).sum()), rr["topk"]
+
+    rng = np.random.default_rng(1)
+    eps, checked = 1e-6, 0
+    for pn, gn in [("x", "dX"), ("Wr", "dWr"), ("Wg", "dWg"), ("Wu", "dWu"), ("Wd", "dWd"),
+                   ("Wsd", "dWsd")]:
+        flat = p[pn].reshape(-1)
+        for idx in rng.choice(flat.size, size=min(flat.size, 12), replace=False):
+            old = flat[idx]
+            flat[idx] = old + eps
+            lp, tp = loss()
+            flat[idx] = old - eps
+            lm, tm = loss()
+            flat[idx] = old
+            if not (np.array_equal(tp, r["topk"]) and np.array_equal(tm, r["topk"])):
+                continue
+            an = g[gn].reshape(-1)[idx]
+            assert abs((lp - lm) / (2 * eps) - an) <= 1e-6 * max(1.0, abs(an)), (gn, idx)
+            checked += 1
+    assert checked >= 40
