@@ -274,6 +274,19 @@ moe_status_t moe_fp8_quantize(int rows, int cols, int mode, const void* in, uint
  * overwritten). Errors: INVALID_ARG, CUDA. */
 moe_status_t moe_diag_wait_timeout(void* ws, moe_stream_t stream);
 
+/* Auxiliary-loss-free load balancing: one update of the per-expert router
+ * logit bias ("Scalable Training of Mixture-of-Experts Models with Megatron
+ * Core", §7 Load Balancing, "auxiliary-loss-free biasing"; the pages give no
+ * rule): with c_e the tokens expert e received in the last forward (the
+ * `counts` output) and c_mean their mean over the E experts,
+ *   b_e <- b_e + rate * sign(c_mean - c_e),   sign(0) = 0,
+ * so under-loaded experts become more likely to be selected and over-loaded
+ * ones less. The comparison is exact (integers: E*c_e against sum of c).
+ * counts: E int32, b: E fp32 (updated in place), device pointers, enqueued
+ * on `stream`. Errors: INVALID_ARG (null, E outside 1..256, rate not
+ * finite), CUDA. */
+moe_status_t moe_update_bias(int E, const int32_t* counts, float rate, float* b, moe_stream_t stream);
+
 /* MOE_ABI_VERSION of the loaded library. */
 int moe_abi_version(void);
 

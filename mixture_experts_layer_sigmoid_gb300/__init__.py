@@ -34,7 +34,8 @@ MOE_FLAG_FOLD_GATES = 2
 # Names the library exports (include/moe.h).
 EXPORTS = ("moe_plan_create", "moe_plan_destroy", "moe_workspace_size", "moe_forward",
            "moe_backward", "moe_read_status", "moe_status_string", "moe_stage_times",
-           "moe_route_static", "moe_fp8_quantize", "moe_diag_wait_timeout", "moe_abi_version")
+           "moe_route_static", "moe_fp8_quantize", "moe_diag_wait_timeout", "moe_update_bias",
+           "moe_abi_version")
 MOE_Q_ROWS, MOE_Q_TILES, MOE_Q_COLS_T, MOE_Q_TILES_T = 0, 1, 2, 3
 
 
@@ -96,6 +97,7 @@ def load_library() -> ctypes.CDLL:
         lib.moe_fp8_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp,
                                          _vp, _vp]
         lib.moe_diag_wait_timeout.argtypes = [_vp, _vp]
+        lib.moe_update_bias.argtypes = [ctypes.c_int, _vp, ctypes.c_float, _vp, _vp]
         lib.moe_abi_version.argtypes = []
         for n in EXPORTS:
             if n not in ("moe_status_string", "moe_abi_version"):
@@ -169,6 +171,13 @@ def moe_fp8_quantize(rows: int, cols: int, mode: int, x: int, codes: int, scales
     st = load_library().moe_fp8_quantize(rows, cols, mode, x, codes, scales, codes_t, scales_t, stream)
     if st != MOE_OK:
         raise MoEError(st, "moe_fp8_quantize")
+
+
+def moe_update_bias(E: int, counts: int, rate: float, b: int, stream: int) -> None:
+    """Auxiliary-loss-free bias update: b_e += rate * sign(mean count - count_e)."""
+    st = load_library().moe_update_bias(E, counts, rate, b, stream)
+    if st != MOE_OK:
+        raise MoEError(st, "moe_update_bias")
 
 
 # ------------------------------------------------- torch-allocated wrapper

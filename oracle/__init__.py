@@ -116,6 +116,16 @@ def capacity_keep(topk, E, C):
     return keep
 
 
+def update_bias(b, counts, rate):
+    """Auxiliary-loss-free load balancing ("Scalable Training of
+    Mixture-of-Experts Models with Megatron Core", §7 Load Balancing, no rule
+    printed): b_e + rate * sign(mean(counts) - counts_e), sign(0) = 0, in
+    fp32 as the bias is stored."""
+    counts = np.asarray(counts, np.int64)
+    d = counts.sum() - len(counts) * counts          # E * (mean - c_e), exact
+    return (np.asarray(b, np.float32) + np.float32(rate) * np.sign(d).astype(np.float32)).astype(np.float32)
+
+
 def capacity(T, k, E, factor):
     """Rows an expert computes: ceil(factor * T * k / E)."""
     return int(np.ceil(np.float64(np.float32(factor)) * T * k / E))

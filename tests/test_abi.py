@@ -83,3 +83,11 @@ def test_valid_config_without_gpu_fails_cleanly(lib):
     st = lib.moe_plan_create(ctypes.byref(_cfg()), 0, ctypes.byref(plan))
     assert st in (moe.MOE_ERR_CUDA, moe.MOE_ERR_INVALID_ARG)
     assert plan.value is None
+
+
+def test_update_bias_rejects_bad_arguments(lib):
+    buf = ctypes.c_void_p(16)        # never dereferenced: rejected before any launch
+    for E, counts, rate, b in ((0, buf, 0.1, buf), (257, buf, 0.1, buf), (8, None, 0.1, buf),
+                               (8, buf, 0.1, None), (8, buf, float("nan"), buf),
+                               (8, buf, float("inf"), buf)):
+        assert lib.moe_update_bias(E, counts, rate, b, None) == moe.MOE_ERR_INVALID_ARG

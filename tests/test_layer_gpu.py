@@ -199,3 +199,20 @@ def test_forward_backward_capture_in_a_cuda_graph():
     assert torch.equal(y, eager["y"])
     for k, v in grads.items():
         assert torch.equal(v, eager[k]), k
+
+
+def test_update_bias_matches_oracle():
+    import oracle
+    import mixture_experts_layer_sigmoid_gb300 as moe
+    rng = np.random.default_rng(3)
+    for E in (1, 8, 37, 256):
+        counts = rng.integers(0, 500, E).astype(np.int32)
+        if E == 8:
+            counts[:] = 40                         # balanced: no change
+        b = rng.standard_normal(E).astype(np.float32)
+        c_d = torch.as_tensor(counts).cuda()
+        b_d = torch.as_tensor(b).cuda()
+        moe.moe_update_bias(E, c_d.data_ptr(), 0.01, b_d.data_ptr(),
+                            torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        assert np.array_equal(b_d.cpu().numpy(), oracle.update_bias(b, counts, 0.01)), E

@@ -392,3 +392,22 @@ def test_capacity_backward_finite_differences(score):
             assert abs((lp - lm) / (2 * eps) - an) <= 1e-6 * max(1.0, abs(an)), (gn, idx)
             checked += 1
     assert checked >= 40
+
+
+# ------------------------------------------ auxiliary-loss-free bias update
+def test_update_bias_moves_load_towards_the_mean():
+    counts = np.array([10, 2, 6, 6, 0, 12], np.int32)        # mean 6
+    b = np.array([0.5, -0.25, 0.0, 1.0, 0.0, -1.0], np.float32)
+    nb = oracle.update_bias(b, counts, 0.125)
+    np.testing.assert_array_equal(nb, np.array([0.375, -0.125, 0.0, 1.0, 0.125, -1.125], np.float32))
+    # a balanced load leaves the bias unchanged; the step sizes are +-rate or 0
+    assert np.array_equal(oracle.update_bias(b, np.full(6, 7, np.int32), 0.3), b)
+    d = oracle.update_bias(np.zeros(6, np.float32), counts, 1.0)
+    assert set(d.tolist()) <= {-1.0, 0.0, 1.0}
+
+
+def test_update_bias_mean_is_compared_exactly():
+    # mean 10/3: no expert is at the mean; a float mean could misclassify
+    counts = np.array([3, 3, 4], np.int32)
+    nb = oracle.update_bias(np.zeros(3, np.float32), counts, 1.0)
+    np.testing.assert_array_equal(nb, np.array([1.0, 1.0, -1.0], np.float32))
