@@ -89,7 +89,8 @@ typedef struct {
                     (token, slot) assignments it received, the earliest tokens
                     first; a dropped assignment adds nothing to y, gets no
                     expert gradient and has dg = 0 (its routing gradient still
-                    flows through the other slots' renormalised gates). */
+                    flows through the other slots' renormalised gates).
+                    MOE_FP8_BLOCK with capacity_factor > 0: UNSUPPORTED. */
 } moe_config_t;
 
 /* Plan flag: bracket every kernel launch of moe_forward / moe_backward with

@@ -133,6 +133,10 @@ moe_status_t check_config(const moe_config_t* c)
     if (c->dtype != MOE_FP32 && c->dtype != MOE_BF16 && c->dtype != MOE_FP8_BLOCK)
         return MOE_ERR_INVALID_ARG;
     if (c->dtype == MOE_FP8_BLOCK && c->Fs > 0) return MOE_ERR_UNSUPPORTED;
+    // a dropped assignment keeps its row of Xp (the router gradient needs it),
+    // which would enter the 128-token quantisation blocks of the FP8 weight
+    // gradients; dropping is built for the bf16 and fp32 layers only
+    if (c->dtype == MOE_FP8_BLOCK && c->capacity_factor > 0.f) return MOE_ERR_UNSUPPORTED;
     // int32 row indices: R_pad * max(H, F) elements must stay addressable per
     // buffer with 32-bit row numbers
     const long long R = (long long)c->T_max * c->top_k + (long long)c->E * kTileM;

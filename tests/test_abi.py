@@ -58,6 +58,12 @@ def test_plan_create_rejects_bad_configs(lib, bad):
     assert plan.value is None
 
 
+def test_fp8_with_capacity_dropping_is_reported_unsupported(lib):
+    plan = ctypes.c_void_p()
+    assert lib.moe_plan_create(ctypes.byref(_cfg(dtype=2, capacity_factor=1.0)), 0,
+                               ctypes.byref(plan)) == moe.MOE_ERR_UNSUPPORTED
+
+
 def test_fp8_with_shared_expert_is_reported_unsupported(lib):
     plan = ctypes.c_void_p()
     assert lib.moe_plan_create(ctypes.byref(_cfg(dtype=2, Fs=256)), 0, ctypes.byref(plan)) == moe.MOE_ERR_UNSUPPORTED

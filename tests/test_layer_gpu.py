@@ -26,6 +26,10 @@ CASES = {
     "rows_in_cta_pairs": mi.scaled(W["mixtral_8x7b"], T=1100, H=256, E=4, k=2, F=256),
     "qwen_e128_tiled_router": mi.scaled(W["qwen3_235b"], T=700, H=256, E=128, F=128),
     "deepseek_e256_sigmoid_shared": mi.scaled(W["deepseek_v3"], T=512, H=256, E=256, F=128, Fs=128),
+    # degenerate sizes: one token (one router block, one padded row per expert)
+    "one_token": mi.scaled(W["mixtral_8x7b"], T=1, H=128, E=4, k=2, F=128),
+    "one_token_fp32_shared": mi.scaled(W["deepseek_v3"], T=1, H=128, E=8, k=3, F=128, Fs=128,
+                                       dtype=mi.FP32),
 }
 
 
