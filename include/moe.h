@@ -252,9 +252,10 @@ moe_status_t moe_route_static(moe_plan_t plan, int T, const void* x, const float
  * Mixture-of-Experts Models with Megatron Core", §5, blockwise FP8).
  *   MOE_Q_ROWS:    1x128 blocks along rows: codes rows x cols,
  *                  scales rows x cols/128.
- *   MOE_Q_TILES:   128x128 blocks: codes rows x cols and the transposed
- *                  codes_t cols x rows; scales (rows/128) x (cols/128) and
- *                  scales_t (cols/128) x (rows/128).
+ *   MOE_Q_TILES:   128x128 blocks: codes rows x cols, scales (rows/128) x
+ *                  (cols/128); with codes_t and scales_t (both or neither)
+ *                  also the transposed codes_t cols x rows and scales_t
+ *                  (cols/128) x (rows/128).
  *   MOE_Q_COLS_T:  per column over 128-row blocks, transposed output:
  *                  codes_t cols x rows, scales_t cols x rows/128.
  *   MOE_Q_TILES_T: 128x128 blocks, transposed output: codes_t cols x rows,

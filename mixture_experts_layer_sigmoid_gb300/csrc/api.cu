@@ -26,7 +26,7 @@ struct Layout {
     size_t topk, gates, selsc, counts, kept, poff, meta, tiletab, pairtab, rowof, slotof;
     size_t Xp, A, U, Hh, Yp, As, Us, Hs, saved_bytes;
     // workspace
-    size_t status, hist, blkbase, Ys, dYp, dA, dU, dXp, dz, WrT, dAs, dUs, dXs, dgpart, ws_bytes;
+    size_t status, hist, blkbase, Ys, dYp, dA, dU, dXp, dz, WrT, wrpart, dAs, dUs, dXs, dgpart, ws_bytes;
     bool fold;   // Hh and Yp live in the workspace (MOE_FLAG_FOLD_GATES)
     // blockwise FP8 (saved: permuted activations and weights; ws: the rest)
     size_t Xq, sX, WgQ, sWg, WuQ, sWu, WgQT, sWgT, WuQT, sWuT, WdQ, sWd, WdQT, sWdT;
@@ -73,10 +73,10 @@ Layout make_layout(const moe_config_t& c, int T)
     L.sX = take(q8 ? 4 * Rp * (c.H / 128) : 0);
     L.WgQ = take(q8 ? EHF : 0);   L.sWg = take(q8 ? 4 * sHF : 0);
     L.WuQ = take(q8 ? EHF : 0);   L.sWu = take(q8 ? 4 * sHF : 0);
-    L.WgQT = take(q8 ? EHF : 0);  L.sWgT = take(q8 ? 4 * sHF : 0);
-    L.WuQT = take(q8 ? EHF : 0);  L.sWuT = take(q8 ? 4 * sHF : 0);
+    L.WgQT = take(0);  L.sWgT = take(0);   // (one orientation of the weight codes)
+    L.WuQT = take(0);  L.sWuT = take(0);
     L.WdQ = take(q8 ? EHF : 0);   L.sWd = take(q8 ? 4 * sHF : 0);
-    L.WdQT = take(q8 ? EHF : 0);  L.sWdT = take(q8 ? 4 * sHF : 0);
+    L.WdQT = take(0);  L.sWdT = take(0);
     L.saved_bytes = o;
     o = 0;
     L.status = take(256);
@@ -89,6 +89,7 @@ Layout make_layout(const moe_config_t& c, int T)
     L.dXp = take(es * L.Rp_max * c.H);
     L.dz = take(sizeof(float) * L.R);
     L.WrT = take(sizeof(float) * (size_t)c.E * c.H);
+    L.wrpart = take(sizeof(float) * (size_t)L.MT_max * c.H);
     L.dAs = take(es * (size_t)T * c.Fs);
     L.dUs = take(es * (size_t)T * c.Fs);
     L.dXs = take(c.Fs ? es * (size_t)T * c.H : 0);
@@ -555,7 +556,8 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
         MOE_STAGE(ST_FC1S_WGRAD, gemm(d));
     }
     // router backward and the unpermute-reduce of dX
-    MOE_STAGE(ST_ROUTER_WGRAD, launch_router_wgrad<T>(Xp, slotof, poff, counts, dz, H, E, k, a->dWr, s));
+    MOE_STAGE(ST_ROUTER_WGRAD, launch_router_wgrad<T>(Xp, slotof, poff, meta, L.MT_max, dz, H, E,
+                                   reinterpret_cast<float*>(ws + L.wrpart), a->dWr, s));
     MOE_STAGE(ST_TRANSPOSE, launch_transpose_f32(a->Wr, H, E, WrT, s));
     MOE_STAGE(ST_UNPERMUTE, launch_unpermute_reduce<T>(dXp, dXs, rowof, topk, dz, WrT, T_, H, k,
                                         static_cast<T*>(a->dX), s));
@@ -603,12 +605,14 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
     MOE_STAGE(ST_PERMUTE, launch_permute_quant(x, rowof, poff, counts, T_, H, E, k, Xp, u8(sv, L.Xq),
                                                f32(sv, L.sX), s));
+    // one orientation of the weight codes: the forward GEMMs read them
+    // MN-major, the data-gradient GEMMs K-major
     MOE_STAGE(ST_WQUANT, launch_quant_w(static_cast<const T*>(a->W_gate), E, H, F, u8(sv, L.WgQ),
-                                        f32(sv, L.sWg), u8(sv, L.WgQT), f32(sv, L.sWgT), s));
+                                        f32(sv, L.sWg), nullptr, nullptr, s));
     MOE_STAGE(ST_WQUANT, launch_quant_w(static_cast<const T*>(a->W_up), E, H, F, u8(sv, L.WuQ),
-                                        f32(sv, L.sWu), u8(sv, L.WuQT), f32(sv, L.sWuT), s));
+                                        f32(sv, L.sWu), nullptr, nullptr, s));
     MOE_STAGE(ST_WQUANT, launch_quant_w(static_cast<const T*>(a->W_down), E, F, H, u8(sv, L.WdQ),
-                                        f32(sv, L.sWd), u8(sv, L.WdQT), f32(sv, L.sWdT), s));
+                                        f32(sv, L.sWd), nullptr, nullptr, s));
     GemmDesc d;
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
@@ -616,8 +620,8 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(sv, L.Xq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(sv, L.sX); d.lds_a = H / 128;
-    d.B0 = u8(sv, L.WgQT); d.B1 = u8(sv, L.WuQT); d.ldb = H; d.b_rows = E * F;
-    d.SB0 = f32(sv, L.sWgT); d.SB1 = f32(sv, L.sWuT);
+    d.B0 = u8(sv, L.WgQ); d.B1 = u8(sv, L.WuQ); d.ldb = F; d.b_rows = E * H; d.b_kmajor = 0;
+    d.SB0 = f32(sv, L.sWg); d.SB1 = f32(sv, L.sWu);
     d.O0 = A; d.O1 = U; d.O2 = Hh; d.ldo = F; d.status = status;
     if (L.fold) { d.gates = gates; d.slot_of = slotof; }   // Hh = g silu(A) U
     MOE_STAGE(ST_FC1, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
@@ -628,7 +632,7 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.hq); d.lda = F; d.a_rows = Rp; d.SA0 = f32(ws, L.sh); d.lds_a = F / 128;
-    d.B0 = u8(sv, L.WdQT); d.ldb = F; d.b_rows = E * H; d.SB0 = f32(sv, L.sWdT);
+    d.B0 = u8(sv, L.WdQ); d.ldb = H; d.b_rows = E * F; d.SB0 = f32(sv, L.sWd); d.b_kmajor = 0;
     d.O0 = Yp; d.ldo = H; d.status = status;
     MOE_STAGE(ST_FC2, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
     MOE_STAGE(ST_COMBINE, launch_combine<T>(Yp, nullptr, rowof, L.fold ? nullptr : gates, T_, H, k,
@@ -693,7 +697,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.dYq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(ws, L.sdY); d.lds_a = H / 128;
-    d.B0 = u8(sv, L.WdQ); d.ldb = H; d.b_rows = E * F; d.SB0 = f32(sv, L.sWd);
+    d.B0 = u8(sv, L.WdQ); d.ldb = H; d.b_rows = E * F; d.SB0 = f32(sv, L.sWd); d.b_kmajor = 1;
     d.X0 = A; d.X1 = U; d.O0 = dA; d.O1 = dU; d.ldo = F; d.status = status;
     if (L.fold) {
         d.gates = gates; d.slot_of = slotof; d.dg_part = dgpart; d.dg_ld = F / 64;
@@ -725,7 +729,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.dAq); d.A1 = u8(ws, L.dUq); d.lda = F; d.a_rows = Rp;
     d.SA0 = f32(ws, L.sdA); d.SA1 = f32(ws, L.sdU); d.lds_a = F / 128;
-    d.B0 = u8(sv, L.WgQ); d.B1 = u8(sv, L.WuQ); d.ldb = F; d.b_rows = E * H;
+    d.B0 = u8(sv, L.WgQ); d.B1 = u8(sv, L.WuQ); d.ldb = F; d.b_rows = E * H; d.b_kmajor = 1;
     d.SB0 = f32(sv, L.sWg); d.SB1 = f32(sv, L.sWu);
     d.O0 = dXp; d.ldo = H; d.status = status;
     MOE_STAGE(ST_FC1_DGRAD, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
@@ -745,7 +749,8 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.O0 = a->dW_gate; d.O1 = a->dW_up; d.ldo = F; d.o_estride = (long long)H * F; d.status = status;
     MOE_STAGE(ST_FC1_WGRAD, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
     // router backward and the unpermute-reduce of dX
-    MOE_STAGE(ST_ROUTER_WGRAD, launch_router_wgrad<T>(Xp, slotof, poff, counts, dz, H, E, k, a->dWr, s));
+    MOE_STAGE(ST_ROUTER_WGRAD, launch_router_wgrad<T>(Xp, slotof, poff, meta, L.MT_max, dz, H, E,
+                                   reinterpret_cast<float*>(ws + L.wrpart), a->dWr, s));
     MOE_STAGE(ST_TRANSPOSE, launch_transpose_f32(a->Wr, H, E, WrT, s));
     MOE_STAGE(ST_UNPERMUTE, launch_unpermute_reduce<T>(dXp, nullptr, rowof, topk, dz, WrT, T_, H, k,
                                                        static_cast<T*>(a->dX), s));
@@ -850,7 +855,7 @@ moe_status_t moe_fp8_quantize(int rows, int cols, int mode, const void* in, uint
         e = launch_quant_rows(x, nullptr, rows, cols, codes, scales, s);
         break;
     case MOE_Q_TILES:
-        if (!codes || !scales || !codes_t || !scales_t) return MOE_ERR_INVALID_ARG;
+        if (!codes || !scales || (!codes_t) != (!scales_t)) return MOE_ERR_INVALID_ARG;
         e = launch_quant_w(x, 1, rows, cols, codes, scales, codes_t, scales_t, s);
         break;
     case MOE_Q_COLS_T:

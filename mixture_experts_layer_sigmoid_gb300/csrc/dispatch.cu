@@ -210,54 +210,73 @@ gate_dz_kernel(const float* __restrict__ dg_part, int nslots, const int* __restr
     if (lane == 0) router_dz(dg, g, selsc + (size_t)t * k, k, score, dz + (size_t)t * k);
 }
 
-// dWr[h][e] = sum over expert e's rows r of Xp[r][h] dz[slot(r)]. Block
-// (64 columns h, expert e), 256 threads = 32 row phases x 8 column groups of
-// 8 columns (one 16-byte vector each). The segment is walked in chunks of 256
-// rows whose dz values are first gathered into shared memory; each phase sums
-// every 32nd row of a chunk, and the 32 phases are added in fixed order.
+// dWr[h][e] = sum over expert e's rows r of Xp[r][h] dz[slot(r)], in two
+// passes so that a hot expert's rows are spread over many blocks.
+// Pass 1, block (128-row tile, 64 columns h): 256 threads = 32 row phases x
+// 8 column groups of 8 columns (one 16-byte vector each); each phase sums
+// rows ph, ph + 32, ph + 64, ph + 96 of the tile (pad rows, slot -1, add 0),
+// and the 32 phases are added in fixed order into part[tile][h].
 template <typename T>
 __global__ void __launch_bounds__(256)
-router_wgrad_kernel(const T* __restrict__ Xp, const int* __restrict__ slot_of,
-                    const int* __restrict__ poff, const int* __restrict__ counts,
-                    const float* __restrict__ dz, int H, int E, float* __restrict__ dWr)
+router_wgrad_tile_kernel(const T* __restrict__ Xp, const int* __restrict__ slot_of,
+                         const int* __restrict__ meta, const float* __restrict__ dz, int H,
+                         float* __restrict__ part)
 {
     constexpr int V = 16 / sizeof(T);            // columns per vector
     constexpr int CG = 64 / V;                   // column groups per block
     constexpr int PH = 256 / CG;                 // row phases
-    __shared__ float part[PH][64 + 1];
-    __shared__ float dzs[256];
-    const int e = blockIdx.y;
+    constexpr int RPT = kTileM / PH;             // rows per thread
+    __shared__ float red[PH][64 + 1];
+    __shared__ float dzs[kTileM];
+    const int tile = blockIdx.x;
+    if (tile >= meta[0]) return;                 // block-uniform
     const int cg = threadIdx.x % CG, ph = threadIdx.x / CG;
-    const int h0 = blockIdx.x * 64 + cg * V;
-    const int r0 = poff[e], n = counts[e];
+    const int h0 = blockIdx.y * 64 + cg * V;
+    const int r0 = tile * kTileM;
+    if (threadIdx.x < kTileM) {
+        const int slot = slot_of[r0 + threadIdx.x];
+        dzs[threadIdx.x] = slot >= 0 ? dz[slot] : 0.f;
+    }
+    float xv[RPT][V];
+    if (h0 < H) {
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) Vec<T>::load(Xp + (size_t)(r0 + ph + PH * i) * H + h0, xv[i]);
+    }
+    __syncthreads();
     float acc[V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) acc[i] = 0.f;
-    for (int c0 = 0; c0 < n; c0 += 256) {
-        __syncthreads();
-        if (c0 + (int)threadIdx.x < n) dzs[threadIdx.x] = dz[slot_of[r0 + c0 + threadIdx.x]];
-        __syncthreads();
-        const int m = min(256, n - c0);
-        if (h0 < H) {
-#pragma unroll 4
-            for (int i = ph; i < m; i += PH) {
-                const float d = dzs[i];
-                float xv[V];
-                Vec<T>::load(Xp + (size_t)(r0 + c0 + i) * H + h0, xv);
+    for (int j = 0; j < V; ++j) acc[j] = 0.f;
+    if (h0 < H) {
 #pragma unroll
-                for (int j = 0; j < V; ++j) acc[j] = fmaf(xv[j], d, acc[j]);
-            }
+        for (int i = 0; i < RPT; ++i) {
+            const float d = dzs[ph + PH * i];
+#pragma unroll
+            for (int j = 0; j < V; ++j) acc[j] = fmaf(xv[i][j], d, acc[j]);
         }
     }
 #pragma unroll
-    for (int j = 0; j < V; ++j) part[ph][cg * V + j] = acc[j];
+    for (int j = 0; j < V; ++j) red[ph][cg * V + j] = acc[j];
     __syncthreads();
     if (threadIdx.x < 64) {
-        const int h = blockIdx.x * 64 + threadIdx.x;
+        const int h = blockIdx.y * 64 + threadIdx.x;
         float v = 0.f;
-        for (int p2 = 0; p2 < PH; ++p2) v += part[p2][threadIdx.x];
-        if (h < H) dWr[(size_t)h * E + e] = v;
+        for (int p2 = 0; p2 < PH; ++p2) v += red[p2][threadIdx.x];
+        if (h < H) part[(size_t)tile * H + h] = v;
     }
+}
+
+// Pass 2: dWr[h][e] = sum of part[tile][h] over expert e's tiles, in tile
+// order (0 for an empty expert).
+__global__ void __launch_bounds__(256)
+router_wgrad_sum_kernel(const float* __restrict__ part, const int* __restrict__ poff, int H, int E,
+                        float* __restrict__ dWr)
+{
+    const int h = blockIdx.x * 256 + threadIdx.x, e = blockIdx.y;
+    if (h >= H) return;
+    const int a = poff[e] / kTileM, z = poff[e + 1] / kTileM;
+    float v = 0.f;
+    for (int tile = a; tile < z; ++tile) v += part[(size_t)tile * H + h];
+    dWr[(size_t)h * E + e] = v;
 }
 
 __global__ void transpose_kernel(const float* __restrict__ in, int rows, int cols, float* __restrict__ out)
@@ -359,13 +378,16 @@ cudaError_t launch_gate_dz(const float* dg_part, int nslots, const int* row_of, 
 }
 
 template <typename T>
-cudaError_t launch_router_wgrad(const T* Xp, const int* slot_of, const int* poff,
-                                const int* counts, const float* dz, int H, int E, int k,
-                                float* dWr, cudaStream_t s)
+cudaError_t launch_router_wgrad(const T* Xp, const int* slot_of, const int* poff, const int* meta,
+                                int MT_max, const float* dz, int H, int E, float* part, float* dWr,
+                                cudaStream_t s)
 {
-    (void)k;
-    dim3 grid((H + 63) / 64, E);
-    router_wgrad_kernel<T><<<grid, 256, 0, s>>>(Xp, slot_of, poff, counts, dz, H, E, dWr);
+    if (MT_max > 0) {
+        dim3 grid1(MT_max, (H + 63) / 64);
+        router_wgrad_tile_kernel<T><<<grid1, 256, 0, s>>>(Xp, slot_of, meta, dz, H, part);
+    }
+    dim3 grid2((H + 255) / 256, E);
+    router_wgrad_sum_kernel<<<grid2, 256, 0, s>>>(part, poff, H, E, dWr);
     return cudaGetLastError();
 }
 
@@ -394,7 +416,7 @@ cudaError_t launch_unpermute_reduce(const T* dXp, const T* dXs, const int* row_o
                                              const float*, const float*, const int*, const int*, \
                                              int, int, int, int, int, T*, float*, cudaStream_t); \
     template cudaError_t launch_router_wgrad<T>(const T*, const int*, const int*, const int*,    \
-                                                const float*, int, int, int, float*,             \
+                                                int, const float*, int, int, float*, float*,     \
                                                 cudaStream_t);                                   \
     template cudaError_t launch_unpermute_reduce<T>(const T*, const T*, const int*, const int*,  \
                                                     const float*, const float*, int, int, int,   \

@@ -7,7 +7,11 @@
 // (rows = output rows) carries one fp32 scale per row and 128-deep K block,
 // B one per 128x128 block, so
 //   C[r][n] = sum_kb sA[r][kb] sB[kb][n/128] (sum_{k in kb} qA[r][k] qB[k][n]).
-// Both operands are stored K-major in E4M3.
+// A is stored K-major in E4M3; B is K-major, or (forward GEMMs, B_MN) the
+// weights' natural [E][K][N] codes read MN-major, so a weight matrix is
+// quantised in one orientation and serves both the forward GEMM (MN-major)
+// and the data-gradient GEMM (K-major); its 128x128 block scales are then
+// read as [E][K/128][N/128].
 //
 // Ten warps per CTA: warp 0 TMA producer (stages of A 128x128 B and this
 // CTA's share of B, 128-byte swizzle); warp 1 TMEM allocator and, in the
@@ -53,10 +57,11 @@ struct QCfg {
     static constexpr int SMEM = 1024 + STAGES * STAGE + 256;
 };
 
-// f8f6f4 instruction descriptor: E4M3 A and B (format 0), fp32 D, K-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int N, int M)
+// f8f6f4 instruction descriptor: E4M3 A and B (format 0), fp32 D, A K-major,
+// B K-major or MN-major (bit 16).
+__host__ __device__ constexpr uint32_t idesc_e4m3(int N, int M, bool b_mn)
 {
-    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+    return (1u << 4) | (b_mn ? (1u << 16) : 0u) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_e4m3(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
@@ -195,7 +200,7 @@ __device__ __forceinline__ QTile qdecode(const GemmDesc& d, int w, int num_m, in
     return t;
 }
 
-template <int EPI, int SCHED, int DUAL, bool PAIR>
+template <int EPI, int SCHED, int DUAL, bool PAIR, bool B_MN>
 __global__ void __launch_bounds__(kQThreads, 1)
 gemm_fp8_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                 const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
@@ -203,7 +208,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__
 {
     using C = QCfg<PAIR>;
     constexpr int NW = (DUAL == DUAL_N) ? QBN / 2 : QBN;   // output columns per tile
-    constexpr uint32_t IDESC = idesc_e4m3(kPCols, PAIR ? 2 * QBM : QBM);
+    static_assert(!B_MN || (SCHED == SCHED_ROWS && DUAL != DUAL_K && !kSplitN), "MN-major B: forward GEMMs");
+    constexpr uint32_t IDESC = idesc_e4m3(kPCols, PAIR ? 2 * QBM : QBM, B_MN);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
@@ -310,7 +316,20 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__
                     const CUtensorMap* p0 = (DUAL == DUAL_N) ? &mB0 : bm;
                     const CUtensorMap* p1 = (DUAL == DUAL_N) ? &mB1 : bm;
                     const int r1 = (DUAL == DUAL_N) ? brow : brow + 128;
-                    if (PAIR) {
+                    if (B_MN) {
+                        // MN-major: each part is one 128-column x 128-deep stripe of
+                        // the expert's [K][N] codes, at column n0 (part 1: DUAL_N, the
+                        // same columns of B1; otherwise the next 128 columns)
+                        const int n0 = t.n * NW;
+                        const int c1 = (DUAL == DUAL_N) ? n0 : n0 + 128;
+                        const int krow = t.e * d.K + kx;
+                        if (PAIR) {
+                            load(b_dst, rank ? p1 : p0, s, rank ? c1 : n0, krow);
+                        } else {
+                            load(b_dst, p0, s, n0, krow);
+                            load(b_dst + 128 * QBK, p1, s, c1, krow);
+                        }
+                    } else if (PAIR) {
                         load(b_dst, rank ? p1 : p0, s, kx, rank ? r1 : brow);
                     } else {
                         load(b_dst, p0, s, kx, brow);
@@ -348,7 +367,10 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__
 #pragma unroll
                             for (int k = 0; k < QBK / 32; ++k) {
                                 const uint64_t ad = ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
-                                const uint64_t bd = ptx::smem_desc_sw128(bh + k * 32, 16, 1024);
+                                // MN-major: 32 rows of 128 bytes per K=32 step, stripes of
+                                // 128 columns 16 KB apart
+                                const uint64_t bd = B_MN ? ptx::smem_desc_sw128(bh + k * 4096, 128 * QBK, 1024)
+                                                         : ptx::smem_desc_sw128(bh + k * 32, 16, 1024);
                                 if (PAIR) mma_e4m3_pair(dt, ad, bd, IDESC, k > 0 ? 1u : 0u);
                                 else mma_e4m3(dt, ad, bd, IDESC, k > 0 ? 1u : 0u);
                             }
@@ -421,7 +443,13 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__
                     if (arow_ok) sa = (second ? d.SA1 : d.SA0)[(size_t)arow * d.lds_a + kk];
                     const size_t kbs = d.K / 128;
                     const size_t e0 = (size_t)t.e * (d.N / 128);
-                    if (DUAL == DUAL_N) {
+                    if (B_MN) {
+                        // natural block layout [E][K/128][N/128]
+                        const float* sbrow = d.SB0 + ((size_t)t.e * kbs + kk) * (d.N / 128);
+                        sb_lo = sbrow[nb_lo];
+                        if (DUAL == DUAL_N) sb_hi = d.SB1[((size_t)t.e * kbs + kk) * (d.N / 128) + nb_hi];
+                        else if (hi_ok) sb_hi = sbrow[nb_hi];
+                    } else if (DUAL == DUAL_N) {
                         sb_lo = d.SB0[(e0 + nb_lo) * kbs + kk];
                         sb_hi = d.SB1[(e0 + nb_hi) * kbs + kk];
                     } else {
@@ -638,7 +666,7 @@ bool map8(CUtensorMap* m, const void* ptr, long long rows, long long cols, long 
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int EPI, int SCHED, int DUAL>
+template <int EPI, int SCHED, int DUAL, bool B_MN>
 int qpair_slots()
 {
     static int slots = -1;
@@ -655,7 +683,7 @@ int qpair_slots()
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_fp8_kernel<EPI, SCHED, DUAL, true>, &cfg) != cudaSuccess)
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_fp8_kernel<EPI, SCHED, DUAL, true, B_MN>, &cfg) != cudaSuccess)
             n = 0;
         cudaGetLastError();
         slots = n;
@@ -663,7 +691,7 @@ int qpair_slots()
     return slots;
 }
 
-template <int EPI, int SCHED, int DUAL, bool PAIR>
+template <int EPI, int SCHED, int DUAL, bool PAIR, bool B_MN>
 cudaError_t qrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
 {
     using C = QCfg<PAIR>;
@@ -678,8 +706,13 @@ cudaError_t qrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s
     if (SCHED == SCHED_ROWS) {
         ok &= map8(&mA0, d.A0, d.a_rows, d.K, d.lda, QBM);
         ok &= map8(&mA1, d.A1 ? d.A1 : d.A0, d.a_rows, d.K, d.lda, QBM);
-        ok &= map8(&mB0, d.B0, d.b_rows, d.K, d.ldb, BROWS);
-        ok &= map8(&mB1, d.B1 ? d.B1 : d.B0, d.b_rows, d.K, d.ldb, BROWS);
+        if (B_MN) {   // [E*K][N] codes, 128-column x 128-row boxes
+            ok &= map8(&mB0, d.B0, d.b_rows, d.N, d.ldb, QBK);
+            ok &= map8(&mB1, d.B1 ? d.B1 : d.B0, d.b_rows, d.N, d.ldb, QBK);
+        } else {      // [E*N][K] codes
+            ok &= map8(&mB0, d.B0, d.b_rows, d.K, d.ldb, BROWS);
+            ok &= map8(&mB1, d.B1 ? d.B1 : d.B0, d.b_rows, d.K, d.ldb, BROWS);
+        }
         const long long m_units = PAIR ? (max_m_tiles + 1) / 2 : max_m_tiles;
         units = m_units * num_n;
     } else {
@@ -694,10 +727,10 @@ cudaError_t qrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s
     if (units <= 0) return cudaSuccess;
     if (!PAIR) {
         const int grid = (int)(units < num_sms ? units : num_sms);
-        gemm_fp8_kernel<EPI, SCHED, DUAL, false><<<grid, kQThreads, C::SMEM, s>>>(mA0, mA1, mB0, mB1, d);
+        gemm_fp8_kernel<EPI, SCHED, DUAL, false, B_MN><<<grid, kQThreads, C::SMEM, s>>>(mA0, mA1, mB0, mB1, d);
         return cudaGetLastError();
     }
-    const int slots = qpair_slots<EPI, SCHED, DUAL>();
+    const int slots = qpair_slots<EPI, SCHED, DUAL, B_MN>();
     if (slots <= 0) return cudaErrorLaunchOutOfResources;
     const long long clusters = units < slots ? units : slots;
     cudaLaunchConfig_t cfg = {};
@@ -712,27 +745,27 @@ cudaError_t qrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI, SCHED, DUAL, true>, mA0, mA1, mB0, mB1, d);
+    return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI, SCHED, DUAL, true, B_MN>, mA0, mA1, mB0, mB1, d);
 }
 
 // CTA pairs when the row units come in (mostly) complete pairs, or the
 // weight-gradient rows split into 256-row pair tiles.
-template <int EPI, int SCHED, int DUAL>
+template <int EPI, int SCHED, int DUAL, bool B_MN = false>
 cudaError_t qrun_any(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
 {
     const bool pair = (SCHED == SCHED_WGRAD) ? d.M_out % (2 * QBM) == 0
                                              : d.pair_tab != nullptr && d.prefer_pair;
-    if (pair) return qrun<EPI, SCHED, DUAL, true>(d, max_m_tiles, num_sms, s);
-    return qrun<EPI, SCHED, DUAL, false>(d, max_m_tiles, num_sms, s);
+    if (pair) return qrun<EPI, SCHED, DUAL, true, B_MN>(d, max_m_tiles, num_sms, s);
+    return qrun<EPI, SCHED, DUAL, false, B_MN>(d, max_m_tiles, num_sms, s);
 }
 
-template <int EPI, int SCHED, int DUAL>
+template <int EPI, int SCHED, int DUAL, bool B_MN = false>
 cudaError_t qattr()
 {
-    cudaError_t e = cudaFuncSetAttribute(gemm_fp8_kernel<EPI, SCHED, DUAL, false>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_fp8_kernel<EPI, SCHED, DUAL, false, B_MN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<false>::SMEM);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gemm_fp8_kernel<EPI, SCHED, DUAL, true>,
+    return cudaFuncSetAttribute(gemm_fp8_kernel<EPI, SCHED, DUAL, true, B_MN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<true>::SMEM);
 }
 
@@ -744,8 +777,8 @@ cudaError_t gemm_fp8_prepare(int device)
     if (!enc8()) return cudaErrorNotSupported;
     cudaError_t e = cudaSuccess;
     auto acc = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
-    acc(qattr<EPI_SWIGLU_FWD, SCHED_ROWS, DUAL_N>());
-    acc(qattr<EPI_STORE, SCHED_ROWS, DUAL_NONE>());
+    acc(qattr<EPI_SWIGLU_FWD, SCHED_ROWS, DUAL_N, true>());
+    acc(qattr<EPI_STORE, SCHED_ROWS, DUAL_NONE, true>());
     acc(qattr<EPI_SWIGLU_BWD, SCHED_ROWS, DUAL_NONE>());
     acc(qattr<EPI_STORE, SCHED_ROWS, DUAL_K>());
     acc(qattr<EPI_WGRAD, SCHED_WGRAD, DUAL_NONE>());
@@ -758,11 +791,20 @@ cudaError_t launch_gemm_fp8(const GemmDesc& d, int max_m_tiles, int num_sms, cud
     if (!enc8()) return cudaErrorNotSupported;
     if (d.sched == SCHED_ROWS) {
         switch (d.epi) {
-        case EPI_SWIGLU_FWD: return qrun_any<EPI_SWIGLU_FWD, SCHED_ROWS, DUAL_N>(d, max_m_tiles, num_sms, s);
-        case EPI_SWIGLU_BWD: return qrun_any<EPI_SWIGLU_BWD, SCHED_ROWS, DUAL_NONE>(d, max_m_tiles, num_sms, s);
+        // forward GEMMs read the weights' natural codes MN-major (b_kmajor 0),
+        // the data-gradient GEMMs K-major (b_kmajor 1)
+        case EPI_SWIGLU_FWD:
+            if (d.b_kmajor) return cudaErrorInvalidValue;
+            return qrun_any<EPI_SWIGLU_FWD, SCHED_ROWS, DUAL_N, true>(d, max_m_tiles, num_sms, s);
+        case EPI_SWIGLU_BWD:
+            if (!d.b_kmajor) return cudaErrorInvalidValue;
+            return qrun_any<EPI_SWIGLU_BWD, SCHED_ROWS, DUAL_NONE>(d, max_m_tiles, num_sms, s);
         case EPI_STORE:
-            return d.dual == DUAL_K ? qrun_any<EPI_STORE, SCHED_ROWS, DUAL_K>(d, max_m_tiles, num_sms, s)
-                                    : qrun_any<EPI_STORE, SCHED_ROWS, DUAL_NONE>(d, max_m_tiles, num_sms, s);
+            if (d.dual == DUAL_K)
+                return d.b_kmajor ? qrun_any<EPI_STORE, SCHED_ROWS, DUAL_K>(d, max_m_tiles, num_sms, s)
+                                  : cudaErrorInvalidValue;
+            return d.b_kmajor ? cudaErrorInvalidValue
+                              : qrun_any<EPI_STORE, SCHED_ROWS, DUAL_NONE, true>(d, max_m_tiles, num_sms, s);
         default: return cudaErrorInvalidValue;
         }
     }

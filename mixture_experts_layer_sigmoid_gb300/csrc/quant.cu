@@ -12,8 +12,8 @@
 //   quant_rows_kernel     [rows][C] bf16 -> codes [rows][C], 1x128 scales
 //   quant_t_kernel        [rows][C] bf16 -> transposed codes [C][rows], scales
 //                         per column over 128 rows, or per 128x128 tile
-//   quant_w_kernel        weights [E][R][C] -> 128x128-block codes in both
-//                         orientations ([E][R][C] and [E][C][R])
+//   quant_w_kernel        weights [E][R][C] -> 128x128-block codes [E][R][C]
+//                         (and optionally [E][C][R])
 #include "internal.h"
 
 #include <cuda_fp8.h>
@@ -287,8 +287,8 @@ quant_t_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__ row
     write_transposed(qs, qT + (size_t)c0 * rows_cap + r0, rows_cap);
 }
 
-// 128x128 block (rb, cb) of expert e of W [E][R][C] -> codes in both
-// orientations and the block's scale in both scale layouts.
+// 128x128 block (rb, cb) of expert e of W [E][R][C] -> codes and the block's
+// scale, and (qT, sT given) the transposed codes and scale layout too.
 __global__ void __launch_bounds__(256)
 quant_w_kernel(const __nv_bfloat16* __restrict__ W, int R, int C, uint8_t* __restrict__ q,
                float* __restrict__ s, uint8_t* __restrict__ qT, float* __restrict__ sT)
@@ -302,9 +302,10 @@ quant_w_kernel(const __nv_bfloat16* __restrict__ W, int R, int C, uint8_t* __res
     const float sc = block_scale(block_max(load_tile(W + base + (size_t)r0 * C + c0, C, tile), red));
     if (threadIdx.x == 0) {
         s[((size_t)e * (R / 128) + rb) * (C / 128) + cb] = sc;
-        sT[((size_t)e * (C / 128) + cb) * (R / 128) + rb] = sc;
+        if (sT) sT[((size_t)e * (C / 128) + cb) * (R / 128) + rb] = sc;
     }
     encode_rows(tile, sc, nullptr, nullptr, qs, q + base + (size_t)r0 * C + c0, C);
+    if (!qT) return;                      // block-uniform
     __syncthreads();
     write_transposed(qs, qT + base + (size_t)c0 * R + r0, R);
 }

@@ -55,155 +55,248 @@ __device__ __forceinline__ void gates_of(const float* sel_z, int k, int score, f
     }
 }
 
+// Top-k of one token held by a warp (lane l has the logits of experts
+// l + 32 i in z[i], -inf past E): k rounds of a warp-shuffle argmax, larger
+// logit first and the lower expert index on equal values (score order equals
+// logit order for softmax and sigmoid), or the replayed experts; lane 0
+// writes the token's experts, gates and selected scores, and sel[0..k).
+template <int EPL>
+__device__ __forceinline__ void warp_route_token(const float (&z)[EPL], int t, int E, int k, int score,
+                                                 const int* replay, DeviceStatus* status, int lane,
+                                                 int* topk, float* gates, float* selsc, int* sel)
+{
+    unsigned taken = 0;
+    int sel_e[kMaxK];
+    float sel_z[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+        if (j >= k) break;
+        if (replay) {
+            // the given expert's logit, from the lane that holds it
+            const int e = replay_expert(replay, (size_t)t * k + j, E, lane == 0 ? status : nullptr);
+            float zi = z[0];
+#pragma unroll
+            for (int i = 1; i < EPL; ++i)
+                if ((e >> 5) == i) zi = z[i];
+            sel_e[j] = e;
+            sel_z[j] = __shfl_sync(0xffffffffu, zi, e & 31);
+            continue;
+        }
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u) && better(z[i], e, bv, bi)) { bv = z[i]; bi = e; }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        }
+        sel_e[j] = bi;
+        sel_z[j] = bv;
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    }
+    if (lane == 0) {
+        float sc[kMaxK], den;
+        gates_of(sel_z, k, score, sc, den);
+        for (int j = 0; j < k; ++j) {
+            topk[(size_t)t * k + j] = sel_e[j];
+            gates[(size_t)t * k + j] = sc[j] / den;
+            selsc[(size_t)t * k + j] = sc[j];
+            sel[j] = sel_e[j];
+        }
+    }
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Router for E > 32. A block routes kRouterTokens = 32 tokens: warps 0-3 sum
+// the logits over the first half of H and warps 4-7 over the second half,
+// and thread (warp w, lane l) accumulates tokens 8 (w % 4) .. +8 against
+// experts l + 32 i (8 x EPL fp32 FMA chains, h ascending within a half).
+// Chunks of HC rows of Wr per half arrive through a two-stage cp.async ring;
+// x chunks are register-prefetched and staged transposed in fp32, so two
+// 16-byte shared loads give a thread its 8 tokens' values of one h. The two
+// halves are added in fixed order, then one warp per token selects the top k.
 template <typename T, int EPL>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, EPL <= 4 ? 3 : 2)
 router_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float* __restrict__ b,
               int T_, int H, int E, int k, int score, int* __restrict__ topk,
               float* __restrict__ gates, float* __restrict__ selsc, int* __restrict__ hist,
               const int* __restrict__ replay, DeviceStatus* __restrict__ status)
 {
-    constexpr int HC = 32;                 // h chunk
-    constexpr int EW = EPL * 32;           // padded expert width
-    __shared__ float xs[kRouterTokens][HC + 1];
-    __shared__ float ws[HC][EW];
+    constexpr int EW = EPL * 32;                          // padded expert width
+    constexpr int HC = (2048 / EW) < 16 ? 2048 / EW : 16; // rows of H per half per chunk
+    constexpr int TQ = 8;                                 // tokens per thread
+    constexpr int V = 16 / sizeof(T);                     // x values per 16-byte load
+    constexpr int XSEG = HC / V;                          // 16-byte pieces per token row per half
+    constexpr int XPIECES = 2 * kRouterTokens * XSEG;     // <= 256
+    static_assert(XPIECES <= 256 && HC % V == 0, "x staging");
+    static_assert(4 * HC * EW >= kRouterTokens * EW, "partial sums reuse the Wr ring");
+    __shared__ __align__(16) float ws[2][2][HC][EW];      // [stage][half][h][expert]
+    __shared__ __align__(16) float xs[2][2][HC][kRouterTokens];   // [stage][half][h][token]
     __shared__ int sel_s[kRouterTokens][kMaxK];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int half = warp >> 2, tq0 = (warp & 3) * TQ;
     const int t0 = blockIdx.x * kRouterTokens;
-    float acc[4][EPL];
+    const int Hh = H / 2;                 // H is a multiple of 128
+    const int nchunk = Hh / HC;
+    const int E4 = E / 4;
+    const bool vec_w = (E & 3) == 0;      // Wr rows are 16-byte aligned
+
+    // This thread's 16-byte pieces of a Wr chunk (at most 4: 2 HC EW / 4 <= 1024
+    // pieces per chunk), as offsets from the chunk's first row; with E not a
+    // multiple of 4 the chunk is copied in 4-byte pieces instead.
+    constexpr int kMaxPieces = (2 * HC * EW / 4 + 255) / 256;
+    int goff[kMaxPieces], soff[kMaxPieces];
+    int npieces = 0;
+    if (vec_w) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+        for (int j = 0; j < kMaxPieces; ++j) {
+            const int i = tid + 256 * j;
+            goff[j] = soff[j] = 0;
+            if (i < 2 * HC * E4) {
+                const int hf = i / (HC * E4), r = (i / E4) % HC, c4 = i % E4;
+                goff[j] = (hf * Hh + r) * E + 4 * c4;
+                soff[j] = (hf * HC + r) * EW + 4 * c4;
+                npieces = j + 1;
+            }
+        }
+    }
+    auto issue_w = [&](int c, int st) {
+        const float* src = Wr + (size_t)c * HC * E;
+        float* dst = &ws[st][0][0][0];
+        if (vec_w) {
+#pragma unroll
+            for (int j = 0; j < kMaxPieces; ++j)
+                if (j < npieces) cp_async16(dst + soff[j], src + goff[j]);
+        } else {
+            for (int i = tid; i < 2 * HC * E; i += 256) {
+                const int hf = i / (HC * E), r = (i / E) % HC, e = i % E;
+                cp_async4(dst + (hf * HC + r) * EW + e, src + (size_t)(hf * Hh + r) * E + e);
+            }
+        }
+        cp_async_commit();
+    };
+    // x piece of this thread: (half, token, segment) of chunk c
+    const int xhf = tid / (kRouterTokens * XSEG), xtok = (tid / XSEG) % kRouterTokens, xseg = tid % XSEG;
+    const bool xload = tid < XPIECES && t0 + xtok < T_;
+    auto load_x = [&](int c, uint4& u) {
+        if (xload)
+            u = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + xtok) * H + xhf * Hh + c * HC + xseg * V);
+        else
+            u = make_uint4(0, 0, 0, 0);
+    };
+    auto store_x = [&](int st, const uint4& u) {
+        if (tid < XPIECES) {
+            const T* p = reinterpret_cast<const T*>(&u);
+#pragma unroll
+            for (int i = 0; i < V; ++i) xs[st][xhf][xseg * V + i][xtok] = to_f32(p[i]);
+        }
+    };
+
+    float acc[TQ][EPL];
+#pragma unroll
+    for (int q = 0; q < TQ; ++q)
 #pragma unroll
         for (int i = 0; i < EPL; ++i) acc[q][i] = 0.f;
 
-    // register double buffering: chunk c+1 is fetched from global memory
-    // while chunk c is multiplied out of shared memory
-    constexpr int WPT = HC * EW / 256;            // Wr values per thread per chunk
-    constexpr int XPT = kRouterTokens * HC / 256; // x values per thread per chunk
-    float wreg[WPT], xreg[XPT];
-    auto fetch = [&](int h0) {
-#pragma unroll
-        for (int i = 0; i < WPT; ++i) {
-            const int idx = tid + 256 * i, hh = idx / EW, e = idx % EW;
-            wreg[i] = (e < E) ? __ldg(Wr + (size_t)(h0 + hh) * E + e) : 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < XPT; ++i) {
-            const int idx = tid + 256 * i, tt = idx / HC, hh = idx % HC;
-            const int t = t0 + tt;
-            xreg[i] = (t < T_) ? to_f32(x[(size_t)t * H + h0 + hh]) : 0.f;
-        }
-    };
-    fetch(0);
-    for (int h0 = 0; h0 < H; h0 += HC) {
-#pragma unroll
-        for (int i = 0; i < WPT; ++i) {
-            const int idx = tid + 256 * i;
-            ws[idx / EW][idx % EW] = wreg[i];
-        }
-#pragma unroll
-        for (int i = 0; i < XPT; ++i) {
-            const int idx = tid + 256 * i;
-            xs[idx / HC][idx % HC] = xreg[i];
+    uint4 xr;
+    issue_w(0, 0);
+    load_x(0, xr);
+    for (int c = 0; c < nchunk; ++c) {
+        const int st = c & 1;
+        store_x(st, xr);
+        if (c + 1 < nchunk) {
+            issue_w(c + 1, st ^ 1);
+            load_x(c + 1, xr);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
         }
         __syncthreads();
-        if (h0 + HC < H) fetch(h0 + HC);
-#pragma unroll 4
+#pragma unroll
         for (int hh = 0; hh < HC; ++hh) {
             float wv[EPL];
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) wv[i] = ws[hh][lane + 32 * i];
+            for (int i = 0; i < EPL; ++i) wv[i] = ws[st][half][hh][lane + 32 * i];
+            const float4 xa = *reinterpret_cast<const float4*>(&xs[st][half][hh][tq0]);
+            const float4 xb = *reinterpret_cast<const float4*>(&xs[st][half][hh][tq0 + 4]);
+            const float xv[TQ] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float xv = xs[warp * 4 + q][hh];
+            for (int q = 0; q < TQ; ++q)
 #pragma unroll
-                for (int i = 0; i < EPL; ++i) acc[q][i] = fmaf(xv, wv[i], acc[q][i]);
-            }
+                for (int i = 0; i < EPL; ++i) acc[q][i] = fmaf(xv[q], wv[i], acc[q][i]);
         }
         __syncthreads();
     }
 
+    // second half's sums through shared memory (the Wr ring is free now)
+    float* part = &ws[0][0][0][0];        // [token][EW]
+    if (half == 1) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int tt = warp * 4 + q;
-        const int t = t0 + tt;
-        if (t >= T_) continue;                       // warp-uniform
-        float z[EPL];
+        for (int q = 0; q < TQ; ++q)
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            int e = lane + 32 * i;
-            z[i] = (e < E) ? acc[q][i] + (b ? b[e] : 0.f) : -INFINITY;
-        }
-        unsigned taken = 0;
-        int sel_e[kMaxK];
-        float sel_z[kMaxK];
+            for (int i = 0; i < EPL; ++i) part[(tq0 + q) * EW + lane + 32 * i] = acc[q][i];
+    }
+    __syncthreads();
+    if (half == 0) {
 #pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
-            if (j >= k) break;
-            if (replay) {
-                // the given expert's logit, from the lane that holds it
-                const int e = replay_expert(replay, (size_t)t * k + j, E, lane == 0 ? status : nullptr);
-                float zi = z[0];
-#pragma unroll
-                for (int i = 1; i < EPL; ++i)
-                    if ((e >> 5) == i) zi = z[i];
-                sel_e[j] = e;
-                sel_z[j] = __shfl_sync(0xffffffffu, zi, e & 31);
-                continue;
-            }
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
+        for (int q = 0; q < TQ; ++q) {
+            const int tt = tq0 + q, t = t0 + tt;
+            if (t >= T_) break;                   // warp-uniform
+            float z[EPL];
 #pragma unroll
             for (int i = 0; i < EPL; ++i) {
-                int e = lane + 32 * i;
-                if (e < E && !((taken >> i) & 1u) && better(z[i], e, bv, bi)) { bv = z[i]; bi = e; }
+                const int e = lane + 32 * i;
+                z[i] = (e < E) ? (acc[q][i] + part[tt * EW + e]) + (b ? b[e] : 0.f) : -INFINITY;
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-            }
-            sel_e[j] = bi;
-            sel_z[j] = bv;
-            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        }
-        if (lane == 0) {
-            float sc[kMaxK], den;
-            gates_of(sel_z, k, score, sc, den);
-            for (int j = 0; j < k; ++j) {
-                topk[(size_t)t * k + j] = sel_e[j];
-                gates[(size_t)t * k + j] = sc[j] / den;
-                selsc[(size_t)t * k + j] = sc[j];
-                sel_s[tt][j] = sel_e[j];
-            }
+            warp_route_token<EPL>(z, t, E, k, score, replay, status, lane, topk, gates, selsc, sel_s[tt]);
         }
     }
     __syncthreads();
     const int ntok = min(kRouterTokens, T_ - t0);
     for (int e = tid; e < E; e += 256) {
-        int c = 0;
+        int cnt = 0;
         for (int tt = 0; tt < ntok; ++tt)
-            for (int j = 0; j < k; ++j) c += (sel_s[tt][j] == e);
-        hist[(size_t)blockIdx.x * E + e] = c;
+            for (int j = 0; j < k; ++j) cnt += (sel_s[tt][j] == e);
+        hist[(size_t)blockIdx.x * E + e] = cnt;
     }
 }
 
 // Router for E <= 32. A block routes kRouterTokens tokens: lane l of every
 // warp owns token l, warp w sums the logits of all experts over the w-th
-// eighth of H (16-byte x loads; each Wr row is read once per warp as a
-// broadcast), then one thread per token adds the eight partial sums in warp
-// order, selects the top k (largest logit, lower expert index on equality)
-// and writes the gates.
+// NW-th of H (16-byte x loads, four in flight; each Wr row is read once per
+// warp as a broadcast), then one thread per token adds the NW partial sums in
+// warp order, selects the top k (largest logit, lower expert index on
+// equality) and writes the gates.
 template <typename T, int EMAX>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__((EMAX <= 16 ? 16 : 8) * 32, 1)
 router_small_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float* __restrict__ b,
                     int T_, int H, int E, int k, int score, int* __restrict__ topk,
                     float* __restrict__ gates, float* __restrict__ selsc, int* __restrict__ hist,
                     const int* __restrict__ replay, DeviceStatus* __restrict__ status)
 {
     constexpr int V = 16 / sizeof(T);
-    constexpr int NW = 8;
+    constexpr int NW = EMAX <= 16 ? 16 : 8;
     __shared__ float part[NW][kRouterTokens][EMAX + 1];
     __shared__ int sel_s[kRouterTokens][kMaxK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -212,20 +305,30 @@ router_small_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
     const int hs = H / NW;                       // H is a multiple of 128
-    const int h_lo = warp * hs, h_hi = h_lo + hs;
-    if (t < T_) {
-        for (int h0 = h_lo; h0 < h_hi; h0 += V) {
-            const uint4 u = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h0);
-            const T* p = reinterpret_cast<const T*>(&u);
+    const int h_lo = warp * hs;
+    const int nv = hs / V;
+    auto fma_vec = [&](const uint4& u, int h0) {
+        const T* p = reinterpret_cast<const T*>(&u);
 #pragma unroll
-            for (int i = 0; i < V; ++i) {
-                const float xv = to_f32(p[i]);
-                const float* wrow = Wr + (size_t)(h0 + i) * E;
+        for (int i = 0; i < V; ++i) {
+            const float xv = to_f32(p[i]);
+            const float* wrow = Wr + (size_t)(h0 + i) * E;
 #pragma unroll
-                for (int e = 0; e < EMAX; ++e)
-                    if (e < E) acc[e] = fmaf(xv, __ldg(wrow + e), acc[e]);
-            }
+            for (int e = 0; e < EMAX; ++e)
+                if (e < E) acc[e] = fmaf(xv, __ldg(wrow + e), acc[e]);
         }
+    };
+    if (t < T_) {
+        const T* xr = x + (size_t)t * H + h_lo;
+        int v = 0;
+        for (; v + 4 <= nv; v += 4) {
+            uint4 u[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) u[q] = *reinterpret_cast<const uint4*>(xr + (v + q) * V);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) fma_vec(u[q], h_lo + (v + q) * V);
+        }
+        for (; v < nv; ++v) fma_vec(*reinterpret_cast<const uint4*>(xr + v * V), h_lo + v * V);
     }
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) part[warp][lane][e] = acc[e];
@@ -382,10 +485,10 @@ cudaError_t launch_router(const T* x, const float* Wr, const float* b, int T_, i
 {
     const int nblk = (T_ + kRouterTokens - 1) / kRouterTokens;
     if (E <= 8)
-        router_small_kernel<T, 8><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
+        router_small_kernel<T, 8><<<nblk, 512, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
                                                                replay, status);
     else if (E <= 16)
-        router_small_kernel<T, 16><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
+        router_small_kernel<T, 16><<<nblk, 512, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
                                                                replay, status);
     else if (E <= 32)
         router_small_kernel<T, 32><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
