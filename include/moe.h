@@ -253,9 +253,11 @@ moe_status_t moe_route_static(moe_plan_t plan, int T, const void* x, const float
  *   MOE_Q_ROWS:    1x128 blocks along rows: codes rows x cols,
  *                  scales rows x cols/128.
  *   MOE_Q_TILES:   128x128 blocks: codes rows x cols, scales (rows/128) x
- *                  (cols/128); with codes_t and scales_t (both or neither)
- *                  also the transposed codes_t cols x rows and scales_t
- *                  (cols/128) x (rows/128).
+ *                  (cols/128).
+ *   With MOE_Q_ROWS or MOE_Q_TILES, when codes_t and scales_t are both
+ *   given, the same pass also writes the 128x128-block codes of the
+ *   transpose, codes_t cols x rows with scales_t (cols/128) x (rows/128)
+ *   (the layer quantises its gradients this way, reading them once).
  *   MOE_Q_COLS_T:  per column over 128-row blocks, transposed output:
  *                  codes_t cols x rows, scales_t cols x rows/128.
  *   MOE_Q_TILES_T: 128x128 blocks, transposed output: codes_t cols x rows,

@@ -607,12 +607,13 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
                                                f32(sv, L.sX), s));
     // one orientation of the weight codes: the forward GEMMs read them
     // MN-major, the data-gradient GEMMs K-major
-    MOE_STAGE(ST_WQUANT, launch_quant_w(static_cast<const T*>(a->W_gate), E, H, F, u8(sv, L.WgQ),
-                                        f32(sv, L.sWg), nullptr, nullptr, s));
-    MOE_STAGE(ST_WQUANT, launch_quant_w(static_cast<const T*>(a->W_up), E, H, F, u8(sv, L.WuQ),
-                                        f32(sv, L.sWu), nullptr, nullptr, s));
-    MOE_STAGE(ST_WQUANT, launch_quant_w(static_cast<const T*>(a->W_down), E, F, H, u8(sv, L.WdQ),
-                                        f32(sv, L.sWd), nullptr, nullptr, s));
+    auto wquant = [&](const void* W, int R, int C, uint8_t* q, float* sc) {
+        return launch_quant(QuantJob{static_cast<const T*>(W), nullptr, E * R, C, 128, q, sc, 1, nullptr,
+                                     nullptr, 0}, s);
+    };
+    MOE_STAGE(ST_WQUANT, wquant(a->W_gate, H, F, u8(sv, L.WgQ), f32(sv, L.sWg)));
+    MOE_STAGE(ST_WQUANT, wquant(a->W_up, H, F, u8(sv, L.WuQ), f32(sv, L.sWu)));
+    MOE_STAGE(ST_WQUANT, wquant(a->W_down, F, H, u8(sv, L.WdQ), f32(sv, L.sWd)));
     GemmDesc d;
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
@@ -625,7 +626,8 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     d.O0 = A; d.O1 = U; d.O2 = Hh; d.ldo = F; d.status = status;
     if (L.fold) { d.gates = gates; d.slot_of = slotof; }   // Hh = g silu(A) U
     MOE_STAGE(ST_FC1, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
-    MOE_STAGE(ST_QROWS, launch_quant_rows(Hh, meta + 1, Rp, F, u8(ws, L.hq), f32(ws, L.sh), s));
+    MOE_STAGE(ST_QROWS, launch_quant(QuantJob{Hh, meta + 1, Rp, F, Rp, u8(ws, L.hq), f32(ws, L.sh), 0,
+                                              nullptr, nullptr, 0}, s));
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
     d.N = H; d.K = F; d.E = E;
@@ -689,7 +691,9 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
         MOE_STAGE(ST_GATEGRAD, launch_gate_grad<T>(dY, Yp, rowof, topk, gates, selsc, poff, counts, T_, H,
                                                    E, k, c.score, dYp, dz, s));
     // fc2 dgrad + SwiGLU backward
-    MOE_STAGE(ST_QROWS, launch_quant_rows(dYp, meta + 1, Rp, H, u8(ws, L.dYq), f32(ws, L.sdY), s));
+    // dYp once: 1x128 row codes (fc2 dgrad) and transposed 128x128-tile codes (fc2 wgrad)
+    MOE_STAGE(ST_QROWS, launch_quant(QuantJob{dYp, meta + 1, Rp, H, Rp, u8(ws, L.dYq), f32(ws, L.sdY), 0,
+                                              u8(ws, L.dYpTq), f32(ws, L.sdYpT), 1}, s));
     GemmDesc d;
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_BWD; d.dual = DUAL_NONE;
@@ -707,8 +711,8 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     if (L.fold)
         MOE_STAGE(ST_GATEDZ, launch_gate_dz(dgpart, F / 64, rowof, gates, selsc, T_, k, c.score, dz, s));
     // fc2 wgrad: dWd[e] = h_e^T dYp_e
-    MOE_STAGE(ST_QT, launch_quant_t(Hh, meta + 1, Rp, F, 0, u8(ws, L.hTq), f32(ws, L.shT), s));
-    MOE_STAGE(ST_QT, launch_quant_t(dYp, meta + 1, Rp, H, 1, u8(ws, L.dYpTq), f32(ws, L.sdYpT), s));
+    MOE_STAGE(ST_QT, launch_quant(QuantJob{Hh, meta + 1, Rp, F, Rp, nullptr, nullptr, 0, u8(ws, L.hTq),
+                                           f32(ws, L.shT), 0}, s));
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
     d.N = H; d.M_out = F; d.E = E;
@@ -720,8 +724,11 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.O0 = a->dW_down; d.ldo = H; d.o_estride = (long long)F * H; d.status = status;
     MOE_STAGE(ST_FC2_WGRAD, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
     // fc1 dgrad: dXp = dA Wg^T + dU Wu^T
-    MOE_STAGE(ST_QROWS, launch_quant_rows(dA, meta + 1, Rp, F, u8(ws, L.dAq), f32(ws, L.sdA), s));
-    MOE_STAGE(ST_QROWS, launch_quant_rows(dU, meta + 1, Rp, F, u8(ws, L.dUq), f32(ws, L.sdU), s));
+    // dA, dU once each: row codes (fc1 dgrad) and transposed tile codes (fc1 wgrad)
+    MOE_STAGE(ST_QROWS, launch_quant(QuantJob{dA, meta + 1, Rp, F, Rp, u8(ws, L.dAq), f32(ws, L.sdA), 0,
+                                              u8(ws, L.dATq), f32(ws, L.sdAT), 1}, s));
+    MOE_STAGE(ST_QROWS, launch_quant(QuantJob{dU, meta + 1, Rp, F, Rp, u8(ws, L.dUq), f32(ws, L.sdU), 0,
+                                              u8(ws, L.dUTq), f32(ws, L.sdUT), 1}, s));
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
     d.N = H; d.K = F; d.E = E;
@@ -734,9 +741,8 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.O0 = dXp; d.ldo = H; d.status = status;
     MOE_STAGE(ST_FC1_DGRAD, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
     // fc1 wgrad: dWg[e] = Xp_e^T dA_e, dWu[e] = Xp_e^T dU_e
-    MOE_STAGE(ST_QT, launch_quant_t(Xp, meta + 1, Rp, H, 0, u8(ws, L.XpTq), f32(ws, L.sXpT), s));
-    MOE_STAGE(ST_QT, launch_quant_t(dA, meta + 1, Rp, F, 1, u8(ws, L.dATq), f32(ws, L.sdAT), s));
-    MOE_STAGE(ST_QT, launch_quant_t(dU, meta + 1, Rp, F, 1, u8(ws, L.dUTq), f32(ws, L.sdUT), s));
+    MOE_STAGE(ST_QT, launch_quant(QuantJob{Xp, meta + 1, Rp, H, Rp, nullptr, nullptr, 0, u8(ws, L.XpTq),
+                                           f32(ws, L.sXpT), 0}, s));
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
     d.N = F; d.M_out = H; d.E = E;
@@ -851,17 +857,18 @@ moe_status_t moe_fp8_quantize(int rows, int cols, int mode, const void* in, uint
     cudaError_t e;
     switch (mode) {
     case MOE_Q_ROWS:
+    case MOE_Q_TILES: {
         if (!codes || !scales) return MOE_ERR_INVALID_ARG;
-        e = launch_quant_rows(x, nullptr, rows, cols, codes, scales, s);
+        const bool t = codes_t && scales_t;   // also the transposed 128x128-tile codes
+        e = launch_quant(QuantJob{x, nullptr, rows, cols, rows, codes, scales, mode == MOE_Q_TILES ? 1 : 0,
+                                  t ? codes_t : nullptr, t ? scales_t : nullptr, 1}, s);
         break;
-    case MOE_Q_TILES:
-        if (!codes || !scales || (!codes_t) != (!scales_t)) return MOE_ERR_INVALID_ARG;
-        e = launch_quant_w(x, 1, rows, cols, codes, scales, codes_t, scales_t, s);
-        break;
+    }
     case MOE_Q_COLS_T:
     case MOE_Q_TILES_T:
         if (!codes_t || !scales_t) return MOE_ERR_INVALID_ARG;
-        e = launch_quant_t(x, nullptr, rows, cols, mode == MOE_Q_TILES_T ? 1 : 0, codes_t, scales_t, s);
+        e = launch_quant(QuantJob{x, nullptr, rows, cols, rows, nullptr, nullptr, 0, codes_t, scales_t,
+                                  mode == MOE_Q_TILES_T ? 1 : 0}, s);
         break;
     default:
         return MOE_ERR_INVALID_ARG;

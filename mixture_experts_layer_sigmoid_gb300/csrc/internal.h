@@ -142,12 +142,20 @@ cudaError_t launch_unpermute_reduce(const T* dXp, const T* dXs, const int* row_o
 cudaError_t launch_permute_quant(const __nv_bfloat16* x, const int* row_of, const int* poff,
                                  const int* counts, int T_, int H, int E, int k, __nv_bfloat16* Xp,
                                  uint8_t* Xq, float* sX, cudaStream_t s);
-cudaError_t launch_quant_rows(const __nv_bfloat16* in, const int* rows_dev, int rows_max, int C,
-                              uint8_t* q, float* sc, cudaStream_t s);
-cudaError_t launch_quant_t(const __nv_bfloat16* in, const int* rows_dev, int rows_cap, int C,
-                           int tiles, uint8_t* qT, float* sT, cudaStream_t s);
-cudaError_t launch_quant_w(const __nv_bfloat16* W, int E, int R, int C, uint8_t* q, float* sc,
-                           uint8_t* qT, float* sT, cudaStream_t s);
+// One pass of the tile quantiser over in[rows][C] (bf16, rows = *rows_dev or
+// rows_max, both multiples of 128, as is C). q != null: codes [rows][C] with
+// 1x128 row-block scales s[rows][C/128] (q_tiles 0) or one scale per 128x128
+// tile s[rows/128][C/128] (q_tiles 1). qT != null: transposed codes
+// [C][rows_cap] with per-column scales over 128 rows sT[C][rows_cap/128]
+// (t_tiles 0) or per-tile scales sT[C/128][rows_cap/128] (t_tiles 1).
+struct QuantJob {
+    const __nv_bfloat16* in;
+    const int* rows_dev;
+    int rows_max, C, rows_cap;
+    uint8_t* q; float* s; int q_tiles;
+    uint8_t* qT; float* sT; int t_tiles;
+};
+cudaError_t launch_quant(const QuantJob& j, cudaStream_t s);
 
 // Configuration and device of a plan; false for a null plan.
 bool plan_info(const moe_plan_s* plan, moe_config_t* cfg, int* device);

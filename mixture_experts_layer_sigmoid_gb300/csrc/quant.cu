@@ -9,11 +9,10 @@
 //
 // Kernels:
 //   permute_quant_kernel  x -> permuted rows Xp (bf16) and their 1x128 codes
-//   quant_rows_kernel     [rows][C] bf16 -> codes [rows][C], 1x128 scales
-//   quant_t_kernel        [rows][C] bf16 -> transposed codes [C][rows], scales
-//                         per column over 128 rows, or per 128x128 tile
-//   quant_w_kernel        weights [E][R][C] -> 128x128-block codes [E][R][C]
-//                         (and optionally [E][C][R])
+//   quant_tiles_kernel    [rows][C] bf16 in 128x128 tiles -> any of: codes
+//                         [rows][C] with 1x128 row scales or one scale per
+//                         tile (weights), transposed codes [C][rows] with
+//                         per-column (over 128 rows) or per-tile scales
 #include "internal.h"
 
 #include <cuda_fp8.h>
@@ -26,21 +25,44 @@ __device__ __forceinline__ float block_scale(float amax)
     return amax == 0.f ? 1.f : __fdiv_rn(amax, 448.f);
 }
 
-// E4M3(v / s), rounded to nearest even and saturated, given r = 1/s rounded
-// to nearest. y = v r is within two units in the last place of the rounded
-// quotient, so both round to the same E4M3 value unless y lies within a few
-// units of a rounding midpoint (the 20 mantissa bits E4M3 drops are within 4
-// of half) or below the E4M3 normal range, where the rounding position moves;
-// those rare values take the IEEE division itself.
-__device__ __forceinline__ uint8_t e4m3(float v, float s, float r)
+// The E4M3 codes of two values at once (scales s0, s1, rounded reciprocals
+// r0, r1). The fp32 quotient RN(v / s) is formed with Markstein's correction
+// of the product (P. Markstein, "Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
+//   y0 = RN(v r),  y1 = RN(y0 + r RN(v - s y0))   (two fused multiply-adds),
+// in packed f32x2 arithmetic. For a block maximum amax (bf16) with scale
+// s = RN(amax / 448) >= 2^-112 and every bf16 v with |v| <= amax, E4M3(y1)
+// equals E4M3(RN(v / s)): an exhaustive check over all such pairs
+// (tests/e4m3_quotient_check.c) finds no difference;
+// below that the remainder can underflow, and such tiny scales take the IEEE
+// division. x.x of the packed pair is the low byte.
+constexpr float kMinFastScale = 0x1p-112f;
+__device__ __forceinline__ uint64_t f2_pack(float a, float b)
 {
-    float y = v * r;
-    const uint32_t b = __float_as_uint(y) & 0x7fffffffu;
-    if (b != 0u) {
-        const int dist = (int)(b & 0xFFFFFu) - 0x80000;
-        if ((b >> 23) < 121u || (dist >= -4 && dist <= 4)) y = __fdiv_rn(v, s);
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v)
+{
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+    return f;
+}
+__device__ __forceinline__ uint32_t e4m3x2(float v0, float v1, float s0, float s1, float r0, float r1)
+{
+    float2 y;
+    if (s0 >= kMinFastScale && s1 >= kMinFastScale) {
+        const uint64_t v = f2_pack(v0, v1), r = f2_pack(r0, r1), ns = f2_pack(-s0, -s1);
+        uint64_t y0, e, y1;
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y0) : "l"(v), "l"(r));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(ns), "l"(y0), "l"(v));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(y1) : "l"(e), "l"(r), "l"(y0));
+        y = f2_unpack(y1);
+    } else {
+        y = make_float2(__fdiv_rn(v0, s0), __fdiv_rn(v1, s1));
     }
-    return (uint8_t)__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
 }
 
 // 8 bf16 -> 8 fp32
@@ -58,12 +80,9 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8])
 __device__ __forceinline__ uint2 codes8(const float (&v)[8], float s)
 {
     const float r = __frcp_rn(s);
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) lo |= (uint32_t)e4m3(v[i], s, r) << (8 * i);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) hi |= (uint32_t)e4m3(v[4 + i], s, r) << (8 * i);
-    return make_uint2(lo, hi);
+    const uint32_t p0 = e4m3x2(v[0], v[1], s, s, r, r), p1 = e4m3x2(v[2], v[3], s, s, r, r);
+    const uint32_t p2 = e4m3x2(v[4], v[5], s, s, r, r), p3 = e4m3x2(v[6], v[7], s, s, r, r);
+    return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
 }
 
 // amax over the 16 lanes that share one 128-element block (8 values each)
@@ -116,26 +135,6 @@ permute_quant_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict_
             reinterpret_cast<uint2*>(Xq + (size_t)rows[j] * H)[v] = c;
             if ((threadIdx.x & 15) == 0) sX[(size_t)rows[j] * nb + v / 16] = s;
         }
-    }
-}
-
-// One block per row (rows < *rows_dev); C a multiple of 128.
-__global__ void __launch_bounds__(128)
-quant_rows_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__ rows_dev,
-                  int rows_fixed, int C, uint8_t* __restrict__ q, float* __restrict__ s)
-{
-    const int r = blockIdx.x;
-    if (r >= (rows_dev ? *rows_dev : rows_fixed)) return;
-    const int nv = C / 8, nb = C / 128;
-    for (int v0 = 0; v0 < nv; v0 += blockDim.x) {
-        const int v = v0 + threadIdx.x;
-        const bool act = v < nv;
-        float f[8];
-        unpack8(act ? reinterpret_cast<const uint4*>(in + (size_t)r * C)[v] : make_uint4(0, 0, 0, 0), f);
-        const float sc = block_scale(amax16(f));
-        if (!act) continue;
-        reinterpret_cast<uint2*>(q + (size_t)r * C)[v] = codes8(f, sc);
-        if ((threadIdx.x & 15) == 0) s[(size_t)r * nb + v / 16] = sc;
     }
 }
 
@@ -204,14 +203,15 @@ __device__ __forceinline__ void encode_rows(__nv_bfloat16 (*tile)[136], float sc
         uint32_t w[4];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t word = 0;
+            uint32_t pr[2];
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int c = 4 * q4 + b;
-                word |= (uint32_t)(sc_col ? e4m3(f[c], sc_col[c0 + c], rc_col[c0 + c]) : e4m3(f[c], sc, rc))
-                        << (8 * b);
+            for (int b = 0; b < 2; ++b) {
+                const int c = 4 * q4 + 2 * b;
+                pr[b] = sc_col ? e4m3x2(f[c], f[c + 1], sc_col[c0 + c], sc_col[c0 + c + 1], rc_col[c0 + c],
+                                        rc_col[c0 + c + 1])
+                               : e4m3x2(f[c], f[c + 1], sc, sc, rc, rc);
             }
-            w[q4] = word;
+            w[q4] = pr[0] | (pr[1] << 16);
         }
         const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(qs + qs_off(rr, c0)) = v;
@@ -246,68 +246,122 @@ __device__ __forceinline__ void write_transposed(const uint8_t* qs, uint8_t* dst
             make_uint4(o[j][0], o[j][1], o[j][2], o[j][3]);
 }
 
-// Tile (128 rows x 128 columns) of in [rows][C] -> qT [C][rows_cap].
-// tiles == 0: one scale per column of the tile, sT[c][rb] (row stride
-// rows_cap/128); tiles == 1: one scale per tile, sT[cb][rb].
-__global__ void __launch_bounds__(256)
-quant_t_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__ rows_dev,
-               int rows_fixed, int C, int rows_cap, int tiles, uint8_t* __restrict__ qT,
-               float* __restrict__ sT)
+// One pass over a bf16 matrix in[rows][C] (rows and C multiples of 128) in
+// 128x128 tiles; a persistent block stages each tile in shared memory and
+// has the next tile's loads in flight while it encodes the current one. Outputs (template modes):
+//   QM 1: row codes q[rows][C], one scale per row and 128 columns, s[rows][C/128]
+//   QM 2: tile codes q[rows][C], one scale per tile, s[rows/128][C/128]
+//   TM 1: transposed codes qT[C][rows_cap], one scale per column and 128 rows,
+//         sT[C][rows_cap/128]
+//   TM 2: transposed codes qT[C][rows_cap], one scale per tile, sT[C/128][rows_cap/128]
+// Expert-stacked weights [E][R][C] with R a multiple of 128 are rows = E R.
+template <int QM, int TM>
+__global__ void __launch_bounds__(256, 2)
+quant_tiles_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__ rows_dev,
+                   int rows_fixed, int C, int rows_cap, uint8_t* __restrict__ q,
+                   float* __restrict__ s, uint8_t* __restrict__ qT, float* __restrict__ sT)
 {
     __shared__ __align__(16) __nv_bfloat16 tile[128][136];
-    __shared__ __align__(16) uint8_t qs[128 * kQS];
+    __shared__ __align__(16) uint8_t qs[TM ? 128 * kQS : 16];
     __shared__ float red[256];
     __shared__ float scol[128], rcol[128];
-    const int cb = blockIdx.x, rb = blockIdx.y;
-    const int r0 = rb * 128, c0 = cb * 128;
-    if (r0 >= (rows_dev ? *rows_dev : rows_fixed)) return;
-    const float at = load_tile(in + (size_t)r0 * C + c0, C, tile);
-    float sc = 0.f;
-    if (tiles) {
-        sc = block_scale(block_max(at, red));
-        if (threadIdx.x == 0) sT[(size_t)cb * (rows_cap / 128) + rb] = sc;
-    } else {
-        __syncthreads();
-        // column amax: threads (c = tid % 128, half = tid / 128) over 64 rows each
-        const int c = threadIdx.x & 127, half = threadIdx.x >> 7;
-        float a = 0.f;
-        for (int rr = half * 64; rr < half * 64 + 64; ++rr) a = fmaxf(a, fabsf(__bfloat162float(tile[rr][c])));
-        red[threadIdx.x] = a;
-        __syncthreads();
-        if (half == 0) {
-            const float s1 = block_scale(fmaxf(red[c], red[c + 128]));
-            scol[c] = s1;
-            rcol[c] = __frcp_rn(s1);
-            sT[(size_t)(c0 + c) * (rows_cap / 128) + rb] = s1;
+    const int rows = rows_dev ? *rows_dev : rows_fixed;
+    const int ncb = C / 128;
+    const int ntiles = (rows / 128) * ncb;
+    const int tid = threadIdx.x, sub = tid & 15;   // 16 threads per tile row, 8 columns each
+    uint4 u[8];                                     // rows (tid / 16) + 16 j of the tile
+    auto fetch = [&](int t) {
+        const int rb = t / ncb, cb = t - rb * ncb;
+        const __nv_bfloat16* src = in + (size_t)rb * 128 * C + (size_t)cb * 128 + sub * 8;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) u[j] = *reinterpret_cast<const uint4*>(src + (size_t)((tid >> 4) + 16 * j) * C);
+    };
+    int t = blockIdx.x;
+    if (t < ntiles) fetch(t);
+    for (; t < ntiles; t += gridDim.x) {
+        const int rb = t / ncb, cb = t - rb * ncb;
+        const int r0 = rb * 128, c0 = cb * 128;
+        // stage the tile, then put the next tile's loads in flight for the
+        // whole of this tile's encoding
+#pragma unroll
+        for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(&tile[(tid >> 4) + 16 * j][sub * 8]) = u[j];
+        if (t + (int)gridDim.x < ntiles) fetch(t + gridDim.x);
+        // row codes and amax from this thread's own staged values
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int rr = (tid >> 4) + 16 * j;
+            float f[8];
+            unpack8(*reinterpret_cast<const uint4*>(&tile[rr][sub * 8]), f);
+            if (QM == 1) {
+                const float ra = amax16(f);                 // the row's 128 values are on 16 lanes
+                const float sr = block_scale(ra);
+                *reinterpret_cast<uint2*>(q + (size_t)(r0 + rr) * C + c0 + sub * 8) = codes8(f, sr);
+                if (sub == 0) s[(size_t)(r0 + rr) * ncb + cb] = sr;
+                amax = fmaxf(amax, ra);                     // the tile's amax too (TM 2)
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+            }
         }
+        float st = 1.f;
+        if (QM == 2 || TM == 2) st = block_scale(block_max(amax, red));   // also a barrier
+        else __syncthreads();                                              // the tile is staged
+        if (QM == 2) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int rr = (tid >> 4) + 16 * j;
+                float f[8];
+                unpack8(*reinterpret_cast<const uint4*>(&tile[rr][sub * 8]), f);
+                *reinterpret_cast<uint2*>(q + (size_t)(r0 + rr) * C + c0 + sub * 8) = codes8(f, st);
+            }
+            if (tid == 0) s[(size_t)rb * ncb + cb] = st;
+        }
+        if (TM) {
+            if (TM == 1) {
+                // column amax: threads (c = tid % 128, half = tid / 128) over 64 rows each
+                const int c = tid & 127, half = tid >> 7;
+                float a = 0.f;
+                for (int rr = half * 64; rr < half * 64 + 64; ++rr) a = fmaxf(a, fabsf(__bfloat162float(tile[rr][c])));
+                red[tid] = a;
+                __syncthreads();
+                if (half == 0) {
+                    const float s1 = block_scale(fmaxf(red[c], red[c + 128]));
+                    scol[c] = s1;
+                    rcol[c] = __frcp_rn(s1);
+                    sT[(size_t)(c0 + c) * (rows_cap / 128) + rb] = s1;
+                }
+                __syncthreads();
+            } else if (tid == 0) {
+                sT[(size_t)cb * (rows_cap / 128) + rb] = st;
+            }
+            encode_rows(tile, st, TM == 1 ? scol : nullptr, rcol, qs, nullptr, 0);
+            __syncthreads();
+            write_transposed(qs, qT + (size_t)c0 * rows_cap + r0, rows_cap);
+        }
+        __syncthreads();   // shared buffers are free for the next tile
     }
-    __syncthreads();
-    encode_rows(tile, tiles ? sc : 1.f, tiles ? nullptr : scol, rcol, qs, nullptr, 0);
-    __syncthreads();
-    write_transposed(qs, qT + (size_t)c0 * rows_cap + r0, rows_cap);
 }
 
-// 128x128 block (rb, cb) of expert e of W [E][R][C] -> codes and the block's
-// scale, and (qT, sT given) the transposed codes and scale layout too.
-__global__ void __launch_bounds__(256)
-quant_w_kernel(const __nv_bfloat16* __restrict__ W, int R, int C, uint8_t* __restrict__ q,
-               float* __restrict__ s, uint8_t* __restrict__ qT, float* __restrict__ sT)
+template <int QM, int TM>
+cudaError_t run_quant(const QuantJob& j, cudaStream_t st)
 {
-    __shared__ __align__(16) __nv_bfloat16 tile[128][136];
-    __shared__ __align__(16) uint8_t qs[128 * kQS];
-    __shared__ float red[8];
-    const int cb = blockIdx.x, rb = blockIdx.y, e = blockIdx.z;
-    const size_t base = (size_t)e * R * C;
-    const int r0 = rb * 128, c0 = cb * 128;
-    const float sc = block_scale(block_max(load_tile(W + base + (size_t)r0 * C + c0, C, tile), red));
-    if (threadIdx.x == 0) {
-        s[((size_t)e * (R / 128) + rb) * (C / 128) + cb] = sc;
-        if (sT) sT[((size_t)e * (C / 128) + cb) * (R / 128) + rb] = sc;
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_tiles_kernel<QM, TM>, 256, 0) !=
+                cudaSuccess || per_sm < 1)
+            per_sm = 1;
     }
-    encode_rows(tile, sc, nullptr, nullptr, qs, q + base + (size_t)r0 * C + c0, C);
-    if (!qT) return;                      // block-uniform
-    __syncthreads();
-    write_transposed(qs, qT + base + (size_t)c0 * R + r0, R);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidValue;
+    const long long tiles = (long long)(j.rows_max / 128) * (j.C / 128);
+    if (tiles <= 0) return cudaSuccess;
+    const long long grid = tiles < (long long)sms * per_sm ? tiles : (long long)sms * per_sm;
+    quant_tiles_kernel<QM, TM><<<(unsigned)grid, 256, 0, st>>>(j.in, j.rows_dev, j.rows_max, j.C,
+                                                               j.rows_cap, j.q, j.s, j.qT, j.sT);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -320,28 +374,20 @@ cudaError_t launch_permute_quant(const __nv_bfloat16* x, const int* row_of, cons
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_rows(const __nv_bfloat16* in, const int* rows_dev, int rows_max, int C,
-                              uint8_t* q, float* sc, cudaStream_t s)
+cudaError_t launch_quant(const QuantJob& j, cudaStream_t s)
 {
-    if (rows_max <= 0) return cudaSuccess;
-    quant_rows_kernel<<<rows_max, 128, 0, s>>>(in, rows_dev, rows_max, C, q, sc);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_quant_t(const __nv_bfloat16* in, const int* rows_dev, int rows_cap, int C,
-                           int tiles, uint8_t* qT, float* sT, cudaStream_t s)
-{
-    dim3 grid(C / 128, rows_cap / 128);
-    quant_t_kernel<<<grid, 256, 0, s>>>(in, rows_dev, rows_cap, C, rows_cap, tiles, qT, sT);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_quant_w(const __nv_bfloat16* W, int E, int R, int C, uint8_t* q, float* sc,
-                           uint8_t* qT, float* sT, cudaStream_t s)
-{
-    dim3 grid(C / 128, R / 128, E);
-    quant_w_kernel<<<grid, 256, 0, s>>>(W, R, C, q, sc, qT, sT);
-    return cudaGetLastError();
+    if (j.C % 128 || j.rows_max % 128 || j.rows_cap % 128) return cudaErrorInvalidValue;
+    const int qm = j.q ? (j.q_tiles ? 2 : 1) : 0;
+    const int tm = j.qT ? (j.t_tiles ? 2 : 1) : 0;
+    switch (qm * 3 + tm) {
+    case 1: return run_quant<0, 1>(j, s);
+    case 2: return run_quant<0, 2>(j, s);
+    case 3: return run_quant<1, 0>(j, s);
+    case 5: return run_quant<1, 2>(j, s);
+    case 6: return run_quant<2, 0>(j, s);
+    case 8: return run_quant<2, 2>(j, s);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace moe

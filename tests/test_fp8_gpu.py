@@ -19,13 +19,14 @@ from harness import TIE_REL, rel_errors, to_np, upload
 pytestmark = pytest.mark.gpu
 
 
-def _quant(x, mode):
+def _quant(x, mode, with_t=False):
     R, C = x.shape
     dev = x.device
     codes = torch.empty((R, C), dtype=torch.uint8, device=dev)
     codes_t = torch.empty((C, R), dtype=torch.uint8, device=dev)
     if mode == moe.MOE_Q_ROWS:
-        sc, sct = torch.empty((R, C // 128), device=dev), None
+        sc = torch.empty((R, C // 128), device=dev)
+        sct = torch.empty((C // 128, R // 128), device=dev) if with_t else None
     elif mode == moe.MOE_Q_TILES:
         sc, sct = torch.empty((R // 128, C // 128), device=dev), torch.empty((C // 128, R // 128), device=dev)
     elif mode == moe.MOE_Q_COLS_T:
@@ -59,6 +60,11 @@ def test_quantisers_match_oracle_bit_for_bit():
     oc, os_ = oracle.fp8_quantize(xf, oracle.FP8_COLS)
     assert np.array_equal(ct, oc.T) and np.array_equal(st, os_.T)
     _, _, ct, st = _quant(xd, moe.MOE_Q_TILES_T)
+    assert np.array_equal(ct, oct_) and np.array_equal(st, ost)
+    # one pass: 1x128 row codes and the transpose's 128x128-block codes
+    c, s, ct, st = _quant(xd, moe.MOE_Q_ROWS, with_t=True)
+    oc, os_ = oracle.fp8_quantize(xf, oracle.FP8_ROWS)
+    assert np.array_equal(c, oc) and np.array_equal(s, os_)
     assert np.array_equal(ct, oct_) and np.array_equal(st, ost)
 
 
