@@ -23,9 +23,9 @@
 // They release a partial buffer with a relaxed mbarrier arrive: a release
 // arrive would first wait for their outstanding scale loads and stores, and
 // that wait, once per k block, cost more than the MMAs themselves.
-// PAIR: clusters of two CTAs issue M = 256 MMAs (A rows split between the
-// CTAs, B columns split between them), so each SM loads 32 KB per 128-deep
-// k block for 128 x 256 x 128 MACs.
+// PAIR (in the template, not dispatched: see qrun_any): clusters of two CTAs
+// issue M = 256 MMAs (A rows split between the CTAs, B columns split between
+// them), so each SM loads 32 KB per 128-deep k block for 128 x 256 x 128 MACs.
 #include "internal.h"
 #include "epilogue.cuh"
 #include "ptx.cuh"
@@ -748,25 +748,23 @@ cudaError_t qrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s
     return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI, SCHED, DUAL, true, B_MN>, mA0, mA1, mB0, mB1, d);
 }
 
-// CTA pairs when the row units come in (mostly) complete pairs, or the
-// weight-gradient rows split into 256-row pair tiles.
+// Single CTAs for every FP8 GEMM. The engine releases a TMEM partial buffer
+// once per 128-deep k block, and in a CTA pair that release crosses to the
+// peer CTA's barrier; on the Qwen3-shaped FP8 layer single CTAs took the row
+// GEMMs 8-12% and the weight-gradient GEMMs 1-3% below the pair times (step
+// 17.77 -> 16.85 ms), although a pair loads less per SM. The pair
+// instantiation (qrun<..., true>) stays available to the template.
 template <int EPI, int SCHED, int DUAL, bool B_MN = false>
 cudaError_t qrun_any(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
 {
-    const bool pair = (SCHED == SCHED_WGRAD) ? d.M_out % (2 * QBM) == 0
-                                             : d.pair_tab != nullptr && d.prefer_pair;
-    if (pair) return qrun<EPI, SCHED, DUAL, true, B_MN>(d, max_m_tiles, num_sms, s);
     return qrun<EPI, SCHED, DUAL, false, B_MN>(d, max_m_tiles, num_sms, s);
 }
 
 template <int EPI, int SCHED, int DUAL, bool B_MN = false>
 cudaError_t qattr()
 {
-    cudaError_t e = cudaFuncSetAttribute(gemm_fp8_kernel<EPI, SCHED, DUAL, false, B_MN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<false>::SMEM);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gemm_fp8_kernel<EPI, SCHED, DUAL, true, B_MN>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<true>::SMEM);
+    return cudaFuncSetAttribute(gemm_fp8_kernel<EPI, SCHED, DUAL, false, B_MN>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<false>::SMEM);
 }
 
 }  // namespace

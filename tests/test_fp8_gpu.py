@@ -71,10 +71,10 @@ def test_quantisers_match_oracle_bit_for_bit():
 FP8_CASES = {
     "qwen_fp8_small": mi.scaled(mi.WORKLOADS["qwen3_235b_fp8"], T=600, H=256, E=8, k=4, F=256),
     "qwen_fp8_ragged": mi.scaled(mi.WORKLOADS["qwen3_235b_fp8"], T=450, H=384, E=16, k=8, F=384),
-    # T*k >= 512*E: row GEMMs in CTA pairs (odd tile counts leave ghost halves),
-    # N = F = 384 ends in a half column tile, fc2 wgrad (M = F) single-CTA
-    "qwen_fp8_rows_in_cta_pairs": mi.scaled(mi.WORKLOADS["qwen3_235b_fp8"], T=1100, H=256, E=4, k=2,
-                                            F=384),
+    # T*k >= 512*E: many row tiles per expert (odd tile counts), N = F = 384
+    # ends in a half column tile
+    "qwen_fp8_many_rows_per_expert": mi.scaled(mi.WORKLOADS["qwen3_235b_fp8"], T=1100, H=256, E=4, k=2,
+                                               F=384),
 }
 
 
@@ -83,7 +83,7 @@ def test_fp8_layer_matches_oracle(name):
     _fp8_parity(name, False)
 
 
-@pytest.mark.parametrize("name", ["qwen_fp8_small", "qwen_fp8_rows_in_cta_pairs"])
+@pytest.mark.parametrize("name", ["qwen_fp8_small", "qwen_fp8_many_rows_per_expert"])
 def test_fp8_folded_gates_match_oracle(name):
     """Memory-efficient permutation on the FP8 layer: g h is quantised for
     fc2 instead of h; the same deviation bounds hold."""
