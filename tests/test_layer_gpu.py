@@ -26,6 +26,12 @@ CASES = {
     "rows_in_cta_pairs": mi.scaled(W["mixtral_8x7b"], T=1100, H=256, E=4, k=2, F=256),
     "qwen_e128_tiled_router": mi.scaled(W["qwen3_235b"], T=700, H=256, E=128, F=128),
     "deepseek_e256_sigmoid_shared": mi.scaled(W["deepseek_v3"], T=512, H=256, E=256, F=128, Fs=128),
+    # tiled router for E > 32: E not a multiple of 4 (Wr rows copied in 4-byte
+    # pieces), E/32 rounded up to 2 and 4 experts per lane, a ragged last
+    # router block (T = 257), and fp32 activations through the same kernel
+    "e37_router_unaligned_rows": mi.scaled(W["qwen3_235b"], T=300, H=256, E=37, k=3, F=128),
+    "e100_router_ragged_block": mi.scaled(W["deepseek_v3"], T=257, H=384, E=100, k=6, F=128, Fs=0),
+    "fp32_e42_router": mi.scaled(W["qwen3_235b"], T=97, H=128, E=42, k=2, F=128, dtype=mi.FP32),
     # degenerate sizes: one token (one router block, one padded row per expert)
     "one_token": mi.scaled(W["mixtral_8x7b"], T=1, H=128, E=4, k=2, F=128),
     "one_token_fp32_shared": mi.scaled(W["deepseek_v3"], T=1, H=128, E=8, k=3, F=128, Fs=128,
