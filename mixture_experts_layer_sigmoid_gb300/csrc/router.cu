@@ -389,44 +389,61 @@ router_small_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const
     }
 }
 
-__global__ void __launch_bounds__(kMaxE)
+// Four threads per expert (kScanParts); part p of expert e sums and bases
+// router blocks [p nblk / 4, (p + 1) nblk / 4), the parts in block order.
+constexpr int kScanParts = 4;
+
+__global__ void __launch_bounds__(kScanParts * kMaxE)
 scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ counts,
             int* __restrict__ poff, int* __restrict__ blkbase, int* __restrict__ tile_tab,
             int* __restrict__ meta, int* __restrict__ slot_of, int* __restrict__ pair_tab,
             int* __restrict__ pair_off, int cap, int* __restrict__ kept)
 {
     __shared__ int sc[kMaxE];
-    const int e = threadIdx.x;
-    int c = 0;
+    __shared__ int part_sum[kScanParts][kMaxE];
+    const int e = threadIdx.x % kMaxE, part = threadIdx.x / kMaxE;
+    const int b0 = (int)((long long)nblk * part / kScanParts);
+    const int b1 = (int)((long long)nblk * (part + 1) / kScanParts);
+    int cp = 0;
     if (e < E)
-        for (int blk = 0; blk < nblk; ++blk) c += hist[(size_t)blk * E + e];
-    const int pc = (c + kTileM - 1) / kTileM * kTileM;
-    sc[e] = (e < E) ? pc : 0;
+        for (int blk = b0; blk < b1; ++blk) cp += hist[(size_t)blk * E + e];
+    part_sum[part][e] = cp;
     __syncthreads();
-    // inclusive Hillis-Steele scan over kMaxE entries
+    int c = 0, before = 0;            // the expert's count; this part's rows before b0
+#pragma unroll
+    for (int q = 0; q < kScanParts; ++q) {
+        if (q < part) before += part_sum[q][e];
+        c += part_sum[q][e];
+    }
+    const int pc = (c + kTileM - 1) / kTileM * kTileM;
+    if (part == 0) sc[e] = (e < E) ? pc : 0;
+    __syncthreads();
+    // inclusive Hillis-Steele scan over kMaxE entries (part 0 threads)
     for (int off = 1; off < kMaxE; off <<= 1) {
-        int v = (e >= off) ? sc[e - off] : 0;
+        int v = (part == 0 && e >= off) ? sc[e - off] : 0;
         __syncthreads();
-        sc[e] += v;
+        if (part == 0) sc[e] += v;
         __syncthreads();
     }
     const int start = sc[e] - ((e < E) ? pc : 0);
     if (e < E) {
-        counts[e] = c;
-        // capacity-limited dropping: the segment keeps all c rows (the router
-        // gradient needs them) but only the first min(c, cap) are computed
-        if (kept) kept[e] = (cap >= 0 && c > cap) ? cap : c;
-        poff[e] = start;
-        int run = start;
-        for (int blk = 0; blk < nblk; ++blk) {
+        int run = start + before;
+        for (int blk = b0; blk < b1; ++blk) {
             blkbase[(size_t)blk * E + e] = run;
             run += hist[(size_t)blk * E + e];
         }
-        for (int i = 0; i < pc / kTileM; ++i) tile_tab[start / kTileM + i] = e;
-        for (int r = start + c; r < start + pc; ++r) slot_of[r] = -1;
+        if (part == 0) {
+            counts[e] = c;
+            // capacity-limited dropping: the segment keeps all c rows (the router
+            // gradient needs them) but only the first min(c, cap) are computed
+            if (kept) kept[e] = (cap >= 0 && c > cap) ? cap : c;
+            poff[e] = start;
+            for (int i = 0; i < pc / kTileM; ++i) tile_tab[start / kTileM + i] = e;
+            for (int r = start + c; r < start + pc; ++r) slot_of[r] = -1;
+        }
     }
     const int total = sc[kMaxE - 1];
-    if (e == 0) {
+    if (threadIdx.x == 0) {
         poff[E] = total;
         meta[0] = total / kTileM;
         meta[1] = total;
@@ -435,18 +452,20 @@ scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ cou
         // pairs of consecutive tiles of one expert (the last one may be alone)
         const int np = (e < E) ? (pc / kTileM + 1) / 2 : 0;
         __syncthreads();
-        sc[e] = np;
+        if (part == 0) sc[e] = np;
         __syncthreads();
         for (int off = 1; off < kMaxE; off <<= 1) {
-            int v = (e >= off) ? sc[e - off] : 0;
+            int v = (part == 0 && e >= off) ? sc[e - off] : 0;
             __syncthreads();
-            sc[e] += v;
+            if (part == 0) sc[e] += v;
             __syncthreads();
         }
-        const int pstart = sc[e] - np;
-        for (int i = 0; i < np; ++i) pair_tab[pstart + i] = start / kTileM + 2 * i;
-        if (e < E) pair_off[e] = pstart;   // first pair of expert e
-        if (e == 0) {
+        if (part == 0) {
+            const int pstart = sc[e] - np;
+            for (int i = 0; i < np; ++i) pair_tab[pstart + i] = start / kTileM + 2 * i;
+            if (e < E) pair_off[e] = pstart;   // first pair of expert e
+        }
+        if (threadIdx.x == 0) {
             meta[2] = sc[kMaxE - 1];
             pair_off[E] = sc[kMaxE - 1];
         }
@@ -515,8 +534,8 @@ cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff
                         int* pair_off, int cap, int* kept)
 {
     if (pair_tab && !pair_off) return cudaErrorInvalidValue;
-    scan_kernel<<<1, kMaxE, 0, s>>>(hist, nblk, E, counts, poff, blkbase, tile_tab, meta, slot_of,
-                                    pair_tab, pair_off, cap, kept);
+    scan_kernel<<<1, kScanParts * kMaxE, 0, s>>>(hist, nblk, E, counts, poff, blkbase, tile_tab, meta,
+                                                 slot_of, pair_tab, pair_off, cap, kept);
     return cudaGetLastError();
 }
 
