@@ -6,7 +6,8 @@
 // §5 ("Selective precision"): the router runs in FP32.
 //
 // Kernels:
-//   router_small_kernel (E <= 32) and router_kernel (tiled, larger E): logits z = x Wr + b (fp32 FMA, fixed summation order),
+//   router_small_kernel (E <= 32) and router_kernel (tiled, larger E):
+//                  logits z = x Wr + b (fp32 FMA, fixed summation order),
 //                  warp-shuffle top-k on z (score order equals logit order for
 //                  both softmax and sigmoid; equal values go to the lower
 //                  expert index), renormalised gates, and a per-block expert
