@@ -556,8 +556,8 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
         MOE_STAGE(ST_FC1S_WGRAD, gemm(d));
     }
     // router backward and the unpermute-reduce of dX
-    MOE_STAGE(ST_ROUTER_WGRAD, launch_router_wgrad<T>(Xp, slotof, poff, meta, L.MT_max, dz, H, E,
-                                   reinterpret_cast<float*>(ws + L.wrpart), a->dWr, s));
+    MOE_STAGE(ST_ROUTER_WGRAD, launch_router_wgrad<T>(static_cast<const T*>(a->x), slotof, poff, meta,
+                                   L.MT_max, dz, H, E, k, reinterpret_cast<float*>(ws + L.wrpart), a->dWr, s));
     MOE_STAGE(ST_TRANSPOSE, launch_transpose_f32(a->Wr, H, E, WrT, s));
     MOE_STAGE(ST_UNPERMUTE, launch_unpermute_reduce<T>(dXp, dXs, rowof, topk, dz, WrT, T_, H, k,
                                         static_cast<T*>(a->dX), s));
@@ -755,8 +755,8 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.O0 = a->dW_gate; d.O1 = a->dW_up; d.ldo = F; d.o_estride = (long long)H * F; d.status = status;
     MOE_STAGE(ST_FC1_WGRAD, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
     // router backward and the unpermute-reduce of dX
-    MOE_STAGE(ST_ROUTER_WGRAD, launch_router_wgrad<T>(Xp, slotof, poff, meta, L.MT_max, dz, H, E,
-                                   reinterpret_cast<float*>(ws + L.wrpart), a->dWr, s));
+    MOE_STAGE(ST_ROUTER_WGRAD, launch_router_wgrad<T>(static_cast<const T*>(a->x), slotof, poff, meta,
+                                   L.MT_max, dz, H, E, k, reinterpret_cast<float*>(ws + L.wrpart), a->dWr, s));
     MOE_STAGE(ST_TRANSPOSE, launch_transpose_f32(a->Wr, H, E, WrT, s));
     MOE_STAGE(ST_UNPERMUTE, launch_unpermute_reduce<T>(dXp, nullptr, rowof, topk, dz, WrT, T_, H, k,
                                                        static_cast<T*>(a->dX), s));

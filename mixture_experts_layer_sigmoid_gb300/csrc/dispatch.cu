@@ -211,15 +211,17 @@ gate_dz_kernel(const float* __restrict__ dg_part, int nslots, const int* __restr
 }
 
 // dWr[h][e] = sum over expert e's rows r of Xp[r][h] dz[slot(r)], in two
-// passes so that a hot expert's rows are spread over many blocks.
+// passes so that a hot expert's rows are spread over many blocks. Row r of
+// Xp is token slot(r) / k of x, so the values are read from x itself (T H
+// elements, mostly from L2, instead of the R H of Xp).
 // Pass 1, block (128-row tile, 64 columns h): 256 threads = 32 row phases x
 // 8 column groups of 8 columns (one 16-byte vector each); each phase sums
 // rows ph, ph + 32, ph + 64, ph + 96 of the tile (pad rows, slot -1, add 0),
 // and the 32 phases are added in fixed order into part[tile][h].
 template <typename T>
 __global__ void __launch_bounds__(256)
-router_wgrad_tile_kernel(const T* __restrict__ Xp, const int* __restrict__ slot_of,
-                         const int* __restrict__ meta, const float* __restrict__ dz, int H,
+router_wgrad_tile_kernel(const T* __restrict__ x, const int* __restrict__ slot_of,
+                         const int* __restrict__ meta, const float* __restrict__ dz, int H, int k,
                          float* __restrict__ part)
 {
     constexpr int V = 16 / sizeof(T);            // columns per vector
@@ -228,6 +230,7 @@ router_wgrad_tile_kernel(const T* __restrict__ Xp, const int* __restrict__ slot_
     constexpr int RPT = kTileM / PH;             // rows per thread
     __shared__ float red[PH][64 + 1];
     __shared__ float dzs[kTileM];
+    __shared__ int toks[kTileM];
     const int tile = blockIdx.x;
     if (tile >= meta[0]) return;                 // block-uniform
     const int cg = threadIdx.x % CG, ph = threadIdx.x / CG;
@@ -236,23 +239,28 @@ router_wgrad_tile_kernel(const T* __restrict__ Xp, const int* __restrict__ slot_
     if (threadIdx.x < kTileM) {
         const int slot = slot_of[r0 + threadIdx.x];
         dzs[threadIdx.x] = slot >= 0 ? dz[slot] : 0.f;
-    }
-    float xv[RPT][V];
-    if (h0 < H) {
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) Vec<T>::load(Xp + (size_t)(r0 + ph + PH * i) * H + h0, xv[i]);
+        toks[threadIdx.x] = slot >= 0 ? slot / k : -1;
     }
     __syncthreads();
+    float xv[RPT][V];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+        const int tok = toks[ph + PH * i];
+        if (h0 < H && tok >= 0) {
+            Vec<T>::load(x + (size_t)tok * H + h0, xv[i]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < V; ++j) xv[i][j] = 0.f;
+        }
+    }
     float acc[V];
 #pragma unroll
     for (int j = 0; j < V; ++j) acc[j] = 0.f;
-    if (h0 < H) {
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-            const float d = dzs[ph + PH * i];
+    for (int i = 0; i < RPT; ++i) {
+        const float d = dzs[ph + PH * i];
 #pragma unroll
-            for (int j = 0; j < V; ++j) acc[j] = fmaf(xv[i][j], d, acc[j]);
-        }
+        for (int j = 0; j < V; ++j) acc[j] = fmaf(xv[i][j], d, acc[j]);
     }
 #pragma unroll
     for (int j = 0; j < V; ++j) red[ph][cg * V + j] = acc[j];
@@ -378,13 +386,13 @@ cudaError_t launch_gate_dz(const float* dg_part, int nslots, const int* row_of, 
 }
 
 template <typename T>
-cudaError_t launch_router_wgrad(const T* Xp, const int* slot_of, const int* poff, const int* meta,
-                                int MT_max, const float* dz, int H, int E, float* part, float* dWr,
-                                cudaStream_t s)
+cudaError_t launch_router_wgrad(const T* x, const int* slot_of, const int* poff, const int* meta,
+                                int MT_max, const float* dz, int H, int E, int k, float* part,
+                                float* dWr, cudaStream_t s)
 {
     if (MT_max > 0) {
         dim3 grid1(MT_max, (H + 63) / 64);
-        router_wgrad_tile_kernel<T><<<grid1, 256, 0, s>>>(Xp, slot_of, meta, dz, H, part);
+        router_wgrad_tile_kernel<T><<<grid1, 256, 0, s>>>(x, slot_of, meta, dz, H, k, part);
     }
     dim3 grid2((H + 255) / 256, E);
     router_wgrad_sum_kernel<<<grid2, 256, 0, s>>>(part, poff, H, E, dWr);
@@ -416,8 +424,8 @@ cudaError_t launch_unpermute_reduce(const T* dXp, const T* dXs, const int* row_o
                                              const float*, const float*, const int*, const int*, \
                                              int, int, int, int, int, T*, float*, cudaStream_t); \
     template cudaError_t launch_router_wgrad<T>(const T*, const int*, const int*, const int*,    \
-                                                int, const float*, int, int, float*, float*,     \
-                                                cudaStream_t);                                   \
+                                                int, const float*, int, int, int, float*,        \
+                                                float*, cudaStream_t);                           \
     template cudaError_t launch_unpermute_reduce<T>(const T*, const T*, const int*, const int*,  \
                                                     const float*, const float*, int, int, int,   \
                                                     T*, cudaStream_t);

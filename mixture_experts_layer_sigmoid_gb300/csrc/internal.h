@@ -127,11 +127,12 @@ cudaError_t launch_gate_grad(const T* dY, const T* Yp, const int* row_of, const 
 // Folded routing weights: dz from the fc2-dgrad partial dot products.
 cudaError_t launch_gate_dz(const float* dg_part, int nslots, const int* row_of, const float* gates,
                            const float* selsc, int T_, int k, int score, float* dz, cudaStream_t s);
+// x: the layer input (row r of the permuted buffer is token slot_of[r] / k);
 // part: MT_max x H fp32 scratch (per-tile partial sums).
 template <typename T>
-cudaError_t launch_router_wgrad(const T* Xp, const int* slot_of, const int* poff, const int* meta,
-                                int MT_max, const float* dz, int H, int E, float* part, float* dWr,
-                                cudaStream_t s);
+cudaError_t launch_router_wgrad(const T* x, const int* slot_of, const int* poff, const int* meta,
+                                int MT_max, const float* dz, int H, int E, int k, float* part,
+                                float* dWr, cudaStream_t s);
 cudaError_t launch_transpose_f32(const float* in, int rows, int cols, float* out, cudaStream_t s);
 template <typename T>
 cudaError_t launch_unpermute_reduce(const T* dXp, const T* dXs, const int* row_of,
