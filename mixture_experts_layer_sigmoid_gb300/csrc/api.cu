@@ -57,7 +57,8 @@ Layout make_layout(const moe_config_t& c, int T)
     L.pairtab = take(sizeof(int) * ((size_t)L.MT_max + c.E + 1));   // pairs, then E+1 pair offsets
     L.rowof = take(sizeof(int) * L.R);
     L.slotof = take(sizeof(int) * L.Rp_max);
-    L.Xp = take(es * L.Rp_max * c.H);
+    // (the FP8 layer keeps only the codes of the permuted rows)
+    L.Xp = take(c.dtype == MOE_FP8_BLOCK ? 0 : es * L.Rp_max * c.H);
     L.A = take(es * L.Rp_max * c.F);
     L.U = take(es * L.Rp_max * c.F);
     L.fold = (c.flags & MOE_FLAG_FOLD_GATES) != 0;
@@ -587,7 +588,6 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     int* pairtab = reinterpret_cast<int*>(sv + L.pairtab);
     int* rowof = reinterpret_cast<int*>(sv + L.rowof);
     int* slotof = reinterpret_cast<int*>(sv + L.slotof);
-    T* Xp = reinterpret_cast<T*>(sv + L.Xp);
     T* A = reinterpret_cast<T*>(sv + L.A);
     T* U = reinterpret_cast<T*>(sv + L.U);
     T* Hh = reinterpret_cast<T*>((L.fold ? ws : sv) + L.Hh);
@@ -603,7 +603,7 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
                                    reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab,
                                    pairtab + L.MT_max, capacity(c, T_), kept));
     MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
-    MOE_STAGE(ST_PERMUTE, launch_permute_quant(x, rowof, poff, counts, T_, H, E, k, Xp, u8(sv, L.Xq),
+    MOE_STAGE(ST_PERMUTE, launch_permute_quant(x, rowof, poff, counts, T_, H, E, k, nullptr, u8(sv, L.Xq),
                                                f32(sv, L.sX), s));
     // one orientation of the weight codes: the forward GEMMs read them
     // MN-major, the data-gradient GEMMs K-major
@@ -668,7 +668,6 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     const int* pairtab = reinterpret_cast<const int*>(sv + L.pairtab);
     const int* rowof = reinterpret_cast<const int*>(sv + L.rowof);
     const int* slotof = reinterpret_cast<const int*>(sv + L.slotof);
-    const T* Xp = reinterpret_cast<const T*>(sv + L.Xp);
     const T* A = reinterpret_cast<const T*>(sv + L.A);
     const T* U = reinterpret_cast<const T*>(sv + L.U);
     T* Hh = reinterpret_cast<T*>((L.fold ? ws : sv) + L.Hh);   // folded: recomputed below
@@ -741,8 +740,9 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.O0 = dXp; d.ldo = H; d.status = status;
     MOE_STAGE(ST_FC1_DGRAD, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
     // fc1 wgrad: dWg[e] = Xp_e^T dA_e, dWu[e] = Xp_e^T dU_e
-    MOE_STAGE(ST_QT, launch_quant(QuantJob{Xp, meta + 1, Rp, H, Rp, nullptr, nullptr, 0, u8(ws, L.XpTq),
-                                           f32(ws, L.sXpT), 0}, s));
+    // the permuted rows are token rows of x (no bf16 copy of them is kept)
+    MOE_STAGE(ST_QT, launch_quant(QuantJob{static_cast<const T*>(a->x), meta + 1, Rp, H, Rp, nullptr,
+                                           nullptr, 0, u8(ws, L.XpTq), f32(ws, L.sXpT), 0, slotof, k}, s));
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
     d.N = F; d.M_out = H; d.E = E;

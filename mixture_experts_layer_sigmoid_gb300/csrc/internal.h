@@ -140,6 +140,7 @@ cudaError_t launch_unpermute_reduce(const T* dXp, const T* dXs, const int* row_o
                                     int H, int k, T* dX, cudaStream_t s);
 
 // blockwise FP8 quantisers (quant.cu)
+// Xp may be null (codes only).
 cudaError_t launch_permute_quant(const __nv_bfloat16* x, const int* row_of, const int* poff,
                                  const int* counts, int T_, int H, int E, int k, __nv_bfloat16* Xp,
                                  uint8_t* Xq, float* sX, cudaStream_t s);
@@ -149,12 +150,16 @@ cudaError_t launch_permute_quant(const __nv_bfloat16* x, const int* row_of, cons
 // tile s[rows/128][C/128] (q_tiles 1). qT != null: transposed codes
 // [C][rows_cap] with per-column scales over 128 rows sT[C][rows_cap/128]
 // (t_tiles 0) or per-tile scales sT[C/128][rows_cap/128] (t_tiles 1).
+// gather_slot != null: row r of the input is row gather_slot[r] / gather_k of
+// `in` (the token of a permuted row), or zeros where gather_slot[r] < 0.
 struct QuantJob {
     const __nv_bfloat16* in;
     const int* rows_dev;
     int rows_max, C, rows_cap;
     uint8_t* q; float* s; int q_tiles;
     uint8_t* qT; float* sT; int t_tiles;
+    const int* gather_slot = nullptr;
+    int gather_k = 1;
 };
 cudaError_t launch_quant(const QuantJob& j, cudaStream_t s);
 

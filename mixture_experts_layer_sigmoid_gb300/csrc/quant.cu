@@ -8,7 +8,8 @@
 // value v is stored as E4M3(v / s), rounded to nearest even and saturated.
 //
 // Kernels:
-//   permute_quant_kernel  x -> permuted rows Xp (bf16) and their 1x128 codes
+//   permute_quant_kernel  x -> the 1x128 codes of the permuted rows (and,
+//                         optionally, the bf16 permuted rows Xp)
 //   quant_tiles_kernel    [rows][C] bf16 in 128x128 tiles -> any of: codes
 //                         [rows][C] with 1x128 row scales or one scale per
 //                         tile (weights), transposed codes [C][rows] with
@@ -110,7 +111,7 @@ permute_quant_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict_
         const int e = b - T_;
         for (int r = poff[e] + counts[e]; r < poff[e + 1]; ++r) {
             for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-                reinterpret_cast<uint4*>(Xp + (size_t)r * H)[v] = make_uint4(0, 0, 0, 0);
+                if (Xp) reinterpret_cast<uint4*>(Xp + (size_t)r * H)[v] = make_uint4(0, 0, 0, 0);
                 reinterpret_cast<uint2*>(Xq + (size_t)r * H)[v] = make_uint2(0, 0);
             }
             for (int j = threadIdx.x; j < nb; j += blockDim.x) sX[(size_t)r * nb + j] = 1.f;
@@ -131,7 +132,7 @@ permute_quant_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict_
         if (!act) continue;
         const uint2 c = codes8(f, s);
         for (int j = 0; j < k; ++j) {
-            reinterpret_cast<uint4*>(Xp + (size_t)rows[j] * H)[v] = u;
+            if (Xp) reinterpret_cast<uint4*>(Xp + (size_t)rows[j] * H)[v] = u;
             reinterpret_cast<uint2*>(Xq + (size_t)rows[j] * H)[v] = c;
             if ((threadIdx.x & 15) == 0) sX[(size_t)rows[j] * nb + v / 16] = s;
         }
@@ -255,11 +256,14 @@ __device__ __forceinline__ void write_transposed(const uint8_t* qs, uint8_t* dst
 //         sT[C][rows_cap/128]
 //   TM 2: transposed codes qT[C][rows_cap], one scale per tile, sT[C/128][rows_cap/128]
 // Expert-stacked weights [E][R][C] with R a multiple of 128 are rows = E R.
+// With a gather map, row r is token gather_slot[r] / gather_k of the input
+// (the permuted rows of the layer input without their bf16 copy).
 template <int QM, int TM>
 __global__ void __launch_bounds__(256, 2)
 quant_tiles_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__ rows_dev,
                    int rows_fixed, int C, int rows_cap, uint8_t* __restrict__ q,
-                   float* __restrict__ s, uint8_t* __restrict__ qT, float* __restrict__ sT)
+                   float* __restrict__ s, uint8_t* __restrict__ qT, float* __restrict__ sT,
+                   const int* __restrict__ gslot, int gk)
 {
     __shared__ __align__(16) __nv_bfloat16 tile[128][136];
     __shared__ __align__(16) uint8_t qs[TM ? 128 * kQS : 16];
@@ -270,13 +274,32 @@ quant_tiles_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__
     const int ntiles = (rows / 128) * ncb;
     const int tid = threadIdx.x, sub = tid & 15;   // 16 threads per tile row, 8 columns each
     uint4 u[8];                                     // rows (tid / 16) + 16 j of the tile
+    // With a gather map, row r of the tile is token gslot[r] / gk of `in`
+    // (zeros for a pad row); the map entries of this thread's rows are read
+    // one tile ahead of their data, so the data loads never wait on them.
+    int sl[8];
+    auto load_slots = [&](int t) {
+        const int rb = t / ncb;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sl[j] = gslot[rb * 128 + (tid >> 4) + 16 * j];
+    };
     auto fetch = [&](int t) {
         const int rb = t / ncb, cb = t - rb * ncb;
-        const __nv_bfloat16* src = in + (size_t)rb * 128 * C + (size_t)cb * 128 + sub * 8;
+        if (gslot) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) u[j] = *reinterpret_cast<const uint4*>(src + (size_t)((tid >> 4) + 16 * j) * C);
+            for (int j = 0; j < 8; ++j)
+                u[j] = sl[j] >= 0 ? *reinterpret_cast<const uint4*>(in + (size_t)(sl[j] / gk) * C +
+                                                                    (size_t)cb * 128 + sub * 8)
+                                  : make_uint4(0, 0, 0, 0);
+            if (t + (int)gridDim.x < ntiles) load_slots(t + gridDim.x);
+        } else {
+            const __nv_bfloat16* src = in + (size_t)rb * 128 * C + (size_t)cb * 128 + sub * 8;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) u[j] = *reinterpret_cast<const uint4*>(src + (size_t)((tid >> 4) + 16 * j) * C);
+        }
     };
     int t = blockIdx.x;
+    if (gslot && t < ntiles) load_slots(t);
     if (t < ntiles) fetch(t);
     for (; t < ntiles; t += gridDim.x) {
         const int rb = t / ncb, cb = t - rb * ncb;
@@ -360,7 +383,8 @@ cudaError_t run_quant(const QuantJob& j, cudaStream_t st)
     if (tiles <= 0) return cudaSuccess;
     const long long grid = tiles < (long long)sms * per_sm ? tiles : (long long)sms * per_sm;
     quant_tiles_kernel<QM, TM><<<(unsigned)grid, 256, 0, st>>>(j.in, j.rows_dev, j.rows_max, j.C,
-                                                               j.rows_cap, j.q, j.s, j.qT, j.sT);
+                                                               j.rows_cap, j.q, j.s, j.qT, j.sT,
+                                                               j.gather_slot, j.gather_k);
     return cudaGetLastError();
 }
 
