@@ -478,13 +478,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                             // operand) is written by this thread straight from registers
                             __nv_bfloat16* Hp = fold && d.O2 ? static_cast<__nv_bfloat16*>(d.O2) + o : nullptr;
                             if (valid) {
+                                // all 64 columns of a and u in flight at once (one
+                                // load round trip per 64-column unit)
+                                uint4 ra[8], ru[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    ra[i] = reinterpret_cast<const uint4*>(X0)[i];
+                                    ru[i] = reinterpret_cast<const uint4*>(X1)[i];
+                                }
                                 float av[32], uv[32];
 #pragma unroll
                                 for (int hf = 0; hf < 2; ++hf) {
                                     float (&dd)[32] = hf ? d1 : d0;
                                     float (&ee)[32] = hf ? e1 : e0;
-                                    load32_bf16(X0 + 32 * hf, av);
-                                    load32_bf16(X1 + 32 * hf, uv);
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&ra[4 * hf + i]);
+                                        const __nv_bfloat162* hu = reinterpret_cast<const __nv_bfloat162*>(&ru[4 * hf + i]);
+#pragma unroll
+                                        for (int jj = 0; jj < 4; ++jj) {
+                                            const float2 fa = __bfloat1622float2(ha[jj]);
+                                            const float2 fu = __bfloat1622float2(hu[jj]);
+                                            av[8 * i + 2 * jj] = fa.x; av[8 * i + 2 * jj + 1] = fa.y;
+                                            uv[8 * i + 2 * jj] = fu.x; uv[8 * i + 2 * jj + 1] = fu.y;
+                                        }
+                                    }
                                     if (fold) {
 #pragma unroll
                                         for (int i = 0; i < 32; ++i) {
