@@ -17,6 +17,10 @@ namespace {
 template <typename T> struct Vec;
 template <> struct Vec<float> {
     static constexpr int N = 4;
+    __device__ static void unpack(const uint4& q, float (&v)[4]) {
+        v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y);
+        v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
+    }
     __device__ static void load(const float* p, float (&v)[4]) {
         float4 q = *reinterpret_cast<const float4*>(p);
         v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
@@ -27,14 +31,16 @@ template <> struct Vec<float> {
 };
 template <> struct Vec<__nv_bfloat16> {
     static constexpr int N = 8;
-    __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
-        uint4 q = *reinterpret_cast<const uint4*>(p);
+    __device__ static void unpack(const uint4& q, float (&v)[8]) {
         const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float2 f = __bfloat1622float2(h[i]);
             v[2 * i] = f.x; v[2 * i + 1] = f.y;
         }
+    }
+    __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
+        unpack(*reinterpret_cast<const uint4*>(p), v);
     }
     __device__ static void store(__nv_bfloat16* p, const float (&v)[8]) {
         uint4 q;
@@ -44,6 +50,21 @@ template <> struct Vec<__nv_bfloat16> {
         *reinterpret_cast<uint4*>(p) = q;
     }
 };
+
+// The 16-byte vectors at column vector v of a token's k rows, all loads in
+// flight together (slots past k untouched). KM >= k is a compile-time bound
+// (2, 4 or 8), so the slot arrays stay in registers.
+template <typename T, int KM>
+__device__ __forceinline__ void load_rows(const T* __restrict__ base, const int (&rows)[KM], int k,
+                                          int H, int v, uint4 (&raw)[KM])
+{
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+        if (j < k) raw[j] = *reinterpret_cast<const uint4*>(base + (size_t)rows[j] * H + v * Vec<T>::N);
+}
+
+// Slot bound of a launch: the smallest of 2, 4, 8 that holds k.
+inline int slot_bound(int k) { return k <= 2 ? 2 : (k <= 4 ? 4 : 8); }
 
 constexpr int kRowThreads = 128;
 
@@ -58,7 +79,7 @@ __device__ void zero_pad_rows(T* buf, int H, int e, const int* poff, const int* 
 }
 
 // Blocks [0, T): copy x[t] to its k rows. Blocks [T, T+E): zero pad rows.
-template <typename T>
+template <typename T, int KM>
 __global__ void __launch_bounds__(kRowThreads)
 permute_kernel(const T* __restrict__ x, const int* __restrict__ row_of, const int* __restrict__ poff,
                const int* __restrict__ counts, int T_, int H, int k, T* __restrict__ Xp)
@@ -66,37 +87,45 @@ permute_kernel(const T* __restrict__ x, const int* __restrict__ row_of, const in
     const int b = blockIdx.x;
     if (b >= T_) { zero_pad_rows(Xp, H, b - T_, poff, counts); return; }
     constexpr int V = 16 / sizeof(T);
-    int rows[kMaxK];
-    for (int j = 0; j < k; ++j) rows[j] = row_of[(size_t)b * k + j];
+    int rows[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) rows[j] = j < k ? row_of[(size_t)b * k + j] : 0;
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)b * H);
     for (int v = threadIdx.x; v < H / V; v += kRowThreads) {
         uint4 q = src[v];
-        for (int j = 0; j < k; ++j) reinterpret_cast<uint4*>(Xp + (size_t)rows[j] * H)[v] = q;
+#pragma unroll
+        for (int j = 0; j < KM; ++j)
+            if (j < k) reinterpret_cast<uint4*>(Xp + (size_t)rows[j] * H)[v] = q;
     }
 }
 
 // y[t] = sum_j gates[t, j] Yp[row_of(t, j)] (+ Ys[t]), fp32, slot order.
-template <typename T>
+template <typename T, int KM>
 __global__ void __launch_bounds__(kRowThreads)
 combine_kernel(const T* __restrict__ Yp, const T* __restrict__ Ys, const int* __restrict__ row_of,
                const float* __restrict__ gates, int H, int k, T* __restrict__ y)
 {
     constexpr int V = Vec<T>::N;
     const int t = blockIdx.x;
-    int rows[kMaxK];
-    float g[kMaxK];
+    int rows[KM];
+    float g[KM];
     // gates == null: the routing weights were folded into the expert
     // activations, so the expert outputs are already weighted
-    for (int j = 0; j < k; ++j) {
-        rows[j] = row_of[(size_t)t * k + j];
-        g[j] = gates ? gates[(size_t)t * k + j] : 1.f;
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        rows[j] = j < k ? row_of[(size_t)t * k + j] : 0;
+        g[j] = (gates && j < k) ? gates[(size_t)t * k + j] : 1.f;
     }
     for (int v = threadIdx.x; v < H / V; v += kRowThreads) {
         float acc[V], in[V];
 #pragma unroll
         for (int i = 0; i < V; ++i) acc[i] = 0.f;
-        for (int j = 0; j < k; ++j) {
-            Vec<T>::load(Yp + (size_t)rows[j] * H + v * V, in);
+        uint4 raw[KM];
+        load_rows<T, KM>(Yp, rows, k, H, v, raw);
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+            if (j >= k) break;
+            Vec<T>::unpack(raw[j], in);
 #pragma unroll
             for (int i = 0; i < V; ++i) acc[i] = fmaf(g[j], in[i], acc[i]);
         }
@@ -136,7 +165,7 @@ __device__ __forceinline__ void router_dz(const float* dg, const float* g, const
 //   softmax: dz_j = g_j (dg_j - sum_i g_i dg_i)
 //   sigmoid: dz_j = s_j (1 - s_j) (dg_j - sum_i g_i dg_i) / sum_i s_i
 // Blocks [T, T+E) zero the pad rows of dYp.
-template <typename T>
+template <typename T, int KM>
 __global__ void __launch_bounds__(kRowThreads)
 gate_grad_kernel(const T* __restrict__ dY, const T* __restrict__ Yp, const int* __restrict__ row_of,
                  const float* __restrict__ gates, const float* __restrict__ selsc,
@@ -148,17 +177,23 @@ gate_grad_kernel(const T* __restrict__ dY, const T* __restrict__ Yp, const int* 
     constexpr int V = Vec<T>::N;
     __shared__ float red[kRowThreads / 32][kMaxK];
     const int t = b;
-    int rows[kMaxK];
-    float g[kMaxK], dot[kMaxK];
-    for (int j = 0; j < kMaxK; ++j) {
+    int rows[KM];
+    float g[kMaxK], dot[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
         dot[j] = 0.f;
-        if (j < k) { rows[j] = row_of[(size_t)t * k + j]; g[j] = gates[(size_t)t * k + j]; }
+        rows[j] = j < k ? row_of[(size_t)t * k + j] : 0;
+        g[j] = j < k ? gates[(size_t)t * k + j] : 0.f;
     }
     for (int v = threadIdx.x; v < H / V; v += kRowThreads) {
         float dy[V], yp[V], o[V];
         Vec<T>::load(dY + (size_t)t * H + v * V, dy);
-        for (int j = 0; j < k; ++j) {
-            Vec<T>::load(Yp + (size_t)rows[j] * H + v * V, yp);
+        uint4 raw[KM];
+        load_rows<T, KM>(Yp, rows, k, H, v, raw);
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+            if (j >= k) break;
+            Vec<T>::unpack(raw[j], yp);
             float s = 0.f;
 #pragma unroll
             for (int i = 0; i < V; ++i) { s = fmaf(dy[i], yp[i], s); o[i] = g[j] * dy[i]; }
@@ -167,7 +202,9 @@ gate_grad_kernel(const T* __restrict__ dY, const T* __restrict__ Yp, const int* 
         }
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int j = 0; j < k; ++j) {
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+        if (j >= k) break;
         float s = dot[j];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -354,7 +391,11 @@ template <typename T>
 cudaError_t launch_permute(const T* x, const int* row_of, const int* poff, const int* counts,
                            int T_, int H, int E, int k, T* Xp, cudaStream_t s)
 {
-    permute_kernel<T><<<T_ + E, kRowThreads, 0, s>>>(x, row_of, poff, counts, T_, H, k, Xp);
+    switch (slot_bound(k)) {
+    case 2: permute_kernel<T, 2><<<T_ + E, kRowThreads, 0, s>>>(x, row_of, poff, counts, T_, H, k, Xp); break;
+    case 4: permute_kernel<T, 4><<<T_ + E, kRowThreads, 0, s>>>(x, row_of, poff, counts, T_, H, k, Xp); break;
+    default: permute_kernel<T, 8><<<T_ + E, kRowThreads, 0, s>>>(x, row_of, poff, counts, T_, H, k, Xp); break;
+    }
     return cudaGetLastError();
 }
 
@@ -362,7 +403,11 @@ template <typename T>
 cudaError_t launch_combine(const T* Yp, const T* Ys, const int* row_of, const float* gates,
                            int T_, int H, int k, T* y, cudaStream_t s)
 {
-    combine_kernel<T><<<T_, kRowThreads, 0, s>>>(Yp, Ys, row_of, gates, H, k, y);
+    switch (slot_bound(k)) {
+    case 2: combine_kernel<T, 2><<<T_, kRowThreads, 0, s>>>(Yp, Ys, row_of, gates, H, k, y); break;
+    case 4: combine_kernel<T, 4><<<T_, kRowThreads, 0, s>>>(Yp, Ys, row_of, gates, H, k, y); break;
+    default: combine_kernel<T, 8><<<T_, kRowThreads, 0, s>>>(Yp, Ys, row_of, gates, H, k, y); break;
+    }
     return cudaGetLastError();
 }
 
@@ -373,8 +418,14 @@ cudaError_t launch_gate_grad(const T* dY, const T* Yp, const int* row_of, const 
                              float* dz, cudaStream_t s)
 {
     (void)topk;
-    gate_grad_kernel<T><<<T_ + E, kRowThreads, 0, s>>>(dY, Yp, row_of, gates, selsc, poff, counts,
-                                                       T_, H, k, score, dYp, dz);
+    switch (slot_bound(k)) {
+    case 2: gate_grad_kernel<T, 2><<<T_ + E, kRowThreads, 0, s>>>(dY, Yp, row_of, gates, selsc, poff, counts,
+                                                       T_, H, k, score, dYp, dz); break;
+    case 4: gate_grad_kernel<T, 4><<<T_ + E, kRowThreads, 0, s>>>(dY, Yp, row_of, gates, selsc, poff, counts,
+                                                       T_, H, k, score, dYp, dz); break;
+    default: gate_grad_kernel<T, 8><<<T_ + E, kRowThreads, 0, s>>>(dY, Yp, row_of, gates, selsc, poff, counts,
+                                                       T_, H, k, score, dYp, dz); break;
+    }
     return cudaGetLastError();
 }
 
