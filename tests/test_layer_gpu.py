@@ -141,10 +141,22 @@ def test_empty_experts_get_zero_gradients():
     compare_all(w, inp, r, gpu, ref)
 
 
-def test_deterministic_bitwise():
-    w = CASES["deepseek_small"]
+# (case, folded gates) for the determinism and CUDA-graph tests: bf16 with a
+# shared expert, fp32, the blockwise-FP8 layer, and the folded order
+REPEAT_CASES = [("deepseek_small", False), ("fp32_sigmoid_shared", False), ("fp8_small", False),
+                ("deepseek_small", True), ("fp8_small", True)]
+FP8_SMALL = mi.scaled(W["qwen3_235b_fp8"], T=600, H=256, E=8, k=4, F=256)
+
+
+def _case(name):
+    return FP8_SMALL if name == "fp8_small" else CASES[name]
+
+
+@pytest.mark.parametrize("name,fold", REPEAT_CASES)
+def test_deterministic_bitwise(name, fold):
+    w = _case(name)
     inp = mi.make_inputs(w)
-    a, layer = run_gpu(w, inp)
+    a, layer = run_gpu(w, inp, fold=fold)
     b, _ = run_gpu(w, inp, layer=layer)
     for k in a:
         assert torch.equal(a[k], b[k]), k
@@ -177,15 +189,16 @@ def test_bad_call_arguments_are_rejected_before_launch():
     assert st == moe.MOE_ERR_INVALID_ARG
 
 
-def test_forward_backward_capture_in_a_cuda_graph():
+@pytest.mark.parametrize("name,fold", REPEAT_CASES)
+def test_forward_backward_capture_in_a_cuda_graph(name, fold):
     """A call enqueues kernels only (no host synchronisation, no allocation),
     so forward + backward can be captured once and replayed; the replay
     reproduces the eager results bit for bit."""
     import mixture_experts_layer_sigmoid_gb300 as moe
-    w = CASES["deepseek_small"]
+    w = _case(name)
     inp = mi.make_inputs(w)
     g = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
-    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, Fs=w.Fs)
+    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=w.dtype, Fs=w.Fs, fold_gates=fold)
     args = (g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"], g["Wsg"], g["Wsu"], g["Wsd"])
     y = torch.empty_like(g["x"])
     grads = None
