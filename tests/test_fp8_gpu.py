@@ -91,7 +91,12 @@ def test_fp8_folded_gates_match_oracle(name):
 
 
 def _fp8_parity(name, fold):
-    w = FP8_CASES[name]
+    print(name, fp8_layer_parity(FP8_CASES[name], fold))
+
+
+def fp8_layer_parity(w, fold=False):
+    """The FP8 layer on workload w against the oracle's FP8 layer (bounds in
+    the module docstring); returns the error report."""
     inp = mi.make_inputs(w)
     g = upload(inp)
     layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=moe.MOE_FP8_BLOCK,
@@ -129,4 +134,4 @@ def _fp8_parity(name, fold):
                 assert np.all(gb == 0)
             else:
                 assert np.linalg.norm(gb - wb) / nw <= 4e-2, gname
-    print(name, rep)
+    return rep
