@@ -372,7 +372,10 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
     d.N = F; d.K = H; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
-    d.prefer_pair = (long long)T_ * k >= 512ll * E;
+    // a pair reads each [Wg | Wu] column tile once for both of an expert's
+    // 128-row units; that pays from two units per expert on (the other row
+    // GEMMs only from four)
+    d.prefer_pair = (long long)T_ * k >= 256ll * E;
     d.A0 = Xp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = a->W_gate; d.B1 = a->W_up; d.ldb = F; d.b_kmajor = 0; d.b_estride = (long long)H * F;
     d.b_rows = E * H;
