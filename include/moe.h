@@ -230,10 +230,11 @@ moe_status_t moe_stage_times(moe_plan_t plan, moe_stage_time_t* out, int capacit
  * segment starts) and row_of (T×k), from x (T×H act), Wr (H×E fp32) and the
  * optional bias b (E fp32). All pointers are caller-owned device pointers,
  * 16-byte aligned; nothing is allocated or freed.
- * Scratch: a 4 MiB array inside the library's device image, held on every GPU
+ * Scratch: a 64 MiB array inside the library's device image, held on every GPU
  * that loads the library until the process exits. A call needs about
- * 8·T·k + 8·ceil(T/32)·E + 508·min(E, T·k) bytes of it; larger T returns
- * MOE_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ * 8·T·k + 8·ceil(T/32)·E + 508·min(E, T·k) bytes of it, plus up to 32·T·E
+ * for E > 32 (the router's partial logits over at most 8 splits of H); larger
+ * T returns MOE_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any
  * stream capture. All calls share the array and it keeps the last call's

@@ -26,7 +26,7 @@ struct Layout {
     size_t topk, gates, selsc, counts, kept, poff, meta, tiletab, pairtab, rowof, slotof;
     size_t Xp, A, U, Hh, Yp, As, Us, Hs, saved_bytes;
     // workspace
-    size_t status, hist, blkbase, Ys, dYp, dA, dU, dXp, dz, WrT, wrpart, dAs, dUs, dXs, dgpart, ws_bytes;
+    size_t status, hist, blkbase, zpart, Ys, dYp, dA, dU, dXp, dz, WrT, wrpart, dAs, dUs, dXs, dgpart, ws_bytes;
     bool fold;   // Hh and Yp live in the workspace (MOE_FLAG_FOLD_GATES)
     // blockwise FP8 (saved: permuted activations and weights; ws: the rest)
     size_t Xq, sX, WgQ, sWg, WuQ, sWu, WgQT, sWgT, WuQT, sWuT, WdQ, sWd, WdQT, sWdT;
@@ -83,6 +83,8 @@ Layout make_layout(const moe_config_t& c, int T)
     L.status = take(256);
     L.hist = take(sizeof(int) * (size_t)L.NB * c.E);
     L.blkbase = take(sizeof(int) * (size_t)L.NB * c.E);
+    // partial logits of the H-split router
+    L.zpart = take(sizeof(float) * router_zpart_floats(T, c.H, c.E));
     L.Ys = take(c.Fs ? es * (size_t)T * c.H : 0);
     L.dYp = take(es * L.Rp_max * c.H);
     L.dA = take(es * L.Rp_max * c.F);
@@ -354,7 +356,8 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
 
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
     MOE_STAGE(ST_ROUTER, launch_router<T>(x, a->Wr, a->b, T_, H, E, k, c.score, topk, gates, selsc,
-                              reinterpret_cast<int*>(ws + L.hist), s, a->replay_topk, status));
+                              reinterpret_cast<int*>(ws + L.hist), s, a->replay_topk, status,
+                              reinterpret_cast<float*>(ws + L.zpart), router_zpart_floats(T_, H, E)));
     MOE_STAGE(ST_SCAN, launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
                          reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab,
                                    pairtab + L.MT_max, capacity(c, T_), kept));
@@ -601,7 +604,9 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
 
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
     MOE_STAGE(ST_ROUTER, launch_router<T>(x, a->Wr, a->b, T_, H, E, k, c.score, topk, gates, selsc,
-                                          reinterpret_cast<int*>(ws + L.hist), s, a->replay_topk, status));
+                                          reinterpret_cast<int*>(ws + L.hist), s, a->replay_topk, status,
+                                          reinterpret_cast<float*>(ws + L.zpart),
+                                          router_zpart_floats(T_, H, E)));
     MOE_STAGE(ST_SCAN, launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
                                    reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab,
                                    pairtab + L.MT_max, capacity(c, T_), kept));

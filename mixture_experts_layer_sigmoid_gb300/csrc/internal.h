@@ -21,6 +21,7 @@ constexpr int kRouterTokens = 32;
 // Largest number of routed experts / top-k the kernels accept.
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;
+constexpr int kRouterSplitMax = 8;   // H splits of the tiled router (partial logits in the workspace)
 // Device-side wait limit of the pipelined kernels, in nanoseconds.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
@@ -106,7 +107,11 @@ template <typename T>
 cudaError_t launch_router(const T* x, const float* Wr, const float* b, int T_, int H, int E, int k,
                           int score, int* topk, float* gates, float* selsc, int* hist,
                           cudaStream_t s,
-                          const int* replay = nullptr, DeviceStatus* status = nullptr);
+                          const int* replay = nullptr, DeviceStatus* status = nullptr,
+                          float* zpart = nullptr, size_t zpart_floats = 0);
+// fp32 entries of the partial-logit buffer launch_router needs for T tokens
+// (0 when the router for this H and E runs unsplit).
+size_t router_zpart_floats(int T, int H, int E);
 cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff, int* blkbase,
                         int* tile_tab, int* meta, int* slot_of, cudaStream_t s,
                         int* pair_tab = nullptr, int* pair_off = nullptr, int cap = -1,

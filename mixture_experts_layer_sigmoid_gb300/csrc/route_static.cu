@@ -27,7 +27,7 @@
 namespace moe {
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(4) << 20;   // 4 MiB
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;   // 64 MiB
 static __device__ __align__(256) unsigned char g_route_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -52,7 +52,7 @@ cudaError_t scratch_address(int device, void** out)
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
 struct StaticLayout {
-    size_t selsc, hist, blkbase, tiletab, meta, slotof, bytes;
+    size_t selsc, hist, blkbase, tiletab, meta, slotof, zpart, bytes;
 };
 
 // Offsets of the routing scratch inside the static array for T tokens.
@@ -70,6 +70,7 @@ StaticLayout static_layout(const moe_config_t& c, int T)
     L.tiletab = o; o = up256(o + sizeof(int) * (Rp / kTileM));
     L.meta = o;    o = up256(o + sizeof(int) * 4);
     L.slotof = o;  o = up256(o + sizeof(int) * Rp);
+    L.zpart = o;   o = up256(o + sizeof(float) * router_zpart_floats(T, c.H, c.E));
     L.bytes = o;
     return L;
 }
@@ -113,15 +114,18 @@ moe_status_t moe_route_static(moe_plan_t plan, int T, const void* x, const float
         int* tiletab = reinterpret_cast<int*>(s8 + L.tiletab);
         int* meta = reinterpret_cast<int*>(s8 + L.meta);
         int* slotof = reinterpret_cast<int*>(s8 + L.slotof);
+        float* zpart = reinterpret_cast<float*>(s8 + L.zpart);
+        const size_t nz = router_zpart_floats(T, c.H, c.E);
         cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
         const int nb = (T + kRouterTokens - 1) / kRouterTokens;
         cudaError_t e;
         if (c.dtype == MOE_FP32)
             e = launch_router<float>(static_cast<const float*>(x), Wr, b, T, c.H, c.E, c.top_k,
-                                     c.score, topk_idx, gates, selsc, hist, s);
+                                     c.score, topk_idx, gates, selsc, hist, s, nullptr, nullptr, zpart, nz);
         else
             e = launch_router<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(x), Wr, b, T, c.H,
-                                             c.E, c.top_k, c.score, topk_idx, gates, selsc, hist, s);
+                                             c.E, c.top_k, c.score, topk_idx, gates, selsc, hist, s,
+                                             nullptr, nullptr, zpart, nz);
         if (e == cudaSuccess)
             e = launch_scan(hist, nb, c.E, counts, offsets, blkbase, tiletab, meta, slotof, s);
         if (e == cudaSuccess) e = launch_index(topk_idx, blkbase, T, c.E, c.top_k, row_of, slotof, s);

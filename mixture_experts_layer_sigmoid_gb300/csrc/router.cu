@@ -26,6 +26,9 @@ namespace {
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 
+// Rows of each half of H per chunk of the tiled router (EPL experts per lane).
+constexpr int router_chunk_rows(int epl) { return (2048 / (epl * 32)) < 16 ? 2048 / (epl * 32) : 16; }
+
 // (value, index) ordering: larger value first, then lower index.
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
@@ -136,15 +139,16 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // x chunks are register-prefetched and staged transposed in fp32, so two
 // 16-byte shared loads give a thread its 8 tokens' values of one h. The two
 // halves are added in fixed order, then one warp per token selects the top k.
-template <typename T, int EPL>
+template <typename T, int EPL, bool SPLIT>
 __global__ void __launch_bounds__(256, EPL <= 4 ? 3 : 2)
 router_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float* __restrict__ b,
               int T_, int H, int E, int k, int score, int* __restrict__ topk,
               float* __restrict__ gates, float* __restrict__ selsc, int* __restrict__ hist,
-              const int* __restrict__ replay, DeviceStatus* __restrict__ status)
+              const int* __restrict__ replay, DeviceStatus* __restrict__ status,
+              float* __restrict__ zpart)
 {
     constexpr int EW = EPL * 32;                          // padded expert width
-    constexpr int HC = (2048 / EW) < 16 ? 2048 / EW : 16; // rows of H per half per chunk
+    constexpr int HC = router_chunk_rows(EPL);           // rows of H per half per chunk
     constexpr int TQ = 8;                                 // tokens per thread
     constexpr int V = 16 / sizeof(T);                     // x values per 16-byte load
     constexpr int XSEG = HC / V;                          // 16-byte pieces per token row per half
@@ -159,7 +163,15 @@ router_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float
     const int half = warp >> 2, tq0 = (warp & 3) * TQ;
     const int t0 = blockIdx.x * kRouterTokens;
     const int Hh = H / 2;                 // H is a multiple of 128
-    const int nchunk = Hh / HC;
+    // split blockIdx.y of gridDim.y takes the y-th of gridDim.y equal ranges
+    // of chunks of both halves (the split count divides the chunk count) and
+    // leaves its partial logits in zpart, for router_finish_kernel to route; a
+    // grid of one split routes here
+    const int nchunk = Hh / HC / (SPLIT ? (int)gridDim.y : 1);
+    if (SPLIT) {
+        Wr += (size_t)blockIdx.y * nchunk * HC * E;
+        x += (size_t)blockIdx.y * nchunk * HC;
+    }
     const int E4 = E / 4;
     const bool vec_w = (E & 3) == 0;      // Wr rows are 16-byte aligned
 
@@ -259,6 +271,22 @@ router_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float
             for (int i = 0; i < EPL; ++i) part[(tq0 + q) * EW + lane + 32 * i] = acc[q][i];
     }
     __syncthreads();
+    if (SPLIT) {
+        if (half == 0) {
+            float* zp = zpart + (size_t)blockIdx.y * T_ * E;
+#pragma unroll
+            for (int q = 0; q < TQ; ++q) {
+                const int tt = tq0 + q, t = t0 + tt;
+                if (t >= T_) break;               // warp-uniform
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) {
+                    const int e = lane + 32 * i;
+                    if (e < E) zp[(size_t)t * E + e] = acc[q][i] + part[tt * EW + e];
+                }
+            }
+        }
+        return;
+    }
     if (half == 0) {
 #pragma unroll
         for (int q = 0; q < TQ; ++q) {
@@ -276,6 +304,49 @@ router_kernel(const T* __restrict__ x, const float* __restrict__ Wr, const float
     __syncthreads();
     const int ntok = min(kRouterTokens, T_ - t0);
     for (int e = tid; e < E; e += 256) {
+        int cnt = 0;
+        for (int tt = 0; tt < ntok; ++tt)
+            for (int j = 0; j < k; ++j) cnt += (sel_s[tt][j] == e);
+        hist[(size_t)blockIdx.x * E + e] = cnt;
+    }
+}
+
+// Second pass of a split router: the logits of a token are its splits'
+// partial sums added in split order, plus the bias; one warp routes each token
+// (kRouterTokens / 8 per warp) and the block counts its tokens' experts like
+// router_kernel.
+template <int EPL>
+__global__ void __launch_bounds__(256)
+router_finish_kernel(const float* __restrict__ zpart, int S, const float* __restrict__ b, int T_, int E,
+                     int k, int score, int* __restrict__ topk, float* __restrict__ gates,
+                     float* __restrict__ selsc, int* __restrict__ hist, const int* __restrict__ replay,
+                     DeviceStatus* __restrict__ status)
+{
+    constexpr int TPW = kRouterTokens / 8;
+    __shared__ int sel_s[kRouterTokens][kMaxK];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * kRouterTokens;
+#pragma unroll 1
+    for (int q = 0; q < TPW; ++q) {
+        const int tt = warp * TPW + q, t = t0 + tt;
+        if (t >= T_) break;                       // warp-uniform
+        float z[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) {
+                float v = zpart[(size_t)t * E + e];
+                for (int sp = 1; sp < S; ++sp) v += zpart[((size_t)sp * T_ + t) * E + e];
+                z[i] = v + (b ? b[e] : 0.f);
+            } else {
+                z[i] = -INFINITY;
+            }
+        }
+        warp_route_token<EPL>(z, t, E, k, score, replay, status, lane, topk, gates, selsc, sel_s[tt]);
+    }
+    __syncthreads();
+    const int ntok = min(kRouterTokens, T_ - t0);
+    for (int e = threadIdx.x; e < E; e += 256) {
         int cnt = 0;
         for (int tt = 0; tt < ntok; ++tt)
             for (int j = 0; j < k; ++j) cnt += (sel_s[tt][j] == e);
@@ -495,13 +566,48 @@ index_kernel(const int* __restrict__ topk, const int* __restrict__ blkbase, int 
     }
 }
 
+// H splits of the tiled router: the largest count up to kRouterSplitMax that
+// divides the number of chunks in each half of H. It depends on H and E alone, so a
+// token's logits (and hence its routing) do not depend on the batch it comes
+// in, on the entry point, or on the GPU's SM count.
+int router_split_count(int H, int E)
+{
+    if (E <= 32) return 1;
+    const int epl = E <= 64 ? 2 : (E <= 128 ? 4 : 8);
+    const int nchunk = (H / 2) / router_chunk_rows(epl);
+    for (int S = kRouterSplitMax; S > 1; --S)
+        if (nchunk % S == 0) return S;
+    return 1;
+}
+
+template <typename T, int EPL>
+cudaError_t run_router_tiled(const T* x, const float* Wr, const float* b, int T_, int H, int E, int k,
+                             int score, int* topk, float* gates, float* selsc, int* hist,
+                             cudaStream_t s, const int* replay, DeviceStatus* status, float* zpart,
+                             size_t zpart_floats)
+{
+    const int nblk = (T_ + kRouterTokens - 1) / kRouterTokens;
+    const int S = router_split_count(H, E);
+    if (S > 1 && (!zpart || zpart_floats < (size_t)S * T_ * E)) return cudaErrorInvalidValue;
+    if (S == 1) {
+        router_kernel<T, EPL, false><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc,
+                                                          hist, replay, status, nullptr);
+        return cudaGetLastError();
+    }
+    router_kernel<T, EPL, true><<<dim3(nblk, S), 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates,
+                                                              selsc, hist, replay, status, zpart);
+    router_finish_kernel<EPL><<<nblk, 256, 0, s>>>(zpart, S, b, T_, E, k, score, topk, gates, selsc, hist,
+                                                   replay, status);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 template <typename T>
 cudaError_t launch_router(const T* x, const float* Wr, const float* b, int T_, int H, int E, int k,
                           int score, int* topk, float* gates, float* selsc, int* hist,
                           cudaStream_t s,
-                          const int* replay, DeviceStatus* status)
+                          const int* replay, DeviceStatus* status, float* zpart, size_t zpart_floats)
 {
     const int nblk = (T_ + kRouterTokens - 1) / kRouterTokens;
     if (E <= 8)
@@ -514,21 +620,29 @@ cudaError_t launch_router(const T* x, const float* Wr, const float* b, int T_, i
         router_small_kernel<T, 32><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
                                                                replay, status);
     else if (E <= 64)
-        router_kernel<T, 2><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
-                                                               replay, status);
+        return run_router_tiled<T, 2>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist, s, replay, status,
+                                      zpart, zpart_floats);
     else if (E <= 128)
-        router_kernel<T, 4><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
-                                                               replay, status);
+        return run_router_tiled<T, 4>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist, s, replay, status,
+                                      zpart, zpart_floats);
     else
-        router_kernel<T, 8><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist,
-                                                               replay, status);
+        return run_router_tiled<T, 8>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist, s, replay, status,
+                                      zpart, zpart_floats);
     return cudaGetLastError();
 }
 template cudaError_t launch_router<float>(const float*, const float*, const float*, int, int, int,
-                                          int, int, int*, float*, float*, int*, cudaStream_t, const int*, DeviceStatus*);
+                                          int, int, int*, float*, float*, int*, cudaStream_t, const int*,
+                                          DeviceStatus*, float*, size_t);
 template cudaError_t launch_router<__nv_bfloat16>(const __nv_bfloat16*, const float*, const float*,
                                                   int, int, int, int, int, int*, float*, float*,
-                                                  int*, cudaStream_t, const int*, DeviceStatus*);
+                                                  int*, cudaStream_t, const int*, DeviceStatus*, float*,
+                                                  size_t);
+
+size_t router_zpart_floats(int T, int H, int E)
+{
+    const int S = router_split_count(H, E);
+    return S > 1 ? (size_t)S * T * E : 0;
+}
 
 cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff, int* blkbase,
                         int* tile_tab, int* meta, int* slot_of, cudaStream_t s, int* pair_tab,
