@@ -193,7 +193,11 @@ __device__ __forceinline__ float block_max(float a, float* red)
 __device__ __forceinline__ void encode_rows(__nv_bfloat16 (*tile)[136], float sc, const float* sc_col,
                                             const float* rc_col, uint8_t* qs, uint8_t* dst, size_t ld)
 {
-    const int rr = threadIdx.x >> 1, hf = threadIdx.x & 1;
+    // lanes 0-15 of a warp take 16 consecutive rows at one column half and
+    // lanes 16-31 the same rows at the other, so that each 8-lane phase of a
+    // 16-byte shared load meets 8 different bank groups (row stride 68 words)
+    const int lane = threadIdx.x & 31;
+    const int rr = (threadIdx.x >> 5) * 16 + (lane & 15), hf = lane >> 4;
     const float rc = __frcp_rn(sc);
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
@@ -204,15 +208,15 @@ __device__ __forceinline__ void encode_rows(__nv_bfloat16 (*tile)[136], float sc
         uint32_t w[4];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t pr[2];
-#pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                const int c = 4 * q4 + 2 * b;
-                pr[b] = sc_col ? e4m3x2(f[c], f[c + 1], sc_col[c0 + c], sc_col[c0 + c + 1], rc_col[c0 + c],
-                                        rc_col[c0 + c + 1])
-                               : e4m3x2(f[c], f[c + 1], sc, sc, rc, rc);
+            const int c = 4 * q4;
+            if (sc_col) {   // 16-byte aligned per-column scales and reciprocals
+                const float4 a = reinterpret_cast<const float4*>(sc_col + c0)[q4];
+                const float4 r = reinterpret_cast<const float4*>(rc_col + c0)[q4];
+                w[q4] = e4m3x2(f[c], f[c + 1], a.x, a.y, r.x, r.y) |
+                        (e4m3x2(f[c + 2], f[c + 3], a.z, a.w, r.z, r.w) << 16);
+            } else {
+                w[q4] = e4m3x2(f[c], f[c + 1], sc, sc, rc, rc) | (e4m3x2(f[c + 2], f[c + 3], sc, sc, rc, rc) << 16);
             }
-            w[q4] = pr[0] | (pr[1] << 16);
         }
         const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(qs + qs_off(rr, c0)) = v;
@@ -259,7 +263,7 @@ __device__ __forceinline__ void write_transposed(const uint8_t* qs, uint8_t* dst
 // With a gather map, row r is token gather_slot[r] / gather_k of the input
 // (the permuted rows of the layer input without their bf16 copy).
 template <int QM, int TM>
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256, (QM == 0 && TM == 1) ? 3 : 2)
 quant_tiles_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__ rows_dev,
                    int rows_fixed, int C, int rows_cap, uint8_t* __restrict__ q,
                    float* __restrict__ s, uint8_t* __restrict__ qT, float* __restrict__ sT,
@@ -268,7 +272,9 @@ quant_tiles_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__
     __shared__ __align__(16) __nv_bfloat16 tile[128][136];
     __shared__ __align__(16) uint8_t qs[TM ? 128 * kQS : 16];
     __shared__ float red[256];
-    __shared__ float scol[128], rcol[128];
+    __shared__ __align__(16) float scol[128];
+    __shared__ __align__(16) float rcol[128];
+    __shared__ __align__(16) float colmax[TM == 1 ? 8 : 1][128];   // per warp, per tile column
     const int rows = rows_dev ? *rows_dev : rows_fixed;
     const int ncb = C / 128;
     const int ntiles = (rows / 128) * ncb;
@@ -308,6 +314,35 @@ quant_tiles_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__
         // whole of this tile's encoding
 #pragma unroll
         for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(&tile[(tid >> 4) + 16 * j][sub * 8]) = u[j];
+        if (TM == 1) {
+            // per-column amax of this thread's 8 rows, then of the warp's 16
+            // (lanes l and l ^ 16 hold the same columns), one partial per warp
+            // (bf16 pairs: the largest magnitude of bf16 values is exact in bf16)
+            __nv_bfloat162 cm[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cm[i] = __float2bfloat162_rn(0.f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u[j]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) cm[i] = __hmax2(cm[i], __habs2(h[i]));
+            }
+            float cf[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t bits = *reinterpret_cast<const uint32_t*>(&cm[i]);
+                bits = __shfl_xor_sync(0xffffffffu, bits, 16);
+                const __nv_bfloat162 other = *reinterpret_cast<const __nv_bfloat162*>(&bits);
+                const float2 m = __bfloat1622float2(__hmax2(cm[i], other));
+                cf[2 * i] = m.x;
+                cf[2 * i + 1] = m.y;
+            }
+            if ((tid & 31) < 16) {
+                float4* dst = reinterpret_cast<float4*>(&colmax[tid >> 5][sub * 8]);
+                dst[0] = make_float4(cf[0], cf[1], cf[2], cf[3]);
+                dst[1] = make_float4(cf[4], cf[5], cf[6], cf[7]);
+            }
+        }
         if (t + (int)gridDim.x < ntiles) fetch(t + gridDim.x);
         // row codes and amax from this thread's own staged values
         float amax = 0.f;
@@ -342,17 +377,16 @@ quant_tiles_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__
         }
         if (TM) {
             if (TM == 1) {
-                // column amax: threads (c = tid % 128, half = tid / 128) over 64 rows each
-                const int c = tid & 127, half = tid >> 7;
-                float a = 0.f;
-                for (int rr = half * 64; rr < half * 64 + 64; ++rr) a = fmaxf(a, fabsf(__bfloat162float(tile[rr][c])));
-                red[tid] = a;
-                __syncthreads();
-                if (half == 0) {
-                    const float s1 = block_scale(fmaxf(red[c], red[c + 128]));
-                    scol[c] = s1;
-                    rcol[c] = __frcp_rn(s1);
-                    sT[(size_t)(c0 + c) * (rows_cap / 128) + rb] = s1;
+                // column amax from the eight warps' partials (written before
+                // the barrier that follows the staging)
+                if (tid < 128) {
+                    float a = colmax[0][tid];
+#pragma unroll
+                    for (int w = 1; w < 8; ++w) a = fmaxf(a, colmax[w][tid]);
+                    const float s1 = block_scale(a);
+                    scol[tid] = s1;
+                    rcol[tid] = __frcp_rn(s1);
+                    sT[(size_t)(c0 + tid) * (rows_cap / 128) + rb] = s1;
                 }
                 __syncthreads();
             } else if (tid == 0) {
