@@ -166,6 +166,9 @@ struct DeviceGuard {
 }  // namespace moe
 
 namespace moe {
+
+thread_local unsigned long long t_kernel_launches = 0;
+
 namespace {
 enum Stage : int {
     ST_ROUTER, ST_SCAN, ST_INDEX, ST_PERMUTE, ST_FC1, ST_FC2, ST_FC1S, ST_FC2S, ST_COMBINE,
@@ -183,6 +186,7 @@ const char* const kStageNames[ST_COUNT] = {
 struct StageRec {
     int stage;
     cudaEvent_t start, stop;
+    int kernels;   // kernels the stage's call launched
 };
 }  // namespace
 }  // namespace moe
@@ -267,6 +271,7 @@ moe_status_t moe_stage_times(moe_plan_t plan, moe_stage_time_t* out, int capacit
     if (!g.ok) return MOE_ERR_CUDA;
     int order[ST_COUNT], n = 0;
     int launches[ST_COUNT] = {0};
+    bool seen[ST_COUNT] = {false};
     double ms[ST_COUNT] = {0.0};
     moe_status_t st = MOE_OK;
     for (auto& r : plan->recs) {
@@ -274,7 +279,11 @@ moe_status_t moe_stage_times(moe_plan_t plan, moe_stage_time_t* out, int capacit
         if (cudaEventSynchronize(r.stop) != cudaSuccess ||
             cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
             st = MOE_ERR_CUDA;
-        if (launches[r.stage]++ == 0) order[n++] = r.stage;
+        if (!seen[r.stage]) {
+            seen[r.stage] = true;
+            order[n++] = r.stage;
+        }
+        launches[r.stage] += r.kernels;
         ms[r.stage] += t;
         plan->spare.push_back(r.start);
         plan->spare.push_back(r.stop);
@@ -319,9 +328,11 @@ static cudaError_t run_stage(moe_plan_t p, int stage, cudaStream_t s, Fn&& launc
         }
     }
     cudaError_t e = cudaEventRecord(ev[0], s);
+    const unsigned long long n0 = t_kernel_launches;
     if (e == cudaSuccess) e = launch();
+    const int kernels = (int)(t_kernel_launches - n0);
     if (e == cudaSuccess) e = cudaEventRecord(ev[1], s);
-    p->recs.push_back({stage, ev[0], ev[1]});
+    p->recs.push_back({stage, ev[0], ev[1], kernels});
     return e;
 }
 #define MOE_STAGE(stage, call) \

@@ -58,6 +58,7 @@ moe_status_t moe_update_bias(int E, const int32_t* counts, float rate, float* b,
     if (!counts || !b || E < 1 || E > kMaxE || !(rate == rate) || rate - rate != 0.f)
         return MOE_ERR_INVALID_ARG;
     update_bias_kernel<<<1, kMaxE, 0, reinterpret_cast<cudaStream_t>(stream)>>>(E, counts, rate, b);
+    count_launches();
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -68,5 +69,6 @@ moe_status_t moe_diag_wait_timeout(void* ws, moe_stream_t stream)
     DeviceStatus* st = static_cast<DeviceStatus*>(ws);
     if (cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s) != cudaSuccess) return MOE_ERR_CUDA;
     wait_timeout_kernel<<<1, 32, 0, s>>>(st);
+    count_launches();
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -396,6 +396,7 @@ cudaError_t launch_permute(const T* x, const int* row_of, const int* poff, const
     case 4: permute_kernel<T, 4><<<T_ + E, kRowThreads, 0, s>>>(x, row_of, poff, counts, T_, H, k, Xp); break;
     default: permute_kernel<T, 8><<<T_ + E, kRowThreads, 0, s>>>(x, row_of, poff, counts, T_, H, k, Xp); break;
     }
+    count_launches();
     return cudaGetLastError();
 }
 
@@ -408,6 +409,7 @@ cudaError_t launch_combine(const T* Yp, const T* Ys, const int* row_of, const fl
     case 4: combine_kernel<T, 4><<<T_, kRowThreads, 0, s>>>(Yp, Ys, row_of, gates, H, k, y); break;
     default: combine_kernel<T, 8><<<T_, kRowThreads, 0, s>>>(Yp, Ys, row_of, gates, H, k, y); break;
     }
+    count_launches();
     return cudaGetLastError();
 }
 
@@ -426,6 +428,7 @@ cudaError_t launch_gate_grad(const T* dY, const T* Yp, const int* row_of, const 
     default: gate_grad_kernel<T, 8><<<T_ + E, kRowThreads, 0, s>>>(dY, Yp, row_of, gates, selsc, poff, counts,
                                                        T_, H, k, score, dYp, dz); break;
     }
+    count_launches();
     return cudaGetLastError();
 }
 
@@ -433,6 +436,7 @@ cudaError_t launch_gate_dz(const float* dg_part, int nslots, const int* row_of, 
                            const float* selsc, int T_, int k, int score, float* dz, cudaStream_t s)
 {
     gate_dz_kernel<<<(T_ + 7) / 8, 256, 0, s>>>(dg_part, nslots, row_of, gates, selsc, T_, k, score, dz);
+    count_launches();
     return cudaGetLastError();
 }
 
@@ -447,6 +451,7 @@ cudaError_t launch_router_wgrad(const T* x, const int* slot_of, const int* poff,
     }
     dim3 grid2((H + 255) / 256, E);
     router_wgrad_sum_kernel<<<grid2, 256, 0, s>>>(part, poff, H, E, dWr);
+    count_launches(MT_max > 0 ? 2 : 1);
     return cudaGetLastError();
 }
 
@@ -454,6 +459,7 @@ cudaError_t launch_transpose_f32(const float* in, int rows, int cols, float* out
 {
     dim3 grid((cols + 31) / 32, (rows + 31) / 32);
     transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(in, rows, cols, out);
+    count_launches();
     return cudaGetLastError();
 }
 
@@ -463,6 +469,7 @@ cudaError_t launch_unpermute_reduce(const T* dXp, const T* dXs, const int* row_o
                                     int H, int k, T* dX, cudaStream_t s)
 {
     unpermute_reduce_kernel<T><<<T_, kRowThreads, 0, s>>>(dXp, dXs, row_of, topk, dz, WrT, H, k, dX);
+    count_launches();
     return cudaGetLastError();
 }
 

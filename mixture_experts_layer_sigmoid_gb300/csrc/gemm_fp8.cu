@@ -728,6 +728,7 @@ cudaError_t qrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s
     if (!PAIR) {
         const int grid = (int)(units < num_sms ? units : num_sms);
         gemm_fp8_kernel<EPI, SCHED, DUAL, false, B_MN><<<grid, kQThreads, C::SMEM, s>>>(mA0, mA1, mB0, mB1, d);
+        count_launches();
         return cudaGetLastError();
     }
     const int slots = qpair_slots<EPI, SCHED, DUAL, B_MN>();
@@ -745,6 +746,7 @@ cudaError_t qrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    count_launches();
     return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI, SCHED, DUAL, true, B_MN>, mA0, mA1, mB0, mB1, d);
 }
 

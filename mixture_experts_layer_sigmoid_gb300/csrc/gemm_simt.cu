@@ -206,6 +206,7 @@ cudaError_t launch_gemm_simt_f32(const GemmDesc& d, int max_m_tiles, cudaStream_
         gemm_simt_kernel<2><<<grid, 256, 0, s>>>(d);
     else
         gemm_simt_kernel<1><<<grid, 256, 0, s>>>(d);
+    count_launches();
     return cudaGetLastError();
 }
 

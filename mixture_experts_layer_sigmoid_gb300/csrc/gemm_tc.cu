@@ -698,6 +698,7 @@ cudaError_t run(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
         const int grid = (int)(units < num_sms ? units : num_sms);
         gemm_tc_kernel<BN, B_MN, DUAL, EPI, SCHED, false>
             <<<grid, kThreads, TcCfg<BN, false>::SMEM, s>>>(mA0, mA1, mB0, mB1, mO0, mO1, mO2, d);
+        count_launches();
         return cudaGetLastError();
     }
     const int slots = pair_slots<BN, B_MN, DUAL, EPI, SCHED>();
@@ -715,6 +716,7 @@ cudaError_t run(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    count_launches();
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, B_MN, DUAL, EPI, SCHED, true>, mA0, mA1, mB0,
                               mB1, mO0, mO1, mO2, d);
 }

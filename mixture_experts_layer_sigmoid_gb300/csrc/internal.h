@@ -102,6 +102,11 @@ cudaError_t gemm_tc_prepare(int device);
 cudaError_t launch_gemm_fp8(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s);
 cudaError_t gemm_fp8_prepare(int device);
 
+// Kernels enqueued by this host thread: every launcher adds the launches it
+// made, so a timed stage can report how many kernels it ran.
+extern thread_local unsigned long long t_kernel_launches;
+inline void count_launches(int n = 1) { t_kernel_launches += (unsigned long long)n; }
+
 // ------------------------------------------------------------- routing etc.
 template <typename T>
 cudaError_t launch_router(const T* x, const float* Wr, const float* b, int T_, int H, int E, int k,

@@ -419,6 +419,7 @@ cudaError_t run_quant(const QuantJob& j, cudaStream_t st)
     quant_tiles_kernel<QM, TM><<<(unsigned)grid, 256, 0, st>>>(j.in, j.rows_dev, j.rows_max, j.C,
                                                                j.rows_cap, j.q, j.s, j.qT, j.sT,
                                                                j.gather_slot, j.gather_k);
+    count_launches();
     return cudaGetLastError();
 }
 
@@ -429,6 +430,7 @@ cudaError_t launch_permute_quant(const __nv_bfloat16* x, const int* row_of, cons
                                  uint8_t* Xq, float* sX, cudaStream_t s)
 {
     permute_quant_kernel<<<T_ + E, 128, 0, s>>>(x, row_of, poff, counts, T_, H, k, Xp, Xq, sX);
+    count_launches();
     return cudaGetLastError();
 }
 

@@ -592,12 +592,14 @@ cudaError_t run_router_tiled(const T* x, const float* Wr, const float* b, int T_
     if (S == 1) {
         router_kernel<T, EPL, false><<<nblk, 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc,
                                                           hist, replay, status, nullptr);
+        count_launches();
         return cudaGetLastError();
     }
     router_kernel<T, EPL, true><<<dim3(nblk, S), 256, 0, s>>>(x, Wr, b, T_, H, E, k, score, topk, gates,
                                                               selsc, hist, replay, status, zpart);
     router_finish_kernel<EPL><<<nblk, 256, 0, s>>>(zpart, S, b, T_, E, k, score, topk, gates, selsc, hist,
                                                    replay, status);
+    count_launches(2);
     return cudaGetLastError();
 }
 
@@ -628,6 +630,7 @@ cudaError_t launch_router(const T* x, const float* Wr, const float* b, int T_, i
     else
         return run_router_tiled<T, 8>(x, Wr, b, T_, H, E, k, score, topk, gates, selsc, hist, s, replay, status,
                                       zpart, zpart_floats);
+    count_launches();
     return cudaGetLastError();
 }
 template cudaError_t launch_router<float>(const float*, const float*, const float*, int, int, int,
@@ -651,6 +654,7 @@ cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff
     if (pair_tab && !pair_off) return cudaErrorInvalidValue;
     scan_kernel<<<1, kScanParts * kMaxE, 0, s>>>(hist, nblk, E, counts, poff, blkbase, tile_tab, meta,
                                                  slot_of, pair_tab, pair_off, cap, kept);
+    count_launches();
     return cudaGetLastError();
 }
 
@@ -659,6 +663,7 @@ cudaError_t launch_index(const int* topk, const int* blkbase, int T_, int E, int
 {
     const int nblk = (T_ + kRouterTokens - 1) / kRouterTokens;
     index_kernel<<<nblk, 256, 0, s>>>(topk, blkbase, T_, E, k, row_of, slot_of);
+    count_launches();
     return cudaGetLastError();
 }
 

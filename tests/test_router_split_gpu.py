@@ -68,3 +68,21 @@ def test_route_static_matches_forward_when_the_router_splits_h(name):
     for key in ("topk_idx", "counts", "offsets", "row_of"):
         assert torch.equal(out[key], ref[key]), key
     assert torch.equal(out["gates"], ref["gates"])
+
+
+@pytest.mark.parametrize("E,router_kernels", [(8, 1), (128, 2)])
+def test_stage_times_count_every_kernel_of_a_stage(E, router_kernels):
+    """moe_stage_times reports kernel launches per stage, not calls: the router
+    weight gradient is two kernels (tile partial sums, then their per-expert
+    sums) and the router is two when it splits H (E > 32), one otherwise."""
+    w = mi.scaled(mi.WORKLOADS["qwen3_235b"], T=300, H=384, E=E, k=2, F=128)
+    g = {k: (None if v is None else v.cuda()) for k, v in mi.make_inputs(w).items()}
+    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, stage_timing=True)
+    layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"])
+    layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
+    torch.cuda.synchronize()
+    st = layer.stage_times()
+    assert st["router"][0] == router_kernels
+    assert st["router_wgrad"][0] == 2
+    for name in ("scan", "index", "permute", "fc1_swiglu", "fc2", "combine", "fc1_wgrad"):
+        assert st[name][0] == 1, name
