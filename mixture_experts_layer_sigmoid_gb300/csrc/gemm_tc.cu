@@ -38,7 +38,6 @@ constexpr int TBM = 128;       // MMA M
 constexpr int TBK = 64;        // K block (128 bytes of bf16)
 constexpr int STRIPE = 64 * 128;  // bytes of one 64-wide MN stripe of a 64-deep k block
 constexpr int kThreads = 192;
-constexpr int kSmemBudget = 200 * 1024;
 constexpr int kGroupN = 16;    // n tiles per raster group (row-scheduled GEMMs)
 
 constexpr int kSmemMax = 232448;               // 227 KB per CTA
@@ -145,21 +144,6 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float (&v
 #pragma unroll
         for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
         p[q] = u;
-    }
-}
-__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* src, float (&v)[32])
-{
-    const uint4* p = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 u = p[q];
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float2 f = __bfloat1622float2(h[i]);
-            v[8 * q + 2 * i] = f.x;
-            v[8 * q + 2 * i + 1] = f.y;
-        }
     }
 }
 __device__ __forceinline__ void zero32(float (&v)[32])
