@@ -151,13 +151,19 @@ __device__ __forceinline__ void zero32(float (&v)[32])
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = 0.f;
 }
-__device__ __forceinline__ void tmem_load32f(uint32_t taddr, float (&v)[32])
+// 64 consecutive TMEM columns of this warp's 32 lanes: both 32-column loads
+// in flight, one wait
+__device__ __forceinline__ void tmem_load64f(uint32_t taddr, float (&v0)[32], float (&v1)[32])
 {
-    uint32_t r[32];
-    ptx::tmem_ld32(taddr, r);
+    uint32_t r0[32], r1[32];
+    ptx::tmem_ld32(taddr, r0);
+    ptx::tmem_ld32(taddr + 32, r1);
     ptx::tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 32; ++i) {
+        v0[i] = __uint_as_float(r0[i]);
+        v1[i] = __uint_as_float(r1[i]);
+    }
 }
 
 // PAIR: launched as clusters of 2; the even CTA issues M=256 MMAs whose A
@@ -402,8 +408,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
 #pragma unroll 1
                 for (int u = 0; u < BN / 64; ++u) {
                     if (t.kblocks > 0) {
-                        tmem_load32f(taddr + u * 64, v0);
-                        tmem_load32f(taddr + u * 64 + 32, v1);
+                        tmem_load64f(taddr + u * 64, v0, v1);
                     } else {
                         zero32(v0);
                         zero32(v1);
@@ -423,10 +428,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
 #pragma unroll 1
                     for (int u = 0; u < NW / 64; ++u) {
                         float g0[32], g1[32], u0[32], u1[32], h0[32], h1[32];
-                        tmem_load32f(taddr + u * 64, g0);
-                        tmem_load32f(taddr + u * 64 + 32, g1);
-                        tmem_load32f(taddr + NW + u * 64, u0);
-                        tmem_load32f(taddr + NW + u * 64 + 32, u1);
+                        tmem_load64f(taddr + u * 64, g0, g1);
+                        tmem_load64f(taddr + NW + u * 64, u0, u1);
                         if (warp_in) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
@@ -451,8 +454,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
 #pragma unroll 1
                     for (int u = 0; u < NW / 64; ++u) {
                         float d0[32], d1[32], e0[32], e1[32];
-                        tmem_load32f(taddr + u * 64, d0);
-                        tmem_load32f(taddr + u * 64 + 32, d1);
+                        tmem_load64f(taddr + u * 64, d0, d1);
                         if (warp_in) {
                             const size_t o = (size_t)row * d.ldo + t.n * NW + u * 64;
                             const __nv_bfloat16* X0 = static_cast<const __nv_bfloat16*>(d.X0) + o;
@@ -524,8 +526,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                     // inside the tile's expert or (a pair's ghost half) all past it
 #pragma unroll 1
                     for (int u = 0; u < NW / 64; ++u) {
-                        tmem_load32f(taddr + u * 64, v0);
-                        tmem_load32f(taddr + u * 64 + 32, v1);
+                        tmem_load64f(taddr + u * 64, v0, v1);
                         if (warp_in) {
                             if (!valid) {
                                 zero32(v0);
