@@ -669,8 +669,8 @@ bool map8(CUtensorMap* m, const void* ptr, long long rows, long long cols, long 
 template <int EPI, int SCHED, int DUAL, bool B_MN>
 int qpair_slots()
 {
-    static int slots = -1;
-    if (slots < 0) {
+    // computed once (thread-safe initialisation of a function-local static)
+    static const int slots = [] {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -686,8 +686,8 @@ int qpair_slots()
         if (cudaOccupancyMaxActiveClusters(&n, gemm_fp8_kernel<EPI, SCHED, DUAL, true, B_MN>, &cfg) != cudaSuccess)
             n = 0;
         cudaGetLastError();
-        slots = n;
-    }
+        return n;
+    }();
     return slots;
 }
 

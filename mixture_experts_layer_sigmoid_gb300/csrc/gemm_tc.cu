@@ -614,8 +614,8 @@ cudaError_t set_attr()
 template <int BN, bool B_MN, int DUAL, int EPI, int SCHED>
 int pair_slots()
 {
-    static int slots = -1;
-    if (slots < 0) {
+    // computed once (thread-safe initialisation of a function-local static)
+    static const int slots = [] {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -632,8 +632,8 @@ int pair_slots()
             cudaSuccess)
             n = 0;
         cudaGetLastError();
-        slots = n;
-    }
+        return n;
+    }();
     return slots;
 }
 

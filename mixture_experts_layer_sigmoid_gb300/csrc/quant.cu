@@ -403,12 +403,16 @@ quant_tiles_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__
 template <int QM, int TM>
 cudaError_t run_quant(const QuantJob& j, cudaStream_t st)
 {
-    static int per_sm = 0;
-    if (per_sm == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_tiles_kernel<QM, TM>, 256, 0) !=
-                cudaSuccess || per_sm < 1)
-            per_sm = 1;
-    }
+    // computed once (thread-safe initialisation of a function-local static)
+    static const int per_sm = [] {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_tiles_kernel<QM, TM>, 256, 0) != cudaSuccess ||
+            n < 1) {
+            cudaGetLastError();
+            n = 1;
+        }
+        return n;
+    }();
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
