@@ -51,7 +51,7 @@ extern "C" {
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,          /* null pointer, bad size or enum     */
-    MOE_ERR_UNSUPPORTED = 2,          /* valid request this build cannot run */
+    MOE_ERR_UNSUPPORTED = 2,          /* valid request the library cannot run */
     MOE_ERR_MISALIGNED = 3,           /* a pointer is not 16-byte aligned    */
     MOE_ERR_WORKSPACE_TOO_SMALL = 4,  /* saved or workspace buffer too small */
     MOE_ERR_CUDA = 5,                 /* a CUDA runtime call failed          */
