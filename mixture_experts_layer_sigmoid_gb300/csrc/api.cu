@@ -23,7 +23,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct Layout {
     int T, R, Rp_max, MT_max, NB;
     // saved
-    size_t topk, gates, selsc, counts, kept, poff, meta, tiletab, pairtab, rowof, slotof;
+    size_t topk, gates, selsc, counts, kept, poff, meta, tiletab, pairtab, rowof, slotof, eorder;
     size_t Xp, A, U, Hh, Yp, As, Us, Hs, saved_bytes;
     // workspace
     size_t status, hist, blkbase, zpart, Ys, dYp, dA, dU, dXp, dz, WrT, wrpart, dAs, dUs, dXs, dgpart, ws_bytes;
@@ -51,6 +51,7 @@ Layout make_layout(const moe_config_t& c, int T)
     L.selsc = take(sizeof(float) * L.R);
     L.counts = take(sizeof(int) * c.E);
     L.kept = take(sizeof(int) * c.E);
+    L.eorder = take(sizeof(int) * c.E);   // experts, longest padded segment first
     L.poff = take(sizeof(int) * (c.E + 1));
     L.meta = take(sizeof(int) * 4);
     L.tiletab = take(sizeof(int) * L.MT_max);
@@ -371,7 +372,8 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
                               reinterpret_cast<float*>(ws + L.zpart), router_zpart_floats(T_, H, E)));
     MOE_STAGE(ST_SCAN, launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
                          reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab,
-                                   pairtab + L.MT_max, capacity(c, T_), kept));
+                                   pairtab + L.MT_max, capacity(c, T_), kept,
+                                   reinterpret_cast<int*>(sv + L.eorder)));
     MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
     MOE_STAGE(ST_PERMUTE, launch_permute<T>(x, rowof, poff, counts, T_, H, E, k, Xp, s));
 
@@ -454,6 +456,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     const int* meta = reinterpret_cast<const int*>(sv + L.meta);
     const int* tiletab = reinterpret_cast<const int*>(sv + L.tiletab);
     const int* pairtab = reinterpret_cast<const int*>(sv + L.pairtab);
+    const int* eorder = reinterpret_cast<const int*>(sv + L.eorder);
     const int* rowof = reinterpret_cast<const int*>(sv + L.rowof);
     const int* slotof = reinterpret_cast<const int*>(sv + L.slotof);
     const T* Xp = reinterpret_cast<const T*>(sv + L.Xp);
@@ -512,6 +515,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     d.A0 = Hh; d.lda = F; d.a_rows = L.Rp_max;
     d.B0 = dYp; d.ldb = H; d.b_rows = L.Rp_max;
     d.O0 = a->dW_down; d.ldo = H; d.o_estride = (long long)F * H; d.status = status;
+    d.expert_order = eorder;
     MOE_STAGE(ST_FC2_WGRAD, gemm(d));
     // fc1 dgrad: dXp = dA Wg^T + dU Wu^T
     memset(&d, 0, sizeof d);
@@ -533,6 +537,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     d.A0 = Xp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = dA; d.B1 = dU; d.ldb = F; d.b_rows = L.Rp_max;
     d.O0 = a->dW_gate; d.O1 = a->dW_up; d.ldo = F; d.o_estride = (long long)H * F; d.status = status;
+    d.expert_order = eorder;
     MOE_STAGE(ST_FC1_WGRAD, gemm(d));
 
     T* dXs = nullptr;
@@ -620,7 +625,8 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
                                           router_zpart_floats(T_, H, E)));
     MOE_STAGE(ST_SCAN, launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
                                    reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab,
-                                   pairtab + L.MT_max, capacity(c, T_), kept));
+                                   pairtab + L.MT_max, capacity(c, T_), kept,
+                                   reinterpret_cast<int*>(sv + L.eorder)));
     MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
     MOE_STAGE(ST_PERMUTE, launch_permute_quant(x, rowof, poff, counts, T_, H, E, k, nullptr, u8(sv, L.Xq),
                                                f32(sv, L.sX), s));

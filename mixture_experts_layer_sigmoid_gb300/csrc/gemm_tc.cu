@@ -116,12 +116,24 @@ __device__ __forceinline__ Tile decode_tile(const GemmDesc& d, int w, int num_m,
         t.row0 = t.m * TBM;
         t.kblocks = ((DUAL == DUAL_K) ? 2 * d.K : d.K) / TBK;
     } else {
+        // Experts longest first (the order the scan wrote), so the persistent
+        // units start the longest tiles together and stay in step over them;
+        // within an expert the smaller of the m and n tile counts runs fastest,
+        // so the units working at once cover all of that dimension against a
+        // few slices of the other and read each of those once.
         const int per = num_m * num_n;
-        t.e = w / per;
-        const int r = w % per;
-        const int mu = r % num_m;
+        const int eo = w / per;
+        t.e = d.expert_order ? d.expert_order[eo] : eo;
+        const int r = w - eo * per;
+        int mu;
+        if (num_n < num_m) {
+            t.n = r % num_n;
+            mu = r / num_n;
+        } else {
+            mu = r % num_m;
+            t.n = r / num_m;
+        }
         t.m = PAIR ? 2 * mu + rank : mu;
-        t.n = r / num_m;
         if (d.dense_rows > 0) {
             t.row0 = 0;
             t.kblocks = (d.dense_rows + TBK - 1) / TBK;

@@ -65,6 +65,7 @@ struct GemmDesc {
     const int* pair_tab;  // first tile of each pair of one expert's tiles (or null)
     const int* pair_off;  // E+1: first pair of each expert (with pair_tab)
     int prefer_pair;      // routed rows per expert are large enough for CTA pairs
+    const int* expert_order;  // weight gradients: experts in this order (null: 0..E-1)
     const int* poff;      // E+1 padded segment offsets
     const int* counts;    // E rows computed per expert (token counts, or the
                           // kept counts under capacity-limited dropping)
@@ -120,7 +121,7 @@ size_t router_zpart_floats(int T, int H, int E);
 cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff, int* blkbase,
                         int* tile_tab, int* meta, int* slot_of, cudaStream_t s,
                         int* pair_tab = nullptr, int* pair_off = nullptr, int cap = -1,
-                        int* kept = nullptr);
+                        int* kept = nullptr, int* eorder = nullptr);
 cudaError_t launch_index(const int* topk, const int* blkbase, int T_, int E, int k, int* row_of,
                          int* slot_of, cudaStream_t s);
 template <typename T>

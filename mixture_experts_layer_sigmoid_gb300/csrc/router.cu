@@ -469,9 +469,10 @@ __global__ void __launch_bounds__(kScanParts * kMaxE)
 scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ counts,
             int* __restrict__ poff, int* __restrict__ blkbase, int* __restrict__ tile_tab,
             int* __restrict__ meta, int* __restrict__ slot_of, int* __restrict__ pair_tab,
-            int* __restrict__ pair_off, int cap, int* __restrict__ kept)
+            int* __restrict__ pair_off, int cap, int* __restrict__ kept, int* __restrict__ eorder)
 {
     __shared__ int sc[kMaxE];
+    __shared__ int plen[kMaxE];
     __shared__ int part_sum[kScanParts][kMaxE];
     const int e = threadIdx.x % kMaxE, part = threadIdx.x / kMaxE;
     const int b0 = (int)((long long)nblk * part / kScanParts);
@@ -488,7 +489,7 @@ scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ cou
         c += part_sum[q][e];
     }
     const int pc = (c + kTileM - 1) / kTileM * kTileM;
-    if (part == 0) sc[e] = (e < E) ? pc : 0;
+    if (part == 0) sc[e] = plen[e] = (e < E) ? pc : 0;
     __syncthreads();
     // inclusive Hillis-Steele scan over kMaxE entries (part 0 threads)
     for (int off = 1; off < kMaxE; off <<= 1) {
@@ -541,6 +542,14 @@ scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ cou
             meta[2] = sc[kMaxE - 1];
             pair_off[E] = sc[kMaxE - 1];
         }
+    }
+    // experts by padded segment length, longest first (lower index first on
+    // equal lengths): the order the weight-gradient GEMMs take them in
+    if (eorder && part == 0 && e < E) {
+        const int len = plen[e];
+        int rank = 0;
+        for (int o = 0; o < E; ++o) rank += (plen[o] > len) || (plen[o] == len && o < e);
+        eorder[rank] = e;
     }
 }
 
@@ -649,11 +658,11 @@ size_t router_zpart_floats(int T, int H, int E)
 
 cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff, int* blkbase,
                         int* tile_tab, int* meta, int* slot_of, cudaStream_t s, int* pair_tab,
-                        int* pair_off, int cap, int* kept)
+                        int* pair_off, int cap, int* kept, int* eorder)
 {
     if (pair_tab && !pair_off) return cudaErrorInvalidValue;
     scan_kernel<<<1, kScanParts * kMaxE, 0, s>>>(hist, nblk, E, counts, poff, blkbase, tile_tab, meta,
-                                                 slot_of, pair_tab, pair_off, cap, kept);
+                                                 slot_of, pair_tab, pair_off, cap, kept, eorder);
     count_launches();
     return cudaGetLastError();
 }
