@@ -237,7 +237,10 @@ moe_status_t moe_stage_times(moe_plan_t plan, moe_stage_time_t* out, int capacit
  * T returns MOE_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any
- * stream capture. All calls share the array and it keeps the last call's
+ * stream capture. The address is kept for the life of the process: after a
+ * cudaDeviceReset (or any other teardown of the device's primary context)
+ * it is stale, and neither this entry point nor a plan created before the
+ * reset may be used again on that device. All calls share the array and it keeps the last call's
  * contents (every entry a call reads is written earlier in the same call);
  * calls whose work overlaps on the GPU -- from different streams or host
  * threads -- race on it and must be serialised by the caller.

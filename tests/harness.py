@@ -9,32 +9,40 @@ Training of Mixture-of-Experts Models with Megatron Core", §2):
     by less than 1e-5 relative. For those, any of the tied answers is correct:
     the GPU's choice is checked to be one of them and the oracle then uses
     that choice (router replay) so downstream tensors compare like with like;
-  - floating-point tensors: relative L2 error and max |error| / rms(reference)
-    within the bounds of the dtype (bf16: 1e-2 and 4e-2; fp32: 1e-4 and 1e-3);
-  - bf16 weight gradients (dW_gate, dW_up, dW_down, the shared expert's, and
-    the router's dWr, whose expert columns are sums over each expert's
-    tokens): relative L2 <= 1e-2 over the whole tensor AND over each
-    expert's block, and every element within the first-order forward-error
-    bound of the bf16/fp32 arithmetic that produces it (wgrad_bounds). The
-    max |error| / rms criterion is not used for them: each entry is a sum over
-    the expert's rows of products of bf16-rounded MMA operands, the entries
-    are heavy-tailed (max/rms up to ~15 with skewed routing), and rounding
-    alone then exceeds 4e-2 * rms at the largest entries for any bf16-operand
-    implementation.
+  - every floating-point tensor is reported with the pair (relative L2 error,
+    max |error| / rms(reference)) against the exact fp64 oracle, and y and dX
+    must meet the bounds of the dtype (bf16: 1e-2 and 4e-2; fp32: 1e-4 and
+    1e-3), as must every fp32-layer gradient;
+  - the bf16 router weight gradient dWr must meet relative L2 <= 1e-2, and
+    max |error| <= 4e-2 rms(ref) unless its bf16 emulation (gate gradients
+    from the stored bf16 expert outputs) itself exceeds that, in which case
+    the GPU may not exceed the emulation's by more than 10%; against the
+    emulation its relative L2 error must stay below 1e-3;
+  - bf16 expert weight gradients (dW_gate, dW_up, dW_down and the shared
+    expert's) must meet relative L2 <= 1e-2 over the whole tensor and over
+    each expert's block, and max |error| <= 4e-2 rms(ref) wherever bf16
+    storage of the layer's intermediates allows it. Where it does not --
+    tests/bf16_chain.py emulates that storage exactly, and on heavy-tailed
+    gradients its own max error exceeds 4e-2 rms (tests/test_bf16_chain.py)
+    -- the GPU's max error may not exceed the emulation's by more than 10%.
+    In addition at least 98% of the elements must be the bf16 rounding of the
+    emulated sum up to fp32 summation error, and every element within the
+    envelope of two moved terms (bf16_chain.rounding_check).
 """
 from __future__ import annotations
+
+import json
+import os
 
 import numpy as np
 import torch
 
 import moe_inputs as mi
 import oracle
+import bf16_chain as bc
 
 TIE_REL = 1e-5
 BOUNDS = {mi.BF16: (1e-2, 4e-2), mi.FP32: (1e-4, 1e-3)}
-WGRAD_BOUND_SLACK = 1.5      # headroom over the first-order bound (second-order terms)
-BF16_U = 2.0 ** -8           # bf16 unit roundoff
-FP32_U = 2.0 ** -24          # fp32 unit roundoff, per accumulated term (worst case)
 
 
 def to_np(t):
@@ -60,101 +68,19 @@ def assert_close(name, got, ref, dtype):
     return rl2, mr
 
 
-def _sig(a):
-    return 1.0 / (1.0 + np.exp(-a))
+MAX_FLOOR_MARGIN = 1.10      # GPU max error vs the bf16-storage floor, where that floor exceeds 4e-2
+DWR_EMU_REL_L2 = 1e-3        # dWr against its bf16 emulation (fp32 sums, rare one-ulp operand moves)
 
 
-def _expert_wgrad_bounds(X, Wg, Wu, Wd, g, dY, dYp_rounded=True):
-    """First-order worst-case |error| bounds of the bf16 path's weight
-    gradients of one expert (rows X with gates g and output gradients dY).
-
-    Each stage's error bound is carried forward: a, u (fp32 sums over H,
-    rounded to bf16), h = silu(a) u (bf16), dYp = g dY (bf16), dh = dYp Wd^T
-    (fp32 sum over H), dA = dh u silu'(a) and dU = dh silu(a) (bf16); then
-    the wgrad sums over the M rows (fp32) and the bf16 output rounding."""
-    U, V = BF16_U, FP32_U
-    M, H = X.shape
-    a = X @ Wg
-    uu = X @ Wu
-    s = _sig(a)
-    silu = a * s
-    d1 = s * (1 + a * (1 - s))
-    d2 = s * (1 - s) * (2 + a * (1 - 2 * s))
-    aX = np.abs(X)
-    a_err = U * np.abs(a) + H * V * (aX @ np.abs(Wg))
-    u_err = U * np.abs(uu) + H * V * (aX @ np.abs(Wu))
-    h = silu * uu
-    h_err = U * np.abs(h) + np.abs(d1 * uu) * a_err + np.abs(silu) * u_err
-    dYp = g * dY
-    dYp_err = U * np.abs(dYp) if dYp_rounded else np.zeros_like(dYp)
-    dh = dYp @ Wd.T
-    dh_err = (U + H * V) * (np.abs(dYp) @ np.abs(Wd).T)
-    dU = dh * silu
-    dU_err = U * np.abs(dU) + np.abs(silu) * dh_err + np.abs(dh * d1) * a_err
-    dA = dh * uu * d1
-    dA_err = (U * np.abs(dA) + np.abs(uu * d1) * dh_err + np.abs(dh * d1) * u_err
-              + np.abs(dh * uu * d2) * a_err)
-    mv = M * V
-    bd = (h_err.T @ np.abs(dYp) + np.abs(h).T @ dYp_err + mv * (np.abs(h).T @ np.abs(dYp))
-          + U * np.abs(h.T @ dYp))
-    bg = aX.T @ dA_err + mv * (aX.T @ np.abs(dA)) + U * np.abs(X.T @ dA)
-    bu = aX.T @ dU_err + mv * (aX.T @ np.abs(dU)) + U * np.abs(X.T @ dU)
-    # gate gradient dg = <dY, Yp> with Yp = h Wd (fp32 sum over F, bf16 output)
-    F = Wd.shape[0]
-    yp = h @ Wd
-    yp_err = h_err @ np.abs(Wd) + F * V * (np.abs(h) @ np.abs(Wd)) + U * np.abs(yp)
-    dg_err = (np.abs(dY) * yp_err).sum(1) + H * V * (np.abs(dY) * np.abs(yp)).sum(1)
-    return bg, bu, bd, dg_err
+def _floor_check(name, mr, floor):
+    assert mr <= max(4e-2, MAX_FLOOR_MARGIN * floor), (
+        f"{name}: max/rms {mr:.3e} above 4e-2 and above {MAX_FLOOR_MARGIN} x the bf16-storage "
+        f"floor {floor:.3e}")
 
 
-def wgrad_bounds(w, inp, r):
-    """Elementwise error bounds for every weight gradient of the bf16 path:
-    the experts' (stacked E×…), the shared expert's and the router's dWr.
-
-    dWr[h][e] = sum over e's tokens of x[t][h] dz[t][e]; dz is linear in the
-    gate gradients dg = <dY, Yp>, whose error comes from the bf16 expert
-    output Yp (h rounding, fp32 sum over F, bf16 output) and the fp32 sum
-    over H; the dz formula's coefficients carry it to dz."""
-    U, V = BF16_U, FP32_U
-    x, dY = to_np(inp["x"]), to_np(inp["dY"])
-    Wg, Wu, Wd = to_np(inp["Wg"]), to_np(inp["Wu"]), to_np(inp["Wd"])
-    out = {n: np.zeros_like(v) for n, v in (("dWg", Wg), ("dWu", Wu), ("dWd", Wd))}
-    dg_err = np.zeros_like(r["gates"])
-    for e in range(w.E):
-        toks, slots = np.nonzero(r["topk"] == e)
-        if len(toks) == 0:
-            continue
-        out["dWg"][e], out["dWu"][e], out["dWd"][e], dg_err[toks, slots] = _expert_wgrad_bounds(
-            x[toks], Wg[e], Wu[e], Wd[e], r["gates"][toks, slots][:, None], dY[toks])
-    if w.Fs:
-        out["dWsg"], out["dWsu"], out["dWsd"], _ = _expert_wgrad_bounds(
-            x, to_np(inp["Wsg"]), to_np(inp["Wsu"]), to_np(inp["Wsd"]), np.ones((w.T, 1)), dY,
-            dYp_rounded=False)
-    g = r["gates"]
-    spread = dg_err + (g * dg_err).sum(1, keepdims=True)
-    if w.score == mi.SOFTMAX:
-        dz_err = g * spread
-    else:
-        s = np.take_along_axis(r["scores"], r["topk"].astype(np.int64), 1)
-        dz_err = s * (1 - s) / s.sum(1, keepdims=True) * spread
-    # magnitude of dz itself, for the fp32 accumulation term of the router wgrad
-    dz_mag = np.zeros_like(g)
-    ref_dg = r.get("dg")
-    if ref_dg is not None:
-        spread_m = np.abs(ref_dg) + (g * np.abs(ref_dg)).sum(1, keepdims=True)
-        dz_mag = g * spread_m if w.score == mi.SOFTMAX else s * (1 - s) / s.sum(1, keepdims=True) * spread_m
-    dz_err_dense = np.zeros((w.T, w.E))
-    dz_mag_dense = np.zeros((w.T, w.E))
-    np.put_along_axis(dz_err_dense, r["topk"].astype(np.int64), dz_err, 1)
-    np.put_along_axis(dz_mag_dense, r["topk"].astype(np.int64), dz_mag, 1)
-    counts = np.bincount(r["topk"].ravel(), minlength=w.E)
-    ax = np.abs(x)
-    out["dWr"] = ax.T @ dz_err_dense + counts[None, :] * V * (ax.T @ dz_mag_dense)
-    return out
-
-
-def assert_wgrad(name, got, ref, bound):
-    """bf16 weight gradient: rel L2 (whole and per expert block) + elementwise bound."""
+def assert_wgrad(name, got, ref, wg):
+    """bf16 expert weight gradient against the fp64 oracle and the bf16
+    rounding-chain emulation wg (bf16_chain.WGrad)."""
     assert np.all(np.isfinite(got)), f"{name}: non-finite values"
     rl2, mr = rel_errors(got, ref)
     assert rl2 <= 1e-2, f"{name}: rel L2 {rl2:.3e} > 1e-2"
@@ -165,11 +91,32 @@ def assert_wgrad(name, got, ref, bound):
             assert np.all(g_ == 0), f"{name}[{e}]: expert without tokens has a nonzero gradient"
             continue
         assert np.linalg.norm(g_ - r_) / nr <= 1e-2, f"{name}[{e}]: block rel L2 > 1e-2"
-    ratio = np.abs(got - ref) / (WGRAD_BOUND_SLACK * bound + 1e-30)
-    worst = float(ratio.max())
-    assert worst <= 1.0, (f"{name}: |error| above the bf16 forward-error bound "
-                          f"(worst ratio {worst:.3f} at {np.unravel_index(ratio.argmax(), ratio.shape)})")
-    return rl2, mr, worst
+    _, floor = rel_errors(bc.rn_bf16(wg.S), ref)
+    _floor_check(name, mr, floor)
+    short = name.replace("dW_gate", "dWg").replace("dW_up", "dWu").replace("dW_down", "dWd") \
+        .replace("dWs_gate", "dWsg").replace("dWs_up", "dWsu").replace("dWs_down", "dWsd")
+    ratio, miss, worst = bc.rounding_check(got, wg, short)
+    assert miss <= bc.TIGHT_MISS_FRAC, (f"{name}: {100 * miss:.2f}% of the elements are not the bf16 "
+                                        f"rounding of the emulated sum (at most "
+                                        f"{100 * bc.TIGHT_MISS_FRAC}% may be)")
+    assert worst <= 1.0, f"{name}: an element is outside its deviation envelope (ratio {worst:.3f})"
+    exact = float(np.mean(got == bc.rn_bf16(wg.S)))
+    return dict(rel_l2=rl2, max_rms=mr, floor_max_rms=floor, exact_frac=exact,
+                tight_miss_frac=miss, worst_envelope_ratio=worst)
+
+
+def assert_dwr_bf16(got, ref, emu):
+    """Router weight gradient of the bf16 layer (fp32 output): the contract
+    pair against the oracle (max error against the bf16-storage floor where
+    that exceeds 4e-2), and relative L2 against its bf16 emulation."""
+    assert np.all(np.isfinite(got)), "dWr: non-finite values"
+    rl2, mr = rel_errors(got, ref)
+    assert rl2 <= 1e-2, f"dWr: rel L2 {rl2:.3e} > 1e-2"
+    _, floor = rel_errors(emu, ref)
+    _floor_check("dWr", mr, floor)
+    emu_l2 = float(np.linalg.norm(got - emu) / np.linalg.norm(ref)) if np.linalg.norm(ref) > 0 else 0.0
+    assert emu_l2 <= DWR_EMU_REL_L2, f"dWr: rel L2 against the bf16 emulation {emu_l2:.3e}"
+    return dict(rel_l2=rl2, max_rms=mr, floor_max_rms=floor, emu_rel_l2=emu_l2)
 
 
 def upload(inp, device="cuda"):
@@ -250,26 +197,51 @@ def oracle_layer(w, inp, r, backward=True):
 GRAD_NAMES = [("dX", "dX"), ("dWr", "dWr"), ("dW_gate", "dWg"), ("dW_up", "dWu"),
               ("dW_down", "dWd"), ("dWs_gate", "dWsg"), ("dWs_up", "dWsu"), ("dWs_down", "dWsd")]
 EXPERT_WGRADS = {"dWg", "dWu", "dWd", "dWsg", "dWsu", "dWsd"}
-COLUMN_BLOCKS = {"dWr"}      # one block per expert column
 
 
-def compare_all(w, inp, r, gpu, ref, backward=True):
-    """Compare every output and gradient with the rules of this module."""
+def compare_all(w, inp, r, gpu, ref, backward=True, fold=False):
+    """Compare every output and gradient with the rules of this module.
+    Returns, per tensor, the benchmark spec's pair (relative L2, max|err|/rms) against
+    the fp64 oracle (plus, for bf16 expert weight gradients, the bf16-storage
+    floor of the second and the rounding-consistency figures)."""
     report = {"y": assert_close("y", to_np(gpu["y"]), ref["y"], w.dtype)}
     if not backward:
         return report
-    bounds = wgrad_bounds(w, inp, dict(r, dg=ref.get("dg"))) if w.dtype == mi.BF16 else None
+    chain = dwr = None
+    if w.dtype == mi.BF16:
+        d = {k: to_np(inp[k]) for k in ("x", "Wg", "Wu", "Wd", "Wsg", "Wsu", "Wsd", "dY")}
+        chain = bc.layer_wgrads(d["x"], d["Wg"], d["Wu"], d["Wd"], r["topk"], r["gates"], d["dY"],
+                                d["Wsg"], d["Wsu"], d["Wsd"], fold=fold, keep=r.get("keep"))
+        sel = np.take_along_axis(r["scores"], r["topk"].astype(np.int64), 1)
+        dwr = bc.layer_dwr(d["x"], d["Wg"], d["Wu"], d["Wd"], r["topk"], r["gates"], sel, d["dY"],
+                           w.score, w.E, fold=fold, keep=r.get("keep"))[0]
     for gname, oname in GRAD_NAMES:
         if oname not in ref:
             continue
         got = to_np(gpu[gname])
-        if bounds is not None and oname in EXPERT_WGRADS:
-            report[gname] = assert_wgrad(gname, got, ref[oname], bounds[oname])
-        elif bounds is not None and oname in COLUMN_BLOCKS:
-            report[gname] = assert_wgrad(gname, got.T, ref[oname].T, bounds[oname].T)
+        if chain is not None and oname in EXPERT_WGRADS:
+            report[gname] = assert_wgrad(gname, got, ref[oname], chain[oname])
+        elif dwr is not None and oname == "dWr":
+            report[gname] = assert_dwr_bf16(got, ref[oname], dwr)
         else:
             report[gname] = assert_close(gname, got, ref[oname], w.dtype)
     return report
+
+
+def write_report(case, report):
+    """Append one case's parity figures to the JSON-lines file named by the
+    MOE_PARITY_REPORT environment variable (no-op when it is unset)."""
+    path = os.environ.get("MOE_PARITY_REPORT")
+    if not path:
+        return
+    def conv(v):
+        if isinstance(v, dict):
+            return {k: conv(x) for k, x in v.items()}
+        if isinstance(v, (tuple, list)):
+            return [conv(x) for x in v]
+        return float(v) if isinstance(v, (float, np.floating)) else v
+    with open(path, "a") as f:
+        f.write(json.dumps({"case": case, **conv(report)}) + "\n")
 
 
 def full_parity(w: mi.Workload, backward=True, fold=False, capacity_factor=0.0):
@@ -281,6 +253,10 @@ def full_parity(w: mi.Workload, backward=True, fold=False, capacity_factor=0.0):
         r["keep"] = oracle.capacity_keep(r["topk"], w.E, C)
     np.testing.assert_allclose(gpu["gates"].numpy(), r["gates"], rtol=1e-4, atol=1e-6)
     ref = oracle_layer(w, inp, r, backward)
-    report = compare_all(w, inp, r, gpu, ref, backward)
+    report = compare_all(w, inp, r, gpu, ref, backward, fold=fold)
     report["near_ties"] = nties
+    dt = {mi.FP32: "fp32", mi.BF16: "bf16", mi.FP8_BLOCK: "fp8"}[w.dtype]
+    write_report(f"{w.name} T{w.T} H{w.H} E{w.E} k{w.k} F{w.F} Fs{w.Fs} {dt}"
+                 + (" fold" if fold else "") + (f" cf{capacity_factor}" if capacity_factor else ""),
+                 report)
     return report, gpu

@@ -3,10 +3,10 @@
 The quantiser the layer uses must give the oracle's E4M3 bytes and fp32
 scales bit for bit on the same bf16 input, in all four block layouts. The
 whole layer (forward and backward) must match the oracle's FP8 layer within
-the FP8 bounds: relative L2 <= 4e-2, and max |error| <= 1.5e-1 * rms(ref)
-for outputs and activation gradients; weight gradients within 4e-2 relative
-L2 over the tensor and over every expert's block ("Scalable Training of
-Mixture-of-Experts Models with Megatron Core", §5, blockwise FP8)."""
+the FP8 bounds on every output and gradient: relative L2 <= 4e-2 and
+max |error| <= 1.5e-1 * rms(ref); weight gradients also within 4e-2 relative
+L2 over every expert's block ("Scalable Training of Mixture-of-Experts
+Models with Megatron Core", §5, blockwise FP8)."""
 import numpy as np
 import pytest
 import torch
@@ -14,7 +14,7 @@ import torch
 import moe_inputs as mi
 import oracle
 import mixture_experts_layer_sigmoid_gb300 as moe
-from harness import TIE_REL, rel_errors, to_np, upload
+from harness import TIE_REL, rel_errors, to_np, upload, write_report
 
 pytestmark = pytest.mark.gpu
 
@@ -126,7 +126,7 @@ def fp8_layer_parity(w, fold=False):
         want = ref[oname]
         rl2, mr = rel_errors(got, want)
         rep[gname] = (rl2, mr)
-        assert rl2 <= 4e-2, (gname, rl2)
+        assert rl2 <= 4e-2 and mr <= 1.5e-1, (gname, rl2, mr)
         blocks = zip(got.T, want.T) if gname == "dWr" else zip(got, want)
         for gb, wb in blocks:
             nw = np.linalg.norm(wb)
@@ -134,4 +134,5 @@ def fp8_layer_parity(w, fold=False):
                 assert np.all(gb == 0)
             else:
                 assert np.linalg.norm(gb - wb) / nw <= 4e-2, gname
+    write_report(f"{w.name} T{w.T} H{w.H} E{w.E} k{w.k} F{w.F} fp8" + (" fold" if fold else ""), rep)
     return rep

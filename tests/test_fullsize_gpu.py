@@ -7,8 +7,11 @@ The whole layer runs on the GPU; the fp64 oracle then checks
   - y and dX rows of sampled tokens (first, last, hottest-expert and tied
     tokens), computed one by one by the oracle's per-token form,
   - sampled entries of the expert weight gradients (hottest and coldest
-    non-empty expert, and the shared expert), each within the forward-error
-    bound of the bf16 arithmetic.
+    non-empty expert, and the shared expert): all but at most one must be
+    the bf16 rounding of the bf16 rounding-chain emulation's sum
+    (tests/bf16_chain.py) up to fp32 summation error, and every one within
+    its deviation envelope; the pair (rel L2, max|err| / rms) against the
+    exact fp64 entries is reported, with rms taken over the whole GPU tensor.
 dWr needs every routed token's expert outputs, so at these sizes it is
 covered by the mid-size tests only.
 """
@@ -18,7 +21,8 @@ import torch
 
 import moe_inputs as mi
 import oracle
-from harness import TIE_REL, WGRAD_BOUND_SLACK, _expert_wgrad_bounds, rel_errors, to_np
+import bf16_chain as bc
+from harness import TIE_REL, rel_errors, to_np, write_report
 
 pytestmark = pytest.mark.gpu
 
@@ -105,31 +109,47 @@ def test_full_size_layer(name):
     ref = oracle.dw_entries(x, dY, W, r["topk"], r["gates"], ents)
     gpu_name = dict(dWg="dW_gate", dWu="dW_up", dWd="dW_down", dWsg="dWs_gate", dWsu="dWs_up",
                     dWsd="dWs_down")
+    rms = {n: float(gr[m].float().pow(2).mean().sqrt().item()) for n, m in gpu_name.items() if m in gr}
+    errs = {}
+    worst, misses = 0.0, 0
     for (n, e, i, j), want in zip(ents, ref):
         t = gr[gpu_name[n]]
         got = float((t[i, j] if n.startswith("dWs") else t[e, i, j]).item())
         f = i if n in ("dWd", "dWsd") else j
-        if n.startswith("dWs"):
+        shared = n.startswith("dWs")
+        if shared:
             rows = np.arange(w.T)
-            gate = np.ones((w.T, 1))
+            gate = np.ones(w.T)
             Wg_, Wu_, Wd_ = (to_np(g[m]) for m in ("Wsg", "Wsu", "Wsd"))
         else:
             rows, slots = np.nonzero(r["topk"] == e)
-            gate = r["gates"][rows, slots][:, None]
+            gate = r["gates"][rows, slots]
             Wg_, Wu_, Wd_ = to_np(g["Wg"][e]), to_np(g["Wu"][e]), to_np(g["Wd"][e])
-        bg, bu, bd, _ = _expert_wgrad_bounds(x[rows], Wg_[:, [f]], Wu_[:, [f]], Wd_[[f], :], gate,
-                                             dY[rows], dYp_rounded=not n.startswith("dWs"))
-        bound = {"dWg": bg, "dWu": bu, "dWd": bd, "dWsg": bg, "dWsu": bu, "dWsd": bd}[n]
-        bnd = bound[0, j] if n in ("dWd", "dWsd") else bound[i, 0]
-        assert abs(got - want) <= WGRAD_BOUND_SLACK * bnd, (n, e, i, j, got, want, bnd)
+        c = bc.expert_chain(x[rows], Wg_[:, [f]], Wu_[:, [f]], Wd_[[f], :], gate, dY[rows],
+                            scale_dy=not shared)
+        key = n.replace("dWs", "dW")
+        at = (0, j) if key == "dWd" else (i, 0)
+        tight, env = bc.entry_check(got, c, key, *at)
+        misses += tight > 1.0
+        worst = max(worst, env)
+        assert env <= 1.0, (n, e, i, j, got, want, float(c[key][at]))
+        errs.setdefault(n, []).append((got, want))
+    # a sample of 18-27 entries: at most one may miss the tight rounding bound
+    assert misses <= 1, f"{misses} sampled entries are not the bf16 rounding of the emulated sum"
+    report = {"tight_misses": int(misses), "worst_envelope_ratio": float(worst)}
+    for n, pairs in errs.items():
+        got_, want_ = np.array(pairs).T
+        report[gpu_name[n] + "_sampled"] = (float(np.linalg.norm(got_ - want_) / np.linalg.norm(want_)),
+                                            float(np.abs(got_ - want_).max() / rms[n]))
+    print(name, report)
+    write_report(f"{name} full size, sampled weight-gradient entries", report)
 
 
 def test_full_size_fp8_layer():
     """Qwen3-shaped layer in blockwise FP8: routing bit-exact, the layer's
     weight quantiser bit-exact against the oracle on sampled experts, and
-    sampled output rows within the E4M3 deviation scale of the exact layer
-    (an output passes through up to ~6 successive E4M3 roundings of 3.6% rms
-    each: at most 9% relative, as pinned on the oracle's FP8 layer)."""
+    sampled y and dX rows within the FP8 bounds (relative L2 <= 4e-2,
+    max|err| <= 1.5e-1 rms) of the oracle's FP8 layer."""
     import mixture_experts_layer_sigmoid_gb300 as moe
     w = mi.WORKLOADS["qwen3_235b_fp8"]
     g = mi.make_inputs(w, "cuda")
@@ -164,14 +184,23 @@ def test_full_size_fp8_layer():
         oc, os_ = oracle.fp8_quantize(W.float().cpu().numpy(), oracle.FP8_TILES)
         assert np.array_equal(codes.cpu().numpy(), oc) and np.array_equal(sc.cpu().numpy(), os_)
         assert np.array_equal(codes_t.cpu().numpy(), oc.T)
-    # sampled rows against the exact layer
-    toks = np.array(sorted({0, w.T - 1, int(np.nonzero((r["topk"] == hot).any(1))[0][0]), 777}))
+    # sampled rows against the oracle's FP8 layer run on those tokens alone:
+    # y and dX of a token depend only on its own row (1x128 activation blocks,
+    # 128x128 weight blocks of its experts), and dz only on its selected
+    # experts' scores, so the layer restricted to the sampled tokens and the
+    # experts they select (renumbered) gives their rows exactly
+    toks = np.array(sorted({0, w.T - 1, int(np.nonzero((r["topk"] == hot).any(1))[0][0])}))
     need = sorted(set(r["topk"][toks].ravel().tolist()))
-    Wx = oracle.ExpertWeights(w.E, {e: _bits(g["Wg"][e]) for e in need},
-                              {e: _bits(g["Wu"][e]) for e in need},
-                              {e: _bits(g["Wd"][e]) for e in need})
-    tr = oracle.token_rows(x[toks], dY[toks], Wr, Wx, r["topk"][toks], r["gates"][toks],
-                           r["scores"][toks], w.score)
+    renum = np.full(w.E, -1, np.int32)
+    renum[need] = np.arange(len(need), dtype=np.int32)
+    topk_s = renum[r["topk"][toks]]
+    stack = lambda n: np.stack([to_np(g[n][e]) for e in need])
+    q = oracle.layer_fp8(x[toks], Wr[:, need], stack("Wg"), stack("Wu"), stack("Wd"), topk_s,
+                         r["gates"][toks], r["scores"][toks][:, need], w.score, dY[toks])
+    report = {}
     for nm, got in (("y", to_np(y)[toks]), ("dX", to_np(gr["dX"])[toks])):
-        rl2, _ = rel_errors(got, tr[nm])
-        assert 0.0 < rl2 < 0.09, (nm, rl2)
+        rl2, mr = rel_errors(got, q[nm])
+        report[nm + "_rows"] = (rl2, mr)
+        assert rl2 <= 4e-2 and mr <= 1.5e-1, (nm, rl2, mr)
+    print("qwen3_235b_fp8", report)
+    write_report("qwen3_235b_fp8 full size, sampled token rows", report)

@@ -175,3 +175,73 @@ def test_fp8_single_expert_matches_independent_fp8_swiglu():
         close = np.isclose(q[n], v, rtol=1e-9, atol=1e-9 * np.abs(v).max())
         assert close.mean() > 0.999, (n, close.mean())
         assert np.linalg.norm(q[n] - v) / np.linalg.norm(v) < 1e-3, n
+
+
+def _q_cols_segment(X):
+    """Per column over 128-row blocks counted from the segment's first row
+    (the last block may be shorter)."""
+    out = np.empty_like(X)
+    for r in range(0, X.shape[0], 128):
+        for c in range(X.shape[1]):
+            v = X[r:r + 128, c]
+            a = np.float32(np.abs(v.astype(np.float32)).max())
+            out[r:r + 128, c] = _cast(v, np.float32(a / np.float32(448)) if a else np.float32(1))
+    return out
+
+
+@pytest.mark.parametrize("fold", [False, True])
+def test_fp8_multi_expert_matches_independent_fp8_swiglu(fold):
+    """Several experts with ragged segments (more than one 128-token block,
+    the last one partial): the weight-gradient operands are quantised per
+    expert segment, in 128-token blocks counted from the segment's first row.
+    An independent FP8 layer (torch's E4M3 codec, rows gathered per expert
+    with numpy) must give the oracle's y and weight gradients."""
+    T, H, E, k, F = 333, 256, 3, 2, 256
+    p = _layer(T=T, H=H, E=E, k=k, F=F, Fs=0, score=oracle.SOFTMAX, seed=21)
+    b = np.array([0.8, 0.0, -0.9])                    # uneven loads: all segments ragged
+    r = oracle.route(p["x"], p["Wr"], b, k, oracle.SOFTMAX)
+    counts = np.bincount(r["topk"].ravel(), minlength=E)
+    assert np.all(counts > 128) and np.all(counts % 128 != 0) and len(set(counts)) == E
+    q = oracle.layer_fp8(p["x"], p["Wr"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"],
+                         r["scores"], oracle.SOFTMAX, p["dY"], fold=fold)
+    bf = lambda v: torch.from_numpy(np.ascontiguousarray(v)).to(torch.bfloat16).double().numpy()
+    y = np.zeros((T, H))
+    ref = {n: np.zeros_like(p[w]) for n, w in (("dWg", "Wg"), ("dWu", "Wu"), ("dWd", "Wd"))}
+    for e in range(E):
+        toks, slots = np.nonzero(r["topk"] == e)          # the expert's rows, token order
+        g = r["gates"][toks, slots][:, None]
+        X = p["x"][toks]
+        Wg, Wu, Wd = _q_tiles(p["Wg"][e]), _q_tiles(p["Wu"][e]), _q_tiles(p["Wd"][e])
+        xq = _q_rows(X)
+        a32, u32 = xq @ Wg, xq @ Wu
+        h32 = a32 / (1 + np.exp(-a32)) * u32
+        h = bf(g * h32) if fold else bf(h32)
+        a, u = bf(a32), bf(u32)
+        Yp = bf(_q_rows(h) @ Wd)
+        y[toks] += Yp if fold else g * Yp
+        dYp = bf(p["dY"][toks]) if fold else bf(g * p["dY"][toks])   # stored bf16
+        dh = _q_rows(dYp) @ Wd.T
+        sg = 1 / (1 + np.exp(-a))
+        if fold:
+            hr = a * sg * u
+            dh = g * dh
+            h = bf(g * hr)
+        dA = bf(dh * u * sg * (1 + a * (1 - sg)))
+        dU = bf(dh * a * sg)
+        ref["dWd"][e] = _q_cols_segment(h).T @ _q_tiles(dYp)
+        ref["dWg"][e] = _q_cols_segment(X).T @ _q_tiles(dA)
+        ref["dWu"][e] = _q_cols_segment(X).T @ _q_tiles(dU)
+    ref["y"] = y
+    for n, v in ref.items():
+        close = np.isclose(q[n], v, rtol=1e-9, atol=1e-9 * np.abs(v).max())
+        assert close.mean() > 0.999, (n, close.mean())
+        assert np.linalg.norm(q[n] - v) / np.linalg.norm(v) < 1e-3, n
+    # a block origin at a multiple of 128 of the whole permuted buffer, instead
+    # of each segment's first row, gives visibly different weight gradients
+    e = 1
+    toks, slots = np.nonzero(r["topk"] == e)
+    off = counts[0]                                   # segment start in an unpadded buffer
+    X = p["x"][toks]
+    shifted = np.concatenate([np.zeros(((off % 128), H)), X])
+    wrong = _q_cols_segment(shifted)[off % 128:]
+    assert np.linalg.norm(wrong - _q_cols_segment(X)) > 1e-3 * np.linalg.norm(X)

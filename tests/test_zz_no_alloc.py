@@ -27,11 +27,14 @@ def _p(t):
     return None if t is None else t.data_ptr()
 
 
-def test_route_static_matches_forward_on_two_calls_in_a_row():
+@pytest.mark.parametrize("dtype", [mi.FP32, mi.BF16, mi.FP8_BLOCK])
+def test_route_static_matches_forward_on_two_calls_in_a_row(dtype):
+    """fp32 activations route through the fp32 router; the bf16 and the
+    blockwise-FP8 layers both route from bf16 activations."""
     lib = moe.load_library()
-    base = mi.scaled(mi.WORKLOADS["qwen3_235b"], T=520, H=384, E=32, F=384)
+    base = mi.scaled(mi.WORKLOADS["qwen3_235b"], T=520, H=384, E=32, F=384, dtype=dtype)
     cases = [base, mi.scaled(base, T=333, seed=base.seed + 7)]
-    layer = moe.MoELayer(base.H, base.E, base.F, base.k, base.T, score=base.score)
+    layer = moe.MoELayer(base.H, base.E, base.F, base.k, base.T, score=base.score, dtype=dtype)
     stream = torch.cuda.current_stream().cuda_stream
     for w in cases:
         g = {k: (None if v is None else v.cuda()) for k, v in mi.make_inputs(w, with_grad_out=False).items()}
