@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 typedef enum {
     MOE_OK = 0,
@@ -150,6 +150,12 @@ typedef struct {
                               over the sum of their scores). Indices outside
                               [0, E) are clamped and reported as
                               MOE_ERR_INVALID_ARG in the status word. */
+    const void*  weight_cache; /* optional in (MOE_FP8_BLOCK plans): expert
+                              weights quantised by moe_quantize_weights. When
+                              given, W_gate, W_up and W_down are not read (they
+                              may be NULL) and the call quantises no weights;
+                              the matching moe_backward must be given the same
+                              cache. Other dtypes: must be NULL. */
 } moe_fwd_args_t;
 
 /* Backward arguments. Gradients are overwritten (not accumulated); experts
@@ -172,6 +178,10 @@ typedef struct {
     void*        dWs_gate; /* out, H×Fs act (NULL iff Fs == 0)                */
     void*        dWs_up;
     void*        dWs_down;
+    const void*  weight_cache; /* MOE_FP8_BLOCK: the cache given to the
+                              forward (W_gate, W_up, W_down then unread), or
+                              NULL when the forward quantised the bf16
+                              weights itself. Other dtypes: NULL. */
 } moe_bwd_args_t;
 
 /* Validate `cfg` for `device` and build a plan (host memory only).
@@ -271,6 +281,32 @@ moe_status_t moe_route_static(moe_plan_t plan, int T, const void* x, const float
 enum { MOE_Q_ROWS = 0, MOE_Q_TILES = 1, MOE_Q_COLS_T = 2, MOE_Q_TILES_T = 3 };
 moe_status_t moe_fp8_quantize(int rows, int cols, int mode, const void* in, uint8_t* codes,
                               float* scales, uint8_t* codes_t, float* scales_t, moe_stream_t stream);
+
+/* Quantised expert weights for MOE_FP8_BLOCK plans ("Scalable Training of
+ * Mixture-of-Experts Models with Megatron Core", §5 Kernel and shape
+ * optimization: grouped quantization of the experts' weights, done once
+ * and kept). A caller that keeps E4M3 weights between steps -- they change
+ * once per optimizer step, while a step may run several forward/backward
+ * passes -- quantises them once into a caller-owned device buffer, the
+ * weight cache, and passes it as weight_cache to moe_forward and
+ * moe_backward, which then skip their own weight quantisation.
+ *
+ * moe_weight_cache_size: bytes of the cache for this plan (0 for plans
+ * that are not MOE_FP8_BLOCK). Errors: INVALID_ARG.
+ *
+ * moe_quantize_weights: quantise W_gate, W_up (E x H x F bf16) and W_down
+ * (E x F x H bf16) into `cache` (cache_bytes >= the size above), enqueued
+ * on `stream`. The cache holds each matrix's E4M3 codes in its own layout
+ * and one fp32 scale per 128x128 block (amax / 448, 1 for an all-zero
+ * block), exactly the codes the layer would produce inside moe_forward;
+ * its internal layout is private to the library version. 16-byte aligned
+ * device pointers, owned by the caller.
+ * Errors: INVALID_ARG (null), UNSUPPORTED (plan not MOE_FP8_BLOCK),
+ * MISALIGNED, WORKSPACE_TOO_SMALL (cache_bytes), CUDA. */
+moe_status_t moe_weight_cache_size(moe_plan_t plan, size_t* bytes);
+moe_status_t moe_quantize_weights(moe_plan_t plan, const void* W_gate, const void* W_up,
+                                  const void* W_down, void* cache, size_t cache_bytes,
+                                  moe_stream_t stream);
 
 /* Failure-detection check. Every pipelined kernel of the library waits on
  * its shared-memory mbarriers with a bounded wait (2 s); when a wait runs out

@@ -35,7 +35,7 @@ MOE_FLAG_FOLD_GATES = 2
 EXPORTS = ("moe_plan_create", "moe_plan_destroy", "moe_workspace_size", "moe_forward",
            "moe_backward", "moe_read_status", "moe_status_string", "moe_stage_times",
            "moe_route_static", "moe_fp8_quantize", "moe_diag_wait_timeout", "moe_update_bias",
-           "moe_abi_version")
+           "moe_weight_cache_size", "moe_quantize_weights", "moe_abi_version")
 MOE_Q_ROWS, MOE_Q_TILES, MOE_Q_COLS_T, MOE_Q_TILES_T = 0, 1, 2, 3
 
 
@@ -51,13 +51,13 @@ _vp = ctypes.c_void_p
 class moe_fwd_args_t(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("x", "Wr", "b", "W_gate", "W_up", "W_down", "Ws_gate", "Ws_up",
                                    "Ws_down", "y", "topk_idx", "gates", "counts", "offsets",
-                                   "row_of", "replay_topk")]
+                                   "row_of", "replay_topk", "weight_cache")]
 
 
 class moe_bwd_args_t(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("dY", "x", "Wr", "W_gate", "W_up", "W_down", "Ws_gate", "Ws_up",
                                    "Ws_down", "dX", "dWr", "dW_gate", "dW_up", "dW_down", "dWs_gate",
-                                   "dWs_up", "dWs_down")]
+                                   "dWs_up", "dWs_down", "weight_cache")]
 
 
 class moe_stage_time_t(ctypes.Structure):
@@ -98,6 +98,8 @@ def load_library() -> ctypes.CDLL:
                                          _vp, _vp]
         lib.moe_diag_wait_timeout.argtypes = [_vp, _vp]
         lib.moe_update_bias.argtypes = [ctypes.c_int, _vp, ctypes.c_float, _vp, _vp]
+        lib.moe_weight_cache_size.argtypes = [_vp, P(ctypes.c_size_t)]
+        lib.moe_quantize_weights.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
         lib.moe_abi_version.argtypes = []
         for n in EXPORTS:
             if n not in ("moe_status_string", "moe_abi_version"):
@@ -173,6 +175,21 @@ def moe_fp8_quantize(rows: int, cols: int, mode: int, x: int, codes: int, scales
         raise MoEError(st, "moe_fp8_quantize")
 
 
+def moe_weight_cache_size(plan: int) -> int:
+    n = ctypes.c_size_t()
+    st = load_library().moe_weight_cache_size(plan, ctypes.byref(n))
+    if st != MOE_OK:
+        raise MoEError(st, "moe_weight_cache_size")
+    return n.value
+
+
+def moe_quantize_weights(plan: int, W_gate: int, W_up: int, W_down: int, cache: int, cache_bytes: int,
+                         stream: int) -> None:
+    st = load_library().moe_quantize_weights(plan, W_gate, W_up, W_down, cache, cache_bytes, stream)
+    if st != MOE_OK:
+        raise MoEError(st, "moe_quantize_weights")
+
+
 def moe_update_bias(E: int, counts: int, rate: float, b: int, stream: int) -> None:
     """Auxiliary-loss-free bias update: b_e += rate * sign(mean count - count_e)."""
     st = load_library().moe_update_bias(E, counts, rate, b, stream)
@@ -226,10 +243,23 @@ class MoELayer:
     def stream(self) -> int:
         return self.torch.cuda.current_stream(self.device).cuda_stream
 
+    def quantize_weights(self, W_gate, W_up, W_down, cache=None):
+        """FP8 plans: the weight cache (a uint8 device tensor) holding the
+        E4M3 codes and scales of the expert weights; pass it as weight_cache
+        to forward and backward."""
+        t = self.torch
+        n = moe_weight_cache_size(self.plan)
+        if cache is None:
+            cache = t.empty(n, dtype=t.uint8, device=self.device)
+        moe_quantize_weights(self.plan, W_gate.data_ptr(), W_up.data_ptr(), W_down.data_ptr(),
+                             cache.data_ptr(), cache.numel(), self.stream())
+        return cache
+
     def forward(self, x, Wr, b, W_gate, W_up, W_down, Ws_gate=None, Ws_up=None, Ws_down=None,
-                routing: bool = False, y=None, replay_topk=None):
+                routing: bool = False, y=None, replay_topk=None, weight_cache=None):
         """replay_topk: optional T×k int32 device tensor of experts to route to
-        (router replay) instead of the top-k selection."""
+        (router replay) instead of the top-k selection. weight_cache: FP8
+        plans, from quantize_weights (W_gate, W_up, W_down may then be None)."""
         t = self.torch
         T = x.shape[0]
         saved, ws = self.buffers(T)
@@ -247,19 +277,23 @@ class MoELayer:
                            Ws_down=_ptr(Ws_down), y=_ptr(y), topk_idx=_ptr(out.get("topk_idx")),
                            gates=_ptr(out.get("gates")), counts=_ptr(out.get("counts")),
                            offsets=_ptr(out.get("offsets")), row_of=_ptr(out.get("row_of")),
-                           replay_topk=_ptr(replay_topk))
+                           replay_topk=_ptr(replay_topk), weight_cache=_ptr(weight_cache))
         moe_forward(self.plan, T, a, saved.data_ptr(), saved.numel(), ws.data_ptr(), ws.numel(),
                     self.stream())
         return (y, out) if routing else y
 
     def backward(self, dY, x, Wr, W_gate, W_up, W_down, Ws_gate=None, Ws_up=None, Ws_down=None,
-                 grads=None):
+                 grads=None, weight_cache=None, like=None):
+        """weight_cache: the cache given to the forward (FP8 plans). like:
+        (W_gate, W_up, W_down)-shaped templates for the gradients when the
+        weights themselves are not passed."""
         t = self.torch
         T = x.shape[0]
         saved, ws = self.buffers(T)
         if grads is None:
-            grads = dict(dX=t.empty_like(x), dWr=t.empty_like(Wr), dW_gate=t.empty_like(W_gate),
-                         dW_up=t.empty_like(W_up), dW_down=t.empty_like(W_down))
+            lg, lu, ld = like if like is not None else (W_gate, W_up, W_down)
+            grads = dict(dX=t.empty_like(x), dWr=t.empty_like(Wr), dW_gate=t.empty_like(lg),
+                         dW_up=t.empty_like(lu), dW_down=t.empty_like(ld))
             if Ws_gate is not None:
                 grads.update(dWs_gate=t.empty_like(Ws_gate), dWs_up=t.empty_like(Ws_up),
                              dWs_down=t.empty_like(Ws_down))
@@ -269,7 +303,8 @@ class MoELayer:
                            Ws_down=_ptr(Ws_down), dX=_ptr(g["dX"]), dWr=_ptr(g["dWr"]),
                            dW_gate=_ptr(g["dW_gate"]), dW_up=_ptr(g["dW_up"]),
                            dW_down=_ptr(g["dW_down"]), dWs_gate=_ptr(g.get("dWs_gate")),
-                           dWs_up=_ptr(g.get("dWs_up")), dWs_down=_ptr(g.get("dWs_down")))
+                           dWs_up=_ptr(g.get("dWs_up")), dWs_down=_ptr(g.get("dWs_down")),
+                           weight_cache=_ptr(weight_cache))
         moe_backward(self.plan, T, a, saved.data_ptr(), saved.numel(), ws.data_ptr(), ws.numel(),
                      self.stream())
         return grads

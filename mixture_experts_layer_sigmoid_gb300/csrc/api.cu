@@ -115,6 +115,32 @@ Layout make_layout(const moe_config_t& c, int T)
     return L;
 }
 
+// Quantised expert weights of an FP8 plan, in a caller-owned buffer
+// (moe_quantize_weights): E4M3 codes of W_gate, W_up (E x H x F) and W_down
+// (E x F x H) in their natural layouts, each followed by its 128x128-block
+// fp32 scales [E][rows/128][cols/128].
+struct WeightCache {
+    size_t WgQ, sWg, WuQ, sWu, WdQ, sWd, bytes;
+};
+
+WeightCache cache_layout(const moe_config_t& c)
+{
+    WeightCache W;
+    if (c.dtype != MOE_FP8_BLOCK) {
+        W = WeightCache{0, 0, 0, 0, 0, 0, 0};
+        return W;
+    }
+    const size_t EHF = (size_t)c.E * c.H * c.F;
+    const size_t sHF = (size_t)(c.H / 128) * (c.F / 128) * c.E;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
+    W.WgQ = take(EHF); W.sWg = take(4 * sHF);
+    W.WuQ = take(EHF); W.sWu = take(4 * sHF);
+    W.WdQ = take(EHF); W.sWd = take(4 * sHF);
+    W.bytes = o;
+    return W;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Rows each expert computes under capacity-limited dropping:
@@ -588,6 +614,31 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
 }
 
 // ---------------------------------------------------------- blockwise FP8
+// E4M3 weight codes and scales a call uses: the caller's cache, or the copy
+// the forward quantises into `saved`.
+struct WQ {
+    uint8_t *gq, *uq, *dq;
+    float *gs, *us, *ds;
+};
+static WQ weight_codes(const moe_config_t& c, const Layout& L, uint8_t* sv, const void* cache)
+{
+    WQ w;
+    if (cache) {
+        const WeightCache C = cache_layout(c);
+        uint8_t* b = static_cast<uint8_t*>(const_cast<void*>(cache));
+        w.gq = b + C.WgQ; w.uq = b + C.WuQ; w.dq = b + C.WdQ;
+        w.gs = reinterpret_cast<float*>(b + C.sWg);
+        w.us = reinterpret_cast<float*>(b + C.sWu);
+        w.ds = reinterpret_cast<float*>(b + C.sWd);
+    } else {
+        w.gq = sv + L.WgQ; w.uq = sv + L.WuQ; w.dq = sv + L.WdQ;
+        w.gs = reinterpret_cast<float*>(sv + L.sWg);
+        w.us = reinterpret_cast<float*>(sv + L.sWu);
+        w.ds = reinterpret_cast<float*>(sv + L.sWd);
+    }
+    return w;
+}
+
 // Same stages as the bf16 layer; the expert GEMMs take E4M3 operands with
 // fp32 block scales (A: 1x128 along K, B: 128x128), all K-major, produced by
 // the quantisers in quant.cu; intermediates and outputs stay bf16.
@@ -631,14 +682,19 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     MOE_STAGE(ST_PERMUTE, launch_permute_quant(x, rowof, poff, counts, T_, H, E, k, nullptr, u8(sv, L.Xq),
                                                f32(sv, L.sX), s));
     // one orientation of the weight codes: the forward GEMMs read them
-    // MN-major, the data-gradient GEMMs K-major
-    auto wquant = [&](const void* W, int R, int C, uint8_t* q, float* sc) {
-        return launch_quant(QuantJob{static_cast<const T*>(W), nullptr, E * R, C, 128, q, sc, 1, nullptr,
-                                     nullptr, 0}, s);
-    };
-    MOE_STAGE(ST_WQUANT, wquant(a->W_gate, H, F, u8(sv, L.WgQ), f32(sv, L.sWg)));
-    MOE_STAGE(ST_WQUANT, wquant(a->W_up, H, F, u8(sv, L.WuQ), f32(sv, L.sWu)));
-    MOE_STAGE(ST_WQUANT, wquant(a->W_down, F, H, u8(sv, L.WdQ), f32(sv, L.sWd)));
+    // MN-major, the data-gradient GEMMs K-major. Pre-quantised weights
+    // (moe_quantize_weights) are read from the caller's cache; otherwise the
+    // bf16 weights are quantised into the saved buffer for this step.
+    const WQ wq = weight_codes(c, L, sv, a->weight_cache);
+    if (!a->weight_cache) {
+        auto wquant = [&](const void* W, int R, int C, uint8_t* q, float* sc) {
+            return launch_quant(QuantJob{static_cast<const T*>(W), nullptr, E * R, C, 128, q, sc, 1, nullptr,
+                                         nullptr, 0}, s);
+        };
+        MOE_STAGE(ST_WQUANT, wquant(a->W_gate, H, F, wq.gq, wq.gs));
+        MOE_STAGE(ST_WQUANT, wquant(a->W_up, H, F, wq.uq, wq.us));
+        MOE_STAGE(ST_WQUANT, wquant(a->W_down, F, H, wq.dq, wq.ds));
+    }
     GemmDesc d;
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
@@ -646,8 +702,8 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(sv, L.Xq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(sv, L.sX); d.lds_a = H / 128;
-    d.B0 = u8(sv, L.WgQ); d.B1 = u8(sv, L.WuQ); d.ldb = F; d.b_rows = E * H; d.b_kmajor = 0;
-    d.SB0 = f32(sv, L.sWg); d.SB1 = f32(sv, L.sWu);
+    d.B0 = wq.gq; d.B1 = wq.uq; d.ldb = F; d.b_rows = E * H; d.b_kmajor = 0;
+    d.SB0 = wq.gs; d.SB1 = wq.us;
     d.O0 = A; d.O1 = U; d.O2 = Hh; d.ldo = F; d.status = status;
     if (L.fold) { d.gates = gates; d.slot_of = slotof; }   // Hh = g silu(A) U
     MOE_STAGE(ST_FC1, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
@@ -659,7 +715,7 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.hq); d.lda = F; d.a_rows = Rp; d.SA0 = f32(ws, L.sh); d.lds_a = F / 128;
-    d.B0 = u8(sv, L.WdQ); d.ldb = H; d.b_rows = E * F; d.SB0 = f32(sv, L.sWd); d.b_kmajor = 0;
+    d.B0 = wq.dq; d.ldb = H; d.b_rows = E * F; d.SB0 = wq.ds; d.b_kmajor = 0;
     d.O0 = Yp; d.ldo = H; d.status = status;
     MOE_STAGE(ST_FC2, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
     MOE_STAGE(ST_COMBINE, launch_combine<T>(Yp, nullptr, rowof, L.fold ? nullptr : gates, T_, H, k,
@@ -707,6 +763,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     auto u8 = [&](uint8_t* base, size_t off) { return base + off; };
     auto f32 = [&](uint8_t* base, size_t off) { return reinterpret_cast<float*>(base + off); };
     const T* dY = static_cast<const T*>(a->dY);
+    const WQ wq = weight_codes(c, L, sv, a->weight_cache);
 
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
     if (L.fold)
@@ -725,7 +782,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.dYq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(ws, L.sdY); d.lds_a = H / 128;
-    d.B0 = u8(sv, L.WdQ); d.ldb = H; d.b_rows = E * F; d.SB0 = f32(sv, L.sWd); d.b_kmajor = 1;
+    d.B0 = wq.dq; d.ldb = H; d.b_rows = E * F; d.SB0 = wq.ds; d.b_kmajor = 1;
     d.X0 = A; d.X1 = U; d.O0 = dA; d.O1 = dU; d.ldo = F; d.status = status;
     if (L.fold) {
         d.gates = gates; d.slot_of = slotof; d.dg_part = dgpart; d.dg_ld = F / 64;
@@ -760,8 +817,8 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.dAq); d.A1 = u8(ws, L.dUq); d.lda = F; d.a_rows = Rp;
     d.SA0 = f32(ws, L.sdA); d.SA1 = f32(ws, L.sdU); d.lds_a = F / 128;
-    d.B0 = u8(sv, L.WgQ); d.B1 = u8(sv, L.WuQ); d.ldb = F; d.b_rows = E * H; d.b_kmajor = 1;
-    d.SB0 = f32(sv, L.sWg); d.SB1 = f32(sv, L.sWu);
+    d.B0 = wq.gq; d.B1 = wq.uq; d.ldb = F; d.b_rows = E * H; d.b_kmajor = 1;
+    d.SB0 = wq.gs; d.SB1 = wq.us;
     d.O0 = dXp; d.ldo = H; d.status = status;
     MOE_STAGE(ST_FC1_DGRAD, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
     // fc1 wgrad: dWg[e] = Xp_e^T dA_e, dWu[e] = Xp_e^T dU_e
@@ -805,12 +862,17 @@ moe_status_t moe_forward(moe_plan_t plan, int T, const moe_fwd_args_t* a, void* 
     moe_status_t st = check_call(plan, T, saved, saved_bytes, ws, ws_bytes);
     if (st != MOE_OK) return st;
     const bool shared = plan->cfg.Fs > 0;
-    if (!a->x || !a->Wr || !a->W_gate || !a->W_up || !a->W_down || !a->y) return MOE_ERR_INVALID_ARG;
+    // a weight cache (FP8 plans only) replaces the bf16 expert weights
+    if (a->weight_cache && plan->cfg.dtype != MOE_FP8_BLOCK) return MOE_ERR_INVALID_ARG;
+    const bool wneed = a->weight_cache == nullptr;
+    if (!a->x || !a->Wr || (wneed && (!a->W_gate || !a->W_up || !a->W_down)) || !a->y)
+        return MOE_ERR_INVALID_ARG;
     if (shared != (a->Ws_gate != nullptr) || shared != (a->Ws_up != nullptr) ||
         shared != (a->Ws_down != nullptr))
         return MOE_ERR_INVALID_ARG;
     const void* ptrs[] = {a->x, a->Wr, a->b, a->W_gate, a->W_up, a->W_down, a->Ws_gate, a->Ws_up,
-                          a->Ws_down, a->y, a->topk_idx, a->gates, a->counts, a->offsets, a->row_of};
+                          a->Ws_down, a->y, a->topk_idx, a->gates, a->counts, a->offsets, a->row_of,
+                          a->weight_cache};
     for (const void* q : ptrs)
         if (q && !aligned16(q)) return MOE_ERR_MISALIGNED;
     DeviceGuard g(plan->device);
@@ -830,15 +892,17 @@ moe_status_t moe_backward(moe_plan_t plan, int T, const moe_bwd_args_t* a, const
     moe_status_t st = check_call(plan, T, saved, saved_bytes, ws, ws_bytes);
     if (st != MOE_OK) return st;
     const bool shared = plan->cfg.Fs > 0;
-    if (!a->dY || !a->x || !a->Wr || !a->W_gate || !a->W_up || !a->W_down || !a->dX || !a->dWr ||
-        !a->dW_gate || !a->dW_up || !a->dW_down)
+    if (a->weight_cache && plan->cfg.dtype != MOE_FP8_BLOCK) return MOE_ERR_INVALID_ARG;
+    const bool wneed = a->weight_cache == nullptr;
+    if (!a->dY || !a->x || !a->Wr || (wneed && (!a->W_gate || !a->W_up || !a->W_down)) || !a->dX ||
+        !a->dWr || !a->dW_gate || !a->dW_up || !a->dW_down)
         return MOE_ERR_INVALID_ARG;
     const void* sh[] = {a->Ws_gate, a->Ws_up, a->Ws_down, a->dWs_gate, a->dWs_up, a->dWs_down};
     for (const void* q : sh)
         if (shared != (q != nullptr)) return MOE_ERR_INVALID_ARG;
     const void* ptrs[] = {a->dY, a->x, a->Wr, a->W_gate, a->W_up, a->W_down, a->Ws_gate,
                           a->Ws_up, a->Ws_down, a->dX, a->dWr, a->dW_gate, a->dW_up, a->dW_down,
-                          a->dWs_gate, a->dWs_up, a->dWs_down};
+                          a->dWs_gate, a->dWs_up, a->dWs_down, a->weight_cache};
     for (const void* q : ptrs)
         if (q && !aligned16(q)) return MOE_ERR_MISALIGNED;
     DeviceGuard g(plan->device);
@@ -898,5 +962,38 @@ moe_status_t moe_fp8_quantize(int rows, int cols, int mode, const void* in, uint
     default:
         return MOE_ERR_INVALID_ARG;
     }
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_weight_cache_size(moe_plan_t plan, size_t* bytes)
+{
+    if (!plan || !bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = cache_layout(plan->cfg).bytes;
+    return MOE_OK;
+}
+
+moe_status_t moe_quantize_weights(moe_plan_t plan, const void* W_gate, const void* W_up,
+                                  const void* W_down, void* cache, size_t cache_bytes,
+                                  moe_stream_t stream)
+{
+    if (!plan || !W_gate || !W_up || !W_down || !cache) return MOE_ERR_INVALID_ARG;
+    const moe_config_t& c = plan->cfg;
+    if (c.dtype != MOE_FP8_BLOCK) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(W_gate) || !aligned16(W_up) || !aligned16(W_down) || !aligned16(cache))
+        return MOE_ERR_MISALIGNED;
+    const WeightCache C = cache_layout(c);
+    if (cache_bytes < C.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return MOE_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* b = static_cast<uint8_t*>(cache);
+    const int E = c.E, H = c.H, F = c.F;
+    auto wquant = [&](const void* W, int R, int Cc, size_t q, size_t sc) {
+        return launch_quant(QuantJob{static_cast<const __nv_bfloat16*>(W), nullptr, E * R, Cc, 128, b + q,
+                                     reinterpret_cast<float*>(b + sc), 1, nullptr, nullptr, 0}, s);
+    };
+    cudaError_t e = wquant(W_gate, H, F, C.WgQ, C.sWg);
+    if (e == cudaSuccess) e = wquant(W_up, H, F, C.WuQ, C.sWu);
+    if (e == cudaSuccess) e = wquant(W_down, F, H, C.WdQ, C.sWd);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -31,7 +31,7 @@ def test_header_declares_the_bound_names():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_entry_points():
         assert hasattr(lib, name), name
-    assert moe.moe_abi_version() == 2
+    assert moe.moe_abi_version() == 3
 
 
 def test_status_strings(lib):
@@ -79,6 +79,9 @@ def test_null_arguments(lib):
     assert lib.moe_backward(None, 16, ctypes.byref(bargs), None, 0, None, 0, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_read_status(None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_plan_destroy(None) == moe.MOE_OK
+    n = ctypes.c_size_t()
+    assert lib.moe_weight_cache_size(None, ctypes.byref(n)) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_weights(None, None, None, None, None, 0, None) == moe.MOE_ERR_INVALID_ARG
 
 
 def test_valid_config_without_gpu_fails_cleanly(lib):

@@ -136,3 +136,50 @@ def fp8_layer_parity(w, fold=False):
                 assert np.linalg.norm(gb - wb) / nw <= 4e-2, gname
     write_report(f"{w.name} T{w.T} H{w.H} E{w.E} k{w.k} F{w.F} fp8" + (" fold" if fold else ""), rep)
     return rep
+
+
+@pytest.mark.parametrize("fold", [False, True])
+def test_fp8_weight_cache_gives_identical_results(fold):
+    """Weights quantised once by moe_quantize_weights and passed as the
+    weight cache (the bf16 weights not passed at all) give the same bits as
+    the layer quantising them inside every forward; the cache holds the
+    oracle's 128x128-block codes."""
+    w = FP8_CASES["qwen_fp8_ragged"]
+    g = upload(mi.make_inputs(w))
+    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=moe.MOE_FP8_BLOCK, fold_gates=fold)
+    y0 = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"])
+    gr0 = layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
+    torch.cuda.synchronize()
+    ref = {"y": y0.clone(), **{k: v.clone() for k, v in gr0.items()}}
+    cache = layer.quantize_weights(g["Wg"], g["Wu"], g["Wd"])
+    like = (g["Wg"], g["Wu"], g["Wd"])
+    for _ in range(2):                         # the cache is reused across steps
+        y1 = layer.forward(g["x"], g["Wr"], g["b"], None, None, None, weight_cache=cache)
+        gr1 = layer.backward(g["dY"], g["x"], g["Wr"], None, None, None, weight_cache=cache, like=like)
+        torch.cuda.synchronize()
+        assert layer.status(w.T) == 0
+        assert torch.equal(y1, ref["y"])
+        for k, v in gr1.items():
+            assert torch.equal(v, ref[k]), k
+    # the cache's first block: W_gate codes of expert 0 and their scales
+    oc, os_ = oracle.fp8_quantize(g["Wg"][0].float().cpu().numpy(), oracle.FP8_TILES)
+    n = w.H * w.F
+    assert np.array_equal(cache[:n].cpu().numpy().reshape(w.H, w.F), oc)
+    # scales follow the codes of all experts, 256-byte aligned
+    off = -(-(w.E * n) // 256) * 256
+    sc = cache[off:off + 4 * os_.size].cpu().view(torch.float32).numpy().reshape(os_.shape)
+    assert np.array_equal(sc, os_)
+
+
+def test_weight_cache_is_refused_outside_fp8():
+    w = mi.scaled(FP8_CASES["qwen_fp8_small"], dtype=mi.BF16)
+    g = upload(mi.make_inputs(w))
+    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score)
+    assert moe.moe_weight_cache_size(layer.plan) == 0
+    with pytest.raises(moe.MoEError) as e:
+        layer.quantize_weights(g["Wg"], g["Wu"], g["Wd"], cache=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+    with pytest.raises(moe.MoEError) as e:
+        layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"],
+                      weight_cache=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
