@@ -325,11 +325,43 @@ def fp8_quantize(X, mode):
     return codes, scales
 
 
+MX_ROWS, MX_COLS = 0, 1
+
+
+def mx_exponent(amax):
+    """MXFP8 block exponent e (scale 2^e, UE8M0 byte e + 127) of a block
+    maximum: the smallest e with amax <= 448 2^e, in [-127, 127]."""
+    lib = _load()
+    lib.oracle_mx_exponent.restype = ctypes.c_int
+    lib.oracle_mx_exponent.argtypes = [ctypes.c_float]
+    return int(lib.oracle_mx_exponent(float(amax)))
+
+
+def mx_quantize(X, mode):
+    """(codes, UE8M0 scale bytes) of an fp32 matrix in MXFP8: mode MX_ROWS
+    (1x32 along rows, scales M x K/32) or MX_COLS (per column over 32-row
+    blocks, scales ceil(M/32) x K)."""
+    lib = _load()
+    X = np.ascontiguousarray(X, np.float32)
+    M, K = X.shape
+    codes = np.empty((M, K), np.uint8)
+    scales = np.empty((M, K // 32) if mode == MX_ROWS else ((M + 31) // 32, K), np.uint8)
+    rc = lib.oracle_mx_quantize(M, K, mode, X.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                codes.ctypes.data_as(ctypes.c_void_p), scales.ctypes.data_as(ctypes.c_void_p))
+    if rc:
+        raise ValueError("oracle_mx_quantize: bad arguments")
+    return codes, scales
+
+
+RECIPE_BLOCK, RECIPE_MX = 0, 1
+
+
 def layer_fp8(x, Wr, Wg, Wu, Wd, topk, gates, scores, score, dY=None, Wsg=None, Wsu=None,
-              Wsd=None, fold=False):
-    """Blockwise-FP8 layer: y, and when dY is given every gradient. fold: the
-    memory-efficient permutation's order (routing weight folded into h
-    before fc2), with its rounding points."""
+              Wsd=None, fold=False, recipe=RECIPE_BLOCK):
+    """FP8 layer: y, and when dY is given every gradient. recipe: RECIPE_BLOCK
+    (blockwise FP8, fp32 block scales) or RECIPE_MX (MXFP8, 1x32 blocks with
+    power-of-two scales). fold: the memory-efficient permutation's order
+    (routing weight folded into h before fc2), with its rounding points."""
     lib = _load()
     x, Wr, Wg, Wu, Wd = _f64(x), _f64(Wr), _f64(Wg), _f64(Wu), _f64(Wd)
     Wsg, Wsu, Wsd = _f64(Wsg), _f64(Wsu), _f64(Wsd)
@@ -349,7 +381,7 @@ def layer_fp8(x, Wr, Wg, Wu, Wd, topk, gates, scores, score, dY=None, Wsg=None, 
                               _d(out["y"]), _d(out.get("dX")), _d(out.get("dWr")),
                               _d(out.get("dWg")), _d(out.get("dWu")), _d(out.get("dWd")),
                               _d(out.get("dWsg")), _d(out.get("dWsu")), _d(out.get("dWsd")),
-                              _d(out.get("dg")), 1 if fold else 0)
+                              _d(out.get("dg")), 1 if fold else 0, int(recipe))
     if rc:
         raise ValueError("oracle_layer_fp8: bad arguments")
     return out

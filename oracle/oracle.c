@@ -789,6 +789,91 @@ int oracle_fp8_quantize(int M, int K, int mode, const float* X, unsigned char* c
     return 0;
 }
 
+/* ---------------------------------------------------------------- MXFP8 */
+/*
+ * MXFP8 ("Scalable Training of Mixture-of-Experts Models with Megatron
+ * Core", §5 Platform-specific recipes: MXFP8, the default FP8 recipe on
+ * Blackwell, with 1x32 granularity). Every block of 32 consecutive values
+ * along a GEMM's contraction dimension shares one power-of-two scale
+ * 2^e, stored as an UE8M0 byte (e + 127); each value is stored as the
+ * E4M3 code of v / 2^e (round to nearest even, saturating; the division by
+ * a power of two is exact).
+ * Reading of the scale (the pages give no rule): e is the smallest integer
+ * with amax <= 448 * 2^e, so that no value of the block saturates, clamped
+ * to the UE8M0 range [-127, 127]; an all-zero block takes e = -127.
+ */
+int oracle_mx_exponent(float amax)
+{
+    if (!(amax > 0.0f)) return -127;
+    int p;
+    double m = frexp((double)amax, &p);        /* amax = m 2^p, m in [0.5, 1) */
+    /* 448 = 0.875 * 2^9: amax <= 448 2^e  <=>  m 2^p <= 0.875 2^(9 + e) */
+    int e = (m <= 0.875) ? p - 9 : p - 8;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+/* Quantise-dequantise n values v[i*stride] as one MX block; optionally the
+ * codes and the UE8M0 scale byte. */
+static void mx_block(double* v, int n, long stride, unsigned char* codes, unsigned char* sc)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float f = fabsf((float)v[(long)i * stride]);
+        if (f > amax) amax = f;
+    }
+    int e = oracle_mx_exponent(amax);
+    for (int i = 0; i < n; ++i) {
+        double q = ldexp((double)(float)v[(long)i * stride], -e);     /* exact */
+        unsigned char c = oracle_e4m3_encode((float)q);
+        if (codes) codes[(long)i * stride] = c;
+        v[(long)i * stride] = ldexp(oracle_e4m3_decode(c), e);
+    }
+    if (sc) *sc = (unsigned char)(e + 127);
+}
+
+/* 1x32 blocks along the rows of an M x K matrix (K a multiple of 32). */
+static void mx_rows(int M, int K, double* X)
+{
+    for (int m = 0; m < M; ++m)
+        for (int k0 = 0; k0 < K; k0 += 32) mx_block(X + (long)m * K + k0, 32, 1, NULL, NULL);
+}
+
+/* Per column, blocks of 32 consecutive rows (the last block may be short). */
+static void mx_cols(int M, int N, double* X)
+{
+    for (int n = 0; n < N; ++n)
+        for (int m0 = 0; m0 < M; m0 += 32) {
+            int len = M - m0 < 32 ? M - m0 : 32;
+            mx_block(X + (long)m0 * N + n, len, N, NULL, NULL);
+        }
+}
+
+/* MX codes and UE8M0 scale bytes of one fp32 matrix, for comparison with a
+ * GPU quantiser. mode 0: 1x32 along rows (scales M x K/32); mode 1: per
+ * column over 32-row blocks (scales ceil(M/32) x K). */
+int oracle_mx_quantize(int M, int K, int mode, const float* X, unsigned char* codes, unsigned char* scales)
+{
+    if (M <= 0 || K <= 0 || mode < 0 || mode > 1) return -1;
+    if (mode == 0 && K % 32) return -1;
+    double* v = (double*)malloc(sizeof(double) * (size_t)M * K);
+    for (size_t i = 0; i < (size_t)M * K; ++i) v[i] = X[i];
+    if (mode == 0) {
+        for (int m = 0; m < M; ++m)
+            for (int k0 = 0; k0 < K; k0 += 32)
+                mx_block(v + (long)m * K + k0, 32, 1, codes + (long)m * K + k0, scales + (long)m * (K / 32) + k0 / 32);
+    } else {
+        for (int n = 0; n < K; ++n)
+            for (int m0 = 0; m0 < M; m0 += 32) {
+                int len = M - m0 < 32 ? M - m0 : 32;
+                mx_block(v + (long)m0 * K + n, len, K, codes + (long)m0 * K + n, scales + (long)(m0 / 32) * K + n);
+            }
+    }
+    free(v);
+    return 0;
+}
+
 static double* dup(const double* p, size_t n)
 {
     double* q = (double*)malloc(sizeof(double) * (n ? n : 1));
@@ -848,19 +933,62 @@ static void gemm_nt(int M, int N, int K, const double* A, const double* B, doubl
  * the bf16-stored a, u, as the backward pass recomputes it), dh = g_r dh',
  * and the fc2 weight gradient uses h' recomputed from the stored a, u.
  */
+/*
+ * recipe 0: blockwise FP8 (fp32 scales; 1x128 blocks along K for the operand
+ * indexing output rows, 128x128 for the other). recipe 1: MXFP8 (1x32 blocks
+ * along K for both operands of every GEMM, so each weight is quantised once
+ * per orientation: along H for fc1 and along F for fc1's data gradient; Wd
+ * along F for fc2 and along H for fc2's data gradient).
+ */
+#define RECIPE_BLOCK 0
+#define RECIPE_MX 1
+
+/* the quantisation of X (rows x cols) whose contraction dimension runs along
+ * its rows (by_row 1: blocks within a row) or its columns (by_row 0) */
+static void q_act(int recipe, int by_row, int rows, int cols, double* X)
+{
+    if (recipe == RECIPE_MX) {
+        if (by_row) mx_rows(rows, cols, X); else mx_cols(rows, cols, X);
+    } else {
+        if (by_row) qdq_rows(rows, cols, X); else qdq_cols(rows, cols, X);
+    }
+}
+/* the second operand of a GEMM (128x128 blocks, or MX blocks along K) */
+static void q_other(int recipe, int by_row, int rows, int cols, double* X)
+{
+    if (recipe == RECIPE_MX) {
+        if (by_row) mx_rows(rows, cols, X); else mx_cols(rows, cols, X);
+    } else {
+        qdq_tiles(rows, cols, X);
+    }
+}
+
 static void swiglu_fp8(int M, int H, int F, const double* X, const double* Wg, const double* Wu,
                        const double* Wd, double* Y, const double* dYr, double* dX, double* dWg,
-                       double* dWu, double* dWd, const double* g, double* dg)
+                       double* dWu, double* dWd, const double* g, double* dg, int recipe)
 {
     size_t mf = (size_t)(M > 0 ? M : 1) * F, mh = (size_t)(M > 0 ? M : 1) * H;
     double* Xq = dup(X, (size_t)M * H);
-    qdq_rows(M, H, Xq);
+    q_act(recipe, 1, M, H, Xq);                       /* fc1 A: K = H along rows */
+    /* fc1 B: Wg, Wu (H x F) with K = H along their columns; fc2 B: Wd (F x H)
+     * with K = F along its columns */
     double* Wgq = dup(Wg, (size_t)H * F);
     double* Wuq = dup(Wu, (size_t)H * F);
     double* Wdq = dup(Wd, (size_t)F * H);
-    qdq_tiles(H, F, Wgq);
-    qdq_tiles(H, F, Wuq);
-    qdq_tiles(F, H, Wdq);
+    q_other(recipe, 0, H, F, Wgq);
+    q_other(recipe, 0, H, F, Wuq);
+    q_other(recipe, 0, F, H, Wdq);
+    /* the data gradients contract the weights along their other dimension:
+     * the same codes in the blockwise recipe, a second quantisation in MX */
+    double *Wgb = Wgq, *Wub = Wuq, *Wdb = Wdq;
+    if (recipe == RECIPE_MX && dYr) {
+        Wgb = dup(Wg, (size_t)H * F);
+        Wub = dup(Wu, (size_t)H * F);
+        Wdb = dup(Wd, (size_t)F * H);
+        mx_rows(H, F, Wgb);
+        mx_rows(H, F, Wub);
+        mx_rows(F, H, Wdb);
+    }
     double* A = (double*)malloc(sizeof(double) * mf);
     double* U = (double*)malloc(sizeof(double) * mf);
     double* Hh = (double*)malloc(sizeof(double) * mf);
@@ -873,16 +1001,16 @@ static void swiglu_fp8(int M, int H, int F, const double* X, const double* Wg, c
         U[i] = bf16r(U[i]);
     }
     double* Hq = dup(Hh, (size_t)M * F);
-    qdq_rows(M, F, Hq);
+    q_act(recipe, 1, M, F, Hq);                       /* fc2 A: K = F */
     gemm(M, H, F, Hq, Wdq, Y);
     for (size_t i = 0; i < (size_t)M * H; ++i) Y[i] = bf16r(Y[i]);
     free(Hq);
     if (dYr) {
-        /* fc2 dgrad: dh = q(dYr) Wd_q^T (Wd's 128x128 blocks, used transposed) */
+        /* fc2 dgrad: dh = q(dYr) q(Wd)^T, K = H */
         double* dYq = dup(dYr, (size_t)M * H);
-        qdq_rows(M, H, dYq);
+        q_act(recipe, 1, M, H, dYq);
         double* dh = (double*)malloc(sizeof(double) * mf);
-        gemm_nt(M, F, H, dYq, Wdq, dh);
+        gemm_nt(M, F, H, dYq, Wdb, dh);
         double* dA = (double*)malloc(sizeof(double) * mf);
         double* dU = (double*)malloc(sizeof(double) * mf);
         if (g) {
@@ -902,33 +1030,35 @@ static void swiglu_fp8(int M, int H, int F, const double* X, const double* Wg, c
             dA[i] = bf16r(dh[i] * U[i] * dsilu(A[i]));
             dU[i] = bf16r(dh[i] * silu(A[i]));
         }
-        /* fc2 wgrad: dWd = q_col(h)^T q_tile(dYr) */
+        /* fc2 wgrad: dWd = q(h)^T q(dYr), K = the expert's rows (blocks along
+         * the rows, counted from the segment's first row) */
         double* Hc = dup(Hh, (size_t)M * F);
-        qdq_cols(M, F, Hc);
+        q_act(recipe, 0, M, F, Hc);
         double* dYt = dup(dYr, (size_t)M * H);
-        qdq_tiles(M, H, dYt);
+        q_other(recipe, 0, M, H, dYt);
         gemm_tn(F, H, M, Hc, dYt, dWd);
-        /* fc1 dgrad: dX = q(dA) Wg_q^T + q(dU) Wu_q^T */
+        /* fc1 dgrad: dX = q(dA) q(Wg)^T + q(dU) q(Wu)^T, K = F */
         double* dAq = dup(dA, mf);
         double* dUq = dup(dU, mf);
-        qdq_rows(M, F, dAq);
-        qdq_rows(M, F, dUq);
+        q_act(recipe, 1, M, F, dAq);
+        q_act(recipe, 1, M, F, dUq);
         double* t1 = (double*)malloc(sizeof(double) * mh);
-        gemm_nt(M, H, F, dAq, Wgq, dX);
-        gemm_nt(M, H, F, dUq, Wuq, t1);
+        gemm_nt(M, H, F, dAq, Wgb, dX);
+        gemm_nt(M, H, F, dUq, Wub, t1);
         for (size_t i = 0; i < (size_t)M * H; ++i) dX[i] += t1[i];
-        /* fc1 wgrad: dWg = q_col(X)^T q_tile(dA), dWu = q_col(X)^T q_tile(dU) */
+        /* fc1 wgrad: dWg = q(X)^T q(dA), dWu = q(X)^T q(dU), K = rows */
         double* Xc = dup(X, (size_t)M * H);
-        qdq_cols(M, H, Xc);
+        q_act(recipe, 0, M, H, Xc);
         double* dAt = dup(dA, mf);
         double* dUt = dup(dU, mf);
-        qdq_tiles(M, F, dAt);
-        qdq_tiles(M, F, dUt);
+        q_other(recipe, 0, M, F, dAt);
+        q_other(recipe, 0, M, F, dUt);
         gemm_tn(H, F, M, Xc, dAt, dWg);
         gemm_tn(H, F, M, Xc, dUt, dWu);
         free(dYq); free(dh); free(dA); free(dU); free(Hc); free(dYt); free(dAq); free(dUq);
         free(t1); free(Xc); free(dAt); free(dUt);
     }
+    if (Wgb != Wgq) { free(Wgb); free(Wub); free(Wdb); }
     free(Xq); free(Wgq); free(Wuq); free(Wdq); free(A); free(U); free(Hh);
 }
 
@@ -944,10 +1074,11 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
                      const int* topk, const double* gates, const double* scores,
                      const double* dY, double* y,
                      double* dX, double* dWr, double* dWg, double* dWu, double* dWd,
-                     double* dWsg, double* dWsu, double* dWsd, double* dg_out, int fold)
+                     double* dWsg, double* dWsu, double* dWsd, double* dg_out, int fold,
+                     int recipe)
 {
     if (T <= 0 || H <= 0 || H % 128 || E <= 0 || k <= 0 || k > E || k > 1024 || F <= 0 ||
-        F % 128 || Fs < 0 || Fs % 128)
+        F % 128 || Fs < 0 || Fs % 128 || recipe < 0 || recipe > 1)
         return -1;
     const int R = T * k;
     int* counts = (int*)malloc(sizeof(int) * E);
@@ -971,7 +1102,7 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
         if (M == 0) continue;
         swiglu_fp8(M, H, F, Xp + (size_t)offsets[e] * H, Wg + (size_t)e * H * F,
                    Wu + (size_t)e * H * F, Wd + (size_t)e * F * H, Yp + (size_t)offsets[e] * H,
-                   NULL, NULL, NULL, NULL, NULL, fold ? grow + offsets[e] : NULL, NULL);
+                   NULL, NULL, NULL, NULL, NULL, fold ? grow + offsets[e] : NULL, NULL, recipe);
     }
     for (int t = 0; t < T; ++t)
         for (int h = 0; h < H; ++h) {
@@ -984,7 +1115,7 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
     double* Ys = NULL;
     if (Fs > 0) {
         Ys = (double*)malloc(sizeof(double) * (size_t)T * H);
-        swiglu_fp8(T, H, Fs, x, Wsg, Wsu, Wsd, Ys, NULL, NULL, NULL, NULL, NULL, NULL, NULL);
+        swiglu_fp8(T, H, Fs, x, Wsg, Wsu, Wsd, Ys, NULL, NULL, NULL, NULL, NULL, NULL, NULL, recipe);
         for (size_t i = 0; i < (size_t)T * H; ++i) y[i] += Ys[i];
     }
     if (dY) {
@@ -1013,7 +1144,7 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
             swiglu_fp8(M, H, F, Xp + (size_t)offsets[e] * H, Wg + (size_t)e * H * F,
                        Wu + (size_t)e * H * F, Wd + (size_t)e * F * H, Ytmp,
                        dYp + (size_t)offsets[e] * H, dXp + (size_t)offsets[e] * H, dWg_e, dWu_e,
-                       dWd_e, fold ? grow + offsets[e] : NULL, fold ? dgr + offsets[e] : NULL);
+                       dWd_e, fold ? grow + offsets[e] : NULL, fold ? dgr + offsets[e] : NULL, recipe);
         }
         if (fold) {
             for (int r = 0; r < R; ++r) dg[slot_of[r]] = dgr[r];
@@ -1043,7 +1174,7 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
             }
         if (Fs > 0) {
             double* dXs = (double*)malloc(sizeof(double) * (size_t)T * H);
-            swiglu_fp8(T, H, Fs, x, Wsg, Wsu, Wsd, Ytmp, dY, dXs, dWsg, dWsu, dWsd, NULL, NULL);
+            swiglu_fp8(T, H, Fs, x, Wsg, Wsu, Wsd, Ytmp, dY, dXs, dWsg, dWsu, dWsd, NULL, NULL, recipe);
             for (size_t i = 0; i < (size_t)T * H; ++i) dX[i] += dXs[i];
             free(dXs);
         }
