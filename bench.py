@@ -62,7 +62,8 @@ def stage_bytes(name: str, w: mi.Workload) -> float:
     rows, E, F = (w.T, 1, w.Fs) if shared else (w.R, w.E, w.F)
     H = w.H
     o = 4 if w.dtype == mi.FP32 else 2
-    a = 4 if w.dtype == mi.FP32 else (1 + 4 / 128 if w.dtype == mi.FP8_BLOCK else 2)
+    a = 4 if w.dtype == mi.FP32 else (1 + 4 / 128 if w.dtype == mi.FP8_BLOCK else
+                                      1 + 1 / 32 if w.dtype == mi.MXFP8 else 2)
     RH, RF, EHF = rows * H, rows * F, E * H * F
     return {"fc1_swiglu": a * (RH + 2 * EHF) + o * 3 * RF,
             "fc2": a * (RF + EHF) + o * RH,
@@ -271,7 +272,7 @@ def run_reference(args, w):
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
-    from mixture_experts_layer_sigmoid_gb300 import MoELayer, MOE_BF16, MOE_FP32, MOE_FP8_BLOCK
+    from mixture_experts_layer_sigmoid_gb300 import MoELayer, MOE_BF16, MOE_FP32, MOE_FP8_BLOCK, MOE_MXFP8
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -284,7 +285,8 @@ def run_ours(args, w):
 
     inp = mi.make_inputs(w, dev)
     layer = MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score,
-                     dtype={mi.FP32: MOE_FP32, mi.BF16: MOE_BF16, mi.FP8_BLOCK: MOE_FP8_BLOCK}[w.dtype],
+                     dtype={mi.FP32: MOE_FP32, mi.BF16: MOE_BF16, mi.FP8_BLOCK: MOE_FP8_BLOCK,
+                            mi.MXFP8: MOE_MXFP8}[w.dtype],
                      Fs=w.Fs, device=local, stage_timing=True, fold_gates=args.fold_gates)
     x, dY = inp["x"], inp["dY"]
     W = (inp["Wr"], inp["Wg"], inp["Wu"], inp["Wd"], inp["Wsg"], inp["Wsu"], inp["Wsd"])
@@ -397,7 +399,7 @@ def run_ours(args, w):
     jm = job_metrics(world, ms, flops, w.T)
     value = jm["tflops"]
     peaks, peaks_kind = load_peaks()
-    peak_sust, peak_name = choose_peak(peaks, peaks_kind, clocks, w.dtype == mi.FP8_BLOCK)
+    peak_sust, peak_name = choose_peak(peaks, peaks_kind, clocks, w.dtype in (mi.FP8_BLOCK, mi.MXFP8))
 
     # ---- roofline of the dominant kernel (largest device time in the timed
     # region): the slower of its FLOPs at the tensor peak and its algorithmic
@@ -455,7 +457,7 @@ def run_ours(args, w):
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": {mi.BF16: "bf16", mi.FP32: "f32", mi.FP8_BLOCK: "e4m3"}[w.dtype],
+                "dtype": {mi.BF16: "bf16", mi.FP32: "f32", mi.FP8_BLOCK: "e4m3", mi.MXFP8: "e4m3"}[w.dtype],
                 "data": "synthetic",
                 "tokens_per_s": jm["tokens_per_s"],
                 "pct_of_tensor_peak": 100.0 * value / world / peak_sust,
@@ -500,7 +502,7 @@ def main():
                     help="comma-separated shape overrides, e.g. F=4096,T=2048 (profiling runs)")
     args = ap.parse_args()
     w = mi.WORKLOADS[args.workload]
-    if args.weight_cache and w.dtype != mi.FP8_BLOCK:
+    if args.weight_cache and w.dtype not in (mi.FP8_BLOCK, mi.MXFP8):
         ap.error("--weight-cache applies to the FP8 workloads only")
     if args.override:
         kv = dict(item.split("=") for item in args.override.split(","))

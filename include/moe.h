@@ -68,8 +68,19 @@ typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
  *     K for the operand indexing output rows, 128x128 for the other), fp32
  *     accumulation ("Scalable Training of Mixture-of-Experts Models with
  *     Megatron Core", §5, blockwise FP8). The router stays fp32. Layers with
- *     a shared expert are not supported in this mode (MOE_ERR_UNSUPPORTED). */
-typedef enum { MOE_FP32 = 0, MOE_BF16 = 1, MOE_FP8_BLOCK = 2 } moe_dtype_t;
+ *     a shared expert are not supported in this mode (MOE_ERR_UNSUPPORTED).
+ *   MOE_MXFP8: bf16 activations, weights and gradients; every expert GEMM
+ *     runs on E4M3 operands in the MXFP8 recipe ("Scalable Training of
+ *     Mixture-of-Experts Models with Megatron Core", §5 Platform-specific
+ *     recipes: the default FP8 recipe on Blackwell, 1x32 granularity): each
+ *     32 consecutive values along the GEMM's contraction dimension share one
+ *     power-of-two scale 2^e (an UE8M0 byte), e the smallest integer with
+ *     amax <= 448 2^e; the tensor cores apply the scales. Both operands of
+ *     every GEMM are blocked along K, so weights (and the activations and
+ *     gradients that feed two GEMMs) are quantised once per orientation.
+ *     The router stays fp32. Layers with a shared expert or with
+ *     capacity_factor > 0 are not supported (MOE_ERR_UNSUPPORTED). */
+typedef enum { MOE_FP32 = 0, MOE_BF16 = 1, MOE_FP8_BLOCK = 2, MOE_MXFP8 = 3 } moe_dtype_t;
 
 typedef struct {
     int H;       /* hidden size; multiple of 128                          */
@@ -150,7 +161,7 @@ typedef struct {
                               over the sum of their scores). Indices outside
                               [0, E) are clamped and reported as
                               MOE_ERR_INVALID_ARG in the status word. */
-    const void*  weight_cache; /* optional in (MOE_FP8_BLOCK plans): expert
+    const void*  weight_cache; /* optional in (FP8-recipe plans): expert
                               weights quantised by moe_quantize_weights. When
                               given, W_gate, W_up and W_down are not read (they
                               may be NULL) and the call quantises no weights;
@@ -178,7 +189,7 @@ typedef struct {
     void*        dWs_gate; /* out, H×Fs act (NULL iff Fs == 0)                */
     void*        dWs_up;
     void*        dWs_down;
-    const void*  weight_cache; /* MOE_FP8_BLOCK: the cache given to the
+    const void*  weight_cache; /* FP8 recipes: the cache given to the
                               forward (W_gate, W_up, W_down then unread), or
                               NULL when the forward quantised the bf16
                               weights itself. Other dtypes: NULL. */
@@ -282,7 +293,7 @@ enum { MOE_Q_ROWS = 0, MOE_Q_TILES = 1, MOE_Q_COLS_T = 2, MOE_Q_TILES_T = 3 };
 moe_status_t moe_fp8_quantize(int rows, int cols, int mode, const void* in, uint8_t* codes,
                               float* scales, uint8_t* codes_t, float* scales_t, moe_stream_t stream);
 
-/* Quantised expert weights for MOE_FP8_BLOCK plans ("Scalable Training of
+/* Quantised expert weights for MOE_FP8_BLOCK and MOE_MXFP8 plans ("Scalable Training of
  * Mixture-of-Experts Models with Megatron Core", §5 Kernel and shape
  * optimization: grouped quantization of the experts' weights, done once
  * and kept). A caller that keeps E4M3 weights between steps -- they change
@@ -292,21 +303,43 @@ moe_status_t moe_fp8_quantize(int rows, int cols, int mode, const void* in, uint
  * moe_backward, which then skip their own weight quantisation.
  *
  * moe_weight_cache_size: bytes of the cache for this plan (0 for plans
- * that are not MOE_FP8_BLOCK). Errors: INVALID_ARG.
+ * that use neither FP8 recipe). Errors: INVALID_ARG.
  *
  * moe_quantize_weights: quantise W_gate, W_up (E x H x F bf16) and W_down
  * (E x F x H bf16) into `cache` (cache_bytes >= the size above), enqueued
  * on `stream`. The cache holds each matrix's E4M3 codes in its own layout
- * and one fp32 scale per 128x128 block (amax / 448, 1 for an all-zero
- * block), exactly the codes the layer would produce inside moe_forward;
- * its internal layout is private to the library version. 16-byte aligned
- * device pointers, owned by the caller.
- * Errors: INVALID_ARG (null), UNSUPPORTED (plan not MOE_FP8_BLOCK),
+ * with the plan's scales (MOE_FP8_BLOCK: one fp32 scale per 128x128 block,
+ * amax / 448, 1 for an all-zero block; MOE_MXFP8: the codes of both
+ * orientations, each with its UE8M0 scale per 32 values), exactly the codes
+ * the layer would produce inside moe_forward; its internal layout is
+ * private to the library version. 16-byte aligned device pointers, owned by
+ * the caller.
+ * Errors: INVALID_ARG (null), UNSUPPORTED (plan uses neither FP8 recipe),
  * MISALIGNED, WORKSPACE_TOO_SMALL (cache_bytes), CUDA. */
 moe_status_t moe_weight_cache_size(moe_plan_t plan, size_t* bytes);
 moe_status_t moe_quantize_weights(moe_plan_t plan, const void* W_gate, const void* W_up,
                                   const void* W_down, void* cache, size_t cache_bytes,
                                   moe_stream_t stream);
+
+/* MXFP8 quantiser used by the MOE_MXFP8 layer, on a row-major rows x cols
+ * bf16 device matrix (both multiples of 128). Blocks of 32 values share the
+ * scale 2^e, e the smallest integer with amax <= 448 2^e, clamped to
+ * [-127, 127] (-127 for an all-zero block), stored as the UE8M0 byte
+ * e + 127; a value is stored as the E4M3 code of v 2^-e (round to nearest
+ * even). Scales are written as "scale atoms", the layout the GEMMs copy into
+ * tensor memory: for an operand read as [n][K], one 512-byte atom per
+ * 128-row tile t and 128-deep K block b at (t * K/128 + b) * 512, whose byte
+ * 16 (m % 32) + 4 (m / 32) + j holds the scale of tile row m and 32-deep
+ * sub-block j.
+ *   codes, scales (optional): blocks along the rows; codes rows x cols,
+ *     atoms of the [rows][K = cols] operand (rows * cols / 32 bytes).
+ *   codes_c, scales_c (optional): blocks down the columns (32 rows each);
+ *     col_transposed 1: codes cols x rows (the transpose), col_transposed 0:
+ *     codes rows x cols in place; atoms of the [cols][K = rows] operand.
+ * At least one pair must be given. Enqueued on `stream`.
+ * Errors: INVALID_ARG, MISALIGNED, CUDA. */
+moe_status_t moe_mx_quantize(int rows, int cols, const void* in, uint8_t* codes, uint8_t* scales,
+                             uint8_t* codes_c, uint8_t* scales_c, int col_transposed, moe_stream_t stream);
 
 /* Failure-detection check. Every pipelined kernel of the library waits on
  * its shared-memory mbarriers with a bounded wait (2 s); when a wait runs out

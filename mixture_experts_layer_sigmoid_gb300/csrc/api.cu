@@ -28,11 +28,49 @@ struct Layout {
     // workspace
     size_t status, hist, blkbase, zpart, Ys, dYp, dA, dU, dXp, dz, WrT, wrpart, dAs, dUs, dXs, dgpart, ws_bytes;
     bool fold;   // Hh and Yp live in the workspace (MOE_FLAG_FOLD_GATES)
-    // blockwise FP8 (saved: permuted activations and weights; ws: the rest)
-    size_t Xq, sX, WgQ, sWg, WuQ, sWu, WgQT, sWgT, WuQT, sWuT, WdQ, sWd, WdQT, sWdT;
+    // FP8 recipes (saved: permuted activations and, unless the caller passes a
+    // weight cache, the weight codes; ws: the rest)
+    size_t Xq, sX, wcache;
     size_t hq, sh, dYq, sdY, dAq, sdA, dUq, sdU, hTq, shT, dYpTq, sdYpT, XpTq, sXpT, dATq, sdAT,
         dUTq, sdUT;
 };
+
+bool fp8_recipe(const moe_config_t& c) { return c.dtype == MOE_FP8_BLOCK || c.dtype == MOE_MXFP8; }
+
+// Quantised expert weights of an FP8 plan (the caller's weight cache, or the
+// copy a forward makes in `saved`): for W_gate, W_up (E x H x F) and W_down
+// (E x F x H), in this order, q[i] E4M3 codes in the matrix's natural layout
+// and s[i] its scales.
+//   MOE_FP8_BLOCK: fp32 scales of 128x128 blocks [E][rows/128][cols/128]; the
+//     same codes serve the forward GEMMs (read MN-major) and the data-gradient
+//     GEMMs (K-major), so q[3..5] = q[0..2].
+//   MOE_MXFP8: q[0..2] are the forward orientation (32-element blocks along
+//     the matrix's first dimension, the forward GEMM's K, read MN-major) and
+//     q[3..5] the data-gradient orientation (blocks along the second
+//     dimension, read K-major), each with its UE8M0 scale atoms.
+struct WeightCache {
+    size_t q[6], s[6], bytes;
+};
+
+WeightCache cache_layout(const moe_config_t& c)
+{
+    WeightCache W;
+    memset(&W, 0, sizeof W);
+    if (!fp8_recipe(c)) return W;
+    const size_t EHF = (size_t)c.E * c.H * c.F;
+    const bool mx = c.dtype == MOE_MXFP8;
+    const size_t sc = mx ? EHF / 32 : 4 * (size_t)(c.H / 128) * (c.F / 128) * c.E;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
+    for (int i = 0; i < (mx ? 6 : 3); ++i) {
+        W.q[i] = take(EHF);
+        W.s[i] = take(sc);
+    }
+    if (!mx)
+        for (int i = 3; i < 6; ++i) { W.q[i] = W.q[i - 3]; W.s[i] = W.s[i - 3]; }
+    W.bytes = o;
+    return W;
+}
 
 Layout make_layout(const moe_config_t& c, int T)
 {
@@ -58,8 +96,8 @@ Layout make_layout(const moe_config_t& c, int T)
     L.pairtab = take(sizeof(int) * ((size_t)L.MT_max + c.E + 1));   // pairs, then E+1 pair offsets
     L.rowof = take(sizeof(int) * L.R);
     L.slotof = take(sizeof(int) * L.Rp_max);
-    // (the FP8 layer keeps only the codes of the permuted rows)
-    L.Xp = take(c.dtype == MOE_FP8_BLOCK ? 0 : es * L.Rp_max * c.H);
+    // (the FP8 layers keep only the codes of the permuted rows)
+    L.Xp = take(fp8_recipe(c) ? 0 : es * L.Rp_max * c.H);
     L.A = take(es * L.Rp_max * c.F);
     L.U = take(es * L.Rp_max * c.F);
     L.fold = (c.flags & MOE_FLAG_FOLD_GATES) != 0;
@@ -68,17 +106,13 @@ Layout make_layout(const moe_config_t& c, int T)
     L.As = take(es * (size_t)T * c.Fs);
     L.Us = take(es * (size_t)T * c.Fs);
     L.Hs = take(es * (size_t)T * c.Fs);
-    const bool q8 = c.dtype == MOE_FP8_BLOCK;
-    const size_t Rp = L.Rp_max, HF = (size_t)c.H * c.F, EHF = (size_t)c.E * HF;
-    const size_t sHF = (size_t)(c.H / 128) * (c.F / 128) * c.E;
-    L.Xq = take(q8 ? Rp * c.H : 0);
-    L.sX = take(q8 ? 4 * Rp * (c.H / 128) : 0);
-    L.WgQ = take(q8 ? EHF : 0);   L.sWg = take(q8 ? 4 * sHF : 0);
-    L.WuQ = take(q8 ? EHF : 0);   L.sWu = take(q8 ? 4 * sHF : 0);
-    L.WgQT = take(0);  L.sWgT = take(0);   // (one orientation of the weight codes)
-    L.WuQT = take(0);  L.sWuT = take(0);
-    L.WdQ = take(q8 ? EHF : 0);   L.sWd = take(q8 ? 4 * sHF : 0);
-    L.WdQT = take(0);  L.sWdT = take(0);
+    const bool q8 = c.dtype == MOE_FP8_BLOCK, mx = c.dtype == MOE_MXFP8, anyq = q8 || mx;
+    const size_t Rp = L.Rp_max;
+    // scale bytes of a codes array: blockwise per 128 values (fp32), MX per 32 (one byte)
+    auto scb = [&](size_t n128) { return q8 ? 4 * n128 : mx ? 4 * n128 : 0; };
+    L.Xq = take(anyq ? Rp * c.H : 0);
+    L.sX = take(scb(Rp * (c.H / 128)));
+    L.wcache = take(cache_layout(c).bytes);
     L.saved_bytes = o;
     o = 0;
     L.status = take(256);
@@ -97,48 +131,25 @@ Layout make_layout(const moe_config_t& c, int T)
     L.dAs = take(es * (size_t)T * c.Fs);
     L.dUs = take(es * (size_t)T * c.Fs);
     L.dXs = take(c.Fs ? es * (size_t)T * c.H : 0);
-    L.hq = take(q8 ? Rp * c.F : 0);       L.sh = take(q8 ? 4 * Rp * (c.F / 128) : 0);
-    L.dYq = take(q8 ? Rp * c.H : 0);      L.sdY = take(q8 ? 4 * Rp * (c.H / 128) : 0);
-    L.dAq = take(q8 ? Rp * c.F : 0);      L.sdA = take(q8 ? 4 * Rp * (c.F / 128) : 0);
-    L.dUq = take(q8 ? Rp * c.F : 0);      L.sdU = take(q8 ? 4 * Rp * (c.F / 128) : 0);
-    L.hTq = take(q8 ? Rp * c.F : 0);      L.shT = take(q8 ? 4 * (Rp / 128) * c.F : 0);
-    L.dYpTq = take(q8 ? Rp * c.H : 0);    L.sdYpT = take(q8 ? 4 * (Rp / 128) * (c.H / 128) : 0);
-    L.XpTq = take(q8 ? Rp * c.H : 0);     L.sXpT = take(q8 ? 4 * (Rp / 128) * c.H : 0);
-    L.dATq = take(q8 ? Rp * c.F : 0);     L.sdAT = take(q8 ? 4 * (Rp / 128) * (c.F / 128) : 0);
+    // blockwise: 1x128 row scales, per-column or per-tile transposed scales;
+    // MX: one byte per 32 values whatever the orientation
+    const size_t RF32 = Rp * c.F / 32, RH32 = Rp * c.H / 32;
+    L.hq = take(anyq ? Rp * c.F : 0);     L.sh = take(mx ? RF32 : scb(Rp * (c.F / 128)));
+    L.dYq = take(anyq ? Rp * c.H : 0);    L.sdY = take(mx ? RH32 : scb(Rp * (c.H / 128)));
+    L.dAq = take(anyq ? Rp * c.F : 0);    L.sdA = take(mx ? RF32 : scb(Rp * (c.F / 128)));
+    L.dUq = take(anyq ? Rp * c.F : 0);    L.sdU = take(mx ? RF32 : scb(Rp * (c.F / 128)));
+    L.hTq = take(anyq ? Rp * c.F : 0);    L.shT = take(mx ? RF32 : scb((Rp / 128) * c.F));
+    L.dYpTq = take(anyq ? Rp * c.H : 0);  L.sdYpT = take(mx ? RH32 : scb((Rp / 128) * (c.H / 128)));
+    L.XpTq = take(anyq ? Rp * c.H : 0);   L.sXpT = take(mx ? RH32 : scb((Rp / 128) * c.H));
+    L.dATq = take(anyq ? Rp * c.F : 0);   L.sdAT = take(mx ? RF32 : scb((Rp / 128) * (c.F / 128)));
     L.dgpart = take(L.fold ? sizeof(float) * L.Rp_max * (c.F / 64) : 0);
     if (L.fold) {
         L.Hh = take(es * L.Rp_max * c.F);
         L.Yp = take(es * L.Rp_max * c.H);
     }
-    L.dUTq = take(q8 ? Rp * c.F : 0);     L.sdUT = take(q8 ? 4 * (Rp / 128) * (c.F / 128) : 0);
+    L.dUTq = take(anyq ? Rp * c.F : 0);   L.sdUT = take(mx ? RF32 : scb((Rp / 128) * (c.F / 128)));
     L.ws_bytes = o;
     return L;
-}
-
-// Quantised expert weights of an FP8 plan, in a caller-owned buffer
-// (moe_quantize_weights): E4M3 codes of W_gate, W_up (E x H x F) and W_down
-// (E x F x H) in their natural layouts, each followed by its 128x128-block
-// fp32 scales [E][rows/128][cols/128].
-struct WeightCache {
-    size_t WgQ, sWg, WuQ, sWu, WdQ, sWd, bytes;
-};
-
-WeightCache cache_layout(const moe_config_t& c)
-{
-    WeightCache W;
-    if (c.dtype != MOE_FP8_BLOCK) {
-        W = WeightCache{0, 0, 0, 0, 0, 0, 0};
-        return W;
-    }
-    const size_t EHF = (size_t)c.E * c.H * c.F;
-    const size_t sHF = (size_t)(c.H / 128) * (c.F / 128) * c.E;
-    size_t o = 0;
-    auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
-    W.WgQ = take(EHF); W.sWg = take(4 * sHF);
-    W.WuQ = take(EHF); W.sWu = take(4 * sHF);
-    W.WdQ = take(EHF); W.sWd = take(4 * sHF);
-    W.bytes = o;
-    return W;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -161,13 +172,13 @@ moe_status_t check_config(const moe_config_t* c)
         !(c->capacity_factor >= 0.f) || !std::isfinite(c->capacity_factor))
         return MOE_ERR_INVALID_ARG;
     if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
-    if (c->dtype != MOE_FP32 && c->dtype != MOE_BF16 && c->dtype != MOE_FP8_BLOCK)
+    if (c->dtype != MOE_FP32 && c->dtype != MOE_BF16 && c->dtype != MOE_FP8_BLOCK && c->dtype != MOE_MXFP8)
         return MOE_ERR_INVALID_ARG;
-    if (c->dtype == MOE_FP8_BLOCK && c->Fs > 0) return MOE_ERR_UNSUPPORTED;
+    if (fp8_recipe(*c) && c->Fs > 0) return MOE_ERR_UNSUPPORTED;
     // a dropped assignment keeps its row of Xp (the router gradient needs it),
     // which would enter the 128-token quantisation blocks of the FP8 weight
     // gradients; dropping is built for the bf16 and fp32 layers only
-    if (c->dtype == MOE_FP8_BLOCK && c->capacity_factor > 0.f) return MOE_ERR_UNSUPPORTED;
+    if (fp8_recipe(*c) && c->capacity_factor > 0.f) return MOE_ERR_UNSUPPORTED;
     // int32 row indices: R_pad * max(H, F) elements must stay addressable per
     // buffer with 32-bit row numbers
     const long long R = (long long)c->T_max * c->top_k + (long long)c->E * kTileM;
@@ -264,6 +275,7 @@ moe_status_t moe_plan_create(const moe_config_t* cfg, int device, moe_plan_t* ou
         if (!g.ok) return MOE_ERR_CUDA;
         if (cfg->dtype == MOE_BF16 && gemm_tc_prepare(device) != cudaSuccess) return MOE_ERR_CUDA;
         if (cfg->dtype == MOE_FP8_BLOCK && gemm_fp8_prepare(device) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cfg->dtype == MOE_MXFP8 && gemm_mx_prepare(device) != cudaSuccess) return MOE_ERR_CUDA;
     }
     moe_plan_s* p = new (std::nothrow) moe_plan_s;
     if (!p) return MOE_ERR_CUDA;
@@ -617,26 +629,45 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
 // E4M3 weight codes and scales a call uses: the caller's cache, or the copy
 // the forward quantises into `saved`.
 struct WQ {
-    uint8_t *gq, *uq, *dq;
-    float *gs, *us, *ds;
+    uint8_t* q[6];   // gate, up, down: forward orientation, then data-gradient orientation
+    void* s[6];
 };
 static WQ weight_codes(const moe_config_t& c, const Layout& L, uint8_t* sv, const void* cache)
 {
     WQ w;
-    if (cache) {
-        const WeightCache C = cache_layout(c);
-        uint8_t* b = static_cast<uint8_t*>(const_cast<void*>(cache));
-        w.gq = b + C.WgQ; w.uq = b + C.WuQ; w.dq = b + C.WdQ;
-        w.gs = reinterpret_cast<float*>(b + C.sWg);
-        w.us = reinterpret_cast<float*>(b + C.sWu);
-        w.ds = reinterpret_cast<float*>(b + C.sWd);
-    } else {
-        w.gq = sv + L.WgQ; w.uq = sv + L.WuQ; w.dq = sv + L.WdQ;
-        w.gs = reinterpret_cast<float*>(sv + L.sWg);
-        w.us = reinterpret_cast<float*>(sv + L.sWu);
-        w.ds = reinterpret_cast<float*>(sv + L.sWd);
+    const WeightCache C = cache_layout(c);
+    uint8_t* b = cache ? static_cast<uint8_t*>(const_cast<void*>(cache)) : sv + L.wcache;
+    for (int i = 0; i < 6; ++i) {
+        w.q[i] = b + C.q[i];
+        w.s[i] = b + C.s[i];
     }
     return w;
+}
+
+// Quantise W_gate, W_up, W_down into the weight codes w (both orientations).
+static cudaError_t quantize_weights(const moe_config_t& c, const void* Wg, const void* Wu, const void* Wd,
+                                    const WQ& w, cudaStream_t s)
+{
+    using T = __nv_bfloat16;
+    const int E = c.E, H = c.H, F = c.F;
+    const void* W[3] = {Wg, Wu, Wd};
+    const int R[3] = {H, H, F}, Cc[3] = {F, F, H};
+    for (int i = 0; i < 3; ++i) {
+        cudaError_t e;
+        if (c.dtype == MOE_MXFP8) {
+            // one pass: row codes (the data-gradient orientation) and in-place
+            // column codes (the forward orientation, K = R[i] per expert)
+            MxQuantJob j{static_cast<const T*>(W[i]), nullptr, E * R[i], Cc[i], 128, w.q[3 + i],
+                         static_cast<uint8_t*>(w.s[3 + i]), w.q[i], static_cast<uint8_t*>(w.s[i]), 2};
+            j.grp = R[i];
+            e = launch_mx_quant(j, s);
+        } else {
+            e = launch_quant(QuantJob{static_cast<const T*>(W[i]), nullptr, E * R[i], Cc[i], 128, w.q[i],
+                                      static_cast<float*>(w.s[i]), 1, nullptr, nullptr, 0}, s);
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // Same stages as the bf16 layer; the expert GEMMs take E4M3 operands with
@@ -686,15 +717,8 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     // (moe_quantize_weights) are read from the caller's cache; otherwise the
     // bf16 weights are quantised into the saved buffer for this step.
     const WQ wq = weight_codes(c, L, sv, a->weight_cache);
-    if (!a->weight_cache) {
-        auto wquant = [&](const void* W, int R, int C, uint8_t* q, float* sc) {
-            return launch_quant(QuantJob{static_cast<const T*>(W), nullptr, E * R, C, 128, q, sc, 1, nullptr,
-                                         nullptr, 0}, s);
-        };
-        MOE_STAGE(ST_WQUANT, wquant(a->W_gate, H, F, wq.gq, wq.gs));
-        MOE_STAGE(ST_WQUANT, wquant(a->W_up, H, F, wq.uq, wq.us));
-        MOE_STAGE(ST_WQUANT, wquant(a->W_down, F, H, wq.dq, wq.ds));
-    }
+    if (!a->weight_cache)
+        MOE_STAGE(ST_WQUANT, quantize_weights(c, a->W_gate, a->W_up, a->W_down, wq, s));
     GemmDesc d;
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
@@ -702,8 +726,8 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(sv, L.Xq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(sv, L.sX); d.lds_a = H / 128;
-    d.B0 = wq.gq; d.B1 = wq.uq; d.ldb = F; d.b_rows = E * H; d.b_kmajor = 0;
-    d.SB0 = wq.gs; d.SB1 = wq.us;
+    d.B0 = wq.q[0]; d.B1 = wq.q[1]; d.ldb = F; d.b_rows = E * H; d.b_kmajor = 0;
+    d.SB0 = static_cast<float*>(wq.s[0]); d.SB1 = static_cast<float*>(wq.s[1]);
     d.O0 = A; d.O1 = U; d.O2 = Hh; d.ldo = F; d.status = status;
     if (L.fold) { d.gates = gates; d.slot_of = slotof; }   // Hh = g silu(A) U
     MOE_STAGE(ST_FC1, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
@@ -715,7 +739,7 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.hq); d.lda = F; d.a_rows = Rp; d.SA0 = f32(ws, L.sh); d.lds_a = F / 128;
-    d.B0 = wq.dq; d.ldb = H; d.b_rows = E * F; d.SB0 = wq.ds; d.b_kmajor = 0;
+    d.B0 = wq.q[2]; d.ldb = H; d.b_rows = E * F; d.SB0 = static_cast<float*>(wq.s[2]); d.b_kmajor = 0;
     d.O0 = Yp; d.ldo = H; d.status = status;
     MOE_STAGE(ST_FC2, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
     MOE_STAGE(ST_COMBINE, launch_combine<T>(Yp, nullptr, rowof, L.fold ? nullptr : gates, T_, H, k,
@@ -782,7 +806,7 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.dYq); d.lda = H; d.a_rows = Rp; d.SA0 = f32(ws, L.sdY); d.lds_a = H / 128;
-    d.B0 = wq.dq; d.ldb = H; d.b_rows = E * F; d.SB0 = wq.ds; d.b_kmajor = 1;
+    d.B0 = wq.q[5]; d.ldb = H; d.b_rows = E * F; d.SB0 = static_cast<float*>(wq.s[5]); d.b_kmajor = 1;
     d.X0 = A; d.X1 = U; d.O0 = dA; d.O1 = dU; d.ldo = F; d.status = status;
     if (L.fold) {
         d.gates = gates; d.slot_of = slotof; d.dg_part = dgpart; d.dg_ld = F / 64;
@@ -817,8 +841,8 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = u8(ws, L.dAq); d.A1 = u8(ws, L.dUq); d.lda = F; d.a_rows = Rp;
     d.SA0 = f32(ws, L.sdA); d.SA1 = f32(ws, L.sdU); d.lds_a = F / 128;
-    d.B0 = wq.gq; d.B1 = wq.uq; d.ldb = F; d.b_rows = E * H; d.b_kmajor = 1;
-    d.SB0 = wq.gs; d.SB1 = wq.us;
+    d.B0 = wq.q[3]; d.B1 = wq.q[4]; d.ldb = F; d.b_rows = E * H; d.b_kmajor = 1;
+    d.SB0 = static_cast<float*>(wq.s[3]); d.SB1 = static_cast<float*>(wq.s[4]);
     d.O0 = dXp; d.ldo = H; d.status = status;
     MOE_STAGE(ST_FC1_DGRAD, launch_gemm_fp8(d, L.MT_max, p->num_sms, s));
     // fc1 wgrad: dWg[e] = Xp_e^T dA_e, dWu[e] = Xp_e^T dU_e
@@ -845,6 +869,211 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     return MOE_OK;
 }
 
+// ------------------------------------------------------------------ MXFP8
+// The blockwise-FP8 layer's stages with the MXFP8 recipe: every GEMM operand
+// is quantised in 32-element blocks along the GEMM's K with power-of-two
+// scales (quant_mx.cu), so the activations and gradients that feed a data
+// GEMM and a weight-gradient GEMM get one quantisation per orientation, like
+// the weights, and the grouped GEMMs apply the scales in the tensor cores.
+static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, uint8_t* sv,
+                                    uint8_t* ws, cudaStream_t s)
+{
+    using T = __nv_bfloat16;
+    const moe_config_t& c = p->cfg;
+    const Layout L = make_layout(c, T_);
+    const int H = c.H, E = c.E, k = c.top_k, F = c.F, Rp = L.Rp_max;
+    DeviceStatus* status = reinterpret_cast<DeviceStatus*>(ws + L.status);
+    int* topk = reinterpret_cast<int*>(sv + L.topk);
+    float* gates = reinterpret_cast<float*>(sv + L.gates);
+    float* selsc = reinterpret_cast<float*>(sv + L.selsc);
+    int* counts = reinterpret_cast<int*>(sv + L.counts);
+    int* kept = reinterpret_cast<int*>(sv + L.kept);
+    int* poff = reinterpret_cast<int*>(sv + L.poff);
+    int* meta = reinterpret_cast<int*>(sv + L.meta);
+    int* tiletab = reinterpret_cast<int*>(sv + L.tiletab);
+    int* pairtab = reinterpret_cast<int*>(sv + L.pairtab);
+    int* rowof = reinterpret_cast<int*>(sv + L.rowof);
+    int* slotof = reinterpret_cast<int*>(sv + L.slotof);
+    T* A = reinterpret_cast<T*>(sv + L.A);
+    T* U = reinterpret_cast<T*>(sv + L.U);
+    T* Hh = reinterpret_cast<T*>((L.fold ? ws : sv) + L.Hh);
+    T* Yp = reinterpret_cast<T*>((L.fold ? ws : sv) + L.Yp);
+    const T* x = static_cast<const T*>(a->x);
+
+    MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
+    MOE_STAGE(ST_ROUTER, launch_router<T>(x, a->Wr, a->b, T_, H, E, k, c.score, topk, gates, selsc,
+                                          reinterpret_cast<int*>(ws + L.hist), s, a->replay_topk, status,
+                                          reinterpret_cast<float*>(ws + L.zpart),
+                                          router_zpart_floats(T_, H, E)));
+    MOE_STAGE(ST_SCAN, launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
+                                   reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab,
+                                   pairtab + L.MT_max, capacity(c, T_), kept,
+                                   reinterpret_cast<int*>(sv + L.eorder)));
+    MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
+    MOE_STAGE(ST_PERMUTE, launch_mx_permute(x, rowof, poff, counts, T_, H, E, k, sv + L.Xq, sv + L.sX, s));
+    const WQ wq = weight_codes(c, L, sv, a->weight_cache);
+    if (!a->weight_cache)
+        MOE_STAGE(ST_WQUANT, quantize_weights(c, a->W_gate, a->W_up, a->W_down, wq, s));
+    auto xs = [](void* v) { return static_cast<const uint8_t*>(v); };
+    GemmDesc d;
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
+    d.N = F; d.K = H; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.A0 = sv + L.Xq; d.lda = H; d.a_rows = Rp; d.XA0 = sv + L.sX;
+    d.B0 = wq.q[0]; d.B1 = wq.q[1]; d.ldb = F; d.b_rows = E * H; d.b_kmajor = 0;
+    d.XB0 = xs(wq.s[0]); d.XB1 = xs(wq.s[1]);
+    d.O0 = A; d.O1 = U; d.O2 = Hh; d.ldo = F; d.status = status;
+    if (L.fold) { d.gates = gates; d.slot_of = slotof; }   // Hh = g silu(A) U
+    MOE_STAGE(ST_FC1, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    {
+        MxQuantJob j{Hh, meta + 1, Rp, F, Rp, ws + L.hq, ws + L.sh, nullptr, nullptr, 0};
+        MOE_STAGE(ST_QROWS, launch_mx_quant(j, s));
+    }
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
+    d.N = H; d.K = F; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.A0 = ws + L.hq; d.lda = F; d.a_rows = Rp; d.XA0 = ws + L.sh;
+    d.B0 = wq.q[2]; d.ldb = H; d.b_rows = E * F; d.XB0 = xs(wq.s[2]); d.b_kmajor = 0;
+    d.O0 = Yp; d.ldo = H; d.status = status;
+    MOE_STAGE(ST_FC2, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    MOE_STAGE(ST_COMBINE, launch_combine<T>(Yp, nullptr, rowof, L.fold ? nullptr : gates, T_, H, k,
+                                            static_cast<T*>(a->y), s));
+
+    if (a->topk_idx) MOE_CUDA(cudaMemcpyAsync(a->topk_idx, topk, sizeof(int) * L.R, cudaMemcpyDeviceToDevice, s));
+    if (a->gates) MOE_CUDA(cudaMemcpyAsync(a->gates, gates, sizeof(float) * L.R, cudaMemcpyDeviceToDevice, s));
+    if (a->counts) MOE_CUDA(cudaMemcpyAsync(a->counts, counts, sizeof(int) * E, cudaMemcpyDeviceToDevice, s));
+    if (a->offsets) MOE_CUDA(cudaMemcpyAsync(a->offsets, poff, sizeof(int) * (E + 1), cudaMemcpyDeviceToDevice, s));
+    if (a->row_of) MOE_CUDA(cudaMemcpyAsync(a->row_of, rowof, sizeof(int) * L.R, cudaMemcpyDeviceToDevice, s));
+    return MOE_OK;
+}
+
+static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
+                                     const uint8_t* svc, uint8_t* ws, cudaStream_t s)
+{
+    using T = __nv_bfloat16;
+    const moe_config_t& c = p->cfg;
+    const Layout L = make_layout(c, T_);
+    const int H = c.H, E = c.E, k = c.top_k, F = c.F, Rp = L.Rp_max;
+    uint8_t* sv = const_cast<uint8_t*>(svc);   // only read below
+    DeviceStatus* status = reinterpret_cast<DeviceStatus*>(ws + L.status);
+    const int* topk = reinterpret_cast<const int*>(sv + L.topk);
+    const float* gates = reinterpret_cast<const float*>(sv + L.gates);
+    const float* selsc = reinterpret_cast<const float*>(sv + L.selsc);
+    const int* counts = reinterpret_cast<const int*>(sv + L.counts);
+    const int* kept = reinterpret_cast<const int*>(sv + L.kept);
+    const int* poff = reinterpret_cast<const int*>(sv + L.poff);
+    const int* meta = reinterpret_cast<const int*>(sv + L.meta);
+    const int* tiletab = reinterpret_cast<const int*>(sv + L.tiletab);
+    const int* pairtab = reinterpret_cast<const int*>(sv + L.pairtab);
+    const int* eorder = reinterpret_cast<const int*>(sv + L.eorder);
+    const int* rowof = reinterpret_cast<const int*>(sv + L.rowof);
+    const int* slotof = reinterpret_cast<const int*>(sv + L.slotof);
+    const T* A = reinterpret_cast<const T*>(sv + L.A);
+    const T* U = reinterpret_cast<const T*>(sv + L.U);
+    T* Hh = reinterpret_cast<T*>((L.fold ? ws : sv) + L.Hh);   // folded: recomputed below
+    const T* Yp = reinterpret_cast<const T*>(sv + L.Yp);
+    T* dYp = reinterpret_cast<T*>(ws + L.dYp);
+    T* dA = reinterpret_cast<T*>(ws + L.dA);
+    T* dU = reinterpret_cast<T*>(ws + L.dU);
+    T* dXp = reinterpret_cast<T*>(ws + L.dXp);
+    float* dz = reinterpret_cast<float*>(ws + L.dz);
+    float* WrT = reinterpret_cast<float*>(ws + L.WrT);
+    float* dgpart = reinterpret_cast<float*>(ws + L.dgpart);
+    const T* dY = static_cast<const T*>(a->dY);
+    const WQ wq = weight_codes(c, L, sv, a->weight_cache);
+    auto xs = [](void* v) { return static_cast<const uint8_t*>(v); };
+
+    MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
+    if (L.fold)
+        MOE_STAGE(ST_GATEGRAD, launch_permute<T>(dY, rowof, poff, counts, T_, H, E, k, dYp, s));
+    else
+        MOE_STAGE(ST_GATEGRAD, launch_gate_grad<T>(dY, Yp, rowof, topk, gates, selsc, poff, counts, T_, H,
+                                                   E, k, c.score, dYp, dz, s));
+    // dYp once: row codes (fc2 dgrad, K = H) and transposed column codes (fc2 wgrad, K = tokens)
+    {
+        MxQuantJob j{dYp, meta + 1, Rp, H, Rp, ws + L.dYq, ws + L.sdY, ws + L.dYpTq, ws + L.sdYpT, 1};
+        MOE_STAGE(ST_QROWS, launch_mx_quant(j, s));
+    }
+    GemmDesc d;
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_BWD; d.dual = DUAL_NONE;
+    d.N = F; d.K = H; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.A0 = ws + L.dYq; d.lda = H; d.a_rows = Rp; d.XA0 = ws + L.sdY;
+    d.B0 = wq.q[5]; d.ldb = H; d.b_rows = E * F; d.XB0 = xs(wq.s[5]); d.b_kmajor = 1;
+    d.X0 = A; d.X1 = U; d.O0 = dA; d.O1 = dU; d.ldo = F; d.status = status;
+    if (L.fold) {
+        d.gates = gates; d.slot_of = slotof; d.dg_part = dgpart; d.dg_ld = F / 64;
+        d.O2 = Hh;   // g h, recomputed for the fc2 weight gradient
+    }
+    MOE_STAGE(ST_FC2_DGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    if (L.fold)
+        MOE_STAGE(ST_GATEDZ, launch_gate_dz(dgpart, F / 64, rowof, gates, selsc, T_, k, c.score, dz, s));
+    // fc2 wgrad: dWd[e] = h_e^T dYp_e
+    {
+        MxQuantJob j{Hh, meta + 1, Rp, F, Rp, nullptr, nullptr, ws + L.hTq, ws + L.shT, 1};
+        MOE_STAGE(ST_QT, launch_mx_quant(j, s));
+    }
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
+    d.N = H; d.M_out = F; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.A0 = ws + L.hTq; d.lda = Rp; d.XA0 = ws + L.shT;
+    d.B0 = ws + L.dYpTq; d.ldb = Rp; d.XB0 = ws + L.sdYpT;
+    d.rows_cap = Rp; d.expert_order = eorder;
+    d.O0 = a->dW_down; d.ldo = H; d.o_estride = (long long)F * H; d.status = status;
+    MOE_STAGE(ST_FC2_WGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    // dA, dU once each: row codes (fc1 dgrad, K = F) and transposed column codes (fc1 wgrad)
+    {
+        MxQuantJob ja{dA, meta + 1, Rp, F, Rp, ws + L.dAq, ws + L.sdA, ws + L.dATq, ws + L.sdAT, 1};
+        MOE_STAGE(ST_QROWS, launch_mx_quant(ja, s));
+        MxQuantJob ju{dU, meta + 1, Rp, F, Rp, ws + L.dUq, ws + L.sdU, ws + L.dUTq, ws + L.sdUT, 1};
+        MOE_STAGE(ST_QROWS, launch_mx_quant(ju, s));
+    }
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
+    d.N = H; d.K = F; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.A0 = ws + L.dAq; d.A1 = ws + L.dUq; d.lda = F; d.a_rows = Rp;
+    d.XA0 = ws + L.sdA; d.XA1 = ws + L.sdU;
+    d.B0 = wq.q[3]; d.B1 = wq.q[4]; d.ldb = F; d.b_rows = E * H; d.b_kmajor = 1;
+    d.XB0 = xs(wq.s[3]); d.XB1 = xs(wq.s[4]);
+    d.O0 = dXp; d.ldo = H; d.status = status;
+    MOE_STAGE(ST_FC1_DGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    // fc1 wgrad: the permuted rows are token rows of x (no bf16 copy of them is kept)
+    {
+        MxQuantJob j{static_cast<const T*>(a->x), meta + 1, Rp, H, Rp, nullptr, nullptr, ws + L.XpTq,
+                     ws + L.sXpT, 1};
+        j.gather_slot = slotof;
+        j.gather_k = k;
+        MOE_STAGE(ST_QT, launch_mx_quant(j, s));
+    }
+    memset(&d, 0, sizeof d);
+    d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
+    d.N = F; d.M_out = H; d.E = E;
+    d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.A0 = ws + L.XpTq; d.lda = Rp; d.XA0 = ws + L.sXpT;
+    d.B0 = ws + L.dATq; d.B1 = ws + L.dUTq; d.ldb = Rp;
+    d.XB0 = ws + L.sdAT; d.XB1 = ws + L.sdUT;
+    d.rows_cap = Rp; d.expert_order = eorder;
+    d.O0 = a->dW_gate; d.O1 = a->dW_up; d.ldo = F; d.o_estride = (long long)H * F; d.status = status;
+    MOE_STAGE(ST_FC1_WGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    MOE_STAGE(ST_ROUTER_WGRAD, launch_router_wgrad<T>(static_cast<const T*>(a->x), slotof, poff, meta,
+                                   L.MT_max, dz, H, E, k, reinterpret_cast<float*>(ws + L.wrpart), a->dWr, s));
+    MOE_STAGE(ST_TRANSPOSE, launch_transpose_f32(a->Wr, H, E, WrT, s));
+    MOE_STAGE(ST_UNPERMUTE, launch_unpermute_reduce<T>(dXp, nullptr, rowof, topk, dz, WrT, T_, H, k,
+                                                       static_cast<T*>(a->dX), s));
+    return MOE_OK;
+}
+
 static moe_status_t check_call(moe_plan_t plan, int T, const void* saved, size_t saved_bytes,
                                const void* ws, size_t ws_bytes)
 {
@@ -863,7 +1092,7 @@ moe_status_t moe_forward(moe_plan_t plan, int T, const moe_fwd_args_t* a, void* 
     if (st != MOE_OK) return st;
     const bool shared = plan->cfg.Fs > 0;
     // a weight cache (FP8 plans only) replaces the bf16 expert weights
-    if (a->weight_cache && plan->cfg.dtype != MOE_FP8_BLOCK) return MOE_ERR_INVALID_ARG;
+    if (a->weight_cache && !fp8_recipe(plan->cfg)) return MOE_ERR_INVALID_ARG;
     const bool wneed = a->weight_cache == nullptr;
     if (!a->x || !a->Wr || (wneed && (!a->W_gate || !a->W_up || !a->W_down)) || !a->y)
         return MOE_ERR_INVALID_ARG;
@@ -882,6 +1111,8 @@ moe_status_t moe_forward(moe_plan_t plan, int T, const moe_fwd_args_t* a, void* 
         return forward_impl<float>(plan, T, a, static_cast<uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
     if (plan->cfg.dtype == MOE_FP8_BLOCK)
         return forward_fp8_impl(plan, T, a, static_cast<uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
+    if (plan->cfg.dtype == MOE_MXFP8)
+        return forward_mx_impl(plan, T, a, static_cast<uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
     return forward_impl<__nv_bfloat16>(plan, T, a, static_cast<uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
 }
 
@@ -892,7 +1123,7 @@ moe_status_t moe_backward(moe_plan_t plan, int T, const moe_bwd_args_t* a, const
     moe_status_t st = check_call(plan, T, saved, saved_bytes, ws, ws_bytes);
     if (st != MOE_OK) return st;
     const bool shared = plan->cfg.Fs > 0;
-    if (a->weight_cache && plan->cfg.dtype != MOE_FP8_BLOCK) return MOE_ERR_INVALID_ARG;
+    if (a->weight_cache && !fp8_recipe(plan->cfg)) return MOE_ERR_INVALID_ARG;
     const bool wneed = a->weight_cache == nullptr;
     if (!a->dY || !a->x || !a->Wr || (wneed && (!a->W_gate || !a->W_up || !a->W_down)) || !a->dX ||
         !a->dWr || !a->dW_gate || !a->dW_up || !a->dW_down)
@@ -912,6 +1143,8 @@ moe_status_t moe_backward(moe_plan_t plan, int T, const moe_bwd_args_t* a, const
         return backward_impl<float>(plan, T, a, static_cast<const uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
     if (plan->cfg.dtype == MOE_FP8_BLOCK)
         return backward_fp8_impl(plan, T, a, static_cast<const uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
+    if (plan->cfg.dtype == MOE_MXFP8)
+        return backward_mx_impl(plan, T, a, static_cast<const uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
     return backward_impl<__nv_bfloat16>(plan, T, a, static_cast<const uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
 }
 
@@ -978,22 +1211,31 @@ moe_status_t moe_quantize_weights(moe_plan_t plan, const void* W_gate, const voi
 {
     if (!plan || !W_gate || !W_up || !W_down || !cache) return MOE_ERR_INVALID_ARG;
     const moe_config_t& c = plan->cfg;
-    if (c.dtype != MOE_FP8_BLOCK) return MOE_ERR_UNSUPPORTED;
+    if (!fp8_recipe(c)) return MOE_ERR_UNSUPPORTED;
     if (!aligned16(W_gate) || !aligned16(W_up) || !aligned16(W_down) || !aligned16(cache))
         return MOE_ERR_MISALIGNED;
-    const WeightCache C = cache_layout(c);
-    if (cache_bytes < C.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (cache_bytes < cache_layout(c).bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
     DeviceGuard g(plan->device);
     if (!g.ok) return MOE_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    uint8_t* b = static_cast<uint8_t*>(cache);
-    const int E = c.E, H = c.H, F = c.F;
-    auto wquant = [&](const void* W, int R, int Cc, size_t q, size_t sc) {
-        return launch_quant(QuantJob{static_cast<const __nv_bfloat16*>(W), nullptr, E * R, Cc, 128, b + q,
-                                     reinterpret_cast<float*>(b + sc), 1, nullptr, nullptr, 0}, s);
-    };
-    cudaError_t e = wquant(W_gate, H, F, C.WgQ, C.sWg);
-    if (e == cudaSuccess) e = wquant(W_up, H, F, C.WuQ, C.sWu);
-    if (e == cudaSuccess) e = wquant(W_down, F, H, C.WdQ, C.sWd);
+    Layout L;
+    memset(&L, 0, sizeof L);
+    const WQ w = weight_codes(c, L, nullptr, cache);
+    return quantize_weights(c, W_gate, W_up, W_down, w, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_mx_quantize(int rows, int cols, const void* in, uint8_t* codes, uint8_t* scales,
+                             uint8_t* codes_c, uint8_t* scales_c, int col_transposed, moe_stream_t stream)
+{
+    if (rows < 1 || cols < 1 || rows % 128 || cols % 128 || !in) return MOE_ERR_INVALID_ARG;
+    if ((codes == nullptr) != (scales == nullptr) || (codes_c == nullptr) != (scales_c == nullptr) ||
+        (!codes && !codes_c) || (col_transposed != 0 && col_transposed != 1))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(in) || (codes && !aligned16(codes)) || (codes_c && !aligned16(codes_c)))
+        return MOE_ERR_MISALIGNED;
+    MxQuantJob j{static_cast<const __nv_bfloat16*>(in), nullptr, rows, cols, rows, codes, scales, codes_c,
+                 scales_c, col_transposed ? 1 : 2};
+    j.grp = rows;
+    const cudaError_t e = launch_mx_quant(j, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -1,0 +1,691 @@
+// gemm_mx.cu -- persistent grouped GEMM on MXFP8 operands (E4M3 values, one
+// UE8M0 power-of-two scale per 32 consecutive values along K, for both A and
+// B) with fp32 accumulation, for the MOE_MXFP8 layer.
+//
+// "Scalable Training of Mixture-of-Experts Models with Megatron Core", §5
+// (Platform-specific recipes): MXFP8, the default FP8 recipe on Blackwell,
+// with 1x32 granularity. The tensor cores apply the scales inside the MMA
+// (tcgen05.mma.kind::mxf8f6f4.block_scale): each MMA of K = 32 multiplies
+// the products of row m of A and column n of B by 2^(eA[m] + eB[n]) before
+// accumulating, so the whole K loop accumulates in tensor memory, with no
+// per-block promotion in registers (the blockwise-FP8 engine's limit).
+//
+// Ten warps per CTA: warp 0 loads each 128-deep k block (A: 128 rows x 128
+// bytes, B: 256 rows, 128-byte swizzle, by TMA; the operands' scale atoms,
+// 512 bytes each, by bulk copies); warp 1 allocates tensor memory and one
+// thread issues, per k block, tcgen05.cp of the scale atoms into a ring of
+// tensor-memory columns and four N = 256 MMAs (K = 32 each, the scale
+// sub-block chosen by the instruction descriptor's scale-factor IDs);
+// warps 2-9 wait for a finished tile, copy its 128 x 256 fp32 accumulator
+// into registers (two warps per TMEM lane quarter, 128 columns each), release
+// it to the next tile and run the fused epilogue from registers.
+//
+// Scale atoms (quant_mx.cu): an operand read as [rows][K] keeps, per 128-row
+// tile and 128-deep K block, 512 bytes whose byte 16 (m % 32) + 4 (m / 32) + j
+// is the scale of tile row m and 32-deep sub-block j. tcgen05.cp.32x128b.warpx4
+// puts the atom's 32 rows of 16 bytes into every TMEM lane quarter, four
+// 32-bit columns each: lane 32 q + r, column c + j holds the scales of rows
+// r + 32 j, one byte per sub-block.
+#include "internal.h"
+#include "epilogue.cuh"
+#include "ptx.cuh"
+
+#include <cudaTypedefs.h>
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int XBM = 128, XBK = 128, XBN = 256;   // rows per CTA, K block (bytes), MMA N
+constexpr int kXThreads = 320;
+constexpr int kXSmemMax = 232448;
+constexpr int kXGroupN = 16;
+constexpr int kAccCols = 256;                    // the accumulator
+constexpr int kSfCols = 12;                      // scale columns of one stage: A 4, B 2 x 4
+
+struct XCfg {
+    static constexpr int A_BYTES = XBM * XBK;
+    static constexpr int B_BYTES = XBN * XBK;
+    static constexpr int SF_BYTES = 3 * 512;     // A atom, then B atoms of the two 128-column parts
+    static constexpr int STAGE = A_BYTES + B_BYTES + 2048;   // (SF region padded to keep 1 KB alignment)
+    static constexpr int STAGES = (kXSmemMax - 1024 - 256) / STAGE;
+    static constexpr int SMEM = 1024 + STAGES * STAGE + 256;
+};
+static_assert(kAccCols + kSfCols * XCfg::STAGES <= 512, "tensor memory");
+
+// kind::mxf8f6f4 instruction descriptor: E4M3 A and B (format 0), fp32 D,
+// UE8M0 scales (bit 23), A K-major, B K-major or MN-major (bit 16), the
+// scale-factor IDs of A (bits 29-30) and B (bits 4-5) select the byte of
+// each 32-bit scale column (the 32-deep sub-block).
+__host__ __device__ constexpr uint32_t idesc_mx(int N, int M, bool b_mn, int sf_id)
+{
+    return ((uint32_t)sf_id << 4) | (b_mn ? (1u << 16) : 0u) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(M >> 4) << 24) | ((uint32_t)sf_id << 29);
+}
+
+__device__ __forceinline__ void mma_mx(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t sfa, uint32_t sfb, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n"
+        "}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// 32 rows x 16 bytes of shared memory -> every TMEM lane quarter, 4 columns
+__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Shared-memory descriptor of 16-byte rows stored contiguously (no swizzle:
+// 8-row core matrices 128 bytes apart)
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((128u >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((128u >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// one contiguous global -> shared copy, completion counted on `bar`
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v)
+{
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+    return f;
+}
+// 8 fp32 -> 8 bf16 in one 16-byte store
+__device__ __forceinline__ void st8(__nv_bfloat16* dst, const float* v)
+{
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    *reinterpret_cast<uint4*>(dst) = u;
+}
+// eight consecutive accumulators (four packed pairs) starting at pair p
+__device__ __forceinline__ void get8(const uint64_t* acc, int p, float* v)
+{
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = unpack2(acc[p + i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+
+struct XTile {
+    int e, m, n, row0, kblocks, kb0, valid_end, alloc_end;
+};
+
+template <int DUAL, int SCHED>
+__device__ __forceinline__ void xtile_counts(const GemmDesc& d, int& num_m, int& num_n, int& total)
+{
+    constexpr int NW = (DUAL == DUAL_N) ? XBN / 2 : XBN;
+    num_n = (d.N + NW - 1) / NW;
+    if (SCHED == SCHED_ROWS) {
+        num_m = d.meta[0];
+        total = num_m * num_n;
+    } else {
+        num_m = d.M_out / XBM;
+        total = d.E * num_m * num_n;
+    }
+}
+
+// Row-scheduled tiles go expert by expert; within an expert, groups of
+// kXGroupN column tiles walk its 128-row tiles. Weight-gradient tiles take
+// the experts longest first (the order the scan wrote) and walk each
+// expert's (m, n) grid with the smaller count fastest.
+template <int DUAL, int SCHED>
+__device__ __forceinline__ XTile xdecode(const GemmDesc& d, int w, int num_m, int num_n)
+{
+    XTile t;
+    if (SCHED == SCHED_ROWS) {
+        const int q = w / num_n;
+        const int e = d.tile_tab[q];
+        const int u0 = d.poff[e] / XBM;
+        const int nu = d.poff[e + 1] / XBM - u0;
+        w -= u0 * num_n;
+        const int group = w / (nu * kXGroupN);
+        const int r = w - group * nu * kXGroupN;
+        const int gsz = min(kXGroupN, num_n - group * kXGroupN);
+        t.m = u0 + r / gsz;
+        t.n = group * kXGroupN + r % gsz;
+        t.e = e;
+        t.row0 = t.m * XBM;
+        t.valid_end = d.poff[t.e] + d.counts[t.e];
+        t.alloc_end = d.poff[t.e + 1];
+        t.kblocks = ((DUAL == DUAL_K) ? 2 * d.K : d.K) / XBK;
+        t.kb0 = 0;
+    } else {
+        const int per = num_m * num_n;
+        const int eo = w / per;
+        t.e = d.expert_order ? d.expert_order[eo] : eo;
+        const int r = w - eo * per;
+        if (num_n < num_m) {
+            t.n = r % num_n;
+            t.m = r / num_n;
+        } else {
+            t.m = r % num_m;
+            t.n = r / num_m;
+        }
+        t.row0 = d.poff[t.e];
+        t.kb0 = t.row0 / XBK;
+        t.kblocks = (d.poff[t.e + 1] - t.row0) / XBK;
+        t.valid_end = t.alloc_end = 0;
+    }
+    return t;
+}
+
+template <int EPI, int SCHED, int DUAL, bool B_MN>
+__global__ void __launch_bounds__(kXThreads, 1)
+gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
+               const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
+               const GemmDesc d)
+{
+    using C = XCfg;
+    constexpr int NW = (DUAL == DUAL_N) ? XBN / 2 : XBN;   // output columns per tile
+    static_assert(!B_MN || (SCHED == SCHED_ROWS && DUAL != DUAL_K), "MN-major B: forward GEMMs");
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+    // full[S], empty[S], accf, acce, final
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 3);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bar0 = ptx::smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    const uint32_t accf_bar = bar0 + 8u * (2 * C::STAGES);
+    const uint32_t acce_bar = bar0 + 8u * (2 * C::STAGES + 1);
+    const uint32_t final_bar = bar0 + 8u * (2 * C::STAGES + 2);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        ptx::mbar_init(accf_bar, 1);
+        ptx::mbar_init(acce_bar, 8);   // the eight epilogue warps
+        ptx::mbar_init(final_bar, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&mA0);
+        ptx::prefetch_tmap(&mB0);
+        if (DUAL != DUAL_NONE) {
+            ptx::prefetch_tmap(&mA1);
+            ptx::prefetch_tmap(&mB1);
+        }
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    int num_m, num_n, total;
+    xtile_counts<DUAL, SCHED>(d, num_m, num_n, total);
+    auto wait_uniform = [&](uint32_t bar, uint32_t parity, int where) -> bool {
+        int ok = 1;
+        if (lane == 0) ok = ptx::wait_bounded(bar, parity, abort_flag, d.status, where) ? 1 : 0;
+        return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
+    // the 128-row tiles of B's two 128-column parts (part 1: the same columns
+    // of B1 for DUAL_N, else the next 128 columns) and whether part 1 exists
+    auto bparts = [&](const XTile& t, int& nb_lo, int& nb_hi, bool& hi_ok) {
+        nb_lo = (DUAL == DUAL_N) ? t.n : 2 * t.n;
+        nb_hi = (DUAL == DUAL_N) ? t.n : 2 * t.n + 1;
+        hi_ok = (DUAL == DUAL_N) || nb_hi < d.N / 128;
+    };
+
+    if (warp == 0) {
+        // ---------------------------------------------------- loads
+        uint32_t it = 0;
+        const int kb_half = d.K / XBK;
+        bool ok = true;
+        for (int w = blockIdx.x; ok && w < total; w += gridDim.x) {
+            const XTile t = xdecode<DUAL, SCHED>(d, w, num_m, num_n);
+            int nb_lo, nb_hi;
+            bool hi_ok;
+            bparts(t, nb_lo, nb_hi, hi_ok);
+            for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
+                const int s = it % C::STAGES;
+                const uint32_t ph = (it / C::STAGES) & 1u;
+                if (!wait_uniform(empty_bar(s), ph ^ 1u, 21)) { ok = false; break; }
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(full_bar(s), C::A_BYTES + C::B_BYTES + C::SF_BYTES);
+                    const uint32_t a_dst = ptx::smem_u32(smem + s * C::STAGE);
+                    const uint32_t b_dst = a_dst + C::A_BYTES;
+                    const uint32_t sf_dst = b_dst + C::B_BYTES;
+                    int kx, arow, brow;
+                    const CUtensorMap* am = &mA0;
+                    const CUtensorMap* bm = &mB0;
+                    const uint8_t* xa = d.XA0;
+                    const uint8_t* xb = d.XB0;
+                    size_t a_atom, b_atom_lo, b_atom_hi;
+                    if (SCHED == SCHED_ROWS) {
+                        const bool second = (DUAL == DUAL_K) && kb >= kb_half;
+                        const int kk = second ? kb - kb_half : kb;
+                        kx = kk * XBK;
+                        arow = t.row0;
+                        brow = t.e * d.N + t.n * NW;
+                        if (second) { am = &mA1; bm = &mB1; xa = d.XA1; xb = d.XB1; }
+                        const size_t KB = (size_t)(d.K / XBK);
+                        const size_t ebase = (size_t)t.e * (d.N / 128);
+                        a_atom = ((size_t)t.m * KB + kk) * 512;
+                        b_atom_lo = ((ebase + nb_lo) * KB + kk) * 512;
+                        b_atom_hi = ((ebase + (hi_ok ? nb_hi : nb_lo)) * KB + kk) * 512;
+                    } else {
+                        const int kg = t.kb0 + kb;
+                        kx = kg * XBK;
+                        arow = t.m * XBM;
+                        brow = t.n * NW;
+                        const size_t KB = (size_t)(d.rows_cap / XBK);
+                        a_atom = ((size_t)t.m * KB + kg) * 512;
+                        b_atom_lo = ((size_t)nb_lo * KB + kg) * 512;
+                        b_atom_hi = ((size_t)(hi_ok ? nb_hi : nb_lo) * KB + kg) * 512;
+                    }
+                    ptx::tma_load_2d(a_dst, am, full_bar(s), kx, arow);
+                    const CUtensorMap* p0 = (DUAL == DUAL_N) ? &mB0 : bm;
+                    const CUtensorMap* p1 = (DUAL == DUAL_N) ? &mB1 : bm;
+                    const int r1 = (DUAL == DUAL_N) ? brow : brow + 128;
+                    if (B_MN) {
+                        const int n0 = t.n * NW;
+                        const int c1 = (DUAL == DUAL_N) ? n0 : n0 + 128;
+                        const int krow = t.e * d.K + kx;
+                        ptx::tma_load_2d(b_dst, p0, full_bar(s), n0, krow);
+                        ptx::tma_load_2d(b_dst + 128 * XBK, p1, full_bar(s), c1, krow);
+                    } else {
+                        ptx::tma_load_2d(b_dst, p0, full_bar(s), kx, brow);
+                        ptx::tma_load_2d(b_dst + 128 * XBK, p1, full_bar(s), kx, r1);
+                        ptx::tma_load_2d(b_dst + 64 * XBK, p0, full_bar(s), kx, brow + 64);
+                        ptx::tma_load_2d(b_dst + 192 * XBK, p1, full_bar(s), kx, r1 + 64);
+                    }
+                    const uint8_t* xb1 = (DUAL == DUAL_N) ? d.XB1 : xb;
+                    bulk_load(sf_dst, xa + a_atom, 512, full_bar(s));
+                    bulk_load(sf_dst + 512, xb + b_atom_lo, 512, full_bar(s));
+                    bulk_load(sf_dst + 1024, ((DUAL == DUAL_N) ? xb1 : xb) + b_atom_hi, 512, full_bar(s));
+                }
+                __syncwarp();
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------- MMA issuer
+        uint32_t it = 0, tc = 0;
+        bool ok = true;
+        for (int w = blockIdx.x; ok && w < total; w += gridDim.x) {
+            const XTile t = xdecode<DUAL, SCHED>(d, w, num_m, num_n);
+            if (t.kblocks == 0) continue;                  // an expert without rows: zeros
+            if (!wait_uniform(acce_bar, (tc & 1u) ^ 1u, 22)) { ok = false; break; }
+            ptx::tc_fence_after();
+            for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
+                const int s = it % C::STAGES;
+                const uint32_t ph = (it / C::STAGES) & 1u;
+                if (!wait_uniform(full_bar(s), ph, 23)) { ok = false; break; }
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t a_addr = ptx::smem_u32(smem + s * C::STAGE);
+                    const uint32_t b_addr = a_addr + C::A_BYTES;
+                    const uint32_t sf_addr = b_addr + C::B_BYTES;
+                    const uint32_t sfa = tmem_base + (uint32_t)(kAccCols + kSfCols * s);
+                    const uint32_t sfb = sfa + 4;
+                    tmem_cp_atom(sfa, smem_desc_plain(sf_addr));
+                    tmem_cp_atom(sfb, smem_desc_plain(sf_addr + 512));
+                    tmem_cp_atom(sfb + 4, smem_desc_plain(sf_addr + 1024));
+#pragma unroll
+                    for (int k = 0; k < XBK / 32; ++k) {
+                        const uint64_t ad = ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
+                        // MN-major: 32 rows of 128 bytes per K=32 step, stripes of
+                        // 128 columns 16 KB apart
+                        const uint64_t bd = B_MN ? ptx::smem_desc_sw128(b_addr + k * 4096, 128 * XBK, 1024)
+                                                 : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
+                        mma_mx(tmem_base, ad, bd, idesc_mx(XBN, XBM, B_MN, k), sfa, sfb, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    ptx::tc_commit(empty_bar(s));
+                }
+                __syncwarp();
+            }
+            if (ok && lane == 0) ptx::tc_commit(accf_bar);
+            __syncwarp();
+            ++tc;
+        }
+        // every MMA issued by this warp has completed before TMEM is freed
+        if (lane == 0) {
+            ptx::tc_commit(final_bar);
+            volatile int never = 0;
+            ptx::wait_bounded(final_bar, 0, &never, d.status, 24);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------- accumulator + epilogue
+        const int q = warp & 3;                  // TMEM lane quarter
+        const int hh = (warp - 2) >> 2;          // 64-column half of each part
+        const int r_in = q * 32 + lane;          // row of the CTA's 128
+        // This thread takes part-0 columns [64hh, +64) of its row into acc
+        // pairs 0-31 and part-1 columns [64hh, +64) into pairs 32-63; part 0 is
+        // tile columns [0, 128) (DUAL_N: B0), part 1 [128, 256) (DUAL_N: B1).
+        uint32_t tc = 0;
+        for (int w = blockIdx.x; w < total; w += gridDim.x) {
+            const XTile t = xdecode<DUAL, SCHED>(d, w, num_m, num_n);
+            const int arow = (SCHED == SCHED_ROWS) ? t.row0 + r_in : t.m * XBM + r_in;
+            const bool arow_ok = (SCHED == SCHED_ROWS) ? arow < d.a_rows : true;
+            (void)arow_ok;
+            int nb_lo, nb_hi;
+            bool hi_ok;
+            bparts(t, nb_lo, nb_hi, hi_ok);
+            const int col_lo = (DUAL == DUAL_N) ? t.n * NW + 64 * hh : nb_lo * 128 + 64 * hh;
+            const int col_hi = (DUAL == DUAL_N) ? col_lo : nb_hi * 128 + 64 * hh;
+            uint64_t acc[64];
+            if (t.kblocks > 0) {
+                if (!wait_uniform(accf_bar, tc & 1u, 25)) break;
+                ptx::tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + 64u * hh;
+#pragma unroll
+                for (int c = 0; c < 8; c += 2) {
+                    uint32_t r0[16], r1[16];
+                    tmem_ld16(taddr + (c < 4 ? 16 * c : 128 + 16 * (c - 4)), r0);
+                    tmem_ld16(taddr + (c < 4 ? 16 * (c + 1) : 128 + 16 * (c - 3)), r1);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        acc[8 * c + i] = pack2(r0[2 * i], r0[2 * i + 1]);
+                        acc[8 * (c + 1) + i] = pack2(r1[2 * i], r1[2 * i + 1]);
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                // relaxed: the accumulator has been read (tcgen05.wait::ld)
+                if (lane == 0) ptx::mbar_arrive_relaxed(acce_bar);
+                ++tc;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) acc[j] = 0ull;
+            }
+            // ---- epilogue from registers (pairs 0-31: part-0 columns, 32-63: part 1)
+            float v[8], x[8];
+            if (SCHED == SCHED_WGRAD) {
+                const size_t ob = (size_t)t.e * d.o_estride + (size_t)arow * d.ldo;
+                __nv_bfloat16* Olo = static_cast<__nv_bfloat16*>(d.O0) + ob + col_lo;
+                __nv_bfloat16* Ohi = static_cast<__nv_bfloat16*>(DUAL == DUAL_N ? d.O1 : d.O0) + ob + col_hi;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    get8(acc, 4 * j, v);
+                    st8(Olo + 8 * j, v);
+                }
+                if (hi_ok) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        get8(acc, 32 + 4 * j, v);
+                        st8(Ohi + 8 * j, v);
+                    }
+                }
+            } else if (arow < t.alloc_end) {
+                const bool valid = arow < t.valid_end;
+                const size_t orow = (size_t)arow * d.ldo;
+                // routing weight of the row when it is folded into h
+                const float grow = (d.gates && valid) ? d.gates[d.slot_of[arow]] : 1.f;
+                if (EPI == EPI_SWIGLU_FWD) {
+                    __nv_bfloat16* O0 = static_cast<__nv_bfloat16*>(d.O0) + orow + col_lo;
+                    __nv_bfloat16* O1 = static_cast<__nv_bfloat16*>(d.O1) + orow + col_lo;
+                    __nv_bfloat16* O2 = static_cast<__nv_bfloat16*>(d.O2) + orow + col_lo;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float hv[8];
+                        get8(acc, 4 * j, v);
+                        get8(acc, 32 + 4 * j, x);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            if (valid) {
+                                const SwigluFwd r(v[i], x[i]);
+                                hv[i] = r.h * grow;
+                            } else {
+                                v[i] = x[i] = hv[i] = 0.f;
+                            }
+                        }
+                        st8(O0 + 8 * j, v);
+                        st8(O1 + 8 * j, x);
+                        st8(O2 + 8 * j, hv);
+                    }
+                } else if (EPI == EPI_SWIGLU_BWD) {
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+                        if (part == 1 && !hi_ok) break;
+                        const size_t o = orow + (part ? col_hi : col_lo);
+                        const __nv_bfloat16* X0 = static_cast<const __nv_bfloat16*>(d.X0) + o;
+                        const __nv_bfloat16* X1 = static_cast<const __nv_bfloat16*>(d.X1) + o;
+                        __nv_bfloat16* O0 = static_cast<__nv_bfloat16*>(d.O0) + o;
+                        __nv_bfloat16* O1 = static_cast<__nv_bfloat16*>(d.O1) + o;
+                        const bool fold = d.gates != nullptr;
+                        // folded gates: g h (the fc2 weight-gradient operand), from registers
+                        __nv_bfloat16* O2 = fold && d.O2 ? static_cast<__nv_bfloat16*>(d.O2) + o : nullptr;
+                        float dgp = 0.f;
+#pragma unroll
+                        for (int j0 = 0; j0 < 8; j0 += 2) {
+                            uint4 ua[2], uu[2];
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                ua[j] = valid ? *reinterpret_cast<const uint4*>(X0 + 8 * (j0 + j)) : make_uint4(0, 0, 0, 0);
+                                uu[j] = valid ? *reinterpret_cast<const uint4*>(X1 + 8 * (j0 + j)) : make_uint4(0, 0, 0, 0);
+                            }
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                uint4 oa, ou, oh;
+                                const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&ua[j]);
+                                const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&uu[j]);
+                                __nv_bfloat162* da2 = reinterpret_cast<__nv_bfloat162*>(&oa);
+                                __nv_bfloat162* du2 = reinterpret_cast<__nv_bfloat162*>(&ou);
+                                __nv_bfloat162* dh2 = reinterpret_cast<__nv_bfloat162*>(&oh);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float2 dh = unpack2(acc[32 * part + 4 * (j0 + j) + i]);
+                                    const float2 av = __bfloat1622float2(a2[i]);
+                                    const float2 uv = __bfloat1622float2(u2[i]);
+                                    // pad rows (a = u = 0) give dA = dU = 0
+                                    if (fold) {
+                                        const SwigluBwdFold r0(dh.x, grow, av.x, uv.x);
+                                        const SwigluBwdFold r1(dh.y, grow, av.y, uv.y);
+                                        dgp = fmaf(dh.x, r0.h, dgp);
+                                        dgp = fmaf(dh.y, r1.h, dgp);
+                                        da2[i] = __floats2bfloat162_rn(r0.dA, r1.dA);
+                                        du2[i] = __floats2bfloat162_rn(r0.dU, r1.dU);
+                                        dh2[i] = __floats2bfloat162_rn(r0.h * grow, r1.h * grow);
+                                    } else {
+                                        const SwigluBwd r0(dh.x, av.x, uv.x);
+                                        const SwigluBwd r1(dh.y, av.y, uv.y);
+                                        da2[i] = __floats2bfloat162_rn(r0.dA, r1.dA);
+                                        du2[i] = __floats2bfloat162_rn(r0.dU, r1.dU);
+                                    }
+                                }
+                                *reinterpret_cast<uint4*>(O0 + 8 * (j0 + j)) = oa;
+                                *reinterpret_cast<uint4*>(O1 + 8 * (j0 + j)) = ou;
+                                if (O2) *reinterpret_cast<uint4*>(O2 + 8 * (j0 + j)) = oh;
+                            }
+                        }
+                        if (fold) {
+                            const int col = part ? col_hi : col_lo;
+                            d.dg_part[(size_t)arow * d.dg_ld + col / 64] = dgp;   // 0 past the computed rows
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+                        if (part == 1 && !hi_ok) break;
+                        __nv_bfloat16* O0 = static_cast<__nv_bfloat16*>(d.O0) + orow + (part ? col_hi : col_lo);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            get8(acc, 32 * part + 4 * j, v);
+                            if (!valid) {
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) v[i] = 0.f;
+                            }
+                            st8(O0 + 8 * j, v);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 g_encx = nullptr;
+std::once_flag g_encx_once;
+bool encx()
+{
+    std::call_once(g_encx_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encx = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encx != nullptr;
+}
+
+// Row-major byte matrix rows x cols (row stride ld bytes), boxes of
+// box_rows x 128 bytes, 128-byte swizzle, out-of-bounds reads 0.
+bool mapx(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld, int box_rows)
+{
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld};
+    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1u, 1u};
+    return g_encx(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI, int SCHED, int DUAL, bool B_MN>
+cudaError_t xrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
+{
+    constexpr int NW = (DUAL == DUAL_N) ? XBN / 2 : XBN;
+    CUtensorMap mA0, mA1, mB0, mB1;
+    bool ok = true;
+    long long units;
+    const long long num_n = (d.N + NW - 1) / NW;
+    if (!d.XA0 || !d.XB0 || (DUAL != DUAL_NONE && !d.XB1) || (DUAL == DUAL_K && !d.XA1))
+        return cudaErrorInvalidValue;
+    if (SCHED == SCHED_ROWS) {
+        ok &= mapx(&mA0, d.A0, d.a_rows, d.K, d.lda, XBM);
+        ok &= mapx(&mA1, d.A1 ? d.A1 : d.A0, d.a_rows, d.K, d.lda, XBM);
+        if (B_MN) {   // [E*K][N] codes, 128-column x 128-row boxes
+            ok &= mapx(&mB0, d.B0, d.b_rows, d.N, d.ldb, XBK);
+            ok &= mapx(&mB1, d.B1 ? d.B1 : d.B0, d.b_rows, d.N, d.ldb, XBK);
+        } else {      // [E*N][K] codes, 64-row boxes
+            ok &= mapx(&mB0, d.B0, d.b_rows, d.K, d.ldb, 64);
+            ok &= mapx(&mB1, d.B1 ? d.B1 : d.B0, d.b_rows, d.K, d.ldb, 64);
+        }
+        units = (long long)max_m_tiles * num_n;
+    } else {
+        // A: [M_out][rows_cap], B: [N][rows_cap] (transposed operands)
+        ok &= mapx(&mA0, d.A0, d.M_out, d.rows_cap, d.lda, XBM);
+        mA1 = mA0;
+        ok &= mapx(&mB0, d.B0, d.N, d.rows_cap, d.ldb, 64);
+        ok &= mapx(&mB1, d.B1 ? d.B1 : d.B0, d.N, d.rows_cap, d.ldb, 64);
+        units = (long long)d.E * (d.M_out / XBM) * num_n;
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    if (units <= 0) return cudaSuccess;
+    const int grid = (int)(units < num_sms ? units : num_sms);
+    gemm_mx_kernel<EPI, SCHED, DUAL, B_MN><<<grid, kXThreads, XCfg::SMEM, s>>>(mA0, mA1, mB0, mB1, d);
+    count_launches();
+    return cudaGetLastError();
+}
+
+template <int EPI, int SCHED, int DUAL, bool B_MN = false>
+cudaError_t xattr()
+{
+    return cudaFuncSetAttribute(gemm_mx_kernel<EPI, SCHED, DUAL, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                XCfg::SMEM);
+}
+
+}  // namespace
+
+cudaError_t gemm_mx_prepare(int device)
+{
+    (void)device;
+    if (!encx()) return cudaErrorNotSupported;
+    cudaError_t e = cudaSuccess;
+    auto acc = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
+    acc(xattr<EPI_SWIGLU_FWD, SCHED_ROWS, DUAL_N, true>());
+    acc(xattr<EPI_STORE, SCHED_ROWS, DUAL_NONE, true>());
+    acc(xattr<EPI_SWIGLU_BWD, SCHED_ROWS, DUAL_NONE>());
+    acc(xattr<EPI_STORE, SCHED_ROWS, DUAL_K>());
+    acc(xattr<EPI_WGRAD, SCHED_WGRAD, DUAL_NONE>());
+    acc(xattr<EPI_WGRAD, SCHED_WGRAD, DUAL_N>());
+    return e;
+}
+
+cudaError_t launch_gemm_mx(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
+{
+    if (!encx()) return cudaErrorNotSupported;
+    if (d.sched == SCHED_ROWS) {
+        switch (d.epi) {
+        // forward GEMMs read the weights' codes MN-major (b_kmajor 0), the
+        // data-gradient GEMMs K-major (b_kmajor 1)
+        case EPI_SWIGLU_FWD:
+            if (d.b_kmajor) return cudaErrorInvalidValue;
+            return xrun<EPI_SWIGLU_FWD, SCHED_ROWS, DUAL_N, true>(d, max_m_tiles, num_sms, s);
+        case EPI_SWIGLU_BWD:
+            if (!d.b_kmajor) return cudaErrorInvalidValue;
+            return xrun<EPI_SWIGLU_BWD, SCHED_ROWS, DUAL_NONE, false>(d, max_m_tiles, num_sms, s);
+        case EPI_STORE:
+            if (d.dual == DUAL_K)
+                return d.b_kmajor ? xrun<EPI_STORE, SCHED_ROWS, DUAL_K, false>(d, max_m_tiles, num_sms, s)
+                                  : cudaErrorInvalidValue;
+            return d.b_kmajor ? cudaErrorInvalidValue
+                              : xrun<EPI_STORE, SCHED_ROWS, DUAL_NONE, true>(d, max_m_tiles, num_sms, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    return d.dual == DUAL_N ? xrun<EPI_WGRAD, SCHED_WGRAD, DUAL_N, false>(d, max_m_tiles, num_sms, s)
+                            : xrun<EPI_WGRAD, SCHED_WGRAD, DUAL_NONE, false>(d, max_m_tiles, num_sms, s);
+}
+
+}  // namespace moe

@@ -85,6 +85,8 @@ struct GemmDesc {
     const float* SA0; const float* SA1; int lds_a;   // A: 1x128 blocks along K
     const float* SB0; const float* SB1; int lds_b;   // B: 128x128 blocks
     int rows_cap;   // SCHED_WGRAD: row capacity of the transposed operands
+    // MXFP8 only: UE8M0 scale atoms of the operands (see launch_mx_quant)
+    const uint8_t* XA0; const uint8_t* XA1; const uint8_t* XB0; const uint8_t* XB1;
     // memory-efficient permutation (gates != null): g of permuted row r is
     // gates[slot_of[r]]. SWIGLU_FWD stores O2 = g h; SWIGLU_BWD treats the
     // accumulator as dh', writes dA, dU of dh = g dh', O2 = g h (if O2 is
@@ -173,6 +175,32 @@ struct QuantJob {
     int gather_k = 1;
 };
 cudaError_t launch_quant(const QuantJob& j, cudaStream_t s);
+
+// MXFP8 quantisers (quant_mx.cu). Scale atoms: for an operand read as
+// [rows][K], one 512-byte atom per (128-row tile rt, 128-deep K block kb) at
+// (rt * K/128 + kb) * 512, byte 16 (m % 32) + 4 (m / 32) + j = UE8M0 scale of
+// tile row m and 32-deep sub-block j.
+cudaError_t launch_mx_permute(const __nv_bfloat16* x, const int* row_of, const int* poff, const int* counts,
+                              int T_, int H, int E, int k, uint8_t* Xq, uint8_t* sfX, cudaStream_t s);
+// One pass over in[rows][C] (bf16; rows = *rows_dev or rows_max, multiples
+// of 128, as is C). q != null: row codes q[rows][C] (blocks along rows) with
+// atoms sf. qc != null: column codes (blocks of 32 down each column), either
+// transposed qc[C][rows_cap] with atoms sfc of the [C][rows_cap] operand
+// (col_mode 1), or in place qc[rows][C] for expert-stacked weights
+// [rows / grp][grp][C] read MN-major with K = grp (col_mode 2).
+struct MxQuantJob {
+    const __nv_bfloat16* in;
+    const int* rows_dev;
+    int rows_max, C, rows_cap;
+    uint8_t* q; uint8_t* sf;
+    uint8_t* qc; uint8_t* sfc; int col_mode;
+    int grp = 0;
+    const int* gather_slot = nullptr;
+    int gather_k = 1;
+};
+cudaError_t launch_mx_quant(const MxQuantJob& j, cudaStream_t s);
+cudaError_t launch_gemm_mx(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s);
+cudaError_t gemm_mx_prepare(int device);
 
 // Configuration and device of a plan; false for a null plan.
 bool plan_info(const moe_plan_s* plan, moe_config_t* cfg, int* device);

@@ -118,7 +118,7 @@ def permutation(seed: int, tensor_id: int, n: int) -> torch.Tensor:
 
 # ---------------------------------------------------------------- workloads
 SOFTMAX, SIGMOID = 0, 1
-FP32, BF16, FP8_BLOCK = 0, 1, 2
+FP32, BF16, FP8_BLOCK, MXFP8 = 0, 1, 2, 3
 
 # tensor ids within one seed
 TID = dict(x=1, Wr=2, b=3, Wg=4, Wu=5, Wd=6, Wsg=7, Wsu=8, Wsd=9, dY=10, perm=11)
@@ -167,6 +167,9 @@ WORKLOADS: Dict[str, Workload] = {
                            seed=3000),
     "qwen3_235b_fp8": Workload("qwen3_235b_fp8", T=16384, H=4096, E=128, k=8, F=1536,
                                dtype=FP8_BLOCK, bias="zipf", seed=4000),
+    # the same shape in the MXFP8 recipe (1x32 blocks, power-of-two scales)
+    "qwen3_235b_mxfp8": Workload("qwen3_235b_mxfp8", T=16384, H=4096, E=128, k=8, F=1536,
+                                 dtype=MXFP8, bias="zipf", seed=4000),
 }
 
 
@@ -198,7 +201,7 @@ def make_inputs(w: Workload, device="cpu", with_grad_out: bool = True) -> Dict[s
 
     Layouts (row-major): x T×H; Wr H×E fp32; b E fp32; Wg, Wu E×H×F;
     Wd E×F×H; Wsg, Wsu H×Fs; Wsd Fs×H; dY T×H."""
-    dt = w.torch_dtype if w.dtype != FP8_BLOCK else torch.bfloat16
+    dt = w.torch_dtype if w.dtype not in (FP8_BLOCK, MXFP8) else torch.bfloat16
     g = {}
     g["x"] = normal_tensor(w.seed, TID["x"], (w.T, w.H), 1.0, dt, device)
     g["Wr"] = normal_tensor(w.seed, TID["Wr"], (w.H, w.E), router_std(w.H), torch.float32, device)

@@ -95,12 +95,14 @@ def _fp8_parity(name, fold):
 
 
 def fp8_layer_parity(w, fold=False):
-    """The FP8 layer on workload w against the oracle's FP8 layer (bounds in
-    the module docstring); returns the error report."""
+    """The FP8 layer on workload w (blockwise or MXFP8, by w.dtype) against
+    the oracle's FP8 layer in the same recipe (bounds in the module
+    docstring); returns the error report."""
     inp = mi.make_inputs(w)
     g = upload(inp)
-    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=moe.MOE_FP8_BLOCK,
-                         fold_gates=fold)
+    mx = w.dtype == mi.MXFP8
+    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score,
+                         dtype=moe.MOE_MXFP8 if mx else moe.MOE_FP8_BLOCK, fold_gates=fold)
     y, rt = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"], routing=True)
     gr = layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
     torch.cuda.synchronize()
@@ -114,7 +116,8 @@ def fp8_layer_parity(w, fold=False):
     if mism.any():
         r = oracle.route(d["x"], d["Wr"], d["b"], w.k, w.score, replay_topk=gt, replay_mask=mism)
     ref = oracle.layer_fp8(d["x"], d["Wr"], d["Wg"], d["Wu"], d["Wd"], r["topk"], r["gates"],
-                           r["scores"], w.score, d["dY"], fold=fold)
+                           r["scores"], w.score, d["dY"], fold=fold,
+                           recipe=oracle.RECIPE_MX if mx else oracle.RECIPE_BLOCK)
     rep = {}
     for gname, oname in (("y", "y"), ("dX", "dX")):
         got = to_np(y if gname == "y" else gr[gname])
@@ -134,19 +137,21 @@ def fp8_layer_parity(w, fold=False):
                 assert np.all(gb == 0)
             else:
                 assert np.linalg.norm(gb - wb) / nw <= 4e-2, gname
-    write_report(f"{w.name} T{w.T} H{w.H} E{w.E} k{w.k} F{w.F} fp8" + (" fold" if fold else ""), rep)
+    write_report(f"{w.name} T{w.T} H{w.H} E{w.E} k{w.k} F{w.F} {'mxfp8' if mx else 'fp8'}"
+                 + (" fold" if fold else ""), rep)
     return rep
 
 
-@pytest.mark.parametrize("fold", [False, True])
-def test_fp8_weight_cache_gives_identical_results(fold):
+@pytest.mark.parametrize("fold,dtype", [(False, mi.FP8_BLOCK), (True, mi.FP8_BLOCK), (False, mi.MXFP8)])
+def test_fp8_weight_cache_gives_identical_results(fold, dtype):
     """Weights quantised once by moe_quantize_weights and passed as the
     weight cache (the bf16 weights not passed at all) give the same bits as
-    the layer quantising them inside every forward; the cache holds the
-    oracle's 128x128-block codes."""
-    w = FP8_CASES["qwen_fp8_ragged"]
+    the layer quantising them inside every forward; for the blockwise recipe
+    the cache holds the oracle's 128x128-block codes."""
+    w = mi.scaled(FP8_CASES["qwen_fp8_ragged"], dtype=dtype)
     g = upload(mi.make_inputs(w))
-    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=moe.MOE_FP8_BLOCK, fold_gates=fold)
+    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score,
+                         dtype=moe.MOE_MXFP8 if dtype == mi.MXFP8 else moe.MOE_FP8_BLOCK, fold_gates=fold)
     y0 = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"])
     gr0 = layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
     torch.cuda.synchronize()
@@ -161,6 +166,8 @@ def test_fp8_weight_cache_gives_identical_results(fold):
         assert torch.equal(y1, ref["y"])
         for k, v in gr1.items():
             assert torch.equal(v, ref[k]), k
+    if dtype == mi.MXFP8:
+        return
     # the cache's first block: W_gate codes of expert 0 and their scales
     oc, os_ = oracle.fp8_quantize(g["Wg"][0].float().cpu().numpy(), oracle.FP8_TILES)
     n = w.H * w.F
