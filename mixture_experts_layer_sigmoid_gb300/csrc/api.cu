@@ -920,7 +920,7 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
     d.N = F; d.K = H; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
-    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 256ll * E;
     d.A0 = sv + L.Xq; d.lda = H; d.a_rows = Rp; d.XA0 = sv + L.sX;
     d.B0 = wq.q[0]; d.B1 = wq.q[1]; d.ldb = F; d.b_rows = E * H; d.b_kmajor = 0;
     d.XB0 = xs(wq.s[0]); d.XB1 = xs(wq.s[1]);
@@ -935,7 +935,7 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
     d.N = H; d.K = F; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
-    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 256ll * E;
     d.A0 = ws + L.hq; d.lda = F; d.a_rows = Rp; d.XA0 = ws + L.sh;
     d.B0 = wq.q[2]; d.ldb = H; d.b_rows = E * F; d.XB0 = xs(wq.s[2]); d.b_kmajor = 0;
     d.O0 = Yp; d.ldo = H; d.status = status;
@@ -1003,7 +1003,7 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_BWD; d.dual = DUAL_NONE;
     d.N = F; d.K = H; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
-    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 256ll * E;
     d.A0 = ws + L.dYq; d.lda = H; d.a_rows = Rp; d.XA0 = ws + L.sdY;
     d.B0 = wq.q[5]; d.ldb = H; d.b_rows = E * F; d.XB0 = xs(wq.s[5]); d.b_kmajor = 1;
     d.X0 = A; d.X1 = U; d.O0 = dA; d.O1 = dU; d.ldo = F; d.status = status;
@@ -1023,7 +1023,7 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
     d.N = H; d.M_out = F; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
-    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 256ll * E;
     d.A0 = ws + L.hTq; d.lda = Rp; d.XA0 = ws + L.shT;
     d.B0 = ws + L.dYpTq; d.ldb = Rp; d.XB0 = ws + L.sdYpT;
     d.rows_cap = Rp; d.expert_order = eorder;
@@ -1040,7 +1040,7 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
     d.N = H; d.K = F; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
-    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 256ll * E;
     d.A0 = ws + L.dAq; d.A1 = ws + L.dUq; d.lda = F; d.a_rows = Rp;
     d.XA0 = ws + L.sdA; d.XA1 = ws + L.sdU;
     d.B0 = wq.q[3]; d.B1 = wq.q[4]; d.ldb = F; d.b_rows = E * H; d.b_kmajor = 1;
@@ -1059,7 +1059,7 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
     d.N = F; d.M_out = H; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept;
-    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 256ll * E;
     d.A0 = ws + L.XpTq; d.lda = Rp; d.XA0 = ws + L.sXpT;
     d.B0 = ws + L.dATq; d.B1 = ws + L.dUTq; d.ldb = Rp;
     d.XB0 = ws + L.sdAT; d.XB1 = ws + L.sdUT;

@@ -11,14 +11,22 @@
 // per-block promotion in registers (the blockwise-FP8 engine's limit).
 //
 // Ten warps per CTA: warp 0 loads each 128-deep k block (A: 128 rows x 128
-// bytes, B: 256 rows, 128-byte swizzle, by TMA; the operands' scale atoms,
-// 512 bytes each, by bulk copies); warp 1 allocates tensor memory and one
+// bytes, B: 256 rows, 128-byte swizzle; the operands' scale atoms, 512 bytes
+// each, as 4 x 128-byte boxes; all by TMA); warp 1 allocates tensor memory and one
 // thread issues, per k block, tcgen05.cp of the scale atoms into a ring of
 // tensor-memory columns and four N = 256 MMAs (K = 32 each, the scale
 // sub-block chosen by the instruction descriptor's scale-factor IDs);
 // warps 2-9 wait for a finished tile, copy its 128 x 256 fp32 accumulator
 // into registers (two warps per TMEM lane quarter, 128 columns each), release
 // it to the next tile and run the fused epilogue from registers.
+//
+// CTA pairs (clusters of two, the default wherever the row units come in
+// pairs): the even CTA issues M = 256 MMAs (cta_group::2) with A rows 0-127
+// from its own shared memory and 128-255 from its peer's and B's 256 columns
+// split between the two, so each SM loads 32 KB + 1.5 KB per k block instead
+// of 48 KB + 1.5 KB; every CTA stages its own A scale atom and both B atoms,
+// and tcgen05.cp.cta_group::2 moves each CTA's atoms into its own tensor
+// memory, where its 128 rows of the accumulator live.
 //
 // Scale atoms (quant_mx.cu): an operand read as [rows][K] keeps, per 128-row
 // tile and 128-deep K block, 512 bytes whose byte 16 (m % 32) + 4 (m / 32) + j
@@ -43,15 +51,18 @@ constexpr int kXGroupN = 16;
 constexpr int kAccCols = 256;                    // the accumulator
 constexpr int kSfCols = 12;                      // scale columns of one stage: A 4, B 2 x 4
 
+template <bool PAIR>
 struct XCfg {
     static constexpr int A_BYTES = XBM * XBK;
-    static constexpr int B_BYTES = XBN * XBK;
+    static constexpr int B_ROWS = PAIR ? XBN / 2 : XBN;  // B rows (n) staged by this CTA
+    static constexpr int B_BYTES = B_ROWS * XBK;
     static constexpr int SF_BYTES = 3 * 512;     // A atom, then B atoms of the two 128-column parts
     static constexpr int STAGE = A_BYTES + B_BYTES + 2048;   // (SF region padded to keep 1 KB alignment)
     static constexpr int STAGES = (kXSmemMax - 1024 - 256) / STAGE;
     static constexpr int SMEM = 1024 + STAGES * STAGE + 256;
 };
-static_assert(kAccCols + kSfCols * XCfg::STAGES <= 512, "tensor memory");
+static_assert(kAccCols + kSfCols * XCfg<true>::STAGES <= 512, "tensor memory");
+static_assert(kAccCols + kSfCols * XCfg<false>::STAGES <= 512, "tensor memory");
 
 // kind::mxf8f6f4 instruction descriptor: E4M3 A and B (format 0), fp32 D,
 // UE8M0 scales (bit 23), A K-major, B K-major or MN-major (bit 16), the
@@ -76,10 +87,28 @@ __device__ __forceinline__ void mma_mx(uint32_t tmem_d, uint64_t adesc, uint64_t
         : "memory");
 }
 
+__device__ __forceinline__ void mma_mx_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n"
+        "}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
 // 32 rows x 16 bytes of shared memory -> every TMEM lane quarter, 4 columns
 __device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint64_t sdesc)
 {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// the same in both CTAs of a pair: each CTA's shared memory -> its own TMEM
+__device__ __forceinline__ void tmem_cp_atom_pair(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Shared-memory descriptor of 16-byte rows stored contiguously (no swizzle:
@@ -92,14 +121,6 @@ __device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr)
     d |= (uint64_t)((128u >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;
     return d;
-}
-
-// one contiguous global -> shared copy, completion counted on `bar`
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-                 : "memory");
 }
 
 // 16 consecutive fp32 columns of this thread's TMEM lane.
@@ -150,40 +171,44 @@ struct XTile {
     int e, m, n, row0, kblocks, kb0, valid_end, alloc_end;
 };
 
-template <int DUAL, int SCHED>
+template <int DUAL, int SCHED, bool PAIR>
 __device__ __forceinline__ void xtile_counts(const GemmDesc& d, int& num_m, int& num_n, int& total)
 {
     constexpr int NW = (DUAL == DUAL_N) ? XBN / 2 : XBN;
     num_n = (d.N + NW - 1) / NW;
     if (SCHED == SCHED_ROWS) {
-        num_m = d.meta[0];
+        num_m = PAIR ? d.meta[2] : d.meta[0];
         total = num_m * num_n;
     } else {
-        num_m = d.M_out / XBM;
+        num_m = d.M_out / (PAIR ? 2 * XBM : XBM);
         total = d.E * num_m * num_n;
     }
 }
 
 // Row-scheduled tiles go expert by expert; within an expert, groups of
-// kXGroupN column tiles walk its 128-row tiles. Weight-gradient tiles take
-// the experts longest first (the order the scan wrote) and walk each
-// expert's (m, n) grid with the smaller count fastest.
-template <int DUAL, int SCHED>
-__device__ __forceinline__ XTile xdecode(const GemmDesc& d, int w, int num_m, int num_n)
+// kXGroupN column tiles walk its row units (a 128-row tile, or a pair of one
+// expert's consecutive tiles, the second possibly a "ghost" past the segment
+// that is never stored). Weight-gradient tiles take the experts longest
+// first (the order the scan wrote) and walk each expert's (m, n) grid with
+// the smaller count fastest.
+template <int DUAL, int SCHED, bool PAIR>
+__device__ __forceinline__ XTile xdecode(const GemmDesc& d, int w, int num_m, int num_n, int rank)
 {
     XTile t;
     if (SCHED == SCHED_ROWS) {
         const int q = w / num_n;
-        const int e = d.tile_tab[q];
-        const int u0 = d.poff[e] / XBM;
-        const int nu = d.poff[e + 1] / XBM - u0;
+        const int e = d.tile_tab[PAIR ? d.pair_tab[q] : q];
+        const int u0 = PAIR ? d.pair_off[e] : d.poff[e] / XBM;
+        const int nu = (PAIR ? d.pair_off[e + 1] : d.poff[e + 1] / XBM) - u0;
         w -= u0 * num_n;
         const int group = w / (nu * kXGroupN);
         const int r = w - group * nu * kXGroupN;
         const int gsz = min(kXGroupN, num_n - group * kXGroupN);
-        t.m = u0 + r / gsz;
+        const int mu = u0 + r / gsz;
         t.n = group * kXGroupN + r % gsz;
-        t.e = e;
+        const int first = PAIR ? d.pair_tab[mu] : mu;
+        t.m = first + rank;
+        t.e = d.tile_tab[first];
         t.row0 = t.m * XBM;
         t.valid_end = d.poff[t.e] + d.counts[t.e];
         t.alloc_end = d.poff[t.e + 1];
@@ -194,13 +219,15 @@ __device__ __forceinline__ XTile xdecode(const GemmDesc& d, int w, int num_m, in
         const int eo = w / per;
         t.e = d.expert_order ? d.expert_order[eo] : eo;
         const int r = w - eo * per;
+        int mu;
         if (num_n < num_m) {
             t.n = r % num_n;
-            t.m = r / num_n;
+            mu = r / num_n;
         } else {
-            t.m = r % num_m;
+            mu = r % num_m;
             t.n = r / num_m;
         }
+        t.m = PAIR ? 2 * mu + rank : mu;
         t.row0 = d.poff[t.e];
         t.kb0 = t.row0 / XBK;
         t.kblocks = (d.poff[t.e + 1] - t.row0) / XBK;
@@ -209,13 +236,15 @@ __device__ __forceinline__ XTile xdecode(const GemmDesc& d, int w, int num_m, in
     return t;
 }
 
-template <int EPI, int SCHED, int DUAL, bool B_MN>
+template <int EPI, int SCHED, int DUAL, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(kXThreads, 1)
 gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
+               const __grid_constant__ CUtensorMap mSA0, const __grid_constant__ CUtensorMap mSA1,
+               const __grid_constant__ CUtensorMap mSB0, const __grid_constant__ CUtensorMap mSB1,
                const GemmDesc d)
 {
-    using C = XCfg;
+    using C = XCfg<PAIR>;
     constexpr int NW = (DUAL == DUAL_N) ? XBN / 2 : XBN;   // output columns per tile
     static_assert(!B_MN || (SCHED == SCHED_ROWS && DUAL != DUAL_K), "MN-major B: forward GEMMs");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -225,6 +254,9 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = PAIR ? (int)ptx::cluster_ctarank() : 0;
+    const int unit0 = PAIR ? (int)ptx::cluster_id_x() : (int)blockIdx.x;
+    const int nunits = PAIR ? (int)ptx::nclusters_x() : (int)gridDim.x;
     const uint32_t bar0 = ptx::smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
@@ -238,7 +270,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
             ptx::mbar_init(empty_bar(s), 1);
         }
         ptx::mbar_init(accf_bar, 1);
-        ptx::mbar_init(acce_bar, 8);   // the eight epilogue warps
+        ptx::mbar_init(acce_bar, PAIR ? 16 : 8);   // the epilogue warps (of both CTAs)
         ptx::mbar_init(final_bar, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -251,21 +283,35 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
             ptx::prefetch_tmap(&mB1);
         }
     }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&mSA0);
+        ptx::prefetch_tmap(&mSB0);
+    }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
-        ptx::tmem_relinquish();
+        if (PAIR) {
+            ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), 512);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    if (PAIR) ptx::cluster_sync();   // peer barriers initialised before any remote signal
+    else __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     int num_m, num_n, total;
-    xtile_counts<DUAL, SCHED>(d, num_m, num_n, total);
+    xtile_counts<DUAL, SCHED, PAIR>(d, num_m, num_n, total);
     auto wait_uniform = [&](uint32_t bar, uint32_t parity, int where) -> bool {
         int ok = 1;
         if (lane == 0) ok = ptx::wait_bounded(bar, parity, abort_flag, d.status, where) ? 1 : 0;
         return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
+    auto load = [&](uint32_t dst, const CUtensorMap* m, int s, int x, int y) {
+        if (PAIR) ptx::tma_load_2d_pair(dst, m, ptx::mapa_shared(full_bar(s), 0), x, y);
+        else ptx::tma_load_2d(dst, m, full_bar(s), x, y);
     };
     // the 128-row tiles of B's two 128-column parts (part 1: the same columns
     // of B1 for DUAL_N, else the next 128 columns) and whether part 1 exists
@@ -280,8 +326,8 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
         uint32_t it = 0;
         const int kb_half = d.K / XBK;
         bool ok = true;
-        for (int w = blockIdx.x; ok && w < total; w += gridDim.x) {
-            const XTile t = xdecode<DUAL, SCHED>(d, w, num_m, num_n);
+        for (int w = unit0; ok && w < total; w += nunits) {
+            const XTile t = xdecode<DUAL, SCHED, PAIR>(d, w, num_m, num_n, rank);
             int nb_lo, nb_hi;
             bool hi_ok;
             bparts(t, nb_lo, nb_hi, hi_ok);
@@ -290,39 +336,44 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                 const uint32_t ph = (it / C::STAGES) & 1u;
                 if (!wait_uniform(empty_bar(s), ph ^ 1u, 21)) { ok = false; break; }
                 if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(full_bar(s), C::A_BYTES + C::B_BYTES + C::SF_BYTES);
+                    if (rank == 0)
+                        ptx::mbar_arrive_expect_tx(full_bar(s),
+                                                   (PAIR ? 2 : 1) * (C::A_BYTES + C::B_BYTES + C::SF_BYTES));
                     const uint32_t a_dst = ptx::smem_u32(smem + s * C::STAGE);
                     const uint32_t b_dst = a_dst + C::A_BYTES;
                     const uint32_t sf_dst = b_dst + C::B_BYTES;
                     int kx, arow, brow;
                     const CUtensorMap* am = &mA0;
                     const CUtensorMap* bm = &mB0;
-                    const uint8_t* xa = d.XA0;
-                    const uint8_t* xb = d.XB0;
-                    size_t a_atom, b_atom_lo, b_atom_hi;
+                    const CUtensorMap* sam = &mSA0;
+                    const CUtensorMap* sbm = &mSB0;
+                    int a_atom, b_atom_lo, b_atom_hi;
                     if (SCHED == SCHED_ROWS) {
                         const bool second = (DUAL == DUAL_K) && kb >= kb_half;
                         const int kk = second ? kb - kb_half : kb;
                         kx = kk * XBK;
                         arow = t.row0;
                         brow = t.e * d.N + t.n * NW;
-                        if (second) { am = &mA1; bm = &mB1; xa = d.XA1; xb = d.XB1; }
-                        const size_t KB = (size_t)(d.K / XBK);
-                        const size_t ebase = (size_t)t.e * (d.N / 128);
-                        a_atom = ((size_t)t.m * KB + kk) * 512;
-                        b_atom_lo = ((ebase + nb_lo) * KB + kk) * 512;
-                        b_atom_hi = ((ebase + (hi_ok ? nb_hi : nb_lo)) * KB + kk) * 512;
+                        if (second) { am = &mA1; bm = &mB1; sam = &mSA1; sbm = &mSB1; }
+                        const int KB = d.K / XBK;
+                        const int ebase = t.e * (d.N / 128);
+                        a_atom = t.m * KB + kk;
+                        b_atom_lo = (ebase + nb_lo) * KB + kk;
+                        b_atom_hi = (ebase + (hi_ok ? nb_hi : nb_lo)) * KB + kk;
                     } else {
                         const int kg = t.kb0 + kb;
                         kx = kg * XBK;
                         arow = t.m * XBM;
                         brow = t.n * NW;
-                        const size_t KB = (size_t)(d.rows_cap / XBK);
-                        a_atom = ((size_t)t.m * KB + kg) * 512;
-                        b_atom_lo = ((size_t)nb_lo * KB + kg) * 512;
-                        b_atom_hi = ((size_t)(hi_ok ? nb_hi : nb_lo) * KB + kg) * 512;
+                        const int KB = d.rows_cap / XBK;
+                        a_atom = t.m * KB + kg;
+                        b_atom_lo = nb_lo * KB + kg;
+                        b_atom_hi = (hi_ok ? nb_hi : nb_lo) * KB + kg;
                     }
-                    ptx::tma_load_2d(a_dst, am, full_bar(s), kx, arow);
+                    load(a_dst, am, s, kx, arow);
+                    // B "part 0" = tile columns [0, 128) (DUAL_N: B0 columns), "part 1" =
+                    // [128, 256) (DUAL_N: the same columns of B1). A pair's CTA r stages
+                    // part r; a single CTA stages [part 0 | part 1].
                     const CUtensorMap* p0 = (DUAL == DUAL_N) ? &mB0 : bm;
                     const CUtensorMap* p1 = (DUAL == DUAL_N) ? &mB1 : bm;
                     const int r1 = (DUAL == DUAL_N) ? brow : brow + 128;
@@ -330,65 +381,93 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                         const int n0 = t.n * NW;
                         const int c1 = (DUAL == DUAL_N) ? n0 : n0 + 128;
                         const int krow = t.e * d.K + kx;
-                        ptx::tma_load_2d(b_dst, p0, full_bar(s), n0, krow);
-                        ptx::tma_load_2d(b_dst + 128 * XBK, p1, full_bar(s), c1, krow);
+                        if (PAIR) {
+                            load(b_dst, rank ? p1 : p0, s, rank ? c1 : n0, krow);
+                        } else {
+                            load(b_dst, p0, s, n0, krow);
+                            load(b_dst + 128 * XBK, p1, s, c1, krow);
+                        }
+                    } else if (PAIR) {
+                        load(b_dst, rank ? p1 : p0, s, kx, rank ? r1 : brow);
+                        load(b_dst + 64 * XBK, rank ? p1 : p0, s, kx, (rank ? r1 : brow) + 64);
                     } else {
-                        ptx::tma_load_2d(b_dst, p0, full_bar(s), kx, brow);
-                        ptx::tma_load_2d(b_dst + 128 * XBK, p1, full_bar(s), kx, r1);
-                        ptx::tma_load_2d(b_dst + 64 * XBK, p0, full_bar(s), kx, brow + 64);
-                        ptx::tma_load_2d(b_dst + 192 * XBK, p1, full_bar(s), kx, r1 + 64);
+                        load(b_dst, p0, s, kx, brow);
+                        load(b_dst + 128 * XBK, p1, s, kx, r1);
+                        load(b_dst + 64 * XBK, p0, s, kx, brow + 64);
+                        load(b_dst + 192 * XBK, p1, s, kx, r1 + 64);
                     }
-                    const uint8_t* xb1 = (DUAL == DUAL_N) ? d.XB1 : xb;
-                    bulk_load(sf_dst, xa + a_atom, 512, full_bar(s));
-                    bulk_load(sf_dst + 512, xb + b_atom_lo, 512, full_bar(s));
-                    bulk_load(sf_dst + 1024, ((DUAL == DUAL_N) ? xb1 : xb) + b_atom_hi, 512, full_bar(s));
+                    // scale atoms: this CTA's A rows, and both B parts (the MMA reads
+                    // the scales of all 256 B columns in each CTA's tensor memory)
+                    const CUtensorMap* sb1 = (DUAL == DUAL_N) ? &mSB1 : sbm;
+                    load(sf_dst, sam, s, 0, 4 * a_atom);
+                    load(sf_dst + 512, sbm, s, 0, 4 * b_atom_lo);
+                    load(sf_dst + 1024, sb1, s, 0, 4 * b_atom_hi);
                 }
                 __syncwarp();
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer
-        uint32_t it = 0, tc = 0;
-        bool ok = true;
-        for (int w = blockIdx.x; ok && w < total; w += gridDim.x) {
-            const XTile t = xdecode<DUAL, SCHED>(d, w, num_m, num_n);
-            if (t.kblocks == 0) continue;                  // an expert without rows: zeros
-            if (!wait_uniform(acce_bar, (tc & 1u) ^ 1u, 22)) { ok = false; break; }
-            ptx::tc_fence_after();
-            for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
-                const int s = it % C::STAGES;
-                const uint32_t ph = (it / C::STAGES) & 1u;
-                if (!wait_uniform(full_bar(s), ph, 23)) { ok = false; break; }
+        if (rank == 0) {
+            constexpr int MM = PAIR ? 2 * XBM : XBM;
+            uint32_t it = 0, tc = 0;
+            bool ok = true;
+            for (int w = unit0; ok && w < total; w += nunits) {
+                const XTile t = xdecode<DUAL, SCHED, PAIR>(d, w, num_m, num_n, rank);
+                if (t.kblocks == 0) continue;              // an expert without rows: zeros
+                if (!wait_uniform(acce_bar, (tc & 1u) ^ 1u, 22)) { ok = false; break; }
                 ptx::tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t a_addr = ptx::smem_u32(smem + s * C::STAGE);
-                    const uint32_t b_addr = a_addr + C::A_BYTES;
-                    const uint32_t sf_addr = b_addr + C::B_BYTES;
-                    const uint32_t sfa = tmem_base + (uint32_t)(kAccCols + kSfCols * s);
-                    const uint32_t sfb = sfa + 4;
-                    tmem_cp_atom(sfa, smem_desc_plain(sf_addr));
-                    tmem_cp_atom(sfb, smem_desc_plain(sf_addr + 512));
-                    tmem_cp_atom(sfb + 4, smem_desc_plain(sf_addr + 1024));
+                for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
+                    const int s = it % C::STAGES;
+                    const uint32_t ph = (it / C::STAGES) & 1u;
+                    if (!wait_uniform(full_bar(s), ph, 23)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t a_addr = ptx::smem_u32(smem + s * C::STAGE);
+                        const uint32_t b_addr = a_addr + C::A_BYTES;
+                        const uint32_t sf_addr = b_addr + C::B_BYTES;
+                        const uint32_t sfa = tmem_base + (uint32_t)(kAccCols + kSfCols * s);
+                        const uint32_t sfb = sfa + 4;
+                        if (PAIR) {
+                            tmem_cp_atom_pair(sfa, smem_desc_plain(sf_addr));
+                            tmem_cp_atom_pair(sfb, smem_desc_plain(sf_addr + 512));
+                            tmem_cp_atom_pair(sfb + 4, smem_desc_plain(sf_addr + 1024));
+                        } else {
+                            tmem_cp_atom(sfa, smem_desc_plain(sf_addr));
+                            tmem_cp_atom(sfb, smem_desc_plain(sf_addr + 512));
+                            tmem_cp_atom(sfb + 4, smem_desc_plain(sf_addr + 1024));
+                        }
 #pragma unroll
-                    for (int k = 0; k < XBK / 32; ++k) {
-                        const uint64_t ad = ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
-                        // MN-major: 32 rows of 128 bytes per K=32 step, stripes of
-                        // 128 columns 16 KB apart
-                        const uint64_t bd = B_MN ? ptx::smem_desc_sw128(b_addr + k * 4096, 128 * XBK, 1024)
-                                                 : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
-                        mma_mx(tmem_base, ad, bd, idesc_mx(XBN, XBM, B_MN, k), sfa, sfb, (kb > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < XBK / 32; ++k) {
+                            const uint64_t ad = ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
+                            // MN-major: 32 rows of 128 bytes per K=32 step, stripes of
+                            // 128 columns 16 KB apart (one stripe per CTA in a pair)
+                            const uint64_t bd = B_MN ? ptx::smem_desc_sw128(b_addr + k * 4096, 128 * XBK, 1024)
+                                                     : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
+                            const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+                            if (PAIR) mma_mx_pair(tmem_base, ad, bd, idesc_mx(XBN, MM, B_MN, k), sfa, sfb, acc);
+                            else mma_mx(tmem_base, ad, bd, idesc_mx(XBN, MM, B_MN, k), sfa, sfb, acc);
+                        }
+                        if (PAIR) ptx::tc_commit_pair(empty_bar(s), 3);
+                        else ptx::tc_commit(empty_bar(s));
                     }
-                    ptx::tc_commit(empty_bar(s));
+                    __syncwarp();
+                }
+                if (ok && lane == 0) {
+                    if (PAIR) ptx::tc_commit_pair(accf_bar, 3);
+                    else ptx::tc_commit(accf_bar);
                 }
                 __syncwarp();
+                ++tc;
             }
-            if (ok && lane == 0) ptx::tc_commit(accf_bar);
-            __syncwarp();
-            ++tc;
+            // every MMA issued by this warp has completed before TMEM is freed
+            if (lane == 0) {
+                if (PAIR) ptx::tc_commit_pair(final_bar, 3);
+                else ptx::tc_commit(final_bar);
+            }
         }
-        // every MMA issued by this warp has completed before TMEM is freed
+        // (in a pair, the odd CTA's TMEM is written by its peer's MMAs)
         if (lane == 0) {
-            ptx::tc_commit(final_bar);
             volatile int never = 0;
             ptx::wait_bounded(final_bar, 0, &never, d.status, 24);
         }
@@ -402,8 +481,8 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
         // pairs 0-31 and part-1 columns [64hh, +64) into pairs 32-63; part 0 is
         // tile columns [0, 128) (DUAL_N: B0), part 1 [128, 256) (DUAL_N: B1).
         uint32_t tc = 0;
-        for (int w = blockIdx.x; w < total; w += gridDim.x) {
-            const XTile t = xdecode<DUAL, SCHED>(d, w, num_m, num_n);
+        for (int w = unit0; w < total; w += nunits) {
+            const XTile t = xdecode<DUAL, SCHED, PAIR>(d, w, num_m, num_n, rank);
             const int arow = (SCHED == SCHED_ROWS) ? t.row0 + r_in : t.m * XBM + r_in;
             const bool arow_ok = (SCHED == SCHED_ROWS) ? arow < d.a_rows : true;
             (void)arow_ok;
@@ -432,7 +511,10 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                 ptx::tc_fence_before();
                 __syncwarp();
                 // relaxed: the accumulator has been read (tcgen05.wait::ld)
-                if (lane == 0) ptx::mbar_arrive_relaxed(acce_bar);
+                if (lane == 0) {
+                    if (PAIR) ptx::mbar_arrive_cluster_relaxed(ptx::mapa_shared(acce_bar, 0));
+                    else ptx::mbar_arrive_relaxed(acce_bar);
+                }
                 ++tc;
             } else {
 #pragma unroll
@@ -564,11 +646,13 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
     }
 
     ptx::tc_fence_before();
-    __syncthreads();
+    if (PAIR) ptx::cluster_sync();   // both CTAs done with TMEM and with remote signals
+    else __syncthreads();
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, 512);
+        if (PAIR) ptx::tmem_dealloc_pair(tmem_base, 512);
+        else ptx::tmem_dealloc(tmem_base, 512);
     }
 }
 
@@ -601,48 +685,134 @@ bool mapx(CUtensorMap* m, const void* ptr, long long rows, long long cols, long 
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Scale atoms as a [natoms * 4][128] byte tensor read in 128 x 4 boxes (one atom).
+bool map_atoms(CUtensorMap* m, const void* ptr, long long natoms)
+{
+    cuuint64_t dims[2] = {128u, (cuuint64_t)natoms * 4};
+    cuuint64_t strides[1] = {128u};
+    cuuint32_t box[2] = {128u, 4u};
+    cuuint32_t es[2] = {1u, 1u};
+    return g_encx(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int EPI, int SCHED, int DUAL, bool B_MN>
+int xpair_slots()
+{
+    // computed once (thread-safe initialisation of a function-local static)
+    static const int slots = [] {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(kXThreads, 1, 1);
+        cfg.dynamicSmemBytes = XCfg<true>::SMEM;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, true>, &cfg) != cudaSuccess)
+            n = 0;
+        cudaGetLastError();
+        return n;
+    }();
+    return slots;
+}
+
+template <int EPI, int SCHED, int DUAL, bool B_MN, bool PAIR>
 cudaError_t xrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
 {
     constexpr int NW = (DUAL == DUAL_N) ? XBN / 2 : XBN;
-    CUtensorMap mA0, mA1, mB0, mB1;
+    CUtensorMap mA0, mA1, mB0, mB1, mSA0, mSA1, mSB0, mSB1;
     bool ok = true;
     long long units;
     const long long num_n = (d.N + NW - 1) / NW;
     if (!d.XA0 || !d.XB0 || (DUAL != DUAL_NONE && !d.XB1) || (DUAL == DUAL_K && !d.XA1))
         return cudaErrorInvalidValue;
+    constexpr int BKROWS = PAIR ? 64 : 64;   // K-major B boxes of 64 rows
     if (SCHED == SCHED_ROWS) {
+        const long long KB = d.K / XBK;
         ok &= mapx(&mA0, d.A0, d.a_rows, d.K, d.lda, XBM);
         ok &= mapx(&mA1, d.A1 ? d.A1 : d.A0, d.a_rows, d.K, d.lda, XBM);
+        // atoms of A: one row of atoms per 128-row tile of the permuted rows
+        ok &= map_atoms(&mSA0, d.XA0, (d.a_rows / XBM) * KB);
+        ok &= map_atoms(&mSA1, d.XA1 ? d.XA1 : d.XA0, (d.a_rows / XBM) * KB);
+        // atoms of B: operand rows e N + n, K blocks of d.K
+        const long long b_nrows = (long long)(d.b_rows / d.K) * d.N;   // E * N
+        ok &= map_atoms(&mSB0, d.XB0, (B_MN ? b_nrows : d.b_rows) / 128 * KB);
+        ok &= map_atoms(&mSB1, d.XB1 ? d.XB1 : d.XB0, (B_MN ? b_nrows : d.b_rows) / 128 * KB);
         if (B_MN) {   // [E*K][N] codes, 128-column x 128-row boxes
             ok &= mapx(&mB0, d.B0, d.b_rows, d.N, d.ldb, XBK);
             ok &= mapx(&mB1, d.B1 ? d.B1 : d.B0, d.b_rows, d.N, d.ldb, XBK);
-        } else {      // [E*N][K] codes, 64-row boxes
-            ok &= mapx(&mB0, d.B0, d.b_rows, d.K, d.ldb, 64);
-            ok &= mapx(&mB1, d.B1 ? d.B1 : d.B0, d.b_rows, d.K, d.ldb, 64);
+        } else {      // [E*N][K] codes
+            ok &= mapx(&mB0, d.B0, d.b_rows, d.K, d.ldb, BKROWS);
+            ok &= mapx(&mB1, d.B1 ? d.B1 : d.B0, d.b_rows, d.K, d.ldb, BKROWS);
         }
-        units = (long long)max_m_tiles * num_n;
+        units = (long long)(PAIR ? (max_m_tiles + 1) / 2 : max_m_tiles) * num_n;
     } else {
         // A: [M_out][rows_cap], B: [N][rows_cap] (transposed operands)
+        const long long KB = d.rows_cap / XBK;
         ok &= mapx(&mA0, d.A0, d.M_out, d.rows_cap, d.lda, XBM);
         mA1 = mA0;
-        ok &= mapx(&mB0, d.B0, d.N, d.rows_cap, d.ldb, 64);
-        ok &= mapx(&mB1, d.B1 ? d.B1 : d.B0, d.N, d.rows_cap, d.ldb, 64);
-        units = (long long)d.E * (d.M_out / XBM) * num_n;
+        ok &= mapx(&mB0, d.B0, d.N, d.rows_cap, d.ldb, BKROWS);
+        ok &= mapx(&mB1, d.B1 ? d.B1 : d.B0, d.N, d.rows_cap, d.ldb, BKROWS);
+        ok &= map_atoms(&mSA0, d.XA0, (d.M_out / 128) * KB);
+        mSA1 = mSA0;
+        ok &= map_atoms(&mSB0, d.XB0, (d.N / 128) * KB);
+        ok &= map_atoms(&mSB1, d.XB1 ? d.XB1 : d.XB0, (d.N / 128) * KB);
+        units = (long long)d.E * (d.M_out / (PAIR ? 2 * XBM : XBM)) * num_n;
     }
     if (!ok) return cudaErrorInvalidValue;
     if (units <= 0) return cudaSuccess;
-    const int grid = (int)(units < num_sms ? units : num_sms);
-    gemm_mx_kernel<EPI, SCHED, DUAL, B_MN><<<grid, kXThreads, XCfg::SMEM, s>>>(mA0, mA1, mB0, mB1, d);
+    if (!PAIR) {
+        const int grid = (int)(units < num_sms ? units : num_sms);
+        gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, false><<<grid, kXThreads, XCfg<false>::SMEM, s>>>(
+            mA0, mA1, mB0, mB1, mSA0, mSA1, mSB0, mSB1, d);
+        count_launches();
+        return cudaGetLastError();
+    }
+    const int slots = xpair_slots<EPI, SCHED, DUAL, B_MN>();
+    if (slots <= 0) return cudaErrorLaunchOutOfResources;
+    const long long clusters = units < slots ? units : slots;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(kXThreads, 1, 1);
+    cfg.dynamicSmemBytes = XCfg<true>::SMEM;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     count_launches();
-    return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, true>, mA0, mA1, mB0, mB1, mSA0,
+                              mSA1, mSB0, mSB1, d);
+}
+
+// CTA pairs where the row units come in pairs of one expert's tiles (and
+// always for the weight gradients, whose output rows come in 256s).
+template <int EPI, int SCHED, int DUAL, bool B_MN>
+cudaError_t xrun_any(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
+{
+    const bool pair = (SCHED == SCHED_WGRAD) ? d.M_out % (2 * XBM) == 0 : (d.pair_tab != nullptr && d.prefer_pair);
+    if (pair) return xrun<EPI, SCHED, DUAL, B_MN, true>(d, max_m_tiles, num_sms, s);
+    return xrun<EPI, SCHED, DUAL, B_MN, false>(d, max_m_tiles, num_sms, s);
 }
 
 template <int EPI, int SCHED, int DUAL, bool B_MN = false>
 cudaError_t xattr()
 {
-    return cudaFuncSetAttribute(gemm_mx_kernel<EPI, SCHED, DUAL, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                XCfg::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, XCfg<false>::SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, XCfg<true>::SMEM);
+    return e;
 }
 
 }  // namespace
@@ -671,21 +841,21 @@ cudaError_t launch_gemm_mx(const GemmDesc& d, int max_m_tiles, int num_sms, cuda
         // data-gradient GEMMs K-major (b_kmajor 1)
         case EPI_SWIGLU_FWD:
             if (d.b_kmajor) return cudaErrorInvalidValue;
-            return xrun<EPI_SWIGLU_FWD, SCHED_ROWS, DUAL_N, true>(d, max_m_tiles, num_sms, s);
+            return xrun_any<EPI_SWIGLU_FWD, SCHED_ROWS, DUAL_N, true>(d, max_m_tiles, num_sms, s);
         case EPI_SWIGLU_BWD:
             if (!d.b_kmajor) return cudaErrorInvalidValue;
-            return xrun<EPI_SWIGLU_BWD, SCHED_ROWS, DUAL_NONE, false>(d, max_m_tiles, num_sms, s);
+            return xrun_any<EPI_SWIGLU_BWD, SCHED_ROWS, DUAL_NONE, false>(d, max_m_tiles, num_sms, s);
         case EPI_STORE:
             if (d.dual == DUAL_K)
-                return d.b_kmajor ? xrun<EPI_STORE, SCHED_ROWS, DUAL_K, false>(d, max_m_tiles, num_sms, s)
+                return d.b_kmajor ? xrun_any<EPI_STORE, SCHED_ROWS, DUAL_K, false>(d, max_m_tiles, num_sms, s)
                                   : cudaErrorInvalidValue;
             return d.b_kmajor ? cudaErrorInvalidValue
-                              : xrun<EPI_STORE, SCHED_ROWS, DUAL_NONE, true>(d, max_m_tiles, num_sms, s);
+                              : xrun_any<EPI_STORE, SCHED_ROWS, DUAL_NONE, true>(d, max_m_tiles, num_sms, s);
         default: return cudaErrorInvalidValue;
         }
     }
-    return d.dual == DUAL_N ? xrun<EPI_WGRAD, SCHED_WGRAD, DUAL_N, false>(d, max_m_tiles, num_sms, s)
-                            : xrun<EPI_WGRAD, SCHED_WGRAD, DUAL_NONE, false>(d, max_m_tiles, num_sms, s);
+    return d.dual == DUAL_N ? xrun_any<EPI_WGRAD, SCHED_WGRAD, DUAL_N, false>(d, max_m_tiles, num_sms, s)
+                            : xrun_any<EPI_WGRAD, SCHED_WGRAD, DUAL_NONE, false>(d, max_m_tiles, num_sms, s);
 }
 
 }  // namespace moe

@@ -191,6 +191,7 @@ mx_tiles_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__ ro
         if (COLQ) {
             // unit = (column c, 32-row block j): thread -> column tid & 127, blocks
             // (tid >> 7) and (tid >> 7) + 2; a warp reads 32 consecutive columns
+            uint32_t cw[2][8];   // COLQ 2: the codes of both units, four rows per word
 #pragma unroll
             for (int p = 0; p < 2; ++p) {
                 const int c = tid & 127, j = (tid >> 7) + 2 * p;
@@ -210,16 +211,32 @@ mx_tiles_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__ ro
                     dst[1] = w1;
                     sfc[((size_t)cb * (rows_cap / 128) + rb) * 512 + atom_byte(c, j)] = eb;
                 } else {
-                    const float s = mx_inv(e);
+                    const float sc = mx_inv(e);
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const uint32_t w = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(v[i] * s, v[i + 1] * s),
-                                                                              __NV_SATFINITE, __NV_E4M3);
-                        qc[(size_t)(r0 + 32 * j + i) * C + c0 + c] = (uint8_t)(w & 0xFF);
-                        qc[(size_t)(r0 + 32 * j + i + 1) * C + c0 + c] = (uint8_t)(w >> 8);
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        cw[p][i] = e4m3x4(v[4 * i] * sc, v[4 * i + 1] * sc, v[4 * i + 2] * sc, v[4 * i + 3] * sc);
                     const int e_grp = r0 / grp, kb = (r0 % grp) / 128;
                     sfc[(((size_t)e_grp * C + c0) / 128 * (grp / 128) + kb) * 512 + atom_byte(c, j)] = eb;
+                }
+            }
+            if (COLQ == 2) {
+                // in-place codes: through shared memory (the tile buffer, now
+                // read), then out in 16-byte row chunks
+                constexpr int kCS = 144;                  // code row stride, bytes
+                uint8_t* ct = reinterpret_cast<uint8_t*>(&tile[0][0]);
+                __syncthreads();
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int c = tid & 127, j = (tid >> 7) + 2 * p;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ct[(32 * j + i) * kCS + c] = (uint8_t)(cw[p][i >> 2] >> (8 * (i & 3)));
+                }
+                __syncthreads();
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int idx = tid + 256 * q4, row = idx >> 3, ch = idx & 7;
+                    *reinterpret_cast<uint4*>(qc + (size_t)(r0 + row) * C + c0 + 16 * ch) =
+                        *reinterpret_cast<const uint4*>(ct + row * kCS + 16 * ch);
                 }
             }
         }
