@@ -51,16 +51,21 @@ constexpr int kXGroupN = 16;
 constexpr int kAccCols = 256;                    // the accumulator
 constexpr int kSfCols = 12;                      // scale columns of one stage: A 4, B 2 x 4
 
-template <bool PAIR>
+// STG: bytes of epilogue staging for TMA stores (the weight-gradient GEMMs:
+// 8 warps x two 32-row x 128-byte buffers)
+template <bool PAIR, int STG = 0>
 struct XCfg {
     static constexpr int A_BYTES = XBM * XBK;
     static constexpr int B_ROWS = PAIR ? XBN / 2 : XBN;  // B rows (n) staged by this CTA
     static constexpr int B_BYTES = B_ROWS * XBK;
     static constexpr int SF_BYTES = 3 * 512;     // A atom, then B atoms of the two 128-column parts
     static constexpr int STAGE = A_BYTES + B_BYTES + 2048;   // (SF region padded to keep 1 KB alignment)
-    static constexpr int STAGES = (kXSmemMax - 1024 - 256) / STAGE;
-    static constexpr int SMEM = 1024 + STAGES * STAGE + 256;
+    static constexpr int STAGES = (kXSmemMax - 1024 - 256 - STG) / STAGE;
+    static constexpr int SMEM = 1024 + STAGES * STAGE + STG + 256;
 };
+constexpr int kWgradStaging = 8 * 2 * 4096;
+template <int SCHED>
+constexpr int staging_bytes() { return SCHED == SCHED_WGRAD ? kWgradStaging : 0; }
 static_assert(kAccCols + kSfCols * XCfg<true>::STAGES <= 512, "tensor memory");
 static_assert(kAccCols + kSfCols * XCfg<false>::STAGES <= 512, "tensor memory");
 
@@ -242,14 +247,16 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
                const __grid_constant__ CUtensorMap mSA0, const __grid_constant__ CUtensorMap mSA1,
                const __grid_constant__ CUtensorMap mSB0, const __grid_constant__ CUtensorMap mSB1,
+               const __grid_constant__ CUtensorMap mO0, const __grid_constant__ CUtensorMap mO1,
                const GemmDesc d)
 {
-    using C = XCfg<PAIR>;
+    using C = XCfg<PAIR, staging_bytes<SCHED>()>;
     constexpr int NW = (DUAL == DUAL_N) ? XBN / 2 : XBN;   // output columns per tile
     static_assert(!B_MN || (SCHED == SCHED_ROWS && DUAL != DUAL_K), "MN-major B: forward GEMMs");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+    const uint32_t staging = ptx::smem_u32(smem + C::STAGES * C::STAGE);   // 1024-aligned
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE + staging_bytes<SCHED>());
     // full[S], empty[S], accf, acce, final
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -523,20 +530,36 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
             // ---- epilogue from registers (pairs 0-31: part-0 columns, 32-63: part 1)
             float v[8], x[8];
             if (SCHED == SCHED_WGRAD) {
-                const size_t ob = (size_t)t.e * d.o_estride + (size_t)arow * d.ldo;
-                __nv_bfloat16* Olo = static_cast<__nv_bfloat16*>(d.O0) + ob + col_lo;
-                __nv_bfloat16* Ohi = static_cast<__nv_bfloat16*>(DUAL == DUAL_N ? d.O1 : d.O0) + ob + col_hi;
+                // this warp's 32 rows x (64 part-0 + 64 part-1) columns go out by
+                // TMA: bf16 into two 128-byte-swizzled staging buffers (16-byte
+                // chunk j of row r at chunk j ^ (r % 8)), one bulk store each
+                const uint32_t stg = staging + (uint32_t)(warp - 2) * 8192u;
+                if (lane == 0) ptx::bulk_wait_read<0>();   // the previous tile's stores have read them
+                __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    get8(acc, 4 * j, v);
-                    st8(Olo + 8 * j, v);
-                }
-                if (hi_ok) {
+                for (int part = 0; part < 2; ++part) {
+                    if (part == 1 && !hi_ok) break;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        get8(acc, 32 + 4 * j, v);
-                        st8(Ohi + 8 * j, v);
+                        get8(acc, 32 * part + 4 * j, v);
+                        uint4 u4;
+                        __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&u4);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) h2[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                        const uint32_t addr = stg + 4096u * part + (uint32_t)lane * 128u +
+                                              (uint32_t)((j ^ (lane & 7)) * 16);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(u4.x), "r"(u4.y),
+                                     "r"(u4.z), "r"(u4.w)
+                                     : "memory");
                     }
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int y = t.e * d.M_out + t.m * XBM + q * 32;
+                    ptx::tma_store_2d(&mO0, stg, col_lo, y);
+                    if (hi_ok) ptx::tma_store_2d(DUAL == DUAL_N ? &mO1 : &mO0, stg + 4096u, col_hi, y);
+                    ptx::bulk_commit();
                 }
             } else if (arow < t.alloc_end) {
                 const bool valid = arow < t.valid_end;
@@ -645,6 +668,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
         }
     }
 
+    if (SCHED == SCHED_WGRAD && warp >= 2 && lane == 0) ptx::bulk_wait_all();   // stores complete before exit
     ptx::tc_fence_before();
     if (PAIR) ptx::cluster_sync();   // both CTAs done with TMEM and with remote signals
     else __syncthreads();
@@ -685,6 +709,26 @@ bool mapx(CUtensorMap* m, const void* ptr, long long rows, long long cols, long 
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major bf16 output rows x cols (row stride ld elements), written in
+// 32-row x 64-column boxes with the 128-byte swizzle.
+bool map_out(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld)
+{
+    if (!ptr) {   // unused output map: any valid map will do
+        static __nv_bfloat16 dummy[64] __attribute__((aligned(16)));
+        ptr = dummy;
+        rows = 1;
+        cols = 64;
+        ld = 64;
+    }
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {64u, rows < 32 ? (cuuint32_t)rows : 32u};
+    cuuint32_t es[2] = {1u, 1u};
+    return g_encx(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Scale atoms as a [natoms * 4][128] byte tensor read in 128 x 4 boxes (one atom).
 bool map_atoms(CUtensorMap* m, const void* ptr, long long natoms)
 {
@@ -710,7 +754,7 @@ int xpair_slots()
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3(2, 1, 1);
         cfg.blockDim = dim3(kXThreads, 1, 1);
-        cfg.dynamicSmemBytes = XCfg<true>::SMEM;
+        cfg.dynamicSmemBytes = XCfg<true, staging_bytes<SCHED>()>::SMEM;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
@@ -726,7 +770,7 @@ template <int EPI, int SCHED, int DUAL, bool B_MN, bool PAIR>
 cudaError_t xrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
 {
     constexpr int NW = (DUAL == DUAL_N) ? XBN / 2 : XBN;
-    CUtensorMap mA0, mA1, mB0, mB1, mSA0, mSA1, mSB0, mSB1;
+    CUtensorMap mA0, mA1, mB0, mB1, mSA0, mSA1, mSB0, mSB1, mO0, mO1;
     bool ok = true;
     long long units;
     const long long num_n = (d.N + NW - 1) / NW;
@@ -764,13 +808,19 @@ cudaError_t xrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s
         ok &= map_atoms(&mSB0, d.XB0, (d.N / 128) * KB);
         ok &= map_atoms(&mSB1, d.XB1 ? d.XB1 : d.XB0, (d.N / 128) * KB);
         units = (long long)d.E * (d.M_out / (PAIR ? 2 * XBM : XBM)) * num_n;
+        ok &= map_out(&mO0, d.O0, (long long)d.E * d.M_out, d.N, d.ldo);
+        ok &= map_out(&mO1, (DUAL == DUAL_N) ? d.O1 : d.O0, (long long)d.E * d.M_out, d.N, d.ldo);
+    }
+    if (SCHED == SCHED_ROWS) {   // (the row GEMMs store with plain 16-byte stores)
+        ok &= map_out(&mO0, nullptr, 0, 0, 0);
+        mO1 = mO0;
     }
     if (!ok) return cudaErrorInvalidValue;
     if (units <= 0) return cudaSuccess;
     if (!PAIR) {
         const int grid = (int)(units < num_sms ? units : num_sms);
-        gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, false><<<grid, kXThreads, XCfg<false>::SMEM, s>>>(
-            mA0, mA1, mB0, mB1, mSA0, mSA1, mSB0, mSB1, d);
+        gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, false><<<grid, kXThreads, XCfg<false, staging_bytes<SCHED>()>::SMEM, s>>>(
+            mA0, mA1, mB0, mB1, mSA0, mSA1, mSB0, mSB1, mO0, mO1, d);
         count_launches();
         return cudaGetLastError();
     }
@@ -785,13 +835,13 @@ cudaError_t xrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     cfg.blockDim = dim3(kXThreads, 1, 1);
-    cfg.dynamicSmemBytes = XCfg<true>::SMEM;
+    cfg.dynamicSmemBytes = XCfg<true, staging_bytes<SCHED>()>::SMEM;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     count_launches();
     return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, true>, mA0, mA1, mB0, mB1, mSA0,
-                              mSA1, mSB0, mSB1, d);
+                              mSA1, mSB0, mSB1, mO0, mO1, d);
 }
 
 // CTA pairs where the row units come in pairs of one expert's tiles (and
@@ -808,10 +858,11 @@ template <int EPI, int SCHED, int DUAL, bool B_MN = false>
 cudaError_t xattr()
 {
     cudaError_t e = cudaFuncSetAttribute(gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, XCfg<false>::SMEM);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         XCfg<false, staging_bytes<SCHED>()>::SMEM);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, XCfg<true>::SMEM);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, XCfg<true, staging_bytes<SCHED>()>::SMEM);
     return e;
 }
 
