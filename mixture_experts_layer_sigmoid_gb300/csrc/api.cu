@@ -926,11 +926,8 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
     d.XB0 = xs(wq.s[0]); d.XB1 = xs(wq.s[1]);
     d.O0 = A; d.O1 = U; d.O2 = Hh; d.ldo = F; d.status = status;
     if (L.fold) { d.gates = gates; d.slot_of = slotof; }   // Hh = g silu(A) U
+    d.Qrows = ws + L.hq; d.Qatoms = ws + L.sh;              // fc2's A operand, from the epilogue
     MOE_STAGE(ST_FC1, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
-    {
-        MxQuantJob j{Hh, meta + 1, Rp, F, Rp, ws + L.hq, ws + L.sh, nullptr, nullptr, 0};
-        MOE_STAGE(ST_QROWS, launch_mx_quant(j, s));
-    }
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
     d.N = H; d.K = F; d.E = E;

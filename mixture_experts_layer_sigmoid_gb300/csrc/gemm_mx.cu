@@ -36,6 +36,7 @@
 // r + 32 j, one byte per sub-block.
 #include "internal.h"
 #include "epilogue.cuh"
+#include "mx.cuh"
 #include "ptx.cuh"
 
 #include <cudaTypedefs.h>
@@ -570,23 +571,42 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                     __nv_bfloat16* O0 = static_cast<__nv_bfloat16*>(d.O0) + orow + col_lo;
                     __nv_bfloat16* O1 = static_cast<__nv_bfloat16*>(d.O1) + orow + col_lo;
                     __nv_bfloat16* O2 = static_cast<__nv_bfloat16*>(d.O2) + orow + col_lo;
+                    // this thread's 64 columns of h are two whole 32-column MX blocks
+                    // of its row: their codes (of the stored bf16 values) and scales
+                    // go out here, as fc2's A operand
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float hv[8];
-                        get8(acc, 4 * j, v);
-                        get8(acc, 32 + 4 * j, x);
+                    for (int blk = 0; blk < 2; ++blk) {
+                        float hb[32];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            if (valid) {
-                                const SwigluFwd r(v[i], x[i]);
-                                hv[i] = r.h * grow;
-                            } else {
-                                v[i] = x[i] = hv[i] = 0.f;
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int j = 4 * blk + jj;
+                            float hv[8];
+                            get8(acc, 4 * j, v);
+                            get8(acc, 32 + 4 * j, x);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                if (valid) {
+                                    const SwigluFwd r(v[i], x[i]);
+                                    hv[i] = r.h * grow;
+                                } else {
+                                    v[i] = x[i] = hv[i] = 0.f;
+                                }
+                                hb[8 * jj + i] = __bfloat162float(__float2bfloat16_rn(hv[i]));
                             }
+                            st8(O0 + 8 * j, v);
+                            st8(O1 + 8 * j, x);
+                            st8(O2 + 8 * j, hv);
                         }
-                        st8(O0 + 8 * j, v);
-                        st8(O1 + 8 * j, x);
-                        st8(O2 + 8 * j, hv);
+                        if (d.Qrows) {
+                            uint4 c0, c1;
+                            const int e = encode32(hb, c0, c1);
+                            const int col = col_lo + 32 * blk;
+                            uint4* dst = reinterpret_cast<uint4*>(d.Qrows + (size_t)arow * d.N + col);
+                            dst[0] = c0;
+                            dst[1] = c1;
+                            d.Qatoms[((size_t)(arow >> 7) * (d.N / 128) + (col >> 7)) * 512 +
+                                     atom_byte(arow & 127, (col & 127) >> 5)] = (uint8_t)(e + 127);
+                        }
                     }
                 } else if (EPI == EPI_SWIGLU_BWD) {
 #pragma unroll

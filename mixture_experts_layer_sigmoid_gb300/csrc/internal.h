@@ -87,6 +87,8 @@ struct GemmDesc {
     int rows_cap;   // SCHED_WGRAD: row capacity of the transposed operands
     // MXFP8 only: UE8M0 scale atoms of the operands (see launch_mx_quant)
     const uint8_t* XA0; const uint8_t* XA1; const uint8_t* XB0; const uint8_t* XB1;
+    // MXFP8 SWIGLU_FWD: also the MX row codes [rows][N] of h (O2) and their atoms
+    uint8_t* Qrows; uint8_t* Qatoms;
     // memory-efficient permutation (gates != null): g of permuted row r is
     // gates[slot_of[r]]. SWIGLU_FWD stores O2 = g h; SWIGLU_BWD treats the
     // accumulator as dh', writes dA, dU of dh = g dh', O2 = g h (if O2 is

@@ -27,36 +27,12 @@
 //                      place [rows][C] (expert weights read MN-major), each
 //                      with its scale atoms.
 #include "internal.h"
+#include "mx.cuh"
 
 #include <cuda_fp8.h>
 
 namespace moe {
 namespace {
-
-// e of a block maximum (bf16 or fp32 value, non-negative): amax = 1.f 2^(E-127)
-// with f the 23-bit fraction; amax <= 448 2^e with 448 = 1.75 2^8.
-__device__ __forceinline__ int mx_exp(float amax)
-{
-    const uint32_t b = __float_as_uint(amax);
-    const int E = (int)(b >> 23);
-    if (E == 0) return -127;                       // zero or below 2^-126
-    const int e = (b & 0x7FFFFFu) <= 0x600000u ? E - 135 : E - 134;
-    return e < -127 ? -127 : e;
-}
-
-// 2^-e as an fp32 (e in [-127, 127]; 2^-127 is a subnormal, still exact)
-__device__ __forceinline__ float mx_inv(int e)
-{
-    const int be = 127 - e;                        // biased exponent of 2^-e
-    return be >= 1 ? __uint_as_float((uint32_t)be << 23) : __uint_as_float(0x00400000u);
-}
-
-__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
-{
-    const uint32_t lo = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-    const uint32_t hi = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-    return lo | (hi << 16);
-}
 
 __device__ __forceinline__ void unpack8f(const uint4& u, float* v)
 {
@@ -68,19 +44,6 @@ __device__ __forceinline__ void unpack8f(const uint4& u, float* v)
         v[2 * i + 1] = f.y;
     }
 }
-
-// 32 values -> 32 codes (two 16-byte words) with scale 2^e
-__device__ __forceinline__ void encode32(const float* v, int e, uint4& c0, uint4& c1)
-{
-    const float s = mx_inv(e);
-    uint32_t w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = e4m3x4(v[4 * i] * s, v[4 * i + 1] * s, v[4 * i + 2] * s, v[4 * i + 3] * s);
-    c0 = make_uint4(w[0], w[1], w[2], w[3]);
-    c1 = make_uint4(w[4], w[5], w[6], w[7]);
-}
-
-__device__ __forceinline__ size_t atom_byte(int m, int j) { return (size_t)(16 * (m & 31) + 4 * (m >> 5) + j); }
 
 // Blocks [0, T): token t -> row codes of its k permuted rows. Blocks
 // [T, T+E): pad rows of expert e (zero codes, scale byte 0). One warp per
@@ -176,12 +139,8 @@ mx_tiles_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__ ro
                 float v[32];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) unpack8f(*reinterpret_cast<const uint4*>(&tile[m][32 * j + 8 * c]), v + 8 * c);
-                float a = 0.f;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(v[i]));
-                const int e = mx_exp(a);
                 uint4 w0, w1;
-                encode32(v, e, w0, w1);
+                const int e = encode32(v, w0, w1);
                 uint4* dst = reinterpret_cast<uint4*>(q + (size_t)(r0 + m) * C + c0 + 32 * j);
                 dst[0] = w0;
                 dst[1] = w1;
@@ -205,7 +164,7 @@ mx_tiles_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__ ro
                 const uint8_t eb = (uint8_t)(e + 127);
                 if (COLQ == 1) {
                     uint4 w0, w1;
-                    encode32(v, e, w0, w1);
+                    encode32(v, w0, w1);
                     uint4* dst = reinterpret_cast<uint4*>(qc + (size_t)(c0 + c) * rows_cap + r0 + 32 * j);
                     dst[0] = w0;
                     dst[1] = w1;
