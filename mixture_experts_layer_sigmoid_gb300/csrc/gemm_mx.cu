@@ -64,9 +64,14 @@ struct XCfg {
     static constexpr int STAGES = (kXSmemMax - 1024 - 256 - STG) / STAGE;
     static constexpr int SMEM = 1024 + STAGES * STAGE + STG + 256;
 };
-constexpr int kWgradStaging = 8 * 2 * 4096;
-template <int SCHED>
-constexpr int staging_bytes() { return SCHED == SCHED_WGRAD ? kWgradStaging : 0; }
+constexpr int kStoreStaging = 8 * 2 * 4096;
+// the weight gradients, the plain-store and the SwiGLU-forward row GEMMs
+// store through staging
+template <int EPI, int SCHED>
+constexpr int staging_bytes()
+{
+    return (SCHED == SCHED_WGRAD || EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD) ? kStoreStaging : 0;
+}
 static_assert(kAccCols + kSfCols * XCfg<true>::STAGES <= 512, "tensor memory");
 static_assert(kAccCols + kSfCols * XCfg<false>::STAGES <= 512, "tensor memory");
 
@@ -249,15 +254,15 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                const __grid_constant__ CUtensorMap mSA0, const __grid_constant__ CUtensorMap mSA1,
                const __grid_constant__ CUtensorMap mSB0, const __grid_constant__ CUtensorMap mSB1,
                const __grid_constant__ CUtensorMap mO0, const __grid_constant__ CUtensorMap mO1,
-               const GemmDesc d)
+               const __grid_constant__ CUtensorMap mO2, const GemmDesc d)
 {
-    using C = XCfg<PAIR, staging_bytes<SCHED>()>;
+    using C = XCfg<PAIR, staging_bytes<EPI, SCHED>()>;
     constexpr int NW = (DUAL == DUAL_N) ? XBN / 2 : XBN;   // output columns per tile
     static_assert(!B_MN || (SCHED == SCHED_ROWS && DUAL != DUAL_K), "MN-major B: forward GEMMs");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t staging = ptx::smem_u32(smem + C::STAGES * C::STAGE);   // 1024-aligned
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE + staging_bytes<SCHED>());
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE + staging_bytes<EPI, SCHED>());
     // full[S], empty[S], accf, acce, final
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -530,10 +535,11 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
             }
             // ---- epilogue from registers (pairs 0-31: part-0 columns, 32-63: part 1)
             float v[8], x[8];
-            if (SCHED == SCHED_WGRAD) {
-                // this warp's 32 rows x (64 part-0 + 64 part-1) columns go out by
-                // TMA: bf16 into two 128-byte-swizzled staging buffers (16-byte
-                // chunk j of row r at chunk j ^ (r % 8)), one bulk store each
+            // this warp's 32 rows x (64 part-0 + 64 part-1) columns go out by TMA:
+            // bf16 into two 128-byte-swizzled staging buffers (16-byte chunk j of
+            // row r at chunk j ^ (r % 8)), one bulk store each; zero rows where
+            // `zero` (pad rows of a segment)
+            auto store_staged = [&](int y, bool zero) {
                 const uint32_t stg = staging + (uint32_t)(warp - 2) * 8192u;
                 if (lane == 0) ptx::bulk_wait_read<0>();   // the previous tile's stores have read them
                 __syncwarp();
@@ -546,7 +552,8 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                         uint4 u4;
                         __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&u4);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) h2[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                        for (int i = 0; i < 4; ++i)
+                            h2[i] = zero ? __floats2bfloat162_rn(0.f, 0.f) : __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
                         const uint32_t addr = stg + 4096u * part + (uint32_t)lane * 128u +
                                               (uint32_t)((j ^ (lane & 7)) * 16);
                         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(u4.x), "r"(u4.y),
@@ -557,23 +564,58 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    const int y = t.e * d.M_out + t.m * XBM + q * 32;
                     ptx::tma_store_2d(&mO0, stg, col_lo, y);
                     if (hi_ok) ptx::tma_store_2d(DUAL == DUAL_N ? &mO1 : &mO0, stg + 4096u, col_hi, y);
                     ptx::bulk_commit();
                 }
-            } else if (arow < t.alloc_end) {
-                const bool valid = arow < t.valid_end;
-                const size_t orow = (size_t)arow * d.ldo;
-                // routing weight of the row when it is folded into h
-                const float grow = (d.gates && valid) ? d.gates[d.slot_of[arow]] : 1.f;
-                if (EPI == EPI_SWIGLU_FWD) {
-                    __nv_bfloat16* O0 = static_cast<__nv_bfloat16*>(d.O0) + orow + col_lo;
-                    __nv_bfloat16* O1 = static_cast<__nv_bfloat16*>(d.O1) + orow + col_lo;
-                    __nv_bfloat16* O2 = static_cast<__nv_bfloat16*>(d.O2) + orow + col_lo;
-                    // this thread's 64 columns of h are two whole 32-column MX blocks
-                    // of its row: their codes (of the stored bf16 values) and scales
-                    // go out here, as fc2's A operand
+            };
+            if (SCHED == SCHED_WGRAD) {
+                store_staged(t.e * d.M_out + t.m * XBM + q * 32, false);
+            } else if (EPI == EPI_STORE) {
+                // segments are 128-row aligned: a warp's 32 rows are all inside the
+                // tile's expert or (a pair's ghost half) all past it
+                if (t.row0 + q * 32 < t.alloc_end) store_staged(t.row0 + q * 32, arow >= t.valid_end);
+            } else if (EPI == EPI_SWIGLU_FWD) {
+                // a, u, then h = silu(a) u (g h with the routing weight folded in)
+                // of this warp's 32 rows x 64 columns, through the two staging
+                // buffers; h's MX row codes (fc2's A operand) from this thread
+                if (t.row0 + q * 32 < t.alloc_end) {
+                    const bool valid = arow < t.valid_end;
+                    const float grow = (d.gates && valid) ? d.gates[d.slot_of[arow]] : 1.f;
+                    const int y = t.row0 + q * 32;
+                    const uint32_t stg = staging + (uint32_t)(warp - 2) * 8192u;
+                    auto put = [&](uint32_t buf, int j, const float* f) {
+                        uint4 u4;
+                        __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&u4);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) h2[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+                        const uint32_t addr = buf + (uint32_t)lane * 128u + (uint32_t)((j ^ (lane & 7)) * 16);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(u4.x), "r"(u4.y),
+                                     "r"(u4.z), "r"(u4.w)
+                                     : "memory");
+                    };
+                    if (lane == 0) ptx::bulk_wait_read<0>();   // the previous tile's stores have read them
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        get8(acc, 4 * j, v);
+                        get8(acc, 32 + 4 * j, x);
+                        if (!valid) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) v[i] = x[i] = 0.f;
+                        }
+                        put(stg, j, v);
+                        put(stg + 4096u, j, x);
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&mO0, stg, col_lo, y);
+                        ptx::tma_store_2d(&mO1, stg + 4096u, col_lo, y);
+                        ptx::bulk_commit();
+                        ptx::bulk_wait_read<0>();
+                    }
+                    __syncwarp();
 #pragma unroll
                     for (int blk = 0; blk < 2; ++blk) {
                         float hb[32];
@@ -585,17 +627,10 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                             get8(acc, 32 + 4 * j, x);
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
-                                if (valid) {
-                                    const SwigluFwd r(v[i], x[i]);
-                                    hv[i] = r.h * grow;
-                                } else {
-                                    v[i] = x[i] = hv[i] = 0.f;
-                                }
+                                hv[i] = valid ? SwigluFwd(v[i], x[i]).h * grow : 0.f;
                                 hb[8 * jj + i] = __bfloat162float(__float2bfloat16_rn(hv[i]));
                             }
-                            st8(O0 + 8 * j, v);
-                            st8(O1 + 8 * j, x);
-                            st8(O2 + 8 * j, hv);
+                            put(stg, j, hv);
                         }
                         if (d.Qrows) {
                             uint4 c0, c1;
@@ -608,7 +643,19 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                                      atom_byte(arow & 127, (col & 127) >> 5)] = (uint8_t)(e + 127);
                         }
                     }
-                } else if (EPI == EPI_SWIGLU_BWD) {
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&mO2, stg, col_lo, y);
+                        ptx::bulk_commit();
+                    }
+                }
+            } else if (arow < t.alloc_end) {
+                const bool valid = arow < t.valid_end;
+                const size_t orow = (size_t)arow * d.ldo;
+                // routing weight of the row when it is folded into h
+                const float grow = (d.gates && valid) ? d.gates[d.slot_of[arow]] : 1.f;
+                if (EPI == EPI_SWIGLU_BWD) {
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
                         if (part == 1 && !hi_ok) break;
@@ -668,27 +715,12 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                             d.dg_part[(size_t)arow * d.dg_ld + col / 64] = dgp;   // 0 past the computed rows
                         }
                     }
-                } else {
-#pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        if (part == 1 && !hi_ok) break;
-                        __nv_bfloat16* O0 = static_cast<__nv_bfloat16*>(d.O0) + orow + (part ? col_hi : col_lo);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            get8(acc, 32 * part + 4 * j, v);
-                            if (!valid) {
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) v[i] = 0.f;
-                            }
-                            st8(O0 + 8 * j, v);
-                        }
-                    }
                 }
             }
         }
     }
 
-    if (SCHED == SCHED_WGRAD && warp >= 2 && lane == 0) ptx::bulk_wait_all();   // stores complete before exit
+    if (staging_bytes<EPI, SCHED>() && warp >= 2 && lane == 0) ptx::bulk_wait_all();   // stores complete before exit
     ptx::tc_fence_before();
     if (PAIR) ptx::cluster_sync();   // both CTAs done with TMEM and with remote signals
     else __syncthreads();
@@ -774,7 +806,7 @@ int xpair_slots()
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3(2, 1, 1);
         cfg.blockDim = dim3(kXThreads, 1, 1);
-        cfg.dynamicSmemBytes = XCfg<true, staging_bytes<SCHED>()>::SMEM;
+        cfg.dynamicSmemBytes = XCfg<true, staging_bytes<EPI, SCHED>()>::SMEM;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
@@ -790,7 +822,7 @@ template <int EPI, int SCHED, int DUAL, bool B_MN, bool PAIR>
 cudaError_t xrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
 {
     constexpr int NW = (DUAL == DUAL_N) ? XBN / 2 : XBN;
-    CUtensorMap mA0, mA1, mB0, mB1, mSA0, mSA1, mSB0, mSB1, mO0, mO1;
+    CUtensorMap mA0, mA1, mB0, mB1, mSA0, mSA1, mSB0, mSB1, mO0, mO1, mO2;
     bool ok = true;
     long long units;
     const long long num_n = (d.N + NW - 1) / NW;
@@ -831,16 +863,20 @@ cudaError_t xrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s
         ok &= map_out(&mO0, d.O0, (long long)d.E * d.M_out, d.N, d.ldo);
         ok &= map_out(&mO1, (DUAL == DUAL_N) ? d.O1 : d.O0, (long long)d.E * d.M_out, d.N, d.ldo);
     }
-    if (SCHED == SCHED_ROWS) {   // (the row GEMMs store with plain 16-byte stores)
-        ok &= map_out(&mO0, nullptr, 0, 0, 0);
-        mO1 = mO0;
+    if (SCHED == SCHED_ROWS) {   // (the SwiGLU-backward epilogue stores with plain 16-byte stores)
+        const bool staged = EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD;
+        ok &= map_out(&mO0, staged ? d.O0 : nullptr, d.a_rows, d.N, d.ldo);
+        ok &= map_out(&mO1, EPI == EPI_SWIGLU_FWD ? d.O1 : nullptr, d.a_rows, d.N, d.ldo);
+        ok &= map_out(&mO2, EPI == EPI_SWIGLU_FWD ? d.O2 : nullptr, d.a_rows, d.N, d.ldo);
+    } else {
+        mO2 = mO0;
     }
     if (!ok) return cudaErrorInvalidValue;
     if (units <= 0) return cudaSuccess;
     if (!PAIR) {
         const int grid = (int)(units < num_sms ? units : num_sms);
-        gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, false><<<grid, kXThreads, XCfg<false, staging_bytes<SCHED>()>::SMEM, s>>>(
-            mA0, mA1, mB0, mB1, mSA0, mSA1, mSB0, mSB1, mO0, mO1, d);
+        gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, false><<<grid, kXThreads, XCfg<false, staging_bytes<EPI, SCHED>()>::SMEM, s>>>(
+            mA0, mA1, mB0, mB1, mSA0, mSA1, mSB0, mSB1, mO0, mO1, mO2, d);
         count_launches();
         return cudaGetLastError();
     }
@@ -855,13 +891,13 @@ cudaError_t xrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     cfg.blockDim = dim3(kXThreads, 1, 1);
-    cfg.dynamicSmemBytes = XCfg<true, staging_bytes<SCHED>()>::SMEM;
+    cfg.dynamicSmemBytes = XCfg<true, staging_bytes<EPI, SCHED>()>::SMEM;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     count_launches();
     return cudaLaunchKernelEx(&cfg, gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, true>, mA0, mA1, mB0, mB1, mSA0,
-                              mSA1, mSB0, mSB1, mO0, mO1, d);
+                              mSA1, mSB0, mSB1, mO0, mO1, mO2, d);
 }
 
 // CTA pairs where the row units come in pairs of one expert's tiles (and
@@ -879,10 +915,10 @@ cudaError_t xattr()
 {
     cudaError_t e = cudaFuncSetAttribute(gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         XCfg<false, staging_bytes<SCHED>()>::SMEM);
+                                         XCfg<false, staging_bytes<EPI, SCHED>()>::SMEM);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemm_mx_kernel<EPI, SCHED, DUAL, B_MN, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, XCfg<true, staging_bytes<SCHED>()>::SMEM);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, XCfg<true, staging_bytes<EPI, SCHED>()>::SMEM);
     return e;
 }
 
