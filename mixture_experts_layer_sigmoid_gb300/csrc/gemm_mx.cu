@@ -65,12 +65,11 @@ struct XCfg {
     static constexpr int SMEM = 1024 + STAGES * STAGE + STG + 256;
 };
 constexpr int kStoreStaging = 8 * 2 * 4096;
-// the weight gradients, the plain-store and the SwiGLU-forward row GEMMs
-// store through staging
+// every epilogue stores through staging
 template <int EPI, int SCHED>
 constexpr int staging_bytes()
 {
-    return (SCHED == SCHED_WGRAD || EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD) ? kStoreStaging : 0;
+    return (SCHED == SCHED_WGRAD || SCHED == SCHED_ROWS) ? kStoreStaging : 0;
 }
 static_assert(kAccCols + kSfCols * XCfg<true>::STAGES <= 512, "tensor memory");
 static_assert(kAccCols + kSfCols * XCfg<false>::STAGES <= 512, "tensor memory");
@@ -650,22 +649,27 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                         ptx::bulk_commit();
                     }
                 }
-            } else if (arow < t.alloc_end) {
-                const bool valid = arow < t.valid_end;
-                const size_t orow = (size_t)arow * d.ldo;
-                // routing weight of the row when it is folded into h
-                const float grow = (d.gates && valid) ? d.gates[d.slot_of[arow]] : 1.f;
-                if (EPI == EPI_SWIGLU_BWD) {
+            } else if (EPI == EPI_SWIGLU_BWD) {
+                // dA, dU of this warp's 32 rows x (64 part-0 + 64 part-1) columns,
+                // from dh (the accumulator) and the saved a, u, through the two
+                // staging buffers (folded gates: g h for the fc2 weight gradient
+                // and the partial dot products dg = <dh', h> too)
+                if (t.row0 + q * 32 < t.alloc_end) {
+                    const bool valid = arow < t.valid_end;
+                    const bool fold = d.gates != nullptr;
+                    const float grow = (fold && valid) ? d.gates[d.slot_of[arow]] : 1.f;
+                    const int y = t.row0 + q * 32;
+                    const size_t orow = (size_t)arow * d.ldo;
+                    const uint32_t stg = staging + (uint32_t)(warp - 2) * 8192u;
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
                         if (part == 1 && !hi_ok) break;
-                        const size_t o = orow + (part ? col_hi : col_lo);
+                        if (lane == 0) ptx::bulk_wait_read<0>();   // both buffers free
+                        __syncwarp();
+                        const int col = part ? col_hi : col_lo;
+                        const size_t o = orow + col;
                         const __nv_bfloat16* X0 = static_cast<const __nv_bfloat16*>(d.X0) + o;
                         const __nv_bfloat16* X1 = static_cast<const __nv_bfloat16*>(d.X1) + o;
-                        __nv_bfloat16* O0 = static_cast<__nv_bfloat16*>(d.O0) + o;
-                        __nv_bfloat16* O1 = static_cast<__nv_bfloat16*>(d.O1) + o;
-                        const bool fold = d.gates != nullptr;
-                        // folded gates: g h (the fc2 weight-gradient operand), from registers
                         __nv_bfloat16* O2 = fold && d.O2 ? static_cast<__nv_bfloat16*>(d.O2) + o : nullptr;
                         float dgp = 0.f;
 #pragma unroll
@@ -705,15 +709,25 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                                         du2[i] = __floats2bfloat162_rn(r0.dU, r1.dU);
                                     }
                                 }
-                                *reinterpret_cast<uint4*>(O0 + 8 * (j0 + j)) = oa;
-                                *reinterpret_cast<uint4*>(O1 + 8 * (j0 + j)) = ou;
-                                if (O2) *reinterpret_cast<uint4*>(O2 + 8 * (j0 + j)) = oh;
+                                const int jc = j0 + j;
+                                const uint32_t sw = (uint32_t)lane * 128u + (uint32_t)((jc ^ (lane & 7)) * 16);
+                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg + sw), "r"(oa.x),
+                                             "r"(oa.y), "r"(oa.z), "r"(oa.w)
+                                             : "memory");
+                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg + 4096u + sw),
+                                             "r"(ou.x), "r"(ou.y), "r"(ou.z), "r"(ou.w)
+                                             : "memory");
+                                if (O2) *reinterpret_cast<uint4*>(O2 + 8 * jc) = oh;
                             }
                         }
-                        if (fold) {
-                            const int col = part ? col_hi : col_lo;
-                            d.dg_part[(size_t)arow * d.dg_ld + col / 64] = dgp;   // 0 past the computed rows
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(&mO0, stg, col, y);
+                            ptx::tma_store_2d(&mO1, stg + 4096u, col, y);
+                            ptx::bulk_commit();
                         }
+                        if (fold) d.dg_part[(size_t)arow * d.dg_ld + col / 64] = dgp;   // 0 past the computed rows
                     }
                 }
             }
@@ -863,10 +877,9 @@ cudaError_t xrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s
         ok &= map_out(&mO0, d.O0, (long long)d.E * d.M_out, d.N, d.ldo);
         ok &= map_out(&mO1, (DUAL == DUAL_N) ? d.O1 : d.O0, (long long)d.E * d.M_out, d.N, d.ldo);
     }
-    if (SCHED == SCHED_ROWS) {   // (the SwiGLU-backward epilogue stores with plain 16-byte stores)
-        const bool staged = EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD;
-        ok &= map_out(&mO0, staged ? d.O0 : nullptr, d.a_rows, d.N, d.ldo);
-        ok &= map_out(&mO1, EPI == EPI_SWIGLU_FWD ? d.O1 : nullptr, d.a_rows, d.N, d.ldo);
+    if (SCHED == SCHED_ROWS) {
+        ok &= map_out(&mO0, d.O0, d.a_rows, d.N, d.ldo);
+        ok &= map_out(&mO1, EPI != EPI_STORE ? d.O1 : nullptr, d.a_rows, d.N, d.ldo);
         ok &= map_out(&mO2, EPI == EPI_SWIGLU_FWD ? d.O2 : nullptr, d.a_rows, d.N, d.ldo);
     } else {
         mO2 = mO0;
