@@ -410,17 +410,20 @@ def run_ours(args, w):
     def bound_ms(n):
         return max(stage_flops(n, w) / (peak_sust * 1e12), stage_bytes(n, w) / (hbm * 1e9)) * 1e3
 
+    # One GEMM stage runs once per step as one launch, or two (CTA pairs over
+    # the multi-tile experts, then single CTAs over the one-tile experts):
+    # its work and its device time are per step either way.
     dom = max(gemms, key=lambda n: gemms[n][1])
     launches, tot_ms = gemms[dom]
-    t_launch = tot_ms / launches * 1e-3
+    t_launch = tot_ms / args.steps * 1e-3
     tensor_bound = stage_flops(dom, w) / (peak_sust * 1e12) >= stage_bytes(dom, w) / (hbm * 1e9)
     if tensor_bound:
         achieved, peak, unit = stage_flops(dom, w) / t_launch / 1e12, peak_sust, "TFLOP/s"
     else:
         achieved, peak, unit = stage_bytes(dom, w) / t_launch / 1e9, hbm, "GB/s"
     gemm_ms = sum(v[1] for v in gemms.values()) / args.steps
-    gemm_flops = sum(stage_flops(n, w) * v[0] for n, v in gemms.items()) / args.steps
-    gemm_bound_ms = sum(bound_ms(n) * v[0] for n, v in gemms.items()) / args.steps
+    gemm_flops = sum(stage_flops(n, w) for n in gemms)
+    gemm_bound_ms = sum(bound_ms(n) for n in gemms)
     roofline = {"kernel": dom, "bound": "tensor" if tensor_bound else "hbm", "achieved": achieved,
                 "peak": peak, "unit": unit, "frac": achieved / peak,
                 "peak_source": peak_name if tensor_bound else f"hbm_gbs of {peaks_kind} peaks",
@@ -431,10 +434,11 @@ def run_ours(args, w):
                                       "tensor_frac": gemm_flops / (gemm_ms * 1e-3) / 1e12 / peak_sust,
                                       "roofline_frac": gemm_bound_ms / gemm_ms,
                                       "share_of_step": gemm_ms / ms},
-                "per_gemm": {n: {"ms": v[1] / v[0], "roofline_ms": bound_ms(n),
+                "per_gemm": {n: {"ms": v[1] / args.steps, "launches": v[0] / args.steps,
+                                 "roofline_ms": bound_ms(n),
                                  "bound": "tensor" if stage_flops(n, w) / (peak_sust * 1e12) >=
                                  stage_bytes(n, w) / (hbm * 1e9) else "hbm",
-                                 "frac": bound_ms(n) / (v[1] / v[0])} for n, v in gemms.items()}}
+                                 "frac": bound_ms(n) / (v[1] / args.steps)} for n, v in gemms.items()}}
     per_stage = {n: {"launches_per_step": v[0] / args.steps, "ms_per_step": v[1] / args.steps}
                  for n, v in stages.items()}
     launches_total = sum(v[0] for v in stages.values())

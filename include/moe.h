@@ -68,7 +68,8 @@ typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
  *     K for the operand indexing output rows, 128x128 for the other), fp32
  *     accumulation ("Scalable Training of Mixture-of-Experts Models with
  *     Megatron Core", §5, blockwise FP8). The router stays fp32. Layers with
- *     a shared expert are not supported in this mode (MOE_ERR_UNSUPPORTED).
+ *     a shared expert or with capacity_factor > 0 are not supported in this
+ *     mode (MOE_ERR_UNSUPPORTED).
  *   MOE_MXFP8: bf16 activations, weights and gradients; every expert GEMM
  *     runs on E4M3 operands in the MXFP8 recipe ("Scalable Training of
  *     Mixture-of-Experts Models with Megatron Core", §5 Platform-specific
@@ -101,7 +102,8 @@ typedef struct {
                     first; a dropped assignment adds nothing to y, gets no
                     expert gradient and has dg = 0 (its routing gradient still
                     flows through the other slots' renormalised gates).
-                    MOE_FP8_BLOCK with capacity_factor > 0: UNSUPPORTED. */
+                    MOE_FP8_BLOCK or MOE_MXFP8 with capacity_factor > 0:
+                    UNSUPPORTED. */
 } moe_config_t;
 
 /* Plan flag: bracket every kernel launch of moe_forward / moe_backward with

@@ -37,6 +37,20 @@ struct Layout {
 
 bool fp8_recipe(const moe_config_t& c) { return c.dtype == MOE_FP8_BLOCK || c.dtype == MOE_MXFP8; }
 
+// The split row tables inside the pair-table block (see make_layout).
+struct SplitTabs {
+    int* full_tab;
+    int* full_off;
+    int* tail_tab;
+};
+SplitTabs split_tabs(const Layout& L, int E, const uint8_t* sv)
+{
+    int* pairtab = reinterpret_cast<int*>(const_cast<uint8_t*>(sv) + L.pairtab);
+    int* full_tab = pairtab + L.MT_max + E + 1;
+    int* full_off = full_tab + L.MT_max;
+    return {full_tab, full_off, full_off + E + 1};
+}
+
 // Quantised expert weights of an FP8 plan (the caller's weight cache, or the
 // copy a forward makes in `saved`): for W_gate, W_up (E x H x F) and W_down
 // (E x F x H), in this order, q[i] E4M3 codes in the matrix's natural layout
@@ -91,9 +105,11 @@ Layout make_layout(const moe_config_t& c, int T)
     L.kept = take(sizeof(int) * c.E);
     L.eorder = take(sizeof(int) * c.E);   // experts, longest padded segment first
     L.poff = take(sizeof(int) * (c.E + 1));
-    L.meta = take(sizeof(int) * 4);
+    L.meta = take(sizeof(int) * 8);
     L.tiletab = take(sizeof(int) * L.MT_max);
-    L.pairtab = take(sizeof(int) * ((size_t)L.MT_max + c.E + 1));   // pairs, then E+1 pair offsets
+    // pairs and their E+1 offsets; the pairs of multi-tile experts and their
+    // E+1 offsets; the tiles of one-tile experts
+    L.pairtab = take(sizeof(int) * (2 * ((size_t)L.MT_max + c.E + 1) + c.E));
     L.rowof = take(sizeof(int) * L.R);
     L.slotof = take(sizeof(int) * L.Rp_max);
     // (the FP8 layers keep only the codes of the permuted rows)
@@ -408,10 +424,12 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     MOE_STAGE(ST_ROUTER, launch_router<T>(x, a->Wr, a->b, T_, H, E, k, c.score, topk, gates, selsc,
                               reinterpret_cast<int*>(ws + L.hist), s, a->replay_topk, status,
                               reinterpret_cast<float*>(ws + L.zpart), router_zpart_floats(T_, H, E)));
+    const SplitTabs st = split_tabs(L, E, sv);
     MOE_STAGE(ST_SCAN, launch_scan(reinterpret_cast<int*>(ws + L.hist), L.NB, E, counts, poff,
                          reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab,
                                    pairtab + L.MT_max, capacity(c, T_), kept,
-                                   reinterpret_cast<int*>(sv + L.eorder)));
+                                   reinterpret_cast<int*>(sv + L.eorder), st.full_tab, st.full_off,
+                                   st.tail_tab));
     MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
     MOE_STAGE(ST_PERMUTE, launch_permute<T>(x, rowof, poff, counts, T_, H, E, k, Xp, s));
 
@@ -426,7 +444,8 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
     d.N = F; d.K = H; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
-    // a pair reads each [Wg | Wu] column tile once for both of an expert's
+    d.full_tab = st.full_tab; d.full_off = st.full_off; d.tail_tab = st.tail_tab;
+    // a pair reads each [Wg | Wu] column tile once for two of an expert's
     // 128-row units; that pays from two units per expert on (the other row
     // GEMMs only from four)
     d.prefer_pair = (long long)T_ * k >= 256ll * E;
@@ -441,6 +460,7 @@ static moe_status_t forward_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, 
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
     d.N = H; d.K = F; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.full_tab = st.full_tab; d.full_off = st.full_off; d.tail_tab = st.tail_tab;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = Hh; d.lda = F; d.a_rows = L.Rp_max;
     d.B0 = a->W_down; d.ldb = H; d.b_kmajor = 0; d.b_estride = (long long)F * H; d.b_rows = E * F;
@@ -494,6 +514,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     const int* meta = reinterpret_cast<const int*>(sv + L.meta);
     const int* tiletab = reinterpret_cast<const int*>(sv + L.tiletab);
     const int* pairtab = reinterpret_cast<const int*>(sv + L.pairtab);
+    const SplitTabs st = split_tabs(L, E, sv);
     const int* eorder = reinterpret_cast<const int*>(sv + L.eorder);
     const int* rowof = reinterpret_cast<const int*>(sv + L.rowof);
     const int* slotof = reinterpret_cast<const int*>(sv + L.slotof);
@@ -533,6 +554,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_BWD; d.dual = DUAL_NONE;
     d.N = F; d.K = H; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.full_tab = st.full_tab; d.full_off = st.full_off; d.tail_tab = st.tail_tab;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = dYp; d.lda = H; d.a_rows = L.Rp_max;
     d.B0 = a->W_down; d.ldb = H; d.b_kmajor = 1; d.b_estride = (long long)F * H; d.b_rows = E * F;
@@ -560,6 +582,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
     d.N = H; d.K = F; d.E = E;
     d.tile_tab = tiletab; d.meta = meta; d.poff = poff; d.counts = kept; d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max;
+    d.full_tab = st.full_tab; d.full_off = st.full_off; d.tail_tab = st.tail_tab;
     d.prefer_pair = (long long)T_ * k >= 512ll * E;
     d.A0 = dA; d.A1 = dU; d.lda = F; d.a_rows = L.Rp_max;
     d.B0 = a->W_gate; d.B1 = a->W_up; d.ldb = F; d.b_kmajor = 1; d.b_estride = (long long)H * F;

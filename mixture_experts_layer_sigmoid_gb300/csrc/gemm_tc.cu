@@ -38,7 +38,9 @@ constexpr int TBM = 128;       // MMA M
 constexpr int TBK = 64;        // K block (128 bytes of bf16)
 constexpr int STRIPE = 64 * 128;  // bytes of one 64-wide MN stripe of a 64-deep k block
 constexpr int kThreads = 192;
-constexpr int kGroupN = 16;    // n tiles per raster group (row-scheduled GEMMs)
+constexpr int kGroupN = 16;    // n tiles per raster group (row-scheduled GEMMs) ...
+constexpr int kGroupSpan = 16; // ... or fewer, so that the units sharing a weight tile
+                               // are at most this many tiles apart (experts of <= 8 units)
 
 constexpr int kSmemMax = 232448;               // 227 KB per CTA
 constexpr int kStaging = 4 * 2 * 4096;          // per epilogue warp: 2 x (32 rows x 128 B)
@@ -66,7 +68,9 @@ __device__ __forceinline__ void tile_counts(const GemmDesc& d, int& num_m, int& 
     constexpr int NW = (DUAL == DUAL_N) ? BN / 2 : BN;   // output columns per tile
     if (SCHED == SCHED_ROWS) {
         const int tiles = d.dense_rows > 0 ? (d.dense_rows + TBM - 1) / TBM : d.meta[0];
-        num_m = PAIR ? (d.dense_rows > 0 ? (tiles + 1) / 2 : d.meta[2]) : tiles;
+        if (d.dense_rows > 0) num_m = PAIR ? (tiles + 1) / 2 : tiles;
+        else if (PAIR) num_m = d.meta[d.row_set == ROWSET_FULL_PAIRS ? 3 : 2];
+        else num_m = d.row_set == ROWSET_TAILS ? d.meta[4] : tiles;
         num_n = d.N / NW;
         total = num_m * num_n;
     } else {
@@ -81,25 +85,37 @@ __device__ __forceinline__ Tile decode_tile(const GemmDesc& d, int w, int num_m,
 {
     Tile t;
     if (SCHED == SCHED_ROWS) {
-        // Groups of kGroupN n-tiles: consecutive units share the A rows (one
-        // row unit against kGroupN weight column tiles), and consecutive
-        // groups of them walk the row units, which share the weights. Routed
-        // rows go expert by expert (each expert's block of units x num_n tiles
-        // is contiguous in w), so an expert's weight column group and its rows
-        // stay in L2 while its units pass over them.
+        // Groups of G n-tiles: consecutive units share the A rows (one row
+        // unit against G weight column tiles), and consecutive groups of them
+        // walk the row units, which share the weights. Routed rows go expert
+        // by expert (each expert's block of units x num_n tiles is contiguous
+        // in w), so an expert's weight column group and its rows stay in L2
+        // while its units pass over them. An expert of few units (its rows
+        // stay in L2 across groups) takes narrow groups, so that the nu units
+        // reading one weight tile run within kGroupSpan consecutive tiles of
+        // each other instead of drifting into the next wave; a large one takes
+        // kGroupN, which reads its rows once per kGroupN weight tiles.
+        // (A launch over the one-tile experts has one unit per expert.)
+        const bool tails = !PAIR && d.row_set == ROWSET_TAILS;
         int group, r, u0 = 0, nu = num_m;
         if (d.dense_rows == 0) {
             const int q = w / num_n;                        // some unit of w's expert
-            const int e = d.tile_tab[PAIR ? d.pair_tab[q] : q];
-            u0 = PAIR ? d.pair_off[e] : d.poff[e] / TBM;
-            nu = (PAIR ? d.pair_off[e + 1] : d.poff[e + 1] / TBM) - u0;
+            if (tails) {
+                u0 = q;
+                nu = 1;
+            } else {
+                const int e = d.tile_tab[PAIR ? d.pair_tab[q] : q];
+                u0 = PAIR ? d.pair_off[e] : d.poff[e] / TBM;
+                nu = (PAIR ? d.pair_off[e + 1] : d.poff[e + 1] / TBM) - u0;
+            }
             w -= u0 * num_n;
         }
-        group = w / (nu * kGroupN);
-        r = w - group * nu * kGroupN;
-        const int gsz = min(kGroupN, num_n - group * kGroupN);
+        const int G = nu <= kGroupSpan / 2 ? max(1, kGroupSpan / nu) : kGroupN;
+        group = w / (nu * G);
+        r = w - group * nu * G;
+        const int gsz = min(G, num_n - group * G);
         const int mu = u0 + r / gsz;
-        t.n = group * kGroupN + r % gsz;
+        t.n = group * G + r % gsz;
         if (d.dense_rows > 0) {
             t.m = PAIR ? 2 * mu + rank : mu;
             t.e = 0;
@@ -107,7 +123,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmDesc& d, int w, int num_m,
         } else {
             // a pair's second tile may lie past its expert's segment ("ghost"):
             // its rows are beyond alloc_end, so nothing of it is stored
-            const int first = PAIR ? d.pair_tab[mu] : mu;
+            const int first = PAIR ? d.pair_tab[mu] : (tails ? d.tail_tab[mu] : mu);
             t.m = first + rank;
             t.e = d.tile_tab[first];
             t.valid_end = d.poff[t.e] + d.counts[t.e];
@@ -138,8 +154,10 @@ __device__ __forceinline__ Tile decode_tile(const GemmDesc& d, int w, int num_m,
             t.row0 = 0;
             t.kblocks = (d.dense_rows + TBK - 1) / TBK;
         } else {
+            // K stops at the 64-row block holding the expert's last computed
+            // row: the rest of the segment is zero padding
             t.row0 = d.poff[t.e];
-            t.kblocks = (d.poff[t.e + 1] - d.poff[t.e]) / TBK;
+            t.kblocks = (d.counts[t.e] + TBK - 1) / TBK;
         }
         t.valid_end = t.alloc_end = 0;
     }
@@ -247,6 +265,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
     else __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // a launch over the one-tile experts may follow this grid early: it
+    // shares no output with it (see the end of the kernel)
+    if (PAIR) ptx::griddep_launch_dependents();
 
     int num_m, num_n, total;
     tile_counts<BN, DUAL, SCHED, PAIR>(d, num_m, num_n, total);
@@ -572,6 +593,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
         if (PAIR) ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
         else ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
+    // The one-tile experts' launch starts while the pair launch before it
+    // drains (programmatic dependent launch) and completes only after it, so
+    // the stream's next kernel sees both.
+    if (!PAIR && d.row_set == ROWSET_TAILS) ptx::griddep_wait();
 }
 
 // ------------------------------------------------------------------ host
@@ -680,6 +705,7 @@ cudaError_t run(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
         }
         long long m_tiles = d.dense_rows > 0 ? (d.dense_rows + TBM - 1) / TBM : max_m_tiles;
         if (PAIR) m_tiles = (m_tiles + 1) / 2;
+        else if (d.dense_rows == 0 && d.row_set == ROWSET_TAILS) m_tiles = d.E < m_tiles ? d.E : m_tiles;
         units = m_tiles * (d.N / NW);
     } else {
         // A: [rows][M_out], B: [rows][N], read as 64-row boxes of 64 columns.
@@ -693,6 +719,22 @@ cudaError_t run(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
     if (units <= 0) return cudaSuccess;
     if (!PAIR) {
         const int grid = (int)(units < num_sms ? units : num_sms);
+        if (d.row_set == ROWSET_TAILS) {
+            // after a pair launch: programmatic dependent launch (see the kernel's end)
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.gridDim = dim3((unsigned)grid, 1, 1);
+            cfg.blockDim = dim3(kThreads, 1, 1);
+            cfg.dynamicSmemBytes = TcCfg<BN, false>::SMEM;
+            cfg.stream = s;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            count_launches();
+            return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, B_MN, DUAL, EPI, SCHED, false>, mA0, mA1,
+                                      mB0, mB1, mO0, mO1, mO2, d);
+        }
         gemm_tc_kernel<BN, B_MN, DUAL, EPI, SCHED, false>
             <<<grid, kThreads, TcCfg<BN, false>::SMEM, s>>>(mA0, mA1, mB0, mB1, mO0, mO1, mO2, d);
         count_launches();
@@ -719,7 +761,11 @@ cudaError_t run(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
 }
 
 // Single-CTA or CTA-pair instance: pairs when the row units come in
-// (mostly) complete pairs.
+// (mostly) complete pairs. Routed rows with split tables take two launches:
+// CTA pairs over the experts of two or more tiles, then single CTAs over the
+// one-tile experts (which a pair would compute beside an empty "ghost" tile;
+// an odd last tile of a larger expert keeps its ghost, since a second launch
+// would read that expert's weights again).
 template <int BN, bool B_MN, int DUAL, int EPI, int SCHED>
 cudaError_t run_any(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
 {
@@ -727,6 +773,17 @@ cudaError_t run_any(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_
     if (SCHED == SCHED_WGRAD) pair = d.M_out % (2 * TBM) == 0;
     else if (d.dense_rows > 0) pair = d.dense_rows > TBM;
     else pair = d.pair_tab != nullptr && d.prefer_pair;
+    if (pair && SCHED == SCHED_ROWS && d.dense_rows == 0 && d.full_tab && d.full_off && d.tail_tab) {
+        GemmDesc dp = d;
+        dp.row_set = ROWSET_FULL_PAIRS;
+        dp.pair_tab = d.full_tab;
+        dp.pair_off = d.full_off;
+        const cudaError_t e = run<BN, B_MN, DUAL, EPI, SCHED, true>(dp, max_m_tiles, num_sms, s);
+        if (e != cudaSuccess) return e;
+        GemmDesc dt = d;
+        dt.row_set = ROWSET_TAILS;
+        return run<BN, B_MN, DUAL, EPI, SCHED, false>(dt, max_m_tiles, num_sms, s);
+    }
     if (pair) return run<BN, B_MN, DUAL, EPI, SCHED, true>(d, max_m_tiles, num_sms, s);
     return run<BN, B_MN, DUAL, EPI, SCHED, false>(d, max_m_tiles, num_sms, s);
 }

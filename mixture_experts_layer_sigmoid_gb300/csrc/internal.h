@@ -37,6 +37,12 @@ enum Sched : int {
     SCHED_ROWS = 0,   // M = permuted rows (one expert per 128-row tile), fixed K
     SCHED_WGRAD = 1,  // per expert: M_out x N output, K = the expert's rows
 };
+// Which routed row tiles one launch covers.
+enum RowSet : int {
+    ROWSET_ALL = 0,         // every tile (pairs: a lone last tile runs beside a ghost)
+    ROWSET_FULL_PAIRS = 1,  // CTA pairs over full_tab / full_off (multi-tile experts)
+    ROWSET_TAILS = 2,       // single CTAs over tail_tab (one-tile experts)
+};
 // What the epilogue does with the fp32 accumulator(s).
 enum Epi : int {
     EPI_SWIGLU_FWD = 0,  // acc0 = a, acc1 = u -> O0 = a, O1 = u, O2 = silu(a) u
@@ -61,10 +67,19 @@ struct GemmDesc {
     // row tables (routed groups)
     const int* tile_tab;  // expert of each 128-row tile
     const int* meta;      // meta[0] = number of 128-row tiles, meta[1] = padded rows,
-                          // meta[2] = number of tile pairs
+                          // meta[2] = number of tile pairs, meta[3] = number of
+                          // pairs of multi-tile experts, meta[4] = number of
+                          // one-tile experts
     const int* pair_tab;  // first tile of each pair of one expert's tiles (or null)
     const int* pair_off;  // E+1: first pair of each expert (with pair_tab)
     int prefer_pair;      // routed rows per expert are large enough for CTA pairs
+    // Split row sets (bf16 tensor-core path): the pairs of the experts with
+    // two or more tiles, and the tile of each one-tile expert, so that CTA
+    // pairs never compute a ghost tile for an expert of 128 rows or fewer.
+    const int* full_tab;  // first tile of each pair of a multi-tile expert
+    const int* full_off;  // E+1: first such pair of each expert
+    const int* tail_tab;  // the tiles of the one-tile experts
+    int row_set;          // ROWSET_* (set by the launcher)
     const int* expert_order;  // weight gradients: experts in this order (null: 0..E-1)
     const int* poff;      // E+1 padded segment offsets
     const int* counts;    // E rows computed per expert (token counts, or the
@@ -125,7 +140,8 @@ size_t router_zpart_floats(int T, int H, int E);
 cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff, int* blkbase,
                         int* tile_tab, int* meta, int* slot_of, cudaStream_t s,
                         int* pair_tab = nullptr, int* pair_off = nullptr, int cap = -1,
-                        int* kept = nullptr, int* eorder = nullptr);
+                        int* kept = nullptr, int* eorder = nullptr, int* full_tab = nullptr,
+                        int* full_off = nullptr, int* tail_tab = nullptr);
 cudaError_t launch_index(const int* topk, const int* blkbase, int T_, int E, int k, int* row_of,
                          int* slot_of, cudaStream_t s);
 template <typename T>

@@ -201,6 +201,20 @@ __device__ __forceinline__ uint32_t nclusters_x()
     asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
     return r;
 }
+// Programmatic dependent launch: let the next kernel of the stream (launched
+// with programmatic stream serialization) be scheduled once every CTA of this
+// grid has issued this or exited ...
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// ... and, in that kernel, wait until the preceding grid has completed and its
+// memory operations are visible (no-op in a kernel launched without it).
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n"

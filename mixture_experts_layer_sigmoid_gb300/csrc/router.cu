@@ -469,7 +469,8 @@ __global__ void __launch_bounds__(kScanParts * kMaxE)
 scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ counts,
             int* __restrict__ poff, int* __restrict__ blkbase, int* __restrict__ tile_tab,
             int* __restrict__ meta, int* __restrict__ slot_of, int* __restrict__ pair_tab,
-            int* __restrict__ pair_off, int cap, int* __restrict__ kept, int* __restrict__ eorder)
+            int* __restrict__ pair_off, int cap, int* __restrict__ kept, int* __restrict__ eorder,
+            int* __restrict__ full_tab, int* __restrict__ full_off, int* __restrict__ tail_tab)
 {
     __shared__ int sc[kMaxE];
     __shared__ int plen[kMaxE];
@@ -541,6 +542,44 @@ scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ cou
         if (threadIdx.x == 0) {
             meta[2] = sc[kMaxE - 1];
             pair_off[E] = sc[kMaxE - 1];
+        }
+    }
+    if (full_tab) {
+        // the pairs of the experts with two tiles or more (an odd last tile
+        // beside a ghost, so that a second launch does not read the expert's
+        // weights again); the experts of one tile are listed apart
+        const int nt = (e < E) ? pc / kTileM : 0;
+        const int nf = nt >= 2 ? (nt + 1) / 2 : 0, tl = nt == 1;
+        int* tails = part_sum[1];            // free again: the counts are summed
+        __syncthreads();
+        if (part == 0) {
+            sc[e] = nf;
+            tails[e] = tl;
+        }
+        __syncthreads();
+        for (int off = 1; off < kMaxE; off <<= 1) {
+            int v = 0, u = 0;
+            if (part == 0 && e >= off) {
+                v = sc[e - off];
+                u = tails[e - off];
+            }
+            __syncthreads();
+            if (part == 0) {
+                sc[e] += v;
+                tails[e] += u;
+            }
+            __syncthreads();
+        }
+        if (part == 0) {
+            const int fstart = sc[e] - nf;
+            for (int i = 0; i < nf; ++i) full_tab[fstart + i] = start / kTileM + 2 * i;
+            if (e < E) full_off[e] = fstart;
+            if (tl) tail_tab[tails[e] - 1] = start / kTileM;
+        }
+        if (threadIdx.x == 0) {
+            meta[3] = sc[kMaxE - 1];
+            meta[4] = tails[kMaxE - 1];
+            full_off[E] = sc[kMaxE - 1];
         }
     }
     // experts by padded segment length, longest first (lower index first on
@@ -658,11 +697,14 @@ size_t router_zpart_floats(int T, int H, int E)
 
 cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff, int* blkbase,
                         int* tile_tab, int* meta, int* slot_of, cudaStream_t s, int* pair_tab,
-                        int* pair_off, int cap, int* kept, int* eorder)
+                        int* pair_off, int cap, int* kept, int* eorder, int* full_tab,
+                        int* full_off, int* tail_tab)
 {
     if (pair_tab && !pair_off) return cudaErrorInvalidValue;
+    if (full_tab && (!full_off || !tail_tab)) return cudaErrorInvalidValue;
     scan_kernel<<<1, kScanParts * kMaxE, 0, s>>>(hist, nblk, E, counts, poff, blkbase, tile_tab, meta,
-                                                 slot_of, pair_tab, pair_off, cap, kept, eorder);
+                                                 slot_of, pair_tab, pair_off, cap, kept, eorder,
+                                                 full_tab, full_off, tail_tab);
     count_launches();
     return cudaGetLastError();
 }

@@ -24,6 +24,13 @@ CASES = {
     "k_equals_E": mi.scaled(W["mixtral_8x7b"], T=100, H=128, E=4, k=4, F=128),
     "softmax_bias_k3": mi.scaled(W["qwen3_235b"], T=400, H=256, E=12, k=3, F=256),
     "rows_in_cta_pairs": mi.scaled(W["mixtral_8x7b"], T=1100, H=256, E=4, k=2, F=256),
+    # CTA pairs over the experts of two or more tiles (an odd last tile beside
+    # a ghost) plus single CTAs over the one-tile experts: expert tile counts
+    # 1, 2, 3, 5, 7 (Zipf) and 1-4 with an exactly full 128-row segment
+    # (sigmoid, bias, shared expert)
+    "pairs_and_one_tile_experts_zipf": mi.scaled(W["qwen3_235b"], T=1300, H=256, E=8, k=2, F=256),
+    "deepseek_pairs_and_one_tile_experts": mi.scaled(W["deepseek_v3"], T=1040, H=256, E=16, k=4,
+                                                     F=256, Fs=128),
     "qwen_e128_tiled_router": mi.scaled(W["qwen3_235b"], T=700, H=256, E=128, F=128),
     "deepseek_e256_sigmoid_shared": mi.scaled(W["deepseek_v3"], T=512, H=256, E=256, F=128, Fs=128),
     # tiled router for E > 32: E not a multiple of 4 (Wr rows copied in 4-byte
@@ -48,7 +55,8 @@ def test_layer_matches_oracle(name):
 # Memory-efficient permutation: the same layer with the routing weights
 # folded into the expert activations must meet the same bounds.
 FOLD_CASES = ["tiny_fp32", "mixtral_small", "deepseek_small", "qwen_small_ragged_n",
-              "fp32_sigmoid_shared", "rows_in_cta_pairs", "deepseek_e256_sigmoid_shared"]
+              "fp32_sigmoid_shared", "rows_in_cta_pairs", "deepseek_e256_sigmoid_shared",
+              "deepseek_pairs_and_one_tile_experts"]
 
 
 @pytest.mark.parametrize("name", FOLD_CASES)
@@ -63,10 +71,12 @@ def test_folded_gates_match_oracle(name):
 # drops 37% of all slots; the max/rms bound is relative to the rms of the
 # reference, which shrinks with every dropped expert output while the bf16
 # rounding of the kept ones does not, so that case uses a factor of 2 (14%);
-# the CTA-pair and DeepSeek-shaped cases drop a few assignments (13 and 7).
+# the CTA-pair and DeepSeek-shaped cases drop a few assignments (13 and 7), the
+# Zipf case with one-tile experts 237 of the hottest expert's 887.
 CAPACITY_CASES = [("mixtral_small", 0.6, False), ("qwen_small_ragged_n", 2.0, False),
                   ("fp32_sigmoid_shared", 0.75, False), ("rows_in_cta_pairs", 1.0, False),
-                  ("deepseek_small", 1.5, True), ("mixtral_small", 0.6, True)]
+                  ("deepseek_small", 1.5, True), ("mixtral_small", 0.6, True),
+                  ("pairs_and_one_tile_experts_zipf", 2.0, False)]
 
 
 @pytest.mark.parametrize("name,cf,fold", CAPACITY_CASES)
