@@ -52,8 +52,9 @@ constexpr int kXGroupN = 16;
 constexpr int kAccCols = 256;                    // the accumulator
 constexpr int kSfCols = 12;                      // scale columns of one stage: A 4, B 2 x 4
 
-// STG: bytes of epilogue staging for TMA stores (the weight-gradient GEMMs:
-// 8 warps x two 32-row x 128-byte buffers)
+// STG: bytes of epilogue staging for TMA stores (8 warps x one 32-row x
+// 128-byte buffer, which leaves the CTA-pair engine a fifth operand stage;
+// two per warp for the SwiGLU backward, whose dA and dU leave together)
 template <bool PAIR, int STG = 0>
 struct XCfg {
     static constexpr int A_BYTES = XBM * XBK;
@@ -64,12 +65,13 @@ struct XCfg {
     static constexpr int STAGES = (kXSmemMax - 1024 - 256 - STG) / STAGE;
     static constexpr int SMEM = 1024 + STAGES * STAGE + STG + 256;
 };
-constexpr int kStoreStaging = 8 * 2 * 4096;
+constexpr int kStoreStaging = 8 * 4096;
 // every epilogue stores through staging
 template <int EPI, int SCHED>
 constexpr int staging_bytes()
 {
-    return (SCHED == SCHED_WGRAD || SCHED == SCHED_ROWS) ? kStoreStaging : 0;
+    return EPI == EPI_SWIGLU_BWD ? 2 * kStoreStaging
+                                 : (SCHED == SCHED_WGRAD || SCHED == SCHED_ROWS) ? kStoreStaging : 0;
 }
 static_assert(kAccCols + kSfCols * XCfg<true>::STAGES <= 512, "tensor memory");
 static_assert(kAccCols + kSfCols * XCfg<false>::STAGES <= 512, "tensor memory");
@@ -539,12 +541,12 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
             // row r at chunk j ^ (r % 8)), one bulk store each; zero rows where
             // `zero` (pad rows of a segment)
             auto store_staged = [&](int y, bool zero) {
-                const uint32_t stg = staging + (uint32_t)(warp - 2) * 8192u;
-                if (lane == 0) ptx::bulk_wait_read<0>();   // the previous tile's stores have read them
-                __syncwarp();
+                const uint32_t stg = staging + (uint32_t)(warp - 2) * 4096u;
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
                     if (part == 1 && !hi_ok) break;
+                    if (lane == 0) ptx::bulk_wait_read<0>();   // the buffer's previous store has read it
+                    __syncwarp();
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         get8(acc, 32 * part + 4 * j, v);
@@ -553,19 +555,18 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
                             h2[i] = zero ? __floats2bfloat162_rn(0.f, 0.f) : __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                        const uint32_t addr = stg + 4096u * part + (uint32_t)lane * 128u +
-                                              (uint32_t)((j ^ (lane & 7)) * 16);
+                        const uint32_t addr = stg + (uint32_t)lane * 128u + (uint32_t)((j ^ (lane & 7)) * 16);
                         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(u4.x), "r"(u4.y),
                                      "r"(u4.z), "r"(u4.w)
                                      : "memory");
                     }
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::tma_store_2d(&mO0, stg, col_lo, y);
-                    if (hi_ok) ptx::tma_store_2d(DUAL == DUAL_N ? &mO1 : &mO0, stg + 4096u, col_hi, y);
-                    ptx::bulk_commit();
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (part == 0) ptx::tma_store_2d(&mO0, stg, col_lo, y);
+                        else ptx::tma_store_2d(DUAL == DUAL_N ? &mO1 : &mO0, stg, col_hi, y);
+                        ptx::bulk_commit();
+                    }
                 }
             };
             if (SCHED == SCHED_WGRAD) {
@@ -576,13 +577,14 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                 if (t.row0 + q * 32 < t.alloc_end) store_staged(t.row0 + q * 32, arow >= t.valid_end);
             } else if (EPI == EPI_SWIGLU_FWD) {
                 // a, u, then h = silu(a) u (g h with the routing weight folded in)
-                // of this warp's 32 rows x 64 columns, through the two staging
-                // buffers; h's MX row codes (fc2's A operand) from this thread
+                // of this warp's 32 rows x 64 columns, one after the other through
+                // the warp's staging buffer; h's MX row codes (fc2's A operand)
+                // from this thread
                 if (t.row0 + q * 32 < t.alloc_end) {
                     const bool valid = arow < t.valid_end;
                     const float grow = (d.gates && valid) ? d.gates[d.slot_of[arow]] : 1.f;
                     const int y = t.row0 + q * 32;
-                    const uint32_t stg = staging + (uint32_t)(warp - 2) * 8192u;
+                    const uint32_t stg = staging + (uint32_t)(warp - 2) * 4096u;
                     auto put = [&](uint32_t buf, int j, const float* f) {
                         uint4 u4;
                         __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&u4);
@@ -593,27 +595,27 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                                      "r"(u4.z), "r"(u4.w)
                                      : "memory");
                     };
-                    if (lane == 0) ptx::bulk_wait_read<0>();   // the previous tile's stores have read them
-                    __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        get8(acc, 4 * j, v);
-                        get8(acc, 32 + 4 * j, x);
-                        if (!valid) {
+                    for (int part = 0; part < 2; ++part) {   // a (part-0 columns), then u
+                        if (lane == 0) ptx::bulk_wait_read<0>();   // the buffer's previous store has read it
+                        __syncwarp();
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) v[i] = x[i] = 0.f;
+                        for (int j = 0; j < 8; ++j) {
+                            get8(acc, 32 * part + 4 * j, v);
+                            if (!valid) {
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) v[i] = 0.f;
+                            }
+                            put(stg, j, v);
                         }
-                        put(stg, j, v);
-                        put(stg + 4096u, j, x);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(part ? &mO1 : &mO0, stg, col_lo, y);
+                            ptx::bulk_commit();
+                        }
                     }
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_store_2d(&mO0, stg, col_lo, y);
-                        ptx::tma_store_2d(&mO1, stg + 4096u, col_lo, y);
-                        ptx::bulk_commit();
-                        ptx::bulk_wait_read<0>();
-                    }
+                    if (lane == 0) ptx::bulk_wait_read<0>();
                     __syncwarp();
 #pragma unroll
                     for (int blk = 0; blk < 2; ++blk) {
