@@ -145,15 +145,15 @@ def test_full_size_layer(name):
     write_report(f"{name} full size, sampled weight-gradient entries", report)
 
 
-def test_full_size_fp8_layer():
-    """Qwen3-shaped layer in blockwise FP8: routing bit-exact, the layer's
+def _full_size_fp8_case(wl, dtype, recipe, check_weight_quantiser):
+    """A Qwen3-shaped FP8 layer at full size: routing bit-exact, the layer's
     weight quantiser bit-exact against the oracle on sampled experts, and
     sampled y and dX rows within the FP8 bounds (relative L2 <= 4e-2,
-    max|err| <= 1.5e-1 rms) of the oracle's FP8 layer."""
+    max|err| <= 1.5e-1 rms) of the oracle's FP8 layer in the same recipe."""
     import mixture_experts_layer_sigmoid_gb300 as moe
-    w = mi.WORKLOADS["qwen3_235b_fp8"]
+    w = mi.WORKLOADS[wl]
     g = mi.make_inputs(w, "cuda")
-    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=moe.MOE_FP8_BLOCK)
+    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=dtype)
     y, rt = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"], routing=True)
     gr = layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
     torch.cuda.synchronize()
@@ -170,9 +170,36 @@ def test_full_size_fp8_layer():
     counts = np.bincount(r["topk"].ravel(), minlength=w.E)
     assert np.array_equal(rt["counts"].cpu().numpy(), counts)
     hot = int(np.argmax(counts))
-    # the weight quantiser on two experts' full-size blocks
     for e in (0, hot):
-        W = g["Wg"][e].contiguous()
+        check_weight_quantiser(g["Wg"][e].contiguous())
+    # sampled rows against the oracle's FP8 layer run on those tokens alone:
+    # y and dX of a token depend only on its own row (row blocks of its
+    # activations and gradients, weight blocks of its experts), and dz only on
+    # its selected experts' scores, so the layer restricted to the sampled
+    # tokens and the experts they select (renumbered) gives their rows exactly
+    toks = np.array(sorted({0, w.T - 1, int(np.nonzero((r["topk"] == hot).any(1))[0][0])}))
+    need = sorted(set(r["topk"][toks].ravel().tolist()))
+    renum = np.full(w.E, -1, np.int32)
+    renum[need] = np.arange(len(need), dtype=np.int32)
+    topk_s = renum[r["topk"][toks]]
+    stack = lambda n: np.stack([to_np(g[n][e]) for e in need])
+    q = oracle.layer_fp8(x[toks], Wr[:, need], stack("Wg"), stack("Wu"), stack("Wd"), topk_s,
+                         r["gates"][toks], r["scores"][toks][:, need], w.score, dY[toks],
+                         recipe=recipe)
+    report = {}
+    for nm, got in (("y", to_np(y)[toks]), ("dX", to_np(gr["dX"])[toks])):
+        rl2, mr = rel_errors(got, q[nm])
+        report[nm + "_rows"] = (rl2, mr)
+        assert rl2 <= 4e-2 and mr <= 1.5e-1, (nm, rl2, mr)
+    print(wl, report)
+    write_report(f"{wl} full size, sampled token rows", report)
+
+
+def test_full_size_fp8_layer():
+    """Blockwise FP8 (1x128 / 128x128 fp32 scales)."""
+    import mixture_experts_layer_sigmoid_gb300 as moe
+
+    def check(W):
         R, C = W.shape
         codes = torch.empty((R, C), dtype=torch.uint8, device="cuda")
         codes_t = torch.empty((C, R), dtype=torch.uint8, device="cuda")
@@ -184,23 +211,23 @@ def test_full_size_fp8_layer():
         oc, os_ = oracle.fp8_quantize(W.float().cpu().numpy(), oracle.FP8_TILES)
         assert np.array_equal(codes.cpu().numpy(), oc) and np.array_equal(sc.cpu().numpy(), os_)
         assert np.array_equal(codes_t.cpu().numpy(), oc.T)
-    # sampled rows against the oracle's FP8 layer run on those tokens alone:
-    # y and dX of a token depend only on its own row (1x128 activation blocks,
-    # 128x128 weight blocks of its experts), and dz only on its selected
-    # experts' scores, so the layer restricted to the sampled tokens and the
-    # experts they select (renumbered) gives their rows exactly
-    toks = np.array(sorted({0, w.T - 1, int(np.nonzero((r["topk"] == hot).any(1))[0][0])}))
-    need = sorted(set(r["topk"][toks].ravel().tolist()))
-    renum = np.full(w.E, -1, np.int32)
-    renum[need] = np.arange(len(need), dtype=np.int32)
-    topk_s = renum[r["topk"][toks]]
-    stack = lambda n: np.stack([to_np(g[n][e]) for e in need])
-    q = oracle.layer_fp8(x[toks], Wr[:, need], stack("Wg"), stack("Wu"), stack("Wd"), topk_s,
-                         r["gates"][toks], r["scores"][toks][:, need], w.score, dY[toks])
-    report = {}
-    for nm, got in (("y", to_np(y)[toks]), ("dX", to_np(gr["dX"])[toks])):
-        rl2, mr = rel_errors(got, q[nm])
-        report[nm + "_rows"] = (rl2, mr)
-        assert rl2 <= 4e-2 and mr <= 1.5e-1, (nm, rl2, mr)
-    print("qwen3_235b_fp8", report)
-    write_report("qwen3_235b_fp8 full size, sampled token rows", report)
+
+    _full_size_fp8_case("qwen3_235b_fp8", moe.MOE_FP8_BLOCK, oracle.RECIPE_BLOCK, check)
+
+
+def test_full_size_mxfp8_layer():
+    """MXFP8 (1x32 blocks, UE8M0 scales): the weight quantiser checked in
+    both block directions (1x32 along each row, 32x1 down each column)."""
+    import mixture_experts_layer_sigmoid_gb300 as moe
+    from test_mx_gpu import _atoms_to_scales, _mxq
+
+    def check(W):
+        R, C = W.shape
+        q, sq, qc, sc = _mxq(W, rows=True, cols=1)
+        Wf = W.float().cpu().numpy()
+        oc_r, os_r = oracle.mx_quantize(Wf, oracle.MX_ROWS)
+        oc_c, os_c = oracle.mx_quantize(Wf, oracle.MX_COLS)
+        assert np.array_equal(q, oc_r) and np.array_equal(_atoms_to_scales(sq, R, C), os_r)
+        assert np.array_equal(qc, oc_c.T) and np.array_equal(_atoms_to_scales(sc, C, R), os_c.T)
+
+    _full_size_fp8_case("qwen3_235b_mxfp8", moe.MOE_MXFP8, oracle.RECIPE_MX, check)
