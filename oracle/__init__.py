@@ -357,11 +357,15 @@ RECIPE_BLOCK, RECIPE_MX = 0, 1
 
 
 def layer_fp8(x, Wr, Wg, Wu, Wd, topk, gates, scores, score, dY=None, Wsg=None, Wsu=None,
-              Wsd=None, fold=False, recipe=RECIPE_BLOCK):
+              Wsd=None, fold=False, recipe=RECIPE_BLOCK, keep=None):
     """FP8 layer: y, and when dY is given every gradient. recipe: RECIPE_BLOCK
     (blockwise FP8, fp32 block scales) or RECIPE_MX (MXFP8, 1x32 blocks with
     power-of-two scales). fold: the memory-efficient permutation's order
-    (routing weight folded into h before fc2), with its rounding points."""
+    (routing weight folded into h before fc2), with its rounding points.
+    keep: optional T x k mask of the slots that are not dropped
+    (capacity_keep); a dropped assignment never reaches its expert, so the
+    expert's segment, and every quantisation block counted along it, holds
+    its kept rows alone; its dg is 0."""
     lib = _load()
     x, Wr, Wg, Wu, Wd = _f64(x), _f64(Wr), _f64(Wg), _f64(Wu), _f64(Wd)
     Wsg, Wsu, Wsd = _f64(Wsg), _f64(Wsu), _f64(Wsd)
@@ -381,7 +385,8 @@ def layer_fp8(x, Wr, Wg, Wu, Wd, topk, gates, scores, score, dY=None, Wsg=None, 
                               _d(out["y"]), _d(out.get("dX")), _d(out.get("dWr")),
                               _d(out.get("dWg")), _d(out.get("dWu")), _d(out.get("dWd")),
                               _d(out.get("dWsg")), _d(out.get("dWsu")), _d(out.get("dWsd")),
-                              _d(out.get("dg")), 1 if fold else 0, int(recipe))
+                              _d(out.get("dg")), 1 if fold else 0, int(recipe),
+                              _u8(None if keep is None else np.ascontiguousarray(keep, np.uint8)))
     if rc:
         raise ValueError("oracle_layer_fp8: bad arguments")
     return out

@@ -1075,17 +1075,41 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
                      const double* dY, double* y,
                      double* dX, double* dWr, double* dWg, double* dWu, double* dWd,
                      double* dWsg, double* dWsu, double* dWsd, double* dg_out, int fold,
-                     int recipe)
+                     int recipe, const unsigned char* keep)
 {
     if (T <= 0 || H <= 0 || H % 128 || E <= 0 || k <= 0 || k > E || k > 1024 || F <= 0 ||
         F % 128 || Fs < 0 || Fs % 128 || recipe < 0 || recipe > 1)
         return -1;
-    const int R = T * k;
     int* counts = (int*)malloc(sizeof(int) * E);
     int* offsets = (int*)malloc(sizeof(int) * (E + 1));
-    int* row_of = (int*)malloc(sizeof(int) * R);
-    int* slot_of = (int*)malloc(sizeof(int) * R);
+    int* row_of = (int*)malloc(sizeof(int) * (size_t)T * k);
+    int* slot_of = (int*)malloc(sizeof(int) * (size_t)T * k);
     if (oracle_dispatch(T, E, k, topk, counts, offsets, row_of, slot_of)) return -1;
+    if (keep) {
+        /* capacity-limited dropping: a dropped assignment never reaches its
+         * expert, so each expert's segment holds its kept rows alone (in token
+         * order) and every quantisation block along the tokens is counted from
+         * the segment's first kept row; row_of of a dropped slot is -1 */
+        int row = 0;
+        for (int e = 0; e < E; ++e) {
+            offsets[e] = row;
+            for (int t = 0; t < T; ++t)
+                for (int j = 0; j < k; ++j) {
+                    const int sl = t * k + j;
+                    if (topk[sl] != e) continue;
+                    if (keep[sl]) {
+                        row_of[sl] = row;
+                        slot_of[row] = sl;
+                        ++row;
+                    } else {
+                        row_of[sl] = -1;
+                    }
+                }
+            counts[e] = row - offsets[e];
+        }
+        offsets[E] = row;
+    }
+    const int R = offsets[E];   /* rows that reach an expert */
     /* routing weight of each permuted row (folded variant) */
     double* grow = (double*)malloc(sizeof(double) * (size_t)R);
     for (int r = 0; r < R; ++r) grow[r] = gates[slot_of[r]];
@@ -1093,7 +1117,7 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
     double* Yp = (double*)malloc(sizeof(double) * (size_t)R * H);
     double* dYp = (double*)malloc(sizeof(double) * (size_t)R * H);
     double* dXp = (double*)malloc(sizeof(double) * (size_t)R * H);
-    double* dg = (double*)malloc(sizeof(double) * (size_t)R);
+    double* dg = (double*)calloc((size_t)T * k, sizeof(double));   /* per slot; 0 if dropped */
     for (int r = 0; r < R; ++r)
         memcpy(Xp + (size_t)r * H, x + (size_t)(slot_of[r] / k) * H, sizeof(double) * H);
     /* forward of every expert (Yp), then the gate-scaled output gradients */
@@ -1107,9 +1131,11 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
     for (int t = 0; t < T; ++t)
         for (int h = 0; h < H; ++h) {
             double acc = 0.0;
-            for (int j = 0; j < k; ++j)
-                acc += (fold ? 1.0 : gates[(size_t)t * k + j]) *
-                       Yp[(size_t)row_of[(size_t)t * k + j] * H + h];
+            for (int j = 0; j < k; ++j) {
+                const int row = row_of[(size_t)t * k + j];
+                if (row < 0) continue;   /* dropped */
+                acc += (fold ? 1.0 : gates[(size_t)t * k + j]) * Yp[(size_t)row * H + h];
+            }
             y[(size_t)t * H + h] = acc;
         }
     double* Ys = NULL;
@@ -1168,7 +1194,10 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
         for (int t = 0; t < T; ++t)
             for (int h = 0; h < H; ++h) {
                 double acc = 0.0;
-                for (int j = 0; j < k; ++j) acc += dXp[(size_t)row_of[(size_t)t * k + j] * H + h];
+                for (int j = 0; j < k; ++j) {
+                    const int row = row_of[(size_t)t * k + j];
+                    if (row >= 0) acc += dXp[(size_t)row * H + h];
+                }
                 for (int e = 0; e < E; ++e) acc += dz[(size_t)t * E + e] * Wr[(size_t)h * E + e];
                 dX[(size_t)t * H + h] = acc;
             }
@@ -1180,7 +1209,7 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
         }
         free(Ytmp);
         free(dz);
-        if (dg_out) memcpy(dg_out, dg, sizeof(double) * (size_t)R);
+        if (dg_out) memcpy(dg_out, dg, sizeof(double) * (size_t)T * k);
     }
     free(Ys); free(Xp); free(Yp); free(dYp); free(dXp); free(dg); free(grow);
     free(counts); free(offsets); free(row_of); free(slot_of);

@@ -189,26 +189,35 @@ def _q_cols_segment(X):
     return out
 
 
-@pytest.mark.parametrize("fold", [False, True])
-def test_fp8_multi_expert_matches_independent_fp8_swiglu(fold):
+@pytest.mark.parametrize("fold,drop", [(False, False), (True, False), (False, True), (True, True)])
+def test_fp8_multi_expert_matches_independent_fp8_swiglu(fold, drop):
     """Several experts with ragged segments (more than one 128-token block,
     the last one partial): the weight-gradient operands are quantised per
     expert segment, in 128-token blocks counted from the segment's first row.
     An independent FP8 layer (torch's E4M3 codec, rows gathered per expert
-    with numpy) must give the oracle's y and weight gradients."""
+    with numpy) must give the oracle's y and weight gradients. drop: capacity
+    130 per expert, so each expert's segment is its first 130 assignments
+    (a dropped assignment never reaches the expert) and the dropped slots get
+    dg = 0."""
     T, H, E, k, F = 333, 256, 3, 2, 256
     p = _layer(T=T, H=H, E=E, k=k, F=F, Fs=0, score=oracle.SOFTMAX, seed=21)
     b = np.array([0.8, 0.0, -0.9])                    # uneven loads: all segments ragged
     r = oracle.route(p["x"], p["Wr"], b, k, oracle.SOFTMAX)
     counts = np.bincount(r["topk"].ravel(), minlength=E)
     assert np.all(counts > 128) and np.all(counts % 128 != 0) and len(set(counts)) == E
+    keep = oracle.capacity_keep(r["topk"], E, 130) if drop else np.ones_like(r["topk"], np.uint8)
+    if drop:
+        assert np.all(counts > 130) and (keep == 0).sum() == counts.sum() - 3 * 130
     q = oracle.layer_fp8(p["x"], p["Wr"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"],
-                         r["scores"], oracle.SOFTMAX, p["dY"], fold=fold)
+                         r["scores"], oracle.SOFTMAX, p["dY"], fold=fold,
+                         keep=keep if drop else None)
+    if drop:
+        assert np.all(q["dg"][keep == 0] == 0) and np.all(q["dg"][keep == 1] != 0)
     bf = lambda v: torch.from_numpy(np.ascontiguousarray(v)).to(torch.bfloat16).double().numpy()
     y = np.zeros((T, H))
     ref = {n: np.zeros_like(p[w]) for n, w in (("dWg", "Wg"), ("dWu", "Wu"), ("dWd", "Wd"))}
     for e in range(E):
-        toks, slots = np.nonzero(r["topk"] == e)          # the expert's rows, token order
+        toks, slots = np.nonzero((r["topk"] == e) & (keep == 1))   # the expert's rows, token order
         g = r["gates"][toks, slots][:, None]
         X = p["x"][toks]
         Wg, Wu, Wd = _q_tiles(p["Wg"][e]), _q_tiles(p["Wu"][e]), _q_tiles(p["Wd"][e])
@@ -236,6 +245,8 @@ def test_fp8_multi_expert_matches_independent_fp8_swiglu(fold):
         close = np.isclose(q[n], v, rtol=1e-9, atol=1e-9 * np.abs(v).max())
         assert close.mean() > 0.999, (n, close.mean())
         assert np.linalg.norm(q[n] - v) / np.linalg.norm(v) < 1e-3, n
+    if drop:
+        return
     # a block origin at a multiple of 128 of the whole permuted buffer, instead
     # of each segment's first row, gives visibly different weight gradients
     e = 1

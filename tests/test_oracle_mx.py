@@ -122,21 +122,29 @@ def _layer(T, H, E, k, F, seed):
                 Wd=rng.standard_normal((E, F, H)) * F ** -0.5, dY=rng.standard_normal((T, H)))
 
 
-@pytest.mark.parametrize("fold", [False, True])
-def test_mx_layer_matches_independent_mx_swiglu(fold):
+@pytest.mark.parametrize("fold,drop", [(False, False), (True, False), (False, True), (True, True)])
+def test_mx_layer_matches_independent_mx_swiglu(fold, drop):
+    """drop: capacity 100 per expert; the expert's segment (and its 32-row
+    blocks) is its first 100 assignments, the dropped slots get dg = 0."""
     T, H, E, k, F = 333, 256, 3, 2, 256
     p = _layer(T, H, E, k, F, seed=23)
     b = np.array([0.8, 0.0, -0.9])
     r = oracle.route(p["x"], p["Wr"], b, k, oracle.SOFTMAX)
     counts = np.bincount(r["topk"].ravel(), minlength=E)
     assert np.all(counts % 32 != 0)                   # every segment ends in a partial block
+    keep = oracle.capacity_keep(r["topk"], E, 100) if drop else np.ones_like(r["topk"], np.uint8)
+    if drop:
+        assert np.all(counts > 100)
     q = oracle.layer_fp8(p["x"], p["Wr"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"],
-                         r["scores"], oracle.SOFTMAX, p["dY"], fold=fold, recipe=oracle.RECIPE_MX)
+                         r["scores"], oracle.SOFTMAX, p["dY"], fold=fold, recipe=oracle.RECIPE_MX,
+                         keep=keep if drop else None)
+    if drop:
+        assert np.all(q["dg"][keep == 0] == 0) and np.all(q["dg"][keep == 1] != 0)
     bf = lambda v: torch.from_numpy(np.ascontiguousarray(v)).to(torch.bfloat16).double().numpy()
     y = np.zeros((T, H))
     ref = {n: np.zeros_like(p[w]) for n, w in (("dWg", "Wg"), ("dWu", "Wu"), ("dWd", "Wd"))}
     for e in range(E):
-        toks, slots = np.nonzero(r["topk"] == e)
+        toks, slots = np.nonzero((r["topk"] == e) & (keep == 1))
         g = r["gates"][toks, slots][:, None]
         X = p["x"][toks]
         Wg_f, Wu_f, Wd_f = _mx(p["Wg"][e], 0), _mx(p["Wu"][e], 0), _mx(p["Wd"][e], 0)
