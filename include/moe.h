@@ -68,8 +68,7 @@ typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
  *     K for the operand indexing output rows, 128x128 for the other), fp32
  *     accumulation ("Scalable Training of Mixture-of-Experts Models with
  *     Megatron Core", §5, blockwise FP8). The router stays fp32. Layers with
- *     a shared expert or with capacity_factor > 0 are not supported in this
- *     mode (MOE_ERR_UNSUPPORTED).
+ *     a shared expert are not supported in this mode (MOE_ERR_UNSUPPORTED).
  *   MOE_MXFP8: bf16 activations, weights and gradients; every expert GEMM
  *     runs on E4M3 operands in the MXFP8 recipe ("Scalable Training of
  *     Mixture-of-Experts Models with Megatron Core", §5 Platform-specific
@@ -79,8 +78,8 @@ typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
  *     amax <= 448 2^e; the tensor cores apply the scales. Both operands of
  *     every GEMM are blocked along K, so weights (and the activations and
  *     gradients that feed two GEMMs) are quantised once per orientation.
- *     The router stays fp32. Layers with a shared expert or with
- *     capacity_factor > 0 are not supported (MOE_ERR_UNSUPPORTED). */
+ *     The router stays fp32. Layers with a shared expert are not supported
+ *     (MOE_ERR_UNSUPPORTED). */
 typedef enum { MOE_FP32 = 0, MOE_BF16 = 1, MOE_FP8_BLOCK = 2, MOE_MXFP8 = 3 } moe_dtype_t;
 
 typedef struct {
@@ -102,8 +101,9 @@ typedef struct {
                     first; a dropped assignment adds nothing to y, gets no
                     expert gradient and has dg = 0 (its routing gradient still
                     flows through the other slots' renormalised gates).
-                    MOE_FP8_BLOCK or MOE_MXFP8 with capacity_factor > 0:
-                    UNSUPPORTED. */
+                    In the FP8 recipes a dropped assignment never reaches its
+                    expert: its rows are zeros in every quantisation block
+                    along the tokens (the weight-gradient operands). */
 } moe_config_t;
 
 /* Plan flag: bracket every kernel launch of moe_forward / moe_backward with

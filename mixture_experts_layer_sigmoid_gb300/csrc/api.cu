@@ -23,11 +23,12 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct Layout {
     int T, R, Rp_max, MT_max, NB;
     // saved
-    size_t topk, gates, selsc, counts, kept, poff, meta, tiletab, pairtab, rowof, slotof, eorder;
+    size_t topk, gates, selsc, counts, kept, poff, meta, tiletab, pairtab, rowof, slotof, eorder, slotlive;
     size_t Xp, A, U, Hh, Yp, As, Us, Hs, saved_bytes;
     // workspace
     size_t status, hist, blkbase, zpart, Ys, dYp, dA, dU, dXp, dz, WrT, wrpart, dAs, dUs, dXs, dgpart, ws_bytes;
     bool fold;   // Hh and Yp live in the workspace (MOE_FLAG_FOLD_GATES)
+    bool slotlive_on;   // FP8 recipe with capacity-limited dropping
     // FP8 recipes (saved: permuted activations and, unless the caller passes a
     // weight cache, the weight codes; ws: the rest)
     size_t Xq, sX, wcache;
@@ -112,6 +113,11 @@ Layout make_layout(const moe_config_t& c, int T)
     L.pairtab = take(sizeof(int) * (2 * ((size_t)L.MT_max + c.E + 1) + c.E));
     L.rowof = take(sizeof(int) * L.R);
     L.slotof = take(sizeof(int) * L.Rp_max);
+    // FP8 recipes with capacity-limited dropping: the slot map of the rows an
+    // expert computes (-1 for dropped and pad rows), for the quantisers of the
+    // weight-gradient operands
+    L.slotlive_on = fp8_recipe(c) && c.capacity_factor > 0.f;
+    L.slotlive = take(L.slotlive_on ? sizeof(int) * L.Rp_max : 0);
     // (the FP8 layers keep only the codes of the permuted rows)
     L.Xp = take(fp8_recipe(c) ? 0 : es * L.Rp_max * c.H);
     L.A = take(es * L.Rp_max * c.F);
@@ -194,7 +200,6 @@ moe_status_t check_config(const moe_config_t* c)
     // a dropped assignment keeps its row of Xp (the router gradient needs it),
     // which would enter the 128-token quantisation blocks of the FP8 weight
     // gradients; dropping is built for the bf16 and fp32 layers only
-    if (fp8_recipe(*c) && c->capacity_factor > 0.f) return MOE_ERR_UNSUPPORTED;
     // int32 row indices: R_pad * max(H, F) elements must stay addressable per
     // buffer with 32-bit row numbers
     const long long R = (long long)c->T_max * c->top_k + (long long)c->E * kTileM;
@@ -732,7 +737,10 @@ static moe_status_t forward_fp8_impl(moe_plan_t p, int T_, const moe_fwd_args_t*
                                    reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab,
                                    pairtab + L.MT_max, capacity(c, T_), kept,
                                    reinterpret_cast<int*>(sv + L.eorder)));
-    MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
+    int* slotlive = L.slotlive_on ? reinterpret_cast<int*>(sv + L.slotlive) : nullptr;
+    if (slotlive) MOE_CUDA(cudaMemsetAsync(slotlive, 0xFF, sizeof(int) * (size_t)L.Rp_max, s));
+    MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s,
+                                     poff, kept, slotlive));
     MOE_STAGE(ST_PERMUTE, launch_permute_quant(x, rowof, poff, counts, T_, H, E, k, nullptr, u8(sv, L.Xq),
                                                f32(sv, L.sX), s));
     // one orientation of the weight codes: the forward GEMMs read them
@@ -796,6 +804,8 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     const int* pairtab = reinterpret_cast<const int*>(sv + L.pairtab);
     const int* rowof = reinterpret_cast<const int*>(sv + L.rowof);
     const int* slotof = reinterpret_cast<const int*>(sv + L.slotof);
+    // rows of dropped assignments: zero output gradients, no part in the quantisation blocks
+    const int* slotlive = L.slotlive_on ? reinterpret_cast<const int*>(sv + L.slotlive) : nullptr;
     const T* A = reinterpret_cast<const T*>(sv + L.A);
     const T* U = reinterpret_cast<const T*>(sv + L.U);
     T* Hh = reinterpret_cast<T*>((L.fold ? ws : sv) + L.Hh);   // folded: recomputed below
@@ -814,10 +824,10 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
 
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
     if (L.fold)
-        MOE_STAGE(ST_GATEGRAD, launch_permute<T>(dY, rowof, poff, counts, T_, H, E, k, dYp, s));
+        MOE_STAGE(ST_GATEGRAD, launch_permute<T>(dY, rowof, poff, counts, T_, H, E, k, dYp, s, slotlive));
     else
         MOE_STAGE(ST_GATEGRAD, launch_gate_grad<T>(dY, Yp, rowof, topk, gates, selsc, poff, counts, T_, H,
-                                                   E, k, c.score, dYp, dz, s));
+                                                   E, k, c.score, dYp, dz, s, slotlive));
     // fc2 dgrad + SwiGLU backward
     // dYp once: 1x128 row codes (fc2 dgrad) and transposed 128x128-tile codes (fc2 wgrad)
     MOE_STAGE(ST_QROWS, launch_quant(QuantJob{dYp, meta + 1, Rp, H, Rp, u8(ws, L.dYq), f32(ws, L.sdY), 0,
@@ -871,7 +881,8 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     // fc1 wgrad: dWg[e] = Xp_e^T dA_e, dWu[e] = Xp_e^T dU_e
     // the permuted rows are token rows of x (no bf16 copy of them is kept)
     MOE_STAGE(ST_QT, launch_quant(QuantJob{static_cast<const T*>(a->x), meta + 1, Rp, H, Rp, nullptr,
-                                           nullptr, 0, u8(ws, L.XpTq), f32(ws, L.sXpT), 0, slotof, k}, s));
+                                           nullptr, 0, u8(ws, L.XpTq), f32(ws, L.sXpT), 0,
+                                           slotlive ? slotlive : slotof, k}, s));
     memset(&d, 0, sizeof d);
     d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
     d.N = F; d.M_out = H; d.E = E;
@@ -932,7 +943,10 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
                                    reinterpret_cast<int*>(ws + L.blkbase), tiletab, meta, slotof, s, pairtab,
                                    pairtab + L.MT_max, capacity(c, T_), kept,
                                    reinterpret_cast<int*>(sv + L.eorder)));
-    MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s));
+    int* slotlive = L.slotlive_on ? reinterpret_cast<int*>(sv + L.slotlive) : nullptr;
+    if (slotlive) MOE_CUDA(cudaMemsetAsync(slotlive, 0xFF, sizeof(int) * (size_t)L.Rp_max, s));
+    MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s,
+                                     poff, kept, slotlive));
     MOE_STAGE(ST_PERMUTE, launch_mx_permute(x, rowof, poff, counts, T_, H, E, k, sv + L.Xq, sv + L.sX, s));
     const WQ wq = weight_codes(c, L, sv, a->weight_cache);
     if (!a->weight_cache)
@@ -992,6 +1006,8 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
     const int* eorder = reinterpret_cast<const int*>(sv + L.eorder);
     const int* rowof = reinterpret_cast<const int*>(sv + L.rowof);
     const int* slotof = reinterpret_cast<const int*>(sv + L.slotof);
+    // rows of dropped assignments: zero output gradients, no part in the quantisation blocks
+    const int* slotlive = L.slotlive_on ? reinterpret_cast<const int*>(sv + L.slotlive) : nullptr;
     const T* A = reinterpret_cast<const T*>(sv + L.A);
     const T* U = reinterpret_cast<const T*>(sv + L.U);
     T* Hh = reinterpret_cast<T*>((L.fold ? ws : sv) + L.Hh);   // folded: recomputed below
@@ -1009,10 +1025,10 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
 
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
     if (L.fold)
-        MOE_STAGE(ST_GATEGRAD, launch_permute<T>(dY, rowof, poff, counts, T_, H, E, k, dYp, s));
+        MOE_STAGE(ST_GATEGRAD, launch_permute<T>(dY, rowof, poff, counts, T_, H, E, k, dYp, s, slotlive));
     else
         MOE_STAGE(ST_GATEGRAD, launch_gate_grad<T>(dY, Yp, rowof, topk, gates, selsc, poff, counts, T_, H,
-                                                   E, k, c.score, dYp, dz, s));
+                                                   E, k, c.score, dYp, dz, s, slotlive));
     // dYp once: row codes (fc2 dgrad, K = H) and transposed column codes (fc2 wgrad, K = tokens)
     {
         MxQuantJob j{dYp, meta + 1, Rp, H, Rp, ws + L.dYq, ws + L.sdY, ws + L.dYpTq, ws + L.sdYpT, 1};
@@ -1071,7 +1087,7 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
     {
         MxQuantJob j{static_cast<const T*>(a->x), meta + 1, Rp, H, Rp, nullptr, nullptr, ws + L.XpTq,
                      ws + L.sXpT, 1};
-        j.gather_slot = slotof;
+        j.gather_slot = slotlive ? slotlive : slotof;
         j.gather_k = k;
         MOE_STAGE(ST_QT, launch_mx_quant(j, s));
     }

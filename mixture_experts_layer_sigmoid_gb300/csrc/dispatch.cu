@@ -82,20 +82,25 @@ __device__ void zero_pad_rows(T* buf, int H, int e, const int* poff, const int* 
 template <typename T, int KM>
 __global__ void __launch_bounds__(kRowThreads)
 permute_kernel(const T* __restrict__ x, const int* __restrict__ row_of, const int* __restrict__ poff,
-               const int* __restrict__ counts, int T_, int H, int k, T* __restrict__ Xp)
+               const int* __restrict__ counts, int T_, int H, int k, T* __restrict__ Xp,
+               const int* __restrict__ slot_live)
 {
     const int b = blockIdx.x;
     if (b >= T_) { zero_pad_rows(Xp, H, b - T_, poff, counts); return; }
     constexpr int V = 16 / sizeof(T);
     int rows[KM];
+    bool live[KM];
 #pragma unroll
-    for (int j = 0; j < KM; ++j) rows[j] = j < k ? row_of[(size_t)b * k + j] : 0;
+    for (int j = 0; j < KM; ++j) {
+        rows[j] = j < k ? row_of[(size_t)b * k + j] : 0;
+        live[j] = j < k && (!slot_live || slot_live[rows[j]] >= 0);   // dropped rows: zeros
+    }
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)b * H);
     for (int v = threadIdx.x; v < H / V; v += kRowThreads) {
         uint4 q = src[v];
 #pragma unroll
         for (int j = 0; j < KM; ++j)
-            if (j < k) reinterpret_cast<uint4*>(Xp + (size_t)rows[j] * H)[v] = q;
+            if (j < k) reinterpret_cast<uint4*>(Xp + (size_t)rows[j] * H)[v] = live[j] ? q : make_uint4(0, 0, 0, 0);
     }
 }
 
@@ -170,7 +175,7 @@ __global__ void __launch_bounds__(kRowThreads)
 gate_grad_kernel(const T* __restrict__ dY, const T* __restrict__ Yp, const int* __restrict__ row_of,
                  const float* __restrict__ gates, const float* __restrict__ selsc,
                  const int* __restrict__ poff, const int* __restrict__ counts, int T_, int H, int k,
-                 int score, T* __restrict__ dYp, float* __restrict__ dz)
+                 int score, T* __restrict__ dYp, float* __restrict__ dz, const int* __restrict__ slot_live)
 {
     const int b = blockIdx.x;
     if (b >= T_) { zero_pad_rows(dYp, H, b - T_, poff, counts); return; }
@@ -178,12 +183,14 @@ gate_grad_kernel(const T* __restrict__ dY, const T* __restrict__ Yp, const int* 
     __shared__ float red[kRowThreads / 32][kMaxK];
     const int t = b;
     int rows[KM];
-    float g[kMaxK], dot[KM];
+    float g[kMaxK], gs[KM], dot[KM];
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
         dot[j] = 0.f;
         rows[j] = j < k ? row_of[(size_t)t * k + j] : 0;
         g[j] = j < k ? gates[(size_t)t * k + j] : 0.f;
+        // the output-gradient scale of the row (0 for a dropped assignment)
+        gs[j] = (j < k && slot_live && slot_live[rows[j]] < 0) ? 0.f : g[j];
     }
     for (int v = threadIdx.x; v < H / V; v += kRowThreads) {
         float dy[V], yp[V], o[V];
@@ -196,7 +203,7 @@ gate_grad_kernel(const T* __restrict__ dY, const T* __restrict__ Yp, const int* 
             Vec<T>::unpack(raw[j], yp);
             float s = 0.f;
 #pragma unroll
-            for (int i = 0; i < V; ++i) { s = fmaf(dy[i], yp[i], s); o[i] = g[j] * dy[i]; }
+            for (int i = 0; i < V; ++i) { s = fmaf(dy[i], yp[i], s); o[i] = gs[j] * dy[i]; }
             dot[j] += s;
             Vec<T>::store(dYp + (size_t)rows[j] * H + v * V, o);
         }
@@ -389,12 +396,12 @@ unpermute_reduce_kernel(const T* __restrict__ dXp, const T* __restrict__ dXs,
 
 template <typename T>
 cudaError_t launch_permute(const T* x, const int* row_of, const int* poff, const int* counts,
-                           int T_, int H, int E, int k, T* Xp, cudaStream_t s)
+                           int T_, int H, int E, int k, T* Xp, cudaStream_t s, const int* slot_live)
 {
     switch (slot_bound(k)) {
-    case 2: permute_kernel<T, 2><<<T_ + E, kRowThreads, 0, s>>>(x, row_of, poff, counts, T_, H, k, Xp); break;
-    case 4: permute_kernel<T, 4><<<T_ + E, kRowThreads, 0, s>>>(x, row_of, poff, counts, T_, H, k, Xp); break;
-    default: permute_kernel<T, 8><<<T_ + E, kRowThreads, 0, s>>>(x, row_of, poff, counts, T_, H, k, Xp); break;
+    case 2: permute_kernel<T, 2><<<T_ + E, kRowThreads, 0, s>>>(x, row_of, poff, counts, T_, H, k, Xp, slot_live); break;
+    case 4: permute_kernel<T, 4><<<T_ + E, kRowThreads, 0, s>>>(x, row_of, poff, counts, T_, H, k, Xp, slot_live); break;
+    default: permute_kernel<T, 8><<<T_ + E, kRowThreads, 0, s>>>(x, row_of, poff, counts, T_, H, k, Xp, slot_live); break;
     }
     count_launches();
     return cudaGetLastError();
@@ -417,16 +424,16 @@ template <typename T>
 cudaError_t launch_gate_grad(const T* dY, const T* Yp, const int* row_of, const int* topk,
                              const float* gates, const float* selsc, const int* poff,
                              const int* counts, int T_, int H, int E, int k, int score, T* dYp,
-                             float* dz, cudaStream_t s)
+                             float* dz, cudaStream_t s, const int* slot_live)
 {
     (void)topk;
     switch (slot_bound(k)) {
     case 2: gate_grad_kernel<T, 2><<<T_ + E, kRowThreads, 0, s>>>(dY, Yp, row_of, gates, selsc, poff, counts,
-                                                       T_, H, k, score, dYp, dz); break;
+                                                       T_, H, k, score, dYp, dz, slot_live); break;
     case 4: gate_grad_kernel<T, 4><<<T_ + E, kRowThreads, 0, s>>>(dY, Yp, row_of, gates, selsc, poff, counts,
-                                                       T_, H, k, score, dYp, dz); break;
+                                                       T_, H, k, score, dYp, dz, slot_live); break;
     default: gate_grad_kernel<T, 8><<<T_ + E, kRowThreads, 0, s>>>(dY, Yp, row_of, gates, selsc, poff, counts,
-                                                       T_, H, k, score, dYp, dz); break;
+                                                       T_, H, k, score, dYp, dz, slot_live); break;
     }
     count_launches();
     return cudaGetLastError();
@@ -475,12 +482,13 @@ cudaError_t launch_unpermute_reduce(const T* dXp, const T* dXs, const int* row_o
 
 #define MOE_INST(T)                                                                              \
     template cudaError_t launch_permute<T>(const T*, const int*, const int*, const int*, int, int, \
-                                           int, int, T*, cudaStream_t);                          \
+                                           int, int, T*, cudaStream_t, const int*);              \
     template cudaError_t launch_combine<T>(const T*, const T*, const int*, const float*, int, int, \
                                            int, T*, cudaStream_t);                               \
     template cudaError_t launch_gate_grad<T>(const T*, const T*, const int*, const int*,         \
                                              const float*, const float*, const int*, const int*, \
-                                             int, int, int, int, int, T*, float*, cudaStream_t); \
+                                             int, int, int, int, int, T*, float*, cudaStream_t, \
+                                             const int*);                                        \
     template cudaError_t launch_router_wgrad<T>(const T*, const int*, const int*, const int*,    \
                                                 int, const float*, int, int, int, float*,        \
                                                 float*, cudaStream_t);                           \

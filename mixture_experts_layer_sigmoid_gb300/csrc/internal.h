@@ -142,19 +142,26 @@ cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff
                         int* pair_tab = nullptr, int* pair_off = nullptr, int cap = -1,
                         int* kept = nullptr, int* eorder = nullptr, int* full_tab = nullptr,
                         int* full_off = nullptr, int* tail_tab = nullptr);
+// slot_live (optional, capacity-limited dropping): slot_live[r] = slot_of[r]
+// for the rows an expert computes (r < poff[e] + kept[e]); the caller sets
+// the array to -1 first, so dropped and pad rows read -1.
 cudaError_t launch_index(const int* topk, const int* blkbase, int T_, int E, int k, int* row_of,
-                         int* slot_of, cudaStream_t s);
+                         int* slot_of, cudaStream_t s, const int* poff = nullptr,
+                         const int* kept = nullptr, int* slot_live = nullptr);
+// slot_live (optional): rows it marks -1 (dropped assignments) are written as zeros.
 template <typename T>
 cudaError_t launch_permute(const T* x, const int* row_of, const int* poff, const int* counts,
-                           int T_, int H, int E, int k, T* Xp, cudaStream_t s);
+                           int T_, int H, int E, int k, T* Xp, cudaStream_t s,
+                           const int* slot_live = nullptr);
 template <typename T>
 cudaError_t launch_combine(const T* Yp, const T* Ys, const int* row_of, const float* gates,
                            int T_, int H, int k, T* y, cudaStream_t s);
+// slot_live (optional): the rows of dropped assignments get dYp = 0.
 template <typename T>
 cudaError_t launch_gate_grad(const T* dY, const T* Yp, const int* row_of, const int* topk,
                              const float* gates, const float* selsc, const int* poff,
                              const int* counts, int T_, int H, int E, int k, int score, T* dYp,
-                             float* dz, cudaStream_t s);
+                             float* dz, cudaStream_t s, const int* slot_live = nullptr);
 // Folded routing weights: dz from the fc2-dgrad partial dot products.
 cudaError_t launch_gate_dz(const float* dg_part, int nslots, const int* row_of, const float* gates,
                            const float* selsc, int T_, int k, int score, float* dz, cudaStream_t s);

@@ -594,7 +594,8 @@ scan_kernel(const int* __restrict__ hist, int nblk, int E, int* __restrict__ cou
 
 __global__ void __launch_bounds__(256)
 index_kernel(const int* __restrict__ topk, const int* __restrict__ blkbase, int T_, int E, int k,
-             int* __restrict__ row_of, int* __restrict__ slot_of)
+             int* __restrict__ row_of, int* __restrict__ slot_of, const int* __restrict__ poff,
+             const int* __restrict__ kept, int* __restrict__ slot_live)
 {
     __shared__ int sel[kRouterTokens * kMaxK];
     const int t0 = blockIdx.x * kRouterTokens;
@@ -611,6 +612,7 @@ index_kernel(const int* __restrict__ topk, const int* __restrict__ blkbase, int 
         const int slot = (t0 + tt) * k + (p % k);
         row_of[slot] = row;
         slot_of[row] = slot;
+        if (slot_live && row < poff[e] + kept[e]) slot_live[row] = slot;
     }
 }
 
@@ -710,10 +712,11 @@ cudaError_t launch_scan(const int* hist, int nblk, int E, int* counts, int* poff
 }
 
 cudaError_t launch_index(const int* topk, const int* blkbase, int T_, int E, int k, int* row_of,
-                         int* slot_of, cudaStream_t s)
+                         int* slot_of, cudaStream_t s, const int* poff, const int* kept, int* slot_live)
 {
+    if (slot_live && (!poff || !kept)) return cudaErrorInvalidValue;
     const int nblk = (T_ + kRouterTokens - 1) / kRouterTokens;
-    index_kernel<<<nblk, 256, 0, s>>>(topk, blkbase, T_, E, k, row_of, slot_of);
+    index_kernel<<<nblk, 256, 0, s>>>(topk, blkbase, T_, E, k, row_of, slot_of, poff, kept, slot_live);
     count_launches();
     return cudaGetLastError();
 }

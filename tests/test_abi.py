@@ -58,15 +58,31 @@ def test_plan_create_rejects_bad_configs(lib, bad):
     assert plan.value is None
 
 
-def test_fp8_with_capacity_dropping_is_reported_unsupported(lib):
+@pytest.mark.parametrize("dtype", [2, 3])
+def test_fp8_with_capacity_dropping_passes_validation(lib, dtype):
+    """Both FP8 recipes accept capacity-limited dropping: the config is valid
+    (a plan on a GPU; without one, only the device query fails)."""
     plan = ctypes.c_void_p()
-    assert lib.moe_plan_create(ctypes.byref(_cfg(dtype=2, capacity_factor=1.0)), 0,
+    st = lib.moe_plan_create(ctypes.byref(_cfg(dtype=dtype, capacity_factor=1.0)), 0, ctypes.byref(plan))
+    # (UNSUPPORTED only for a device that is not sm_103)
+    assert st in (moe.MOE_OK, moe.MOE_ERR_CUDA) or (st == moe.MOE_ERR_UNSUPPORTED and not _has_sm103())
+    if st == moe.MOE_OK:
+        assert lib.moe_plan_destroy(plan) == moe.MOE_OK
+
+
+def _has_sm103():
+    try:
+        import torch
+        return torch.cuda.is_available() and torch.cuda.get_device_capability(0) == (10, 3)
+    except Exception:
+        return False
+
+
+@pytest.mark.parametrize("dtype", [2, 3])
+def test_fp8_with_shared_expert_is_reported_unsupported(lib, dtype):
+    plan = ctypes.c_void_p()
+    assert lib.moe_plan_create(ctypes.byref(_cfg(dtype=dtype, Fs=256)), 0,
                                ctypes.byref(plan)) == moe.MOE_ERR_UNSUPPORTED
-
-
-def test_fp8_with_shared_expert_is_reported_unsupported(lib):
-    plan = ctypes.c_void_p()
-    assert lib.moe_plan_create(ctypes.byref(_cfg(dtype=2, Fs=256)), 0, ctypes.byref(plan)) == moe.MOE_ERR_UNSUPPORTED
 
 
 def test_null_arguments(lib):

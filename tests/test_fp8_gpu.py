@@ -94,15 +94,32 @@ def _fp8_parity(name, fold):
     print(name, fp8_layer_parity(FP8_CASES[name], fold))
 
 
-def fp8_layer_parity(w, fold=False):
+# Capacity-limited dropping in both FP8 recipes: a dropped assignment never
+# reaches its expert, so the quantisation blocks of the weight-gradient
+# operands (128 or 32 rows along the tokens) hold the kept rows and zeros.
+FP8_CAPACITY_CASES = [("qwen_fp8_small", mi.FP8_BLOCK, 1.0, False),
+                      ("qwen_fp8_many_rows_per_expert", mi.FP8_BLOCK, 0.8, True),
+                      ("qwen_fp8_small", mi.MXFP8, 1.0, False),
+                      ("qwen_fp8_many_rows_per_expert", mi.MXFP8, 0.8, True),
+                      ("qwen_fp8_ragged", mi.MXFP8, 1.5, False)]
+
+
+@pytest.mark.parametrize("name,dtype,cf,fold", FP8_CAPACITY_CASES)
+def test_fp8_capacity_dropping_matches_oracle(name, dtype, cf, fold):
+    print(name, dtype, cf, fold, fp8_layer_parity(mi.scaled(FP8_CASES[name], dtype=dtype), fold, cf))
+
+
+def fp8_layer_parity(w, fold=False, capacity_factor=0.0):
     """The FP8 layer on workload w (blockwise or MXFP8, by w.dtype) against
     the oracle's FP8 layer in the same recipe (bounds in the module
-    docstring); returns the error report."""
+    docstring); with capacity_factor > 0 the oracle drops the same
+    assignments (capacity_keep). Returns the error report."""
     inp = mi.make_inputs(w)
     g = upload(inp)
     mx = w.dtype == mi.MXFP8
     layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score,
-                         dtype=moe.MOE_MXFP8 if mx else moe.MOE_FP8_BLOCK, fold_gates=fold)
+                         dtype=moe.MOE_MXFP8 if mx else moe.MOE_FP8_BLOCK, fold_gates=fold,
+                         capacity_factor=capacity_factor)
     y, rt = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"], routing=True)
     gr = layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
     torch.cuda.synchronize()
@@ -115,9 +132,14 @@ def fp8_layer_parity(w, fold=False):
     assert not np.any(mism & ~tie)
     if mism.any():
         r = oracle.route(d["x"], d["Wr"], d["b"], w.k, w.score, replay_topk=gt, replay_mask=mism)
+    keep = None
+    if capacity_factor > 0:
+        C = oracle.capacity(w.T, w.k, w.E, capacity_factor)
+        keep = oracle.capacity_keep(r["topk"], w.E, C)
+        assert (keep == 0).any(), "case drops nothing"
     ref = oracle.layer_fp8(d["x"], d["Wr"], d["Wg"], d["Wu"], d["Wd"], r["topk"], r["gates"],
                            r["scores"], w.score, d["dY"], fold=fold,
-                           recipe=oracle.RECIPE_MX if mx else oracle.RECIPE_BLOCK)
+                           recipe=oracle.RECIPE_MX if mx else oracle.RECIPE_BLOCK, keep=keep)
     rep = {}
     for gname, oname in (("y", "y"), ("dX", "dX")):
         got = to_np(y if gname == "y" else gr[gname])
@@ -138,7 +160,8 @@ def fp8_layer_parity(w, fold=False):
             else:
                 assert np.linalg.norm(gb - wb) / nw <= 4e-2, gname
     write_report(f"{w.name} T{w.T} H{w.H} E{w.E} k{w.k} F{w.F} {'mxfp8' if mx else 'fp8'}"
-                 + (" fold" if fold else ""), rep)
+                 + (" fold" if fold else "") + (f" capacity {capacity_factor}" if capacity_factor else ""),
+                 rep)
     return rep
 
 
