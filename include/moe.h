@@ -78,8 +78,9 @@ typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
  *     amax <= 448 2^e; the tensor cores apply the scales. Both operands of
  *     every GEMM are blocked along K, so weights (and the activations and
  *     gradients that feed two GEMMs) are quantised once per orientation.
- *     The router stays fp32. Layers with a shared expert are not supported
- *     (MOE_ERR_UNSUPPORTED). */
+ *     The router stays fp32. A shared expert runs through the same engine
+ *     as a dense group of the T rows; its weights are quantised by every
+ *     forward (the weight cache holds the routed experts' weights). */
 typedef enum { MOE_FP32 = 0, MOE_BF16 = 1, MOE_FP8_BLOCK = 2, MOE_MXFP8 = 3 } moe_dtype_t;
 
 typedef struct {
@@ -166,7 +167,9 @@ typedef struct {
     const void*  weight_cache; /* optional in (FP8-recipe plans): expert
                               weights quantised by moe_quantize_weights. When
                               given, W_gate, W_up and W_down are not read (they
-                              may be NULL) and the call quantises no weights;
+                              may be NULL) and the call quantises none of the
+                              routed experts' weights (an MXFP8 layer's shared
+                              expert weights are still read and quantised);
                               the matching moe_backward must be given the same
                               cache. Other dtypes: must be NULL. */
 } moe_fwd_args_t;
@@ -200,7 +203,8 @@ typedef struct {
 /* Validate `cfg` for `device` and build a plan (host memory only).
  * Errors: INVALID_ARG (null, sizes out of range, unknown flags,
  *         capacity_factor negative or not finite),
- *         UNSUPPORTED (dtype not built, device not sm_103), CUDA. */
+ *         UNSUPPORTED (dtype not built, device not sm_103, MOE_FP8_BLOCK
+ *         with a shared expert), CUDA. */
 moe_status_t moe_plan_create(const moe_config_t* cfg, int device, moe_plan_t* out);
 
 /* Free a plan. NULL is accepted. */

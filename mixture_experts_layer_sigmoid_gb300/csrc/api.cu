@@ -34,6 +34,11 @@ struct Layout {
     size_t Xq, sX, wcache;
     size_t hq, sh, dYq, sdY, dAq, sdA, dUq, sdU, hTq, shT, dYpTq, sdYpT, XpTq, sXpT, dATq, sdAT,
         dUTq, sdUT;
+    // MXFP8 with a shared expert: its weight codes (saved) and the codes of its
+    // dense operands, rows padded to Tp = T rounded up to 128 (workspace)
+    int Tp;
+    size_t wcache_s, xsq, sxs, hsq, shs, dYsq, sdYs, dYsTq, sdYsT, hsTq, shsT, dAsq, sdAs, dUsq, sdUs,
+        dAsTq, sdAsT, dUsTq, sdUsT, xTq, sxT;
 };
 
 bool fp8_recipe(const moe_config_t& c) { return c.dtype == MOE_FP8_BLOCK || c.dtype == MOE_MXFP8; }
@@ -66,6 +71,18 @@ SplitTabs split_tabs(const Layout& L, int E, const uint8_t* sv)
 struct WeightCache {
     size_t q[6], s[6], bytes;
 };
+
+// The shared expert as a one-expert layer of width Fs (its weight codes use
+// the routed weights' cache layout).
+moe_config_t shared_config(const moe_config_t& c)
+{
+    moe_config_t s = c;
+    s.E = 1;
+    s.F = c.Fs;
+    s.Fs = 0;
+    s.top_k = 1;
+    return s;
+}
 
 WeightCache cache_layout(const moe_config_t& c)
 {
@@ -135,6 +152,9 @@ Layout make_layout(const moe_config_t& c, int T)
     L.Xq = take(anyq ? Rp * c.H : 0);
     L.sX = take(scb(Rp * (c.H / 128)));
     L.wcache = take(cache_layout(c).bytes);
+    const bool mxs = mx && c.Fs > 0;
+    L.Tp = (int)align_up((size_t)T, 128);
+    L.wcache_s = take(mxs ? cache_layout(shared_config(c)).bytes : 0);
     L.saved_bytes = o;
     o = 0;
     L.status = take(256);
@@ -170,6 +190,19 @@ Layout make_layout(const moe_config_t& c, int T)
         L.Yp = take(es * L.Rp_max * c.H);
     }
     L.dUTq = take(anyq ? Rp * c.F : 0);   L.sdUT = take(mx ? RF32 : scb((Rp / 128) * (c.F / 128)));
+    {
+        const size_t TpH = mxs ? (size_t)L.Tp * c.H : 0, TpF = mxs ? (size_t)L.Tp * c.Fs : 0;
+        L.xsq = take(TpH);   L.sxs = take(TpH / 32);     // x, rows (shared fc1)
+        L.hsq = take(TpF);   L.shs = take(TpF / 32);     // h_s, rows (shared fc2)
+        L.dYsq = take(TpH);  L.sdYs = take(TpH / 32);    // dY, rows (shared fc2 dgrad)
+        L.dYsTq = take(TpH); L.sdYsT = take(TpH / 32);   // dY, columns (shared fc2 wgrad)
+        L.hsTq = take(TpF);  L.shsT = take(TpF / 32);    // h_s, columns
+        L.dAsq = take(TpF);  L.sdAs = take(TpF / 32);    // dA_s, dU_s: rows and columns
+        L.dUsq = take(TpF);  L.sdUs = take(TpF / 32);
+        L.dAsTq = take(TpF); L.sdAsT = take(TpF / 32);
+        L.dUsTq = take(TpF); L.sdUsT = take(TpF / 32);
+        L.xTq = take(TpH);   L.sxT = take(TpH / 32);     // x, columns (shared fc1 wgrad)
+    }
     L.ws_bytes = o;
     return L;
 }
@@ -196,10 +229,7 @@ moe_status_t check_config(const moe_config_t* c)
     if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
     if (c->dtype != MOE_FP32 && c->dtype != MOE_BF16 && c->dtype != MOE_FP8_BLOCK && c->dtype != MOE_MXFP8)
         return MOE_ERR_INVALID_ARG;
-    if (fp8_recipe(*c) && c->Fs > 0) return MOE_ERR_UNSUPPORTED;
-    // a dropped assignment keeps its row of Xp (the router gradient needs it),
-    // which would enter the 128-token quantisation blocks of the FP8 weight
-    // gradients; dropping is built for the bf16 and fp32 layers only
+    if (c->dtype == MOE_FP8_BLOCK && c->Fs > 0) return MOE_ERR_UNSUPPORTED;
     // int32 row indices: R_pad * max(H, F) elements must stay addressable per
     // buffer with 32-bit row numbers
     const long long R = (long long)c->T_max * c->top_k + (long long)c->E * kTileM;
@@ -660,6 +690,16 @@ struct WQ {
     uint8_t* q[6];   // gate, up, down: forward orientation, then data-gradient orientation
     void* s[6];
 };
+static WQ codes_at(const moe_config_t& c, uint8_t* b)
+{
+    WQ w;
+    const WeightCache C = cache_layout(c);
+    for (int i = 0; i < 6; ++i) {
+        w.q[i] = b + C.q[i];
+        w.s[i] = b + C.s[i];
+    }
+    return w;
+}
 static WQ weight_codes(const moe_config_t& c, const Layout& L, uint8_t* sv, const void* cache)
 {
     WQ w;
@@ -974,7 +1014,41 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
     d.B0 = wq.q[2]; d.ldb = H; d.b_rows = E * F; d.XB0 = xs(wq.s[2]); d.b_kmajor = 0;
     d.O0 = Yp; d.ldo = H; d.status = status;
     MOE_STAGE(ST_FC2, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
-    MOE_STAGE(ST_COMBINE, launch_combine<T>(Yp, nullptr, rowof, L.fold ? nullptr : gates, T_, H, k,
+    T* Ys = nullptr;
+    if (c.Fs) {
+        // the shared expert: a dense group of the T token rows (padded to Tp
+        // in its codes), its weights quantised like a one-expert layer's
+        const moe_config_t cs = shared_config(c);
+        const WQ wqs = codes_at(cs, sv + L.wcache_s);
+        const int Fs = c.Fs, Tp = L.Tp;
+        T* As = reinterpret_cast<T*>(sv + L.As);
+        T* Us = reinterpret_cast<T*>(sv + L.Us);
+        T* Hs = reinterpret_cast<T*>(sv + L.Hs);
+        Ys = reinterpret_cast<T*>(ws + L.Ys);
+        MOE_STAGE(ST_WQUANT, quantize_weights(cs, a->Ws_gate, a->Ws_up, a->Ws_down, wqs, s));
+        {
+            MxQuantJob j{x, nullptr, Tp, H, Tp, ws + L.xsq, ws + L.sxs, nullptr, nullptr, 0};
+            j.rows_valid = T_;
+            MOE_STAGE(ST_QROWS, launch_mx_quant(j, s));
+        }
+        memset(&d, 0, sizeof d);
+        d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_FWD; d.dual = DUAL_N;
+        d.N = Fs; d.K = H; d.E = 1; d.dense_rows = T_;
+        d.A0 = ws + L.xsq; d.lda = H; d.a_rows = Tp; d.XA0 = ws + L.sxs;
+        d.B0 = wqs.q[0]; d.B1 = wqs.q[1]; d.ldb = Fs; d.b_rows = H; d.b_kmajor = 0;
+        d.XB0 = xs(wqs.s[0]); d.XB1 = xs(wqs.s[1]);
+        d.O0 = As; d.O1 = Us; d.O2 = Hs; d.ldo = Fs; d.status = status;
+        d.Qrows = ws + L.hsq; d.Qatoms = ws + L.shs;              // shared fc2's A operand
+        MOE_STAGE(ST_FC1S, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+        memset(&d, 0, sizeof d);
+        d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
+        d.N = H; d.K = Fs; d.E = 1; d.dense_rows = T_;
+        d.A0 = ws + L.hsq; d.lda = Fs; d.a_rows = Tp; d.XA0 = ws + L.shs;
+        d.B0 = wqs.q[2]; d.ldb = H; d.b_rows = Fs; d.XB0 = xs(wqs.s[2]); d.b_kmajor = 0;
+        d.O0 = Ys; d.ldo = H; d.status = status;
+        MOE_STAGE(ST_FC2S, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    }
+    MOE_STAGE(ST_COMBINE, launch_combine<T>(Yp, Ys, rowof, L.fold ? nullptr : gates, T_, H, k,
                                             static_cast<T*>(a->y), s));
 
     if (a->topk_idx) MOE_CUDA(cudaMemcpyAsync(a->topk_idx, topk, sizeof(int) * L.R, cudaMemcpyDeviceToDevice, s));
@@ -1102,10 +1176,81 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
     d.rows_cap = Rp; d.expert_order = eorder;
     d.O0 = a->dW_gate; d.O1 = a->dW_up; d.ldo = F; d.o_estride = (long long)H * F; d.status = status;
     MOE_STAGE(ST_FC1_WGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    T* dXs = nullptr;
+    if (c.Fs) {
+        // the shared expert's backward; its output gradient is dY itself
+        const moe_config_t cs = shared_config(c);
+        const WQ wqs = codes_at(cs, sv + L.wcache_s);
+        const int Fs = c.Fs, Tp = L.Tp;
+        const T* As = reinterpret_cast<const T*>(sv + L.As);
+        const T* Us = reinterpret_cast<const T*>(sv + L.Us);
+        const T* Hs = reinterpret_cast<const T*>(sv + L.Hs);
+        T* dAs = reinterpret_cast<T*>(ws + L.dAs);
+        T* dUs = reinterpret_cast<T*>(ws + L.dUs);
+        dXs = reinterpret_cast<T*>(ws + L.dXs);
+        // dY: row codes (shared fc2 dgrad, K = H), column codes (shared fc2 wgrad, K = tokens)
+        {
+            MxQuantJob j{dY, nullptr, Tp, H, Tp, ws + L.dYsq, ws + L.sdYs, ws + L.dYsTq, ws + L.sdYsT, 1};
+            j.rows_valid = T_;
+            MOE_STAGE(ST_QROWS, launch_mx_quant(j, s));
+        }
+        memset(&d, 0, sizeof d);
+        d.sched = SCHED_ROWS; d.epi = EPI_SWIGLU_BWD; d.dual = DUAL_NONE;
+        d.N = Fs; d.K = H; d.E = 1; d.dense_rows = T_;
+        d.A0 = ws + L.dYsq; d.lda = H; d.a_rows = Tp; d.XA0 = ws + L.sdYs;
+        d.B0 = wqs.q[5]; d.ldb = H; d.b_rows = Fs; d.XB0 = xs(wqs.s[5]); d.b_kmajor = 1;
+        d.X0 = As; d.X1 = Us; d.O0 = dAs; d.O1 = dUs; d.ldo = Fs; d.status = status;
+        MOE_STAGE(ST_FC2S_DGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+        {
+            MxQuantJob j{Hs, nullptr, Tp, Fs, Tp, nullptr, nullptr, ws + L.hsTq, ws + L.shsT, 1};
+            j.rows_valid = T_;
+            MOE_STAGE(ST_QT, launch_mx_quant(j, s));
+        }
+        memset(&d, 0, sizeof d);
+        d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_NONE;
+        d.N = H; d.M_out = Fs; d.E = 1; d.dense_rows = T_;
+        d.A0 = ws + L.hsTq; d.lda = Tp; d.XA0 = ws + L.shsT;
+        d.B0 = ws + L.dYsTq; d.ldb = Tp; d.XB0 = ws + L.sdYsT;
+        d.rows_cap = Tp;
+        d.O0 = a->dWs_down; d.ldo = H; d.o_estride = (long long)Fs * H; d.status = status;
+        MOE_STAGE(ST_FC2S_WGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+        {
+            MxQuantJob ja{dAs, nullptr, Tp, Fs, Tp, ws + L.dAsq, ws + L.sdAs, ws + L.dAsTq, ws + L.sdAsT, 1};
+            ja.rows_valid = T_;
+            MOE_STAGE(ST_QROWS, launch_mx_quant(ja, s));
+            MxQuantJob ju{dUs, nullptr, Tp, Fs, Tp, ws + L.dUsq, ws + L.sdUs, ws + L.dUsTq, ws + L.sdUsT, 1};
+            ju.rows_valid = T_;
+            MOE_STAGE(ST_QROWS, launch_mx_quant(ju, s));
+        }
+        memset(&d, 0, sizeof d);
+        d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_K;
+        d.N = H; d.K = Fs; d.E = 1; d.dense_rows = T_;
+        d.A0 = ws + L.dAsq; d.A1 = ws + L.dUsq; d.lda = Fs; d.a_rows = Tp;
+        d.XA0 = ws + L.sdAs; d.XA1 = ws + L.sdUs;
+        d.B0 = wqs.q[3]; d.B1 = wqs.q[4]; d.ldb = Fs; d.b_rows = H; d.b_kmajor = 1;
+        d.XB0 = xs(wqs.s[3]); d.XB1 = xs(wqs.s[4]);
+        d.O0 = dXs; d.ldo = H; d.status = status;
+        MOE_STAGE(ST_FC1S_DGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+        {
+            MxQuantJob j{static_cast<const T*>(a->x), nullptr, Tp, H, Tp, nullptr, nullptr, ws + L.xTq,
+                         ws + L.sxT, 1};
+            j.rows_valid = T_;
+            MOE_STAGE(ST_QT, launch_mx_quant(j, s));
+        }
+        memset(&d, 0, sizeof d);
+        d.sched = SCHED_WGRAD; d.epi = EPI_WGRAD; d.dual = DUAL_N;
+        d.N = Fs; d.M_out = H; d.E = 1; d.dense_rows = T_;
+        d.A0 = ws + L.xTq; d.lda = Tp; d.XA0 = ws + L.sxT;
+        d.B0 = ws + L.dAsTq; d.B1 = ws + L.dUsTq; d.ldb = Tp;
+        d.XB0 = ws + L.sdAsT; d.XB1 = ws + L.sdUsT;
+        d.rows_cap = Tp;
+        d.O0 = a->dWs_gate; d.O1 = a->dWs_up; d.ldo = Fs; d.o_estride = (long long)H * Fs; d.status = status;
+        MOE_STAGE(ST_FC1S_WGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    }
     MOE_STAGE(ST_ROUTER_WGRAD, launch_router_wgrad<T>(static_cast<const T*>(a->x), slotof, poff, meta,
                                    L.MT_max, dz, H, E, k, reinterpret_cast<float*>(ws + L.wrpart), a->dWr, s));
     MOE_STAGE(ST_TRANSPOSE, launch_transpose_f32(a->Wr, H, E, WrT, s));
-    MOE_STAGE(ST_UNPERMUTE, launch_unpermute_reduce<T>(dXp, nullptr, rowof, topk, dz, WrT, T_, H, k,
+    MOE_STAGE(ST_UNPERMUTE, launch_unpermute_reduce<T>(dXp, dXs, rowof, topk, dz, WrT, T_, H, k,
                                                        static_cast<T*>(a->dX), s));
     return MOE_OK;
 }

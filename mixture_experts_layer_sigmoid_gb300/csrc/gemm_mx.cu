@@ -189,7 +189,12 @@ __device__ __forceinline__ void xtile_counts(const GemmDesc& d, int& num_m, int&
     constexpr int NW = (DUAL == DUAL_N) ? XBN / 2 : XBN;
     num_n = (d.N + NW - 1) / NW;
     if (SCHED == SCHED_ROWS) {
-        num_m = PAIR ? d.meta[2] : d.meta[0];
+        if (d.dense_rows > 0) {   // one dense group of rows (the shared expert)
+            const int tiles = (d.dense_rows + XBM - 1) / XBM;
+            num_m = PAIR ? (tiles + 1) / 2 : tiles;
+        } else {
+            num_m = PAIR ? d.meta[2] : d.meta[0];
+        }
         total = num_m * num_n;
     } else {
         num_m = d.M_out / (PAIR ? 2 * XBM : XBM);
@@ -208,22 +213,32 @@ __device__ __forceinline__ XTile xdecode(const GemmDesc& d, int w, int num_m, in
 {
     XTile t;
     if (SCHED == SCHED_ROWS) {
-        const int q = w / num_n;
-        const int e = d.tile_tab[PAIR ? d.pair_tab[q] : q];
-        const int u0 = PAIR ? d.pair_off[e] : d.poff[e] / XBM;
-        const int nu = (PAIR ? d.pair_off[e + 1] : d.poff[e + 1] / XBM) - u0;
+        int u0 = 0, nu = num_m;
+        if (d.dense_rows == 0) {
+            const int q = w / num_n;
+            const int e = d.tile_tab[PAIR ? d.pair_tab[q] : q];
+            u0 = PAIR ? d.pair_off[e] : d.poff[e] / XBM;
+            nu = (PAIR ? d.pair_off[e + 1] : d.poff[e + 1] / XBM) - u0;
+        }
         w -= u0 * num_n;
         const int group = w / (nu * kXGroupN);
         const int r = w - group * nu * kXGroupN;
         const int gsz = min(kXGroupN, num_n - group * kXGroupN);
         const int mu = u0 + r / gsz;
         t.n = group * kXGroupN + r % gsz;
-        const int first = PAIR ? d.pair_tab[mu] : mu;
-        t.m = first + rank;
-        t.e = d.tile_tab[first];
+        if (d.dense_rows > 0) {
+            // a pair's second tile may lie past the rows ("ghost"): not stored
+            t.m = PAIR ? 2 * mu + rank : mu;
+            t.e = 0;
+            t.valid_end = t.alloc_end = d.dense_rows;
+        } else {
+            const int first = PAIR ? d.pair_tab[mu] : mu;
+            t.m = first + rank;
+            t.e = d.tile_tab[first];
+            t.valid_end = d.poff[t.e] + d.counts[t.e];
+            t.alloc_end = d.poff[t.e + 1];
+        }
         t.row0 = t.m * XBM;
-        t.valid_end = d.poff[t.e] + d.counts[t.e];
-        t.alloc_end = d.poff[t.e + 1];
         t.kblocks = ((DUAL == DUAL_K) ? 2 * d.K : d.K) / XBK;
         t.kb0 = 0;
     } else {
@@ -240,9 +255,15 @@ __device__ __forceinline__ XTile xdecode(const GemmDesc& d, int w, int num_m, in
             t.n = r / num_m;
         }
         t.m = PAIR ? 2 * mu + rank : mu;
-        t.row0 = d.poff[t.e];
-        t.kb0 = t.row0 / XBK;
-        t.kblocks = (d.poff[t.e + 1] - t.row0) / XBK;
+        if (d.dense_rows > 0) {   // K = the dense rows, padded to the operands' rows_cap
+            t.row0 = 0;
+            t.kb0 = 0;
+            t.kblocks = (d.dense_rows + XBK - 1) / XBK;
+        } else {
+            t.row0 = d.poff[t.e];
+            t.kb0 = t.row0 / XBK;
+            t.kblocks = (d.poff[t.e + 1] - t.row0) / XBK;
+        }
         t.valid_end = t.alloc_end = 0;
     }
     return t;
@@ -863,7 +884,8 @@ cudaError_t xrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s
             ok &= mapx(&mB0, d.B0, d.b_rows, d.K, d.ldb, BKROWS);
             ok &= mapx(&mB1, d.B1 ? d.B1 : d.B0, d.b_rows, d.K, d.ldb, BKROWS);
         }
-        units = (long long)(PAIR ? (max_m_tiles + 1) / 2 : max_m_tiles) * num_n;
+        const long long m_tiles = d.dense_rows > 0 ? (d.dense_rows + XBM - 1) / XBM : max_m_tiles;
+        units = (PAIR ? (m_tiles + 1) / 2 : m_tiles) * num_n;
     } else {
         // A: [M_out][rows_cap], B: [N][rows_cap] (transposed operands)
         const long long KB = d.rows_cap / XBK;
@@ -880,9 +902,11 @@ cudaError_t xrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s
         ok &= map_out(&mO1, (DUAL == DUAL_N) ? d.O1 : d.O0, (long long)d.E * d.M_out, d.N, d.ldo);
     }
     if (SCHED == SCHED_ROWS) {
-        ok &= map_out(&mO0, d.O0, d.a_rows, d.N, d.ldo);
-        ok &= map_out(&mO1, EPI != EPI_STORE ? d.O1 : nullptr, d.a_rows, d.N, d.ldo);
-        ok &= map_out(&mO2, EPI == EPI_SWIGLU_FWD ? d.O2 : nullptr, d.a_rows, d.N, d.ldo);
+        // a dense group's outputs hold its rows alone (the operand codes are padded)
+        const long long orows = d.dense_rows > 0 ? d.dense_rows : d.a_rows;
+        ok &= map_out(&mO0, d.O0, orows, d.N, d.ldo);
+        ok &= map_out(&mO1, EPI != EPI_STORE ? d.O1 : nullptr, orows, d.N, d.ldo);
+        ok &= map_out(&mO2, EPI == EPI_SWIGLU_FWD ? d.O2 : nullptr, orows, d.N, d.ldo);
     } else {
         mO2 = mO0;
     }
@@ -920,7 +944,9 @@ cudaError_t xrun(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s
 template <int EPI, int SCHED, int DUAL, bool B_MN>
 cudaError_t xrun_any(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s)
 {
-    const bool pair = (SCHED == SCHED_WGRAD) ? d.M_out % (2 * XBM) == 0 : (d.pair_tab != nullptr && d.prefer_pair);
+    const bool pair = (SCHED == SCHED_WGRAD) ? d.M_out % (2 * XBM) == 0
+                      : d.dense_rows > 0 ? d.dense_rows > XBM
+                                         : (d.pair_tab != nullptr && d.prefer_pair);
     if (pair) return xrun<EPI, SCHED, DUAL, B_MN, true>(d, max_m_tiles, num_sms, s);
     return xrun<EPI, SCHED, DUAL, B_MN, false>(d, max_m_tiles, num_sms, s);
 }

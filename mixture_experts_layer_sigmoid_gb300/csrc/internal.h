@@ -222,6 +222,7 @@ struct MxQuantJob {
     int grp = 0;
     const int* gather_slot = nullptr;
     int gather_k = 1;
+    int rows_valid = 0;   // > 0: rows from here on (up to rows_max) read as zeros
 };
 cudaError_t launch_mx_quant(const MxQuantJob& j, cudaStream_t s);
 cudaError_t launch_gemm_mx(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s);

@@ -100,13 +100,15 @@ mx_permute_kernel(const __nv_bfloat16* __restrict__ x, const int* __restrict__ r
 //           MN-major with K = grp); atoms of operand row e C + c:
 //           sfc[((e C + c0) / 128 * grp/128 + kb) * 512].
 // With a gather map, row r of the input is token gslot[r] / gk of `in`
-// (zeros where gslot[r] < 0). Rows beyond *rows_dev (or rows_fixed) are
-// not visited.
+// (zeros where gslot[r] < 0); with rows_valid > 0, rows from rows_valid on
+// read as zeros (a dense group of rows padded to a multiple of 128). Rows
+// beyond *rows_dev (or rows_fixed) are not visited.
 template <bool ROWQ, int COLQ>
 __global__ void __launch_bounds__(256)
 mx_tiles_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__ rows_dev, int rows_fixed,
                 int C, int rows_cap, int grp, uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                uint8_t* __restrict__ qc, uint8_t* __restrict__ sfc, const int* __restrict__ gslot, int gk)
+                uint8_t* __restrict__ qc, uint8_t* __restrict__ sfc, const int* __restrict__ gslot, int gk,
+                int rows_valid)
 {
     __shared__ __align__(16) __nv_bfloat16 tile[128][136];
     const int rows = rows_dev ? *rows_dev : rows_fixed;
@@ -125,6 +127,8 @@ mx_tiles_kernel(const __nv_bfloat16* __restrict__ in, const int* __restrict__ ro
                 const int sl = gslot[r0 + rr];
                 u = sl >= 0 ? *reinterpret_cast<const uint4*>(in + (size_t)(sl / gk) * C + c0 + ch * 8)
                             : make_uint4(0, 0, 0, 0);
+            } else if (rows_valid > 0 && r0 + rr >= rows_valid) {
+                u = make_uint4(0, 0, 0, 0);   // padding rows of a dense group
             } else {
                 u = *reinterpret_cast<const uint4*>(in + (size_t)(r0 + rr) * C + c0 + ch * 8);
             }
@@ -216,7 +220,7 @@ cudaError_t run_mx(const MxQuantJob& j, cudaStream_t st)
     const long long grid = tiles < cap ? tiles : cap;
     mx_tiles_kernel<ROWQ, COLQ><<<(unsigned)grid, 256, 0, st>>>(j.in, j.rows_dev, j.rows_max, j.C, j.rows_cap,
                                                               j.grp, j.q, j.sf, j.qc, j.sfc, j.gather_slot,
-                                                              j.gather_k);
+                                                              j.gather_k, j.rows_valid);
     count_launches();
     return cudaGetLastError();
 }

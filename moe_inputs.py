@@ -170,6 +170,10 @@ WORKLOADS: Dict[str, Workload] = {
     # the same shape in the MXFP8 recipe (1x32 blocks, power-of-two scales)
     "qwen3_235b_mxfp8": Workload("qwen3_235b_mxfp8", T=16384, H=4096, E=128, k=8, F=1536,
                                  dtype=MXFP8, bias="zipf", seed=4000),
+    # the DeepSeek-V3 shape (with its shared expert) in the MXFP8 recipe, on
+    # the bf16 workload's inputs
+    "deepseek_v3_mxfp8": Workload("deepseek_v3_mxfp8", T=8192, H=7168, E=256, k=8, F=2048, Fs=2048,
+                                  score=SIGMOID, dtype=MXFP8, bias="normal", seed=2000),
 }
 
 

@@ -78,11 +78,18 @@ def _has_sm103():
         return False
 
 
-@pytest.mark.parametrize("dtype", [2, 3])
-def test_fp8_with_shared_expert_is_reported_unsupported(lib, dtype):
+def test_blockwise_fp8_with_shared_expert_is_reported_unsupported(lib):
     plan = ctypes.c_void_p()
-    assert lib.moe_plan_create(ctypes.byref(_cfg(dtype=dtype, Fs=256)), 0,
+    assert lib.moe_plan_create(ctypes.byref(_cfg(dtype=2, Fs=256)), 0,
                                ctypes.byref(plan)) == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_mxfp8_with_shared_expert_passes_validation(lib):
+    plan = ctypes.c_void_p()
+    st = lib.moe_plan_create(ctypes.byref(_cfg(dtype=3, Fs=256)), 0, ctypes.byref(plan))
+    assert st in (moe.MOE_OK, moe.MOE_ERR_CUDA) or (st == moe.MOE_ERR_UNSUPPORTED and not _has_sm103())
+    if st == moe.MOE_OK:
+        assert lib.moe_plan_destroy(plan) == moe.MOE_OK
 
 
 def test_null_arguments(lib):

@@ -119,9 +119,10 @@ def fp8_layer_parity(w, fold=False, capacity_factor=0.0):
     mx = w.dtype == mi.MXFP8
     layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score,
                          dtype=moe.MOE_MXFP8 if mx else moe.MOE_FP8_BLOCK, fold_gates=fold,
-                         capacity_factor=capacity_factor)
-    y, rt = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"], routing=True)
-    gr = layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
+                         capacity_factor=capacity_factor, Fs=w.Fs)
+    ws = (g["Wsg"], g["Wsu"], g["Wsd"])
+    y, rt = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"], *ws, routing=True)
+    gr = layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], *ws)
     torch.cuda.synchronize()
     assert layer.status(w.T) == 0
     d = {k: to_np(v) for k, v in inp.items()}
@@ -138,7 +139,8 @@ def fp8_layer_parity(w, fold=False, capacity_factor=0.0):
         keep = oracle.capacity_keep(r["topk"], w.E, C)
         assert (keep == 0).any(), "case drops nothing"
     ref = oracle.layer_fp8(d["x"], d["Wr"], d["Wg"], d["Wu"], d["Wd"], r["topk"], r["gates"],
-                           r["scores"], w.score, d["dY"], fold=fold,
+                           r["scores"], w.score, d["dY"], Wsg=d.get("Wsg"), Wsu=d.get("Wsu"),
+                           Wsd=d.get("Wsd"), fold=fold,
                            recipe=oracle.RECIPE_MX if mx else oracle.RECIPE_BLOCK, keep=keep)
     rep = {}
     for gname, oname in (("y", "y"), ("dX", "dX")):
@@ -146,7 +148,8 @@ def fp8_layer_parity(w, fold=False, capacity_factor=0.0):
         rl2, mr = rel_errors(got, ref[oname])
         rep[gname] = (rl2, mr)
         assert rl2 <= 4e-2 and mr <= 1.5e-1, (gname, rl2, mr)
-    for gname, oname in (("dWr", "dWr"), ("dW_gate", "dWg"), ("dW_up", "dWu"), ("dW_down", "dWd")):
+    shared = (("dWs_gate", "dWsg"), ("dWs_up", "dWsu"), ("dWs_down", "dWsd")) if w.Fs else ()
+    for gname, oname in (("dWr", "dWr"), ("dW_gate", "dWg"), ("dW_up", "dWu"), ("dW_down", "dWd")) + shared:
         got = to_np(gr[gname])
         want = ref[oname]
         rl2, mr = rel_errors(got, want)

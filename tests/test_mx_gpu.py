@@ -77,6 +77,13 @@ MX_CASES = {
                                          F=384),
     "mx_sigmoid_e64": mi.scaled(mi.WORKLOADS["deepseek_v3"], T=300, H=256, E=64, k=6, F=128, Fs=0,
                                 dtype=mi.MXFP8),
+    # DeepSeek-shaped with the shared expert: a dense group of T = 300 rows
+    # (codes padded to 384; CTA pairs with a ghost half; Fs != F)
+    "mx_deepseek_shared": mi.scaled(mi.WORKLOADS["deepseek_v3"], T=300, H=256, E=16, k=4, F=256,
+                                    Fs=384, dtype=mi.MXFP8),
+    # one dense tile of 100 rows (single CTAs)
+    "mx_shared_one_tile": mi.scaled(mi.WORKLOADS["deepseek_v3"], T=100, H=256, E=8, k=2, F=128,
+                                    Fs=256, dtype=mi.MXFP8),
 }
 
 
@@ -85,9 +92,13 @@ def test_mx_layer_matches_oracle(name):
     print(name, fp8_layer_parity(MX_CASES[name], False))
 
 
-@pytest.mark.parametrize("name", ["mx_small", "mx_many_rows_per_expert"])
+@pytest.mark.parametrize("name", ["mx_small", "mx_many_rows_per_expert", "mx_deepseek_shared"])
 def test_mx_folded_gates_match_oracle(name):
     print(name, "folded", fp8_layer_parity(MX_CASES[name], True))
+
+
+def test_mx_shared_expert_with_capacity_dropping_matches_oracle():
+    print("mx_deepseek_shared capacity", fp8_layer_parity(MX_CASES["mx_deepseek_shared"], False, 1.0))
 
 
 def test_mx_layer_is_deterministic_and_graph_capturable():
