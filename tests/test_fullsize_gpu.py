@@ -153,9 +153,10 @@ def _full_size_fp8_case(wl, dtype, recipe, check_weight_quantiser):
     import mixture_experts_layer_sigmoid_gb300 as moe
     w = mi.WORKLOADS[wl]
     g = mi.make_inputs(w, "cuda")
-    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=dtype)
-    y, rt = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"], routing=True)
-    gr = layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"])
+    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=dtype, Fs=w.Fs)
+    ws = (g["Wsg"], g["Wsu"], g["Wsd"])
+    y, rt = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"], *ws, routing=True)
+    gr = layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], *ws)
     torch.cuda.synchronize()
     assert layer.status(w.T) == 0
     assert torch.isfinite(y).all() and torch.isfinite(gr["dX"]).all()
@@ -174,9 +175,10 @@ def _full_size_fp8_case(wl, dtype, recipe, check_weight_quantiser):
         check_weight_quantiser(g["Wg"][e].contiguous())
     # sampled rows against the oracle's FP8 layer run on those tokens alone:
     # y and dX of a token depend only on its own row (row blocks of its
-    # activations and gradients, weight blocks of its experts), and dz only on
-    # its selected experts' scores, so the layer restricted to the sampled
-    # tokens and the experts they select (renumbered) gives their rows exactly
+    # activations and gradients, weight blocks of its experts and of the
+    # shared expert), and dz only on its selected experts' scores, so the
+    # layer restricted to the sampled tokens and the experts they select
+    # (renumbered) gives their rows exactly
     toks = np.array(sorted({0, w.T - 1, int(np.nonzero((r["topk"] == hot).any(1))[0][0])}))
     need = sorted(set(r["topk"][toks].ravel().tolist()))
     renum = np.full(w.E, -1, np.int32)
@@ -185,7 +187,7 @@ def _full_size_fp8_case(wl, dtype, recipe, check_weight_quantiser):
     stack = lambda n: np.stack([to_np(g[n][e]) for e in need])
     q = oracle.layer_fp8(x[toks], Wr[:, need], stack("Wg"), stack("Wu"), stack("Wd"), topk_s,
                          r["gates"][toks], r["scores"][toks][:, need], w.score, dY[toks],
-                         recipe=recipe)
+                         Wsg=to_np(g["Wsg"]), Wsu=to_np(g["Wsu"]), Wsd=to_np(g["Wsd"]), recipe=recipe)
     report = {}
     for nm, got in (("y", to_np(y)[toks]), ("dX", to_np(gr["dX"])[toks])):
         rl2, mr = rel_errors(got, q[nm])
@@ -231,3 +233,18 @@ def test_full_size_mxfp8_layer():
         assert np.array_equal(qc, oc_c.T) and np.array_equal(_atoms_to_scales(sc, C, R), os_c.T)
 
     _full_size_fp8_case("qwen3_235b_mxfp8", moe.MOE_MXFP8, oracle.RECIPE_MX, check)
+
+
+def test_full_size_deepseek_mxfp8_layer():
+    """The DeepSeek-V3 shape in MXFP8, with its shared expert (a dense group
+    of the 8192 token rows through the same engine)."""
+    import mixture_experts_layer_sigmoid_gb300 as moe
+    from test_mx_gpu import _atoms_to_scales, _mxq
+
+    def check(W):
+        R, C = W.shape
+        q, sq, _, _ = _mxq(W, rows=True, cols=None)
+        oc_r, os_r = oracle.mx_quantize(W.float().cpu().numpy(), oracle.MX_ROWS)
+        assert np.array_equal(q, oc_r) and np.array_equal(_atoms_to_scales(sq, R, C), os_r)
+
+    _full_size_fp8_case("deepseek_v3_mxfp8", moe.MOE_MXFP8, oracle.RECIPE_MX, check)
