@@ -353,14 +353,62 @@ def mx_quantize(X, mode):
     return codes, scales
 
 
-RECIPE_BLOCK, RECIPE_MX = 0, 1
+NV_ROWS, NV_COLS = 0, 1
+
+
+def e2m1_decode(codes):
+    """fp64 values of 4-bit E2M1 codes (format definition)."""
+    lib = _load()
+    lib.oracle_e2m1_decode.restype = ctypes.c_double
+    lib.oracle_e2m1_decode.argtypes = [ctypes.c_ubyte]
+    return np.array([lib.oracle_e2m1_decode(int(c)) for c in np.asarray(codes).ravel()]).reshape(np.shape(codes))
+
+
+def e2m1_encode(values):
+    """E2M1 codes of fp32 values (nearest, ties to the even code, saturating)."""
+    lib = _load()
+    lib.oracle_e2m1_encode.restype = ctypes.c_ubyte
+    lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+    v = np.asarray(values, np.float32)
+    return np.array([lib.oracle_e2m1_encode(float(f)) for f in v.ravel()], np.uint8).reshape(v.shape)
+
+
+def nv_tensor_scale(amax):
+    """NVFP4 per-tensor fp32 scale S = 2688 / amax (1 for an all-zero tensor)."""
+    lib = _load()
+    lib.oracle_nv_tensor_scale.restype = ctypes.c_float
+    lib.oracle_nv_tensor_scale.argtypes = [ctypes.c_float]
+    return np.float32(lib.oracle_nv_tensor_scale(float(amax)))
+
+
+def nv_quantize(X, mode):
+    """(codes, E4M3 scale bytes, tensor scale S) of an fp32 matrix as one
+    NVFP4 tensor: mode NV_ROWS (1x16 along rows, scales M x K/16) or NV_COLS
+    (per column over 16-row blocks, scales ceil(M/16) x K). Codes are one
+    4-bit code per byte."""
+    lib = _load()
+    X = np.ascontiguousarray(X, np.float32)
+    M, K = X.shape
+    codes = np.empty((M, K), np.uint8)
+    scales = np.empty((M, K // 16) if mode == NV_ROWS else ((M + 15) // 16, K), np.uint8)
+    S = ctypes.c_float(0.0)
+    rc = lib.oracle_nv_quantize(M, K, mode, X.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                codes.ctypes.data_as(ctypes.c_void_p), scales.ctypes.data_as(ctypes.c_void_p),
+                                ctypes.byref(S))
+    if rc:
+        raise ValueError("oracle_nv_quantize: bad arguments")
+    return codes, scales, np.float32(S.value)
+
+
+RECIPE_BLOCK, RECIPE_MX, RECIPE_NV = 0, 1, 2
 
 
 def layer_fp8(x, Wr, Wg, Wu, Wd, topk, gates, scores, score, dY=None, Wsg=None, Wsu=None,
               Wsd=None, fold=False, recipe=RECIPE_BLOCK, keep=None):
     """FP8 layer: y, and when dY is given every gradient. recipe: RECIPE_BLOCK
-    (blockwise FP8, fp32 block scales) or RECIPE_MX (MXFP8, 1x32 blocks with
-    power-of-two scales). fold: the memory-efficient permutation's order
+    (blockwise FP8, fp32 block scales), RECIPE_MX (MXFP8, 1x32 blocks with
+    power-of-two scales) or RECIPE_NV (NVFP4: E2M1 values, 1x16 blocks with
+    E4M3 scales, one fp32 scale per expert operand). fold: the memory-efficient permutation's order
     (routing weight folded into h before fc2), with its rounding points.
     keep: optional T x k mask of the slots that are not dropped
     (capacity_keep); a dropped assignment never reaches its expert, so the

@@ -874,6 +874,137 @@ int oracle_mx_quantize(int M, int K, int mode, const float* X, unsigned char* co
     return 0;
 }
 
+/* ---------------------------------------------------------------- NVFP4 */
+/*
+ * NVFP4 ("Scalable Training of Mixture-of-Experts Models with Megatron
+ * Core", §5 Platform-specific recipes: the framework also provides NVFP4 for
+ * Blackwell; §5 Kernel and shape optimization: grouped quantisation ahead
+ * of the grouped NVFP4 GEMMs). The pages give none of the recipe's
+ * parameters; the reading here is the NVFP4 format itself, applied like the
+ * MXFP8 recipe (1-D blocks along each GEMM's contraction dimension):
+ *   - values E2M1: 1 sign, 2 exponent, 1 mantissa bit, magnitudes
+ *     {0, 0.5, 1, 1.5, 2, 3, 4, 6}; encoding rounds to nearest, ties to the
+ *     even code (mantissa bit 0), and saturates to +-6; a negative value that
+ *     rounds to zero keeps its sign bit;
+ *   - blocks of 16 consecutive values along K, each with an unsigned E4M3
+ *     scale, plus one fp32 scale S per tensor, S = 2688 / amax (2688 =
+ *     448 * 6: the tensor's largest block gets the largest E4M3 scale), S = 1
+ *     for an all-zero tensor;
+ *   - per block, in fp32 (each operation rounded to nearest even):
+ *     a = max |v|, sb = E4M3(a * S / 6) (the product first),
+ *     s = the value of sb, r = S / s, and each value is stored as
+ *     E2M1(v * r) (all codes 0 when s = 0); it is read as q * s / S;
+ *   - a "tensor" is one expert's operand of one grouped GEMM (grouped
+ *     quantisation quantises each expert's part on its own), with the gate
+ *     and up projections one tensor [Wg | Wu] and their gradients one tensor
+ *     [dA | dU], as in a fused fc1 whose output is [a | u].
+ */
+double oracle_e2m1_decode(unsigned char c)
+{
+    static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    double v = mag[c & 7];
+    return (c & 8) ? -v : v;
+}
+
+/* E2M1 code (4 bits) of an fp32 value: nearest magnitude, ties to the even
+ * code, saturating at 6. */
+unsigned char oracle_e2m1_encode(float f)
+{
+    double m = fabs((double)f);
+    unsigned char c;
+    if (m <= 0.25) c = 0;
+    else if (m < 0.75) c = 1;
+    else if (m <= 1.25) c = 2;
+    else if (m < 1.75) c = 3;
+    else if (m <= 2.5) c = 4;
+    else if (m < 3.5) c = 5;
+    else if (m <= 5.0) c = 6;
+    else c = 7;
+    return (unsigned char)(c | (f < 0.0f ? 8 : 0));
+}
+
+/* per-tensor scale of a tensor whose largest magnitude is amax */
+float oracle_nv_tensor_scale(float amax) { return amax > 0.0f ? 2688.0f / amax : 1.0f; }
+
+/* Quantise-dequantise n values v[i*stride] as one NVFP4 block of a tensor
+ * with scale S; optionally the codes (one per byte) and the E4M3 scale byte. */
+static void nv_block(double* v, int n, long stride, float S, unsigned char* codes, unsigned char* sc)
+{
+    float a = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float f = fabsf((float)v[(long)i * stride]);
+        if (f > a) a = f;
+    }
+    float t = a * S;
+    float sf = t / 6.0f;
+    unsigned char sb = oracle_e4m3_encode(sf);
+    float s = (float)oracle_e4m3_decode(sb);
+    float r = s > 0.0f ? S / s : 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float x = (float)v[(long)i * stride];
+        unsigned char c = s > 0.0f ? oracle_e2m1_encode(x * r) : (unsigned char)0;
+        if (codes) codes[(long)i * stride] = c;
+        v[(long)i * stride] = oracle_e2m1_decode(c) * (double)s / (double)S;
+    }
+    if (sc) *sc = sb;
+}
+
+static float amax_of(const double* X, size_t n)
+{
+    float a = 0.0f;
+    for (size_t i = 0; i < n; ++i) {
+        float f = fabsf((float)X[i]);
+        if (f > a) a = f;
+    }
+    return a;
+}
+
+/* 1x16 blocks along the rows of an M x K matrix (K a multiple of 16), or
+ * (by_row 0) per column over 16-row blocks (the last block may be short),
+ * with the tensor scale of amax. */
+static void nv_qdq(int by_row, int M, int K, double* X, float amax)
+{
+    const float S = oracle_nv_tensor_scale(amax);
+    if (by_row) {
+        for (int m = 0; m < M; ++m)
+            for (int k0 = 0; k0 < K; k0 += 16) nv_block(X + (long)m * K + k0, 16, 1, S, NULL, NULL);
+    } else {
+        for (int n = 0; n < K; ++n)
+            for (int m0 = 0; m0 < M; m0 += 16) {
+                int len = M - m0 < 16 ? M - m0 : 16;
+                nv_block(X + (long)m0 * K + n, len, K, S, NULL, NULL);
+            }
+    }
+}
+
+/* NVFP4 codes (one per byte, low 4 bits) and E4M3 scale bytes of one fp32
+ * matrix as a single tensor, for comparison with a GPU quantiser. mode 0:
+ * 1x16 along rows (scales M x K/16); mode 1: per column over 16-row blocks
+ * (scales ceil(M/16) x K). *S_out receives the tensor scale. */
+int oracle_nv_quantize(int M, int K, int mode, const float* X, unsigned char* codes, unsigned char* scales,
+                       float* S_out)
+{
+    if (M <= 0 || K <= 0 || mode < 0 || mode > 1) return -1;
+    if (mode == 0 && K % 16) return -1;
+    double* v = (double*)malloc(sizeof(double) * (size_t)M * K);
+    for (size_t i = 0; i < (size_t)M * K; ++i) v[i] = X[i];
+    const float S = oracle_nv_tensor_scale(amax_of(v, (size_t)M * K));
+    if (mode == 0) {
+        for (int m = 0; m < M; ++m)
+            for (int k0 = 0; k0 < K; k0 += 16)
+                nv_block(v + (long)m * K + k0, 16, 1, S, codes + (long)m * K + k0, scales + (long)m * (K / 16) + k0 / 16);
+    } else {
+        for (int n = 0; n < K; ++n)
+            for (int m0 = 0; m0 < M; m0 += 16) {
+                int len = M - m0 < 16 ? M - m0 : 16;
+                nv_block(v + (long)m0 * K + n, len, K, S, codes + (long)m0 * K + n, scales + (long)(m0 / 16) * K + n);
+            }
+    }
+    if (S_out) *S_out = S;
+    free(v);
+    return 0;
+}
+
 static double* dup(const double* p, size_t n)
 {
     double* q = (double*)malloc(sizeof(double) * (n ? n : 1));
@@ -938,25 +1069,33 @@ static void gemm_nt(int M, int N, int K, const double* A, const double* B, doubl
  * indexing output rows, 128x128 for the other). recipe 1: MXFP8 (1x32 blocks
  * along K for both operands of every GEMM, so each weight is quantised once
  * per orientation: along H for fc1 and along F for fc1's data gradient; Wd
- * along F for fc2 and along H for fc2's data gradient).
+ * along F for fc2 and along H for fc2's data gradient). recipe 2: NVFP4
+ * (1x16 blocks along K like MXFP8, E4M3 block scales under one fp32 scale
+ * per tensor: per expert operand, [Wg | Wu] and [dA | dU] one tensor each).
  */
 #define RECIPE_BLOCK 0
 #define RECIPE_MX 1
+#define RECIPE_NV 2
 
 /* the quantisation of X (rows x cols) whose contraction dimension runs along
- * its rows (by_row 1: blocks within a row) or its columns (by_row 0) */
-static void q_act(int recipe, int by_row, int rows, int cols, double* X)
+ * its rows (by_row 1: blocks within a row) or its columns (by_row 0); amax:
+ * the largest magnitude of the NVFP4 tensor X belongs to (recipe 2) */
+static void q_act(int recipe, int by_row, int rows, int cols, double* X, float amax)
 {
-    if (recipe == RECIPE_MX) {
+    if (recipe == RECIPE_NV) {
+        nv_qdq(by_row, rows, cols, X, amax);
+    } else if (recipe == RECIPE_MX) {
         if (by_row) mx_rows(rows, cols, X); else mx_cols(rows, cols, X);
     } else {
         if (by_row) qdq_rows(rows, cols, X); else qdq_cols(rows, cols, X);
     }
 }
-/* the second operand of a GEMM (128x128 blocks, or MX blocks along K) */
-static void q_other(int recipe, int by_row, int rows, int cols, double* X)
+/* the second operand of a GEMM (128x128 blocks, or MX / NVFP4 blocks along K) */
+static void q_other(int recipe, int by_row, int rows, int cols, double* X, float amax)
 {
-    if (recipe == RECIPE_MX) {
+    if (recipe == RECIPE_NV) {
+        nv_qdq(by_row, rows, cols, X, amax);
+    } else if (recipe == RECIPE_MX) {
         if (by_row) mx_rows(rows, cols, X); else mx_cols(rows, cols, X);
     } else {
         qdq_tiles(rows, cols, X);
@@ -968,26 +1107,31 @@ static void swiglu_fp8(int M, int H, int F, const double* X, const double* Wg, c
                        double* dWu, double* dWd, const double* g, double* dg, int recipe)
 {
     size_t mf = (size_t)(M > 0 ? M : 1) * F, mh = (size_t)(M > 0 ? M : 1) * H;
+    /* NVFP4 tensor maxima: x, [Wg | Wu], Wd (h, dY, [dA | dU] below) */
+    const float aX = amax_of(X, (size_t)M * H);
+    const float aWgu = fmaxf(amax_of(Wg, (size_t)H * F), amax_of(Wu, (size_t)H * F));
+    const float aWd = amax_of(Wd, (size_t)F * H);
     double* Xq = dup(X, (size_t)M * H);
-    q_act(recipe, 1, M, H, Xq);                       /* fc1 A: K = H along rows */
+    q_act(recipe, 1, M, H, Xq, aX);                   /* fc1 A: K = H along rows */
     /* fc1 B: Wg, Wu (H x F) with K = H along their columns; fc2 B: Wd (F x H)
      * with K = F along its columns */
     double* Wgq = dup(Wg, (size_t)H * F);
     double* Wuq = dup(Wu, (size_t)H * F);
     double* Wdq = dup(Wd, (size_t)F * H);
-    q_other(recipe, 0, H, F, Wgq);
-    q_other(recipe, 0, H, F, Wuq);
-    q_other(recipe, 0, F, H, Wdq);
+    q_other(recipe, 0, H, F, Wgq, aWgu);
+    q_other(recipe, 0, H, F, Wuq, aWgu);
+    q_other(recipe, 0, F, H, Wdq, aWd);
     /* the data gradients contract the weights along their other dimension:
-     * the same codes in the blockwise recipe, a second quantisation in MX */
+     * the same codes in the blockwise recipe, a second quantisation in MX
+     * and NVFP4 (the same tensor scale in NVFP4) */
     double *Wgb = Wgq, *Wub = Wuq, *Wdb = Wdq;
-    if (recipe == RECIPE_MX && dYr) {
+    if (recipe != RECIPE_BLOCK && dYr) {
         Wgb = dup(Wg, (size_t)H * F);
         Wub = dup(Wu, (size_t)H * F);
         Wdb = dup(Wd, (size_t)F * H);
-        mx_rows(H, F, Wgb);
-        mx_rows(H, F, Wub);
-        mx_rows(F, H, Wdb);
+        q_other(recipe, 1, H, F, Wgb, aWgu);
+        q_other(recipe, 1, H, F, Wub, aWgu);
+        q_other(recipe, 1, F, H, Wdb, aWd);
     }
     double* A = (double*)malloc(sizeof(double) * mf);
     double* U = (double*)malloc(sizeof(double) * mf);
@@ -1001,14 +1145,15 @@ static void swiglu_fp8(int M, int H, int F, const double* X, const double* Wg, c
         U[i] = bf16r(U[i]);
     }
     double* Hq = dup(Hh, (size_t)M * F);
-    q_act(recipe, 1, M, F, Hq);                       /* fc2 A: K = F */
+    q_act(recipe, 1, M, F, Hq, amax_of(Hh, (size_t)M * F));   /* fc2 A: K = F */
     gemm(M, H, F, Hq, Wdq, Y);
     for (size_t i = 0; i < (size_t)M * H; ++i) Y[i] = bf16r(Y[i]);
     free(Hq);
     if (dYr) {
         /* fc2 dgrad: dh = q(dYr) q(Wd)^T, K = H */
+        const float aDY = amax_of(dYr, (size_t)M * H);
         double* dYq = dup(dYr, (size_t)M * H);
-        q_act(recipe, 1, M, H, dYq);
+        q_act(recipe, 1, M, H, dYq, aDY);
         double* dh = (double*)malloc(sizeof(double) * mf);
         gemm_nt(M, F, H, dYq, Wdb, dh);
         double* dA = (double*)malloc(sizeof(double) * mf);
@@ -1033,26 +1178,27 @@ static void swiglu_fp8(int M, int H, int F, const double* X, const double* Wg, c
         /* fc2 wgrad: dWd = q(h)^T q(dYr), K = the expert's rows (blocks along
          * the rows, counted from the segment's first row) */
         double* Hc = dup(Hh, (size_t)M * F);
-        q_act(recipe, 0, M, F, Hc);
+        q_act(recipe, 0, M, F, Hc, amax_of(Hh, (size_t)M * F));
         double* dYt = dup(dYr, (size_t)M * H);
-        q_other(recipe, 0, M, H, dYt);
+        q_other(recipe, 0, M, H, dYt, aDY);
         gemm_tn(F, H, M, Hc, dYt, dWd);
         /* fc1 dgrad: dX = q(dA) q(Wg)^T + q(dU) q(Wu)^T, K = F */
+        const float aDAU = fmaxf(amax_of(dA, (size_t)M * F), amax_of(dU, (size_t)M * F));
         double* dAq = dup(dA, mf);
         double* dUq = dup(dU, mf);
-        q_act(recipe, 1, M, F, dAq);
-        q_act(recipe, 1, M, F, dUq);
+        q_act(recipe, 1, M, F, dAq, aDAU);
+        q_act(recipe, 1, M, F, dUq, aDAU);
         double* t1 = (double*)malloc(sizeof(double) * mh);
         gemm_nt(M, H, F, dAq, Wgb, dX);
         gemm_nt(M, H, F, dUq, Wub, t1);
         for (size_t i = 0; i < (size_t)M * H; ++i) dX[i] += t1[i];
         /* fc1 wgrad: dWg = q(X)^T q(dA), dWu = q(X)^T q(dU), K = rows */
         double* Xc = dup(X, (size_t)M * H);
-        q_act(recipe, 0, M, H, Xc);
+        q_act(recipe, 0, M, H, Xc, aX);
         double* dAt = dup(dA, mf);
         double* dUt = dup(dU, mf);
-        q_other(recipe, 0, M, F, dAt);
-        q_other(recipe, 0, M, F, dUt);
+        q_other(recipe, 0, M, F, dAt, aDAU);
+        q_other(recipe, 0, M, F, dUt, aDAU);
         gemm_tn(H, F, M, Xc, dAt, dWg);
         gemm_tn(H, F, M, Xc, dUt, dWu);
         free(dYq); free(dh); free(dA); free(dU); free(Hc); free(dYt); free(dAq); free(dUq);
@@ -1078,7 +1224,7 @@ int oracle_layer_fp8(int T, int H, int E, int k, int F, int Fs, int score_fn,
                      int recipe, const unsigned char* keep)
 {
     if (T <= 0 || H <= 0 || H % 128 || E <= 0 || k <= 0 || k > E || k > 1024 || F <= 0 ||
-        F % 128 || Fs < 0 || Fs % 128 || recipe < 0 || recipe > 1)
+        F % 128 || Fs < 0 || Fs % 128 || recipe < 0 || recipe > 2)
         return -1;
     int* counts = (int*)malloc(sizeof(int) * E);
     int* offsets = (int*)malloc(sizeof(int) * (E + 1));
