@@ -884,8 +884,9 @@ int oracle_mx_quantize(int M, int K, int mode, const float* X, unsigned char* co
  * MXFP8 recipe (1-D blocks along each GEMM's contraction dimension):
  *   - values E2M1: 1 sign, 2 exponent, 1 mantissa bit, magnitudes
  *     {0, 0.5, 1, 1.5, 2, 3, 4, 6}; encoding rounds to nearest, ties to the
- *     even code (mantissa bit 0), and saturates to +-6; a negative value that
- *     rounds to zero keeps its sign bit;
+ *     even code (mantissa bit 0), and saturates to +-6; every value keeps
+ *     its sign bit, zero included (-0 and a negative value that rounds to
+ *     zero are the code 8, as a signed-zero format conversion gives);
  *   - blocks of 16 consecutive values along K, each with an unsigned E4M3
  *     scale, plus one fp32 scale S per tensor, S = 2688 / amax (2688 =
  *     448 * 6: the tensor's largest block gets the largest E4M3 scale), S = 1
@@ -907,7 +908,7 @@ double oracle_e2m1_decode(unsigned char c)
 }
 
 /* E2M1 code (4 bits) of an fp32 value: nearest magnitude, ties to the even
- * code, saturating at 6. */
+ * code, saturating at 6, with the value's sign bit. */
 unsigned char oracle_e2m1_encode(float f)
 {
     double m = fabs((double)f);
@@ -920,7 +921,7 @@ unsigned char oracle_e2m1_encode(float f)
     else if (m < 3.5) c = 5;
     else if (m <= 5.0) c = 6;
     else c = 7;
-    return (unsigned char)(c | (f < 0.0f ? 8 : 0));
+    return (unsigned char)(c | (signbit(f) ? 8 : 0));
 }
 
 /* per-tensor scale of a tensor whose largest magnitude is amax */

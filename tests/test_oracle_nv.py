@@ -36,12 +36,12 @@ _GRID = np.array([_e2m1_from_bits(c) for c in range(8)])
 
 def _e2m1_brute(f):
     """Nearest E2M1 code of an fp32 value (ties to the code whose mantissa bit
-    is 0), saturating at 6; a negative value keeps the sign bit."""
+    is 0), saturating at 6, with the value's sign bit (-0 included)."""
     m = min(abs(float(f)), 6.0)                        # saturation
     d = np.abs(_GRID - m)
     best = np.flatnonzero(d == d.min())
     c = int(best[0]) if len(best) == 1 else int([b for b in best if b % 2 == 0][0])
-    return c | (8 if f < 0 else 0)
+    return c | (8 if np.signbit(f) else 0)
 
 
 def test_e2m1_decode_is_the_format():
@@ -57,6 +57,7 @@ def test_e2m1_encode_is_nearest_ties_to_even():
     vals = np.concatenate([_GRID, mids, mids + 1e-6, mids - 1e-6, rng.uniform(-9, 9, 2000),
                            [6.0001, 7.0, 1e30, 1e-30, 0.0]]).astype(np.float32)
     vals = np.concatenate([vals, -vals])
+    assert np.signbit(vals[-1])                          # -0.0 is among them
     got = oracle.e2m1_encode(vals)
     want = np.array([_e2m1_brute(v) for v in vals], np.uint8)
     assert np.array_equal(got, want)
@@ -227,12 +228,13 @@ def test_nv_layer_matches_independent_nv_swiglu(fold, drop):
 
 @pytest.mark.parametrize("fold", [False, True])
 def test_nv_layer_tracks_the_exact_layer(fold):
-    """An E2M1 rounding perturbs a value by up to 1/6 of its block's largest
-    magnitude (half the grid step 2 at the top of the range, relative to 6),
-    and the E4M3 block scale adds up to 2^-4 relative; with the values spread
-    over the grid the rms perturbation is about 10%, and an output passes
-    through a few such roundings: within ~30% rms of the exact layer, well
-    apart from it, and apart from the MXFP8 layer."""
+    """An E2M1 rounding perturbs a value by up to a sixth of its block's
+    largest magnitude (half the grid step 2 at the top of the range, relative
+    to 6), and the E4M3 block scale adds up to 2^-4 relative; for Gaussian
+    blocks of 16 the rms perturbation is about 12-15% of a value, a GEMM of
+    two quantised operands ~0.2, and an output passes through up to three
+    such GEMMs: 0.2-0.3 rms from the exact layer on these inputs (within
+    0.4), well apart from it, and about 3.5x the MXFP8 layer's distance."""
     p = _layer(T=150, H=256, E=4, k=2, F=256, seed=5)
     r = oracle.route(p["x"], p["Wr"], None, 2, oracle.SOFTMAX)
     q = oracle.layer_fp8(p["x"], p["Wr"], p["Wg"], p["Wu"], p["Wd"], r["topk"], r["gates"],
@@ -248,5 +250,5 @@ def test_nv_layer_tracks_the_exact_layer(fold):
             continue
         rel = np.linalg.norm(q[n] - g[n]) / np.linalg.norm(g[n])
         rel_mx = np.linalg.norm(qm[n] - g[n]) / np.linalg.norm(g[n])
-        assert 0.03 < rel < 0.3, (n, rel)
+        assert 0.03 < rel < 0.4, (n, rel)
         assert rel > 2 * rel_mx, (n, rel, rel_mx)       # coarser than MXFP8
