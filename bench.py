@@ -55,15 +55,18 @@ def stage_bytes(name: str, w: mi.Workload) -> float:
     """Algorithmic DRAM bytes of one launch of a grouped-GEMM stage: each
     operand read once and each output written once (routed rows R = T k, no
     padding rows). Operands are E4M3 codes (1 byte, plus one fp32 scale per
-    128 elements) in the FP8 layer and bf16 otherwise; stored outputs are
-    bf16 (fp32 in the fp32 layer)."""
+    128 elements) in the blockwise FP8 layer, E4M3 codes plus one scale byte
+    per 32 in MXFP8, E2M1 codes (half a byte) plus one scale byte per 16 in
+    NVFP4, and bf16 otherwise; stored outputs are bf16 (fp32 in the fp32
+    layer)."""
     shared = name.startswith("shared_")
     base = name[len("shared_"):] if shared else name
     rows, E, F = (w.T, 1, w.Fs) if shared else (w.R, w.E, w.F)
     H = w.H
     o = 4 if w.dtype == mi.FP32 else 2
     a = 4 if w.dtype == mi.FP32 else (1 + 4 / 128 if w.dtype == mi.FP8_BLOCK else
-                                      1 + 1 / 32 if w.dtype == mi.MXFP8 else 2)
+                                      1 + 1 / 32 if w.dtype == mi.MXFP8 else
+                                      0.5 + 1 / 16 if w.dtype == mi.NVFP4 else 2)
     RH, RF, EHF = rows * H, rows * F, E * H * F
     return {"fc1_swiglu": a * (RH + 2 * EHF) + o * 3 * RF,
             "fc2": a * (RF + EHF) + o * RH,
@@ -83,11 +86,12 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def choose_peak(peaks, kind, clocks, fp8):
+def choose_peak(peaks, kind, clocks, fp8, fp4=False):
     """Tensor peak for this run's clocks: the burst cuBLAS figure unless the
     run's median SM clock is within 5% of the clock the sustained figure was
     measured at (a power-capped, seconds-long loop). FP8 takes twice the bf16
-    figure (nominal 4.5 vs 2.25 PFLOP/s dense). Returns (peak, description)."""
+    figure (nominal 4.5 vs 2.25 PFLOP/s dense), FP4 six times (nominal 13.5).
+    Returns (peak, description)."""
     burst = peaks["bf16_tflops"]
     sust = peaks.get("bf16_tflops_sustained", burst)
     sust_mhz = (peaks.get("clocks_under_load") or {}).get("sm_mhz_median")
@@ -99,7 +103,9 @@ def choose_peak(peaks, kind, clocks, fp8):
         peak, desc = burst, (f"bf16_tflops (burst) of {kind} peaks (this run's median SM clock "
                              f"{med if med is None else round(med)} MHz is above the "
                              f"{sust_mhz} MHz of the sustained measurement)")
-    if fp8:
+    if fp4:
+        peak, desc = 6.0 * peak, "6 x " + desc + " (nominal fp4/bf16 ratio)"
+    elif fp8:
         peak, desc = 2.0 * peak, "2 x " + desc + " (nominal fp8/bf16 ratio)"
     return peak, desc
 
@@ -272,7 +278,8 @@ def run_reference(args, w):
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
-    from mixture_experts_layer_sigmoid_gb300 import MoELayer, MOE_BF16, MOE_FP32, MOE_FP8_BLOCK, MOE_MXFP8
+    from mixture_experts_layer_sigmoid_gb300 import (MoELayer, MOE_BF16, MOE_FP32, MOE_FP8_BLOCK, MOE_MXFP8,
+                                                     MOE_NVFP4)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -286,7 +293,7 @@ def run_ours(args, w):
     inp = mi.make_inputs(w, dev)
     layer = MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score,
                      dtype={mi.FP32: MOE_FP32, mi.BF16: MOE_BF16, mi.FP8_BLOCK: MOE_FP8_BLOCK,
-                            mi.MXFP8: MOE_MXFP8}[w.dtype],
+                            mi.MXFP8: MOE_MXFP8, mi.NVFP4: MOE_NVFP4}[w.dtype],
                      Fs=w.Fs, device=local, stage_timing=True, fold_gates=args.fold_gates)
     x, dY = inp["x"], inp["dY"]
     W = (inp["Wr"], inp["Wg"], inp["Wu"], inp["Wd"], inp["Wsg"], inp["Wsu"], inp["Wsd"])
@@ -399,7 +406,8 @@ def run_ours(args, w):
     jm = job_metrics(world, ms, flops, w.T)
     value = jm["tflops"]
     peaks, peaks_kind = load_peaks()
-    peak_sust, peak_name = choose_peak(peaks, peaks_kind, clocks, w.dtype in (mi.FP8_BLOCK, mi.MXFP8))
+    peak_sust, peak_name = choose_peak(peaks, peaks_kind, clocks, w.dtype in (mi.FP8_BLOCK, mi.MXFP8),
+                                       w.dtype == mi.NVFP4)
 
     # ---- roofline of the dominant kernel (largest device time in the timed
     # region): the slower of its FLOPs at the tensor peak and its algorithmic
@@ -464,7 +472,8 @@ def run_ours(args, w):
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": {mi.BF16: "bf16", mi.FP32: "f32", mi.FP8_BLOCK: "e4m3", mi.MXFP8: "e4m3"}[w.dtype],
+                "dtype": {mi.BF16: "bf16", mi.FP32: "f32", mi.FP8_BLOCK: "e4m3", mi.MXFP8: "e4m3",
+                          mi.NVFP4: "e2m1"}[w.dtype],
                 "data": "synthetic",
                 "tokens_per_s": jm["tokens_per_s"],
                 "pct_of_tensor_peak": 100.0 * value / world / peak_sust,
@@ -509,7 +518,7 @@ def main():
                     help="comma-separated shape overrides, e.g. F=4096,T=2048 (profiling runs)")
     args = ap.parse_args()
     w = mi.WORKLOADS[args.workload]
-    if args.weight_cache and w.dtype not in (mi.FP8_BLOCK, mi.MXFP8):
+    if args.weight_cache and w.dtype not in (mi.FP8_BLOCK, mi.MXFP8, mi.NVFP4):
         ap.error("--weight-cache applies to the FP8 workloads only")
     if args.override:
         kv = dict(item.split("=") for item in args.override.split(","))

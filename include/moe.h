@@ -80,8 +80,18 @@ typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
  *     gradients that feed two GEMMs) are quantised once per orientation.
  *     The router stays fp32. A shared expert runs through the same engine
  *     as a dense group of the T rows; its weights are quantised by every
- *     forward (the weight cache holds the routed experts' weights). */
-typedef enum { MOE_FP32 = 0, MOE_BF16 = 1, MOE_FP8_BLOCK = 2, MOE_MXFP8 = 3 } moe_dtype_t;
+ *     forward (the weight cache holds the routed experts' weights).
+ *   MOE_NVFP4: as MOE_MXFP8, with every expert GEMM on NVFP4 operands
+ *     ("Scalable Training of Mixture-of-Experts Models with Megatron Core",
+ *     §5 Platform-specific recipes: NVFP4 for Blackwell): E2M1 values, one
+ *     unsigned E4M3 scale per 16 values along K and one fp32 scale
+ *     S = 2688 / amax per tensor -- one expert's part of a grouped operand
+ *     (or a dense operand), with the gate and up projections [W_gate | W_up]
+ *     and their output gradients one tensor each; the tensor cores apply the
+ *     block scales (tcgen05.mma.kind::mxf4nvf4, .scale_vec::4X) and the GEMM
+ *     epilogue divides out the two tensor scales. Requires H, F and Fs to be
+ *     multiples of 256. */
+typedef enum { MOE_FP32 = 0, MOE_BF16 = 1, MOE_FP8_BLOCK = 2, MOE_MXFP8 = 3, MOE_NVFP4 = 4 } moe_dtype_t;
 
 typedef struct {
     int H;       /* hidden size; multiple of 128                          */
@@ -204,7 +214,8 @@ typedef struct {
  * Errors: INVALID_ARG (null, sizes out of range, unknown flags,
  *         capacity_factor negative or not finite),
  *         UNSUPPORTED (dtype not built, device not sm_103, MOE_FP8_BLOCK
- *         with a shared expert), CUDA. */
+ *         with a shared expert, MOE_NVFP4 with H, F or Fs not a multiple of
+ *         256), CUDA. */
 moe_status_t moe_plan_create(const moe_config_t* cfg, int device, moe_plan_t* out);
 
 /* Free a plan. NULL is accepted. */
@@ -299,7 +310,7 @@ enum { MOE_Q_ROWS = 0, MOE_Q_TILES = 1, MOE_Q_COLS_T = 2, MOE_Q_TILES_T = 3 };
 moe_status_t moe_fp8_quantize(int rows, int cols, int mode, const void* in, uint8_t* codes,
                               float* scales, uint8_t* codes_t, float* scales_t, moe_stream_t stream);
 
-/* Quantised expert weights for MOE_FP8_BLOCK and MOE_MXFP8 plans ("Scalable Training of
+/* Quantised expert weights for MOE_FP8_BLOCK, MOE_MXFP8 and MOE_NVFP4 plans ("Scalable Training of
  * Mixture-of-Experts Models with Megatron Core", §5 Kernel and shape
  * optimization: grouped quantization of the experts' weights, done once
  * and kept). A caller that keeps E4M3 weights between steps -- they change
@@ -309,18 +320,20 @@ moe_status_t moe_fp8_quantize(int rows, int cols, int mode, const void* in, uint
  * moe_backward, which then skip their own weight quantisation.
  *
  * moe_weight_cache_size: bytes of the cache for this plan (0 for plans
- * that use neither FP8 recipe). Errors: INVALID_ARG.
+ * without quantised experts). Errors: INVALID_ARG.
  *
  * moe_quantize_weights: quantise W_gate, W_up (E x H x F bf16) and W_down
  * (E x F x H bf16) into `cache` (cache_bytes >= the size above), enqueued
  * on `stream`. The cache holds each matrix's E4M3 codes in its own layout
  * with the plan's scales (MOE_FP8_BLOCK: one fp32 scale per 128x128 block,
  * amax / 448, 1 for an all-zero block; MOE_MXFP8: the codes of both
- * orientations, each with its UE8M0 scale per 32 values), exactly the codes
+ * orientations, each with its UE8M0 scale per 32 values; MOE_NVFP4: the
+ * E2M1 codes of both orientations with their E4M3 scales per 16 values, and
+ * each expert's tensor maxima of [W_gate | W_up] and W_down), exactly the codes
  * the layer would produce inside moe_forward; its internal layout is
  * private to the library version. 16-byte aligned device pointers, owned by
  * the caller.
- * Errors: INVALID_ARG (null), UNSUPPORTED (plan uses neither FP8 recipe),
+ * Errors: INVALID_ARG (null), UNSUPPORTED (plan has no quantised experts),
  * MISALIGNED, WORKSPACE_TOO_SMALL (cache_bytes), CUDA. */
 moe_status_t moe_weight_cache_size(moe_plan_t plan, size_t* bytes);
 moe_status_t moe_quantize_weights(moe_plan_t plan, const void* W_gate, const void* W_up,
@@ -346,6 +359,28 @@ moe_status_t moe_quantize_weights(moe_plan_t plan, const void* W_gate, const voi
  * Errors: INVALID_ARG, MISALIGNED, CUDA. */
 moe_status_t moe_mx_quantize(int rows, int cols, const void* in, uint8_t* codes, uint8_t* scales,
                              uint8_t* codes_c, uint8_t* scales_c, int col_transposed, moe_stream_t stream);
+
+/* NVFP4 quantiser used by the MOE_NVFP4 layer, on a row-major rows x cols
+ * bf16 device matrix (both multiples of 128) taken as one tensor: its
+ * largest magnitude goes to *amax (a device float, overwritten), the tensor
+ * scale is S = 2688 / amax (1 for an all-zero matrix), and each block of
+ * 16 values gets the E4M3 scale sb = E4M3(a S / 6) (a the block's largest
+ * magnitude; s its value) and the E2M1 codes of v (S / s) (nearest, ties to
+ * the even code, saturating at 6; zero codes when s = 0), every step an
+ * fp32 operation rounded to nearest even. Codes are packed two per byte,
+ * the lower-index value in the low 4 bits. Scale atoms: for an operand read
+ * as [n][K], one 512-byte atom per 128-row tile t and 64-value K chunk b at
+ * (t * K/64 + b) * 512, whose byte 16 (m % 32) + 4 (m / 32) + j holds the
+ * scale of tile row m and 16-value sub-block j.
+ *   codes, scales (optional): blocks along the rows; codes rows x cols/2
+ *     bytes, atoms of the [rows][K = cols] operand (rows * cols / 16 bytes).
+ *   codes_t, scales_t (optional): blocks down the columns (16 rows each),
+ *     codes of the transpose, cols x rows/2 bytes; atoms of the
+ *     [cols][K = rows] operand.
+ * At least one pair must be given. Enqueued on `stream`.
+ * Errors: INVALID_ARG, MISALIGNED, CUDA. */
+moe_status_t moe_nv_quantize(int rows, int cols, const void* in, float* amax, uint8_t* codes, uint8_t* scales,
+                             uint8_t* codes_t, uint8_t* scales_t, moe_stream_t stream);
 
 /* Failure-detection check. Every pipelined kernel of the library waits on
  * its shared-memory mbarriers with a bounded wait (2 s); when a wait runs out

@@ -27,7 +27,7 @@ MOE_ERR_WORKSPACE_TOO_SMALL = 4
 MOE_ERR_CUDA = 5
 MOE_ERR_DEVICE_TIMEOUT = 6
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
-MOE_FP32, MOE_BF16, MOE_FP8_BLOCK, MOE_MXFP8 = 0, 1, 2, 3
+MOE_FP32, MOE_BF16, MOE_FP8_BLOCK, MOE_MXFP8, MOE_NVFP4 = 0, 1, 2, 3, 4
 MOE_FLAG_STAGE_TIMING = 1
 MOE_FLAG_FOLD_GATES = 2
 
@@ -35,7 +35,8 @@ MOE_FLAG_FOLD_GATES = 2
 EXPORTS = ("moe_plan_create", "moe_plan_destroy", "moe_workspace_size", "moe_forward",
            "moe_backward", "moe_read_status", "moe_status_string", "moe_stage_times",
            "moe_route_static", "moe_fp8_quantize", "moe_diag_wait_timeout", "moe_update_bias",
-           "moe_weight_cache_size", "moe_quantize_weights", "moe_mx_quantize", "moe_abi_version")
+           "moe_weight_cache_size", "moe_quantize_weights", "moe_mx_quantize", "moe_nv_quantize",
+           "moe_abi_version")
 MOE_Q_ROWS, MOE_Q_TILES, MOE_Q_COLS_T, MOE_Q_TILES_T = 0, 1, 2, 3
 
 
@@ -101,6 +102,7 @@ def load_library() -> ctypes.CDLL:
         lib.moe_weight_cache_size.argtypes = [_vp, P(ctypes.c_size_t)]
         lib.moe_quantize_weights.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
         lib.moe_mx_quantize.argtypes = [ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp]
+        lib.moe_nv_quantize.argtypes = [ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
         lib.moe_abi_version.argtypes = []
         for n in EXPORTS:
             if n not in ("moe_status_string", "moe_abi_version"):
@@ -196,6 +198,13 @@ def moe_mx_quantize(rows: int, cols: int, x: int, codes: int, scales: int, codes
     st = load_library().moe_mx_quantize(rows, cols, x, codes, scales, codes_c, scales_c, col_transposed, stream)
     if st != MOE_OK:
         raise MoEError(st, "moe_mx_quantize")
+
+
+def moe_nv_quantize(rows: int, cols: int, x: int, amax: int, codes: int, scales: int, codes_t: int,
+                    scales_t: int, stream: int) -> None:
+    st = load_library().moe_nv_quantize(rows, cols, x, amax, codes, scales, codes_t, scales_t, stream)
+    if st != MOE_OK:
+        raise MoEError(st, "moe_nv_quantize")
 
 
 def moe_update_bias(E: int, counts: int, rate: float, b: int, stream: int) -> None:

@@ -39,9 +39,20 @@ struct Layout {
     int Tp;
     size_t wcache_s, xsq, sxs, hsq, shs, dYsq, sdYs, dYsTq, sdYsT, hsTq, shsT, dAsq, sdAs, dUsq, sdUs,
         dAsTq, sdAsT, dUsTq, sdUsT, xTq, sxT;
+    size_t amax;   // NVFP4 tensor maxima (workspace)
+    size_t amax_x; // NVFP4: the maxima of x's tensors (saved: each expert's rows, then the shared expert's)
 };
+// NVFP4 tensor maxima in the workspace: h, dY, [dA | dU] per expert, then the
+// shared expert's three (x's maxima are kept in the saved buffer)
+enum { AMAX_H = 0, AMAX_DY = 1, AMAX_DAU = 2, kAmaxKinds = 3 };
 
-bool fp8_recipe(const moe_config_t& c) { return c.dtype == MOE_FP8_BLOCK || c.dtype == MOE_MXFP8; }
+// the quantised-expert recipes; the block-scaled ones (MXFP8, NVFP4) share
+// the MX layer's stages
+bool fp8_recipe(const moe_config_t& c)
+{
+    return c.dtype == MOE_FP8_BLOCK || c.dtype == MOE_MXFP8 || c.dtype == MOE_NVFP4;
+}
+bool bs_recipe(const moe_config_t& c) { return c.dtype == MOE_MXFP8 || c.dtype == MOE_NVFP4; }
 
 // The split row tables inside the pair-table block (see make_layout).
 struct SplitTabs {
@@ -68,8 +79,13 @@ SplitTabs split_tabs(const Layout& L, int E, const uint8_t* sv)
 //     the matrix's first dimension, the forward GEMM's K, read MN-major) and
 //     q[3..5] the data-gradient orientation (blocks along the second
 //     dimension, read K-major), each with its UE8M0 scale atoms.
+//   MOE_NVFP4: q[0..2] the forward orientation as each expert's transpose
+//     (W_gate^T, W_up^T: E x F x H; W_down^T: E x H x F; read K-major), q[3..5]
+//     the data-gradient orientation in the natural layout, E2M1 codes two per
+//     byte with E4M3 scale atoms; amax: each expert's largest magnitude of
+//     [W_gate | W_up] (E floats), then of W_down (E floats).
 struct WeightCache {
-    size_t q[6], s[6], bytes;
+    size_t q[6], s[6], amax, bytes;
 };
 
 // The shared expert as a one-expert layer of width Fs (its weight codes use
@@ -90,16 +106,17 @@ WeightCache cache_layout(const moe_config_t& c)
     memset(&W, 0, sizeof W);
     if (!fp8_recipe(c)) return W;
     const size_t EHF = (size_t)c.E * c.H * c.F;
-    const bool mx = c.dtype == MOE_MXFP8;
-    const size_t sc = mx ? EHF / 32 : 4 * (size_t)(c.H / 128) * (c.F / 128) * c.E;
+    const bool mx = c.dtype == MOE_MXFP8, nv = c.dtype == MOE_NVFP4;
+    const size_t sc = nv ? EHF / 16 : mx ? EHF / 32 : 4 * (size_t)(c.H / 128) * (c.F / 128) * c.E;
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
-    for (int i = 0; i < (mx ? 6 : 3); ++i) {
-        W.q[i] = take(EHF);
+    for (int i = 0; i < (mx || nv ? 6 : 3); ++i) {
+        W.q[i] = take(nv ? EHF / 2 : EHF);
         W.s[i] = take(sc);
     }
-    if (!mx)
+    if (!mx && !nv)
         for (int i = 3; i < 6; ++i) { W.q[i] = W.q[i - 3]; W.s[i] = W.s[i - 3]; }
+    W.amax = take(nv ? sizeof(float) * 2 * (size_t)c.E : 0);
     W.bytes = o;
     return W;
 }
@@ -145,16 +162,20 @@ Layout make_layout(const moe_config_t& c, int T)
     L.As = take(es * (size_t)T * c.Fs);
     L.Us = take(es * (size_t)T * c.Fs);
     L.Hs = take(es * (size_t)T * c.Fs);
-    const bool q8 = c.dtype == MOE_FP8_BLOCK, mx = c.dtype == MOE_MXFP8, anyq = q8 || mx;
+    const bool q8 = c.dtype == MOE_FP8_BLOCK, mx = c.dtype == MOE_MXFP8, nv = c.dtype == MOE_NVFP4;
+    const bool bs = mx || nv, anyq = q8 || bs;
     const size_t Rp = L.Rp_max;
-    // scale bytes of a codes array: blockwise per 128 values (fp32), MX per 32 (one byte)
-    auto scb = [&](size_t n128) { return q8 ? 4 * n128 : mx ? 4 * n128 : 0; };
-    L.Xq = take(anyq ? Rp * c.H : 0);
+    // scale bytes of a codes array: blockwise per 128 values (fp32), MX per
+    // 32 (one byte), NVFP4 per 16 (one byte); code bytes: NVFP4 two values a byte
+    auto scb = [&](size_t n128) { return q8 ? 4 * n128 : mx ? 4 * n128 : nv ? 8 * n128 : 0; };
+    auto cbt = [&](size_t n) { return anyq ? (nv ? n / 2 : n) : 0; };
+    L.Xq = take(cbt(Rp * c.H));
     L.sX = take(scb(Rp * (c.H / 128)));
     L.wcache = take(cache_layout(c).bytes);
-    const bool mxs = mx && c.Fs > 0;
+    const bool mxs = bs && c.Fs > 0;
     L.Tp = (int)align_up((size_t)T, 128);
     L.wcache_s = take(mxs ? cache_layout(shared_config(c)).bytes : 0);
+    L.amax_x = take(nv ? sizeof(float) * ((size_t)c.E + 1) : 0);
     L.saved_bytes = o;
     o = 0;
     L.status = take(256);
@@ -174,35 +195,39 @@ Layout make_layout(const moe_config_t& c, int T)
     L.dUs = take(es * (size_t)T * c.Fs);
     L.dXs = take(c.Fs ? es * (size_t)T * c.H : 0);
     // blockwise: 1x128 row scales, per-column or per-tile transposed scales;
-    // MX: one byte per 32 values whatever the orientation
-    const size_t RF32 = Rp * c.F / 32, RH32 = Rp * c.H / 32;
-    L.hq = take(anyq ? Rp * c.F : 0);     L.sh = take(mx ? RF32 : scb(Rp * (c.F / 128)));
-    L.dYq = take(anyq ? Rp * c.H : 0);    L.sdY = take(mx ? RH32 : scb(Rp * (c.H / 128)));
-    L.dAq = take(anyq ? Rp * c.F : 0);    L.sdA = take(mx ? RF32 : scb(Rp * (c.F / 128)));
-    L.dUq = take(anyq ? Rp * c.F : 0);    L.sdU = take(mx ? RF32 : scb(Rp * (c.F / 128)));
-    L.hTq = take(anyq ? Rp * c.F : 0);    L.shT = take(mx ? RF32 : scb((Rp / 128) * c.F));
-    L.dYpTq = take(anyq ? Rp * c.H : 0);  L.sdYpT = take(mx ? RH32 : scb((Rp / 128) * (c.H / 128)));
-    L.XpTq = take(anyq ? Rp * c.H : 0);   L.sXpT = take(mx ? RH32 : scb((Rp / 128) * c.H));
-    L.dATq = take(anyq ? Rp * c.F : 0);   L.sdAT = take(mx ? RF32 : scb((Rp / 128) * (c.F / 128)));
+    // MX (NVFP4): one byte per 32 (16) values whatever the orientation
+    const size_t RF32 = Rp * c.F / (nv ? 16 : 32), RH32 = Rp * c.H / (nv ? 16 : 32);
+    L.hq = take(cbt(Rp * c.F));     L.sh = take(bs ? RF32 : scb(Rp * (c.F / 128)));
+    L.dYq = take(cbt(Rp * c.H));    L.sdY = take(bs ? RH32 : scb(Rp * (c.H / 128)));
+    L.dAq = take(cbt(Rp * c.F));    L.sdA = take(bs ? RF32 : scb(Rp * (c.F / 128)));
+    L.dUq = take(cbt(Rp * c.F));    L.sdU = take(bs ? RF32 : scb(Rp * (c.F / 128)));
+    L.hTq = take(cbt(Rp * c.F));    L.shT = take(bs ? RF32 : scb((Rp / 128) * c.F));
+    L.dYpTq = take(cbt(Rp * c.H));  L.sdYpT = take(bs ? RH32 : scb((Rp / 128) * (c.H / 128)));
+    L.XpTq = take(cbt(Rp * c.H));   L.sXpT = take(bs ? RH32 : scb((Rp / 128) * c.H));
+    L.dATq = take(cbt(Rp * c.F));   L.sdAT = take(bs ? RF32 : scb((Rp / 128) * (c.F / 128)));
     L.dgpart = take(L.fold ? sizeof(float) * L.Rp_max * (c.F / 64) : 0);
     if (L.fold) {
         L.Hh = take(es * L.Rp_max * c.F);
         L.Yp = take(es * L.Rp_max * c.H);
     }
-    L.dUTq = take(anyq ? Rp * c.F : 0);   L.sdUT = take(mx ? RF32 : scb((Rp / 128) * (c.F / 128)));
+    L.dUTq = take(cbt(Rp * c.F));   L.sdUT = take(bs ? RF32 : scb((Rp / 128) * (c.F / 128)));
     {
         const size_t TpH = mxs ? (size_t)L.Tp * c.H : 0, TpF = mxs ? (size_t)L.Tp * c.Fs : 0;
-        L.xsq = take(TpH);   L.sxs = take(TpH / 32);     // x, rows (shared fc1)
-        L.hsq = take(TpF);   L.shs = take(TpF / 32);     // h_s, rows (shared fc2)
-        L.dYsq = take(TpH);  L.sdYs = take(TpH / 32);    // dY, rows (shared fc2 dgrad)
-        L.dYsTq = take(TpH); L.sdYsT = take(TpH / 32);   // dY, columns (shared fc2 wgrad)
-        L.hsTq = take(TpF);  L.shsT = take(TpF / 32);    // h_s, columns
-        L.dAsq = take(TpF);  L.sdAs = take(TpF / 32);    // dA_s, dU_s: rows and columns
-        L.dUsq = take(TpF);  L.sdUs = take(TpF / 32);
-        L.dAsTq = take(TpF); L.sdAsT = take(TpF / 32);
-        L.dUsTq = take(TpF); L.sdUsT = take(TpF / 32);
-        L.xTq = take(TpH);   L.sxT = take(TpH / 32);     // x, columns (shared fc1 wgrad)
+        const size_t vb = nv ? 2 : 1, sb = nv ? 16 : 32;   // values per code byte, per scale byte
+        L.xsq = take(TpH / vb);   L.sxs = take(TpH / sb);     // x, rows (shared fc1)
+        L.hsq = take(TpF / vb);   L.shs = take(TpF / sb);     // h_s, rows (shared fc2)
+        L.dYsq = take(TpH / vb);  L.sdYs = take(TpH / sb);    // dY, rows (shared fc2 dgrad)
+        L.dYsTq = take(TpH / vb); L.sdYsT = take(TpH / sb);   // dY, columns (shared fc2 wgrad)
+        L.hsTq = take(TpF / vb);  L.shsT = take(TpF / sb);    // h_s, columns
+        L.dAsq = take(TpF / vb);  L.sdAs = take(TpF / sb);    // dA_s, dU_s: rows and columns
+        L.dUsq = take(TpF / vb);  L.sdUs = take(TpF / sb);
+        L.dAsTq = take(TpF / vb); L.sdAsT = take(TpF / sb);
+        L.dUsTq = take(TpF / vb); L.sdUsT = take(TpF / sb);
+        L.xTq = take(TpH / vb);   L.sxT = take(TpH / sb);     // x, columns (shared fc1 wgrad)
     }
+    // NVFP4 tensor maxima of the activations and gradients (per expert: h, dY,
+    // [dA | dU]; then the shared expert's), recomputed by each call
+    L.amax = take(nv ? sizeof(float) * kAmaxKinds * ((size_t)c.E + 1) : 0);
     L.ws_bytes = o;
     return L;
 }
@@ -227,9 +252,12 @@ moe_status_t check_config(const moe_config_t* c)
         !(c->capacity_factor >= 0.f) || !std::isfinite(c->capacity_factor))
         return MOE_ERR_INVALID_ARG;
     if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
-    if (c->dtype != MOE_FP32 && c->dtype != MOE_BF16 && c->dtype != MOE_FP8_BLOCK && c->dtype != MOE_MXFP8)
+    if (c->dtype != MOE_FP32 && c->dtype != MOE_BF16 && c->dtype != MOE_FP8_BLOCK && c->dtype != MOE_MXFP8 &&
+        c->dtype != MOE_NVFP4)
         return MOE_ERR_INVALID_ARG;
     if (c->dtype == MOE_FP8_BLOCK && c->Fs > 0) return MOE_ERR_UNSUPPORTED;
+    // NVFP4 data GEMMs take whole 256-value k blocks of H, F and Fs
+    if (c->dtype == MOE_NVFP4 && (c->H % 256 || c->F % 256 || c->Fs % 256)) return MOE_ERR_UNSUPPORTED;
     // int32 row indices: R_pad * max(H, F) elements must stay addressable per
     // buffer with 32-bit row numbers
     const long long R = (long long)c->T_max * c->top_k + (long long)c->E * kTileM;
@@ -263,14 +291,14 @@ enum Stage : int {
     ST_ROUTER, ST_SCAN, ST_INDEX, ST_PERMUTE, ST_FC1, ST_FC2, ST_FC1S, ST_FC2S, ST_COMBINE,
     ST_GATEGRAD, ST_FC2_DGRAD, ST_FC2_WGRAD, ST_FC1_DGRAD, ST_FC1_WGRAD, ST_FC2S_DGRAD,
     ST_FC2S_WGRAD, ST_FC1S_DGRAD, ST_FC1S_WGRAD, ST_ROUTER_WGRAD, ST_TRANSPOSE, ST_UNPERMUTE,
-    ST_WQUANT, ST_QROWS, ST_QT, ST_GATEDZ, ST_COUNT
+    ST_WQUANT, ST_QROWS, ST_QT, ST_GATEDZ, ST_AMAX, ST_COUNT
 };
 const char* const kStageNames[ST_COUNT] = {
     "router", "scan", "index", "permute", "fc1_swiglu", "fc2", "shared_fc1_swiglu", "shared_fc2",
     "combine", "gate_grad", "fc2_dgrad_swiglu", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad",
     "shared_fc2_dgrad", "shared_fc2_wgrad", "shared_fc1_dgrad", "shared_fc1_wgrad",
     "router_wgrad", "wr_transpose", "unpermute_reduce", "fp8_weight_quant", "fp8_quant_rows",
-    "fp8_quant_t", "gate_dz"
+    "fp8_quant_t", "gate_dz", "nv_amax"
 };
 struct StageRec {
     int stage;
@@ -327,6 +355,7 @@ moe_status_t moe_plan_create(const moe_config_t* cfg, int device, moe_plan_t* ou
         if (cfg->dtype == MOE_BF16 && gemm_tc_prepare(device) != cudaSuccess) return MOE_ERR_CUDA;
         if (cfg->dtype == MOE_FP8_BLOCK && gemm_fp8_prepare(device) != cudaSuccess) return MOE_ERR_CUDA;
         if (cfg->dtype == MOE_MXFP8 && gemm_mx_prepare(device) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cfg->dtype == MOE_NVFP4 && gemm_nv_prepare(device) != cudaSuccess) return MOE_ERR_CUDA;
     }
     moe_plan_s* p = new (std::nothrow) moe_plan_s;
     if (!p) return MOE_ERR_CUDA;
@@ -689,6 +718,7 @@ static moe_status_t backward_impl(moe_plan_t p, int T_, const moe_bwd_args_t* a,
 struct WQ {
     uint8_t* q[6];   // gate, up, down: forward orientation, then data-gradient orientation
     void* s[6];
+    float* amax;     // NVFP4: per expert, [W_gate | W_up] then W_down
 };
 static WQ codes_at(const moe_config_t& c, uint8_t* b)
 {
@@ -698,18 +728,12 @@ static WQ codes_at(const moe_config_t& c, uint8_t* b)
         w.q[i] = b + C.q[i];
         w.s[i] = b + C.s[i];
     }
+    w.amax = reinterpret_cast<float*>(b + C.amax);
     return w;
 }
 static WQ weight_codes(const moe_config_t& c, const Layout& L, uint8_t* sv, const void* cache)
 {
-    WQ w;
-    const WeightCache C = cache_layout(c);
-    uint8_t* b = cache ? static_cast<uint8_t*>(const_cast<void*>(cache)) : sv + L.wcache;
-    for (int i = 0; i < 6; ++i) {
-        w.q[i] = b + C.q[i];
-        w.s[i] = b + C.s[i];
-    }
-    return w;
+    return codes_at(c, cache ? static_cast<uint8_t*>(const_cast<void*>(cache)) : sv + L.wcache);
 }
 
 // Quantise W_gate, W_up, W_down into the weight codes w (both orientations).
@@ -720,6 +744,31 @@ static cudaError_t quantize_weights(const moe_config_t& c, const void* Wg, const
     const int E = c.E, H = c.H, F = c.F;
     const void* W[3] = {Wg, Wu, Wd};
     const int R[3] = {H, H, F}, Cc[3] = {F, F, H};
+    if (c.dtype == MOE_NVFP4) {
+        // each expert's tensor maxima ([W_gate | W_up] into one), then one pass
+        // per matrix: row codes (the data-gradient orientation) and each
+        // expert's transposed codes (the forward orientation, K-major)
+        cudaError_t e = cudaMemsetAsync(w.amax, 0, sizeof(float) * 2 * (size_t)E, s);
+        NvQuantJob j[3];
+        for (int i = 0; i < 3 && e == cudaSuccess; ++i) {
+            memset(&j[i], 0, sizeof j[i]);
+            j[i].in = static_cast<const T*>(W[i]);
+            j[i].rows_max = E * R[i];
+            j[i].C = Cc[i];
+            j[i].rows_cap = E * R[i];
+            j[i].q = w.q[3 + i];
+            j[i].sf = static_cast<uint8_t*>(w.s[3 + i]);
+            j[i].qc = w.q[i];
+            j[i].sfc = static_cast<uint8_t*>(w.s[i]);
+            j[i].grp = R[i];
+            j[i].seg_rows = R[i];
+            j[i].gather_k = 1;
+            j[i].amax = w.amax + (i == 2 ? E : 0);
+            e = launch_nv_amax(j[i], w.amax + (i == 2 ? E : 0), s);
+        }
+        for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = launch_nv_quant(j[i], s);
+        return e;
+    }
     for (int i = 0; i < 3; ++i) {
         cudaError_t e;
         if (c.dtype == MOE_MXFP8) {
@@ -943,12 +992,42 @@ static moe_status_t backward_fp8_impl(moe_plan_t p, int T_, const moe_bwd_args_t
     return MOE_OK;
 }
 
-// ------------------------------------------------------------------ MXFP8
+// ------------------------------------------------------- MXFP8 and NVFP4
 // The blockwise-FP8 layer's stages with the MXFP8 recipe: every GEMM operand
 // is quantised in 32-element blocks along the GEMM's K with power-of-two
 // scales (quant_mx.cu), so the activations and gradients that feed a data
 // GEMM and a weight-gradient GEMM get one quantisation per orientation, like
 // the weights, and the grouped GEMMs apply the scales in the tensor cores.
+// NVFP4 takes the same stages with 16-value E2M1 blocks (quant_nv.cu,
+// gemm_nv.cu); each tensor first gets its largest magnitude (a maximum pass
+// per expert segment, stage nv_amax), for its fp32 tensor scale, and every
+// GEMM reads its weights K-major.
+
+// NVFP4 quantisation job over the routed rows (one tensor per expert
+// segment) or over a dense group of T rows padded to Tp
+static NvQuantJob nv_job(const Layout& L, int T_, const int* meta, const int* poff, int E, bool dense,
+                         const __nv_bfloat16* in, int C, uint8_t* q, uint8_t* sf, uint8_t* qc, uint8_t* sfc,
+                         const float* amax)
+{
+    NvQuantJob j;
+    memset(&j, 0, sizeof j);
+    j.in = in;
+    j.C = C;
+    j.q = q; j.sf = sf; j.qc = qc; j.sfc = sfc;
+    j.gather_k = 1;
+    j.amax = amax;
+    if (dense) {
+        j.rows_max = j.rows_cap = j.grp = L.Tp;
+        j.rows_valid = T_;
+    } else {
+        j.rows_dev = meta + 1;
+        j.rows_max = j.rows_cap = j.grp = L.Rp_max;
+        j.seg_off = poff;
+        j.nseg = E;
+    }
+    return j;
+}
+
 static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* a, uint8_t* sv,
                                     uint8_t* ws, cudaStream_t s)
 {
@@ -956,6 +1035,11 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
     const moe_config_t& c = p->cfg;
     const Layout L = make_layout(c, T_);
     const int H = c.H, E = c.E, k = c.top_k, F = c.F, Rp = L.Rp_max;
+    const bool nv = c.dtype == MOE_NVFP4;
+    float* am = nv ? reinterpret_cast<float*>(ws + L.amax) : nullptr;   // [3][E], then the shared expert's
+    auto gemm = [&](const GemmDesc& g) {
+        return nv ? launch_gemm_nv(g, L.MT_max, p->num_sms, s) : launch_gemm_mx(g, L.MT_max, p->num_sms, s);
+    };
     DeviceStatus* status = reinterpret_cast<DeviceStatus*>(ws + L.status);
     int* topk = reinterpret_cast<int*>(sv + L.topk);
     float* gates = reinterpret_cast<float*>(sv + L.gates);
@@ -987,7 +1071,17 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
     if (slotlive) MOE_CUDA(cudaMemsetAsync(slotlive, 0xFF, sizeof(int) * (size_t)L.Rp_max, s));
     MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s,
                                      poff, kept, slotlive));
-    MOE_STAGE(ST_PERMUTE, launch_mx_permute(x, rowof, poff, counts, T_, H, E, k, sv + L.Xq, sv + L.sX, s));
+    float* amx = nv ? reinterpret_cast<float*>(sv + L.amax_x) : nullptr;   // x's maxima, kept for backward
+    if (nv) {
+        // each expert's maximum over the rows it keeps, then every token's k
+        // rows in their experts' tensor scales (x read twice, not gathered)
+        MOE_CUDA(cudaMemsetAsync(am, 0, sizeof(float) * kAmaxKinds * ((size_t)E + 1), s));
+        MOE_CUDA(cudaMemsetAsync(amx, 0, sizeof(float) * ((size_t)E + 1), s));
+        MOE_STAGE(ST_PERMUTE, launch_nv_permute(x, topk, rowof, poff, counts, kept, T_, H, E, k, amx, sv + L.Xq,
+                                                sv + L.sX, s));
+    } else {
+        MOE_STAGE(ST_PERMUTE, launch_mx_permute(x, rowof, poff, counts, T_, H, E, k, sv + L.Xq, sv + L.sX, s));
+    }
     const WQ wq = weight_codes(c, L, sv, a->weight_cache);
     if (!a->weight_cache)
         MOE_STAGE(ST_WQUANT, quantize_weights(c, a->W_gate, a->W_up, a->W_down, wq, s));
@@ -1003,8 +1097,19 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
     d.XB0 = xs(wq.s[0]); d.XB1 = xs(wq.s[1]);
     d.O0 = A; d.O1 = U; d.O2 = Hh; d.ldo = F; d.status = status;
     if (L.fold) { d.gates = gates; d.slot_of = slotof; }   // Hh = g silu(A) U
-    d.Qrows = ws + L.hq; d.Qatoms = ws + L.sh;              // fc2's A operand, from the epilogue
-    MOE_STAGE(ST_FC1, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    if (nv) {   // [Wg^T | Wu^T] K-major; h is quantised after its maximum is known
+        d.nv = 1; d.gA = amx; d.gB = wq.amax;
+        d.ldb = H; d.b_rows = E * F; d.b_kmajor = 1;
+    } else {
+        d.Qrows = ws + L.hq; d.Qatoms = ws + L.sh;          // fc2's A operand, from the epilogue
+    }
+    MOE_STAGE(ST_FC1, gemm(d));
+    if (nv) {
+        NvQuantJob j = nv_job(L, T_, meta, poff, E, false, Hh, F, ws + L.hq, ws + L.sh, nullptr, nullptr,
+                              am + AMAX_H * E);
+        MOE_STAGE(ST_AMAX, launch_nv_amax(j, am + AMAX_H * E, s));
+        MOE_STAGE(ST_QROWS, launch_nv_quant(j, s));
+    }
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
     d.N = H; d.K = F; d.E = E;
@@ -1012,8 +1117,12 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
     d.pair_tab = pairtab; d.pair_off = pairtab + L.MT_max; d.prefer_pair = (long long)T_ * k >= 256ll * E;
     d.A0 = ws + L.hq; d.lda = F; d.a_rows = Rp; d.XA0 = ws + L.sh;
     d.B0 = wq.q[2]; d.ldb = H; d.b_rows = E * F; d.XB0 = xs(wq.s[2]); d.b_kmajor = 0;
+    if (nv) {   // Wd^T K-major
+        d.nv = 1; d.gA = am + AMAX_H * E; d.gB = wq.amax + E;
+        d.ldb = F; d.b_rows = E * H; d.b_kmajor = 1;
+    }
     d.O0 = Yp; d.ldo = H; d.status = status;
-    MOE_STAGE(ST_FC2, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    MOE_STAGE(ST_FC2, gemm(d));
     T* Ys = nullptr;
     if (c.Fs) {
         // the shared expert: a dense group of the T token rows (padded to Tp
@@ -1026,7 +1135,13 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
         T* Hs = reinterpret_cast<T*>(sv + L.Hs);
         Ys = reinterpret_cast<T*>(ws + L.Ys);
         MOE_STAGE(ST_WQUANT, quantize_weights(cs, a->Ws_gate, a->Ws_up, a->Ws_down, wqs, s));
-        {
+        float* ams = nv ? am + kAmaxKinds * E : nullptr;   // the shared expert's h, dY, [dA | dU]
+        if (nv) {
+            NvQuantJob j = nv_job(L, T_, meta, poff, E, true, x, H, ws + L.xsq, ws + L.sxs, nullptr, nullptr,
+                                  amx + E);
+            MOE_STAGE(ST_AMAX, launch_nv_amax(j, amx + E, s));
+            MOE_STAGE(ST_QROWS, launch_nv_quant(j, s));
+        } else {
             MxQuantJob j{x, nullptr, Tp, H, Tp, ws + L.xsq, ws + L.sxs, nullptr, nullptr, 0};
             j.rows_valid = T_;
             MOE_STAGE(ST_QROWS, launch_mx_quant(j, s));
@@ -1038,15 +1153,30 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
         d.B0 = wqs.q[0]; d.B1 = wqs.q[1]; d.ldb = Fs; d.b_rows = H; d.b_kmajor = 0;
         d.XB0 = xs(wqs.s[0]); d.XB1 = xs(wqs.s[1]);
         d.O0 = As; d.O1 = Us; d.O2 = Hs; d.ldo = Fs; d.status = status;
-        d.Qrows = ws + L.hsq; d.Qatoms = ws + L.shs;              // shared fc2's A operand
-        MOE_STAGE(ST_FC1S, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+        if (nv) {
+            d.nv = 1; d.gA = amx + E; d.gB = wqs.amax;
+            d.ldb = H; d.b_rows = Fs; d.b_kmajor = 1;
+        } else {
+            d.Qrows = ws + L.hsq; d.Qatoms = ws + L.shs;          // shared fc2's A operand
+        }
+        MOE_STAGE(ST_FC1S, gemm(d));
+        if (nv) {
+            NvQuantJob j = nv_job(L, T_, meta, poff, E, true, Hs, Fs, ws + L.hsq, ws + L.shs, nullptr, nullptr,
+                                  ams + AMAX_H);
+            MOE_STAGE(ST_AMAX, launch_nv_amax(j, ams + AMAX_H, s));
+            MOE_STAGE(ST_QROWS, launch_nv_quant(j, s));
+        }
         memset(&d, 0, sizeof d);
         d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
         d.N = H; d.K = Fs; d.E = 1; d.dense_rows = T_;
         d.A0 = ws + L.hsq; d.lda = Fs; d.a_rows = Tp; d.XA0 = ws + L.shs;
         d.B0 = wqs.q[2]; d.ldb = H; d.b_rows = Fs; d.XB0 = xs(wqs.s[2]); d.b_kmajor = 0;
+        if (nv) {
+            d.nv = 1; d.gA = ams + AMAX_H; d.gB = wqs.amax + 1;
+            d.ldb = Fs; d.b_rows = H; d.b_kmajor = 1;
+        }
         d.O0 = Ys; d.ldo = H; d.status = status;
-        MOE_STAGE(ST_FC2S, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+        MOE_STAGE(ST_FC2S, gemm(d));
     }
     MOE_STAGE(ST_COMBINE, launch_combine<T>(Yp, Ys, rowof, L.fold ? nullptr : gates, T_, H, k,
                                             static_cast<T*>(a->y), s));
@@ -1096,6 +1226,19 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
     const T* dY = static_cast<const T*>(a->dY);
     const WQ wq = weight_codes(c, L, sv, a->weight_cache);
     auto xs = [](void* v) { return static_cast<const uint8_t*>(v); };
+    const bool nv = c.dtype == MOE_NVFP4;
+    float* am = nv ? reinterpret_cast<float*>(ws + L.amax) : nullptr;   // [3][E], then the shared expert's
+    auto gemm = [&](const GemmDesc& g) {
+        return nv ? launch_gemm_nv(g, L.MT_max, p->num_sms, s) : launch_gemm_mx(g, L.MT_max, p->num_sms, s);
+    };
+    // NVFP4: each tensor's maximum (one array for a pair that shares a
+    // tensor scale), then its codes
+    auto nvq = [&](const NvQuantJob& j, int stage) -> moe_status_t {
+        MOE_STAGE(ST_AMAX, launch_nv_amax(j, const_cast<float*>(j.amax), s));
+        MOE_STAGE(stage, launch_nv_quant(j, s));
+        return MOE_OK;
+    };
+    if (nv) MOE_CUDA(cudaMemsetAsync(am, 0, sizeof(float) * kAmaxKinds * ((size_t)E + 1), s));
 
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
     if (L.fold)
@@ -1104,7 +1247,11 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
         MOE_STAGE(ST_GATEGRAD, launch_gate_grad<T>(dY, Yp, rowof, topk, gates, selsc, poff, counts, T_, H,
                                                    E, k, c.score, dYp, dz, s, slotlive));
     // dYp once: row codes (fc2 dgrad, K = H) and transposed column codes (fc2 wgrad, K = tokens)
-    {
+    if (nv) {
+        const moe_status_t r = nvq(nv_job(L, T_, meta, poff, E, false, dYp, H, ws + L.dYq, ws + L.sdY, ws + L.dYpTq,
+                                          ws + L.sdYpT, am + AMAX_DY * E), ST_QROWS);
+        if (r != MOE_OK) return r;
+    } else {
         MxQuantJob j{dYp, meta + 1, Rp, H, Rp, ws + L.dYq, ws + L.sdY, ws + L.dYpTq, ws + L.sdYpT, 1};
         MOE_STAGE(ST_QROWS, launch_mx_quant(j, s));
     }
@@ -1121,11 +1268,16 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
         d.gates = gates; d.slot_of = slotof; d.dg_part = dgpart; d.dg_ld = F / 64;
         d.O2 = Hh;   // g h, recomputed for the fc2 weight gradient
     }
-    MOE_STAGE(ST_FC2_DGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    if (nv) { d.nv = 1; d.gA = am + AMAX_DY * E; d.gB = wq.amax + E; }
+    MOE_STAGE(ST_FC2_DGRAD, gemm(d));
     if (L.fold)
         MOE_STAGE(ST_GATEDZ, launch_gate_dz(dgpart, F / 64, rowof, gates, selsc, T_, k, c.score, dz, s));
     // fc2 wgrad: dWd[e] = h_e^T dYp_e
-    {
+    if (nv) {
+        const moe_status_t r = nvq(nv_job(L, T_, meta, poff, E, false, Hh, F, nullptr, nullptr, ws + L.hTq,
+                                          ws + L.shT, am + AMAX_H * E), ST_QT);
+        if (r != MOE_OK) return r;
+    } else {
         MxQuantJob j{Hh, meta + 1, Rp, F, Rp, nullptr, nullptr, ws + L.hTq, ws + L.shT, 1};
         MOE_STAGE(ST_QT, launch_mx_quant(j, s));
     }
@@ -1138,9 +1290,20 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
     d.B0 = ws + L.dYpTq; d.ldb = Rp; d.XB0 = ws + L.sdYpT;
     d.rows_cap = Rp; d.expert_order = eorder;
     d.O0 = a->dW_down; d.ldo = H; d.o_estride = (long long)F * H; d.status = status;
-    MOE_STAGE(ST_FC2_WGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    if (nv) { d.nv = 1; d.gA = am + AMAX_H * E; d.gB = am + AMAX_DY * E; }
+    MOE_STAGE(ST_FC2_WGRAD, gemm(d));
     // dA, dU once each: row codes (fc1 dgrad, K = F) and transposed column codes (fc1 wgrad)
-    {
+    if (nv) {   // one tensor [dA | dU] per expert
+        float* g = am + AMAX_DAU * E;
+        const NvQuantJob ja = nv_job(L, T_, meta, poff, E, false, dA, F, ws + L.dAq, ws + L.sdA, ws + L.dATq,
+                                     ws + L.sdAT, g);
+        const NvQuantJob ju = nv_job(L, T_, meta, poff, E, false, dU, F, ws + L.dUq, ws + L.sdU, ws + L.dUTq,
+                                     ws + L.sdUT, g);
+        MOE_STAGE(ST_AMAX, launch_nv_amax(ja, g, s));
+        MOE_STAGE(ST_AMAX, launch_nv_amax(ju, g, s));
+        MOE_STAGE(ST_QROWS, launch_nv_quant(ja, s));
+        MOE_STAGE(ST_QROWS, launch_nv_quant(ju, s));
+    } else {
         MxQuantJob ja{dA, meta + 1, Rp, F, Rp, ws + L.dAq, ws + L.sdA, ws + L.dATq, ws + L.sdAT, 1};
         MOE_STAGE(ST_QROWS, launch_mx_quant(ja, s));
         MxQuantJob ju{dU, meta + 1, Rp, F, Rp, ws + L.dUq, ws + L.sdU, ws + L.dUTq, ws + L.sdUT, 1};
@@ -1156,9 +1319,17 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
     d.B0 = wq.q[3]; d.B1 = wq.q[4]; d.ldb = F; d.b_rows = E * H; d.b_kmajor = 1;
     d.XB0 = xs(wq.s[3]); d.XB1 = xs(wq.s[4]);
     d.O0 = dXp; d.ldo = H; d.status = status;
-    MOE_STAGE(ST_FC1_DGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    if (nv) { d.nv = 1; d.gA = am + AMAX_DAU * E; d.gB = wq.amax; }
+    MOE_STAGE(ST_FC1_DGRAD, gemm(d));
     // fc1 wgrad: the permuted rows are token rows of x (no bf16 copy of them is kept)
-    {
+    const float* amx = nv ? reinterpret_cast<const float*>(sv + L.amax_x) : nullptr;   // from the forward
+    if (nv) {
+        NvQuantJob j = nv_job(L, T_, meta, poff, E, false, static_cast<const T*>(a->x), H, nullptr, nullptr,
+                              ws + L.XpTq, ws + L.sXpT, amx);
+        j.gather_slot = slotlive ? slotlive : slotof;
+        j.gather_k = k;
+        MOE_STAGE(ST_QT, launch_nv_quant(j, s));
+    } else {
         MxQuantJob j{static_cast<const T*>(a->x), meta + 1, Rp, H, Rp, nullptr, nullptr, ws + L.XpTq,
                      ws + L.sXpT, 1};
         j.gather_slot = slotlive ? slotlive : slotof;
@@ -1175,7 +1346,8 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
     d.XB0 = ws + L.sdAT; d.XB1 = ws + L.sdUT;
     d.rows_cap = Rp; d.expert_order = eorder;
     d.O0 = a->dW_gate; d.O1 = a->dW_up; d.ldo = F; d.o_estride = (long long)H * F; d.status = status;
-    MOE_STAGE(ST_FC1_WGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+    if (nv) { d.nv = 1; d.gA = amx; d.gB = am + AMAX_DAU * E; }
+    MOE_STAGE(ST_FC1_WGRAD, gemm(d));
     T* dXs = nullptr;
     if (c.Fs) {
         // the shared expert's backward; its output gradient is dY itself
@@ -1188,8 +1360,13 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
         T* dAs = reinterpret_cast<T*>(ws + L.dAs);
         T* dUs = reinterpret_cast<T*>(ws + L.dUs);
         dXs = reinterpret_cast<T*>(ws + L.dXs);
+        float* ams = nv ? am + kAmaxKinds * E : nullptr;   // the shared expert's h, dY, [dA | dU]
         // dY: row codes (shared fc2 dgrad, K = H), column codes (shared fc2 wgrad, K = tokens)
-        {
+        if (nv) {
+            const moe_status_t r = nvq(nv_job(L, T_, meta, poff, E, true, dY, H, ws + L.dYsq, ws + L.sdYs,
+                                              ws + L.dYsTq, ws + L.sdYsT, ams + AMAX_DY), ST_QROWS);
+            if (r != MOE_OK) return r;
+        } else {
             MxQuantJob j{dY, nullptr, Tp, H, Tp, ws + L.dYsq, ws + L.sdYs, ws + L.dYsTq, ws + L.sdYsT, 1};
             j.rows_valid = T_;
             MOE_STAGE(ST_QROWS, launch_mx_quant(j, s));
@@ -1200,8 +1377,13 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
         d.A0 = ws + L.dYsq; d.lda = H; d.a_rows = Tp; d.XA0 = ws + L.sdYs;
         d.B0 = wqs.q[5]; d.ldb = H; d.b_rows = Fs; d.XB0 = xs(wqs.s[5]); d.b_kmajor = 1;
         d.X0 = As; d.X1 = Us; d.O0 = dAs; d.O1 = dUs; d.ldo = Fs; d.status = status;
-        MOE_STAGE(ST_FC2S_DGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
-        {
+        if (nv) { d.nv = 1; d.gA = ams + AMAX_DY; d.gB = wqs.amax + 1; }
+        MOE_STAGE(ST_FC2S_DGRAD, gemm(d));
+        if (nv) {
+            const moe_status_t r = nvq(nv_job(L, T_, meta, poff, E, true, Hs, Fs, nullptr, nullptr, ws + L.hsTq,
+                                              ws + L.shsT, ams + AMAX_H), ST_QT);
+            if (r != MOE_OK) return r;
+        } else {
             MxQuantJob j{Hs, nullptr, Tp, Fs, Tp, nullptr, nullptr, ws + L.hsTq, ws + L.shsT, 1};
             j.rows_valid = T_;
             MOE_STAGE(ST_QT, launch_mx_quant(j, s));
@@ -1213,8 +1395,19 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
         d.B0 = ws + L.dYsTq; d.ldb = Tp; d.XB0 = ws + L.sdYsT;
         d.rows_cap = Tp;
         d.O0 = a->dWs_down; d.ldo = H; d.o_estride = (long long)Fs * H; d.status = status;
-        MOE_STAGE(ST_FC2S_WGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
-        {
+        if (nv) { d.nv = 1; d.gA = ams + AMAX_H; d.gB = ams + AMAX_DY; }
+        MOE_STAGE(ST_FC2S_WGRAD, gemm(d));
+        if (nv) {
+            float* g = ams + AMAX_DAU;
+            const NvQuantJob ja = nv_job(L, T_, meta, poff, E, true, dAs, Fs, ws + L.dAsq, ws + L.sdAs,
+                                         ws + L.dAsTq, ws + L.sdAsT, g);
+            const NvQuantJob ju = nv_job(L, T_, meta, poff, E, true, dUs, Fs, ws + L.dUsq, ws + L.sdUs,
+                                         ws + L.dUsTq, ws + L.sdUsT, g);
+            MOE_STAGE(ST_AMAX, launch_nv_amax(ja, g, s));
+            MOE_STAGE(ST_AMAX, launch_nv_amax(ju, g, s));
+            MOE_STAGE(ST_QROWS, launch_nv_quant(ja, s));
+            MOE_STAGE(ST_QROWS, launch_nv_quant(ju, s));
+        } else {
             MxQuantJob ja{dAs, nullptr, Tp, Fs, Tp, ws + L.dAsq, ws + L.sdAs, ws + L.dAsTq, ws + L.sdAsT, 1};
             ja.rows_valid = T_;
             MOE_STAGE(ST_QROWS, launch_mx_quant(ja, s));
@@ -1230,8 +1423,12 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
         d.B0 = wqs.q[3]; d.B1 = wqs.q[4]; d.ldb = Fs; d.b_rows = H; d.b_kmajor = 1;
         d.XB0 = xs(wqs.s[3]); d.XB1 = xs(wqs.s[4]);
         d.O0 = dXs; d.ldo = H; d.status = status;
-        MOE_STAGE(ST_FC1S_DGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
-        {
+        if (nv) { d.nv = 1; d.gA = ams + AMAX_DAU; d.gB = wqs.amax; }
+        MOE_STAGE(ST_FC1S_DGRAD, gemm(d));
+        if (nv) {
+            MOE_STAGE(ST_QT, launch_nv_quant(nv_job(L, T_, meta, poff, E, true, static_cast<const T*>(a->x), H,
+                                                    nullptr, nullptr, ws + L.xTq, ws + L.sxT, amx + E), s));
+        } else {
             MxQuantJob j{static_cast<const T*>(a->x), nullptr, Tp, H, Tp, nullptr, nullptr, ws + L.xTq,
                          ws + L.sxT, 1};
             j.rows_valid = T_;
@@ -1245,7 +1442,8 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
         d.XB0 = ws + L.sdAsT; d.XB1 = ws + L.sdUsT;
         d.rows_cap = Tp;
         d.O0 = a->dWs_gate; d.O1 = a->dWs_up; d.ldo = Fs; d.o_estride = (long long)H * Fs; d.status = status;
-        MOE_STAGE(ST_FC1S_WGRAD, launch_gemm_mx(d, L.MT_max, p->num_sms, s));
+        if (nv) { d.nv = 1; d.gA = amx + E; d.gB = ams + AMAX_DAU; }
+        MOE_STAGE(ST_FC1S_WGRAD, gemm(d));
     }
     MOE_STAGE(ST_ROUTER_WGRAD, launch_router_wgrad<T>(static_cast<const T*>(a->x), slotof, poff, meta,
                                    L.MT_max, dz, H, E, k, reinterpret_cast<float*>(ws + L.wrpart), a->dWr, s));
@@ -1292,7 +1490,7 @@ moe_status_t moe_forward(moe_plan_t plan, int T, const moe_fwd_args_t* a, void* 
         return forward_impl<float>(plan, T, a, static_cast<uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
     if (plan->cfg.dtype == MOE_FP8_BLOCK)
         return forward_fp8_impl(plan, T, a, static_cast<uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
-    if (plan->cfg.dtype == MOE_MXFP8)
+    if (bs_recipe(plan->cfg))
         return forward_mx_impl(plan, T, a, static_cast<uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
     return forward_impl<__nv_bfloat16>(plan, T, a, static_cast<uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
 }
@@ -1324,7 +1522,7 @@ moe_status_t moe_backward(moe_plan_t plan, int T, const moe_bwd_args_t* a, const
         return backward_impl<float>(plan, T, a, static_cast<const uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
     if (plan->cfg.dtype == MOE_FP8_BLOCK)
         return backward_fp8_impl(plan, T, a, static_cast<const uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
-    if (plan->cfg.dtype == MOE_MXFP8)
+    if (bs_recipe(plan->cfg))
         return backward_mx_impl(plan, T, a, static_cast<const uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
     return backward_impl<__nv_bfloat16>(plan, T, a, static_cast<const uint8_t*>(saved), static_cast<uint8_t*>(ws), s);
 }
@@ -1419,4 +1617,28 @@ moe_status_t moe_mx_quantize(int rows, int cols, const void* in, uint8_t* codes,
     j.grp = rows;
     const cudaError_t e = launch_mx_quant(j, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_nv_quantize(int rows, int cols, const void* in, float* amax, uint8_t* codes, uint8_t* scales,
+                             uint8_t* codes_t, uint8_t* scales_t, moe_stream_t stream)
+{
+    if (rows < 1 || cols < 1 || rows % 128 || cols % 128 || !in || !amax) return MOE_ERR_INVALID_ARG;
+    if ((codes == nullptr) != (scales == nullptr) || (codes_t == nullptr) != (scales_t == nullptr) ||
+        (!codes && !codes_t))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(in) || (codes && !aligned16(codes)) || (codes_t && !aligned16(codes_t)) ||
+        (reinterpret_cast<uintptr_t>(amax) & 3u))
+        return MOE_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    NvQuantJob j;
+    memset(&j, 0, sizeof j);
+    j.in = static_cast<const __nv_bfloat16*>(in);
+    j.rows_max = j.rows_cap = j.grp = rows;
+    j.C = cols;
+    j.q = codes; j.sf = scales; j.qc = codes_t; j.sfc = scales_t;
+    j.gather_k = 1;
+    j.amax = amax;
+    if (cudaMemsetAsync(amax, 0, sizeof(float), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_nv_amax(j, amax, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return launch_nv_quant(j, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

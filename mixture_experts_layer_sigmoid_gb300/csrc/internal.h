@@ -104,6 +104,11 @@ struct GemmDesc {
     const uint8_t* XA0; const uint8_t* XA1; const uint8_t* XB0; const uint8_t* XB1;
     // MXFP8 SWIGLU_FWD: also the MX row codes [rows][N] of h (O2) and their atoms
     uint8_t* Qrows; uint8_t* Qatoms;
+    // NVFP4 operands (nv != 0; the same atoms fields, 64-value K chunks): the
+    // largest magnitude of each expert's A and B tensors (index 0 for a
+    // dense group), whose tensor scales the epilogue divides out
+    int nv;
+    const float* gA; const float* gB;
     // memory-efficient permutation (gates != null): g of permuted row r is
     // gates[slot_of[r]]. SWIGLU_FWD stores O2 = g h; SWIGLU_BWD treats the
     // accumulator as dh', writes dA, dU of dh = g dh', O2 = g h (if O2 is
@@ -225,8 +230,43 @@ struct MxQuantJob {
     int rows_valid = 0;   // > 0: rows from here on (up to rows_max) read as zeros
 };
 cudaError_t launch_mx_quant(const MxQuantJob& j, cudaStream_t s);
+
+// NVFP4 quantisation (quant_nv.cu, encoding in nv.cuh): [rows][C] bf16 in
+// 128 x 128 tiles -> row codes q[rows][C/2] (16-value blocks along rows)
+// and/or transposed codes qc (16-row blocks down columns, per group of grp
+// rows: column c of group g at qc[((g C + c) grp + r) / 2]), each with 512-byte
+// scale atoms per 128-row tile and 64-value K chunk. The tensor of a
+// 128-row tile (for its fp32 scale 2688 / amax[tensor]): the padded segment
+// of seg_off (nseg + 1 offsets) holding it, else row / seg_rows (seg_rows 0:
+// one tensor). Gather and rows_valid as in MxQuantJob.
+struct NvQuantJob {
+    const __nv_bfloat16* in;
+    const int* rows_dev;     // rows to visit (device), or null: rows_max
+    int rows_max, C, rows_cap;
+    uint8_t* q; uint8_t* sf;
+    uint8_t* qc; uint8_t* sfc;
+    int grp;
+    const int* seg_off; int nseg;
+    int seg_rows;
+    const float* amax;       // quantisation: per-tensor largest magnitudes
+    const int* gather_slot; int gather_k;
+    int rows_valid;
+};
+// atomicMax of each tile's largest magnitude into amax[tensor] (amax zeroed
+// by the caller)
+cudaError_t launch_nv_amax(const NvQuantJob& j, float* amax, cudaStream_t s);
+cudaError_t launch_nv_quant(const NvQuantJob& j, cudaStream_t s);
+// The permuted rows' NVFP4 row codes (K = H) from x: each expert's maximum
+// over the rows it keeps (amax zeroed by the caller), then each token's k
+// rows in their experts' tensor scales; pad rows get zero codes.
+cudaError_t launch_nv_permute(const __nv_bfloat16* x, const int* topk, const int* row_of, const int* poff,
+                              const int* counts, const int* kept, int T_, int H, int E, int k, float* amax,
+                              uint8_t* Xq, uint8_t* sfX, cudaStream_t s);
 cudaError_t launch_gemm_mx(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s);
 cudaError_t gemm_mx_prepare(int device);
+// NVFP4 operands (d.nv, d.gA, d.gB set; every B K-major)
+cudaError_t launch_gemm_nv(const GemmDesc& d, int max_m_tiles, int num_sms, cudaStream_t s);
+cudaError_t gemm_nv_prepare(int device);
 
 // Configuration and device of a plan; false for a null plan.
 bool plan_info(const moe_plan_s* plan, moe_config_t* cfg, int* device);

@@ -118,7 +118,7 @@ def permutation(seed: int, tensor_id: int, n: int) -> torch.Tensor:
 
 # ---------------------------------------------------------------- workloads
 SOFTMAX, SIGMOID = 0, 1
-FP32, BF16, FP8_BLOCK, MXFP8 = 0, 1, 2, 3
+FP32, BF16, FP8_BLOCK, MXFP8, NVFP4 = 0, 1, 2, 3, 4
 
 # tensor ids within one seed
 TID = dict(x=1, Wr=2, b=3, Wg=4, Wu=5, Wd=6, Wsg=7, Wsu=8, Wsd=9, dY=10, perm=11)
@@ -174,6 +174,12 @@ WORKLOADS: Dict[str, Workload] = {
     # the bf16 workload's inputs
     "deepseek_v3_mxfp8": Workload("deepseek_v3_mxfp8", T=8192, H=7168, E=256, k=8, F=2048, Fs=2048,
                                   score=SIGMOID, dtype=MXFP8, bias="normal", seed=2000),
+    # the same two shapes in the NVFP4 recipe (E2M1 values, 1x16 blocks with
+    # E4M3 scales, one fp32 scale per expert tensor)
+    "qwen3_235b_nvfp4": Workload("qwen3_235b_nvfp4", T=16384, H=4096, E=128, k=8, F=1536,
+                                 dtype=NVFP4, bias="zipf", seed=4000),
+    "deepseek_v3_nvfp4": Workload("deepseek_v3_nvfp4", T=8192, H=7168, E=256, k=8, F=2048, Fs=2048,
+                                  score=SIGMOID, dtype=NVFP4, bias="normal", seed=2000),
 }
 
 
@@ -205,7 +211,7 @@ def make_inputs(w: Workload, device="cpu", with_grad_out: bool = True) -> Dict[s
 
     Layouts (row-major): x T×H; Wr H×E fp32; b E fp32; Wg, Wu E×H×F;
     Wd E×F×H; Wsg, Wsu H×Fs; Wsd Fs×H; dY T×H."""
-    dt = w.torch_dtype if w.dtype not in (FP8_BLOCK, MXFP8) else torch.bfloat16
+    dt = w.torch_dtype if w.dtype not in (FP8_BLOCK, MXFP8, NVFP4) else torch.bfloat16
     g = {}
     g["x"] = normal_tensor(w.seed, TID["x"], (w.T, w.H), 1.0, dt, device)
     g["Wr"] = normal_tensor(w.seed, TID["Wr"], (w.H, w.E), router_std(w.H), torch.float32, device)

@@ -92,6 +92,32 @@ def test_mxfp8_with_shared_expert_passes_validation(lib):
         assert lib.moe_plan_destroy(plan) == moe.MOE_OK
 
 
+def test_nvfp4_needs_256_multiples(lib):
+    """NVFP4 data GEMMs take 256-value k blocks: H, F and Fs must be
+    multiples of 256 (UNSUPPORTED otherwise, before any device work)."""
+    for bad in (dict(H=384), dict(F=384), dict(Fs=128)):
+        plan = ctypes.c_void_p()
+        assert lib.moe_plan_create(ctypes.byref(_cfg(dtype=4, **bad)), 0,
+                                   ctypes.byref(plan)) == moe.MOE_ERR_UNSUPPORTED
+        assert plan.value is None
+    plan = ctypes.c_void_p()
+    st = lib.moe_plan_create(ctypes.byref(_cfg(dtype=4, Fs=256, capacity_factor=1.0)), 0, ctypes.byref(plan))
+    assert st in (moe.MOE_OK, moe.MOE_ERR_CUDA) or (st == moe.MOE_ERR_UNSUPPORTED and not _has_sm103())
+    if st == moe.MOE_OK:
+        assert lib.moe_plan_destroy(plan) == moe.MOE_OK
+
+
+def test_nv_quantize_validates_arguments(lib):
+    buf = ctypes.create_string_buffer(64)
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    q = lambda *a: lib.moe_nv_quantize(*a, None)
+    assert q(100, 128, p, p, p, p, None, None) == moe.MOE_ERR_INVALID_ARG   # rows % 128
+    assert q(128, 128, None, p, p, p, None, None) == moe.MOE_ERR_INVALID_ARG  # no input
+    assert q(128, 128, p, None, p, p, None, None) == moe.MOE_ERR_INVALID_ARG  # no amax
+    assert q(128, 128, p, p, p, None, None, None) == moe.MOE_ERR_INVALID_ARG  # codes without scales
+    assert q(128, 128, p, p, None, None, None, None) == moe.MOE_ERR_INVALID_ARG  # no output
+
+
 def test_null_arguments(lib):
     assert lib.moe_plan_create(None, 0, None) == moe.MOE_ERR_INVALID_ARG
     s, w = ctypes.c_size_t(), ctypes.c_size_t()

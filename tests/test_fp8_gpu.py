@@ -117,9 +117,10 @@ def fp8_layer_parity(w, fold=False, capacity_factor=0.0):
     inp = mi.make_inputs(w)
     g = upload(inp)
     mx = w.dtype == mi.MXFP8
+    nv = w.dtype == mi.NVFP4
     layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score,
-                         dtype=moe.MOE_MXFP8 if mx else moe.MOE_FP8_BLOCK, fold_gates=fold,
-                         capacity_factor=capacity_factor, Fs=w.Fs)
+                         dtype=moe.MOE_NVFP4 if nv else moe.MOE_MXFP8 if mx else moe.MOE_FP8_BLOCK,
+                         fold_gates=fold, capacity_factor=capacity_factor, Fs=w.Fs)
     ws = (g["Wsg"], g["Wsu"], g["Wsd"])
     y, rt = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"], *ws, routing=True)
     gr = layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], *ws)
@@ -141,20 +142,31 @@ def fp8_layer_parity(w, fold=False, capacity_factor=0.0):
     ref = oracle.layer_fp8(d["x"], d["Wr"], d["Wg"], d["Wu"], d["Wd"], r["topk"], r["gates"],
                            r["scores"], w.score, d["dY"], Wsg=d.get("Wsg"), Wsu=d.get("Wsu"),
                            Wsd=d.get("Wsd"), fold=fold,
-                           recipe=oracle.RECIPE_MX if mx else oracle.RECIPE_BLOCK, keep=keep)
+                           recipe=oracle.RECIPE_NV if nv else oracle.RECIPE_MX if mx else oracle.RECIPE_BLOCK,
+                           keep=keep)
     rep = {}
+
+    def check(gname, got, want):
+        rl2, mr = rel_errors(got, want)
+        if nv:
+            # NVFP4: an intermediate's E2M1 code one step off (a one-ulp bf16
+            # difference on a rounding boundary) shifts a row of the output
+            # (bounds in test_nv_gpu's docstring)
+            rms = np.sqrt(np.mean(np.square(want))) if want.size else 0.0
+            far = float(np.mean(np.abs(got - want) > 1.5e-1 * rms)) if rms > 0 else 0.0
+            rep[gname] = (rl2, mr, far)
+            assert rl2 <= 4e-2 and far <= 1e-3 and mr <= 1.0, (gname, rl2, mr, far)
+        else:
+            rep[gname] = (rl2, mr)
+            assert rl2 <= 4e-2 and mr <= 1.5e-1, (gname, rl2, mr)
+
     for gname, oname in (("y", "y"), ("dX", "dX")):
-        got = to_np(y if gname == "y" else gr[gname])
-        rl2, mr = rel_errors(got, ref[oname])
-        rep[gname] = (rl2, mr)
-        assert rl2 <= 4e-2 and mr <= 1.5e-1, (gname, rl2, mr)
+        check(gname, to_np(y if gname == "y" else gr[gname]), ref[oname])
     shared = (("dWs_gate", "dWsg"), ("dWs_up", "dWsu"), ("dWs_down", "dWsd")) if w.Fs else ()
     for gname, oname in (("dWr", "dWr"), ("dW_gate", "dWg"), ("dW_up", "dWu"), ("dW_down", "dWd")) + shared:
         got = to_np(gr[gname])
         want = ref[oname]
-        rl2, mr = rel_errors(got, want)
-        rep[gname] = (rl2, mr)
-        assert rl2 <= 4e-2 and mr <= 1.5e-1, (gname, rl2, mr)
+        check(gname, got, want)
         blocks = zip(got.T, want.T) if gname == "dWr" else zip(got, want)
         for gb, wb in blocks:
             nw = np.linalg.norm(wb)
@@ -162,7 +174,7 @@ def fp8_layer_parity(w, fold=False, capacity_factor=0.0):
                 assert np.all(gb == 0)
             else:
                 assert np.linalg.norm(gb - wb) / nw <= 4e-2, gname
-    write_report(f"{w.name} T{w.T} H{w.H} E{w.E} k{w.k} F{w.F} {'mxfp8' if mx else 'fp8'}"
+    write_report(f"{w.name} T{w.T} H{w.H} E{w.E} k{w.k} F{w.F} {'nvfp4' if nv else 'mxfp8' if mx else 'fp8'}"
                  + (" fold" if fold else "") + (f" capacity {capacity_factor}" if capacity_factor else ""),
                  rep)
     return rep

@@ -248,3 +248,91 @@ def test_full_size_deepseek_mxfp8_layer():
         assert np.array_equal(q, oc_r) and np.array_equal(_atoms_to_scales(sq, R, C), os_r)
 
     _full_size_fp8_case("deepseek_v3_mxfp8", moe.MOE_MXFP8, oracle.RECIPE_MX, check)
+
+
+def _full_size_nv_case(wl):
+    """NVFP4 at full size. A token's rows no longer depend on its own values
+    alone (each expert tensor's fp32 scale comes from the expert's whole
+    segment), so the oracle checks what it can compute exactly: the weight
+    quantiser bit for bit on sampled experts in both orientations, and the
+    weight gradients of the coldest non-empty expert -- every token routed
+    to it is given to the oracle's NVFP4 layer, so that expert's segment
+    (its tensors and tensor scales) is complete -- within the NVFP4 bounds
+    of test_nv_gpu; sampled y and dX rows are checked against the exact
+    layer's rows within the E2M1 error scale (rel L2 < 0.4, the bound the
+    oracle's own NVFP4 layer meets against the exact one)."""
+    import mixture_experts_layer_sigmoid_gb300 as moe
+    from test_nv_gpu import _atoms_to_scales, _nvq, _unpack
+    w = mi.WORKLOADS[wl]
+    g = mi.make_inputs(w, "cuda")
+    layer = moe.MoELayer(w.H, w.E, w.F, w.k, w.T, score=w.score, dtype=moe.MOE_NVFP4, Fs=w.Fs)
+    ws = (g["Wsg"], g["Wsu"], g["Wsd"])
+    y, rt = layer.forward(g["x"], g["Wr"], g["b"], g["Wg"], g["Wu"], g["Wd"], *ws, routing=True)
+    gr = layer.backward(g["dY"], g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], *ws)
+    torch.cuda.synchronize()
+    assert layer.status(w.T) == 0
+    assert torch.isfinite(y).all() and torch.isfinite(gr["dX"]).all()
+    x, dY, Wr, b = to_np(g["x"]), to_np(g["dY"]), to_np(g["Wr"]), to_np(g["b"])
+    r = oracle.route(x, Wr, b, w.k, w.score)
+    gt = rt["topk_idx"].cpu().numpy()
+    tie = (r["gap_set"] < TIE_REL) | (r["gap_order"] < TIE_REL)
+    mism = np.any(gt != r["topk"], axis=1)
+    assert not np.any(mism & ~tie)
+    if mism.any():
+        r = oracle.route(x, Wr, b, w.k, w.score, replay_topk=gt, replay_mask=mism)
+    counts = np.bincount(r["topk"].ravel(), minlength=w.E)
+    assert np.array_equal(rt["counts"].cpu().numpy(), counts)
+    hot = int(np.argmax(counts))
+    nonempty = np.nonzero(counts)[0]
+    cold = int(nonempty[np.argmin(counts[nonempty])])
+    for e in (0, hot):
+        W = g["Wg"][e].contiguous()
+        R, C = W.shape
+        amax, q, sq, qt, st = _nvq(W)
+        Wf = W.float().cpu().numpy()
+        oc_r, os_r, _ = oracle.nv_quantize(Wf, oracle.NV_ROWS)
+        oc_c, os_c, _ = oracle.nv_quantize(Wf, oracle.NV_COLS)
+        assert amax == np.abs(Wf).max()
+        assert np.array_equal(_unpack(q, R, C), oc_r) and np.array_equal(_atoms_to_scales(sq, R, C), os_r)
+        assert np.array_equal(_unpack(qt, C, R), oc_c.T) and np.array_equal(_atoms_to_scales(st, C, R), os_c.T)
+    # the coldest expert's weight gradients, its whole segment in the oracle
+    toks = np.nonzero((r["topk"] == cold).any(1))[0]
+    need = sorted(set(r["topk"][toks].ravel().tolist()))
+    renum = np.full(w.E, -1, np.int32)
+    renum[need] = np.arange(len(need), dtype=np.int32)
+    stack = lambda n: np.stack([to_np(g[n][e]) for e in need])
+    q = oracle.layer_fp8(x[toks], Wr[:, need], stack("Wg"), stack("Wu"), stack("Wd"), renum[r["topk"][toks]],
+                         r["gates"][toks], r["scores"][toks][:, need], w.score, dY[toks],
+                         recipe=oracle.RECIPE_NV)
+    report = {"cold_expert_rows": int(counts[cold])}
+    for gname, oname in (("dW_gate", "dWg"), ("dW_up", "dWu"), ("dW_down", "dWd")):
+        got = to_np(gr[gname][cold])
+        want = q[oname][renum[cold]]
+        rl2, mr = rel_errors(got, want)
+        rms = np.sqrt(np.mean(np.square(want)))
+        far = float(np.mean(np.abs(got - want) > 1.5e-1 * rms))
+        report[gname + "_cold"] = (rl2, mr, far)
+        assert rl2 <= 4e-2 and far <= 1e-3 and mr <= 1.0, (gname, rl2, mr, far)
+    # sampled rows against the exact layer, within the E2M1 error scale
+    rows = np.array(sorted({0, w.T - 1, int(toks[0])}))
+    needr = sorted(set(r["topk"][rows].ravel().tolist()))
+    We = oracle.ExpertWeights(w.E, {e: _bits(g["Wg"][e]) for e in needr},
+                              {e: _bits(g["Wu"][e]) for e in needr},
+                              {e: _bits(g["Wd"][e]) for e in needr},
+                              *(None if g[n] is None else _bits(g[n]) for n in ("Wsg", "Wsu", "Wsd")))
+    tr = oracle.token_rows(x[rows], dY[rows], Wr, We, r["topk"][rows], r["gates"][rows], r["scores"][rows],
+                           w.score)
+    for nm, got in (("y", to_np(y)[rows]), ("dX", to_np(gr["dX"])[rows])):
+        rl2, mr = rel_errors(got, tr[nm])
+        report[nm + "_rows_vs_exact"] = (rl2, mr)
+        assert 0.02 < rl2 < 0.4, (nm, rl2)
+    print(wl, report)
+    write_report(f"{wl} full size", report)
+
+
+def test_full_size_nvfp4_layer():
+    _full_size_nv_case("qwen3_235b_nvfp4")
+
+
+def test_full_size_deepseek_nvfp4_layer():
+    _full_size_nv_case("deepseek_v3_nvfp4")
