@@ -174,12 +174,14 @@ typedef struct {
                               over the sum of their scores). Indices outside
                               [0, E) are clamped and reported as
                               MOE_ERR_INVALID_ARG in the status word. */
-    const void*  weight_cache; /* optional in (FP8-recipe plans): expert
-                              weights quantised by moe_quantize_weights. When
-                              given, W_gate, W_up and W_down are not read (they
-                              may be NULL) and the call quantises none of the
-                              routed experts' weights (an MXFP8 layer's shared
-                              expert weights are still read and quantised);
+    const void*  weight_cache; /* optional in (quantised-expert plans:
+                              FP8_BLOCK, MXFP8, NVFP4): expert weights
+                              quantised by moe_quantize_weights. When given,
+                              W_gate, W_up and W_down are not read (they may
+                              be NULL) and the call quantises none of the
+                              routed experts' weights (an MXFP8 or NVFP4
+                              layer's shared expert weights are still read and
+                              quantised);
                               the matching moe_backward must be given the same
                               cache. Other dtypes: must be NULL. */
 } moe_fwd_args_t;
@@ -204,7 +206,7 @@ typedef struct {
     void*        dWs_gate; /* out, H×Fs act (NULL iff Fs == 0)                */
     void*        dWs_up;
     void*        dWs_down;
-    const void*  weight_cache; /* FP8 recipes: the cache given to the
+    const void*  weight_cache; /* quantised recipes: the cache given to the
                               forward (W_gate, W_up, W_down then unread), or
                               NULL when the forward quantised the bf16
                               weights itself. Other dtypes: NULL. */

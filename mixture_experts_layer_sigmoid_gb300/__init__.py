@@ -261,9 +261,10 @@ class MoELayer:
         return self.torch.cuda.current_stream(self.device).cuda_stream
 
     def quantize_weights(self, W_gate, W_up, W_down, cache=None):
-        """FP8 plans: the weight cache (a uint8 device tensor) holding the
-        E4M3 codes and scales of the expert weights; pass it as weight_cache
-        to forward and backward."""
+        """Quantised-expert plans (FP8_BLOCK, MXFP8, NVFP4): the weight cache
+        (a uint8 device tensor) holding the codes and scales of the expert
+        weights (NVFP4: also each expert's tensor maxima); pass it as
+        weight_cache to forward and backward."""
         t = self.torch
         n = moe_weight_cache_size(self.plan)
         if cache is None:
