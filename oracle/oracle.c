@@ -649,26 +649,26 @@ double oracle_e4m3_decode(unsigned char c)
     return s ? -v : v;
 }
 
-/* Nearest E4M3 code to f (ties to the even code), saturating to +-448. */
+/* Nearest E4M3 code to f (ties to the even code), saturating to +-448.
+ * Below 2^-6 the values are the subnormals m 2^-9 (m = 0..7; m = 8 is the
+ * smallest normal, code 8); above, a = 2^E (1 + m/8) with E = floor(log2 a),
+ * the code (E + 7) << 3 | m, a mantissa that rounds up to 8 carrying into
+ * the exponent. Every step is exact in double (power-of-two scaling of a
+ * float), rint rounds half to even. */
 unsigned char oracle_e4m3_encode(float f)
 {
     if (f != f) return 0x7F;
-    unsigned char sign = (f < 0.0f || (f == 0.0f && signbit(f))) ? 0x80 : 0x00;
+    unsigned char sign = signbit(f) ? 0x80 : 0x00;
     double a = fabs((double)f);
     if (a >= 448.0) return sign | 0x7E;
-    /* codes 0..126 are the finite non-negative values in increasing order */
-    int lo = 0, hi = 126;
-    while (lo < hi) {                      /* largest code with value <= a */
-        int mid = (lo + hi + 1) / 2;
-        if (oracle_e4m3_decode((unsigned char)mid) <= a) lo = mid; else hi = mid - 1;
-    }
-    int c = lo;
-    if (c < 126) {
-        double d0 = a - oracle_e4m3_decode((unsigned char)c);
-        double d1 = oracle_e4m3_decode((unsigned char)(c + 1)) - a;
-        if (d1 < d0 || (d1 == d0 && (c & 1))) c = c + 1;
-    }
-    return sign | (unsigned char)c;
+    if (a < 0.015625) return sign | (unsigned char)rint(ldexp(a, 9));
+    int p;
+    frexp(a, &p);                          /* a = g 2^p, g in [0.5, 1) */
+    int E = p - 1;
+    int m = (int)rint((ldexp(a, -E) - 1.0) * 8.0);
+    int code = ((E + 7) << 3) + m;         /* m = 8 carries into the exponent */
+    if (code > 0x7E) code = 0x7E;
+    return sign | (unsigned char)code;
 }
 
 /* v rounded to bfloat16 (via fp32, ties to even) */

@@ -39,6 +39,16 @@ def test_e4m3_encode_matches_torch_and_saturates():
     assert list(oracle.e4m3_encode(big)) == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE]
 
 
+def test_e4m3_encode_every_bf16_value_matches_torch():
+    """Every finite bf16 value within the E4M3 range, both signs."""
+    bits = np.arange(0x0000, 0x7F80, dtype=np.uint32)
+    vals = (bits << 16).view(np.float32)
+    vals = vals[vals <= 448.0]
+    vals = np.concatenate([vals, -vals])
+    ref = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(vals), ref)
+
+
 @pytest.mark.parametrize("mode", [oracle.FP8_ROWS, oracle.FP8_TILES, oracle.FP8_COLS])
 def test_block_quantiser_exactness_and_locality(mode):
     rng = np.random.default_rng(1)
