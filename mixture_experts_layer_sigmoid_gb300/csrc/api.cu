@@ -40,10 +40,12 @@ struct Layout {
     size_t wcache_s, xsq, sxs, hsq, shs, dYsq, sdYs, dYsTq, sdYsT, hsTq, shsT, dAsq, sdAs, dUsq, sdUs,
         dAsTq, sdAsT, dUsTq, sdUsT, xTq, sxT;
     size_t amax;   // NVFP4 tensor maxima (workspace)
-    size_t amax_x; // NVFP4: the maxima of x's tensors (saved: each expert's rows, then the shared expert's)
+    size_t amax_x; // NVFP4 (saved): the maxima of x's tensors (each expert's rows, then the shared
+                   // expert's), then those of h, for the backward
 };
-// NVFP4 tensor maxima in the workspace: h, dY, [dA | dU] per expert, then the
-// shared expert's three (x's maxima are kept in the saved buffer)
+// NVFP4 tensor maxima in the workspace: h (the backward's g h recomputed
+// with folded gates), dY, [dA | dU] per expert, then the shared expert's
+// three (the forward's x and h maxima are kept in the saved buffer)
 enum { AMAX_H = 0, AMAX_DY = 1, AMAX_DAU = 2, kAmaxKinds = 3 };
 
 // the quantised-expert recipes; the block-scaled ones (MXFP8, NVFP4) share
@@ -175,7 +177,7 @@ Layout make_layout(const moe_config_t& c, int T)
     const bool mxs = bs && c.Fs > 0;
     L.Tp = (int)align_up((size_t)T, 128);
     L.wcache_s = take(mxs ? cache_layout(shared_config(c)).bytes : 0);
-    L.amax_x = take(nv ? sizeof(float) * ((size_t)c.E + 1) : 0);
+    L.amax_x = take(nv ? sizeof(float) * 2 * ((size_t)c.E + 1) : 0);
     L.saved_bytes = o;
     o = 0;
     L.status = take(256);
@@ -1036,7 +1038,6 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
     const Layout L = make_layout(c, T_);
     const int H = c.H, E = c.E, k = c.top_k, F = c.F, Rp = L.Rp_max;
     const bool nv = c.dtype == MOE_NVFP4;
-    float* am = nv ? reinterpret_cast<float*>(ws + L.amax) : nullptr;   // [3][E], then the shared expert's
     auto gemm = [&](const GemmDesc& g) {
         return nv ? launch_gemm_nv(g, L.MT_max, p->num_sms, s) : launch_gemm_mx(g, L.MT_max, p->num_sms, s);
     };
@@ -1071,12 +1072,13 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
     if (slotlive) MOE_CUDA(cudaMemsetAsync(slotlive, 0xFF, sizeof(int) * (size_t)L.Rp_max, s));
     MOE_STAGE(ST_INDEX, launch_index(topk, reinterpret_cast<int*>(ws + L.blkbase), T_, E, k, rowof, slotof, s,
                                      poff, kept, slotlive));
-    float* amx = nv ? reinterpret_cast<float*>(sv + L.amax_x) : nullptr;   // x's maxima, kept for backward
+    // x's and h's maxima, kept for the backward
+    float* amx = nv ? reinterpret_cast<float*>(sv + L.amax_x) : nullptr;
+    float* amh = nv ? amx + E + 1 : nullptr;
     if (nv) {
         // each expert's maximum over the rows it keeps, then every token's k
         // rows in their experts' tensor scales (x read twice, not gathered)
-        MOE_CUDA(cudaMemsetAsync(am, 0, sizeof(float) * kAmaxKinds * ((size_t)E + 1), s));
-        MOE_CUDA(cudaMemsetAsync(amx, 0, sizeof(float) * ((size_t)E + 1), s));
+        MOE_CUDA(cudaMemsetAsync(amx, 0, sizeof(float) * 2 * ((size_t)E + 1), s));
         MOE_STAGE(ST_PERMUTE, launch_nv_permute(x, topk, rowof, poff, counts, kept, T_, H, E, k, amx, sv + L.Xq,
                                                 sv + L.sX, s));
     } else {
@@ -1097,19 +1099,16 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
     d.XB0 = xs(wq.s[0]); d.XB1 = xs(wq.s[1]);
     d.O0 = A; d.O1 = U; d.O2 = Hh; d.ldo = F; d.status = status;
     if (L.fold) { d.gates = gates; d.slot_of = slotof; }   // Hh = g silu(A) U
-    if (nv) {   // [Wg^T | Wu^T] K-major; h is quantised after its maximum is known
-        d.nv = 1; d.gA = amx; d.gB = wq.amax;
+    if (nv) {   // [Wg^T | Wu^T] K-major; the epilogue folds each expert's max |h| into amh
+        d.nv = 1; d.gA = amx; d.gB = wq.amax; d.amaxO = amh;
         d.ldb = H; d.b_rows = E * F; d.b_kmajor = 1;
     } else {
         d.Qrows = ws + L.hq; d.Qatoms = ws + L.sh;          // fc2's A operand, from the epilogue
     }
     MOE_STAGE(ST_FC1, gemm(d));
-    if (nv) {
-        NvQuantJob j = nv_job(L, T_, meta, poff, E, false, Hh, F, ws + L.hq, ws + L.sh, nullptr, nullptr,
-                              am + AMAX_H * E);
-        MOE_STAGE(ST_AMAX, launch_nv_amax(j, am + AMAX_H * E, s));
-        MOE_STAGE(ST_QROWS, launch_nv_quant(j, s));
-    }
+    if (nv)
+        MOE_STAGE(ST_QROWS, launch_nv_quant(nv_job(L, T_, meta, poff, E, false, Hh, F, ws + L.hq, ws + L.sh, nullptr,
+                                                   nullptr, amh), s));
     memset(&d, 0, sizeof d);
     d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
     d.N = H; d.K = F; d.E = E;
@@ -1118,7 +1117,7 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
     d.A0 = ws + L.hq; d.lda = F; d.a_rows = Rp; d.XA0 = ws + L.sh;
     d.B0 = wq.q[2]; d.ldb = H; d.b_rows = E * F; d.XB0 = xs(wq.s[2]); d.b_kmajor = 0;
     if (nv) {   // Wd^T K-major
-        d.nv = 1; d.gA = am + AMAX_H * E; d.gB = wq.amax + E;
+        d.nv = 1; d.gA = amh; d.gB = wq.amax + E;
         d.ldb = F; d.b_rows = E * H; d.b_kmajor = 1;
     }
     d.O0 = Yp; d.ldo = H; d.status = status;
@@ -1135,7 +1134,6 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
         T* Hs = reinterpret_cast<T*>(sv + L.Hs);
         Ys = reinterpret_cast<T*>(ws + L.Ys);
         MOE_STAGE(ST_WQUANT, quantize_weights(cs, a->Ws_gate, a->Ws_up, a->Ws_down, wqs, s));
-        float* ams = nv ? am + kAmaxKinds * E : nullptr;   // the shared expert's h, dY, [dA | dU]
         if (nv) {
             NvQuantJob j = nv_job(L, T_, meta, poff, E, true, x, H, ws + L.xsq, ws + L.sxs, nullptr, nullptr,
                                   amx + E);
@@ -1154,25 +1152,22 @@ static moe_status_t forward_mx_impl(moe_plan_t p, int T_, const moe_fwd_args_t* 
         d.XB0 = xs(wqs.s[0]); d.XB1 = xs(wqs.s[1]);
         d.O0 = As; d.O1 = Us; d.O2 = Hs; d.ldo = Fs; d.status = status;
         if (nv) {
-            d.nv = 1; d.gA = amx + E; d.gB = wqs.amax;
+            d.nv = 1; d.gA = amx + E; d.gB = wqs.amax; d.amaxO = amh + E;
             d.ldb = H; d.b_rows = Fs; d.b_kmajor = 1;
         } else {
             d.Qrows = ws + L.hsq; d.Qatoms = ws + L.shs;          // shared fc2's A operand
         }
         MOE_STAGE(ST_FC1S, gemm(d));
-        if (nv) {
-            NvQuantJob j = nv_job(L, T_, meta, poff, E, true, Hs, Fs, ws + L.hsq, ws + L.shs, nullptr, nullptr,
-                                  ams + AMAX_H);
-            MOE_STAGE(ST_AMAX, launch_nv_amax(j, ams + AMAX_H, s));
-            MOE_STAGE(ST_QROWS, launch_nv_quant(j, s));
-        }
+        if (nv)
+            MOE_STAGE(ST_QROWS, launch_nv_quant(nv_job(L, T_, meta, poff, E, true, Hs, Fs, ws + L.hsq, ws + L.shs,
+                                                       nullptr, nullptr, amh + E), s));
         memset(&d, 0, sizeof d);
         d.sched = SCHED_ROWS; d.epi = EPI_STORE; d.dual = DUAL_NONE;
         d.N = H; d.K = Fs; d.E = 1; d.dense_rows = T_;
         d.A0 = ws + L.hsq; d.lda = Fs; d.a_rows = Tp; d.XA0 = ws + L.shs;
         d.B0 = wqs.q[2]; d.ldb = H; d.b_rows = Fs; d.XB0 = xs(wqs.s[2]); d.b_kmajor = 0;
         if (nv) {
-            d.nv = 1; d.gA = ams + AMAX_H; d.gB = wqs.amax + 1;
+            d.nv = 1; d.gA = amh + E; d.gB = wqs.amax + 1;
             d.ldb = Fs; d.b_rows = H; d.b_kmajor = 1;
         }
         d.O0 = Ys; d.ldo = H; d.status = status;
@@ -1239,6 +1234,12 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
         return MOE_OK;
     };
     if (nv) MOE_CUDA(cudaMemsetAsync(am, 0, sizeof(float) * kAmaxKinds * ((size_t)E + 1), s));
+    // the forward's x and h maxima
+    const float* amx = nv ? reinterpret_cast<const float*>(sv + L.amax_x) : nullptr;
+    const float* amh = nv ? amx + E + 1 : nullptr;
+    // h of the fc2 weight gradient: the forward's, or g h recomputed by the
+    // fc2-dgrad epilogue (folded gates), which also takes its maxima
+    const float* amh_b = nv ? (L.fold ? am + AMAX_H * E : amh) : nullptr;
 
     MOE_CUDA(cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s));
     if (L.fold)
@@ -1268,15 +1269,18 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
         d.gates = gates; d.slot_of = slotof; d.dg_part = dgpart; d.dg_ld = F / 64;
         d.O2 = Hh;   // g h, recomputed for the fc2 weight gradient
     }
-    if (nv) { d.nv = 1; d.gA = am + AMAX_DY * E; d.gB = wq.amax + E; }
+    if (nv) {   // the epilogue folds each expert's max |dA|, |dU| (and |g h|) into the workspace
+        d.nv = 1; d.gA = am + AMAX_DY * E; d.gB = wq.amax + E;
+        d.amaxO = am + AMAX_DAU * E;
+        if (L.fold) d.amaxO2 = am + AMAX_H * E;
+    }
     MOE_STAGE(ST_FC2_DGRAD, gemm(d));
     if (L.fold)
         MOE_STAGE(ST_GATEDZ, launch_gate_dz(dgpart, F / 64, rowof, gates, selsc, T_, k, c.score, dz, s));
     // fc2 wgrad: dWd[e] = h_e^T dYp_e
     if (nv) {
-        const moe_status_t r = nvq(nv_job(L, T_, meta, poff, E, false, Hh, F, nullptr, nullptr, ws + L.hTq,
-                                          ws + L.shT, am + AMAX_H * E), ST_QT);
-        if (r != MOE_OK) return r;
+        MOE_STAGE(ST_QT, launch_nv_quant(nv_job(L, T_, meta, poff, E, false, Hh, F, nullptr, nullptr, ws + L.hTq,
+                                                ws + L.shT, amh_b), s));
     } else {
         MxQuantJob j{Hh, meta + 1, Rp, F, Rp, nullptr, nullptr, ws + L.hTq, ws + L.shT, 1};
         MOE_STAGE(ST_QT, launch_mx_quant(j, s));
@@ -1290,19 +1294,15 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
     d.B0 = ws + L.dYpTq; d.ldb = Rp; d.XB0 = ws + L.sdYpT;
     d.rows_cap = Rp; d.expert_order = eorder;
     d.O0 = a->dW_down; d.ldo = H; d.o_estride = (long long)F * H; d.status = status;
-    if (nv) { d.nv = 1; d.gA = am + AMAX_H * E; d.gB = am + AMAX_DY * E; }
+    if (nv) { d.nv = 1; d.gA = amh_b; d.gB = am + AMAX_DY * E; }
     MOE_STAGE(ST_FC2_WGRAD, gemm(d));
     // dA, dU once each: row codes (fc1 dgrad, K = F) and transposed column codes (fc1 wgrad)
-    if (nv) {   // one tensor [dA | dU] per expert
-        float* g = am + AMAX_DAU * E;
-        const NvQuantJob ja = nv_job(L, T_, meta, poff, E, false, dA, F, ws + L.dAq, ws + L.sdA, ws + L.dATq,
-                                     ws + L.sdAT, g);
-        const NvQuantJob ju = nv_job(L, T_, meta, poff, E, false, dU, F, ws + L.dUq, ws + L.sdU, ws + L.dUTq,
-                                     ws + L.sdUT, g);
-        MOE_STAGE(ST_AMAX, launch_nv_amax(ja, g, s));
-        MOE_STAGE(ST_AMAX, launch_nv_amax(ju, g, s));
-        MOE_STAGE(ST_QROWS, launch_nv_quant(ja, s));
-        MOE_STAGE(ST_QROWS, launch_nv_quant(ju, s));
+    if (nv) {   // one tensor [dA | dU] per expert, its maxima from the fc2-dgrad epilogue
+        const float* g = am + AMAX_DAU * E;
+        MOE_STAGE(ST_QROWS, launch_nv_quant(nv_job(L, T_, meta, poff, E, false, dA, F, ws + L.dAq, ws + L.sdA,
+                                                   ws + L.dATq, ws + L.sdAT, g), s));
+        MOE_STAGE(ST_QROWS, launch_nv_quant(nv_job(L, T_, meta, poff, E, false, dU, F, ws + L.dUq, ws + L.sdU,
+                                                   ws + L.dUTq, ws + L.sdUT, g), s));
     } else {
         MxQuantJob ja{dA, meta + 1, Rp, F, Rp, ws + L.dAq, ws + L.sdA, ws + L.dATq, ws + L.sdAT, 1};
         MOE_STAGE(ST_QROWS, launch_mx_quant(ja, s));
@@ -1322,7 +1322,6 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
     if (nv) { d.nv = 1; d.gA = am + AMAX_DAU * E; d.gB = wq.amax; }
     MOE_STAGE(ST_FC1_DGRAD, gemm(d));
     // fc1 wgrad: the permuted rows are token rows of x (no bf16 copy of them is kept)
-    const float* amx = nv ? reinterpret_cast<const float*>(sv + L.amax_x) : nullptr;   // from the forward
     if (nv) {
         NvQuantJob j = nv_job(L, T_, meta, poff, E, false, static_cast<const T*>(a->x), H, nullptr, nullptr,
                               ws + L.XpTq, ws + L.sXpT, amx);
@@ -1377,12 +1376,11 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
         d.A0 = ws + L.dYsq; d.lda = H; d.a_rows = Tp; d.XA0 = ws + L.sdYs;
         d.B0 = wqs.q[5]; d.ldb = H; d.b_rows = Fs; d.XB0 = xs(wqs.s[5]); d.b_kmajor = 1;
         d.X0 = As; d.X1 = Us; d.O0 = dAs; d.O1 = dUs; d.ldo = Fs; d.status = status;
-        if (nv) { d.nv = 1; d.gA = ams + AMAX_DY; d.gB = wqs.amax + 1; }
+        if (nv) { d.nv = 1; d.gA = ams + AMAX_DY; d.gB = wqs.amax + 1; d.amaxO = ams + AMAX_DAU; }
         MOE_STAGE(ST_FC2S_DGRAD, gemm(d));
         if (nv) {
-            const moe_status_t r = nvq(nv_job(L, T_, meta, poff, E, true, Hs, Fs, nullptr, nullptr, ws + L.hsTq,
-                                              ws + L.shsT, ams + AMAX_H), ST_QT);
-            if (r != MOE_OK) return r;
+            MOE_STAGE(ST_QT, launch_nv_quant(nv_job(L, T_, meta, poff, E, true, Hs, Fs, nullptr, nullptr,
+                                                    ws + L.hsTq, ws + L.shsT, amh + E), s));
         } else {
             MxQuantJob j{Hs, nullptr, Tp, Fs, Tp, nullptr, nullptr, ws + L.hsTq, ws + L.shsT, 1};
             j.rows_valid = T_;
@@ -1395,18 +1393,14 @@ static moe_status_t backward_mx_impl(moe_plan_t p, int T_, const moe_bwd_args_t*
         d.B0 = ws + L.dYsTq; d.ldb = Tp; d.XB0 = ws + L.sdYsT;
         d.rows_cap = Tp;
         d.O0 = a->dWs_down; d.ldo = H; d.o_estride = (long long)Fs * H; d.status = status;
-        if (nv) { d.nv = 1; d.gA = ams + AMAX_H; d.gB = ams + AMAX_DY; }
+        if (nv) { d.nv = 1; d.gA = amh + E; d.gB = ams + AMAX_DY; }
         MOE_STAGE(ST_FC2S_WGRAD, gemm(d));
         if (nv) {
-            float* g = ams + AMAX_DAU;
-            const NvQuantJob ja = nv_job(L, T_, meta, poff, E, true, dAs, Fs, ws + L.dAsq, ws + L.sdAs,
-                                         ws + L.dAsTq, ws + L.sdAsT, g);
-            const NvQuantJob ju = nv_job(L, T_, meta, poff, E, true, dUs, Fs, ws + L.dUsq, ws + L.sdUs,
-                                         ws + L.dUsTq, ws + L.sdUsT, g);
-            MOE_STAGE(ST_AMAX, launch_nv_amax(ja, g, s));
-            MOE_STAGE(ST_AMAX, launch_nv_amax(ju, g, s));
-            MOE_STAGE(ST_QROWS, launch_nv_quant(ja, s));
-            MOE_STAGE(ST_QROWS, launch_nv_quant(ju, s));
+            const float* g = ams + AMAX_DAU;
+            MOE_STAGE(ST_QROWS, launch_nv_quant(nv_job(L, T_, meta, poff, E, true, dAs, Fs, ws + L.dAsq, ws + L.sdAs,
+                                                       ws + L.dAsTq, ws + L.sdAsT, g), s));
+            MOE_STAGE(ST_QROWS, launch_nv_quant(nv_job(L, T_, meta, poff, E, true, dUs, Fs, ws + L.dUsq, ws + L.sdUs,
+                                                       ws + L.dUsTq, ws + L.sdUsT, g), s));
         } else {
             MxQuantJob ja{dAs, nullptr, Tp, Fs, Tp, ws + L.dAsq, ws + L.sdAs, ws + L.dAsTq, ws + L.sdAsT, 1};
             ja.rows_valid = T_;

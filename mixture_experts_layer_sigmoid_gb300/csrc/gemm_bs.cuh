@@ -234,6 +234,15 @@ __device__ __forceinline__ void get8(const uint64_t* acc, int p, float* v)
     }
 }
 
+// NVFP4: fold a warp's largest magnitude into amax[e] (non-negative floats
+// order like their bit patterns)
+__device__ __forceinline__ void warp_amax(float m, float* amax, int e)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned int*>(amax) + e, __float_as_uint(m));
+}
+
 struct XTile {
     int e, m, n, row0, kblocks, klast, valid_end, alloc_end;   // klast: MMAs in the last k block
 };
@@ -742,6 +751,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                     }
                     if (lane == 0) ptx::bulk_wait_read<0>();
                     __syncwarp();
+                    float hmax = 0.f;   // NVFP4: the largest stored |h|
 #pragma unroll
                     for (int blk = 0; blk < 2; ++blk) {
                         float hb[32];
@@ -755,6 +765,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                             for (int i = 0; i < 8; ++i) {
                                 hv[i] = valid ? SwigluFwd(v[i], x[i]).h * grow : 0.f;
                                 hb[8 * jj + i] = __bfloat162float(__float2bfloat16_rn(hv[i]));
+                                if (NV) hmax = fmaxf(hmax, fabsf(hb[8 * jj + i]));
                             }
                             put(stg, j, hv);
                         }
@@ -775,6 +786,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                         ptx::tma_store_2d(&mO2, stg, col_lo, y);
                         ptx::bulk_commit();
                     }
+                    if (NV && d.amaxO) warp_amax(hmax, d.amaxO, d.dense_rows > 0 ? 0 : t.e);
                 }
             } else if (EPI == EPI_SWIGLU_BWD) {
                 // dA, dU of this warp's 32 rows x (64 part-0 + 64 part-1) columns,
@@ -788,6 +800,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                     const int y = t.row0 + q * 32;
                     const size_t orow = (size_t)arow * d.ldo;
                     const uint32_t stg = staging + (uint32_t)(warp - 2) * 8192u;
+                    float gmax = 0.f, hmax = 0.f;   // NVFP4: the largest stored |dA|, |dU| and |g h|
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
                         if (part == 1 && !hi_ok) break;
@@ -835,6 +848,15 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                                         da2[i] = __floats2bfloat162_rn(r0.dA, r1.dA);
                                         du2[i] = __floats2bfloat162_rn(r0.dU, r1.dU);
                                     }
+                                    if (NV) {
+                                        const float2 fa = __bfloat1622float2(da2[i]), fu = __bfloat1622float2(du2[i]);
+                                        gmax = fmaxf(gmax, fmaxf(fmaxf(fabsf(fa.x), fabsf(fa.y)),
+                                                                 fmaxf(fabsf(fu.x), fabsf(fu.y))));
+                                        if (fold) {
+                                            const float2 fh = __bfloat1622float2(dh2[i]);
+                                            hmax = fmaxf(hmax, fmaxf(fabsf(fh.x), fabsf(fh.y)));
+                                        }
+                                    }
                                 }
                                 const int jc = j0 + j;
                                 const uint32_t sw = (uint32_t)lane * 128u + (uint32_t)((jc ^ (lane & 7)) * 16);
@@ -856,6 +878,9 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ 
                         }
                         if (fold) d.dg_part[(size_t)arow * d.dg_ld + col / 64] = dgp;   // 0 past the computed rows
                     }
+                    const int ge = d.dense_rows > 0 ? 0 : t.e;
+                    if (NV && d.amaxO) warp_amax(gmax, d.amaxO, ge);
+                    if (NV && fold && d.amaxO2) warp_amax(hmax, d.amaxO2, ge);
                 }
             }
         }

@@ -109,6 +109,11 @@ struct GemmDesc {
     // dense group), whose tensor scales the epilogue divides out
     int nv;
     const float* gA; const float* gB;
+    // NVFP4 SwiGLU epilogues: the largest magnitude of the bf16 values they
+    // store, per expert (atomicMax; zeroed by the caller): SWIGLU_FWD h into
+    // amaxO; SWIGLU_BWD [dA | dU] into amaxO and, with folded gates, g h into
+    // amaxO2 (null: not computed)
+    float* amaxO; float* amaxO2;
     // memory-efficient permutation (gates != null): g of permuted row r is
     // gates[slot_of[r]]. SWIGLU_FWD stores O2 = g h; SWIGLU_BWD treats the
     // accumulator as dh', writes dA, dU of dh = g dh', O2 = g h (if O2 is
