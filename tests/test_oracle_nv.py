@@ -252,3 +252,28 @@ def test_nv_layer_tracks_the_exact_layer(fold):
         rel_mx = np.linalg.norm(qm[n] - g[n]) / np.linalg.norm(g[n])
         assert 0.03 < rel < 0.4, (n, rel)
         assert rel > 2 * rel_mx, (n, rel, rel_mx)       # coarser than MXFP8
+
+
+def test_nv_tensor_scale_is_per_expert_and_scale_free():
+    """Scaling one expert's Wd by 4 leaves its E4M3 block scales and E2M1 codes
+    unchanged (its tensor scale absorbs the power of two: every step of the
+    recipe commutes with it), so that expert's rows of y are exactly 4x, and
+    -- each expert being its own tensor -- every other row is unchanged bit
+    for bit. A tensor scale shared across experts would move the other
+    experts' codes once expert 0 holds the largest weight."""
+    T, H, E, k, F = 96, 128, 3, 1, 128
+    p = _layer(T, H, E, k, F, seed=31)
+    for n in ("x", "Wg", "Wu", "Wd"):
+        p[n] = _bf(p[n])
+    r = oracle.route(p["x"], p["Wr"], None, k, oracle.SOFTMAX)
+    run = lambda Wd: oracle.layer_fp8(p["x"], p["Wr"], p["Wg"], p["Wu"], Wd, r["topk"], r["gates"],
+                                      r["scores"], oracle.SOFTMAX, recipe=oracle.RECIPE_NV)["y"]
+    y0 = run(p["Wd"])
+    Wd = p["Wd"].copy()
+    Wd[0] *= 4.0
+    assert np.abs(Wd[0]).max() > np.abs(p["Wd"][1:]).max()     # expert 0 now holds the largest weight
+    y1 = run(Wd)
+    mine = r["topk"][:, 0] == 0
+    assert mine.any() and (~mine).any()
+    assert np.array_equal(y1[mine], 4.0 * y0[mine])
+    assert np.array_equal(y1[~mine], y0[~mine])
