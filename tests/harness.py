@@ -201,7 +201,7 @@ EXPERT_WGRADS = {"dWg", "dWu", "dWd", "dWsg", "dWsu", "dWsd"}
 
 def compare_all(w, inp, r, gpu, ref, backward=True, fold=False):
     """Compare every output and gradient with the rules of this module.
-    Returns, per tensor, the benchmark spec's pair (relative L2, max|err|/rms) against
+    Returns, per tensor, the contract's pair (relative L2, max|err|/rms) against
     the fp64 oracle (plus, for bf16 expert weight gradients, the bf16-storage
     floor of the second and the rounding-consistency figures)."""
     report = {"y": assert_close("y", to_np(gpu["y"]), ref["y"], w.dtype)}
