@@ -104,6 +104,9 @@ NV_CASES = {
     # DeepSeek-shaped with the shared expert: a dense group of T = 300 rows
     # (codes padded to 384), Fs != F
     "nv_deepseek_shared": _nv(mi.WORKLOADS["deepseek_v3"], T=300, H=256, E=16, k=4, F=256, Fs=512),
+    # three tokens: one-row segments (weight-gradient K of two 64-row MMAs), a
+    # shared expert of one padded tile
+    "nv_tiny": _nv(mi.WORKLOADS["deepseek_v3"], T=3, H=256, E=4, k=2, F=256, Fs=256),
 }
 
 
