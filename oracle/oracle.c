@@ -712,6 +712,7 @@ static void qdq_block(double* v, int n, long stride, unsigned char* codes, float
 /* 1x128 blocks along the rows of an M x K matrix (K a multiple of 128). */
 static void qdq_rows(int M, int K, double* X)
 {
+#pragma omp parallel for schedule(static)
     for (int m = 0; m < M; ++m)
         for (int k0 = 0; k0 < K; k0 += 128) qdq_block(X + (long)m * K + k0, 128, 1, NULL, NULL);
 }
@@ -719,6 +720,7 @@ static void qdq_rows(int M, int K, double* X)
 /* Per column, blocks of 128 consecutive rows (the last block may be short). */
 static void qdq_cols(int M, int N, double* X)
 {
+#pragma omp parallel for schedule(static)
     for (int n = 0; n < N; ++n)
         for (int m0 = 0; m0 < M; m0 += 128) {
             int len = M - m0 < 128 ? M - m0 : 128;
@@ -836,6 +838,7 @@ static void mx_block(double* v, int n, long stride, unsigned char* codes, unsign
 /* 1x32 blocks along the rows of an M x K matrix (K a multiple of 32). */
 static void mx_rows(int M, int K, double* X)
 {
+#pragma omp parallel for schedule(static)
     for (int m = 0; m < M; ++m)
         for (int k0 = 0; k0 < K; k0 += 32) mx_block(X + (long)m * K + k0, 32, 1, NULL, NULL);
 }
@@ -843,6 +846,7 @@ static void mx_rows(int M, int K, double* X)
 /* Per column, blocks of 32 consecutive rows (the last block may be short). */
 static void mx_cols(int M, int N, double* X)
 {
+#pragma omp parallel for schedule(static)
     for (int n = 0; n < N; ++n)
         for (int m0 = 0; m0 < M; m0 += 32) {
             int len = M - m0 < 32 ? M - m0 : 32;
@@ -967,9 +971,11 @@ static void nv_qdq(int by_row, int M, int K, double* X, float amax)
 {
     const float S = oracle_nv_tensor_scale(amax);
     if (by_row) {
+#pragma omp parallel for schedule(static)
         for (int m = 0; m < M; ++m)
             for (int k0 = 0; k0 < K; k0 += 16) nv_block(X + (long)m * K + k0, 16, 1, S, NULL, NULL);
     } else {
+#pragma omp parallel for schedule(static)
         for (int n = 0; n < K; ++n)
             for (int m0 = 0; m0 < M; m0 += 16) {
                 int len = M - m0 < 16 ? M - m0 : 16;
